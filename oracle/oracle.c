@@ -1,0 +1,423 @@
+/*
+ * CPU oracle for the FP8 (E4M3) block-scaled GEMM library.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the bench's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * What it computes, and where the definition comes from:
+ *   - E4M3 ("fn" variant, dtype float8_e4m3fn) decode from the bit pattern:
+ *     the format named in "Optimizing FP8 GEMM kernels in JAX with Triton for
+ *     Blackwell GPUs" (format paragraph: E4M3 preferred for its range /
+ *     precision balance) and the dtype in "Triton FP8 CUTLASS-named kernel
+ *     benchmarking" (parameter list: torch.float8_e4m3fn).
+ *   - Quantisation x -> RNE_satfinite(fl32(x / s)) with a per-tensor scale
+ *     s = fl32(amax / 448) or a 1x32 block scale along K equal to the smallest
+ *     power of two >= amax / 448 (the microscaling paragraph of the JAX/Blackwell
+ *     page; "2nd-gen Transformer Engine integrates micro-scaling (MXFP8)" in the
+ *     Triton tutorial ch. 12, section 12.6.1).
+ *   - GEMM C = (sA A)(sB B)^T with A[M,K], B[N,K] row-major: the pseudo-kernel
+ *     of the JAX/Blackwell page (fp32 accumulate, down-converting store), with
+ *     B held K-contiguous.
+ *   - The grouped (MoE) variant: per expert e, rows [off_e, off_e + M_e) of A
+ *     multiply B[e] (MoE paragraph of the JAX/Blackwell page).
+ *   - The grouped raster order of output tiles ("GROUP_M" swizzle of the
+ *     persistent matmul in the Triton tutorial ch. 12, section 12.7).
+ *
+ * All arithmetic is fp64.  Per-block inner sums are exact: each product of two
+ * E4M3 values is an integer multiple of 2^-18 with magnitude <= 448^2 < 2^18,
+ * so any sum of fewer than 2^17 of them fits in the 53-bit significand.
+ * Steps the pages fix in fp32 (fl32(amax/448), fl32(x/s), fl32(sA*sB),
+ * fl32(alpha*acc)) are done in fp32 here too.
+ *
+ * Parity unpinned: the rounding order of the tensor core's fp32 accumulation.
+ * Only the stated tolerance bounds it.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_EXPORT __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------ */
+/* E4M3 decode                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Value of an E4M3 ("fn") bit pattern: 1 sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits.  Exponent field 0 is subnormal (m * 2^-9).  There are no
+ * infinities; only S.1111.111 is NaN, so the largest finite value is
+ * 1.75 * 2^8 = 448. */
+ORACLE_EXPORT double oracle_e4m3_decode(uint8_t code) {
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+ORACLE_EXPORT void oracle_e4m3_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
+/* Round a finite, non-negative real y to the E4M3 grid with round-to-nearest,
+ * ties to even mantissa, then saturate to 448.  Works on the magnitude; the
+ * caller supplies the sign.  Returns the 7-bit magnitude code. */
+static uint8_t e4m3_mag_code(double y) {
+    if (y == 0.0) return 0;
+    /* exponent of the leading bit, clamped to the subnormal range */
+    int E = ilogb(y);
+    if (E < -6) E = -6; /* below 2^-6 the spacing is the subnormal quantum 2^-9 */
+    double quantum = ldexp(1.0, E - 3);
+    double n = y / quantum; /* exact: power-of-two division */
+    double fl = floor(n);
+    double frac = n - fl;
+    double r;
+    if (frac > 0.5)
+        r = fl + 1.0;
+    else if (frac < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    double v = r * quantum; /* rounded magnitude, may carry into next binade */
+    if (v > 448.0) v = 448.0; /* satfinite */
+    /* encode v exactly */
+    if (v < ldexp(1.0, -6)) {
+        int m = (int)(v / ldexp(1.0, -9));
+        return (uint8_t)m;
+    }
+    int e = ilogb(v);
+    int m = (int)((v / ldexp(1.0, e) - 1.0) * 8.0);
+    return (uint8_t)(((e + 7) << 3) | m);
+}
+
+/* E4M3 code of the fp32 value y: RNE, satfinite, NaN -> 0x7F, -0 -> 0x80. */
+ORACLE_EXPORT uint8_t oracle_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (isinf(a)) return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | e4m3_mag_code(a));
+}
+
+/* ------------------------------------------------------------------ */
+/* bf16 rounding                                                       */
+/* ------------------------------------------------------------------ */
+
+/* Round a real value (given in fp64) directly to bf16 (8 significant bits,
+ * fp32 exponent range) with round-to-nearest-even, returned as a float. */
+ORACLE_EXPORT float oracle_bf16_round(double x) {
+    if (isnan(x)) return NAN;
+    if (isinf(x) || x == 0.0) return (float)x;
+    double a = fabs(x);
+    int E = ilogb(a);
+    if (E < -126) E = -126; /* bf16 subnormals share fp32's quantum 2^-133 */
+    double quantum = ldexp(1.0, E - 7);
+    double n = a / quantum;
+    double fl = floor(n);
+    double frac = n - fl;
+    double r;
+    if (frac > 0.5)
+        r = fl + 1.0;
+    else if (frac < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    double v = r * quantum;
+    /* largest finite bf16 is (2 - 2^-7) * 2^127; the RNE overflow threshold
+     * is halfway to 2^128 */
+    if (v >= ldexp(1.0, 128)) v = INFINITY;
+    return (float)(x < 0 ? -v : v);
+}
+
+/* Size of one bf16 unit in the last place at |x|: 2^(floor(log2|x|) - 7) for
+ * normal values, 2^-133 for zero and subnormals. */
+ORACLE_EXPORT double oracle_bf16_ulp(double x) {
+    double a = fabs(x);
+    if (a == 0.0 || a < ldexp(1.0, -126)) return ldexp(1.0, -133);
+    if (isinf(a) || isnan(a)) return INFINITY;
+    return ldexp(1.0, ilogb(a) - 7);
+}
+
+/* ------------------------------------------------------------------ */
+/* Quantisation                                                        */
+/* ------------------------------------------------------------------ */
+
+/* max |x| over non-NaN entries */
+static float amax_of(const float *x, int64_t n, int64_t stride) {
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float v = fabsf(x[i * stride]);
+        if (!isnan(v) && v > m) m = v;
+    }
+    return m;
+}
+
+/* Per-tensor quantisation: s = fl32(amax / 448), q = RNE_satfinite(fl32(x / s)).
+ * When s comes out as 0 (amax = 0, or amax so small that the quotient
+ * underflows) s = 1 is used instead, so no division by zero happens. */
+ORACLE_EXPORT void oracle_quantize_tensor(const float *x, int64_t rows, int64_t cols,
+                                          uint8_t *q, float *scale_out) {
+    float amax = amax_of(x, rows * cols, 1);
+    float s = amax / 448.0f;
+    if (s == 0.0f) s = 1.0f;
+    for (int64_t i = 0; i < rows * cols; ++i) q[i] = oracle_e4m3_encode(x[i] / s);
+    *scale_out = s;
+}
+
+/* The power-of-two block scale: the smallest 2^e with 2^e * 448 >= amax,
+ * clamped to e in [-126, 127]; amax = 0 gives 1. */
+ORACLE_EXPORT float oracle_pow2_scale(float amax) {
+    if (amax == 0.0f || isnan(amax)) return 1.0f;
+    if (isinf(amax)) return ldexpf(1.0f, 127);
+    int e = -126;
+    /* linear search is fine: at most 254 steps, exact comparisons in fp64 */
+    while (e < 127 && ldexp(448.0, e) < (double)amax) ++e;
+    return ldexpf(1.0f, e);
+}
+
+/* 1x32 block quantisation along the contiguous (K) axis.  cols % 32 == 0.
+ * scales: [rows, cols/32] fp32, each a power of two. */
+ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t cols,
+                                           uint8_t *q, float *scales) {
+    int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *blk = x + r * cols + b * 32;
+            float s = oracle_pow2_scale(amax_of(blk, 32, 1));
+            scales[r * nb + b] = s;
+            for (int j = 0; j < 32; ++j) q[r * cols + b * 32 + j] = oracle_e4m3_encode(blk[j] / s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* GEMM                                                                */
+/* ------------------------------------------------------------------ */
+
+enum { ORACLE_OUT_BF16 = 0, ORACLE_OUT_F32 = 1 };
+
+typedef struct {
+    const uint8_t *A, *B;
+    const float *sfa, *sfb; /* block: [M,K/32], [N,K/32]; tensor: 1 value each */
+    int block;
+    int64_t M, N, K;
+    int out_kind;
+    float *C;        /* rounded output (bf16 values held in float, or fp32) */
+    double *exact;   /* nullable: the value before the output rounding */
+    double *bound;   /* nullable: tolerance per element */
+    int64_t row_begin, row_end;
+    const int64_t *pi, *pj; /* sampled mode: element list (nullable) */
+    int64_t n_samples;
+} gemm_job;
+
+static double dec_tab[256];
+static int dec_ready = 0;
+static void ensure_table(void) {
+    if (!dec_ready) {
+        oracle_e4m3_table(dec_tab);
+        dec_ready = 1;
+    }
+}
+
+/* One output element.  Block mode:
+ *   v = sum_kb sfa[i,kb] * sfb[j,kb] * (sum_{k in kb} dec(a_ik) dec(b_jk))
+ * Tensor mode:
+ *   acc = sum_k dec(a_ik) dec(b_jk), alpha = fl32(sA * sB), v = fl32(alpha * acc)
+ * The tolerance bound is 2^-8 * sum_k |sA a_ik| |sB b_jk| + 1 bf16 ulp of the
+ * rounded reference. */
+static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, double *exact,
+                        double *bound) {
+    const uint8_t *a = g->A + i * g->K;
+    const uint8_t *b = g->B + j * g->K;
+    double v, absum = 0.0;
+    if (g->block) {
+        int64_t nb = g->K / 32;
+        double total = 0.0;
+        for (int64_t kb = 0; kb < nb; ++kb) {
+            double part = 0.0, apart = 0.0;
+            for (int64_t k = kb * 32; k < kb * 32 + 32; ++k) {
+                double p = dec_tab[a[k]] * dec_tab[b[k]];
+                part += p;
+                apart += fabs(p);
+            }
+            double sc = (double)g->sfa[i * nb + kb] * (double)g->sfb[j * nb + kb];
+            total += sc * part;
+            absum += fabs(sc) * apart;
+        }
+        v = total;
+    } else {
+        double acc = 0.0, aacc = 0.0;
+        for (int64_t k = 0; k < g->K; ++k) {
+            double p = dec_tab[a[k]] * dec_tab[b[k]];
+            acc += p;
+            aacc += fabs(p);
+        }
+        float alpha = g->sfa[0] * g->sfb[0];
+        v = (double)(float)((double)alpha * acc);
+        absum = fabs((double)g->sfa[0] * (double)g->sfb[0]) * aacc;
+    }
+    float r = (g->out_kind == ORACLE_OUT_BF16) ? oracle_bf16_round(v) : (float)v;
+    *out = r;
+    if (exact) *exact = v;
+    if (bound) *bound = ldexp(absum, -8) + oracle_bf16_ulp((double)r);
+}
+
+static void *gemm_worker(void *arg) {
+    gemm_job *g = (gemm_job *)arg;
+    if (g->pi) {
+        for (int64_t s = g->row_begin; s < g->row_end; ++s)
+            one_element(g, g->pi[s], g->pj[s], &g->C[s], g->exact ? &g->exact[s] : NULL,
+                        g->bound ? &g->bound[s] : NULL);
+        return NULL;
+    }
+    for (int64_t i = g->row_begin; i < g->row_end; ++i)
+        for (int64_t j = 0; j < g->N; ++j) {
+            int64_t o = i * g->N + j;
+            one_element(g, i, j, &g->C[o], g->exact ? &g->exact[o] : NULL,
+                        g->bound ? &g->bound[o] : NULL);
+        }
+    return NULL;
+}
+
+static void run_jobs(gemm_job proto, int64_t n_items, int threads) {
+    if (threads < 1) threads = 1;
+    if (threads > 256) threads = 256;
+    if (n_items < threads) threads = (int)(n_items > 0 ? n_items : 1);
+    pthread_t tid[256];
+    gemm_job jobs[256];
+    int64_t per = (n_items + threads - 1) / threads;
+    int started = 0;
+    for (int t = 0; t < threads; ++t) {
+        jobs[t] = proto;
+        jobs[t].row_begin = t * per;
+        jobs[t].row_end = (t + 1) * per < n_items ? (t + 1) * per : n_items;
+        if (jobs[t].row_begin >= jobs[t].row_end) continue;
+        if (threads == 1 || pthread_create(&tid[t], NULL, gemm_worker, &jobs[t]) != 0) {
+            gemm_worker(&jobs[t]);
+            tid[t] = 0;
+        } else {
+            ++started;
+        }
+    }
+    for (int t = 0; t < threads; ++t)
+        if (threads > 1 && jobs[t].row_begin < jobs[t].row_end && tid[t]) pthread_join(tid[t], NULL);
+}
+
+/* Full GEMM.  block = 0: sfa, sfb each point to one fp32 per-tensor scale.
+ * block = 1: sfa [M, K/32], sfb [N, K/32].  C, exact, bound: [M, N]. */
+ORACLE_EXPORT void oracle_gemm(const uint8_t *A, const uint8_t *B, const float *sfa,
+                               const float *sfb, int block, int64_t M, int64_t N, int64_t K,
+                               int out_kind, float *C, double *exact, double *bound,
+                               int threads) {
+    ensure_table();
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    run_jobs(g, M, threads);
+}
+
+/* Sampled GEMM: only the n elements (pi[s], pj[s]). Outputs are length n. */
+ORACLE_EXPORT void oracle_gemm_sample(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                      const float *sfb, int block, int64_t M, int64_t N,
+                                      int64_t K, int out_kind, const int64_t *pi,
+                                      const int64_t *pj, int64_t n, float *C, double *exact,
+                                      double *bound, int threads) {
+    ensure_table();
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    g.pi = pi; g.pj = pj; g.n_samples = n;
+    run_jobs(g, n, threads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Grouped (MoE) problem list and raster order                         */
+/* ------------------------------------------------------------------ */
+
+/* offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e] */
+ORACLE_EXPORT void oracle_grouped_offsets(const int32_t *counts, int32_t E, int32_t *offsets) {
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+}
+
+/* Grouped raster order of one problem's npm x npn tile grid, group height G:
+ * tiles are walked in bands of G tile-rows; inside a band, down the rows of
+ * one tile-column first, then on to the next column. */
+ORACLE_EXPORT void oracle_raster(int64_t t, int64_t npm, int64_t npn, int64_t G, int64_t *pid_m,
+                                 int64_t *pid_n) {
+    int64_t band = G * npn;
+    int64_t grp = t / band;
+    int64_t first_m = grp * G;
+    int64_t rows_here = npm - first_m < G ? npm - first_m : G;
+    int64_t in_band = t % band;
+    *pid_m = first_m + in_band % rows_here;
+    *pid_n = in_band / rows_here;
+}
+
+/* Tile list of a single GEMM in launch order: out[2t] = pid_m, out[2t+1] = pid_n. */
+ORACLE_EXPORT int64_t oracle_tile_map(int64_t M, int64_t N, int64_t BM, int64_t BN, int64_t G,
+                                      int64_t *out, int64_t cap) {
+    int64_t npm = (M + BM - 1) / BM, npn = (N + BN - 1) / BN, T = npm * npn;
+    for (int64_t t = 0; t < T && t < cap; ++t) oracle_raster(t, npm, npn, G, &out[2 * t], &out[2 * t + 1]);
+    return T;
+}
+
+/* Tile list of a grouped GEMM: experts in index order, expert e owning
+ * ceil(M_e/BM) * ceil(N/BN) consecutive tiles (none when M_e = 0), each
+ * expert's tiles in the grouped raster order above.
+ * out[4t..4t+3] = (expert, m_tile, n_tile, 0).  Returns the tile count. */
+ORACLE_EXPORT int64_t oracle_grouped_tile_map(const int32_t *counts, int32_t E, int64_t N,
+                                              int64_t BM, int64_t BN, int64_t G, int32_t *out,
+                                              int64_t cap) {
+    int64_t npn = (N + BN - 1) / BN, t = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        int64_t npm = (counts[e] + BM - 1) / BM;
+        for (int64_t l = 0; l < npm * npn; ++l, ++t) {
+            int64_t pm, pn;
+            oracle_raster(l, npm, npn, G, &pm, &pn);
+            if (t < cap) {
+                out[4 * t + 0] = e;
+                out[4 * t + 1] = (int32_t)pm;
+                out[4 * t + 2] = (int32_t)pn;
+                out[4 * t + 3] = 0;
+            }
+        }
+    }
+    return t;
+}
+
+/* Grouped GEMM: A [sum M_e, K] with expert e's rows at [off_e, off_e + M_e),
+ * B [E, N, K], sfa [sum M_e, K/32], sfb [E, N, K/32]; C [sum M_e, N].
+ * Each expert is an independent block-scaled GEMM. */
+ORACLE_EXPORT void oracle_grouped_gemm(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                       const float *sfb, const int32_t *counts, int32_t E,
+                                       int64_t N, int64_t K, int out_kind, float *C,
+                                       double *exact, double *bound, int threads) {
+    int64_t off = 0, nb = K / 32;
+    for (int32_t e = 0; e < E; ++e) {
+        int64_t Me = counts[e];
+        if (Me > 0)
+            oracle_gemm(A + off * K, B + (int64_t)e * N * K, sfa + off * nb,
+                        sfb + (int64_t)e * N * nb, 1, Me, N, K, out_kind, C + off * N,
+                        exact ? exact + off * N : NULL, bound ? bound + off * N : NULL, threads);
+        off += Me;
+    }
+}
+
+/* Algorithmic FLOP count of C = A B^T: 2 M N K ("TFLOPS = 2*M*N*K/(t*1e12)"
+ * in the monitoring checklist of the Triton FP8 benchmarking page). */
+ORACLE_EXPORT double oracle_gemm_flops(int64_t M, int64_t N, int64_t K) {
+    return 2.0 * (double)M * (double)N * (double)K;
+}
