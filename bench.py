@@ -1,0 +1,404 @@
+"""FP8 GEMM throughput on GB300: TFLOPS and fraction of the roofline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload large8192|large4096|skinny|moe|square1024]
+
+One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
+scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
+already resident in HBM.  Operand quantisation is data preparation and is
+not timed (it is its own kernel and its own metric).  The default workload is
+the large block-scaled GEMM M=N=K=8192 (1x32 scales along K, N(0,1) with 0.1%
+x50 outliers, bf16 out), the shape the >= 70%-of-peak target is quoted on.
+
+L2: the timed steps rotate over several copies of the inputs whose total is
+larger than 2x the L2, so every step reads its operands from HBM.
+
+Multi-GPU (torchrun, one rank per GPU): replicas only — every rank runs the
+same GEMM on its own GPU, no collective on the data path; value = total FLOPs
+of all ranks / max-over-ranks time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOADS = {
+    "large8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3),
+    "large4096": dict(kind="block", M=4096, N=4096, K=4096, seed=3),
+    "skinny": dict(kind="block", M=128, N=4096, K=4096, seed=2),
+    "moe": dict(kind="grouped", M=32768, N=14336, K=4096, seed=4),
+    "square1024": dict(kind="tensor", M=1024, N=1024, K=1024, seed=1),
+}
+METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def make_inputs(wl: dict, device):
+    """Synthetic operands (CPU, seeded) -> quantised on the GPU by the library."""
+    import synth
+    import fp8_block_scaled_06_gb300 as fp8g
+
+    if wl["kind"] == "grouped":
+        w = synth.moe_grouped(seed=wl["seed"])
+        E, N, K = w.B.shape
+        qa, sa = fp8g.quantize(w.A.to(device), 32)
+        qb, sb = fp8g.quantize(w.B.reshape(E * N, K).to(device), 32)
+        qb = qb.reshape(E, N, K)
+        sb = sb.reshape(E, N, K // 32)
+        counts = torch.from_numpy(w.counts).to(device)
+        return w, dict(qa=qa, sa=sa, qb=qb, sb=sb, counts=counts)
+    if wl["kind"] == "tensor":
+        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32")
+        bs = 0
+    elif wl["M"] == 128:
+        w = synth.skinny_block(seed=wl["seed"])
+        bs = 32
+    else:
+        w = synth.large_block(wl["M"], seed=wl["seed"])
+        bs = 32
+    qa, sa = fp8g.quantize(w.A.to(device), bs)
+    qb, sb = fp8g.quantize(w.B.to(device), bs)
+    return w, dict(qa=qa, sa=sa, qb=qb, sb=sb)
+
+
+def algorithmic_bytes(wl: dict, w) -> int:
+    M, N, K = wl["M"], wl["N"], wl["K"]
+    out_b = 4 if w.out == "f32" else 2
+    if wl["kind"] == "grouped":
+        E = w.B.shape[0]
+        return M * K + E * N * K + 4 * (M * K // 32 + E * N * K // 32) + M * N * out_b + 4 * E
+    sf = 8 if wl["kind"] == "tensor" else 4 * (M * K // 32 + N * K // 32)
+    return M * K + N * K + sf + M * N * out_b
+
+
+def run_once(fp8g, wl, w, t, C, stream):
+    out = fp8g.FP8G_OUT_F32 if w.out == "f32" else fp8g.FP8G_OUT_BF16
+    if wl["kind"] == "grouped":
+        E, N, K = t["qb"].shape
+        fp8g.fp8_grouped_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, t["counts"], E, N, K,
+                              t["qa"].shape[0], None, None, stream)
+    elif wl["kind"] == "tensor":
+        fp8g.fp8_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"], wl["K"], stream)
+    else:
+        fp8g.fp8_gemm_blockscaled(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"],
+                                  wl["K"], stream)
+
+
+def oracle_inputs(wl, w):
+    """The oracle's own quantisation of the workload (done once, untimed)."""
+    import oracle
+    if wl["kind"] == "grouped":
+        E, N, K = w.B.shape
+        qa, sa = oracle.quantize_block32(w.A.numpy())
+        qb, sb = oracle.quantize_block32(w.B.reshape(E * N, K).numpy())
+        offs = oracle.grouped_offsets(w.counts)
+        e = int(np.argmax(w.counts))                 # the largest expert
+        return dict(A=qa[offs[e]:offs[e + 1]], sa=sa[offs[e]:offs[e + 1]],
+                    B=qb.reshape(E, N, K)[e], sb=sb.reshape(E, N, K // 32)[e], block=True,
+                    N=N, K=K, desc=f"rows of expert {e} (all {N} columns)")
+    block = wl["kind"] != "tensor"
+    qfn = oracle.quantize_block32 if block else oracle.quantize_tensor
+    qa, sa = qfn(w.A.numpy())
+    qb, sb = qfn(w.B.numpy())
+    return dict(A=qa, sa=sa, B=qb, sb=sb, block=block, N=wl["N"], K=wl["K"],
+                desc=f"rows of A (all {wl['N']} columns)")
+
+
+def cpu_baseline(oi: dict, budget_s: float = 12.0):
+    """The oracle GEMM as it stands, on this host's cores, over a bounded row
+    sample sized to take about budget_s seconds."""
+    import oracle
+    threads = os.cpu_count() or 1
+    N, K, block = oi["N"], oi["K"], oi["block"]
+    total_rows = oi["A"].shape[0]
+    rows = 1
+    spent = 0.0
+    while True:
+        r = min(rows, total_rows)
+        a = np.ascontiguousarray(oi["A"][:r])
+        s = np.ascontiguousarray(oi["sa"][:r]) if block else oi["sa"]
+        t0 = time.perf_counter()
+        oracle.gemm(a, oi["B"], s, oi["sb"], block, oracle.OUT_BF16, threads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        flops = 2.0 * r * N * K
+        if dt > budget_s / 4 or r == total_rows or spent > budget_s:
+            break
+        rows = int(min(total_rows, max(rows * 2, rows * (budget_s / 3) / max(dt, 1e-3))))
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{r} {oi['desc']}, K={K}: {flops:.3e} FLOP in {dt:.3f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large8192", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    world, rank, local = _dist()
+    wl = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return reference_arm(args, wl, world, rank)
+
+    import fp8_block_scaled_06_gb300 as fp8g
+    fp8g.build()
+    fp8g.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    w, t = make_inputs(wl, device)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"quantiser status {st}"
+    rows = t["qa"].shape[0]
+    out_dt = torch.float32 if w.out == "f32" else torch.bfloat16
+    C = torch.empty((rows, wl["N"]), dtype=out_dt, device=device)
+    flops = w.flops
+    abytes = algorithmic_bytes(wl, w)
+
+    # rotate over input copies whose total exceeds 2x L2
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    in_bytes = sum(v.numel() * v.element_size() for k, v in t.items() if k != "counts")
+    copies = max(1, min(8, -(-2 * l2 // max(in_bytes, 1))))
+    sets = [t] + [{k: v.clone() for k, v in t.items()} for _ in range(copies - 1)]
+    stream = torch.cuda.current_stream(device)
+
+    for i in range(args.warmup):
+        run_once(fp8g, wl, w, sets[i % copies], C, stream)
+    torch.cuda.synchronize(device)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"GEMM status {st} detail {detail}"
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        run_once(fp8g, wl, w, sets[i % copies], C, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"GEMM status {st} detail {detail}"
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # end to end through the C ABI with host buffers: H2D of the inputs from
+    # pinned memory, the GEMM, D2H of C, every step
+    host = {k: v.cpu().pin_memory() for k, v in t.items()}
+    Ch = torch.empty(C.shape, dtype=C.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(v) for k, v in t.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = Ch.numel() * Ch.element_size()
+    e2e_steps = max(3, min(50, args.steps // 20))
+    for _ in range(2):
+        for k in dev_in:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        run_once(fp8g, wl, w, dev_in, C, stream)
+        Ch.copy_(C, non_blocking=True)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k in dev_in:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        run_once(fp8g, wl, w, dev_in, C, stream)
+        Ch.copy_(C, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    peaks = _peaks()
+    fp8_peak = 2.0 * peaks["bf16"]          # measured bf16 burst x nominal fp8/bf16 ratio (2)
+    tflops = flops / (ms * 1e-3) / 1e12
+    hbm_gbs = abytes / (ms * 1e-3) / 1e9
+    tensor_bound = (flops / (fp8_peak * 1e12)) >= (abytes / (peaks["hbm"] * 1e9))
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": round(tflops / fp8_peak, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(hbm_gbs, 1), "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": round(hbm_gbs / peaks["hbm"], 4)}
+    roof["traffic"] = None
+    roof["peak_source"] = (f"{peaks['src']}: fp8 = 2 x bf16 burst {peaks['bf16']} TFLOP/s"
+                           if tensor_bound else f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
+    roof["nominal_frac"] = round(max(flops / 4.5e15, abytes / 8e12) / (ms * 1e-3), 4)
+
+    line = {
+        "metric": METRIC,
+        "value": round(tflops * world, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate",
+        "data": "synthetic (seeded CPU generators, quantised on the GPU)",
+        "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"],
+                   "scales": {"block": "1x32 along K, power of two",
+                              "grouped": "1x32 along K, power of two",
+                              "tensor": "per tensor"}[wl["kind"]],
+                   "out": w.out, "l2": f"inputs rotated over {copies} copies > 2x L2",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": roof,
+        "achieved_hbm_gbs": round(hbm_gbs, 1),
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(oracle_inputs(wl, w))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference_arm(args, wl, world, rank):
+    """The oracle, as it stands, on this host's cores: each step is a bounded
+    row sample of the same workload, the whole run sized to about a minute."""
+    if rank != 0:
+        return
+    import synth
+    if wl["kind"] == "grouped":
+        w = synth.moe_grouped(seed=wl["seed"])
+    elif wl["kind"] == "tensor":
+        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32")
+    elif wl["M"] == 128:
+        w = synth.skinny_block(seed=wl["seed"])
+    else:
+        w = synth.large_block(wl["M"], seed=wl["seed"])
+    oi = oracle_inputs(wl, w)
+    budget = min(10.0, max(0.01, 60.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(oi, budget_s=budget)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = cpu_baseline(oi, budget_s=budget)
+        vals.append(cb["value"])
+    wall = time.perf_counter() - t0
+    v = float(np.median(vals))
+    line = {"metric": METRIC, "impl": "reference", "value": round(v, 6), "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic (seeded CPU generators)",
+            "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"]},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOPS", "cores": cb["cores"],
+                             "kind": "oracle", "sample": cb["sample"]},
+            "e2e": {"value": round(v, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

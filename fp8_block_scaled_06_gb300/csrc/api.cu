@@ -1,0 +1,371 @@
+// C ABI of the FP8 GEMM library: argument checks, TMA tensor-map encoding
+// (cached), per-device status word, kernel choice and launch.
+//
+// TMA rules checked on the host before any launch (Triton tutorial ch. 12,
+// 12.2.3): base address 16-byte aligned, innermost stride 1, every other
+// stride a multiple of 16 bytes, 2-5 dimensions.  Tensor maps are encoded once
+// per (pointer, shape, box) and reused ("create the descriptor outside the
+// loop", 12.8 Q1 of the same chapter).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace fp8g {
+
+// Per-device status word: [0] first error code since the last read, [1] detail.
+__device__ unsigned int g_status_word[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned int *g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+bool g_dev_ok[kMaxDevices] = {};
+std::atomic<uint64_t> g_timeout_ns{0};
+
+uint64_t timeout_ns() {
+    uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
+    if (t == 0) {
+        uint64_t ms = 2000;
+        if (const char *env = std::getenv("FP8G_WAIT_TIMEOUT_MS")) {
+            const long long v = std::atoll(env);
+            if (v > 0) ms = (uint64_t)v;
+        }
+        t = ms * 1000000ull;
+        g_timeout_ns.store(t, std::memory_order_relaxed);
+    }
+    return t;
+}
+
+struct DevInfo {
+    int dev;
+    int num_sms;
+    unsigned int *status;
+};
+
+fp8g_status device_info(DevInfo &di) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8G_ERR_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return FP8G_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev_ok[dev]) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8G_ERR_DEVICE;
+        if (major != 10 || minor != 3) return FP8G_ERR_DEVICE;  // built for sm_103a only
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FP8G_ERR_CUDA;
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return FP8G_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+        g_num_sms[dev] = sms;
+        g_dev_ok[dev] = true;
+    }
+    di.dev = dev;
+    di.num_sms = g_num_sms[dev];
+    di.status = g_status_ptr[dev];
+    return FP8G_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+struct TmapKey {
+    const void *ptr;
+    int rank;
+    uint64_t dims[3];
+    uint32_t box[3];
+    int dev;
+    bool operator==(const TmapKey &o) const {
+        return ptr == o.ptr && rank == o.rank && dev == o.dev &&
+               std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+               std::memcmp(box, o.box, sizeof box) == 0;
+    }
+};
+
+constexpr int kCacheSize = 64;
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+    bool used;
+};
+TmapEntry g_cache[kCacheSize];
+int g_cache_next = 0;
+
+// uint8 tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost, contiguous),
+// 128-byte swizzle, zero fill out of bounds.
+fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint32_t *box, int dev,
+                    CUtensorMap &out) {
+    TmapKey key{};
+    key.ptr = ptr;
+    key.rank = rank;
+    key.dev = dev;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < kCacheSize; ++i)
+        if (g_cache[i].used && g_cache[i].key == key) {
+            out = g_cache[i].map;
+            return FP8G_OK;
+        }
+    cuuint64_t gdim[3], gstride[2];
+    cuuint32_t bdim[3], estr[3];
+    uint64_t stride = 1;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) gstride[i - 1] = stride;
+        stride *= dims[i];
+    }
+    CUtensorMap m;
+    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank,
+                                const_cast<void *>(ptr), gdim, gstride, bdim, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FP8G_ERR_CUDA;
+    TmapEntry &e = g_cache[g_cache_next];
+    g_cache_next = (g_cache_next + 1) % kCacheSize;
+    e.key = key;
+    e.map = m;
+    e.used = true;
+    out = m;
+    return FP8G_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+// Shape / alignment rules common to every GEMM entry point.
+fp8g_status check_common(const void *A, const void *B, const void *C, int out, int64_t M,
+                         int64_t N, int64_t K) {
+    if (A == nullptr || B == nullptr || C == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return FP8G_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    const int64_t esz = out == FP8G_OUT_F32 ? 4 : 2;
+    if ((N * esz) % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    return FP8G_OK;
+}
+
+fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
+                     void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
+                     int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream) {
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_kb = (int32_t)((K + kBK - 1) / kBK);
+    p.npm = (int32_t)((M + kBM - 1) / kBM);
+    p.npn = (int32_t)((N + kc.BN - 1) / kc.BN);
+    p.T = (int64_t)p.npm * p.npn;
+    p.split = kc.split;
+    p.kb_per_split = (p.num_kb + kc.split - 1) / kc.split;
+    p.sa = sa;
+    p.sb = sb;
+    p.sfc = K / 32;
+    p.C = C;
+    p.counts = counts;
+    p.E = E;
+    p.offsets_out = offsets_out;
+    p.tile_map_out = tile_map_out;
+    p.status = di.status;
+    p.timeout_ns = timeout_ns();
+
+    CUtensorMap tmA, tmB;
+    {
+        // grouped with zero rows: A is never read; describe a 1-row tensor
+        const void *a_ptr = M > 0 ? A : B;
+        const uint64_t dA[2] = {(uint64_t)K, (uint64_t)(M > 0 ? M : 1)};
+        const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
+        if ((st = tmap_u8(a_ptr, 2, dA, bA, di.dev, tmA)) != FP8G_OK) return st;
+    }
+    if (mode == kModeGrouped) {
+        const uint64_t dB[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
+        const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.BN, 1u};
+        if ((st = tmap_u8(B, 3, dB, bB, di.dev, tmB)) != FP8G_OK) return st;
+    } else {
+        const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
+        const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.BN};
+        if ((st = tmap_u8(B, 2, dB, bB, di.dev, tmB)) != FP8G_OK) return st;
+    }
+    const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, tmA, tmB, p, kc, stream);
+    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fp8g
+
+using namespace fp8g;
+
+extern "C" {
+
+fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                     void *C, int out, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    fp8g_status st = check_common(A, B, C, out, M, N, K);
+    if (st != FP8G_OK) return st;
+    if (scale_a == nullptr || scale_b == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (!aligned(scale_a, 4) || !aligned(scale_b, 4)) return FP8G_ERR_ALIGNMENT;
+    return run_gemm(kModeTensor, A, B, scale_a, scale_b, C, out, M, N, K, nullptr, 0, nullptr,
+                    nullptr, stream);
+}
+
+fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
+                                 const float *sfb, void *C, int out, int64_t M, int64_t N,
+                                 int64_t K, cudaStream_t stream) {
+    fp8g_status st = check_common(A, B, C, out, M, N, K);
+    if (st != FP8G_OK) return st;
+    if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
+    return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
+                    stream);
+}
+
+fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, const float *sfb,
+                             void *C, int out, const int32_t *counts, int32_t E, int64_t N,
+                             int64_t K, int64_t total_rows, int32_t *offsets_out,
+                             int32_t *tile_map_out, cudaStream_t stream) {
+    if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (E < 1) return FP8G_ERR_INVALID_ARG;
+    if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (total_rows < 0) return FP8G_ERR_INVALID_ARG;
+    if (total_rows > 0) {
+        fp8g_status st = check_common(A, B, C, out, total_rows, N, K);
+        if (st != FP8G_OK) return st;
+    } else {
+        if (B == nullptr) return FP8G_ERR_INVALID_ARG;
+        if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
+        if (N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
+        if (!aligned(B, 16) || K % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    }
+    if (N >= kMaxDim || (int64_t)E * N >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(counts, 4)) return FP8G_ERR_ALIGNMENT;
+    if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
+    if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
+    return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
+                    offsets_out, tile_map_out, stream);
+}
+
+fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
+                              int32_t *BN, int32_t *G, int64_t *max_tiles) {
+    if (N < 1 || K < 1 || total_rows < 0 || E < 1) return FP8G_ERR_INVALID_ARG;
+    if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    const KernelChoice kc = choose_kernel(kModeGrouped, total_rows, N, K, 1);
+    if (BM) *BM = kBM;
+    if (BN) *BN = kc.BN;
+    if (G) *G = kRasterG;
+    // sum_e ceil(M_e / BM) <= floor(total_rows / BM) + E
+    if (max_tiles) *max_tiles = (total_rows / kBM + E) * ((N + kc.BN - 1) / kc.BN);
+    return FP8G_OK;
+}
+
+fp8g_status fp8g_gemm_plan(int block, int64_t M, int64_t N, int64_t K, int32_t *BM, int32_t *BN,
+                           int32_t *G, int32_t *split_k, int32_t *grid) {
+    if (M < 1 || N < 1 || K < 1 || (block != 0 && block != 1)) return FP8G_ERR_INVALID_ARG;
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const KernelChoice kc = choose_kernel(block ? kModeBlock : kModeTensor, M, N, K, di.num_sms);
+    if (BM) *BM = kBM;
+    if (BN) *BN = kc.BN;
+    if (G) *G = kRasterG;
+    if (split_k) *split_k = kc.split;
+    if (grid) *grid = kc.grid;
+    return FP8G_OK;
+}
+
+fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32_t block,
+                               uint8_t *q, float *scales, cudaStream_t stream) {
+    if (x == nullptr || q == nullptr || scales == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
+    if (block != 0 && block != 32) return FP8G_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4)) return FP8G_ERR_ALIGNMENT;
+    if (block == 32 && cols % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (block == 0 && cols % 8 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (rows >= ((int64_t)1 << 40) / cols) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const cudaError_t e =
+        block == 32 ? launch_quantize_block32(x, rows, cols, q, scales, di.num_sms, stream)
+                    : launch_quantize_tensor(x, rows * cols, q, scales, di.status, di.num_sms,
+                                             stream);
+    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+fp8g_status fp8_gemm_status(cudaStream_t stream, int32_t *detail) {
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8G_ERR_CUDA;
+    unsigned int w[2] = {0u, 0u};
+    if (cudaMemcpy(w, di.status, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    if (w[0] != 0u) {
+        const unsigned int zero[2] = {0u, 0u};
+        if (cudaMemcpy(di.status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+    }
+    if (detail) *detail = (int32_t)w[1];
+    return (fp8g_status)w[0];
+}
+
+const char *fp8g_status_string(fp8g_status s) {
+    switch (s) {
+        case FP8G_OK: return "ok";
+        case FP8G_ERR_INVALID_ARG: return "invalid argument";
+        case FP8G_ERR_ALIGNMENT: return "alignment rule broken (16-byte pointers and row strides)";
+        case FP8G_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case FP8G_ERR_SCALE_FORMAT: return "block scale is not a positive power of two";
+        case FP8G_ERR_CUDA: return "CUDA call failed";
+        case FP8G_ERR_TIMEOUT: return "device-side wait timed out; kernel aborted";
+        case FP8G_ERR_DEVICE: return "no usable sm_103 device";
+    }
+    return "unknown status";
+}
+
+void fp8g_set_wait_timeout_ms(uint32_t ms) {
+    if (ms == 0) {
+        g_timeout_ns.store(0, std::memory_order_relaxed);
+        (void)timeout_ns();
+    } else {
+        g_timeout_ns.store((uint64_t)ms * 1000000ull, std::memory_order_relaxed);
+    }
+}
+
+void fp8g_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < kCacheSize; ++i) g_cache[i].used = false;
+    g_cache_next = 0;
+}
+
+int fp8g_version(void) { return 100; }
+
+}  // extern "C"

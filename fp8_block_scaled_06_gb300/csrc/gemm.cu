@@ -1,0 +1,594 @@
+// Persistent, warp-specialised FP8 (E4M3) GEMM for sm_103a.
+//
+//   C = (sA A)(sB B)^T,  A[M,K], B[N,K] row-major, fp32 accumulation in tensor
+//   memory, bf16 or fp32 output.  Three modes: per-tensor scales, 1x32 block
+//   scales along K (applied by the block-scaled tensor-core MMA), and the
+//   grouped (MoE) form of the block-scaled GEMM.
+//
+// Design (GB300-native; the pages' Triton/Pallas kernels are prior art only):
+//   - one CTA per SM, persistent over output tiles in the grouped raster order
+//     (persistent matmul and GROUP_M swizzle: Triton tutorial ch. 12, 12.7);
+//   - warp 0: TMA producer filling a STAGES-deep shared-memory ring, one
+//     mbarrier pair (full / empty) per stage with expect_tx byte accounting
+//     (12.2.1 and 12.3.1 of the tutorial; "one warp loads with TMA" in the
+//     warp-specialisation paragraph of the JAX/Blackwell FP8 GEMM page);
+//   - warp 1: a single thread issues tcgen05.mma (kind::f8f6f4, or
+//     kind::mxf8f6f4.block_scale with UE8M0 scale factors read from tensor
+//     memory) into an fp32 accumulator in tensor memory (12.6.1-12.6.2);
+//   - warp 2 (block modes): stages the fp32 1x32 scales with cp.async,
+//     converts them to UE8M0 bytes in the layout tcgen05.cp expects, and marks
+//     the stage ready; the MMA thread copies them shared -> tensor memory;
+//   - warps 4..19: epilogue; each warp drains its 32-lane quarter of the
+//     accumulator (tcgen05.ld), releases it, scales / rounds and stores.
+//
+// Tensor-memory budget (Triton tutorial ch. 12, 12.8 Q3): a 128 x 256 fp32
+// accumulator is 256 columns.  Per-tensor mode double-buffers it (512 columns);
+// block mode keeps one accumulator plus one scale-factor slot per stage and
+// overlaps the epilogue by releasing the accumulator as soon as it has been
+// copied into registers.
+//
+// Every wait is bounded (globaltimer); on expiry the CTA records
+// FP8G_ERR_TIMEOUT in the status word, all roles leave their loops, in-flight
+// copies and MMAs are drained with bounded waits, and tensor memory is freed.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8g {
+
+namespace {
+
+constexpr int kThreads = 640;  // 20 warps
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 16;
+constexpr int kStgSlots = 4;   // fp32 scale staging ring depth (block modes)
+
+template <int MODE, int BN, int NUM_ACC, int STAGES>
+struct Cfg {
+    static constexpr bool kBlock = MODE != kModeTensor;
+    static constexpr int A_BYTES = kBM * kBK;
+    static constexpr int B_BYTES = BN * kBK;
+    static constexpr int SFA_BYTES = kBlock ? kBM * 4 : 0;
+    static constexpr int SFB_BYTES = kBlock ? BN * 4 : 0;
+    static constexpr int SF_ROWS = kBM + BN;
+    static constexpr int STG_BYTES = kBlock ? SF_ROWS * 16 : 0;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_STG = OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES);
+    static constexpr int OFF_BAR = OFF_STG + kStgSlots * STG_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_GROUP = OFF_MISC + 16;
+    static constexpr int GROUP_BYTES = 2 * (FP8G_MAX_EXPERTS + 1) * 4;
+    static constexpr int SMEM_USED = OFF_GROUP + GROUP_BYTES;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+    static constexpr int ACC_COLS = NUM_ACC * BN;
+    static constexpr int SF_COLS = kBlock ? (kBM / 32 + BN / 32) : 0;
+    static constexpr int SF_COL0 = ACC_COLS;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int CW = BN / 4;  // accumulator columns per epilogue warp
+
+    static_assert(ACC_COLS + STAGES * SF_COLS <= 512, "tensor memory over budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+    static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
+    static_assert(CW % 32 == 0, "epilogue chunk must be a multiple of 32 columns");
+};
+
+struct Tile {
+    int32_t row0, row_end, n0, e, pm, pn;
+};
+
+// Grouped raster order: bands of G tile-rows; inside a band walk down one
+// tile-column, then move to the next column.
+__device__ __forceinline__ void raster(int64_t t, int32_t npm, int32_t npn, int32_t G, int32_t &pm,
+                                       int32_t &pn) {
+    const int64_t band = (int64_t)G * npn;
+    const int64_t grp = t / band;
+    const int32_t first = (int32_t)(grp * G);
+    const int32_t height = min(npm - first, G);
+    const int32_t in_band = (int32_t)(t - grp * band);
+    pm = first + in_band % height;
+    pn = in_band / height;
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ Tile get_tile(int64_t t, const GemmParams &p, const int32_t *row_off,
+                                         const int32_t *tile_off) {
+    Tile ti;
+    if constexpr (MODE == kModeGrouped) {
+        int e = 0;
+        while (tile_off[e + 1] <= t) ++e;
+        const int32_t Me = row_off[e + 1] - row_off[e];
+        const int32_t npm_e = (Me + kBM - 1) / kBM;
+        raster(t - tile_off[e], npm_e, p.npn, kRasterG, ti.pm, ti.pn);
+        ti.row0 = row_off[e] + ti.pm * kBM;
+        ti.row_end = row_off[e + 1];
+        ti.e = e;
+    } else {
+        raster(t, p.npm, p.npn, kRasterG, ti.pm, ti.pn);
+        ti.row0 = ti.pm * kBM;
+        ti.row_end = (int32_t)p.M;
+        ti.e = 0;
+    }
+    ti.n0 = ti.pn * BN;
+    return ti;
+}
+
+__device__ __forceinline__ void record_error(const GemmParams &p, unsigned code, unsigned detail) {
+    if (atomicCAS(&p.status[0], 0u, code) == 0u) atomicExch(&p.status[1], detail);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting
+// (another role timed out) or when this wait itself exceeded the limit.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         const GemmParams &p, unsigned detail) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p, FP8G_ERR_TIMEOUT, detail);
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait: lane 0 waits, the outcome is broadcast, and the
+// warp re-converges before any .sync.aligned tcgen05 instruction follows.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag, const GemmParams &p,
+                                              unsigned detail) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, p, detail) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// fp32 scale (must be a positive power of two, or NaN) -> UE8M0 code.
+__device__ __forceinline__ uint32_t ue8m0_code(uint32_t bits, bool &bad) {
+    const uint32_t ex = (bits >> 23) & 0xFFu;
+    const uint32_t man = bits & 0x7FFFFFu;
+    if (ex == 0xFFu && man != 0u) return 0xFFu;  // NaN scale -> NaN code
+    if ((bits >> 31) != 0u || man != 0u || ex == 0u || ex == 0xFFu) bad = true;
+    return ex;
+}
+
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte-swizzled TMA tiles need 1024-byte alignment in the shared window
+    const uint32_t raw_base = ptx::smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C_::OFF_BAR);
+    auto bar_full = [&](int s) { return ptx::smem_addr(&bars[s]); };
+    auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[STAGES + s]); };
+    auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[2 * STAGES + a]); };
+    auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[2 * STAGES + NUM_ACC + a]); };
+    const uint32_t bar_drain = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC]);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C_::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C_::OFF_MISC + 4);
+    int32_t *row_off = reinterpret_cast<int32_t *>(smem + C_::OFF_GROUP);
+    int32_t *tile_off = row_off + (FP8G_MAX_EXPERTS + 1);
+
+    // ------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar_full(s), C_::kBlock ? 2 : 1);
+            ptx::mbar_init(bar_empty(s), 1);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            ptx::mbar_init(bar_accf(a), 1);
+            ptx::mbar_init(bar_acce(a), kEpiWarps);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C_::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    int64_t T = p.T;
+    if constexpr (MODE == kModeGrouped) {
+        // counts -> row offsets and tile offsets (experts in index order)
+        if (threadIdx.x < FP8G_MAX_EXPERTS)
+            tile_off[threadIdx.x] = threadIdx.x < p.E ? p.counts[threadIdx.x] : 0;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int64_t r = 0, tt = 0;
+            bool bad = false;
+            int32_t cnt[FP8G_MAX_EXPERTS];
+            for (int e = 0; e < p.E; ++e) {
+                cnt[e] = tile_off[e];
+                if (cnt[e] < 0) bad = true;
+            }
+            row_off[0] = 0;
+            for (int e = 0; e < p.E; ++e) {
+                const int32_t c = max(cnt[e], 0);
+                r += c;
+                row_off[e + 1] = (int32_t)(r < (int64_t)INT32_MAX ? r : (int64_t)INT32_MAX);
+            }
+            if (bad || r != p.M) {
+                bad = true;
+                if (blockIdx.x == 0) record_error(p, FP8G_ERR_INVALID_ARG, 1);
+            }
+            tile_off[0] = 0;
+            for (int e = 0; e < p.E; ++e) {
+                const int64_t Me = bad ? 0 : (row_off[e + 1] - row_off[e]);
+                tt += ((Me + kBM - 1) / kBM) * (int64_t)p.npn;
+                tile_off[e + 1] = (int32_t)tt;
+            }
+            if (blockIdx.x == 0 && p.offsets_out != nullptr)
+                for (int e = 0; e <= p.E; ++e) p.offsets_out[e] = row_off[e];
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if constexpr (MODE == kModeGrouped) T = tile_off[p.E];
+    const uint32_t tmem_base = *tmem_slot;
+
+    // ------------------------------------------------------------ roles
+    if (warp == 0) {
+        // ===== TMA producer =====
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+                const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off);
+                if constexpr (MODE == kModeGrouped) {
+                    if (p.tile_map_out != nullptr) {
+                        int4 v = make_int4(ti.e, ti.pm, ti.pn, 0);
+                        *reinterpret_cast<int4 *>(p.tile_map_out + 4 * t) = v;
+                    }
+                }
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
+                        goto roles_done;
+                    ptx::mbar_arrive_expect_tx(bar_full(stage), C_::TX_BYTES);
+                    ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, bar_full(stage),
+                                     kb * kBK, ti.row0);
+                    if constexpr (MODE == kModeGrouped)
+                        ptx::tma_load_3d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB,
+                                         bar_full(stage), kb * kBK, ti.n0, ti.e);
+                    else
+                        ptx::tma_load_2d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB,
+                                         bar_full(stage), kb * kBK, ti.n0);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ===== MMA issuer =====
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int64_t lt = 0;
+            for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+                const int acc = (int)(lt % NUM_ACC);
+                const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
+                if (!wait_bar(bar_acce(acc), acc_par ^ 1u, abort_flag, p, 1 * 256 + 64 + acc))
+                    goto roles_done;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_full(stage), phase, abort_flag, p, 1 * 256 + stage))
+                        goto roles_done;
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = sbase + C_::OFF_A + stage * C_::A_BYTES;
+                    const uint32_t b0 = sbase + C_::OFF_B + stage * C_::B_BYTES;
+                    if constexpr (C_::kBlock) {
+                        const uint32_t sf_tmem = tmem_base + C_::SF_COL0 + stage * C_::SF_COLS;
+                        const uint32_t sfa_s =
+                            sbase + C_::OFF_SF + stage * (C_::SFA_BYTES + C_::SFB_BYTES);
+                        const uint32_t sfb_s = sfa_s + C_::SFA_BYTES;
+                        ptx::tc_cp_32x128b_warpx4(sf_tmem, ptx::desc_sf_chunk(sfa_s));
+#pragma unroll
+                        for (int c = 0; c < BN / 128; ++c)
+                            ptx::tc_cp_32x128b_warpx4(sf_tmem + kBM / 32 + 4 * c,
+                                                      ptx::desc_sf_chunk(sfb_s + c * 512));
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                          ptx::desc_kmajor_sw128(b0 + k * 32),
+                                          ptx::idesc_mxf8(kBM, BN, (uint32_t)k), sf_tmem,
+                                          sf_tmem + kBM / 32, (kb | k) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            ptx::mma_f8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                        ptx::desc_kmajor_sw128(b0 + k * 32), ptx::idesc_f8(kBM, BN),
+                                        (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit(bar_empty(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                ptx::tc_commit(bar_accf(acc));
+            }
+        }
+    } else if (warp == 2) {
+        // ===== scale-factor stager (block modes) =====
+        if constexpr (C_::kBlock) {
+            // Work cursor over (tile, kb) in the same order as the producer.
+            struct Cursor {
+                int64_t t;
+                int kb;
+            };
+            Cursor iss{(int64_t)blockIdx.x, 0}, cvt{(int64_t)blockIdx.x, 0};
+            auto advance = [&](Cursor &c) {
+                if (++c.kb == p.num_kb) {
+                    c.kb = 0;
+                    c.t += gridDim.x;
+                }
+            };
+            const bool vec16 = (p.sfc % 4) == 0;
+            const int64_t a_rows = p.M;
+            auto issue = [&](const Cursor &c, int slot) {
+                const Tile ti = get_tile<MODE, BN>(c.t, p, row_off, tile_off);
+                const uint32_t dst0 = sbase + C_::OFF_STG + slot * C_::STG_BYTES;
+                const float *sfb_base = p.sb + (int64_t)ti.e * p.N * p.sfc;
+#pragma unroll
+                for (int i = 0; i < C_::SF_ROWS / 32; ++i) {
+                    const int r = lane + 32 * i;
+                    const float *src;
+                    bool valid;
+                    if (r < kBM) {
+                        const int64_t row = (int64_t)ti.row0 + r;
+                        valid = row < a_rows;
+                        src = p.sa + (valid ? row : 0) * p.sfc + (int64_t)c.kb * 4;
+                    } else {
+                        const int64_t row = (int64_t)ti.n0 + (r - kBM);
+                        valid = row < p.N;
+                        src = sfb_base + (valid ? row : 0) * p.sfc + (int64_t)c.kb * 4;
+                    }
+                    const uint32_t dst = dst0 + r * 16;
+                    if (vec16) {
+                        ptx::cp_async_16(dst, valid ? src : p.sa, valid ? 16u : 0u);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const bool ok = valid && ((int64_t)c.kb * 4 + j) < p.sfc;
+                            ptx::cp_async_4(dst + 4 * j, ok ? src + j : p.sa, ok ? 4u : 0u);
+                        }
+                    }
+                }
+            };
+            const int64_t total_iters =
+                (T > blockIdx.x) ? ((T - blockIdx.x + gridDim.x - 1) / gridDim.x) * p.num_kb : 0;
+            int64_t issued = 0;
+#pragma unroll 1
+            for (int i = 0; i < kStgSlots - 1; ++i) {
+                if (issued < total_iters) {
+                    issue(iss, i);
+                    advance(iss);
+                    ++issued;
+                }
+                ptx::cp_async_commit();
+            }
+            uint32_t stage = 0, phase = 0;
+            int slot = 0;
+            bool bad = false;
+            for (int64_t it = 0; it < total_iters; ++it) {
+                if (issued < total_iters) {
+                    issue(iss, (slot + kStgSlots - 1) % kStgSlots);
+                    advance(iss);
+                    ++issued;
+                }
+                ptx::cp_async_commit();
+                ptx::cp_async_wait<kStgSlots - 1>();
+                __syncwarp();
+                if (!wait_bar_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, 2 * 256 + stage))
+                    break;
+                const Tile ti = get_tile<MODE, BN>(cvt.t, p, row_off, tile_off);
+                const uint8_t *stg = smem + C_::OFF_STG + slot * C_::STG_BYTES;
+                uint8_t *chunk = smem + C_::OFF_SF + stage * (C_::SFA_BYTES + C_::SFB_BYTES);
+                const int kvalid = (int)(p.sfc - (int64_t)cvt.kb * 4 < 4 ? p.sfc - (int64_t)cvt.kb * 4 : 4);
+                // chunk layout: 32 rows ("datapaths") x 16 bytes; datapath d,
+                // word w holds the 4 K-block codes of tile row 32*w + d.
+#pragma unroll
+                for (int c = 0; c < 1 + BN / 128; ++c) {
+                    uint32_t words[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int r = c * 128 + 32 * w + lane;  // staged row
+                        const uint4 f = *reinterpret_cast<const uint4 *>(stg + r * 16);
+                        int64_t grow;
+                        bool rvalid;
+                        if (c == 0) {
+                            grow = (int64_t)ti.row0 + r;
+                            rvalid = grow < a_rows;
+                        } else {
+                            grow = (int64_t)ti.n0 + (r - kBM);
+                            rvalid = grow < p.N;
+                        }
+                        const uint32_t fb[4] = {f.x, f.y, f.z, f.w};
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t code = 127u;  // 1.0 for padding (data there is zero)
+                            if (rvalid && j < kvalid) code = ue8m0_code(fb[j], bad);
+                            word |= code << (8 * j);
+                        }
+                        words[w] = word;
+                    }
+                    *reinterpret_cast<uint4 *>(chunk + c * 512 + lane * 16) =
+                        make_uint4(words[0], words[1], words[2], words[3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_full(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                slot = (slot + 1) % kStgSlots;
+                advance(cvt);
+            }
+            ptx::cp_async_wait<0>();
+            if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ===== epilogue =====
+        const int ew = warp - kEpiWarp0;
+        const int q = warp & 3;           // tensor-memory lane quarter of this warp
+        const int col0 = (ew >> 2) * C_::CW;
+        float alpha = 1.0f;
+        if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        int64_t lt = 0;
+        for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+            const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off);
+            const int acc = (int)(lt % NUM_ACC);
+            const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
+            if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc)) break;
+            ptx::tc_fence_after();
+            uint32_t r[C_::CW / 32][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + col0;
+#pragma unroll
+            for (int c = 0; c < C_::CW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_acce(acc));
+
+            const int64_t row = (int64_t)ti.row0 + q * 32 + lane;
+            if (row < ti.row_end) {
+                const int64_t ncol0 = (int64_t)ti.n0 + col0;
+                if constexpr (OUT_F32) {
+                    float *out = reinterpret_cast<float *>(p.C) + row * p.N + ncol0;
+#pragma unroll
+                    for (int c = 0; c < C_::CW / 32; ++c)
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            if (ncol0 + c * 32 + v * 4 < p.N) {
+                                float4 o;
+                                o.x = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 0]));
+                                o.y = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 1]));
+                                o.z = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 2]));
+                                o.w = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 3]));
+                                *reinterpret_cast<float4 *>(out + c * 32 + v * 4) = o;
+                            }
+                        }
+                } else {
+                    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.C) + row * p.N + ncol0;
+#pragma unroll
+                    for (int c = 0; c < C_::CW / 32; ++c)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (ncol0 + c * 32 + v * 8 < p.N) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float lo =
+                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h]));
+                                    const float hi =
+                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h + 1]));
+                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                                    pk[h] = *reinterpret_cast<uint32_t *>(&b2);
+                                }
+                                *reinterpret_cast<uint4 *>(out + c * 32 + v * 8) =
+                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                        }
+                }
+            }
+        }
+    }
+
+roles_done:
+    __syncwarp();
+    __syncthreads();
+    if (*abort_flag) {
+        // Drain: wait (bounded) for this CTA's MMAs, then give in-flight TMA
+        // copies a bounded grace period before shared memory is released.
+        if (warp == 1 && lane == 0) {
+            ptx::tc_commit(bar_drain);
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar_drain, 0) && ptx::globaltimer() - t0 < p.timeout_ns) {
+            }
+        }
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 200000ull) {
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C_::TMEM_COLS);
+    }
+}
+
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
+cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+                       int grid, cudaStream_t stream) {
+    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
+    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32>;
+    // The shared-memory opt-in is per device; the flag races benignly (the
+    // attribute set is idempotent).
+    static unsigned long long attr_done = 0ull;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((attr_done & bit) == 0ull) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done |= bit;
+    }
+    kern<<<grid, kThreads, C_::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms) {
+    KernelChoice kc;
+    kc.BN = 256;
+    kc.split = 1;
+    kc.cluster = 1;
+    if (mode == kModeGrouped) {
+        kc.grid = num_sms;
+    } else {
+        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kc.BN - 1) / kc.BN);
+        kc.grid = (int)(tiles < num_sms ? tiles : num_sms);
+        if (kc.grid < 1) kc.grid = 1;
+    }
+    (void)K;
+    return kc;
+}
+
+cudaError_t launch_gemm(int mode, bool out_f32, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const GemmParams &p, const KernelChoice &kc, cudaStream_t stream) {
+    if (mode == kModeTensor) {
+        return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true>(tmA, tmB, p, kc.grid, stream)
+                       : launch_one<kModeTensor, 256, 2, 4, false>(tmA, tmB, p, kc.grid, stream);
+    } else if (mode == kModeBlock) {
+        return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true>(tmA, tmB, p, kc.grid, stream)
+                       : launch_one<kModeBlock, 256, 1, 4, false>(tmA, tmB, p, kc.grid, stream);
+    } else {
+        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true>(tmA, tmB, p, kc.grid, stream)
+                       : launch_one<kModeGrouped, 256, 1, 4, false>(tmA, tmB, p, kc.grid, stream);
+    }
+}
+
+}  // namespace fp8g

@@ -1,0 +1,61 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/fp8gemm.h"
+
+namespace fp8g {
+
+// Tile geometry of the GEMM kernels.  BM = 128 rows (the single-CTA tcgen05
+// M), BK = 128 E4M3 values = 128 bytes per row, which is exactly one 128-byte
+// swizzle span ("TMA block 128x128, 128-byte aligned" in the parameter
+// paragraph of the JAX/Blackwell FP8 GEMM page).
+constexpr int kBM = 128;
+constexpr int kBK = 128;
+constexpr int kRasterG = 8;  // grouped raster band height (GROUP_M)
+
+enum Mode : int { kModeTensor = 0, kModeBlock = 1, kModeGrouped = 2 };
+
+// Everything a GEMM kernel needs besides its tensor maps.
+struct GemmParams {
+    int64_t M;           // rows of A and C (grouped: total rows)
+    int64_t N;           // rows of B, columns of C
+    int64_t K;
+    int32_t num_kb;      // ceil(K / kBK)
+    int32_t npm, npn;    // tile grid (non-grouped)
+    int64_t T;           // tile count (non-grouped)
+    int32_t split;       // K-split factor (cluster size along K), 1 = none
+    int32_t kb_per_split;
+    const float *sa;     // per-tensor: &sA ; block: sfa [M, sfc]
+    const float *sb;     // per-tensor: &sB ; block: sfb [N, sfc] (grouped [E, N, sfc])
+    int64_t sfc;         // K / 32
+    void *C;
+    const int32_t *counts;
+    int32_t E;
+    int32_t *offsets_out;
+    int32_t *tile_map_out;
+    unsigned int *status;  // [0] = first error code, [1] = detail
+    uint64_t timeout_ns;
+};
+
+struct KernelChoice {
+    int BN;
+    int split;
+    int grid;
+    int cluster;
+};
+
+// gemm.cu
+cudaError_t launch_gemm(int mode, bool out_f32, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const GemmParams &p, const KernelChoice &kc, cudaStream_t stream);
+KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
+
+// quant.cu
+cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float *scale,
+                                   unsigned int *status, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, uint8_t *q,
+                                    float *scales, int num_sms, cudaStream_t s);
+
+}  // namespace fp8g

@@ -1,0 +1,187 @@
+/*
+ * fp8gemm — FP8 (E4M3) GEMM library for one GB300 GPU (sm_103a).
+ *
+ *   C[M,N] = (sA . A[M,K]) (sB . B[N,K])^T
+ *
+ * E4M3 operands ("fn" variant: max 448, no infinities, NaN = S.1111.111),
+ * fp32 accumulation in tensor memory, bf16 or fp32 output.  Three GEMM entry
+ * points: per-tensor scales, 1x32 block scales along K, and the grouped (MoE)
+ * form of the block-scaled GEMM.  Plus the operand quantiser that produces the
+ * codes and scales these entry points consume.
+ *
+ * Sources for the operation (page titles, sections):
+ *   [JAX-BW]  "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell
+ *             GPUs: TMA async loads and warp-level primitives" — format and
+ *             parameter paragraph (E4M3, 32-wide microscaling blocks, 128x128
+ *             TMA tiles, multicast of the shared operand), GEMM pseudo-kernel
+ *             (fp32 accumulate, down-converting store), MoE paragraph (grouped
+ *             GEMM over experts).
+ *   [TRITON-FP8] "Triton FP8 CUTLASS-named kernel benchmarking" — parameter
+ *             list (torch.float8_e4m3fn), monitoring checklist (2*M*N*K FLOPs).
+ *   [TUT-12]  "Triton tutorial ch. 12: Hopper / Blackwell architecture
+ *             features" — 12.2.3 (TMA alignment rules), 12.6.1-12.6.2 (TMEM,
+ *             tcgen05, MXFP8 micro-scaling), 12.7 (grouped raster order of a
+ *             persistent matmul), 12.8 Q3 (TMEM column budget).
+ *
+ * Conventions shared by every entry point
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     keeps no reference after the call returns.
+ *   - Calls are asynchronous on `stream` (stream order only).  Host-side
+ *     argument checks are synchronous: a call that fails them launches nothing
+ *     and returns the error.  Errors found on the device (a bad scale value,
+ *     inconsistent group counts, an internal wait that timed out) are recorded
+ *     in a per-device status word read by fp8_gemm_status().
+ *   - Row-major, densely packed: A[M,K] (row stride K), B[N,K] (row stride K),
+ *     C[M,N] (row stride N).  "K-contiguous B" means C = A B^T.
+ *   - Alignment [TUT-12 12.2.3]: every pointer 16-byte aligned, K % 16 == 0,
+ *     N * sizeof(out element) % 16 == 0.  Violations return FP8G_ERR_ALIGNMENT.
+ *   - M, N, K >= 1 (grouped: total_rows >= 0).  M and N need not be multiples
+ *     of the tile; out-of-range rows/columns are neither read past the end nor
+ *     written.
+ *   - Thread safety: calls from several host threads, on any streams, are safe.
+ *   - No call allocates device memory.  The library holds one status word per
+ *     device (a static device variable) and a host-side tensor-map cache.
+ */
+#ifndef FP8GEMM_H
+#define FP8GEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FP8G_API __attribute__((visibility("default")))
+#else
+#define FP8G_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8G_OK = 0,
+    FP8G_ERR_INVALID_ARG = 1,       /* null pointer, bad size, bad enum, counts inconsistent */
+    FP8G_ERR_ALIGNMENT = 2,         /* pointer / row-stride alignment rule broken */
+    FP8G_ERR_UNSUPPORTED_SHAPE = 3, /* K % 32 != 0 for block scales, E > 64, sizes too large */
+    FP8G_ERR_SCALE_FORMAT = 4,      /* a block scale is not a positive power of two */
+    FP8G_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+    FP8G_ERR_TIMEOUT = 6,           /* a device-side wait exceeded its limit; kernel aborted */
+    FP8G_ERR_DEVICE = 7             /* no usable sm_100-family device */
+} fp8g_status;
+
+typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
+
+/* Largest expert count accepted by fp8_grouped_gemm. */
+#define FP8G_MAX_EXPERTS 64
+
+/*
+ * Per-tensor-scaled GEMM [JAX-BW, GEMM pseudo-kernel; TRITON-FP8 dtype].
+ *   C[i,j] = out( fl32( fl32(sA*sB) * acc_ij ) ),  acc_ij = sum_k a_ik b_jk in fp32
+ * A: uint8 E4M3 codes [M,K]; B: uint8 E4M3 codes [N,K]; scale_a, scale_b: device
+ * pointers to one fp32 each; C: [M,N] bf16 (RNE) or fp32 per `out`.
+ * Errors: FP8G_ERR_INVALID_ARG (null pointer, M/N/K < 1, bad `out`),
+ * FP8G_ERR_ALIGNMENT, FP8G_ERR_CUDA (launch failure).
+ */
+FP8G_API fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                     void *C, int out, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * 1x32 block-scaled GEMM [JAX-BW microscaling paragraph; TUT-12 12.6.1 MXFP8].
+ *   C[i,j] = out( sum_kb sfa[i,kb] * sfb[j,kb] * sum_{k in kb} a_ik b_jk )
+ * sfa: fp32 [M, K/32] row-major; sfb: fp32 [N, K/32].  Every scale must be a
+ * positive power of two (2^-126 .. 2^127; NaN propagates as NaN); the tensor
+ * core applies it exactly as an 8-bit exponent.  Any other value records
+ * FP8G_ERR_SCALE_FORMAT in the status word (the output is then unspecified).
+ * K % 32 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE).  Other rules as fp8_gemm.
+ * Skinny problems (few output tiles) split K across a cluster of CTAs that
+ * reduce through distributed shared memory; this needs no workspace.
+ */
+FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
+                                 const float *sfb, void *C, int out, int64_t M, int64_t N,
+                                 int64_t K, cudaStream_t stream);
+
+/*
+ * Grouped (MoE) block-scaled GEMM [JAX-BW MoE paragraph].
+ * Expert e owns rows [off_e, off_e + counts[e]) of A and C, off = exclusive
+ * prefix sum of counts; those rows multiply B[e]:
+ *   C[r, :] = blockscaled(A[r, :], B[e])   for off_e <= r < off_e + counts[e]
+ * A: [total_rows, K] (rows already gathered per expert, expert-contiguous);
+ * B: [E, N, K]; sfa: fp32 [total_rows, K/32]; sfb: fp32 [E, N, K/32];
+ * C: [total_rows, N]; counts: DEVICE int32[E], each >= 0, summing to total_rows
+ * (checked on the device: a mismatch records FP8G_ERR_INVALID_ARG and writes
+ * no output).  Empty experts produce no tiles and no rows.
+ * offsets_out (nullable): device int32[E+1] receives the exclusive prefix.
+ * tile_map_out (nullable): device int32[4 * max_tiles] (see fp8g_grouped_plan)
+ * receives, for linear tile t, (expert, m_tile, n_tile, 0): experts in index
+ * order, expert e's ceil(M_e/BM)*ceil(N/BN) tiles in the grouped raster order.
+ * Entries past the actual tile count are left untouched.
+ * 1 <= E <= FP8G_MAX_EXPERTS.  Other rules as fp8_gemm_blockscaled.
+ */
+FP8G_API fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, const float *sfb,
+                             void *C, int out, const int32_t *counts, int32_t E, int64_t N,
+                             int64_t K, int64_t total_rows, int32_t *offsets_out,
+                             int32_t *tile_map_out, cudaStream_t stream);
+
+/*
+ * Tile configuration fp8_grouped_gemm launches for (N, K, total_rows, E):
+ * tile height BM, width BN, raster group height G, and an upper bound on the
+ * tile count (the capacity tile_map_out needs, in 4-int32 entries).
+ * Host-only, synchronous.  Any output pointer may be null.
+ */
+FP8G_API fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
+                              int32_t *BN, int32_t *G, int64_t *max_tiles);
+
+/*
+ * Tile configuration fp8_gemm / fp8_gemm_blockscaled launch for a shape:
+ * BM, BN, raster group G, K-split factor (1 = none) and grid size in CTAs.
+ * block = 0 per-tensor, 1 block-scaled.  Host-only; needs the current device
+ * to size the grid (FP8G_ERR_DEVICE if none).  Any output pointer may be null.
+ */
+FP8G_API fp8g_status fp8g_gemm_plan(int block, int64_t M, int64_t N, int64_t K, int32_t *BM, int32_t *BN,
+                           int32_t *G, int32_t *split_k, int32_t *grid);
+
+/*
+ * Operand quantiser [JAX-BW microscaling paragraph and the fine-grained
+ * quantisation advice; TRITON-FP8 dtype].
+ * x: device fp32 [rows, cols] row-major; q: device uint8 [rows, cols].
+ * block == 0: per-tensor.  s = fl32(amax/448) over the non-NaN |x| (s = 1 if
+ *   that is 0); scales: device fp32[1] receives s.
+ * block == 32: 1x32 blocks along cols (cols % 32 == 0).  Each block's s is the
+ *   smallest power of two with 448*s >= amax (clamped to 2^-126..2^127; 1 for
+ *   an all-zero block); scales: device fp32 [rows, cols/32].
+ * q = E4M3(fl32(x / s)) rounded to nearest even, saturated to +-448; NaN -> 0x7F.
+ * Alignment: x 16 B, q 8 B aligned; cols % 8 == 0 for block == 0.
+ * Per-tensor mode runs three kernels (amax, quantise, store s).
+ */
+FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32_t block,
+                               uint8_t *q, float *scales, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word (FP8G_OK if no kernel recorded an error since the last call).
+ * `detail` (nullable) receives a kernel-specific code for the first error
+ * (for a timeout: role * 256 + pipeline stage).
+ */
+FP8G_API fp8g_status fp8_gemm_status(cudaStream_t stream, int32_t *detail);
+
+/* Static English description of a status code. */
+FP8G_API const char *fp8g_status_string(fp8g_status status);
+
+/*
+ * Device-side wait limit in milliseconds for kernels launched after this call
+ * (default 2000, or the FP8G_WAIT_TIMEOUT_MS environment variable at load).
+ * 0 restores the default.
+ */
+FP8G_API void fp8g_set_wait_timeout_ms(uint32_t ms);
+
+/* Drops the host tensor-map cache.  Safe to call at any time. */
+FP8G_API void fp8g_shutdown(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+FP8G_API int fp8g_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H */

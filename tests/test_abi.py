@@ -1,0 +1,88 @@
+"""The C ABI library (no GPU needed): it builds, loads, exports every function
+include/fp8gemm.h declares, and its host-side argument checks return the
+documented status codes before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_block_scaled_06_gb300 as fp8g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(fp8\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert {"fp8_gemm", "fp8_gemm_blockscaled", "fp8_grouped_gemm",
+            "fp8g_quantize_e4m3", "fp8_gemm_status"} <= names
+    assert names == set(fp8g.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(fp8g):
+    lib = ctypes.CDLL(fp8g.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(fp8g):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fp8g.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    ours = {ln.split()[-1] for ln in out.splitlines() if " T " in ln and "fp8" in ln}
+    assert ours == _declared_functions()
+
+
+def test_status_strings(fp8g):
+    assert fp8g.fp8g_status_string(0) == "ok"
+    for code in range(1, 8):
+        assert fp8g.fp8g_status_string(code) not in ("ok", "unknown status")
+    assert fp8g.fp8g_version() >= 100
+
+
+def _err(fn, *args):
+    with pytest.raises(fp8g.Fp8gError) as e:
+        fn(*args)
+    return e.value.status
+
+
+def test_host_argument_checks(fp8g):
+    P = 1 << 20                                   # a 16-byte aligned fake address; never dereferenced
+    assert _err(fp8g.fp8_gemm, 0, P, P, P, P, 0, 8, 8, 16, 0) == fp8g.FP8G_ERR_INVALID_ARG
+    assert _err(fp8g.fp8_gemm, P, P, P, P, P, 3, 8, 8, 16, 0) == fp8g.FP8G_ERR_INVALID_ARG
+    assert _err(fp8g.fp8_gemm, P, P, P, P, P, 0, 0, 8, 16, 0) == fp8g.FP8G_ERR_INVALID_ARG
+    assert _err(fp8g.fp8_gemm, P + 8, P, P, P, P, 0, 8, 8, 16, 0) == fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(fp8g.fp8_gemm, P, P, P, P, P, 0, 8, 8, 24, 0) == fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(fp8g.fp8_gemm, P, P, P, P, P, 0, 8, 4, 16, 0) == fp8g.FP8G_ERR_ALIGNMENT  # N*2 % 16
+    assert _err(fp8g.fp8_gemm, P, P, P, P, P, 1, 8, 2, 16, 0) == fp8g.FP8G_ERR_ALIGNMENT  # N*4 % 16
+    assert _err(fp8g.fp8_gemm_blockscaled, P, P, P, P, P, 0, 8, 8, 48, 0) == \
+        fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(fp8g.fp8_gemm_blockscaled, P, P, P + 4, P, P, 0, 8, 8, 64, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(fp8g.fp8_grouped_gemm, P, P, P, P, P, 0, P, 65, 8, 64, 8, None, None, 0) == \
+        fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(fp8g.fp8_grouped_gemm, P, P, P, P, P, 0, 0, 2, 8, 64, 8, None, None, 0) == \
+        fp8g.FP8G_ERR_INVALID_ARG
+    assert _err(fp8g.fp8_grouped_gemm, P, P, P, P, P, 0, P, 2, 8, 64, 8, None, P + 4, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(fp8g.fp8g_quantize_e4m3, P, 4, 40, 32, P, P, 0) == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(fp8g.fp8g_quantize_e4m3, P, 4, 64, 16, P, P, 0) == fp8g.FP8G_ERR_INVALID_ARG
+
+
+def test_grouped_plan_host_only(fp8g):
+    p = fp8g.fp8g_grouped_plan(14336, 4096, 32768, 8)
+    assert p["BM"] == 128 and p["G"] == 8 and p["BN"] in (128, 256)
+    npn = -(-14336 // p["BN"])
+    assert p["max_tiles"] == (32768 // 128 + 8) * npn

@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance (per element): |C - C_ref| <= 2^-8 * sum_k |sA a_ik||sB b_jk| + 1 bf16
+ulp(|C_ref|).  It covers fp32 accumulation in any order (K * 2^-24 << 2^-8 for
+K <= 2^13) plus the output rounding.  Exact cases (identity / permutation /
+exhaustive codes) are compared bit for bit; quantiser codes and scales are
+always bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import fp8_block_scaled_06_gb300 as fp8g
+from gpu_util import assert_codes_equal, assert_within, oracle_out, quant_both, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fp8g, oracle_lib):
+    torch.cuda.init()
+    yield
+
+
+def _tensor_case(A, B, out):
+    qa, sa, qa_o, sa_o = quant_both(A, 0)
+    qb, sb, qb_o, sb_o = quant_both(B, 0)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, False, out)
+    ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, False, oracle_out(out))
+    return C, ref, bound
+
+
+def _block_case(A, B, out):
+    qa, sa, qa_o, sa_o = quant_both(A, 32)
+    qb, sb, qb_o, sb_o = quant_both(B, 32)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, True, out)
+    ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, True, oracle_out(out))
+    return C, ref, bound
+
+
+# ---------------------------------------------------------------- quantiser
+@pytest.mark.parametrize("rows,cols", [(256, 256), (300, 320), (1, 32), (7, 4096)])
+def test_quantize_block32_bitexact(rows, cols):
+    g = torch.Generator().manual_seed(rows + cols)
+    x = torch.randn(rows, cols, generator=g) * torch.exp(torch.randn(rows, 1, generator=g) * 3)
+    if rows > 2 and cols >= 96:
+        x[1, :32] = 0.0                                   # zero block
+        x[2, 32:64] = 1e-40                               # subnormal block
+        x[0, 5] = float("nan")
+        x[0, 70] = float("inf")
+        x[1, 40] = -0.0
+    qg, sg, qo, so = quant_both(x, 32)
+    assert_codes_equal(qg, sg, qo, so)
+
+
+@pytest.mark.parametrize("rows,cols", [(256, 256), (100, 72), (3, 8)])
+def test_quantize_tensor_bitexact(rows, cols):
+    g = torch.Generator().manual_seed(rows * cols)
+    x = torch.randn(rows, cols, generator=g) * 7
+    x[0, 0] = float("nan")
+    qg, sg, qo, so = quant_both(x, 0)
+    assert_codes_equal(qg, sg, qo, so)
+
+
+# --------------------------------------------------------------- per-tensor
+def test_square256_bf16():
+    w = synth.square_tensor(256, seed=0, out="bf16")
+    C, ref, bound = _tensor_case(w.A, w.B, "bf16")
+    assert_within(C, ref, bound, "256^3 per-tensor bf16")
+
+
+def test_square1024_f32():
+    w = synth.square_tensor(1024, seed=1, out="f32")
+    C, ref, bound = _tensor_case(w.A, w.B, "f32")
+    assert_within(C, ref, bound, "1024^3 per-tensor f32")
+
+
+@pytest.mark.parametrize("kind", ["identity", "permutation"])
+def test_exact_identity_permutation(kind):
+    cases = synth.exact_cases(1024, seed=1)
+    C, ref, _ = _tensor_case(cases["A"], cases[kind], "f32")
+    assert np.array_equal(C.view(np.uint32), ref.view(np.uint32)), f"{kind}: not bit-exact"
+
+
+@pytest.mark.parametrize("M,N,K,out", [(200, 264, 384, "bf16"), (1, 8, 16, "bf16"),
+                                       (130, 520, 48, "f32"), (257, 8, 272, "bf16"),
+                                       (129, 4, 1040, "f32")])
+def test_tensor_ragged(M, N, K, out):
+    A = synth.normal((M, K), seed=M)
+    B = synth.normal((N, K), seed=N + 1000)
+    C, ref, bound = _tensor_case(A, B, out)
+    assert_within(C, ref, bound, f"per-tensor {M}x{N}x{K} {out}")
+
+
+# ------------------------------------------------------------- block-scaled
+def test_skinny_128x4096x4096_full():
+    w = synth.skinny_block()
+    C, ref, bound = _block_case(w.A, w.B, "bf16")
+    assert_within(C, ref, bound, "skinny 128x4096x4096")
+
+
+@pytest.mark.parametrize("M,N,K,out", [(300, 392, 320, "bf16"), (129, 136, 128, "f32"),
+                                       (64, 1024, 4096, "bf16"), (1, 8, 32, "bf16"),
+                                       (384, 512, 2048, "f32")])
+def test_block_ragged(M, N, K, out):
+    g = torch.Generator().manual_seed(M * 7 + N)
+    A = synth.with_outliers(synth.normal((M, K), seed=M), g)
+    B = synth.normal((N, K), seed=N) * torch.exp(torch.randn(N, 1, generator=g) * 2)
+    C, ref, bound = _block_case(A, B, out)
+    assert_within(C, ref, bound, f"block {M}x{N}x{K} {out}")
+
+
+def test_block_exhaustive_codes_exact():
+    """Every finite E4M3 code goes through the block-scaled MMA: A's rows hold
+    all 254 finite codes (rotated per row), B = identity (code 1.0), scales 1."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    K = 256
+    M = 128
+    A = np.zeros((M, K), np.uint8)
+    for i in range(M):
+        A[i, :codes.size] = np.roll(codes, i)
+    eye = np.zeros((K, K), np.uint8)
+    eye[np.arange(K), np.arange(K)] = 0x38
+    sfa = np.ones((M, K // 32), np.float32)
+    sfb = np.ones((K, K // 32), np.float32)
+    C = run_gemm(torch.from_numpy(A).cuda(), torch.from_numpy(sfa).cuda(),
+                 torch.from_numpy(eye).cuda(), torch.from_numpy(sfb).cuda(), True, "f32")
+    ref, _, _ = oracle.gemm(A, eye, sfa, sfb, True, oracle.OUT_F32)
+    assert np.array_equal(C.view(np.uint32), ref.view(np.uint32))
+
+
+def test_block_scale_layout_exact():
+    """Distinct power-of-two scales per (row, K-block) on both operands with
+    single-nonzero dot products make every output exact: any mix-up of the
+    scale-factor layout (row, K-block, operand) changes a value."""
+    M, N, K = 256, 512, 512
+    rng = np.random.default_rng(5)
+    A = np.zeros((M, K), np.uint8)
+    B = np.zeros((N, K), np.uint8)
+    ka = rng.integers(0, K, size=M)
+    A[np.arange(M), ka] = rng.integers(0x30, 0x50, size=M)
+    # B row j has one nonzero, at the K position of A row (j % M)
+    B[np.arange(N), ka[np.arange(N) % M]] = rng.integers(0x30, 0x50, size=N)
+    sfa = (2.0 ** rng.integers(-20, 20, size=(M, K // 32))).astype(np.float32)
+    sfb = (2.0 ** rng.integers(-20, 20, size=(N, K // 32))).astype(np.float32)
+    C = run_gemm(torch.from_numpy(A).cuda(), torch.from_numpy(sfa).cuda(),
+                 torch.from_numpy(B).cuda(), torch.from_numpy(sfb).cuda(), True, "f32")
+    ref, _, _ = oracle.gemm(A, B, sfa, sfb, True, oracle.OUT_F32)
+    assert np.array_equal(C.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+def test_large_block_sampled(n):
+    """Full-size large block-scaled GEMM, run exactly as the bench runs it;
+    2048 sampled outputs (plus the four corners) against the oracle."""
+    w = synth.large_block(n, seed=3)
+    C, qa_o, sa_o, qb_o, sb_o = _block_full(w)
+    rng = np.random.default_rng(n)
+    pi = np.concatenate([rng.integers(0, n, 2048), [0, 0, n - 1, n - 1]])
+    pj = np.concatenate([rng.integers(0, n, 2048), [0, n - 1, 0, n - 1]])
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16)
+    assert_within(C[pi, pj], ref, bound, f"{n}^3 block sampled")
+
+
+def _block_full(w):
+    qa, sa, qa_o, sa_o = quant_both(w.A, 32)
+    qb, sb, qb_o, sb_o = quant_both(w.B, 32)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, True, w.out)
+    return C, qa_o, sa_o, qb_o, sb_o
+
+
+# ------------------------------------------------------------------- errors
+def test_scale_format_error_recorded():
+    M = N = K = 256
+    qa = torch.zeros(M, K, dtype=torch.uint8, device="cuda")
+    qb = torch.zeros(N, K, dtype=torch.uint8, device="cuda")
+    sfa = torch.ones(M, K // 32, device="cuda")
+    sfb = torch.ones(N, K // 32, device="cuda")
+    sfa[3, 2] = 0.75                                  # not a power of two
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_gemm_blockscaled(qa, qb, sfa, sfb, C, fp8g.FP8G_OUT_BF16, M, N, K)
+    st, _ = fp8g.fp8_gemm_status()
+    assert st == fp8g.FP8G_ERR_SCALE_FORMAT
+    st, _ = fp8g.fp8_gemm_status()
+    assert st == fp8g.FP8G_OK                         # read clears
+
+
+def test_host_checks_reject_without_launch():
+    qa = torch.zeros(128, 64, dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, device="cuda")
+    C = torch.empty(128, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fp8g.Fp8gError) as e:
+        fp8g.fp8_gemm(qa, qa, s, s, C, 0, 128, 128, 40)        # K % 16 != 0
+    assert e.value.status == fp8g.FP8G_ERR_ALIGNMENT
+    with pytest.raises(fp8g.Fp8gError) as e:
+        fp8g.fp8_gemm(qa.data_ptr() + 1, qa, s, s, C, 0, 128, 128, 64)
+    assert e.value.status == fp8g.FP8G_ERR_ALIGNMENT
+    with pytest.raises(fp8g.Fp8gError) as e:
+        fp8g.fp8_gemm_blockscaled(qa, qa, s, s, C, 0, 128, 128, 48)  # K % 32 != 0
+    assert e.value.status == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert fp8g.fp8_gemm_status()[0] == fp8g.FP8G_OK
+
+
+def test_plan_reports_tiles():
+    p = fp8g.fp8g_gemm_plan(1, 8192, 8192, 8192)
+    assert p["BM"] == 128 and p["BN"] in (128, 256) and p["G"] == 8
+    assert 1 <= p["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count

@@ -1,0 +1,125 @@
+"""GPU parity of the grouped (MoE) block-scaled GEMM: outputs within the
+tolerance, problem offsets and tile map bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import fp8_block_scaled_06_gb300 as fp8g
+from gpu_util import assert_codes_equal, assert_within, quant_both
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fp8g, oracle_lib):
+    yield
+
+
+def _quant_grouped(w):
+    E, N, K = w.B.shape
+    qa, sa, qa_o, sa_o = quant_both(w.A, 32)
+    qb, sb, qb_o, sb_o = quant_both(w.B.reshape(E * N, K), 32)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    return (qa, sa, qb.reshape(E, N, K), sb.reshape(E, N, K // 32),
+            qa_o, sa_o, qb_o.reshape(E, N, K), sb_o.reshape(E, N, K // 32))
+
+
+def _run_grouped(qa, sa, qb, sb, counts, out="bf16"):
+    E, N, K = qb.shape
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, E)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    C = torch.full((max(rows, 1), N), float("nan"), dtype=dt, device="cuda")
+    counts_d = torch.from_numpy(counts.astype(np.int32)).cuda()
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    tmap = torch.full((max(plan["max_tiles"], 1), 4), -1, dtype=torch.int32, device="cuda")
+    o = fp8g.FP8G_OUT_BF16 if out == "bf16" else fp8g.FP8G_OUT_F32
+    fp8g.fp8_grouped_gemm(qa, qb, sa, sb, C, o, counts_d, E, N, K, rows, offs, tmap)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    return C[:rows].float().cpu().numpy(), offs.cpu().numpy(), tmap.cpu().numpy(), plan
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([130, 0, 5, 257], 264, 256),
+    ([1, 1, 4, 0, 0, 300, 2, 128], 512, 384),
+    ([0, 0, 3], 136, 128),
+    ([129], 256, 4160),
+])
+def test_grouped_small_full(counts, N, K):
+    counts = np.array(counts, np.int32)
+    w = synth.small_grouped(counts, N, K, seed=int(counts.sum()) + N)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
+    ref, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts, oracle.OUT_BF16)
+    assert_within(C, ref, bound, f"grouped {counts.tolist()} N={N} K={K}")
+    assert np.array_equal(offs, oracle.grouped_offsets(counts))
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert np.array_equal(tmap[:want.shape[0]], want)
+    assert (tmap[want.shape[0]:] == -1).all()
+
+
+def test_grouped_equals_per_expert_gemms():
+    counts = np.array([200, 0, 77, 130], np.int32)
+    N, K = 392, 512
+    w = synth.small_grouped(counts, N, K, seed=3)
+    qa, sa, qb, sb, *_ = _quant_grouped(w)
+    C, _, _, _ = _run_grouped(qa, sa, qb, sb, counts)
+    off = 0
+    for e, m in enumerate(counts.tolist()):
+        if m == 0:
+            continue
+        Ce = torch.empty(m, N, dtype=torch.bfloat16, device="cuda")
+        fp8g.fp8_gemm_blockscaled(qa[off:off + m], qb[e], sa[off:off + m], sb[e], Ce,
+                                  fp8g.FP8G_OUT_BF16, m, N, K)
+        # same tile math, same accumulation order -> identical bits
+        assert np.array_equal(Ce.float().cpu().numpy(), C[off:off + m])
+        off += m
+
+
+def test_grouped_counts_mismatch_is_reported():
+    counts = np.array([10, 20], np.int32)
+    N, K = 128, 128
+    qa = torch.zeros(31, K, dtype=torch.uint8, device="cuda")      # sum(counts) = 30 != 31
+    qb = torch.zeros(2, N, K, dtype=torch.uint8, device="cuda")
+    sa = torch.ones(31, K // 32, device="cuda")
+    sb = torch.ones(2, N, K // 32, device="cuda")
+    C = torch.full((31, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_grouped_gemm(qa, qb, sa, sb, C, 0, torch.from_numpy(counts).cuda(), 2, N, K, 31)
+    st, _ = fp8g.fp8_gemm_status()
+    assert st == fp8g.FP8G_ERR_INVALID_ARG
+    assert (C.float() == 5.0).all()                                 # nothing written
+
+
+def test_moe_full_size_sampled():
+    """The MoE workload at full size (8 experts, N=14336, K=4096, 32768 routed
+    rows with Zipf counts incl. empty experts): offsets and tile map bit-exact,
+    4096 sampled outputs against the oracle."""
+    w = synth.moe_grouped()
+    counts = w.counts
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
+    E, N, K = qb_o.shape
+    assert np.array_equal(offs, oracle.grouped_offsets(counts))
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert np.array_equal(tmap[:want.shape[0]], want)
+    rng = np.random.default_rng(4)
+    rows = int(counts.sum())
+    pi = rng.integers(0, rows, 4096)
+    pj = rng.integers(0, N, 4096)
+    offs_o = oracle.grouped_offsets(counts)
+    expert = np.searchsorted(offs_o, pi, side="right") - 1
+    got = np.empty(pi.size, np.float32)
+    ref = np.empty(pi.size, np.float32)
+    bound = np.empty(pi.size, np.float64)
+    for e in np.unique(expert):
+        sel = np.flatnonzero(expert == e)
+        r, b, _ = oracle.gemm_sample(qa_o, qb_o[e], sa_o, sb_o[e], True, pi[sel], pj[sel],
+                                     oracle.OUT_BF16)
+        ref[sel] = r
+        bound[sel] = b
+        got[sel] = C[pi[sel], pj[sel]]
+    assert_within(got, ref, bound, "MoE sampled")
