@@ -183,19 +183,56 @@ ORACLE_EXPORT float oracle_pow2_scale(float amax) {
     return ldexpf(1.0f, e);
 }
 
+typedef struct {
+    const float *x;
+    uint8_t *q;
+    float *scales;
+    int64_t cols, r0, r1;
+} quant_job;
+
+static void *quant_block32_rows(void *arg);
+
 /* 1x32 block quantisation along the contiguous (K) axis.  cols % 32 == 0.
- * scales: [rows, cols/32] fp32, each a power of two. */
+ * scales: [rows, cols/32] fp32, each a power of two.  Rows are independent, so
+ * they are split across up to 64 threads (no effect on the result). */
 ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t cols,
                                            uint8_t *q, float *scales) {
+    int nt = (int)(rows * cols / (1 << 20));
+    if (nt < 1) nt = 1;
+    if (nt > 64) nt = 64;
+    if (nt > rows) nt = (int)rows;
+    pthread_t tid[64];
+    quant_job jobs[64];
+    int64_t per = (rows + nt - 1) / nt;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].x = x; jobs[t].q = q; jobs[t].scales = scales; jobs[t].cols = cols;
+        jobs[t].r0 = t * per < rows ? t * per : rows;
+        jobs[t].r1 = (t + 1) * per < rows ? (t + 1) * per : rows;
+        if (nt == 1 || pthread_create(&tid[t], NULL, quant_block32_rows, &jobs[t]) != 0) {
+            quant_block32_rows(&jobs[t]);
+            tid[t] = 0;
+        }
+    }
+    for (int t = 0; t < nt; ++t)
+        if (nt > 1 && tid[t]) pthread_join(tid[t], NULL);
+}
+
+static void *quant_block32_rows(void *arg) {
+    quant_job *j = (quant_job *)arg;
+    const float *x = j->x;
+    uint8_t *q = j->q;
+    float *scales = j->scales;
+    int64_t cols = j->cols;
     int64_t nb = cols / 32;
-    for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t r = j->r0; r < j->r1; ++r) {
         for (int64_t b = 0; b < nb; ++b) {
             const float *blk = x + r * cols + b * 32;
             float s = oracle_pow2_scale(amax_of(blk, 32, 1));
             scales[r * nb + b] = s;
-            for (int j = 0; j < 32; ++j) q[r * cols + b * 32 + j] = oracle_e4m3_encode(blk[j] / s);
+            for (int k = 0; k < 32; ++k) q[r * cols + b * 32 + k] = oracle_e4m3_encode(blk[k] / s);
         }
     }
+    return NULL;
 }
 
 /* ------------------------------------------------------------------ */
