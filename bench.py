@@ -1,7 +1,7 @@
 """FP8 GEMM throughput on GB300: TFLOPS and fraction of the roofline.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload large8192|large4096|skinny|moe|square1024]
+                [--workload large8192|large4096|skinny|moe|square1024|tensor8192]
 
 One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
 scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
@@ -39,6 +39,7 @@ WORKLOADS = {
     "skinny": dict(kind="block", M=128, N=4096, K=4096, seed=2),
     "moe": dict(kind="grouped", M=32768, N=14336, K=4096, seed=4),
     "square1024": dict(kind="tensor", M=1024, N=1024, K=1024, seed=1),
+    "tensor8192": dict(kind="tensor", M=8192, N=8192, K=8192, seed=3),
 }
 METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
 
@@ -130,7 +131,7 @@ def make_inputs(wl: dict, device):
         counts = torch.from_numpy(w.counts).to(device)
         return w, dict(qa=qa, sa=sa, qb=qb, sb=sb, counts=counts)
     if wl["kind"] == "tensor":
-        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32")
+        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")
         bs = 0
     elif wl["M"] == 128:
         w = synth.skinny_block(seed=wl["seed"])
@@ -371,7 +372,7 @@ def reference_arm(args, wl, world, rank):
     if wl["kind"] == "grouped":
         w = synth.moe_grouped(seed=wl["seed"])
     elif wl["kind"] == "tensor":
-        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32")
+        w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")
     elif wl["M"] == 128:
         w = synth.skinny_block(seed=wl["seed"])
     else:

@@ -1,5 +1,6 @@
 // C ABI of the FP8 GEMM library: argument checks, TMA tensor-map encoding
-// (cached), per-device status word, kernel choice and launch.
+// (cached), per-device status word, scale packing temporaries, kernel choice
+// and launch.
 //
 // TMA rules checked on the host before any launch (Triton tutorial ch. 12,
 // 12.2.3): base address 16-byte aligned, innermost stride 1, every other
@@ -45,6 +46,28 @@ uint64_t timeout_ns() {
     return t;
 }
 
+cudaMemPool_t g_pool[kMaxDevices] = {};
+bool g_pool_ok[kMaxDevices] = {};
+
+// Library-owned device memory pool for the packed scale temporaries: memory
+// returned with cudaFreeAsync stays in the pool (release threshold = max), so
+// steady-state calls do not touch the driver allocator.
+fp8g_status scale_pool(int dev, cudaMemPool_t &pool) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_pool_ok[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&g_pool[dev], &props) != cudaSuccess) return FP8G_ERR_CUDA;
+        uint64_t thr = ~0ull;
+        cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &thr);
+        g_pool_ok[dev] = true;
+    }
+    pool = g_pool[dev];
+    return FP8G_OK;
+}
+
 struct DevInfo {
     int dev;
     int num_sms;
@@ -87,18 +110,17 @@ fp8g_status device_info(DevInfo &di) {
 // ------------------------------------------------------------ tensor maps
 struct TmapKey {
     const void *ptr;
-    int rank;
+    int rank, dtype, esize, swizzle, dev;
     uint64_t dims[3];
     uint32_t box[3];
-    int dev;
     bool operator==(const TmapKey &o) const {
-        return ptr == o.ptr && rank == o.rank && dev == o.dev &&
-               std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+        return ptr == o.ptr && rank == o.rank && dtype == o.dtype && esize == o.esize &&
+               swizzle == o.swizzle && dev == o.dev && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
                std::memcmp(box, o.box, sizeof box) == 0;
     }
 };
 
-constexpr int kCacheSize = 64;
+constexpr int kCacheSize = 128;
 struct TmapEntry {
     TmapKey key;
     CUtensorMap map;
@@ -107,13 +129,17 @@ struct TmapEntry {
 TmapEntry g_cache[kCacheSize];
 int g_cache_next = 0;
 
-// uint8 tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost, contiguous),
-// 128-byte swizzle, zero fill out of bounds.
-fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint32_t *box, int dev,
-                    CUtensorMap &out) {
+// Dense row-major tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost,
+// contiguous), element size esize bytes, zero fill out of bounds.
+fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int esize, int rank,
+                        const uint64_t *dims, const uint32_t *box, CUtensorMapSwizzle swz, int dev,
+                        CUtensorMap &out) {
     TmapKey key{};
     key.ptr = ptr;
     key.rank = rank;
+    key.dtype = (int)dtype;
+    key.esize = esize;
+    key.swizzle = (int)swz;
     key.dev = dev;
     for (int i = 0; i < rank; ++i) {
         key.dims[i] = dims[i];
@@ -127,7 +153,7 @@ fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint3
         }
     cuuint64_t gdim[3], gstride[2];
     cuuint32_t bdim[3], estr[3];
-    uint64_t stride = 1;
+    uint64_t stride = (uint64_t)esize;
     for (int i = 0; i < rank; ++i) {
         gdim[i] = dims[i];
         bdim[i] = box[i];
@@ -136,9 +162,8 @@ fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint3
         stride *= dims[i];
     }
     CUtensorMap m;
-    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank,
-                                const_cast<void *>(ptr), gdim, gstride, bdim, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUresult r = g_encode(&m, dtype, (cuuint32_t)rank, const_cast<void *>(ptr), gdim, gstride,
+                                bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return FP8G_ERR_CUDA;
@@ -149,6 +174,13 @@ fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint3
     e.used = true;
     out = m;
     return FP8G_OK;
+}
+
+// E4M3 operand: 128-byte swizzle (the tcgen05 K-major SW128 layout).
+fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint32_t *box, int dev,
+                    CUtensorMap &out) {
+    return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rank, dims, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -197,25 +229,54 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.status = di.status;
     p.timeout_ns = timeout_ns();
 
-    CUtensorMap tmA, tmB;
+    GemmMaps maps;
+    const int64_t rows_a = M > 0 ? M : 1;  // grouped with zero rows: A is never read
+    const void *a_ptr = M > 0 ? A : B;
     {
-        // grouped with zero rows: A is never read; describe a 1-row tensor
-        const void *a_ptr = M > 0 ? A : B;
-        const uint64_t dA[2] = {(uint64_t)K, (uint64_t)(M > 0 ? M : 1)};
+        const uint64_t dA[2] = {(uint64_t)K, (uint64_t)rows_a};
         const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
-        if ((st = tmap_u8(a_ptr, 2, dA, bA, di.dev, tmA)) != FP8G_OK) return st;
+        if ((st = tmap_u8(a_ptr, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
     }
     if (mode == kModeGrouped) {
         const uint64_t dB[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
         const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.BN, 1u};
-        if ((st = tmap_u8(B, 3, dB, bB, di.dev, tmB)) != FP8G_OK) return st;
+        if ((st = tmap_u8(B, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     } else {
         const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
         const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.BN};
-        if ((st = tmap_u8(B, 2, dB, bB, di.dev, tmB)) != FP8G_OK) return st;
+        if ((st = tmap_u8(B, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     }
-    const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, tmA, tmB, p, kc, stream);
-    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+    if (mode == kModeTensor) {
+        const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+    }
+    // Block modes: pack the fp32 scales into UE8M0 chunks (a stream-ordered
+    // temporary from the library pool), run the GEMM, return the temporary.
+    const int32_t zB = mode == kModeGrouped ? E : 1;
+    p.n_rtA = (int32_t)(mode == kModeGrouped ? M / kBM + E : (M + kBM - 1) / kBM);
+    p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
+    if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
+    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB);
+    cudaMemPool_t pool;
+    if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    uint8_t *pkA = static_cast<uint8_t *>(ws);
+    uint8_t *pkB = pkA + bytesA;
+    cudaError_t e = cudaSuccess;
+    if (M > 0)
+        e = launch_pack_scales(sa, M, p.sfc, p.num_kb, p.n_rtA, 1, 0, pkA,
+                               mode == kModeGrouped ? counts : nullptr, E, di.status, stream);
+    if (e == cudaSuccess)
+        e = launch_pack_scales(sb, N, p.sfc, p.num_kb, p.n_rtB, zB, N, pkB, nullptr, 0, di.status,
+                               stream);
+    p.sfa_pk = pkA;
+    p.sfb_pk = pkB;
+    if (e == cudaSuccess) e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
 }  // namespace
@@ -364,6 +425,8 @@ void fp8g_shutdown(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < kCacheSize; ++i) g_cache[i].used = false;
     g_cache_next = 0;
+    for (int d = 0; d < kMaxDevices; ++d)
+        if (g_pool_ok[d]) cudaMemPoolTrimTo(g_pool[d], 0);
 }
 
 int fp8g_version(void) { return 100; }

@@ -15,9 +15,9 @@
 //   - warp 1: a single thread issues tcgen05.mma (kind::f8f6f4, or
 //     kind::mxf8f6f4.block_scale with UE8M0 scale factors read from tensor
 //     memory) into an fp32 accumulator in tensor memory (12.6.1-12.6.2);
-//   - warp 2 (block modes): stages the fp32 1x32 scales with cp.async,
-//     converts them to UE8M0 bytes in the layout tcgen05.cp expects, and marks
-//     the stage ready; the MMA thread copies them shared -> tensor memory;
+//   - block modes: the producer also bulk-copies each stage's scale factors,
+//     pre-packed as UE8M0 bytes in the layout tcgen05.cp reads (scales.cu),
+//     into the stage; the MMA thread copies them shared -> tensor memory;
 //   - warps 4..19: epilogue; each warp drains its 32-lane quarter of the
 //     accumulator (tcgen05.ld), releases it, scales / rounds and stores.
 //
@@ -42,29 +42,25 @@ namespace {
 constexpr int kThreads = 640;  // 20 warps
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
-constexpr int kStgSlots = 4;   // fp32 scale staging ring depth (block modes)
 
 template <int MODE, int BN, int NUM_ACC, int STAGES>
 struct Cfg {
     static constexpr bool kBlock = MODE != kModeTensor;
     static constexpr int A_BYTES = kBM * kBK;
     static constexpr int B_BYTES = BN * kBK;
-    static constexpr int SFA_BYTES = kBlock ? kBM * 4 : 0;
-    static constexpr int SFB_BYTES = kBlock ? BN * 4 : 0;
-    static constexpr int SF_ROWS = kBM + BN;
-    static constexpr int STG_BYTES = kBlock ? SF_ROWS * 16 : 0;
+    static constexpr int CHUNK_BYTES = kBlock ? (kBM + BN) * 4 : 0;  // UE8M0, 4 K-blocks per row
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_STG = OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES);
-    static constexpr int OFF_BAR = OFF_STG + kStgSlots * STG_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK_BYTES;
+    // full[S], empty[S], acc_full[NA], acc_empty[NA], drain
     static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;
-    static constexpr int GROUP_BYTES = 2 * (FP8G_MAX_EXPERTS + 1) * 4;
+    static constexpr int GROUP_BYTES = 3 * (FP8G_MAX_EXPERTS + 1) * 4;
     static constexpr int SMEM_USED = OFF_GROUP + GROUP_BYTES;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + CHUNK_BYTES;
     static constexpr int ACC_COLS = NUM_ACC * BN;
     static constexpr int SF_COLS = kBlock ? (kBM / 32 + BN / 32) : 0;
     static constexpr int SF_COL0 = ACC_COLS;
@@ -75,28 +71,30 @@ struct Cfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
     static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
     static_assert(CW % 32 == 0, "epilogue chunk must be a multiple of 32 columns");
+    static_assert(OFF_SF % 16 == 0 && CHUNK_BYTES % 16 == 0, "bulk-copy alignment");
 };
 
 struct Tile {
     int32_t row0, row_end, n0, e, pm, pn;
+    int32_t rtA;  // 128-row tile of A in the packed scale layout
 };
 
 // Grouped raster order: bands of G tile-rows; inside a band walk down one
-// tile-column, then move to the next column.
-__device__ __forceinline__ void raster(int64_t t, int32_t npm, int32_t npn, int32_t G, int32_t &pm,
+// tile-column, then move to the next column.  (Tile counts fit in 31 bits.)
+__device__ __forceinline__ void raster(int32_t t, int32_t npm, int32_t npn, int32_t G, int32_t &pm,
                                        int32_t &pn) {
-    const int64_t band = (int64_t)G * npn;
-    const int64_t grp = t / band;
-    const int32_t first = (int32_t)(grp * G);
+    const int32_t band = G * npn;
+    const int32_t grp = t / band;
+    const int32_t first = grp * G;
     const int32_t height = min(npm - first, G);
-    const int32_t in_band = (int32_t)(t - grp * band);
+    const int32_t in_band = t - grp * band;
     pm = first + in_band % height;
     pn = in_band / height;
 }
 
 template <int MODE, int BN>
-__device__ __forceinline__ Tile get_tile(int64_t t, const GemmParams &p, const int32_t *row_off,
-                                         const int32_t *tile_off) {
+__device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const int32_t *row_off,
+                                         const int32_t *tile_off, const int32_t *rt_off) {
     Tile ti;
     if constexpr (MODE == kModeGrouped) {
         int e = 0;
@@ -107,11 +105,13 @@ __device__ __forceinline__ Tile get_tile(int64_t t, const GemmParams &p, const i
         ti.row0 = row_off[e] + ti.pm * kBM;
         ti.row_end = row_off[e + 1];
         ti.e = e;
+        ti.rtA = rt_off[e] + ti.pm;
     } else {
         raster(t, p.npm, p.npn, kRasterG, ti.pm, ti.pn);
         ti.row0 = ti.pm * kBM;
         ti.row_end = (int32_t)p.M;
         ti.e = 0;
+        ti.rtA = ti.pm;
     }
     ti.n0 = ti.pn * BN;
     return ti;
@@ -123,8 +123,10 @@ __device__ __forceinline__ void record_error(const GemmParams &p, unsigned code,
 
 // Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting
 // (another role timed out) or when this wait itself exceeded the limit.
+// sleep_ns > 0 backs off between polls (for roles that wait a whole tile).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         const GemmParams &p, unsigned detail) {
+                                         const GemmParams &p, unsigned detail,
+                                         uint32_t sleep_ns = 0) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
@@ -135,6 +137,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             record_error(p, FP8G_ERR_TIMEOUT, detail);
             return false;
         }
+        if (sleep_ns) __nanosleep(sleep_ns);
     }
 }
 
@@ -142,21 +145,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // warp re-converges before any .sync.aligned tcgen05 instruction follows.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
                                               volatile int *abort_flag, const GemmParams &p,
-                                              unsigned detail) {
+                                              unsigned detail, uint32_t sleep_ns = 0) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, p, detail) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, p, detail, sleep_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;
-}
-
-// fp32 scale (must be a positive power of two, or NaN) -> UE8M0 code.
-__device__ __forceinline__ uint32_t ue8m0_code(uint32_t bits, bool &bad) {
-    const uint32_t ex = (bits >> 23) & 0xFFu;
-    const uint32_t man = bits & 0x7FFFFFu;
-    if (ex == 0xFFu && man != 0u) return 0xFFu;  // NaN scale -> NaN code
-    if ((bits >> 31) != 0u || man != 0u || ex == 0u || ex == 0xFFu) bad = true;
-    return ex;
 }
 
 template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
@@ -182,11 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C_::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + C_::OFF_GROUP);
     int32_t *tile_off = row_off + (FP8G_MAX_EXPERTS + 1);
+    int32_t *rt_off = tile_off + (FP8G_MAX_EXPERTS + 1);
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar_full(s), C_::kBlock ? 2 : 1);
+            ptx::mbar_init(bar_full(s), 1);
             ptx::mbar_init(bar_empty(s), 1);
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -205,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C_::TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    int64_t T = p.T;
+    int32_t T = (int32_t)p.T;
     if constexpr (MODE == kModeGrouped) {
         // counts -> row offsets and tile offsets (experts in index order)
         if (threadIdx.x < FP8G_MAX_EXPERTS)
@@ -230,10 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (blockIdx.x == 0) record_error(p, FP8G_ERR_INVALID_ARG, 1);
             }
             tile_off[0] = 0;
+            rt_off[0] = 0;
             for (int e = 0; e < p.E; ++e) {
                 const int64_t Me = bad ? 0 : (row_off[e + 1] - row_off[e]);
                 tt += ((Me + kBM - 1) / kBM) * (int64_t)p.npn;
                 tile_off[e + 1] = (int32_t)tt;
+                // packed scale row tiles of A: counted as the packing kernel does
+                rt_off[e + 1] = rt_off[e] + (max(cnt[e], 0) + kBM - 1) / kBM;
             }
             if (blockIdx.x == 0 && p.offsets_out != nullptr)
                 for (int e = 0; e <= p.E; ++e) p.offsets_out[e] = row_off[e];
@@ -247,29 +245,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ roles
     if (warp == 0) {
-        // ===== TMA producer =====
+        // ===== TMA producer: A, B (and the packed scale chunks) per stage =====
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-                const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off);
+            for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
+                const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
                 if constexpr (MODE == kModeGrouped) {
                     if (p.tile_map_out != nullptr) {
                         int4 v = make_int4(ti.e, ti.pm, ti.pn, 0);
-                        *reinterpret_cast<int4 *>(p.tile_map_out + 4 * t) = v;
+                        *reinterpret_cast<int4 *>(p.tile_map_out + 4 * (int64_t)t) = v;
                     }
                 }
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
-                    ptx::mbar_arrive_expect_tx(bar_full(stage), C_::TX_BYTES);
-                    ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, bar_full(stage),
-                                     kb * kBK, ti.row0);
+                    const uint32_t fb = bar_full(stage);
+                    ptx::mbar_arrive_expect_tx(fb, C_::TX_BYTES);
+                    ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb, kb * kBK,
+                                     ti.row0);
                     if constexpr (MODE == kModeGrouped)
-                        ptx::tma_load_3d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB,
-                                         bar_full(stage), kb * kBK, ti.n0, ti.e);
+                        ptx::tma_load_3d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
+                                         kb * kBK, ti.n0, ti.e);
                     else
-                        ptx::tma_load_2d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB,
-                                         bar_full(stage), kb * kBK, ti.n0);
+                        ptx::tma_load_2d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
+                                         kb * kBK, ti.n0);
+                    if constexpr (C_::kBlock) {
+                        const uint32_t dst = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
+                        const uint8_t *sa_src =
+                            p.sfa_pk + ((int64_t)kb * p.n_rtA + ti.rtA) * 512;
+                        const uint8_t *sb_src =
+                            p.sfb_pk +
+                            (((int64_t)ti.e * p.num_kb + kb) * p.n_rtB + ti.n0 / kBM) * 512;
+                        ptx::bulk_load(dst, sa_src, kBM * 4, fb);
+                        ptx::bulk_load(dst + kBM * 4, sb_src, BN * 4, fb);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -281,9 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ===== MMA issuer =====
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            int64_t lt = 0;
-            for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
-                const int acc = (int)(lt % NUM_ACC);
+            int32_t lt = 0;
+            for (int32_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+                const int acc = lt % NUM_ACC;
                 const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
                 if (!wait_bar(bar_acce(acc), acc_par ^ 1u, abort_flag, p, 1 * 256 + 64 + acc))
                     goto roles_done;
@@ -297,14 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = sbase + C_::OFF_B + stage * C_::B_BYTES;
                     if constexpr (C_::kBlock) {
                         const uint32_t sf_tmem = tmem_base + C_::SF_COL0 + stage * C_::SF_COLS;
-                        const uint32_t sfa_s =
-                            sbase + C_::OFF_SF + stage * (C_::SFA_BYTES + C_::SFB_BYTES);
-                        const uint32_t sfb_s = sfa_s + C_::SFA_BYTES;
-                        ptx::tc_cp_32x128b_warpx4(sf_tmem, ptx::desc_sf_chunk(sfa_s));
+                        const uint32_t sfa_s = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
+                        // one 32-row x 16-byte chunk per 128 tile rows: A, then B
 #pragma unroll
-                        for (int c = 0; c < BN / 128; ++c)
-                            ptx::tc_cp_32x128b_warpx4(sf_tmem + kBM / 32 + 4 * c,
-                                                      ptx::desc_sf_chunk(sfb_s + c * 512));
+                        for (int c = 0; c < 1 + BN / 128; ++c)
+                            ptx::tc_cp_32x128b_warpx4(sf_tmem + 4 * c,
+                                                      ptx::desc_sf_chunk(sfa_s + c * 512));
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
@@ -327,127 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_commit(bar_accf(acc));
             }
         }
-    } else if (warp == 2) {
-        // ===== scale-factor stager (block modes) =====
-        if constexpr (C_::kBlock) {
-            // Work cursor over (tile, kb) in the same order as the producer.
-            struct Cursor {
-                int64_t t;
-                int kb;
-            };
-            Cursor iss{(int64_t)blockIdx.x, 0}, cvt{(int64_t)blockIdx.x, 0};
-            auto advance = [&](Cursor &c) {
-                if (++c.kb == p.num_kb) {
-                    c.kb = 0;
-                    c.t += gridDim.x;
-                }
-            };
-            const bool vec16 = (p.sfc % 4) == 0;
-            const int64_t a_rows = p.M;
-            auto issue = [&](const Cursor &c, int slot) {
-                const Tile ti = get_tile<MODE, BN>(c.t, p, row_off, tile_off);
-                const uint32_t dst0 = sbase + C_::OFF_STG + slot * C_::STG_BYTES;
-                const float *sfb_base = p.sb + (int64_t)ti.e * p.N * p.sfc;
-#pragma unroll
-                for (int i = 0; i < C_::SF_ROWS / 32; ++i) {
-                    const int r = lane + 32 * i;
-                    const float *src;
-                    bool valid;
-                    if (r < kBM) {
-                        const int64_t row = (int64_t)ti.row0 + r;
-                        valid = row < a_rows;
-                        src = p.sa + (valid ? row : 0) * p.sfc + (int64_t)c.kb * 4;
-                    } else {
-                        const int64_t row = (int64_t)ti.n0 + (r - kBM);
-                        valid = row < p.N;
-                        src = sfb_base + (valid ? row : 0) * p.sfc + (int64_t)c.kb * 4;
-                    }
-                    const uint32_t dst = dst0 + r * 16;
-                    if (vec16) {
-                        ptx::cp_async_16(dst, valid ? src : p.sa, valid ? 16u : 0u);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const bool ok = valid && ((int64_t)c.kb * 4 + j) < p.sfc;
-                            ptx::cp_async_4(dst + 4 * j, ok ? src + j : p.sa, ok ? 4u : 0u);
-                        }
-                    }
-                }
-            };
-            const int64_t total_iters =
-                (T > blockIdx.x) ? ((T - blockIdx.x + gridDim.x - 1) / gridDim.x) * p.num_kb : 0;
-            int64_t issued = 0;
-#pragma unroll 1
-            for (int i = 0; i < kStgSlots - 1; ++i) {
-                if (issued < total_iters) {
-                    issue(iss, i);
-                    advance(iss);
-                    ++issued;
-                }
-                ptx::cp_async_commit();
-            }
-            uint32_t stage = 0, phase = 0;
-            int slot = 0;
-            bool bad = false;
-            for (int64_t it = 0; it < total_iters; ++it) {
-                if (issued < total_iters) {
-                    issue(iss, (slot + kStgSlots - 1) % kStgSlots);
-                    advance(iss);
-                    ++issued;
-                }
-                ptx::cp_async_commit();
-                ptx::cp_async_wait<kStgSlots - 1>();
-                __syncwarp();
-                if (!wait_bar_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, 2 * 256 + stage))
-                    break;
-                const Tile ti = get_tile<MODE, BN>(cvt.t, p, row_off, tile_off);
-                const uint8_t *stg = smem + C_::OFF_STG + slot * C_::STG_BYTES;
-                uint8_t *chunk = smem + C_::OFF_SF + stage * (C_::SFA_BYTES + C_::SFB_BYTES);
-                const int kvalid = (int)(p.sfc - (int64_t)cvt.kb * 4 < 4 ? p.sfc - (int64_t)cvt.kb * 4 : 4);
-                // chunk layout: 32 rows ("datapaths") x 16 bytes; datapath d,
-                // word w holds the 4 K-block codes of tile row 32*w + d.
-#pragma unroll
-                for (int c = 0; c < 1 + BN / 128; ++c) {
-                    uint32_t words[4];
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int r = c * 128 + 32 * w + lane;  // staged row
-                        const uint4 f = *reinterpret_cast<const uint4 *>(stg + r * 16);
-                        int64_t grow;
-                        bool rvalid;
-                        if (c == 0) {
-                            grow = (int64_t)ti.row0 + r;
-                            rvalid = grow < a_rows;
-                        } else {
-                            grow = (int64_t)ti.n0 + (r - kBM);
-                            rvalid = grow < p.N;
-                        }
-                        const uint32_t fb[4] = {f.x, f.y, f.z, f.w};
-                        uint32_t word = 0;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t code = 127u;  // 1.0 for padding (data there is zero)
-                            if (rvalid && j < kvalid) code = ue8m0_code(fb[j], bad);
-                            word |= code << (8 * j);
-                        }
-                        words[w] = word;
-                    }
-                    *reinterpret_cast<uint4 *>(chunk + c * 512 + lane * 16) =
-                        make_uint4(words[0], words[1], words[2], words[3]);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_full(stage));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                slot = (slot + 1) % kStgSlots;
-                advance(cvt);
-            }
-            ptx::cp_async_wait<0>();
-            if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
-        }
     } else if (warp >= kEpiWarp0) {
         // ===== epilogue =====
         const int ew = warp - kEpiWarp0;
@@ -455,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = (ew >> 2) * C_::CW;
         float alpha = 1.0f;
         if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
-        int64_t lt = 0;
-        for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
-            const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off);
-            const int acc = (int)(lt % NUM_ACC);
+        int32_t lt = 0;
+        for (int32_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+            const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
+            const int acc = lt % NUM_ACC;
             const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
-            if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc)) break;
+            if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc, 128)) break;
             ptx::tc_fence_after();
             uint32_t r[C_::CW / 32][32];
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + col0;
@@ -539,8 +425,7 @@ roles_done:
 }
 
 template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
-cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
-                       int grid, cudaStream_t stream) {
+cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
     auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32>;
     // The shared-memory opt-in is per device; the flag races benignly (the
@@ -555,7 +440,7 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const Gem
         if (e != cudaSuccess) return e;
         attr_done |= bit;
     }
-    kern<<<grid, kThreads, C_::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    kern<<<grid, kThreads, C_::SMEM_BYTES, stream>>>(maps.A, maps.B, p);
     return cudaGetLastError();
 }
 
@@ -577,17 +462,17 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     return kc;
 }
 
-cudaError_t launch_gemm(int mode, bool out_f32, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmParams &p, const KernelChoice &kc, cudaStream_t stream) {
+cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
+                        const KernelChoice &kc, cudaStream_t stream) {
     if (mode == kModeTensor) {
-        return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true>(tmA, tmB, p, kc.grid, stream)
-                       : launch_one<kModeTensor, 256, 2, 4, false>(tmA, tmB, p, kc.grid, stream);
+        return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true>(maps, p, kc.grid, stream)
+                       : launch_one<kModeTensor, 256, 2, 4, false>(maps, p, kc.grid, stream);
     } else if (mode == kModeBlock) {
-        return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true>(tmA, tmB, p, kc.grid, stream)
-                       : launch_one<kModeBlock, 256, 1, 4, false>(tmA, tmB, p, kc.grid, stream);
+        return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true>(maps, p, kc.grid, stream)
+                       : launch_one<kModeBlock, 256, 1, 4, false>(maps, p, kc.grid, stream);
     } else {
-        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true>(tmA, tmB, p, kc.grid, stream)
-                       : launch_one<kModeGrouped, 256, 1, 4, false>(tmA, tmB, p, kc.grid, stream);
+        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true>(maps, p, kc.grid, stream)
+                       : launch_one<kModeGrouped, 256, 1, 4, false>(maps, p, kc.grid, stream);
     }
 }
 

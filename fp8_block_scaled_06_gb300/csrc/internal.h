@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/fp8gemm.h"
+#include "fp8gemm.h"
 
 namespace fp8g {
 
@@ -38,6 +38,14 @@ struct GemmParams {
     int32_t *tile_map_out;
     unsigned int *status;  // [0] = first error code, [1] = detail
     uint64_t timeout_ns;
+    const uint8_t *sfa_pk; // block modes: packed UE8M0 scale chunks of A and B
+    const uint8_t *sfb_pk;
+    int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
+};
+
+// TMA descriptors of one launch (E4M3 operands).
+struct GemmMaps {
+    CUtensorMap A, B;
 };
 
 struct KernelChoice {
@@ -48,9 +56,16 @@ struct KernelChoice {
 };
 
 // gemm.cu
-cudaError_t launch_gemm(int mode, bool out_f32, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmParams &p, const KernelChoice &kc, cudaStream_t stream);
+cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
+                        const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
+
+// scales.cu: fp32 1x32 scales -> packed UE8M0 chunks
+size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
+cudaError_t launch_pack_scales(const float *src, int64_t rows_total, int64_t sfc, int32_t n_kg,
+                               int32_t n_rt, int32_t z, int64_t z_rows, uint8_t *dst,
+                               const int32_t *counts, int32_t E, unsigned int *status,
+                               cudaStream_t s);
 
 // quant.cu
 cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float *scale,

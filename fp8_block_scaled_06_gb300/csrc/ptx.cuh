@@ -97,6 +97,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// 1-D bulk copy global -> shared completing on an mbarrier (src, dst 16-byte
+// aligned; bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte (or 4-byte) asynchronous global->shared copy; bytes past src_bytes
 // are zero-filled (src_bytes = 0 copies nothing and writes zeros).

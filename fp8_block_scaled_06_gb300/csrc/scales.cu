@@ -1,0 +1,132 @@
+// Scale-factor packing: fp32 1x32 block scales -> UE8M0 bytes in the layout
+// the tensor core's scale-factor copy reads (tcgen05.cp 32x128b.warpx4).
+//
+// The block-scaled MMA (kind::mxf8f6f4, "MXFP8 micro-scaling" of the Triton
+// tutorial ch. 12, 12.6.1) applies one 8-bit power-of-two exponent per row
+// and 32-wide K block.  A positive power of two's UE8M0 code is exactly its
+// fp32 exponent field, so packing is lossless for the scales the API accepts.
+//
+// Packed layout, per operand: chunks of 512 bytes, one per (K group of 4
+// blocks = one 128-wide K stage of the GEMM, tile of 128 rows):
+//   chunk(z, kg, rt) at byte ((z * n_kg + kg) * n_rt + rt) * 512
+//   byte 16 d + 4 w + j = code(row 128 rt + 32 w + d, K block 4 kg + j)
+// so one GEMM stage reads its A chunk (512 B) and its B chunks (BN/128 x 512
+// B, adjacent) with 1-D bulk copies.  Rows past the operand and K blocks past
+// K/32 get code 127 (scale 1.0; the operand data there is zero).
+//
+// Grouped A: row tiles are expert-local (an expert's rows start a new tile),
+// numbered in expert order, like the GEMM's tile list.
+//
+// HBM-bound: each thread reads one row's 16-byte scale groups, 128 threads
+// per 128-row tile, 8 K groups per block.
+#include "internal.h"
+
+namespace fp8g {
+
+namespace {
+
+constexpr int kKgPerBlock = 8;
+
+__device__ __forceinline__ uint32_t code_of(uint32_t bits, bool &bad) {
+    const uint32_t ex = (bits >> 23) & 0xFFu;
+    const uint32_t man = bits & 0x7FFFFFu;
+    if (ex == 0xFFu && man != 0u) return 0xFFu;  // NaN scale -> NaN code
+    if ((bits >> 31) != 0u || man != 0u || ex == 0u || ex == 0xFFu) bad = true;
+    return ex;
+}
+
+__global__ void __launch_bounds__(128) pack_scales_kernel(
+    const float *__restrict__ src, int64_t rows_total, int64_t sfc, int32_t n_kg, int32_t n_rt,
+    int64_t z_rows, uint8_t *__restrict__ dst, const int32_t *__restrict__ counts, int32_t E,
+    unsigned int *status) {
+    __shared__ int32_t row_off[FP8G_MAX_EXPERTS + 1];
+    __shared__ int32_t rt_off[FP8G_MAX_EXPERTS + 1];
+    const int rt = blockIdx.y;
+    const int z = blockIdx.z;
+    const int r = threadIdx.x;
+    int64_t base, limit;
+    if (counts != nullptr) {
+        if (threadIdx.x == 0) {
+            int64_t ro = 0, to = 0;
+            row_off[0] = 0;
+            rt_off[0] = 0;
+            for (int e = 0; e < E; ++e) {
+                const int32_t c = max(counts[e], 0);
+                ro += c;
+                to += (c + kBM - 1) / kBM;
+                row_off[e + 1] = (int32_t)(ro < (int64_t)INT32_MAX ? ro : (int64_t)INT32_MAX);
+                rt_off[e + 1] = (int32_t)to;
+            }
+        }
+        __syncthreads();
+        if (rt >= rt_off[E]) {
+            base = 0;
+            limit = 0;  // padding tile past the last expert
+        } else {
+            int e = 0;
+            while (rt_off[e + 1] <= rt) ++e;
+            base = (int64_t)row_off[e] + (int64_t)(rt - rt_off[e]) * kBM;
+            limit = row_off[e + 1];
+        }
+    } else {
+        base = (int64_t)rt * kBM;
+        limit = rows_total;
+    }
+    const int64_t row = base + r;
+    const bool valid = row < limit && row < rows_total;
+    const float *srow = src + ((int64_t)z * z_rows + (valid ? row : 0)) * sfc;
+    const bool vec = (sfc % 4) == 0;
+    bool bad = false;
+    uint8_t *out = dst + (int64_t)z * n_kg * n_rt * 512 + (int64_t)rt * 512 + (r & 31) * 16 +
+                   (r >> 5) * 4;
+#pragma unroll
+    for (int i = 0; i < kKgPerBlock; ++i) {
+        const int kg = blockIdx.x * kKgPerBlock + i;
+        if (kg >= n_kg) break;
+        uint32_t word = 0x7F7F7F7Fu;
+        if (valid) {
+            uint32_t v[4];
+            const int64_t k0 = (int64_t)kg * 4;
+            if (vec) {
+                const uint4 f = __ldg(reinterpret_cast<const uint4 *>(srow + k0));
+                v[0] = f.x;
+                v[1] = f.y;
+                v[2] = f.z;
+                v[3] = f.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    v[j] = (k0 + j < sfc) ? __float_as_uint(__ldg(srow + k0 + j)) : 0x3F800000u;
+            }
+            word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t c = (k0 + j < sfc) ? code_of(v[j], bad) : 127u;
+                word |= c << (8 * j);
+            }
+        }
+        *reinterpret_cast<uint32_t *>(out + (int64_t)kg * n_rt * 512) = word;
+    }
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
+        if (atomicCAS(&status[0], 0u, (unsigned)FP8G_ERR_SCALE_FORMAT) == 0u)
+            atomicExch(&status[1], 0u);
+}
+
+}  // namespace
+
+size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
+    return (size_t)z * (size_t)n_kg * (size_t)n_rt * 512u;
+}
+
+cudaError_t launch_pack_scales(const float *src, int64_t rows_total, int64_t sfc, int32_t n_kg,
+                               int32_t n_rt, int32_t z, int64_t z_rows, uint8_t *dst,
+                               const int32_t *counts, int32_t E, unsigned int *status,
+                               cudaStream_t s) {
+    if (n_kg <= 0 || n_rt <= 0 || z <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((n_kg + kKgPerBlock - 1) / kKgPerBlock), (unsigned)n_rt, (unsigned)z);
+    pack_scales_kernel<<<grid, 128, 0, s>>>(src, rows_total, sfc, n_kg, n_rt, z_rows, dst, counts,
+                                            E, status);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8g

@@ -39,8 +39,14 @@
  *     of the tile; out-of-range rows/columns are neither read past the end nor
  *     written.
  *   - Thread safety: calls from several host threads, on any streams, are safe.
- *   - No call allocates device memory.  The library holds one status word per
- *     device (a static device variable) and a host-side tensor-map cache.
+ *   - Device memory: fp8_gemm and fp8g_quantize_e4m3 allocate nothing.  The
+ *     block-scaled entry points repack the fp32 scales into the tensor core's
+ *     UE8M0 layout in a temporary of about (rows of A + rows of B) * K/32
+ *     bytes, taken from a library-owned memory pool with
+ *     cudaMallocFromPoolAsync on `stream` and returned with cudaFreeAsync on
+ *     `stream` (stream-ordered, so calls on different streams never share
+ *     it).  The library also holds one status word per device (a static
+ *     device variable) and a host-side tensor-map cache.
  */
 #ifndef FP8GEMM_H
 #define FP8GEMM_H
@@ -93,8 +99,8 @@ FP8G_API fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a
  * core applies it exactly as an 8-bit exponent.  Any other value records
  * FP8G_ERR_SCALE_FORMAT in the status word (the output is then unspecified).
  * K % 32 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE).  Other rules as fp8_gemm.
- * Skinny problems (few output tiles) split K across a cluster of CTAs that
- * reduce through distributed shared memory; this needs no workspace.
+ * Runs two kernels on `stream`: the scale packing (scales -> UE8M0 chunks,
+ * which also performs the scale check) and the GEMM.
  */
 FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
                                  const float *sfb, void *C, int out, int64_t M, int64_t N,
@@ -174,7 +180,9 @@ FP8G_API const char *fp8g_status_string(fp8g_status status);
  */
 FP8G_API void fp8g_set_wait_timeout_ms(uint32_t ms);
 
-/* Drops the host tensor-map cache.  Safe to call at any time. */
+/* Drops the host tensor-map cache and releases the memory the scale-packing
+ * pool holds (pending stream-ordered frees are honoured).  Safe to call at
+ * any time. */
 FP8G_API void fp8g_shutdown(void);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
