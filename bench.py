@@ -351,7 +351,7 @@ def main():
         "achieved_hbm_gbs": round(hbm_gbs, 1),
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOPS",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (1 if wl["kind"] == "tensor" else 3),
         "clocks": clocks,
         "wall_s": round(wall, 3),
     }
