@@ -33,7 +33,7 @@ FP8G_MAX_EXPERTS = 64
 
 # Every symbol include/fp8gemm.h declares.
 EXPORTS = (
-    "fp8_gemm", "fp8_gemm_blockscaled", "fp8_grouped_gemm", "fp8g_grouped_plan",
+    "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
@@ -72,6 +72,8 @@ def load():
         lib.fp8_gemm.argtypes = [P, P, P, P, P, ctypes.c_int, i64, i64, i64, P]
         lib.fp8_gemm_blockscaled.restype = st
         lib.fp8_gemm_blockscaled.argtypes = [P, P, P, P, P, ctypes.c_int, i64, i64, i64, P]
+        lib.fp8_gemm_blockscaled_noalloc.restype = st
+        lib.fp8_gemm_blockscaled_noalloc.argtypes = [P, P, P, P, P, ctypes.c_int, i64, i64, i64, P]
         lib.fp8_grouped_gemm.restype = st
         lib.fp8_grouped_gemm.argtypes = [P, P, P, P, P, ctypes.c_int, P, i32, i64, i64, i64, P,
                                          P, P]
@@ -129,6 +131,14 @@ def fp8_gemm(A, B, scale_a, scale_b, C, out: int, M: int, N: int, K: int, stream
 def fp8_gemm_blockscaled(A, B, sfa, sfb, C, out: int, M: int, N: int, K: int, stream=None):
     _check(load().fp8_gemm_blockscaled(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C), int(out),
                                        M, N, K, _stream(stream)), "fp8_gemm_blockscaled")
+
+
+def fp8_gemm_blockscaled_noalloc(A, B, sfa, sfb, C, out: int, M: int, N: int, K: int,
+                                 stream=None):
+    """Allocation-free fp8_gemm_blockscaled (packed scales in the library's fixed array)."""
+    _check(load().fp8_gemm_blockscaled_noalloc(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C),
+                                               int(out), M, N, K, _stream(stream)),
+           "fp8_gemm_blockscaled_noalloc")
 
 
 def fp8_grouped_gemm(A, B, sfa, sfb, C, out: int, counts, E: int, N: int, K: int,

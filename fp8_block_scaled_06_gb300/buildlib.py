@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 OBJ_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8g.so")
-SOURCES = ["gemm.cu", "scales.cu", "quant.cu", "api.cu"]
+SOURCES = ["gemm.cu", "scales.cu", "quant.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

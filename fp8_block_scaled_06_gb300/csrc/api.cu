@@ -201,9 +201,12 @@ fp8g_status check_common(const void *A, const void *B, const void *C, int out, i
     return FP8G_OK;
 }
 
+}  // namespace
+
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
-                     int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream) {
+                     int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
+                     void *scratch, size_t scratch_bytes) {
     DevInfo di;
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
@@ -258,11 +261,17 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
     const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
     const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB);
-    cudaMemPool_t pool;
-    if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
     void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
-        return FP8G_ERR_CUDA;
+    if (scratch != nullptr) {
+        // caller-provided scratch (the allocation-free entry point)
+        if (bytesA + bytesB > scratch_bytes) return FP8G_ERR_UNSUPPORTED_SHAPE;
+        ws = scratch;
+    } else {
+        cudaMemPool_t pool;
+        if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
+        if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+    }
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
     cudaError_t e = cudaSuccess;
@@ -275,11 +284,10 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
     if (e == cudaSuccess) e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    const cudaError_t ef = scratch != nullptr ? cudaSuccess : cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
-}  // namespace
 }  // namespace fp8g
 
 using namespace fp8g;
@@ -293,7 +301,7 @@ fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const f
     if (scale_a == nullptr || scale_b == nullptr) return FP8G_ERR_INVALID_ARG;
     if (!aligned(scale_a, 4) || !aligned(scale_b, 4)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeTensor, A, B, scale_a, scale_b, C, out, M, N, K, nullptr, 0, nullptr,
-                    nullptr, stream);
+                    nullptr, stream, nullptr, 0);
 }
 
 fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
@@ -305,7 +313,7 @@ fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
     if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
-                    stream);
+                    stream, nullptr, 0);
 }
 
 fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, const float *sfb,
@@ -331,7 +339,7 @@ fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, con
     if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
     if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
-                    offsets_out, tile_map_out, stream);
+                    offsets_out, tile_map_out, stream, nullptr, 0);
 }
 
 fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,

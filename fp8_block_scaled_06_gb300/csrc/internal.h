@@ -60,6 +60,14 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                         const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
 
+// api.cu: checks done by the caller; scratch == nullptr takes the packed
+// scale temporary from the library pool, otherwise uses [scratch,
+// scratch + scratch_bytes) (FP8G_ERR_UNSUPPORTED_SHAPE if it is too small).
+fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
+                     void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
+                     int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
+                     void *scratch, size_t scratch_bytes);
+
 // scales.cu: fp32 1x32 scales -> packed UE8M0 chunks
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const float *src, int64_t rows_total, int64_t sfc, int32_t n_kg,

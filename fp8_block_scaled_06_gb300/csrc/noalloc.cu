@@ -1,0 +1,78 @@
+// Allocation-free variant of the block-scaled GEMM.
+//
+// fp8_gemm_blockscaled repacks the caller's fp32 scales into the tensor
+// core's UE8M0 layout in a temporary taken from a device memory pool.  Some
+// callers cannot have the library allocate device memory at all: for example
+// code running under a strict memory budget or a custom allocator that owns
+// every device byte, or an embedding that forbids allocation calls on its hot
+// path.  fp8_gemm_blockscaled_noalloc does the same work but keeps the packed
+// scales in the fixed device array below, which is part of the library image:
+// it exists on every GPU that loads the library, from load until process exit,
+// and no call allocates or frees anything.
+#include <mutex>
+
+#include "internal.h"
+
+namespace fp8g {
+namespace {
+
+// Packed-scale scratch: (ceil(M/128) + 2 ceil(N/256)) * ceil(K/128) * 512
+// bytes must fit (8 MiB covers e.g. M = N = K = 16384).
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDev = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDev] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in in host code; its device address comes
+// from cudaGetSymbolAddress, once per device, with that device current.
+fp8g_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return FP8G_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return FP8G_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FP8G_OK;
+}
+
+bool is_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace fp8g
+
+using namespace fp8g;
+
+extern "C" {
+
+fp8g_status fp8_gemm_blockscaled_noalloc(const void *A, const void *B, const float *sfa,
+                                         const float *sfb, void *C, int out, int64_t M, int64_t N,
+                                         int64_t K, cudaStream_t stream) {
+    if (A == nullptr || B == nullptr || C == nullptr || sfa == nullptr || sfb == nullptr)
+        return FP8G_ERR_INVALID_ARG;
+    if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
+    const int64_t kMax = (int64_t)1 << 31;
+    if (M >= kMax || N >= kMax || K >= kMax) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!is_aligned(A, 16) || !is_aligned(B, 16) || !is_aligned(C, 16) || !is_aligned(sfa, 16) ||
+        !is_aligned(sfb, 16))
+        return FP8G_ERR_ALIGNMENT;
+    if (K % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    if ((N * (out == FP8G_OUT_F32 ? 4 : 2)) % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    void *scratch = nullptr;
+    const fp8g_status st = noalloc_scratch(&scratch);
+    if (st != FP8G_OK) return st;
+    // run_gemm returns FP8G_ERR_UNSUPPORTED_SHAPE, before launching anything,
+    // when the packed scales would not fit in the array.
+    return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
+                    stream, scratch, kNoAllocScratchBytes);
+}
+
+}  // extern "C"

@@ -107,6 +107,29 @@ FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const fl
                                  int64_t K, cudaStream_t stream);
 
 /*
+ * Allocation-free form of fp8_gemm_blockscaled (the source pages have no
+ * counterpart; this is a library convenience).  For callers that cannot let
+ * the library allocate device memory, e.g. code under a fixed device-memory
+ * budget, behind an allocator that owns every device byte, or on a path where
+ * allocation calls are not allowed.  Same arguments, results and errors as
+ * fp8_gemm_blockscaled, but the repacked scale factors live in a fixed 8 MiB
+ * device array that is part of the library (every GPU that loads the library
+ * holds it until the process exits); no call allocates or frees memory.
+ * Limit: (ceil(M/128) + 2*ceil(N/256)) * ceil(K/128) * 512 bytes must fit in
+ * 8 MiB (e.g. M = N = K = 16384); larger shapes return
+ * FP8G_ERR_UNSUPPORTED_SHAPE without launching.
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  All calls share the one array: calls whose kernels can
+ * overlap on the GPU (different streams without ordering between them) race
+ * and must not be issued.  Nothing in the array needs to start at zero: each
+ * call rewrites the part it reads.
+ */
+FP8G_API fp8g_status fp8_gemm_blockscaled_noalloc(const void *A, const void *B, const float *sfa,
+                                                  const float *sfb, void *C, int out, int64_t M,
+                                                  int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * Grouped (MoE) block-scaled GEMM [JAX-BW MoE paragraph].
  * Expert e owns rows [off_e, off_e + counts[e]) of A and C, off = exclusive
  * prefix sum of counts; those rows multiply B[e]:
