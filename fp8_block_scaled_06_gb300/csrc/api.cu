@@ -274,13 +274,9 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     }
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
-    cudaError_t e = cudaSuccess;
-    if (M > 0)
-        e = launch_pack_scales(sa, M, p.sfc, p.num_kb, p.n_rtA, 1, 0, pkA,
-                               mode == kModeGrouped ? counts : nullptr, E, di.status, stream);
-    if (e == cudaSuccess)
-        e = launch_pack_scales(sb, N, p.sfc, p.num_kb, p.n_rtB, zB, N, pkB, nullptr, 0, di.status,
-                               stream);
+    PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr};
+    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr};
+    cudaError_t e = launch_pack_scales(pa, pb, p.sfc, p.num_kb, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
     if (e == cudaSuccess) e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);

@@ -40,6 +40,7 @@ namespace fp8g {
 namespace {
 
 constexpr int kThreads = 640;  // 20 warps
+constexpr int kMaxSplit = 4;   // K-split cluster size (clusters of <= 4 CTAs co-schedule)
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
 
@@ -153,7 +154,10 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
     return ok != 0;
 }
 
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
+// SPLIT: the CTAs of one cluster share an output tile, each taking a
+// contiguous range of K blocks; their fp32 partials meet in distributed shared
+// memory (see the end of the kernel).
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
@@ -200,6 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C_::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // Everything above touched only shared / tensor memory and kernel
+    // parameters; global memory (which the previous kernel on the stream may
+    // still be writing, or reading) is accessed only after this wait.  The
+    // next kernel may begin its own prologue.
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
     int32_t T = (int32_t)p.T;
     if constexpr (MODE == kModeGrouped) {
         // counts -> row offsets and tile offsets (experts in index order)
@@ -243,12 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MODE == kModeGrouped) T = tile_off[p.E];
     const uint32_t tmem_base = *tmem_slot;
 
+    // work of this CTA: tiles t_first, t_first + t_step, ...; K blocks [kb_begin, kb_end)
+    int32_t t_first = blockIdx.x, t_step = gridDim.x;
+    int kb_begin = 0, kb_end = p.num_kb;
+    if constexpr (SPLIT) {
+        const int rank = (int)ptx::cluster_rank();
+        t_first = (int32_t)ptx::cluster_id_x();
+        t_step = (int32_t)ptx::num_clusters_x();
+        kb_begin = rank * p.num_kb / p.split;
+        kb_end = (rank + 1) * p.num_kb / p.split;
+    }
+
     // ------------------------------------------------------------ roles
     if (warp == 0) {
         // ===== TMA producer: A, B (and the packed scale chunks) per stage =====
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
+            for (int32_t t = t_first; t < T; t += t_step) {
                 const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
                 if constexpr (MODE == kModeGrouped) {
                     if (p.tile_map_out != nullptr) {
@@ -256,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<int4 *>(p.tile_map_out + 4 * (int64_t)t) = v;
                     }
                 }
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = bar_full(stage);
@@ -291,14 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             int32_t lt = 0;
-            for (int32_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+            for (int32_t t = t_first; t < T; t += t_step, ++lt) {
                 const int acc = lt % NUM_ACC;
                 const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
                 if (!wait_bar(bar_acce(acc), acc_par ^ 1u, abort_flag, p, 1 * 256 + 64 + acc))
                     goto roles_done;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar(bar_full(stage), phase, abort_flag, p, 1 * 256 + stage))
                         goto roles_done;
                     ptx::tc_fence_after();
@@ -317,13 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                           ptx::desc_kmajor_sw128(b0 + k * 32),
                                           ptx::idesc_mxf8(kBM, BN, (uint32_t)k), sf_tmem,
-                                          sf_tmem + kBM / 32, (kb | k) != 0 ? 1u : 0u);
+                                          sf_tmem + kBM / 32, (kb != kb_begin || k != 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_f8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                         ptx::desc_kmajor_sw128(b0 + k * 32), ptx::idesc_f8(kBM, BN),
-                                        (kb | k) != 0 ? 1u : 0u);
+                                        (kb != kb_begin || k != 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar_empty(stage));
                     if (++stage == STAGES) {
@@ -342,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha = 1.0f;
         if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
         int32_t lt = 0;
-        for (int32_t t = blockIdx.x; t < T; t += gridDim.x, ++lt) {
+        for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
             const int acc = lt % NUM_ACC;
             const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
@@ -357,6 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar_acce(acc));
 
+            if constexpr (SPLIT) {
+                // fp32 partial of this K range -> own shared memory (the ring is
+                // idle: every MMA, hence every operand read, has completed)
+                float *part = reinterpret_cast<float *>(smem + C_::OFF_A) +
+                              (q * 32 + lane) * (BN + 4) + col0;
+#pragma unroll
+                for (int c = 0; c < C_::CW / 32; ++c)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<uint4 *>(part + c * 32 + v * 4) =
+                            make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2],
+                                       r[c][4 * v + 3]);
+                continue;
+            }
             const int64_t row = (int64_t)ti.row0 + q * 32 + lane;
             if (row < ti.row_end) {
                 const int64_t ncol0 = (int64_t)ti.n0 + col0;
@@ -418,16 +453,89 @@ roles_done:
         }
         __syncthreads();
     }
+    if constexpr (SPLIT) {
+        // Every CTA of the cluster has its partial in shared memory; CTA `rank`
+        // sums column slice `rank` over the cluster in rank order (a fixed
+        // order, so results do not depend on timing) and stores it.
+        ptx::cluster_sync();
+        if (warp >= kEpiWarp0 && t_first < T && !*abort_flag) {
+            const Tile ti = get_tile<MODE, BN>(t_first, p, row_off, tile_off, rt_off);
+            const int S = p.split;  // 2..kMaxSplit
+            const uint32_t rank = ptx::cluster_rank();
+            const int cols = BN / S;
+            const int c4n = cols / 4;
+            float alpha = 1.0f;
+            if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
+            const int nthr = kEpiWarps * 32;
+            for (int u0 = threadIdx.x - kEpiWarp0 * 32; u0 < kBM * c4n; u0 += 2 * nthr) {
+                // two output units per pass; all remote loads issued before any add
+                float4 v[2][kMaxSplit];
+                uint32_t local[2];
+                bool have[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int u = u0 + h * nthr;
+                    have[h] = u < kBM * c4n;
+                    const int row = have[h] ? u / c4n : 0;
+                    const int col = (int)rank * cols + (have[h] ? (u % c4n) * 4 : 0);
+                    local[h] = sbase + C_::OFF_A + (uint32_t)(row * (BN + 4) + col) * 4u;
+#pragma unroll
+                    for (int r = 0; r < kMaxSplit; ++r)
+                        if (r < S) v[h][r] = ptx::ld_cluster_f4(ptx::map_shared(local[h], (uint32_t)r));
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!have[h]) continue;
+                    const int u = u0 + h * nthr;
+                    float4 acc = v[h][0];
+#pragma unroll
+                    for (int r = 1; r < kMaxSplit; ++r)
+                        if (r < S) {
+                            acc.x += v[h][r].x;
+                            acc.y += v[h][r].y;
+                            acc.z += v[h][r].z;
+                            acc.w += v[h][r].w;
+                        }
+                    const int row = u / c4n;
+                    const int col = (int)rank * cols + (u % c4n) * 4;
+                    const int64_t grow = (int64_t)ti.row0 + row;
+                    const int64_t gcol = (int64_t)ti.n0 + col;
+                    if (grow < ti.row_end && gcol < p.N) {
+                        if constexpr (OUT_F32) {
+                            float4 o = make_float4(__fmul_rn(alpha, acc.x), __fmul_rn(alpha, acc.y),
+                                                   __fmul_rn(alpha, acc.z), __fmul_rn(alpha, acc.w));
+                            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) +
+                                                        grow * p.N + gcol) = o;
+                        } else {
+                            __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(alpha, acc.x),
+                                                                      __fmul_rn(alpha, acc.y));
+                            __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(alpha, acc.z),
+                                                                      __fmul_rn(alpha, acc.w));
+                            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) +
+                                                       grow * p.N + gcol) =
+                                make_uint2(*reinterpret_cast<uint32_t *>(&lo),
+                                           *reinterpret_cast<uint32_t *>(&hi));
+                        }
+                    }
+                }
+            }
+        }
+        // no CTA leaves (and frees its shared memory) while others still read it
+        ptx::cluster_sync();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C_::TMEM_COLS);
     }
 }
 
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32>
-cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
+cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
+                       cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
-    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32>;
+    static_assert(!SPLIT || kBM * (BN + 4) * 4 <= STAGES * (C_::A_BYTES + C_::B_BYTES),
+                  "split-K partial must fit in the operand ring");
+    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT>;
     // The shared-memory opt-in is per device; the flag races benignly (the
     // attribute set is idempotent).
     static unsigned long long attr_done = 0ull;
@@ -440,8 +548,28 @@ cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, int grid, cuda
         if (e != cudaSuccess) return e;
         attr_done |= bit;
     }
-    kern<<<grid, kThreads, C_::SMEM_BYTES, stream>>>(maps.A, maps.B, p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the prologue (barrier init, tensor-memory
+    // allocation, descriptor prefetch) overlaps the previous kernel's tail;
+    // the kernel waits (griddepcontrol.wait) before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)kc.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if constexpr (SPLIT) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)kc.split;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, p);
 }
 
 }  // namespace
@@ -453,26 +581,47 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     kc.cluster = 1;
     if (mode == kModeGrouped) {
         kc.grid = num_sms;
-    } else {
-        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kc.BN - 1) / kc.BN);
-        kc.grid = (int)(tiles < num_sms ? tiles : num_sms);
-        if (kc.grid < 1) kc.grid = 1;
+        return kc;
     }
-    (void)K;
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kc.BN - 1) / kc.BN);
+    // Few output tiles: 128-wide tiles, K split over a cluster of S CTAs per
+    // tile (S a power of two <= kMaxSplit and <= the K blocks, S * tiles <= SMs).
+    if (tiles * 2 <= num_sms && num_kb >= 2) {
+        const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+        int S = 1;
+        while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) S *= 2;
+        if (S >= 2) {
+            kc.BN = 128;
+            kc.split = S;
+            kc.cluster = S;
+            kc.grid = (int)(tiles128 * S);
+            return kc;
+        }
+    }
+    kc.grid = (int)(tiles < num_sms ? tiles : num_sms);
+    if (kc.grid < 1) kc.grid = 1;
     return kc;
 }
 
 cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                         const KernelChoice &kc, cudaStream_t stream) {
+    const bool split = kc.split > 1;
     if (mode == kModeTensor) {
-        return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true>(maps, p, kc.grid, stream)
-                       : launch_one<kModeTensor, 256, 2, 4, false>(maps, p, kc.grid, stream);
+        if (split)
+            return out_f32 ? launch_one<kModeTensor, 128, 1, 6, true, true>(maps, p, kc, stream)
+                           : launch_one<kModeTensor, 128, 1, 6, false, true>(maps, p, kc, stream);
+        return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true, false>(maps, p, kc, stream)
+                       : launch_one<kModeTensor, 256, 2, 4, false, false>(maps, p, kc, stream);
     } else if (mode == kModeBlock) {
-        return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true>(maps, p, kc.grid, stream)
-                       : launch_one<kModeBlock, 256, 1, 4, false>(maps, p, kc.grid, stream);
+        if (split)
+            return out_f32 ? launch_one<kModeBlock, 128, 1, 6, true, true>(maps, p, kc, stream)
+                           : launch_one<kModeBlock, 128, 1, 6, false, true>(maps, p, kc, stream);
+        return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
+                       : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
     } else {
-        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true>(maps, p, kc.grid, stream)
-                       : launch_one<kModeGrouped, 256, 1, 4, false>(maps, p, kc.grid, stream);
+        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 256, 1, 4, false, false>(maps, p, kc, stream);
     }
 }
 

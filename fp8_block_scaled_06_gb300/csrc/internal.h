@@ -68,12 +68,20 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes);
 
-// scales.cu: fp32 1x32 scales -> packed UE8M0 chunks
+// scales.cu: fp32 1x32 scales -> packed UE8M0 chunks.  One launch packs
+// two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid
+// rows per z), dst chunks ((z * n_kg + kg) * n_rt + rt) * 512; counts != null
+// numbers A's row tiles per expert.
+struct PackArgs {
+    const float *src;
+    int64_t rows_total, z_rows;
+    int32_t n_rt, nz;
+    uint8_t *dst;
+    const int32_t *counts;
+};
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
-cudaError_t launch_pack_scales(const float *src, int64_t rows_total, int64_t sfc, int32_t n_kg,
-                               int32_t n_rt, int32_t z, int64_t z_rows, uint8_t *dst,
-                               const int32_t *counts, int32_t E, unsigned int *status,
-                               cudaStream_t s);
+cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
+                               int32_t E, unsigned int *status, cudaStream_t s);
 
 // quant.cu
 cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float *scale,

@@ -17,9 +17,11 @@
 // Grouped A: row tiles are expert-local (an expert's rows start a new tile),
 // numbered in expert order, like the GEMM's tile list.
 //
-// HBM-bound: each thread reads one row's 16-byte scale groups, 128 threads
-// per 128-row tile, 8 K groups per block.
+// HBM-bound: one launch packs both operands; each thread reads one row's
+// 16-byte scale groups (all loads issued before any is used), 128 threads per
+// 128-row tile, 8 K groups per block.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8g {
 
@@ -35,23 +37,35 @@ __device__ __forceinline__ uint32_t code_of(uint32_t bits, bool &bad) {
     return ex;
 }
 
-__global__ void __launch_bounds__(128) pack_scales_kernel(
-    const float *__restrict__ src, int64_t rows_total, int64_t sfc, int32_t n_kg, int32_t n_rt,
-    int64_t z_rows, uint8_t *__restrict__ dst, const int32_t *__restrict__ counts, int32_t E,
-    unsigned int *status) {
+struct PackJob {
+    const float *src;
+    int64_t rows_total, z_rows;
+    int32_t n_rt, nz;
+    uint8_t *dst;
+    const int32_t *counts;  // grouped A: expert-local row tiles
+};
+
+// blockIdx.z < a.nz packs operand a (z = blockIdx.z), the rest operand b.
+__global__ void __launch_bounds__(128) pack_scales_kernel(PackJob a, PackJob b, int64_t sfc,
+                                                          int32_t n_kg, int32_t E,
+                                                          unsigned int *status) {
     __shared__ int32_t row_off[FP8G_MAX_EXPERTS + 1];
     __shared__ int32_t rt_off[FP8G_MAX_EXPERTS + 1];
+    ptx::grid_dep_launch();  // the GEMM may start its prologue now
+    const bool first = (int)blockIdx.z < a.nz;
+    const PackJob &j = first ? a : b;
+    const int z = first ? (int)blockIdx.z : (int)blockIdx.z - a.nz;
     const int rt = blockIdx.y;
-    const int z = blockIdx.z;
+    if (rt >= j.n_rt) return;  // block-uniform
     const int r = threadIdx.x;
     int64_t base, limit;
-    if (counts != nullptr) {
+    if (j.counts != nullptr) {
         if (threadIdx.x == 0) {
             int64_t ro = 0, to = 0;
             row_off[0] = 0;
             rt_off[0] = 0;
             for (int e = 0; e < E; ++e) {
-                const int32_t c = max(counts[e], 0);
+                const int32_t c = max(j.counts[e], 0);
                 ro += c;
                 to += (c + kBM - 1) / kBM;
                 row_off[e + 1] = (int32_t)(ro < (int64_t)INT32_MAX ? ro : (int64_t)INT32_MAX);
@@ -70,42 +84,50 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(
         }
     } else {
         base = (int64_t)rt * kBM;
-        limit = rows_total;
+        limit = j.rows_total;
     }
     const int64_t row = base + r;
-    const bool valid = row < limit && row < rows_total;
-    const float *srow = src + ((int64_t)z * z_rows + (valid ? row : 0)) * sfc;
+    const bool valid = row < limit && row < j.rows_total;
+    const float *srow = j.src + ((int64_t)z * j.z_rows + (valid ? row : 0)) * sfc;
     const bool vec = (sfc % 4) == 0;
+    const int kg0 = blockIdx.x * kKgPerBlock;
+    // all loads first (independent), then pack and store
+    uint32_t v[kKgPerBlock][4];
+#pragma unroll
+    for (int i = 0; i < kKgPerBlock; ++i) {
+        const int64_t k0 = (int64_t)(kg0 + i) * 4;
+        const bool in = valid && (kg0 + i) < n_kg;
+        if (vec) {
+            uint4 f = make_uint4(0u, 0u, 0u, 0u);
+            if (in) f = __ldg(reinterpret_cast<const uint4 *>(srow + k0));
+            v[i][0] = f.x;
+            v[i][1] = f.y;
+            v[i][2] = f.z;
+            v[i][3] = f.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[i][q] = (in && k0 + q < sfc) ? __float_as_uint(__ldg(srow + k0 + q)) : 0u;
+        }
+    }
     bool bad = false;
-    uint8_t *out = dst + (int64_t)z * n_kg * n_rt * 512 + (int64_t)rt * 512 + (r & 31) * 16 +
+    uint8_t *out = j.dst + (int64_t)z * n_kg * j.n_rt * 512 + (int64_t)rt * 512 + (r & 31) * 16 +
                    (r >> 5) * 4;
 #pragma unroll
     for (int i = 0; i < kKgPerBlock; ++i) {
-        const int kg = blockIdx.x * kKgPerBlock + i;
-        if (kg >= n_kg) break;
-        uint32_t word = 0x7F7F7F7Fu;
-        if (valid) {
-            uint32_t v[4];
-            const int64_t k0 = (int64_t)kg * 4;
-            if (vec) {
-                const uint4 f = __ldg(reinterpret_cast<const uint4 *>(srow + k0));
-                v[0] = f.x;
-                v[1] = f.y;
-                v[2] = f.z;
-                v[3] = f.w;
-            } else {
+        const int kg = kg0 + i;
+        if (kg < n_kg) {
+            uint32_t word = 0x7F7F7F7Fu;
+            if (valid) {
+                word = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    v[j] = (k0 + j < sfc) ? __float_as_uint(__ldg(srow + k0 + j)) : 0x3F800000u;
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t c = ((int64_t)kg * 4 + q < sfc) ? code_of(v[i][q], bad) : 127u;
+                    word |= c << (8 * q);
+                }
             }
-            word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t c = (k0 + j < sfc) ? code_of(v[j], bad) : 127u;
-                word |= c << (8 * j);
-            }
+            *reinterpret_cast<uint32_t *>(out + (int64_t)kg * j.n_rt * 512) = word;
         }
-        *reinterpret_cast<uint32_t *>(out + (int64_t)kg * n_rt * 512) = word;
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
         if (atomicCAS(&status[0], 0u, (unsigned)FP8G_ERR_SCALE_FORMAT) == 0u)
@@ -118,14 +140,16 @@ size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
     return (size_t)z * (size_t)n_kg * (size_t)n_rt * 512u;
 }
 
-cudaError_t launch_pack_scales(const float *src, int64_t rows_total, int64_t sfc, int32_t n_kg,
-                               int32_t n_rt, int32_t z, int64_t z_rows, uint8_t *dst,
-                               const int32_t *counts, int32_t E, unsigned int *status,
-                               cudaStream_t s) {
-    if (n_kg <= 0 || n_rt <= 0 || z <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((n_kg + kKgPerBlock - 1) / kKgPerBlock), (unsigned)n_rt, (unsigned)z);
-    pack_scales_kernel<<<grid, 128, 0, s>>>(src, rows_total, sfc, n_kg, n_rt, z_rows, dst, counts,
-                                            E, status);
+cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
+                               int32_t E, unsigned int *status, cudaStream_t s) {
+    if (n_kg <= 0) return cudaSuccess;
+    PackJob ja{a.src, a.rows_total, a.z_rows, a.n_rt, a.nz, a.dst, a.counts};
+    PackJob jb{b.src, b.rows_total, b.z_rows, b.n_rt, b.nz, b.dst, b.counts};
+    const int nz = ja.nz + jb.nz;
+    const int ny = ja.n_rt > jb.n_rt ? ja.n_rt : jb.n_rt;
+    if (nz <= 0 || ny <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((n_kg + kKgPerBlock - 1) / kKgPerBlock), (unsigned)ny, (unsigned)nz);
+    pack_scales_kernel<<<grid, 128, 0, s>>>(ja, jb, sfc, n_kg, E, status);
     return cudaGetLastError();
 }
 

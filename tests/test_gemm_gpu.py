@@ -210,6 +210,24 @@ def test_host_checks_reject_without_launch():
 
 
 def test_plan_reports_tiles():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = fp8g.fp8g_gemm_plan(1, 8192, 8192, 8192)
-    assert p["BM"] == 128 and p["BN"] in (128, 256) and p["G"] == 8
-    assert 1 <= p["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count
+    assert p["BM"] == 128 and p["BN"] in (128, 256) and p["G"] == 8 and p["split_k"] == 1
+    assert 1 <= p["grid"] <= sms
+    s = fp8g.fp8g_gemm_plan(1, 128, 4096, 4096)          # few tiles: K split over a cluster
+    assert 2 <= s["split_k"] <= 8 and s["grid"] % s["split_k"] == 0 and s["grid"] <= sms
+    assert s["BN"] * (s["grid"] // s["split_k"]) >= 4096
+
+
+@pytest.mark.parametrize("K", [256, 384, 1024, 4096])
+def test_split_k_ranges(K):
+    """Few tiles -> K split over a cluster; ragged K-block counts per rank."""
+    M, N = 130, 392
+    g = torch.Generator().manual_seed(K)
+    A = synth.normal((M, K), seed=K)
+    B = synth.normal((N, K), seed=K + 1) * torch.exp(torch.randn(N, 1, generator=g))
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["split_k"] >= 2
+    C, ref, bound = _block_case(A, B, "bf16")
+    assert_within(C, ref, bound, f"split-K block {M}x{N}x{K}")
+    C, ref, bound = _tensor_case(A, B, "f32")
+    assert_within(C, ref, bound, f"split-K per-tensor {M}x{N}x{K}")

@@ -63,11 +63,15 @@ def test_grouped_small_full(counts, N, K):
 
 
 def test_grouped_equals_per_expert_gemms():
+    """The grouped GEMM equals one block-scaled GEMM per expert.  The single
+    GEMMs of these small shapes run split-K (a different, fixed summation
+    order), so both are held to the oracle's bound: |grouped - single| <= 2 bound."""
     counts = np.array([200, 0, 77, 130], np.int32)
     N, K = 392, 512
     w = synth.small_grouped(counts, N, K, seed=3)
-    qa, sa, qb, sb, *_ = _quant_grouped(w)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
     C, _, _, _ = _run_grouped(qa, sa, qb, sb, counts)
+    _, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts, oracle.OUT_BF16)
     off = 0
     for e, m in enumerate(counts.tolist()):
         if m == 0:
@@ -75,9 +79,10 @@ def test_grouped_equals_per_expert_gemms():
         Ce = torch.empty(m, N, dtype=torch.bfloat16, device="cuda")
         fp8g.fp8_gemm_blockscaled(qa[off:off + m], qb[e], sa[off:off + m], sb[e], Ce,
                                   fp8g.FP8G_OUT_BF16, m, N, K)
-        # same tile math, same accumulation order -> identical bits
-        assert np.array_equal(Ce.float().cpu().numpy(), C[off:off + m])
+        d = np.abs(Ce.float().cpu().numpy().astype(np.float64) - C[off:off + m])
+        assert (d <= 2 * bound[off:off + m]).all()
         off += m
+    assert fp8g.fp8_gemm_status()[0] == 0
 
 
 def test_grouped_counts_mismatch_is_reported():
