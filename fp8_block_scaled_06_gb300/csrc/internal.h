@@ -14,7 +14,7 @@ namespace fp8g {
 // paragraph of the JAX/Blackwell FP8 GEMM page).
 constexpr int kBM = 128;
 constexpr int kBK = 128;
-constexpr int kRasterG = 8;  // grouped raster band height (GROUP_M)
+constexpr int kRasterG = 16;  // grouped raster band height (GROUP_M)
 
 enum Mode : int { kModeTensor = 0, kModeBlock = 1, kModeGrouped = 2 };
 

@@ -83,6 +83,6 @@ def test_host_argument_checks(fp8g):
 
 def test_grouped_plan_host_only(fp8g):
     p = fp8g.fp8g_grouped_plan(14336, 4096, 32768, 8)
-    assert p["BM"] == 128 and p["G"] == 8 and p["BN"] in (128, 256)
+    assert p["BM"] == 128 and p["G"] == 16 and p["BN"] in (128, 256)
     npn = -(-14336 // p["BN"])
     assert p["max_tiles"] == (32768 // 128 + 8) * npn

@@ -212,7 +212,7 @@ def test_host_checks_reject_without_launch():
 def test_plan_reports_tiles():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = fp8g.fp8g_gemm_plan(1, 8192, 8192, 8192)
-    assert p["BM"] == 128 and p["BN"] in (128, 256) and p["G"] == 8 and p["split_k"] == 1
+    assert p["BM"] == 128 and p["BN"] in (128, 256) and p["G"] == 16 and p["split_k"] == 1
     assert 1 <= p["grid"] <= sms
     s = fp8g.fp8g_gemm_plan(1, 128, 4096, 4096)          # few tiles: K split over a cluster
     assert 2 <= s["split_k"] <= 8 and s["grid"] % s["split_k"] == 0 and s["grid"] <= sms
