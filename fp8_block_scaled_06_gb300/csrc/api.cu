@@ -216,7 +216,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.N = N;
     p.K = K;
     p.num_kb = (int32_t)((K + kBK - 1) / kBK);
-    p.npm = (int32_t)((M + kBM - 1) / kBM);
+    p.npm = (int32_t)((M + kc.BM - 1) / kc.BM);
     p.npn = (int32_t)((N + kc.BN - 1) / kc.BN);
     p.T = (int64_t)p.npm * p.npn;
     p.split = kc.split;
@@ -242,11 +242,11 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     }
     if (mode == kModeGrouped) {
         const uint64_t dB[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
-        const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.BN, 1u};
+        const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.b_rows, 1u};
         if ((st = tmap_u8(B, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     } else {
         const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
-        const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.BN};
+        const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
         if ((st = tmap_u8(B, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     }
     if (mode == kModeTensor) {
@@ -358,7 +358,7 @@ fp8g_status fp8g_gemm_plan(int block, int64_t M, int64_t N, int64_t K, int32_t *
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
     const KernelChoice kc = choose_kernel(block ? kModeBlock : kModeTensor, M, N, K, di.num_sms);
-    if (BM) *BM = kBM;
+    if (BM) *BM = kc.BM;
     if (BN) *BN = kc.BN;
     if (G) *G = kRasterG;
     if (split_k) *split_k = kc.split;

@@ -34,6 +34,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "kernel_common.cuh"
 
 namespace fp8g {
 
@@ -80,19 +81,6 @@ struct Tile {
     int32_t rtA;  // 128-row tile of A in the packed scale layout
 };
 
-// Grouped raster order: bands of G tile-rows; inside a band walk down one
-// tile-column, then move to the next column.  (Tile counts fit in 31 bits.)
-__device__ __forceinline__ void raster(int32_t t, int32_t npm, int32_t npn, int32_t G, int32_t &pm,
-                                       int32_t &pn) {
-    const int32_t band = G * npn;
-    const int32_t grp = t / band;
-    const int32_t first = grp * G;
-    const int32_t height = min(npm - first, G);
-    const int32_t in_band = t - grp * band;
-    pm = first + in_band % height;
-    pn = in_band / height;
-}
-
 template <int MODE, int BN>
 __device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const int32_t *row_off,
                                          const int32_t *tile_off, const int32_t *rt_off) {
@@ -116,42 +104,6 @@ __device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const i
     }
     ti.n0 = ti.pn * BN;
     return ti;
-}
-
-__device__ __forceinline__ void record_error(const GemmParams &p, unsigned code, unsigned detail) {
-    if (atomicCAS(&p.status[0], 0u, code) == 0u) atomicExch(&p.status[1], detail);
-}
-
-// Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting
-// (another role timed out) or when this wait itself exceeded the limit.
-// sleep_ns > 0 backs off between polls (for roles that wait a whole tile).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         const GemmParams &p, unsigned detail,
-                                         uint32_t sleep_ns = 0) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (ptx::globaltimer() - t0 > p.timeout_ns) {
-            *abort_flag = 1;
-            record_error(p, FP8G_ERR_TIMEOUT, detail);
-            return false;
-        }
-        if (sleep_ns) __nanosleep(sleep_ns);
-    }
-}
-
-// Warp-uniform bounded wait: lane 0 waits, the outcome is broadcast, and the
-// warp re-converges before any .sync.aligned tcgen05 instruction follows.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
-                                              volatile int *abort_flag, const GemmParams &p,
-                                              unsigned detail, uint32_t sleep_ns = 0) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, p, detail, sleep_ns) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 // SPLIT: the CTAs of one cluster share an output tile, each taking a
@@ -576,9 +528,12 @@ cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelCh
 
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms) {
     KernelChoice kc;
+    kc.BM = kBM;
     kc.BN = 256;
+    kc.b_rows = 256;
     kc.split = 1;
     kc.cluster = 1;
+    kc.pair = false;
     if (mode == kModeGrouped) {
         kc.grid = num_sms;
         return kc;
@@ -593,11 +548,23 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
         while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) S *= 2;
         if (S >= 2) {
             kc.BN = 128;
+            kc.b_rows = 128;
             kc.split = S;
             kc.cluster = S;
             kc.grid = (int)(tiles128 * S);
             return kc;
         }
+    }
+    // Per-tensor with at least a wave of tiles: 256 x 256 tiles on CTA pairs.
+    if (mode == kModeTensor && tiles >= num_sms) {
+        const int64_t pairs = ((M + 255) / 256) * ((N + 255) / 256);
+        const int64_t clusters = pairs < num_sms / 2 ? pairs : num_sms / 2;
+        kc.BM = 256;
+        kc.b_rows = 128;
+        kc.cluster = 2;
+        kc.pair = true;
+        kc.grid = (int)(2 * clusters);
+        return kc;
     }
     kc.grid = (int)(tiles < num_sms ? tiles : num_sms);
     if (kc.grid < 1) kc.grid = 1;
@@ -607,6 +574,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
 cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                         const KernelChoice &kc, cudaStream_t stream) {
     const bool split = kc.split > 1;
+    if (kc.pair) return launch_gemm_pair(out_f32, maps, p, kc.grid, stream);
     if (mode == kModeTensor) {
         if (split)
             return out_f32 ? launch_one<kModeTensor, 128, 1, 6, true, true>(maps, p, kc, stream)

@@ -1,0 +1,321 @@
+// Per-tensor FP8 GEMM on CTA pairs (tcgen05 cta_group::2), sm_103a.
+//
+// Why: the single-CTA kernel stages 48 KB per 128-wide K step for a 128x256
+// output tile, so four stages fill shared memory and cannot hide the refill
+// latency (measured tensor-pipe activity 64%).  A cluster of two CTAs
+// computes a 256x256 tile with one MMA stream: each CTA loads its own 128 rows
+// of A and 128 rows (one half) of B, 32 KB per K step, so each SM holds six
+// stages and the same MMA work per SM needs two thirds of the bytes.
+//
+// Roles (640 threads per CTA, as in the single-CTA kernel):
+//   warp 0   both CTAs: TMA producer for the CTA's own halves; both complete
+//            on the even CTA's full barrier (TMA cta_group::2)
+//   warp 1   even CTA: the single MMA-issuing thread (M = 256, N = 256)
+//   warps 4-19 both CTAs: epilogue of the CTA's 128 accumulator rows; the
+//            accumulator release is counted on the even CTA's barrier
+// The MMA thread's commits go to both CTAs' barriers (multicast), so each
+// producer learns when a stage is free and each epilogue when its rows are
+// final.  Persistent over 256x256 tiles in the grouped raster order.  Every
+// wait is bounded; tensor memory (256 columns, one accumulator released as
+// soon as it is in registers) is allocated and freed by both CTAs together.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace fp8g {
+
+namespace {
+
+constexpr int kThreads = 640;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 16;
+constexpr int kStages = 6;
+constexpr int kPairBN = 256;                 // output tile: 256 x 256 per pair
+constexpr int kA = kBM * kBK;                // 16 KB: this CTA's 128 rows of A
+constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kA;
+constexpr int kOffBar = kOffB + kStages * kB;
+// full[S], (unused)[S], empty[S], acc_full, acc_empty, drain
+constexpr int kNumBars = 3 * kStages + 3;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kCW = kPairBN / 4;  // columns per epilogue warp
+
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
+
+// Bounded wait with cluster-scope acquire (barriers remote CTAs arrive on).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
+                                                 volatile int *abort_flag, const GemmParams &p,
+                                                 unsigned detail) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p, FP8G_ERR_TIMEOUT, detail);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = ptx::smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_rank();
+    const bool leader = rank == 0;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    auto bar_full = [&](int s) { return ptx::smem_addr(&bars[s]); };
+    auto bar_peer = [&](int s) { return ptx::smem_addr(&bars[kStages + s]); };
+    auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[2 * kStages + s]); };
+    const uint32_t bar_accf = ptx::smem_addr(&bars[3 * kStages]);
+    const uint32_t bar_acce = ptx::smem_addr(&bars[3 * kStages + 1]);
+    const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2]);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+
+    // ------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar_full(s), 1);
+            ptx::mbar_init(bar_peer(s), 1);
+            ptx::mbar_init(bar_empty(s), 1);
+        }
+        ptx::mbar_init(bar_accf, 1);
+        ptx::mbar_init(bar_acce, 2 * kEpiWarps);
+        ptx::mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // both CTAs' barriers and tensor memory exist
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) {
+        // both CTAs must see the same accumulator columns
+        const uint32_t other = ld_cluster_u32(ptx::map_shared(ptx::smem_addr(tmem_slot), rank ^ 1u));
+        if (other != tmem_base) {
+            record_error(p, FP8G_ERR_DEVICE, 0xA11Cu);
+            *abort_flag = 1;
+        }
+    }
+    ptx::grid_dep_wait();  // global memory only after the previous kernel
+    ptx::grid_dep_launch();
+    __syncthreads();
+    const bool run = !*abort_flag;
+
+    const int32_t T = (int32_t)p.T;
+    const int32_t t_first = (int32_t)ptx::cluster_id_x();
+    const int32_t t_step = (int32_t)ptx::num_clusters_x();
+
+    if (run && warp == 0) {
+        // ===== TMA producer (both CTAs): own 128 rows of A, own half of B =====
+        // Both CTAs' copies complete on the even CTA's full barrier (TMA
+        // cta_group::2), which expects both halves; the odd CTA does not arrive.
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            for (int32_t t = t_first; t < T; t += t_step) {
+                int32_t pm, pn;
+                raster(t, p.npm, p.npn, kRasterG, pm, pn);
+                const int32_t row0 = pm * 2 * kBM + (int32_t)rank * kBM;
+                const int32_t nb0 = pn * kPairBN + (int32_t)rank * (kPairBN / 2);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
+                        goto roles_done;
+                    const uint32_t fb = leader ? bar_full(stage) : ptx::map_shared(bar_full(stage), 0);
+                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * (kA + kB));
+                    ptx::tma_load_2d_pair(sbase + kOffA + stage * kA, &tmA, fb, kb * kBK, row0);
+                    ptx::tma_load_2d_pair(sbase + kOffB + stage * kB, &tmB, fb, kb * kBK, nb0);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (run && warp == 1 && leader) {
+        // ===== MMA issuer (even CTA): 256 x 256 x 32 per instruction =====
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int32_t lt = 0;
+            constexpr uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN);
+            for (int32_t t = t_first; t < T; t += t_step, ++lt) {
+                if (!wait_bar_cluster(bar_acce, ((uint32_t)lt & 1u) ^ 1u, abort_flag, p,
+                                      1 * 256 + 64))
+                    goto roles_done;
+                ptx::tc_fence_after();
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_full(stage), phase, abort_flag, p, 1 * 256 + stage))
+                        goto roles_done;
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = sbase + kOffA + stage * kA;
+                    const uint32_t b0 = sbase + kOffB + stage * kB;
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k)
+                        ptx::mma_f8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                         ptx::desc_kmajor_sw128(b0 + k * 32), idesc,
+                                         (kb | k) != 0 ? 1u : 0u);
+                    ptx::tc_commit_pair_mc(bar_empty(stage), 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                ptx::tc_commit_pair_mc(bar_accf, 0x3);
+            }
+        }
+    } else if (run && warp >= kEpiWarp0) {
+        // ===== epilogue (both CTAs): this CTA's 128 rows of the 256 x 256 tile =====
+        const int ew = warp - kEpiWarp0;
+        const int q = warp & 3;
+        const int col0 = (ew >> 2) * kCW;
+        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        const uint32_t acce_leader = ptx::map_shared(bar_acce, 0);
+        int32_t lt = 0;
+        for (int32_t t = t_first; t < T; t += t_step, ++lt) {
+            int32_t pm, pn;
+            raster(t, p.npm, p.npn, kRasterG, pm, pn);
+            if (!wait_bar_warp(bar_accf, (uint32_t)lt & 1u, abort_flag, p, 3 * 256, 128)) break;
+            ptx::tc_fence_after();
+            uint32_t r[kCW / 32][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + col0;
+#pragma unroll
+            for (int c = 0; c < kCW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(acce_leader);
+
+            const int64_t row = (int64_t)pm * 2 * kBM + rank * kBM + q * 32 + lane;
+            if (row < p.M) {
+                const int64_t ncol0 = (int64_t)pn * kPairBN + col0;
+                if constexpr (OUT_F32) {
+                    float *out = reinterpret_cast<float *>(p.C) + row * p.N + ncol0;
+#pragma unroll
+                    for (int c = 0; c < kCW / 32; ++c)
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            if (ncol0 + c * 32 + v * 4 < p.N) {
+                                float4 o;
+                                o.x = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 0]));
+                                o.y = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 1]));
+                                o.z = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 2]));
+                                o.w = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 3]));
+                                *reinterpret_cast<float4 *>(out + c * 32 + v * 4) = o;
+                            }
+                } else {
+                    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.C) + row * p.N + ncol0;
+#pragma unroll
+                    for (int c = 0; c < kCW / 32; ++c)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (ncol0 + c * 32 + v * 8 < p.N) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float lo =
+                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h]));
+                                    const float hi =
+                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h + 1]));
+                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                                    pk[h] = *reinterpret_cast<uint32_t *>(&b2);
+                                }
+                                *reinterpret_cast<uint4 *>(out + c * 32 + v * 8) =
+                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                }
+            }
+        }
+    }
+
+roles_done:
+    __syncwarp();
+    __syncthreads();
+    if (*abort_flag) {
+        if (leader && warp == 1 && lane == 0) {
+            ptx::tc_commit_pair(bar_drain);
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar_drain, 0) && ptx::globaltimer() - t0 < p.timeout_ns) {
+            }
+        }
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 200000ull) {
+        }
+        __syncthreads();
+    }
+    // Neither CTA frees tensor memory (collectively) or leaves while the other
+    // may still arrive on its barriers or its MMAs still run.
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <bool OUT_F32>
+cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
+    auto kern = gemm_pair_kernel<OUT_F32>;
+    static unsigned long long attr_done = 0ull;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((attr_done & bit) == 0ull) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done |= bit;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,
+                             cudaStream_t stream) {
+    return out_f32 ? launch_pair<true>(maps, p, grid, stream)
+                   : launch_pair<false>(maps, p, grid, stream);
+}
+
+}  // namespace fp8g

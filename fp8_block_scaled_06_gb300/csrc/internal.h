@@ -49,16 +49,23 @@ struct GemmMaps {
 };
 
 struct KernelChoice {
-    int BN;
-    int split;
-    int grid;
-    int cluster;
+    int BM;      // output tile rows (256 for a CTA pair)
+    int BN;      // output tile columns
+    int b_rows;  // rows of B per TMA box (a CTA pair loads half of BN each)
+    int split;   // K-split cluster size (1 = none)
+    int grid;    // CTAs launched
+    int cluster; // CTAs per cluster
+    bool pair;   // tcgen05 cta_group::2 kernel (gemm_pair.cu)
 };
 
 // gemm.cu
 cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                         const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
+
+// gemm_pair.cu (per-tensor, CTA pairs)
+cudaError_t launch_gemm_pair(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,
+                             cudaStream_t stream);
 
 // api.cu: checks done by the caller; scratch == nullptr takes the packed
 // scale temporary from the library pool, otherwise uses [scratch,

@@ -231,3 +231,55 @@ def test_split_k_ranges(K):
     assert_within(C, ref, bound, f"split-K block {M}x{N}x{K}")
     C, ref, bound = _tensor_case(A, B, "f32")
     assert_within(C, ref, bound, f"split-K per-tensor {M}x{N}x{K}")
+
+
+# ------------------------------------------------- per-tensor on CTA pairs
+def test_tensor_pair_chosen_for_large():
+    p = fp8g.fp8g_gemm_plan(0, 4096, 4608, 512)
+    assert p["BM"] == 256 and p["BN"] == 256 and p["split_k"] == 1 and p["grid"] % 2 == 0
+
+
+def test_tensor_pair_sampled():
+    M, N, K = 4096, 4608, 512
+    A = synth.normal((M, K), seed=41)
+    B = synth.normal((N, K), seed=42) * 3
+    qa, sa, qa_o, sa_o = quant_both(A, 0)
+    qb, sb, qb_o, sb_o = quant_both(B, 0)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, False, "bf16")
+    rng = np.random.default_rng(7)
+    pi = np.concatenate([rng.integers(0, M, 4096), [0, 255, 256, M - 1, 127, 128]])
+    pj = np.concatenate([rng.integers(0, N, 4096), [N - 1, 0, 255, 256, 4607, 4352]])
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, False, pi, pj, oracle.OUT_BF16)
+    assert_within(C[pi, pj], ref, bound, "pair per-tensor sampled")
+
+
+def test_tensor_pair_ragged_full():
+    M, N, K = 2000, 3000, 640           # partial 256-row and 256-column pair tiles
+    assert fp8g.fp8g_gemm_plan(0, M, N, K)["BM"] == 256
+    A = synth.normal((M, K), seed=43)
+    B = synth.normal((N, K), seed=44)
+    C, ref, bound = _tensor_case(A, B, "f32")
+    assert_within(C, ref, bound, "pair per-tensor ragged")
+
+
+@pytest.mark.parametrize("kind", ["identity", "permutation"])
+def test_tensor_pair_exact(kind):
+    n = 4096
+    A = synth.normal((n, n), seed=45)
+    B = synth.identity(n) if kind == "identity" else synth.permutation_matrix(n, 46)
+    qa, sa, qa_o, sa_o = quant_both(A, 0)
+    qb, sb, qb_o, sb_o = quant_both(B, 0)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, False, "f32")
+    rng = np.random.default_rng(8)
+    pi = rng.integers(0, n, 8192)
+    pj = rng.integers(0, n, 8192)
+    if kind == "permutation":
+        # include the nonzero entry of sampled rows: B[j, pi(j)] = 1
+        perm = np.argmax(qb_o.reshape(n, n) != 0, axis=1)
+        pj[::2] = np.argsort(perm)[rng.integers(0, n, 4096)]
+    ref, _, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, False, pi, pj, oracle.OUT_F32)
+    got = C[pi, pj]
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"{kind}: not bit-exact"
