@@ -249,6 +249,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
         if ((st = tmap_u8(B, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     }
+    maps.SA = maps.A;
+    maps.SB = maps.A;
     if (mode == kModeTensor) {
         const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
         return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
@@ -279,6 +281,19 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     cudaError_t e = launch_pack_scales(pa, pb, p.sfc, p.num_kb, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
+    if (e == cudaSuccess && kc.pair) {
+        // CTA pairs fetch the packed chunks by TMA: each array as rows of 128
+        // uint32 (one 512-byte chunk per row)
+        const uint64_t dSA[2] = {128u, (uint64_t)p.num_kb * (uint64_t)p.n_rtA};
+        const uint32_t bSA[2] = {128u, 1u};
+        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB};
+        const uint32_t bSB[2] = {128u, (uint32_t)pair_sfb_chunks()};
+        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSA, bSA,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
+            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSB, bSB,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
+            e = cudaErrorInvalidValue;
+    }
     if (e == cudaSuccess) e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
     const cudaError_t ef = scratch != nullptr ? cudaSuccess : cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;

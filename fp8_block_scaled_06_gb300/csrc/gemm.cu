@@ -555,8 +555,8 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
             return kc;
         }
     }
-    // Per-tensor with at least a wave of tiles: 256 x 256 tiles on CTA pairs.
-    if (mode == kModeTensor && tiles >= num_sms) {
+    // At least a wave of tiles: 256 x 256 tiles on CTA pairs.
+    if (tiles >= num_sms) {
         const int64_t pairs = ((M + 255) / 256) * ((N + 255) / 256);
         const int64_t clusters = pairs < num_sms / 2 ? pairs : num_sms / 2;
         kc.BM = 256;
@@ -574,7 +574,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
 cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                         const KernelChoice &kc, cudaStream_t stream) {
     const bool split = kc.split > 1;
-    if (kc.pair) return launch_gemm_pair(out_f32, maps, p, kc.grid, stream);
+    if (kc.pair) return launch_gemm_pair(mode, out_f32, maps, p, kc.grid, stream);
     if (mode == kModeTensor) {
         if (split)
             return out_f32 ? launch_one<kModeTensor, 128, 1, 6, true, true>(maps, p, kc, stream)

@@ -35,17 +35,35 @@ constexpr int kStages = 6;
 constexpr int kPairBN = 256;                 // output tile: 256 x 256 per pair
 constexpr int kA = kBM * kBK;                // 16 KB: this CTA's 128 rows of A
 constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kA;
-constexpr int kOffBar = kOffB + kStages * kB;
-// full[S], (unused)[S], empty[S], acc_full, acc_empty, drain
-constexpr int kNumBars = 3 * kStages + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;
+
+// Block-scaled pairs: each CTA's tensor memory holds the scale factors of
+// its own 128 rows of A but of all 256 rows (both halves) of the tile's B,
+// and tcgen05.cp.cta_group::2 copies each CTA's shared memory into its own
+// tensor memory.  (Established on GB300 by the exact scale-layout test: with
+// only the CTA's own half of B's scales the results are wrong.)  So each CTA
+// stages one A chunk and two B chunks of packed scales per K step.
+constexpr int kSfbChunks = 2;
+
+template <int MODE>
+struct PairCfg {
+    static constexpr bool kBlock = MODE != kModeTensor;
+    static constexpr int CHUNK = kBlock ? 512 * (1 + kSfbChunks) : 0;  // packed scales per stage
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + kStages * kA;
+    static constexpr int OFF_SF = OFF_B + kStages * kB;
+    static constexpr int OFF_BAR = OFF_SF + kStages * CHUNK;
+    static constexpr int NUM_BARS = 3 * kStages + 3;  // full, (spare), empty, acc_full, acc_empty, drain
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
+    static constexpr int SF_COLS = kBlock ? 4 + 4 * kSfbChunks : 0;
+    static constexpr uint32_t TMEM_COLS = kBlock ? 512 : 256;
+    static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+    static_assert(256 + kStages * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
+    static_assert(OFF_SF % 128 == 0 && CHUNK % 128 == 0, "TMA destination alignment");
+};
 constexpr int kCW = kPairBN / 4;  // columns per epilogue warp
 
-static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
 // Bounded wait with cluster-scope acquire (barriers remote CTAs arrive on).
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
@@ -70,10 +88,12 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
     return v;
 }
 
-template <bool OUT_F32>
+template <int MODE, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmSA,
+                     const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
+    using PC = PairCfg<MODE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = ptx::smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -83,15 +103,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = ptx::cluster_rank();
     const bool leader = rank == 0;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PC::OFF_BAR);
     auto bar_full = [&](int s) { return ptx::smem_addr(&bars[s]); };
     auto bar_peer = [&](int s) { return ptx::smem_addr(&bars[kStages + s]); };
     auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[2 * kStages + s]); };
     const uint32_t bar_accf = ptx::smem_addr(&bars[3 * kStages]);
     const uint32_t bar_acce = ptx::smem_addr(&bars[3 * kStages + 1]);
     const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2]);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PC::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + PC::OFF_MISC + 4);
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
@@ -109,9 +129,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if constexpr (PC::kBlock) {
+            ptx::prefetch_tmap(&tmSA);
+            ptx::prefetch_tmap(&tmSB);
+        }
     }
     if (warp == 1) {
-        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), PC::TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
@@ -151,9 +175,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = leader ? bar_full(stage) : ptx::map_shared(bar_full(stage), 0);
-                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * (kA + kB));
-                    ptx::tma_load_2d_pair(sbase + kOffA + stage * kA, &tmA, fb, kb * kBK, row0);
-                    ptx::tma_load_2d_pair(sbase + kOffB + stage * kB, &tmB, fb, kb * kBK, nb0);
+                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * PC::TX);
+                    ptx::tma_load_2d_pair(sbase + PC::OFF_A + stage * kA, &tmA, fb, kb * kBK, row0);
+                    ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0);
+                    if constexpr (PC::kBlock) {
+                        // packed UE8M0 chunks (512-byte rows of the packed arrays):
+                        // this CTA's 128 rows of A; B's rows per kSfbChunks
+                        const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
+                        const int32_t rtA = pm * 2 + (int32_t)rank;
+                        const int32_t rtB = pn * 2;  // both 128-row halves of B
+                        ptx::tma_load_2d_pair(dst, &tmSA, fb, 0, kb * p.n_rtA + rtA);
+                        ptx::tma_load_2d_pair(dst + 512, &tmSB, fb, 0, kb * p.n_rtB + rtB);
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -176,13 +209,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_full(stage), phase, abort_flag, p, 1 * 256 + stage))
                         goto roles_done;
                     ptx::tc_fence_after();
-                    const uint32_t a0 = sbase + kOffA + stage * kA;
-                    const uint32_t b0 = sbase + kOffB + stage * kB;
+                    const uint32_t a0 = sbase + PC::OFF_A + stage * kA;
+                    const uint32_t b0 = sbase + PC::OFF_B + stage * kB;
+                    if constexpr (PC::kBlock) {
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
+                        const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k)
-                        ptx::mma_f8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
-                                         ptx::desc_kmajor_sw128(b0 + k * 32), idesc,
-                                         (kb | k) != 0 ? 1u : 0u);
+                        for (int c = 0; c < 1 + kSfbChunks; ++c)
+                            ptx::tc_cp_32x128b_warpx4_pair(sf + 4 * c, ptx::desc_sf_chunk(cs + 512 * c));
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            ptx::mma_mxf8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                               ptx::desc_kmajor_sw128(b0 + k * 32),
+                                               ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k), sf,
+                                               sf + 4, (kb | k) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            ptx::mma_f8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                             ptx::desc_kmajor_sw128(b0 + k * 32), idesc,
+                                             (kb | k) != 0 ? 1u : 0u);
+                    }
                     ptx::tc_commit_pair_mc(bar_empty(stage), 0x3);
                     if (++stage == kStages) {
                         stage = 0;
@@ -197,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - kEpiWarp0;
         const int q = warp & 3;
         const int col0 = (ew >> 2) * kCW;
-        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        float alpha = 1.0f;
+        if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
         const uint32_t acce_leader = ptx::map_shared(bar_acce, 0);
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
@@ -276,27 +324,28 @@ roles_done:
     ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+        ptx::tmem_dealloc_pair(tmem_base, PC::TMEM_COLS);
     }
 }
 
-template <bool OUT_F32>
+template <int MODE, bool OUT_F32>
 cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
-    auto kern = gemm_pair_kernel<OUT_F32>;
+    using PC = PairCfg<MODE>;
+    auto kern = gemm_pair_kernel<MODE, OUT_F32>;
     static unsigned long long attr_done = 0ull;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if ((attr_done & bit) == 0ull) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done |= bit;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = PC::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -307,15 +356,20 @@ cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cud
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, p);
+    return cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.SA, maps.SB, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_pair(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,
-                             cudaStream_t stream) {
-    return out_f32 ? launch_pair<true>(maps, p, grid, stream)
-                   : launch_pair<false>(maps, p, grid, stream);
+int pair_sfb_chunks() { return kSfbChunks; }
+
+cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
+                             int grid, cudaStream_t stream) {
+    if (mode == kModeBlock)
+        return out_f32 ? launch_pair<kModeBlock, true>(maps, p, grid, stream)
+                       : launch_pair<kModeBlock, false>(maps, p, grid, stream);
+    return out_f32 ? launch_pair<kModeTensor, true>(maps, p, grid, stream)
+                   : launch_pair<kModeTensor, false>(maps, p, grid, stream);
 }
 
 }  // namespace fp8g

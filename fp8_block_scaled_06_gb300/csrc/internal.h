@@ -43,9 +43,11 @@ struct GemmParams {
     int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
 };
 
-// TMA descriptors of one launch (E4M3 operands).
+// TMA descriptors of one launch: E4M3 operands and, for block-scaled CTA
+// pairs, the packed scale arrays viewed as rows of 512 bytes (unused ones
+// repeat A's).
 struct GemmMaps {
-    CUtensorMap A, B;
+    CUtensorMap A, B, SA, SB;
 };
 
 struct KernelChoice {
@@ -63,9 +65,10 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                         const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
 
-// gemm_pair.cu (per-tensor, CTA pairs)
-cudaError_t launch_gemm_pair(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,
-                             cudaStream_t stream);
+// gemm_pair.cu (per-tensor and block-scaled, CTA pairs)
+cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
+                             int grid, cudaStream_t stream);
+int pair_sfb_chunks();  // B scale chunks each CTA of a pair stages per K step
 
 // api.cu: checks done by the caller; scratch == nullptr takes the packed
 // scale temporary from the library pool, otherwise uses [scratch,
