@@ -262,7 +262,9 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
     const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
-    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB);
+    // CTA pairs take B's scales replicated for one 128x256b tensor-memory copy
+    // (4 KB per 256 rows and K step instead of 1 KB)
+    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (kc.pair ? 4 : 1);
     void *ws = nullptr;
     if (scratch != nullptr) {
         // caller-provided scratch (the allocation-free entry point)
@@ -276,8 +278,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     }
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
-    PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr};
-    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr};
+    PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
+    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, kc.pair ? 1 : 0};
     cudaError_t e = launch_pack_scales(pa, pb, p.sfc, p.num_kb, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
@@ -286,8 +288,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         // uint32 (one 512-byte chunk per row)
         const uint64_t dSA[2] = {128u, (uint64_t)p.num_kb * (uint64_t)p.n_rtA};
         const uint32_t bSA[2] = {128u, 1u};
-        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB};
-        const uint32_t bSB[2] = {128u, (uint32_t)pair_sfb_chunks()};
+        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB * 4};
+        const uint32_t bSB[2] = {128u, 8u};  // 4 KB: one replicated 256-row block
         if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSA, bSA,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
             tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSB, bSB,

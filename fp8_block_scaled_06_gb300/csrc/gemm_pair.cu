@@ -40,14 +40,18 @@ constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
 // its own 128 rows of A but of all 256 rows (both halves) of the tile's B,
 // and tcgen05.cp.cta_group::2 copies each CTA's shared memory into its own
 // tensor memory.  (Established on GB300 by the exact scale-layout test: with
-// only the CTA's own half of B's scales the results are wrong.)  So each CTA
-// stages one A chunk and two B chunks of packed scales per K step.
-constexpr int kSfbChunks = 2;
+// only the CTA's own half of B's scales the results are wrong.)  Each copy
+// instruction costs the MMA stream about 6% (measured), so per K step: A's
+// 128 rows with one 32x128b.warpx4 copy (replicated over the four lane
+// quarters by the copy) and B's 256 rows with one 128x256b copy from a
+// source the packing kernel already replicated (4 KB).
+constexpr int kSfaBytes = 512;
+constexpr int kSfbBytes = 4096;
 
 template <int MODE>
 struct PairCfg {
     static constexpr bool kBlock = MODE != kModeTensor;
-    static constexpr int CHUNK = kBlock ? 512 * (1 + kSfbChunks) : 0;  // packed scales per stage
+    static constexpr int CHUNK = kBlock ? kSfaBytes + kSfbBytes : 0;  // packed scales per stage
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + kStages * kA;
     static constexpr int OFF_SF = OFF_B + kStages * kB;
@@ -56,7 +60,7 @@ struct PairCfg {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
-    static constexpr int SF_COLS = kBlock ? 4 + 4 * kSfbChunks : 0;
+    static constexpr int SF_COLS = kBlock ? 16 : 0;  // A: cols 0-3, B: cols 8-15
     static constexpr uint32_t TMEM_COLS = kBlock ? 512 : 256;
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
     static_assert(256 + kStages * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
@@ -180,12 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0);
                     if constexpr (PC::kBlock) {
                         // packed UE8M0 chunks (512-byte rows of the packed arrays):
-                        // this CTA's 128 rows of A; B's rows per kSfbChunks
+                        // this CTA's 128 rows of A; the tile's 256 rows of B
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
                         const int32_t rtA = pm * 2 + (int32_t)rank;
-                        const int32_t rtB = pn * 2;  // both 128-row halves of B
                         ptx::tma_load_2d_pair(dst, &tmSA, fb, 0, kb * p.n_rtA + rtA);
-                        ptx::tma_load_2d_pair(dst + 512, &tmSB, fb, 0, kb * p.n_rtB + rtB);
+                        // replicated B block of pair tile pn: 8 rows of 512 B
+                        ptx::tma_load_2d_pair(dst + kSfaBytes, &tmSB, fb, 0,
+                                              (kb * (p.n_rtB / 2) + pn) * 8);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -214,15 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (PC::kBlock) {
                         const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                         const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
-#pragma unroll
-                        for (int c = 0; c < 1 + kSfbChunks; ++c)
-                            ptx::tc_cp_32x128b_warpx4_pair(sf + 4 * c, ptx::desc_sf_chunk(cs + 512 * c));
+                        ptx::tc_cp_32x128b_warpx4_pair(sf, ptx::desc_sf_chunk(cs));
+                        ptx::tc_cp_128x256b_pair(sf + 8, ptx::desc_sf_128x256b(cs + kSfaBytes));
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
                                                ptx::desc_kmajor_sw128(b0 + k * 32),
                                                ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k), sf,
-                                               sf + 4, (kb | k) != 0 ? 1u : 0u);
+                                               sf + 8, (kb | k) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
@@ -360,8 +364,6 @@ cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cud
 }
 
 }  // namespace
-
-int pair_sfb_chunks() { return kSfbChunks; }
 
 cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                              int grid, cudaStream_t stream) {

@@ -68,7 +68,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
 // gemm_pair.cu (per-tensor and block-scaled, CTA pairs)
 cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                              int grid, cudaStream_t stream);
-int pair_sfb_chunks();  // B scale chunks each CTA of a pair stages per K step
+
 
 // api.cu: checks done by the caller; scratch == nullptr takes the packed
 // scale temporary from the library pool, otherwise uses [scratch,
@@ -88,6 +88,7 @@ struct PackArgs {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;
+    int32_t rep;  // B of CTA pairs: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
 };
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,

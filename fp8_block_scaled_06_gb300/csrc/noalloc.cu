@@ -16,9 +16,9 @@
 namespace fp8g {
 namespace {
 
-// Packed-scale scratch: (ceil(M/128) + 2 ceil(N/256)) * ceil(K/128) * 512
-// bytes must fit (8 MiB covers e.g. M = N = K = 16384).
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Packed-scale scratch: at most (ceil(M/128) + 8 ceil(N/256)) * ceil(K/128)
+// * 512 bytes must fit (16 MiB; M = N = K = 8192 needs 10 MiB).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;

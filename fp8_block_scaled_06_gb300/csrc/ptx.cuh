@@ -304,6 +304,10 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
 }
+// 128 lanes x 256 bit (8 columns), no replication: lane L takes source row L.
+__device__ __forceinline__ void tc_cp_128x256b_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrive on the barrier at this shared offset in every CTA of `mask` once
 // all tcgen05 operations issued so far have completed.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
@@ -352,6 +356,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 // TMA with 128-byte swizzle: 8-row x 128-byte swizzle atoms stacked every 1024 B.
 __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
     return smem_desc(saddr, 16, 1024, 2);
+}
+
+// 128 rows x 32 bytes, unswizzled: 8-row x 16-byte core matrices, the two
+// 16-byte halves of a row 128 B apart, 8-row groups every 256 B (the source of
+// one tcgen05.cp 128x256b).
+__device__ __forceinline__ uint64_t desc_sf_128x256b(uint32_t saddr) {
+    return smem_desc(saddr, 128, 256, 0);
 }
 
 // 32 rows x 16 bytes, unswizzled (8-row x 16-byte core matrices every 128 B):

@@ -43,6 +43,7 @@ struct PackJob {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;  // grouped A: expert-local row tiles
+    int32_t rep;            // replicated 256-row layout (B of CTA pairs)
 };
 
 // blockIdx.z < a.nz packs operand a (z = blockIdx.z), the rest operand b.
@@ -126,7 +127,24 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(PackJob a, PackJob b, 
                     word |= c << (8 * q);
                 }
             }
-            *reinterpret_cast<uint32_t *>(out + (int64_t)kg * j.n_rt * 512) = word;
+            if (j.rep) {
+                // 256 B rows x 4 K blocks per (z, kg, 256-row tile) in 4 KB:
+                // the 128-lane x 32-byte source of one tcgen05.cp 128x256b,
+                // lane 32 q + d holding rows 32 w + d of both 128-row halves
+                // (h), the same for every lane quarter q; core matrices of 8
+                // lanes x 16 bytes, the two 16-byte halves 128 B apart, lane
+                // groups of 8 every 256 B.
+                const int h = rt & 1, d = r & 31, w = r >> 5;
+                uint8_t *base = j.dst + ((int64_t)z * n_kg + kg) * (j.n_rt / 2) * 4096 +
+                                (int64_t)(rt >> 1) * 4096 + h * 128 + w * 4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int L = 32 * q + d;
+                    *reinterpret_cast<uint32_t *>(base + (L >> 3) * 256 + (L & 7) * 16) = word;
+                }
+            } else {
+                *reinterpret_cast<uint32_t *>(out + (int64_t)kg * j.n_rt * 512) = word;
+            }
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
@@ -143,8 +161,8 @@ size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
                                int32_t E, unsigned int *status, cudaStream_t s) {
     if (n_kg <= 0) return cudaSuccess;
-    PackJob ja{a.src, a.rows_total, a.z_rows, a.n_rt, a.nz, a.dst, a.counts};
-    PackJob jb{b.src, b.rows_total, b.z_rows, b.n_rt, b.nz, b.dst, b.counts};
+    PackJob ja{a.src, a.rows_total, a.z_rows, a.n_rt, a.nz, a.dst, a.counts, a.rep};
+    PackJob jb{b.src, b.rows_total, b.z_rows, b.n_rt, b.nz, b.dst, b.counts, b.rep};
     const int nz = ja.nz + jb.nz;
     const int ny = ja.n_rt > jb.n_rt ? ja.n_rt : jb.n_rt;
     if (nz <= 0 || ny <= 0) return cudaSuccess;

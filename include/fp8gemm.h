@@ -112,12 +112,12 @@ FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const fl
  * the library allocate device memory, e.g. code under a fixed device-memory
  * budget, behind an allocator that owns every device byte, or on a path where
  * allocation calls are not allowed.  Same arguments, results and errors as
- * fp8_gemm_blockscaled, but the repacked scale factors live in a fixed 8 MiB
+ * fp8_gemm_blockscaled, but the repacked scale factors live in a fixed 16 MiB
  * device array that is part of the library (every GPU that loads the library
  * holds it until the process exits); no call allocates or frees memory.
- * Limit: (ceil(M/128) + 2*ceil(N/256)) * ceil(K/128) * 512 bytes must fit in
- * 8 MiB (e.g. M = N = K = 16384); larger shapes return
- * FP8G_ERR_UNSUPPORTED_SHAPE without launching.
+ * Limit: the repacked scales, at most (ceil(M/128) + 8*ceil(N/256)) *
+ * ceil(K/128) * 512 bytes, must fit in 16 MiB (M = N = K = 8192 needs
+ * 10 MiB); larger shapes return FP8G_ERR_UNSUPPORTED_SHAPE without launching.
  * The first call on a device looks up the array's device address (one
  * cudaGetSymbolAddress with that device current); make that first call before
  * any stream capture.  All calls share the one array: calls whose kernels can
