@@ -262,9 +262,10 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
     const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
-    // CTA pairs take B's scales replicated for one 128x256b tensor-memory copy
-    // (4 KB per 256 rows and K step instead of 1 KB)
-    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (kc.pair ? 4 : 1);
+    // 256-wide tiles take B's scales replicated for one 128x256b tensor-memory
+    // copy (4 KB per 256 rows and K step instead of 1 KB)
+    const bool repB = kc.BN == 256;
+    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (repB ? 4 : 1);
     void *ws = nullptr;
     if (scratch != nullptr) {
         // caller-provided scratch (the allocation-free entry point)
@@ -279,7 +280,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
     PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
-    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, kc.pair ? 1 : 0};
+    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, repB ? 1 : 0};
     cudaError_t e = launch_pack_scales(pa, pb, p.sfc, p.num_kb, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
@@ -359,12 +360,14 @@ fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t 
                               int32_t *BN, int32_t *G, int64_t *max_tiles) {
     if (N < 1 || K < 1 || total_rows < 0 || E < 1) return FP8G_ERR_INVALID_ARG;
     if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    const KernelChoice kc = choose_kernel(kModeGrouped, total_rows, N, K, 1);
-    if (BM) *BM = kBM;
+    DevInfo di;
+    const int sms = device_info(di) == FP8G_OK ? di.num_sms : 148;
+    const KernelChoice kc = choose_kernel(kModeGrouped, total_rows, N, K, sms);
+    if (BM) *BM = kc.BM;
     if (BN) *BN = kc.BN;
     if (G) *G = kRasterG;
     // sum_e ceil(M_e / BM) <= floor(total_rows / BM) + E
-    if (max_tiles) *max_tiles = (total_rows / kBM + E) * ((N + kc.BN - 1) / kc.BN);
+    if (max_tiles) *max_tiles = (total_rows / kc.BM + E) * ((N + kc.BN - 1) / kc.BN);
     return FP8G_OK;
 }
 

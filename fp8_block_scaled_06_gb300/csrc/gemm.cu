@@ -50,7 +50,13 @@ struct Cfg {
     static constexpr bool kBlock = MODE != kModeTensor;
     static constexpr int A_BYTES = kBM * kBK;
     static constexpr int B_BYTES = BN * kBK;
-    static constexpr int CHUNK_BYTES = kBlock ? (kBM + BN) * 4 : 0;  // UE8M0, 4 K-blocks per row
+    // Packed UE8M0 scales per stage (4 K blocks per row): A's 128 rows (512 B,
+    // one replicating 32x128b copy); B's rows: 128 -> 512 B the same way,
+    // 256 -> 4 KB already replicated over the four lane quarters (one
+    // 128x256b copy; each copy instruction costs the MMA stream ~6%).
+    static constexpr bool kRepB = kBlock && BN == 256;
+    static constexpr int SFB_BYTES = kBlock ? (kRepB ? 4096 : BN * 4) : 0;
+    static constexpr int CHUNK_BYTES = kBlock ? kBM * 4 + SFB_BYTES : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
@@ -64,7 +70,8 @@ struct Cfg {
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
     static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + CHUNK_BYTES;
     static constexpr int ACC_COLS = NUM_ACC * BN;
-    static constexpr int SF_COLS = kBlock ? (kBM / 32 + BN / 32) : 0;
+    static constexpr int SF_COLS = kBlock ? (kRepB ? 16 : kBM / 32 + BN / 32) : 0;
+    static constexpr int SFB_COL = kRepB ? 8 : kBM / 32;  // B's scale columns in a slot
     static constexpr int SF_COL0 = ACC_COLS;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int CW = BN / 4;  // accumulator columns per epilogue warp
@@ -163,42 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
     int32_t T = (int32_t)p.T;
-    if constexpr (MODE == kModeGrouped) {
-        // counts -> row offsets and tile offsets (experts in index order)
-        if (threadIdx.x < FP8G_MAX_EXPERTS)
-            tile_off[threadIdx.x] = threadIdx.x < p.E ? p.counts[threadIdx.x] : 0;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int64_t r = 0, tt = 0;
-            bool bad = false;
-            int32_t cnt[FP8G_MAX_EXPERTS];
-            for (int e = 0; e < p.E; ++e) {
-                cnt[e] = tile_off[e];
-                if (cnt[e] < 0) bad = true;
-            }
-            row_off[0] = 0;
-            for (int e = 0; e < p.E; ++e) {
-                const int32_t c = max(cnt[e], 0);
-                r += c;
-                row_off[e + 1] = (int32_t)(r < (int64_t)INT32_MAX ? r : (int64_t)INT32_MAX);
-            }
-            if (bad || r != p.M) {
-                bad = true;
-                if (blockIdx.x == 0) record_error(p, FP8G_ERR_INVALID_ARG, 1);
-            }
-            tile_off[0] = 0;
-            rt_off[0] = 0;
-            for (int e = 0; e < p.E; ++e) {
-                const int64_t Me = bad ? 0 : (row_off[e + 1] - row_off[e]);
-                tt += ((Me + kBM - 1) / kBM) * (int64_t)p.npn;
-                tile_off[e + 1] = (int32_t)tt;
-                // packed scale row tiles of A: counted as the packing kernel does
-                rt_off[e + 1] = rt_off[e] + (max(cnt[e], 0) + kBM - 1) / kBM;
-            }
-            if (blockIdx.x == 0 && p.offsets_out != nullptr)
-                for (int e = 0; e <= p.E; ++e) p.offsets_out[e] = row_off[e];
-        }
-    }
+    if constexpr (MODE == kModeGrouped) grouped_prefix(p, kBM, row_off, tile_off, rt_off);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -250,7 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p.sfb_pk +
                             (((int64_t)ti.e * p.num_kb + kb) * p.n_rtB + ti.n0 / kBM) * 512;
                         ptx::bulk_load(dst, sa_src, kBM * 4, fb);
-                        ptx::bulk_load(dst + kBM * 4, sb_src, BN * 4, fb);
+                        if constexpr (C_::kRepB) {
+                            const uint8_t *sb_rep =
+                                p.sfb_pk +
+                                (((int64_t)ti.e * p.num_kb + kb) * (p.n_rtB / 2) + ti.n0 / 256) *
+                                    4096;
+                            ptx::bulk_load(dst + kBM * 4, sb_rep, C_::SFB_BYTES, fb);
+                        } else {
+                            ptx::bulk_load(dst + kBM * 4, sb_src, BN * 4, fb);
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -280,17 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (C_::kBlock) {
                         const uint32_t sf_tmem = tmem_base + C_::SF_COL0 + stage * C_::SF_COLS;
                         const uint32_t sfa_s = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
-                        // one 32-row x 16-byte chunk per 128 tile rows: A, then B
-#pragma unroll
-                        for (int c = 0; c < 1 + BN / 128; ++c)
-                            ptx::tc_cp_32x128b_warpx4(sf_tmem + 4 * c,
-                                                      ptx::desc_sf_chunk(sfa_s + c * 512));
+                        ptx::tc_cp_32x128b_warpx4(sf_tmem, ptx::desc_sf_chunk(sfa_s));
+                        if constexpr (C_::kRepB)
+                            ptx::tc_cp_128x256b(sf_tmem + C_::SFB_COL,
+                                                ptx::desc_sf_128x256b(sfa_s + kBM * 4));
+                        else
+                            ptx::tc_cp_32x128b_warpx4(sf_tmem + C_::SFB_COL,
+                                                      ptx::desc_sf_chunk(sfa_s + kBM * 4));
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                           ptx::desc_kmajor_sw128(b0 + k * 32),
                                           ptx::idesc_mxf8(kBM, BN, (uint32_t)k), sf_tmem,
-                                          sf_tmem + kBM / 32, (kb != kb_begin || k != 0) ? 1u : 0u);
+                                          sf_tmem + C_::SFB_COL,
+                                          (kb != kb_begin || k != 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
@@ -535,7 +518,18 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     kc.cluster = 1;
     kc.pair = false;
     if (mode == kModeGrouped) {
-        kc.grid = num_sms;
+        // at least a wave of 128 x 256 tiles (counting rows as one problem):
+        // 256 x 256 tiles on CTA pairs inside each expert
+        const int64_t est = (M / kBM) * ((N + 255) / 256);
+        if (est >= num_sms && num_sms >= 2) {
+            kc.BM = 256;
+            kc.b_rows = 128;
+            kc.cluster = 2;
+            kc.pair = true;
+            kc.grid = 2 * (num_sms / 2);
+        } else {
+            kc.grid = num_sms;
+        }
         return kc;
     }
     const int64_t num_kb = (K + kBK - 1) / kBK;

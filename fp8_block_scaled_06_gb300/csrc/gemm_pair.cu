@@ -58,7 +58,8 @@ struct PairCfg {
     static constexpr int OFF_BAR = OFF_SF + kStages * CHUNK;
     static constexpr int NUM_BARS = 3 * kStages + 3;  // full, (spare), empty, acc_full, acc_empty, drain
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int OFF_GROUP = OFF_MISC + 16;  // row_off, tile_off, rt_off [E + 1]
+    static constexpr int SMEM_BYTES = OFF_GROUP + 3 * (FP8G_MAX_EXPERTS + 1) * 4 + 1024;
     static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
     static constexpr int SF_COLS = kBlock ? 16 : 0;  // A: cols 0-3, B: cols 8-15
     static constexpr uint32_t TMEM_COLS = kBlock ? 512 : 256;
@@ -92,6 +93,36 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
     return v;
 }
 
+// One 256 x 256 output tile of a pair: rows [row0, row0 + 256) (the odd CTA
+// takes the second 128), valid below row_end; columns [pn * 256, + 256);
+// expert e; A's packed scale tiles from rtA0.
+struct PairTile {
+    int32_t row0, row_end, pm, pn, e, rtA0;
+};
+
+template <int MODE>
+__device__ __forceinline__ PairTile pair_tile(int32_t t, const GemmParams &p, const int32_t *row_off,
+                                              const int32_t *tile_off, const int32_t *rt_off) {
+    PairTile ti;
+    if constexpr (MODE == kModeGrouped) {
+        int e = 0;
+        while (tile_off[e + 1] <= t) ++e;
+        const int32_t Me = row_off[e + 1] - row_off[e];
+        raster(t - tile_off[e], (Me + 2 * kBM - 1) / (2 * kBM), p.npn, kRasterG, ti.pm, ti.pn);
+        ti.row0 = row_off[e] + ti.pm * 2 * kBM;
+        ti.row_end = row_off[e + 1];
+        ti.e = e;
+        ti.rtA0 = rt_off[e] + 2 * ti.pm;
+    } else {
+        raster(t, p.npm, p.npn, kRasterG, ti.pm, ti.pn);
+        ti.row0 = ti.pm * 2 * kBM;
+        ti.row_end = (int32_t)p.M;
+        ti.e = 0;
+        ti.rtA0 = 2 * ti.pm;
+    }
+    return ti;
+}
+
 template <int MODE, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -116,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PC::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + PC::OFF_MISC + 4);
+    int32_t *row_off = reinterpret_cast<int32_t *>(smem + PC::OFF_GROUP);
+    int32_t *tile_off = row_off + (FP8G_MAX_EXPERTS + 1);
+    int32_t *rt_off = tile_off + (FP8G_MAX_EXPERTS + 1);
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
@@ -159,8 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dep_launch();
     __syncthreads();
     const bool run = !*abort_flag;
-
-    const int32_t T = (int32_t)p.T;
+    int32_t T = (int32_t)p.T;
+    if constexpr (MODE == kModeGrouped) {
+        grouped_prefix(p, 2 * kBM, row_off, tile_off, rt_off);
+        T = tile_off[p.E];
+    }
     const int32_t t_first = (int32_t)ptx::cluster_id_x();
     const int32_t t_step = (int32_t)ptx::num_clusters_x();
 
@@ -171,26 +208,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {
-                int32_t pm, pn;
-                raster(t, p.npm, p.npn, kRasterG, pm, pn);
-                const int32_t row0 = pm * 2 * kBM + (int32_t)rank * kBM;
-                const int32_t nb0 = pn * kPairBN + (int32_t)rank * (kPairBN / 2);
+                const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
+                const int32_t row0 = ti.row0 + (int32_t)rank * kBM;
+                const int32_t nb0 = ti.pn * kPairBN + (int32_t)rank * (kPairBN / 2);
+                if constexpr (MODE == kModeGrouped) {
+                    if (leader && p.tile_map_out != nullptr)
+                        *reinterpret_cast<int4 *>(p.tile_map_out + 4 * (int64_t)t) =
+                            make_int4(ti.e, ti.pm, ti.pn, 0);
+                }
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = leader ? bar_full(stage) : ptx::map_shared(bar_full(stage), 0);
                     if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * PC::TX);
                     ptx::tma_load_2d_pair(sbase + PC::OFF_A + stage * kA, &tmA, fb, kb * kBK, row0);
-                    ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0);
+                    if constexpr (MODE == kModeGrouped)
+                        ptx::tma_load_3d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0,
+                                              ti.e);
+                    else
+                        ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0);
                     if constexpr (PC::kBlock) {
                         // packed UE8M0 chunks (512-byte rows of the packed arrays):
                         // this CTA's 128 rows of A; the tile's 256 rows of B
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
-                        const int32_t rtA = pm * 2 + (int32_t)rank;
-                        ptx::tma_load_2d_pair(dst, &tmSA, fb, 0, kb * p.n_rtA + rtA);
+                        ptx::tma_load_2d_pair(dst, &tmSA, fb, 0,
+                                              kb * p.n_rtA + ti.rtA0 + (int32_t)rank);
                         // replicated B block of pair tile pn: 8 rows of 512 B
                         ptx::tma_load_2d_pair(dst + kSfaBytes, &tmSB, fb, 0,
-                                              (kb * (p.n_rtB / 2) + pn) * 8);
+                                              ((ti.e * p.num_kb + kb) * (p.n_rtB / 2) + ti.pn) * 8);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -253,8 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acce_leader = ptx::map_shared(bar_acce, 0);
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
-            int32_t pm, pn;
-            raster(t, p.npm, p.npn, kRasterG, pm, pn);
+            const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
             if (!wait_bar_warp(bar_accf, (uint32_t)lt & 1u, abort_flag, p, 3 * 256, 128)) break;
             ptx::tc_fence_after();
             uint32_t r[kCW / 32][32];
@@ -266,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(acce_leader);
 
-            const int64_t row = (int64_t)pm * 2 * kBM + rank * kBM + q * 32 + lane;
-            if (row < p.M) {
-                const int64_t ncol0 = (int64_t)pn * kPairBN + col0;
+            const int64_t row = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;
+            if (row < ti.row_end) {
+                const int64_t ncol0 = (int64_t)ti.pn * kPairBN + col0;
                 if constexpr (OUT_F32) {
                     float *out = reinterpret_cast<float *>(p.C) + row * p.N + ncol0;
 #pragma unroll
@@ -370,6 +414,9 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
     if (mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true>(maps, p, grid, stream)
                        : launch_pair<kModeBlock, false>(maps, p, grid, stream);
+    if (mode == kModeGrouped)
+        return out_f32 ? launch_pair<kModeGrouped, true>(maps, p, grid, stream)
+                       : launch_pair<kModeGrouped, false>(maps, p, grid, stream);
     return out_f32 ? launch_pair<kModeTensor, true>(maps, p, grid, stream)
                    : launch_pair<kModeTensor, false>(maps, p, grid, stream);
 }

@@ -55,4 +55,49 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
     return ok != 0;
 }
 
+// Grouped GEMM problem list, computed by every CTA from the device counts:
+// row_off[e] = first row of expert e (exclusive prefix of counts), tile_off[e]
+// = first output tile of expert e (experts in index order, ceil(M_e/bm) *
+// npn tiles each), rt_off[e] = first 128-row tile of expert e in the packed
+// scale layout of A.  Negative counts or a sum other than total_rows record
+// FP8G_ERR_INVALID_ARG (once, CTA 0) and give zero tiles.  CTA 0 also writes
+// offsets_out.  Call with all threads; ends with __syncthreads.
+__device__ __forceinline__ void grouped_prefix(const GemmParams &p, int bm, int32_t *row_off,
+                                               int32_t *tile_off, int32_t *rt_off) {
+    if (threadIdx.x < FP8G_MAX_EXPERTS)
+        tile_off[threadIdx.x] = threadIdx.x < p.E ? p.counts[threadIdx.x] : 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t r = 0, tt = 0;
+        bool bad = false;
+        int32_t cnt[FP8G_MAX_EXPERTS];
+        for (int e = 0; e < p.E; ++e) {
+            cnt[e] = tile_off[e];
+            if (cnt[e] < 0) bad = true;
+        }
+        row_off[0] = 0;
+        for (int e = 0; e < p.E; ++e) {
+            const int32_t c = max(cnt[e], 0);
+            r += c;
+            row_off[e + 1] = (int32_t)(r < (int64_t)INT32_MAX ? r : (int64_t)INT32_MAX);
+        }
+        if (bad || r != p.M) {
+            bad = true;
+            if (blockIdx.x == 0) record_error(p, FP8G_ERR_INVALID_ARG, 1);
+        }
+        tile_off[0] = 0;
+        rt_off[0] = 0;
+        for (int e = 0; e < p.E; ++e) {
+            const int64_t Me = bad ? 0 : (row_off[e + 1] - row_off[e]);
+            tt += ((Me + bm - 1) / bm) * (int64_t)p.npn;
+            tile_off[e + 1] = (int32_t)tt;
+            // packed scale row tiles of A: counted as the packing kernel does
+            rt_off[e + 1] = rt_off[e] + (max(cnt[e], 0) + kBM - 1) / kBM;
+        }
+        if (blockIdx.x == 0 && p.offsets_out != nullptr)
+            for (int e = 0; e <= p.E; ++e) p.offsets_out[e] = row_off[e];
+    }
+    __syncthreads();
+}
+
 }  // namespace fp8g

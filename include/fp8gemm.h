@@ -155,7 +155,8 @@ FP8G_API fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float 
  * Tile configuration fp8_grouped_gemm launches for (N, K, total_rows, E):
  * tile height BM, width BN, raster group height G, and an upper bound on the
  * tile count (the capacity tile_map_out needs, in 4-int32 entries).
- * Host-only, synchronous.  Any output pointer may be null.
+ * Synchronous; uses the current device's SM count (148 when no device is
+ * present).  Any output pointer may be null.
  */
 FP8G_API fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
                               int32_t *BN, int32_t *G, int64_t *max_tiles);

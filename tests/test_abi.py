@@ -83,6 +83,8 @@ def test_host_argument_checks(fp8g):
 
 def test_grouped_plan_host_only(fp8g):
     p = fp8g.fp8g_grouped_plan(14336, 4096, 32768, 8)
-    assert p["BM"] == 128 and p["G"] == 16 and p["BN"] in (128, 256)
+    assert p["BM"] in (128, 256) and p["G"] == 16 and p["BN"] in (128, 256)
     npn = -(-14336 // p["BN"])
-    assert p["max_tiles"] == (32768 // 128 + 8) * npn
+    assert p["max_tiles"] == (32768 // p["BM"] + 8) * npn
+    small = fp8g.fp8g_grouped_plan(256, 256, 300, 3)       # far less than a wave of tiles
+    assert small["BM"] == 128

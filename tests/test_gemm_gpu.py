@@ -309,3 +309,25 @@ def test_block_pair_scale_layout_exact():
     got = C[pi, pj]
     bad = np.flatnonzero(got.view(np.uint32) != ref.view(np.uint32))
     assert bad.size == 0, f"{bad.size} mismatches, e.g. {[(pi[b], pj[b], got[b], ref[b]) for b in bad[:4]]}"
+
+
+def test_block_single_cta_256_tiles():
+    """A block-scaled shape with between half a wave and a wave of 128x256
+    tiles runs on single CTAs with 256-wide tiles (no split, no pair)."""
+    M, N, K = 2048, 2048 - 8, 1024
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = fp8g.fp8g_gemm_plan(1, M, N, K)
+    assert plan["BM"] == 128 and plan["BN"] == 256 and plan["split_k"] == 1, (plan, sms)
+    g = torch.Generator().manual_seed(9)
+    A = synth.with_outliers(synth.normal((M, K), seed=51), g)
+    B = synth.normal((N, K), seed=52) * torch.exp(torch.randn(N, 1, generator=g))
+    qa, sa, qa_o, sa_o = quant_both(A, 32)
+    qb, sb, qb_o, sb_o = quant_both(B, 32)
+    assert_codes_equal(qa, sa, qa_o, sa_o)
+    assert_codes_equal(qb, sb, qb_o, sb_o)
+    C = run_gemm(qa, sa, qb, sb, True, "bf16")
+    rng = np.random.default_rng(10)
+    pi = np.concatenate([rng.integers(0, M, 4096), [0, M - 1, 127, 128]])
+    pj = np.concatenate([rng.integers(0, N, 4096), [N - 1, 0, 255, 256]])
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16)
+    assert_within(C[pi, pj], ref, bound, "block single-CTA 256-wide")

@@ -85,6 +85,41 @@ def test_grouped_equals_per_expert_gemms():
     assert fp8g.fp8_gemm_status()[0] == 0
 
 
+def test_grouped_pair_ragged_sampled():
+    """Enough rows for 256 x 256 tiles on CTA pairs, with experts that are
+    empty, one row, ragged against 128 and 256, and consecutive."""
+    counts = np.array([3000, 0, 70, 9000, 257, 1, 0, 129], np.int32)
+    N, K = 2048, 512
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, counts.size)
+    assert plan["BM"] == 256
+    w = synth.small_grouped(counts, N, K, seed=23)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
+    assert np.array_equal(offs, oracle.grouped_offsets(counts))
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert np.array_equal(tmap[:want.shape[0]], want)
+    rng = np.random.default_rng(24)
+    offs_o = oracle.grouped_offsets(counts)
+    # every expert's first and last row, tile boundaries, plus random rows
+    edge = [offs_o[e] for e in range(counts.size) if counts[e]] + \
+           [offs_o[e + 1] - 1 for e in range(counts.size) if counts[e]] + \
+           [offs_o[0] + 255, offs_o[0] + 256, offs_o[3] + 127, offs_o[3] + 128]
+    pi = np.concatenate([np.array(edge), rng.integers(0, rows, 3000)]).astype(np.int64)
+    pj = rng.integers(0, N, pi.size)
+    expert = np.searchsorted(offs_o, pi, side="right") - 1
+    got = C[pi, pj]
+    ref = np.empty(pi.size, np.float32)
+    bound = np.empty(pi.size, np.float64)
+    for e in np.unique(expert):
+        sel = np.flatnonzero(expert == e)
+        r, b, _ = oracle.gemm_sample(qa_o, qb_o[e], sa_o, sb_o[e], True, pi[sel], pj[sel],
+                                     oracle.OUT_BF16)
+        ref[sel] = r
+        bound[sel] = b
+    assert_within(got, ref, bound, "grouped pair ragged")
+
+
 def test_grouped_counts_mismatch_is_reported():
     counts = np.array([10, 20], np.int32)
     N, K = 128, 128
