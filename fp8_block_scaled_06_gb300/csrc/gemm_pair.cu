@@ -16,8 +16,10 @@
 // The MMA thread's commits go to both CTAs' barriers (multicast), so each
 // producer learns when a stage is free and each epilogue when its rows are
 // final.  Persistent over 256x256 tiles in the grouped raster order.  Every
-// wait is bounded; tensor memory (256 columns, one accumulator released as
-// soon as it is in registers) is allocated and freed by both CTAs together.
+// wait is bounded; tensor memory (512 columns: two accumulators per-tensor,
+// one accumulator plus per-stage scale factors block-scaled; an accumulator
+// is released as soon as it is in registers) is allocated and freed by both
+// CTAs together.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -56,13 +58,18 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + kStages * kA;
     static constexpr int OFF_SF = OFF_B + kStages * kB;
     static constexpr int OFF_BAR = OFF_SF + kStages * CHUNK;
-    static constexpr int NUM_BARS = 3 * kStages + 3;  // full, (spare), empty, acc_full, acc_empty, drain
+    // Accumulators: per-tensor double-buffers the 256-column accumulator (the
+    // next tile's MMAs never wait for the epilogue); block modes keep one and
+    // use the other columns for the scale factors of each stage.
+    static constexpr int NUM_ACC = kBlock ? 1 : 2;
+    // full, (spare), empty [S]; acc_full, acc_empty [NUM_ACC]; drain
+    static constexpr int NUM_BARS = 3 * kStages + 2 * NUM_ACC + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;  // row_off, tile_off, rt_off [E + 1]
     static constexpr int SMEM_BYTES = OFF_GROUP + 3 * (FP8G_MAX_EXPERTS + 1) * 4 + 1024;
     static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
     static constexpr int SF_COLS = kBlock ? 16 : 0;  // A: cols 0-3, B: cols 8-15
-    static constexpr uint32_t TMEM_COLS = kBlock ? 512 : 256;
+    static constexpr uint32_t TMEM_COLS = 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
     static_assert(256 + kStages * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
     static_assert(OFF_SF % 128 == 0 && CHUNK % 128 == 0, "TMA destination alignment");
@@ -142,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_full = [&](int s) { return ptx::smem_addr(&bars[s]); };
     auto bar_peer = [&](int s) { return ptx::smem_addr(&bars[kStages + s]); };
     auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[2 * kStages + s]); };
-    const uint32_t bar_accf = ptx::smem_addr(&bars[3 * kStages]);
-    const uint32_t bar_acce = ptx::smem_addr(&bars[3 * kStages + 1]);
-    const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2]);
+    auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[3 * kStages + a]); };
+    auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[3 * kStages + PC::NUM_ACC + a]); };
+    const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2 * PC::NUM_ACC]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PC::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + PC::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + PC::OFF_GROUP);
@@ -158,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_peer(s), 1);
             ptx::mbar_init(bar_empty(s), 1);
         }
-        ptx::mbar_init(bar_accf, 1);
-        ptx::mbar_init(bar_acce, 2 * kEpiWarps);
+        for (int a = 0; a < PC::NUM_ACC; ++a) {
+            ptx::mbar_init(bar_accf(a), 1);
+            ptx::mbar_init(bar_acce(a), 2 * kEpiWarps);
+        }
         ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -251,7 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t lt = 0;
             constexpr uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN);
             for (int32_t t = t_first; t < T; t += t_step, ++lt) {
-                if (!wait_bar_cluster(bar_acce, ((uint32_t)lt & 1u) ^ 1u, abort_flag, p,
+                const int acc = lt % PC::NUM_ACC;
+                const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
+                const uint32_t d_tmem = tmem_base + acc * kPairBN;
+                if (!wait_bar_cluster(bar_acce(acc), acc_par ^ 1u, abort_flag, p,
                                       1 * 256 + 64))
                     goto roles_done;
                 ptx::tc_fence_after();
@@ -268,14 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_cp_128x256b_pair(sf + 8, ptx::desc_sf_128x256b(cs + kSfaBytes));
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
-                            ptx::mma_mxf8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
+                            ptx::mma_mxf8_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                                ptx::desc_kmajor_sw128(b0 + k * 32),
                                                ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k), sf,
                                                sf + 8, (kb | k) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
-                            ptx::mma_f8_pair(tmem_base, ptx::desc_kmajor_sw128(a0 + k * 32),
+                            ptx::mma_f8_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                              ptx::desc_kmajor_sw128(b0 + k * 32), idesc,
                                              (kb | k) != 0 ? 1u : 0u);
                     }
@@ -285,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                ptx::tc_commit_pair_mc(bar_accf, 0x3);
+                ptx::tc_commit_pair_mc(bar_accf(acc), 0x3);
             }
         }
     } else if (run && warp >= kEpiWarp0) {
@@ -295,20 +307,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = (ew >> 2) * kCW;
         float alpha = 1.0f;
         if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
-        const uint32_t acce_leader = ptx::map_shared(bar_acce, 0);
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
-            if (!wait_bar_warp(bar_accf, (uint32_t)lt & 1u, abort_flag, p, 3 * 256, 128)) break;
+            const int acc = lt % PC::NUM_ACC;
+            const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
+            if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc, 128)) break;
             ptx::tc_fence_after();
             uint32_t r[kCW / 32][32];
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + col0;
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(q * 32) << 16) + acc * kPairBN + col0;
 #pragma unroll
             for (int c = 0; c < kCW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
             ptx::tmem_ld_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(acce_leader);
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_shared(bar_acce(acc), 0));
 
             const int64_t row = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;
             if (row < ti.row_end) {
