@@ -255,6 +255,12 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
         return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
     }
+    if (kc.split > 1) {
+        // split-K (few output tiles): the GEMM converts its own scale chunks
+        // from the fp32 scales (p.sa, p.sb; row stride p.sfc)
+        const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+    }
     // Block modes: pack the fp32 scales into UE8M0 chunks (a stream-ordered
     // temporary from the library pool), run the GEMM, return the temporary.
     const int32_t zB = mode == kModeGrouped ? E : 1;

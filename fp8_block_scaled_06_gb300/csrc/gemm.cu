@@ -44,6 +44,11 @@ constexpr int kThreads = 640;  // 20 warps
 constexpr int kMaxSplit = 4;   // K-split cluster size (clusters of <= 4 CTAs co-schedule)
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
+// Block-scaled split-K: eight epilogue warps per K step convert the stage's
+// fp32 block scales (128 rows of A, 128 of B) into its UE8M0 chunk; two such
+// groups take alternate K steps, each with kSfAhead steps of loads in flight.
+constexpr int kSfWarps = 8;
+constexpr int kSfAhead = 4;
 
 template <int MODE, int BN, int NUM_ACC, int STAGES>
 struct Cfg {
@@ -61,8 +66,8 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK_BYTES;
-    // full[S], empty[S], acc_full[NA], acc_empty[NA], drain
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    // full[S], empty[S], acc_full[NA], acc_empty[NA], drain, split-K receive
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;
     static constexpr int GROUP_BYTES = 3 * (FP8G_MAX_EXPERTS + 1) * 4;
@@ -113,14 +118,104 @@ __device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const i
     return ti;
 }
 
+// Block-scaled split-K, epilogue warp ew: writes the UE8M0 chunk (the layout
+// of scales.cu: byte 16 d + 4 w + j = row 32 w + d, K block j; A's 128 rows,
+// then B's) of every other K step of the tile into the ring, after the
+// stage's empty barrier, and counts one arrival per warp on its full barrier.
+// Rows past the operand and K blocks past K/32 get code 127; a scale that is
+// not a positive normal power of two records FP8G_ERR_SCALE_FORMAT.  Returns
+// false when the CTA is aborting.
+template <int STAGES>
+__device__ __forceinline__ bool convert_scales(const GemmParams &p, const Tile &ti, int kb_begin,
+                                               int kb_end, uint32_t it, int ew, uint32_t sf_base,
+                                               uint32_t chunk_bytes, uint64_t *bars,
+                                               volatile int *abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t h = (uint32_t)(ew / kSfWarps);  // this group's K steps: it + i odd / even
+    const int g = (ew % kSfWarps) * 32 + lane;      // 0..255: A rows, then B rows
+    const bool isB = g >= kBM;
+    const int r = g & (kBM - 1);
+    const int64_t grow = isB ? (int64_t)ti.n0 + r : (int64_t)ti.row0 + r;
+    const bool valid = isB ? grow < p.N : grow < ti.row_end;
+    const float *src = (isB ? p.sb : p.sa) + (valid ? grow : 0) * p.sfc;
+    const uint32_t soff = (isB ? kBM * 4u : 0u) + 16u * (uint32_t)(r & 31) + 4u * (uint32_t)(r >> 5);
+    const bool vec = (p.sfc & 3) == 0;
+    const int n = kb_end - kb_begin;
+    bool bad = false, ok = true;
+    for (int i = ((it & 1u) == h) ? 0 : 1; i < n && ok; i += 2 * kSfAhead) {
+        uint32_t v[kSfAhead][4];
+#pragma unroll
+        for (int j = 0; j < kSfAhead; ++j) {
+            const int ii = i + 2 * j;
+            const int64_t k0 = (int64_t)(kb_begin + ii) * 4;
+            if (vec) {
+                uint4 f = make_uint4(0u, 0u, 0u, 0u);
+                if (valid && ii < n) f = __ldg(reinterpret_cast<const uint4 *>(src + k0));
+                v[j][0] = f.x;
+                v[j][1] = f.y;
+                v[j][2] = f.z;
+                v[j][3] = f.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[j][q] = (valid && ii < n && k0 + q < p.sfc) ? __float_as_uint(__ldg(src + k0 + q))
+                                                                 : 0u;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kSfAhead; ++j) {
+            const int ii = i + 2 * j;
+            if (ii >= n) break;  // warp-uniform
+            const uint32_t gi = it + (uint32_t)ii;
+            const uint32_t stage = gi % STAGES, phase = (gi / STAGES) & 1u;
+            if (!wait_bar_warp(ptx::smem_addr(&bars[STAGES + stage]), phase ^ 1u, abort_flag, p,
+                               5 * 256 + stage)) {
+                ok = false;
+                break;
+            }
+            uint32_t word = 0x7F7F7F7Fu;
+            if (valid) {
+                word = 0;
+                const int64_t k0 = (int64_t)(kb_begin + ii) * 4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    word |= (k0 + q < p.sfc ? ue8m0_code(v[j][q], bad) : 127u) << (8 * q);
+            }
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes + soff),
+                         "r"(word)
+                         : "memory");
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[stage]));
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
+    return ok;
+}
+
 // SPLIT: the CTAs of one cluster share an output tile, each taking a
 // contiguous range of K blocks; their fp32 partials meet in distributed shared
-// memory (see the end of the kernel).
+// memory (see the end of the kernel).  Partial layout in the idle operand
+// ring: S column slices of 128 rows x BN/S floats, each contiguous (one bulk
+// copy), 16-byte groups of a row XOR-swizzled by (row & 7) so that the
+// epilogue's row-per-lane stores do not collide in shared-memory banks.
+// Behind the partial, S receive slots of one slice each.
+template <int BN>
+__device__ __forceinline__ uint32_t split_offset(int S, int row, int col) {
+    const int cols = BN / S;
+    const int s = col / cols, c4 = (col % cols) >> 2;
+    return (uint32_t)(s * kBM * cols + row * cols) * 4u + (uint32_t)((c4 ^ (row & 7)) << 4);
+}
 template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
+    // split-K tiles are few: the kernel converts its own scale chunks instead
+    // of reading chunks that a packing kernel wrote
+    constexpr bool kInlineSF = SPLIT && C_::kBlock;
+    static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
+    constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES : C_::TX_BYTES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA tiles need 1024-byte alignment in the shared window
     const uint32_t raw_base = ptx::smem_addr(smem_raw);
@@ -135,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[2 * STAGES + a]); };
     auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[2 * STAGES + NUM_ACC + a]); };
     const uint32_t bar_drain = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC]);
+    const uint32_t bar_recv = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC + 1]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C_::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C_::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + C_::OFF_GROUP);
@@ -144,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar_full(s), 1);
+            ptx::mbar_init(bar_full(s), kInlineSF ? 1 + kSfWarps : 1);
             ptx::mbar_init(bar_empty(s), 1);
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -152,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_acce(a), kEpiWarps);
         }
         ptx::mbar_init(bar_drain, 1);
+        ptx::mbar_init(bar_recv, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -205,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = bar_full(stage);
-                    ptx::mbar_arrive_expect_tx(fb, C_::TX_BYTES);
+                    ptx::mbar_arrive_expect_tx(fb, kTxBytes);
                     ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb, kb * kBK,
                                      ti.row0);
                     if constexpr (MODE == kModeGrouped)
@@ -214,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         ptx::tma_load_2d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
                                          kb * kBK, ti.n0);
-                    if constexpr (C_::kBlock) {
+                    if constexpr (C_::kBlock && !kInlineSF) {
                         const uint32_t dst = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
                         const uint8_t *sa_src =
                             p.sfa_pk + ((int64_t)kb * p.n_rtA + ti.rtA) * 512;
@@ -298,8 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha = 1.0f;
         if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
         int32_t lt = 0;
+        uint32_t it = 0;  // K steps of this CTA so far (the ring's stage counter)
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
+            if constexpr (kInlineSF) {
+                if (!convert_scales<STAGES>(p, ti, kb_begin, kb_end, it, ew,
+                                            sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag))
+                    break;
+                it += (uint32_t)(kb_end - kb_begin);
+            }
             const int acc = lt % NUM_ACC;
             const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
             if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc, 128)) break;
@@ -315,16 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if constexpr (SPLIT) {
                 // fp32 partial of this K range -> own shared memory (the ring is
-                // idle: every MMA, hence every operand read, has completed)
-                float *part = reinterpret_cast<float *>(smem + C_::OFF_A) +
-                              (q * 32 + lane) * (BN + 4) + col0;
+                // idle: every MMA, hence every operand read, has completed),
+                // then made visible to the bulk copies that send it
+                const int row = q * 32 + lane;
 #pragma unroll
                 for (int c = 0; c < C_::CW / 32; ++c)
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        *reinterpret_cast<uint4 *>(part + c * 32 + v * 4) =
+                        *reinterpret_cast<uint4 *>(
+                            smem + C_::OFF_A + split_offset<BN>(p.split, row, col0 + c * 32 + v * 4)) =
                             make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2],
                                        r[c][4 * v + 3]);
+                ptx::fence_proxy_async_smem();
                 continue;
             }
             const int64_t row = (int64_t)ti.row0 + q * 32 + lane;
@@ -389,74 +495,92 @@ roles_done:
         __syncthreads();
     }
     if constexpr (SPLIT) {
-        // Every CTA of the cluster has its partial in shared memory; CTA `rank`
-        // sums column slice `rank` over the cluster in rank order (a fixed
-        // order, so results do not depend on timing) and stores it.
-        ptx::cluster_sync();
-        if (warp >= kEpiWarp0 && t_first < T && !*abort_flag) {
+        // CTA `rank` owns column slice `rank` of the tile.  After a cluster
+        // barrier (every partial written, every ring idle: an execution
+        // dependency only, so the arrive is relaxed; the partial's writes were
+        // ordered before the copies by the fence above and the CTA barrier at
+        // roles_done, the receive barrier's initialisation by its fence) each CTA pushes
+        // slice o of its partial into receive slot `rank` of CTA o with one
+        // bulk copy, counted in bytes on CTA o's receive barrier.  The owner
+        // sums the S slices in rank order (a fixed order, so results do not
+        // depend on timing) and stores them.  A CTA leaves only when every CTA
+        // has received everything, i.e. when no copy reads or writes its
+        // shared memory any more.
+        const int S = p.split;  // 2..kMaxSplit
+        const uint32_t rank = ptx::cluster_rank();
+        const bool has_tile = t_first < T;  // the same for the whole cluster
+        const uint32_t slice_bytes = (uint32_t)(kBM * (BN / S)) * 4u;
+        const uint32_t part = sbase + C_::OFF_A;
+        const uint32_t recv = part + (uint32_t)(kBM * BN) * 4u;
+        if (threadIdx.x == 0 && has_tile)
+            ptx::mbar_arrive_expect_tx(bar_recv, (uint32_t)(S - 1) * slice_bytes);
+        ptx::cluster_arrive_relaxed();
+        ptx::cluster_wait();
+        if (warp == 0) {
+            if (lane == 0 && has_tile)
+                for (int o = 0; o < S; ++o)
+                    if (o != (int)rank)
+                        ptx::bulk_push(ptx::map_shared(recv + rank * slice_bytes, (uint32_t)o),
+                                       part + (uint32_t)o * slice_bytes, slice_bytes,
+                                       ptx::map_shared(bar_recv, (uint32_t)o));
+            __syncwarp();
+        }
+        bool landed = true;
+        if (warp >= kEpiWarp0 && has_tile)
+            landed = wait_bar_landed_warp(bar_recv, 0, abort_flag, p, 4 * 256);
+        ptx::cluster_arrive_relaxed();
+        if (warp >= kEpiWarp0 && has_tile && landed && !*abort_flag) {
             const Tile ti = get_tile<MODE, BN>(t_first, p, row_off, tile_off, rt_off);
-            const int S = p.split;  // 2..kMaxSplit
-            const uint32_t rank = ptx::cluster_rank();
             const int cols = BN / S;
             const int c4n = cols / 4;
             float alpha = 1.0f;
             if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
             const int nthr = kEpiWarps * 32;
-            for (int u0 = threadIdx.x - kEpiWarp0 * 32; u0 < kBM * c4n; u0 += 2 * nthr) {
-                // two output units per pass; all remote loads issued before any add
-                float4 v[2][kMaxSplit];
-                uint32_t local[2];
-                bool have[2];
+            const float *own = reinterpret_cast<const float *>(smem + C_::OFF_A);
+            const float *rcv = own + kBM * BN;
+            for (int u = threadIdx.x - kEpiWarp0 * 32; u < kBM * c4n; u += nthr) {
+                const int row = u / c4n;
+                const int c4 = u % c4n;
+                const int off = row * cols + ((c4 ^ (row & 7)) << 2);  // floats in a slice
+                float4 v[kMaxSplit];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int u = u0 + h * nthr;
-                    have[h] = u < kBM * c4n;
-                    const int row = have[h] ? u / c4n : 0;
-                    const int col = (int)rank * cols + (have[h] ? (u % c4n) * 4 : 0);
-                    local[h] = sbase + C_::OFF_A + (uint32_t)(row * (BN + 4) + col) * 4u;
+                for (int r = 0; r < kMaxSplit; ++r)
+                    if (r < S)
+                        v[r] = *reinterpret_cast<const float4 *>(
+                            (r == (int)rank ? own + (int)rank * kBM * cols : rcv + r * kBM * cols) +
+                            off);
+                float4 acc = v[0];
 #pragma unroll
-                    for (int r = 0; r < kMaxSplit; ++r)
-                        if (r < S) v[h][r] = ptx::ld_cluster_f4(ptx::map_shared(local[h], (uint32_t)r));
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (!have[h]) continue;
-                    const int u = u0 + h * nthr;
-                    float4 acc = v[h][0];
-#pragma unroll
-                    for (int r = 1; r < kMaxSplit; ++r)
-                        if (r < S) {
-                            acc.x += v[h][r].x;
-                            acc.y += v[h][r].y;
-                            acc.z += v[h][r].z;
-                            acc.w += v[h][r].w;
-                        }
-                    const int row = u / c4n;
-                    const int col = (int)rank * cols + (u % c4n) * 4;
-                    const int64_t grow = (int64_t)ti.row0 + row;
-                    const int64_t gcol = (int64_t)ti.n0 + col;
-                    if (grow < ti.row_end && gcol < p.N) {
-                        if constexpr (OUT_F32) {
-                            float4 o = make_float4(__fmul_rn(alpha, acc.x), __fmul_rn(alpha, acc.y),
-                                                   __fmul_rn(alpha, acc.z), __fmul_rn(alpha, acc.w));
-                            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) +
-                                                        grow * p.N + gcol) = o;
-                        } else {
-                            __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(alpha, acc.x),
-                                                                      __fmul_rn(alpha, acc.y));
-                            __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(alpha, acc.z),
-                                                                      __fmul_rn(alpha, acc.w));
-                            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) +
-                                                       grow * p.N + gcol) =
-                                make_uint2(*reinterpret_cast<uint32_t *>(&lo),
-                                           *reinterpret_cast<uint32_t *>(&hi));
-                        }
+                for (int r = 1; r < kMaxSplit; ++r)
+                    if (r < S) {
+                        acc.x += v[r].x;
+                        acc.y += v[r].y;
+                        acc.z += v[r].z;
+                        acc.w += v[r].w;
+                    }
+                const int col = (int)rank * cols + c4 * 4;
+                const int64_t grow = (int64_t)ti.row0 + row;
+                const int64_t gcol = (int64_t)ti.n0 + col;
+                if (grow < ti.row_end && gcol < p.N) {
+                    if constexpr (OUT_F32) {
+                        float4 o = make_float4(__fmul_rn(alpha, acc.x), __fmul_rn(alpha, acc.y),
+                                               __fmul_rn(alpha, acc.z), __fmul_rn(alpha, acc.w));
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + grow * p.N +
+                                                    gcol) = o;
+                    } else {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(alpha, acc.x),
+                                                                  __fmul_rn(alpha, acc.y));
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(alpha, acc.z),
+                                                                  __fmul_rn(alpha, acc.w));
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) +
+                                                   grow * p.N + gcol) =
+                            make_uint2(*reinterpret_cast<uint32_t *>(&lo),
+                                       *reinterpret_cast<uint32_t *>(&hi));
                     }
                 }
             }
         }
-        // no CTA leaves (and frees its shared memory) while others still read it
-        ptx::cluster_sync();
+        ptx::cluster_wait();
     }
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -468,7 +592,7 @@ template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
 cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
                        cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
-    static_assert(!SPLIT || kBM * (BN + 4) * 4 <= STAGES * (C_::A_BYTES + C_::B_BYTES),
+    static_assert(!SPLIT || 2 * kBM * BN * 4 <= STAGES * (C_::A_BYTES + C_::B_BYTES),
                   "split-K partial must fit in the operand ring");
     auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT>;
     // The shared-memory opt-in is per device; the flag races benignly (the

@@ -19,6 +19,17 @@ __device__ __forceinline__ void raster(int32_t t, int32_t npm, int32_t npn, int3
     pn = in_band / height;
 }
 
+// UE8M0 code of an fp32 block scale: a positive power of two's code is its
+// exponent field (lossless).  A NaN scale gives the NaN code 0xFF; any other
+// scale that is not a positive normal power of two sets `bad`.
+__device__ __forceinline__ uint32_t ue8m0_code(uint32_t bits, bool &bad) {
+    const uint32_t ex = (bits >> 23) & 0xFFu;
+    const uint32_t man = bits & 0x7FFFFFu;
+    if (ex == 0xFFu && man != 0u) return 0xFFu;
+    if ((bits >> 31) != 0u || man != 0u || ex == 0u || ex == 0xFFu) bad = true;
+    return ex;
+}
+
 __device__ __forceinline__ void record_error(const GemmParams &p, unsigned code, unsigned detail) {
     if (atomicCAS(&p.status[0], 0u, code) == 0u) atomicExch(&p.status[1], detail);
 }
@@ -43,6 +54,23 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// Bounded wait that does not give up when the CTA is aborting: for copies
+// that other CTAs make into this CTA's shared memory, which must have landed
+// before the CTA may exit.  Returns false only when the limit expired.
+__device__ __forceinline__ bool wait_bar_landed(uint32_t bar, uint32_t parity,
+                                                volatile int *abort_flag, const GemmParams &p,
+                                                unsigned detail) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            record_error(p, FP8G_ERR_TIMEOUT, detail);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Warp-uniform bounded wait: lane 0 waits, the outcome is broadcast, and the
 // warp re-converges before any .sync.aligned tcgen05 instruction follows.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
@@ -50,6 +78,16 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
                                               unsigned detail, uint32_t sleep_ns = 0) {
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, p, detail, sleep_ns) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_bar_landed_warp(uint32_t bar, uint32_t parity,
+                                                     volatile int *abort_flag,
+                                                     const GemmParams &p, unsigned detail) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar_landed(bar, parity, abort_flag, p, detail) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;

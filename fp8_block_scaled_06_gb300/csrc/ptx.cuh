@@ -101,6 +101,15 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
+// The two halves of cluster_sync, for work placed between them.  The relaxed
+// arrive orders no memory accesses (execution order only; it is much cheaper
+// than the release form, which waits for the thread's prior accesses).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Shared address of the same location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -152,6 +161,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// 1-D bulk copy from this CTA's shared memory to shared memory of a CTA of
+// the cluster (dst and bar are shared::cluster addresses, e.g. from
+// map_shared), completing on that CTA's mbarrier; 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_push(uint32_t dst, uint32_t src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 

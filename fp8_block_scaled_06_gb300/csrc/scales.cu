@@ -22,20 +22,13 @@
 // 128-row tile, 8 K groups per block.
 #include "internal.h"
 #include "ptx.cuh"
+#include "kernel_common.cuh"
 
 namespace fp8g {
 
 namespace {
 
 constexpr int kKgPerBlock = 8;
-
-__device__ __forceinline__ uint32_t code_of(uint32_t bits, bool &bad) {
-    const uint32_t ex = (bits >> 23) & 0xFFu;
-    const uint32_t man = bits & 0x7FFFFFu;
-    if (ex == 0xFFu && man != 0u) return 0xFFu;  // NaN scale -> NaN code
-    if ((bits >> 31) != 0u || man != 0u || ex == 0u || ex == 0xFFu) bad = true;
-    return ex;
-}
 
 struct PackJob {
     const float *src;
@@ -123,7 +116,7 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(PackJob a, PackJob b, 
                 word = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint32_t c = ((int64_t)kg * 4 + q < sfc) ? code_of(v[i][q], bad) : 127u;
+                    const uint32_t c = ((int64_t)kg * 4 + q < sfc) ? ue8m0_code(v[i][q], bad) : 127u;
                     word |= c << (8 * q);
                 }
             }

@@ -45,7 +45,8 @@
  *     bytes, taken from a library-owned memory pool with
  *     cudaMallocFromPoolAsync on `stream` and returned with cudaFreeAsync on
  *     `stream` (stream-ordered, so calls on different streams never share
- *     it).  The library also holds one status word per device (a static
+ *     it).  Shapes with few output tiles (split-K: see fp8g_gemm_plan) skip
+ *     the temporary: the GEMM converts the scales itself.  The library also holds one status word per device (a static
  *     device variable) and a host-side tensor-map cache.
  */
 #ifndef FP8GEMM_H
@@ -100,7 +101,9 @@ FP8G_API fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a
  * FP8G_ERR_SCALE_FORMAT in the status word (the output is then unspecified).
  * K % 32 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE).  Other rules as fp8_gemm.
  * Runs two kernels on `stream`: the scale packing (scales -> UE8M0 chunks,
- * which also performs the scale check) and the GEMM.
+ * which also performs the scale check) and the GEMM; split-K shapes (few
+ * output tiles, plan split > 1) run the GEMM alone, which then converts and
+ * checks the scales of each K step itself.
  */
 FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
                                  const float *sfb, void *C, int out, int64_t M, int64_t N,

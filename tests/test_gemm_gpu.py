@@ -178,13 +178,19 @@ def _block_full(w):
 
 
 # ------------------------------------------------------------------- errors
-def test_scale_format_error_recorded():
-    M = N = K = 256
+@pytest.mark.parametrize("M,N,K,bad_b", [(256, 256, 256, False),    # split-K: in-kernel check
+                                         (200, 392, 320, True),     # split-K, K/32 odd
+                                         (2048, 2048, 256, True)])  # packing kernel's check
+def test_scale_format_error_recorded(M, N, K, bad_b):
     qa = torch.zeros(M, K, dtype=torch.uint8, device="cuda")
     qb = torch.zeros(N, K, dtype=torch.uint8, device="cuda")
     sfa = torch.ones(M, K // 32, device="cuda")
     sfb = torch.ones(N, K // 32, device="cuda")
-    sfa[3, 2] = 0.75                                  # not a power of two
+    if bad_b:
+        sfb[N - 1, K // 32 - 1] = -2.0                # negative
+    else:
+        sfa[3, 2] = 0.75                              # not a power of two
+    assert (fp8g.fp8g_gemm_plan(1, M, N, K)["split_k"] > 1) == (M < 1024)
     C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     fp8g.fp8_gemm_blockscaled(qa, qb, sfa, sfb, C, fp8g.FP8G_OUT_BF16, M, N, K)
     st, _ = fp8g.fp8_gemm_status()
