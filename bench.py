@@ -167,6 +167,23 @@ def run_once(fp8g, wl, w, t, C, stream):
                                   wl["K"], stream)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the dominant kernel, from the ncu capture summarised in
+# profiles/gemm_pair_block_8192_ncu.md.  Valid only for the kernel source that
+# capture measured; workloads without a capture report null.
+TRAFFIC_BYTES = {"large8192": 270_719_232 + 117_440_512}
+
+
+def launches_per_call(fp8g, wl) -> int:
+    """Kernels one call launches: the GEMM, plus the scale-packing kernel on the
+    block-scaled paths that do not split K (split-K converts scales itself)."""
+    if wl["kind"] == "tensor":
+        return 1
+    if wl["kind"] == "grouped":
+        return 2
+    return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
+
+
 def oracle_inputs(wl, w):
     """The oracle's own quantisation of the workload (done once, untimed)."""
     import oracle
@@ -323,7 +340,9 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": round(hbm_gbs, 1), "peak": peaks["hbm"],
                 "unit": "GB/s", "frac": round(hbm_gbs / peaks["hbm"], 4)}
-    roof["traffic"] = None
+    roof["traffic"] = TRAFFIC_BYTES.get(args.workload)
+    roof["timed"] = ("whole call: packing kernel + GEMM kernel"
+                     if launches_per_call(fp8g, wl) == 2 else "the GEMM kernel")
     roof["peak_source"] = (f"{peaks['src']}: fp8 = 2 x bf16 burst {peaks['bf16']} TFLOP/s"
                            if tensor_bound else f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
     roof["nominal_frac"] = round(max(flops / 4.5e15, abytes / 8e12) / (ms * 1e-3), 4)
@@ -351,7 +370,7 @@ def main():
         "achieved_hbm_gbs": round(hbm_gbs, 1),
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOPS",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * (1 if wl["kind"] == "tensor" else 3),
+        "gpu_launches": args.steps * launches_per_call(fp8g, wl),
         "clocks": clocks,
         "wall_s": round(wall, 3),
     }
