@@ -17,7 +17,9 @@
 //     memory) into an fp32 accumulator in tensor memory (12.6.1-12.6.2);
 //   - block modes: the producer also bulk-copies each stage's scale factors,
 //     pre-packed as UE8M0 bytes in the layout tcgen05.cp reads (scales.cu),
-//     into the stage; the MMA thread copies them shared -> tensor memory;
+//     into the stage (split-K: epilogue warps convert them in place); warp 2
+//     copies them shared -> tensor memory and commits them to the stage's
+//     "scales ready" barrier, which the MMA thread waits on;
 //   - warps 4..19: epilogue; each warp drains its 32-lane quarter of the
 //     accumulator (tcgen05.ld), releases it, scales / rounds and stores.
 //
@@ -66,8 +68,9 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK_BYTES;
-    // full[S], empty[S], acc_full[NA], acc_empty[NA], drain, split-K receive
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 2;
+    // full[S], empty[S], acc_full[NA], acc_empty[NA], drain, split-K receive,
+    // drain of the scale-copy thread, scales ready[S]
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;
     static constexpr int GROUP_BYTES = 3 * (FP8G_MAX_EXPERTS + 1) * 4;
@@ -231,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[2 * STAGES + NUM_ACC + a]); };
     const uint32_t bar_drain = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC]);
     const uint32_t bar_recv = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC + 1]);
+    const uint32_t bar_drain_sf = ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC + 2]);
+    auto bar_sfr = [&](int s) { return ptx::smem_addr(&bars[2 * STAGES + 2 * NUM_ACC + 3 + s]); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C_::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C_::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + C_::OFF_GROUP);
@@ -242,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full(s), kInlineSF ? 1 + kSfWarps : 1);
             ptx::mbar_init(bar_empty(s), 1);
+            ptx::mbar_init(bar_sfr(s), 1);
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             ptx::mbar_init(bar_accf(a), 1);
@@ -249,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(bar_drain, 1);
         ptx::mbar_init(bar_recv, 1);
+        ptx::mbar_init(bar_drain_sf, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -349,21 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bar(bar_full(stage), phase, abort_flag, p, 1 * 256 + stage))
-                        goto roles_done;
+                    // block modes: data and scale factors in place (the
+                    // scale-copy thread waited for "full" and committed its copies)
+                    const uint32_t rb = C_::kBlock ? bar_sfr(stage) : bar_full(stage);
+                    if (!wait_bar(rb, phase, abort_flag, p, 1 * 256 + stage)) goto roles_done;
                     ptx::tc_fence_after();
                     const uint32_t a0 = sbase + C_::OFF_A + stage * C_::A_BYTES;
                     const uint32_t b0 = sbase + C_::OFF_B + stage * C_::B_BYTES;
                     if constexpr (C_::kBlock) {
                         const uint32_t sf_tmem = tmem_base + C_::SF_COL0 + stage * C_::SF_COLS;
-                        const uint32_t sfa_s = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
-                        ptx::tc_cp_32x128b_warpx4(sf_tmem, ptx::desc_sf_chunk(sfa_s));
-                        if constexpr (C_::kRepB)
-                            ptx::tc_cp_128x256b(sf_tmem + C_::SFB_COL,
-                                                ptx::desc_sf_128x256b(sfa_s + kBM * 4));
-                        else
-                            ptx::tc_cp_32x128b_warpx4(sf_tmem + C_::SFB_COL,
-                                                      ptx::desc_sf_chunk(sfa_s + kBM * 4));
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
@@ -385,6 +386,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ptx::tc_commit(bar_accf(acc));
+            }
+        }
+    } else if (warp == 2 && C_::kBlock) {
+        // ===== scale-factor copies shared -> tensor memory (block modes) =====
+        // Issued from the MMA thread, each copy stalls the MMA stream; from
+        // their own thread they overlap the previous stages' MMAs.  A stage's
+        // tensor-memory slot is rewritten only after "full" of its next use,
+        // i.e. after the producer saw the MMAs that read it complete.
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            for (int32_t t = t_first; t < T; t += t_step) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!wait_bar(bar_full(stage), phase, abort_flag, p, 2 * 256 + stage))
+                        goto roles_done;
+                    ptx::tc_fence_after();
+                    const uint32_t sf_tmem = tmem_base + C_::SF_COL0 + stage * C_::SF_COLS;
+                    const uint32_t sfa_s = sbase + C_::OFF_SF + stage * C_::CHUNK_BYTES;
+                    ptx::tc_cp_32x128b_warpx4(sf_tmem, ptx::desc_sf_chunk(sfa_s));
+                    if constexpr (C_::kRepB)
+                        ptx::tc_cp_128x256b(sf_tmem + C_::SFB_COL,
+                                            ptx::desc_sf_128x256b(sfa_s + kBM * 4));
+                    else
+                        ptx::tc_cp_32x128b_warpx4(sf_tmem + C_::SFB_COL,
+                                                  ptx::desc_sf_chunk(sfa_s + kBM * 4));
+                    ptx::tc_commit(bar_sfr(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
             }
         }
     } else if (warp >= kEpiWarp0) {
@@ -483,10 +514,11 @@ roles_done:
     if (*abort_flag) {
         // Drain: wait (bounded) for this CTA's MMAs, then give in-flight TMA
         // copies a bounded grace period before shared memory is released.
-        if (warp == 1 && lane == 0) {
-            ptx::tc_commit(bar_drain);
+        if ((warp == 1 || (warp == 2 && C_::kBlock)) && lane == 0) {
+            const uint32_t db = warp == 1 ? bar_drain : bar_drain_sf;
+            ptx::tc_commit(db);
             const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try_wait(bar_drain, 0) && ptx::globaltimer() - t0 < p.timeout_ns) {
+            while (!ptx::mbar_try_wait(db, 0) && ptx::globaltimer() - t0 < p.timeout_ns) {
             }
         }
         const uint64_t t0 = ptx::globaltimer();
