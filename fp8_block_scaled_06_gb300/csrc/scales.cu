@@ -17,9 +17,11 @@
 // Grouped A: row tiles are expert-local (an expert's rows start a new tile),
 // numbered in expert order, like the GEMM's tile list.
 //
-// HBM-bound: one launch packs both operands; each thread reads one row's
-// 16-byte scale groups (all loads issued before any is used), 128 threads per
-// 128-row tile, 8 K groups per block.
+// HBM-bound: one launch packs both operands.  A block takes one 128-row tile
+// and 8 K groups: it reads the tile's 128-byte row segments coalesced (8
+// threads per row, 16 bytes each, all loads issued before any is used),
+// converts them to code words in shared memory, and writes whole 16-byte
+// groups of the output (4 rows' words of one K group).
 #include "internal.h"
 #include "ptx.cuh"
 #include "kernel_common.cuh"
@@ -29,6 +31,8 @@ namespace fp8g {
 namespace {
 
 constexpr int kKgPerBlock = 8;
+constexpr int kThreadsPack = 128;
+constexpr int kRowsPerPass = kThreadsPack / kKgPerBlock;  // 16
 
 struct PackJob {
     const float *src;
@@ -36,22 +40,22 @@ struct PackJob {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;  // grouped A: expert-local row tiles
-    int32_t rep;            // replicated 256-row layout (B of CTA pairs)
+    int32_t rep;            // replicated 256-row layout (B of 256-wide tiles)
 };
 
 // blockIdx.z < a.nz packs operand a (z = blockIdx.z), the rest operand b.
-__global__ void __launch_bounds__(128) pack_scales_kernel(PackJob a, PackJob b, int64_t sfc,
-                                                          int32_t n_kg, int32_t E,
-                                                          unsigned int *status) {
+__global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, PackJob b, int64_t sfc,
+                                                                  int32_t n_kg, int32_t E,
+                                                                  unsigned int *status) {
     __shared__ int32_t row_off[FP8G_MAX_EXPERTS + 1];
     __shared__ int32_t rt_off[FP8G_MAX_EXPERTS + 1];
+    __shared__ uint32_t words[kKgPerBlock][kBM];  // code word of (K group, row of the tile)
     ptx::grid_dep_launch();  // the GEMM may start its prologue now
     const bool first = (int)blockIdx.z < a.nz;
     const PackJob &j = first ? a : b;
     const int z = first ? (int)blockIdx.z : (int)blockIdx.z - a.nz;
     const int rt = blockIdx.y;
     if (rt >= j.n_rt) return;  // block-uniform
-    const int r = threadIdx.x;
     int64_t base, limit;
     if (j.counts != nullptr) {
         if (threadIdx.x == 0) {
@@ -80,64 +84,73 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(PackJob a, PackJob b, 
         base = (int64_t)rt * kBM;
         limit = j.rows_total;
     }
-    const int64_t row = base + r;
-    const bool valid = row < limit && row < j.rows_total;
-    const float *srow = j.src + ((int64_t)z * j.z_rows + (valid ? row : 0)) * sfc;
-    const bool vec = (sfc % 4) == 0;
+    if (limit > j.rows_total) limit = j.rows_total;
     const int kg0 = blockIdx.x * kKgPerBlock;
-    // all loads first (independent), then pack and store
-    uint32_t v[kKgPerBlock][4];
+    const int sub = threadIdx.x % kKgPerBlock;  // K group of this thread's loads
+    const int kg = kg0 + sub;
+    const int64_t k0 = (int64_t)kg * 4;
+    const bool vec = (sfc % 4) == 0;
+    const float *zsrc = j.src + (int64_t)z * j.z_rows * sfc;
+    // all loads first (independent): rows threadIdx.x / 8 + 16 p
+    uint32_t v[kBM / kRowsPerPass][4];
 #pragma unroll
-    for (int i = 0; i < kKgPerBlock; ++i) {
-        const int64_t k0 = (int64_t)(kg0 + i) * 4;
-        const bool in = valid && (kg0 + i) < n_kg;
+    for (int pss = 0; pss < kBM / kRowsPerPass; ++pss) {
+        const int64_t row = base + pss * kRowsPerPass + threadIdx.x / kKgPerBlock;
+        const bool in = row < limit && kg < n_kg;
+        const float *srow = zsrc + (in ? row : 0) * sfc;
         if (vec) {
             uint4 f = make_uint4(0u, 0u, 0u, 0u);
             if (in) f = __ldg(reinterpret_cast<const uint4 *>(srow + k0));
-            v[i][0] = f.x;
-            v[i][1] = f.y;
-            v[i][2] = f.z;
-            v[i][3] = f.w;
+            v[pss][0] = f.x;
+            v[pss][1] = f.y;
+            v[pss][2] = f.z;
+            v[pss][3] = f.w;
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                v[i][q] = (in && k0 + q < sfc) ? __float_as_uint(__ldg(srow + k0 + q)) : 0u;
+                v[pss][q] = (in && k0 + q < sfc) ? __float_as_uint(__ldg(srow + k0 + q)) : 0u;
         }
     }
     bool bad = false;
-    uint8_t *out = j.dst + (int64_t)z * n_kg * j.n_rt * 512 + (int64_t)rt * 512 + (r & 31) * 16 +
-                   (r >> 5) * 4;
 #pragma unroll
-    for (int i = 0; i < kKgPerBlock; ++i) {
-        const int kg = kg0 + i;
-        if (kg < n_kg) {
-            uint32_t word = 0x7F7F7F7Fu;
-            if (valid) {
-                word = 0;
+    for (int pss = 0; pss < kBM / kRowsPerPass; ++pss) {
+        const int r = pss * kRowsPerPass + threadIdx.x / kKgPerBlock;
+        uint32_t word = 0x7F7F7F7Fu;  // rows past the operand: scale 1
+        if (base + r < limit) {
+            word = 0;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t c = ((int64_t)kg * 4 + q < sfc) ? ue8m0_code(v[i][q], bad) : 127u;
-                    word |= c << (8 * q);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t c = (k0 + q < sfc) ? ue8m0_code(v[pss][q], bad) : 127u;
+                word |= c << (8 * q);
             }
-            if (j.rep) {
-                // 256 B rows x 4 K blocks per (z, kg, 256-row tile) in 4 KB:
-                // the 128-lane x 32-byte source of one tcgen05.cp 128x256b,
-                // lane 32 q + d holding rows 32 w + d of both 128-row halves
-                // (h), the same for every lane quarter q; core matrices of 8
-                // lanes x 16 bytes, the two 16-byte halves 128 B apart, lane
-                // groups of 8 every 256 B.
-                const int h = rt & 1, d = r & 31, w = r >> 5;
-                uint8_t *base = j.dst + ((int64_t)z * n_kg + kg) * (j.n_rt / 2) * 4096 +
-                                (int64_t)(rt >> 1) * 4096 + h * 128 + w * 4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int L = 32 * q + d;
-                    *reinterpret_cast<uint32_t *>(base + (L >> 3) * 256 + (L & 7) * 16) = word;
-                }
-            } else {
-                *reinterpret_cast<uint32_t *>(out + (int64_t)kg * j.n_rt * 512) = word;
-            }
+        }
+        words[sub][r] = word;
+    }
+    __syncthreads();
+    // 16-byte output groups: the words of rows d, 32 + d, 64 + d, 96 + d of one
+    // K group (byte 16 d + 4 w of a chunk is row 32 w + d)
+    // per z: n_kg x n_rt chunks of 512 B, or (replicated) n_kg x n_rt / 2 blocks of 4 KB
+    uint8_t *zdst = j.dst + (int64_t)z * n_kg * j.n_rt * (j.rep ? 2048 : 512);
+    const int nk = n_kg - kg0 < kKgPerBlock ? n_kg - kg0 : kKgPerBlock;
+    if (j.rep) {
+        // 4 KB per (z, K group, 256-row tile): the 128-lane x 32-byte source of
+        // one tcgen05.cp 128x256b; lane L = 32 q + d holds rows 32 w + d of
+        // both 128-row halves h (bytes 128 h + 4 w of its 32), identical for
+        // the four lane quarters q; 16-byte core rows, lane groups of 8 every
+        // 256 bytes.
+        const int h = rt & 1;
+        for (int i = threadIdx.x; i < nk * kBM; i += kThreadsPack) {
+            const int g = i / kBM, L = i % kBM, d = L & 31;
+            const uint4 o = make_uint4(words[g][d], words[g][32 + d], words[g][64 + d], words[g][96 + d]);
+            uint8_t *out = zdst + ((int64_t)(kg0 + g) * (j.n_rt / 2) + (rt >> 1)) * 4096 +
+                           (L >> 3) * 256 + (L & 7) * 16 + h * 128;
+            *reinterpret_cast<uint4 *>(out) = o;
+        }
+    } else {
+        for (int i = threadIdx.x; i < nk * 32; i += kThreadsPack) {
+            const int g = i / 32, d = i % 32;
+            const uint4 o = make_uint4(words[g][d], words[g][32 + d], words[g][64 + d], words[g][96 + d]);
+            *reinterpret_cast<uint4 *>(zdst + ((int64_t)(kg0 + g) * j.n_rt + rt) * 512 + 16 * d) = o;
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
@@ -160,7 +173,7 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
     const int ny = ja.n_rt > jb.n_rt ? ja.n_rt : jb.n_rt;
     if (nz <= 0 || ny <= 0) return cudaSuccess;
     dim3 grid((unsigned)((n_kg + kKgPerBlock - 1) / kKgPerBlock), (unsigned)ny, (unsigned)nz);
-    pack_scales_kernel<<<grid, 128, 0, s>>>(ja, jb, sfc, n_kg, E, status);
+    pack_scales_kernel<<<grid, kThreadsPack, 0, s>>>(ja, jb, sfc, n_kg, E, status);
     return cudaGetLastError();
 }
 
