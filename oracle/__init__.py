@@ -11,7 +11,9 @@ file's comments:
 
 - E4M3 decode / RNE-satfinite encode (``float8_e4m3fn``; format paragraph of
   "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell GPUs" and the
-  dtype in "Triton FP8 CUTLASS-named kernel benchmarking").
+  dtype in "Triton FP8 CUTLASS-named kernel benchmarking"); the same for E5M2,
+  the other FP8 format that paragraph weighs, and GEMMs whose operands mix
+  the two (``fmt`` arguments: E4M3 = 0, E5M2 = 1).
 - per-tensor (s = amax/448) and 1x32 power-of-two block quantisation
   (microscaling paragraph of the JAX/Blackwell page; Triton tutorial ch. 12,
   section 12.6.1, MXFP8).
@@ -39,6 +41,8 @@ _lock = threading.Lock()
 
 OUT_BF16 = 0
 OUT_F32 = 1
+E4M3 = 0
+E5M2 = 1
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +72,20 @@ def _L():
             lib.oracle_e4m3_table.argtypes = [P]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e5m2_decode.restype = ctypes.c_double
+            lib.oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e5m2_table.argtypes = [P]
+            lib.oracle_e5m2_encode.restype = ctypes.c_uint8
+            lib.oracle_e5m2_encode.argtypes = [ctypes.c_float]
+            lib.oracle_quantize_tensor_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
+            lib.oracle_pow2_scale_fmt.restype = ctypes.c_float
+            lib.oracle_pow2_scale_fmt.argtypes = [ctypes.c_float, ctypes.c_int]
+            lib.oracle_quantize_block32_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
+            lib.oracle_gemm_fmt.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            i64, i64, i64, ctypes.c_int, P, P, P, ctypes.c_int]
+            lib.oracle_gemm_sample_fmt.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, i64, i64, i64, ctypes.c_int, P,
+                                                   P, i64, P, P, P, ctypes.c_int]
             lib.oracle_bf16_round.restype = ctypes.c_float
             lib.oracle_bf16_round.argtypes = [ctypes.c_double]
             lib.oracle_bf16_ulp.restype = ctypes.c_double
@@ -118,6 +136,20 @@ def e4m3_encode(y: float) -> int:
     return int(_L().oracle_e4m3_encode(float(np.float32(y))))
 
 
+def e5m2_decode(code: int) -> float:
+    return float(_L().oracle_e5m2_decode(int(code) & 0xFF))
+
+
+def e5m2_table() -> np.ndarray:
+    out = np.zeros(256, dtype=np.float64)
+    _L().oracle_e5m2_table(_p(out))
+    return out
+
+
+def e5m2_encode(y: float) -> int:
+    return int(_L().oracle_e5m2_encode(float(np.float32(y))))
+
+
 def bf16_round(x: float) -> float:
     return float(_L().oracle_bf16_round(float(x)))
 
@@ -127,34 +159,35 @@ def bf16_ulp(x: float) -> float:
 
 
 # --------------------------------------------------------------- quantisers
-def quantize_tensor(x: np.ndarray):
+def quantize_tensor(x: np.ndarray, fmt: int = E4M3):
     """Per-tensor: returns (codes uint8 same shape, scale float32 scalar array)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows, cols = x.shape
     q = np.empty((rows, cols), dtype=np.uint8)
     s = np.zeros(1, dtype=np.float32)
-    _L().oracle_quantize_tensor(_p(x), rows, cols, _p(q), _p(s))
+    _L().oracle_quantize_tensor_fmt(_p(x), rows, cols, int(fmt), _p(q), _p(s))
     return q, s
 
 
-def pow2_scale(amax: float) -> float:
-    return float(_L().oracle_pow2_scale(float(np.float32(amax))))
+def pow2_scale(amax: float, fmt: int = E4M3) -> float:
+    return float(_L().oracle_pow2_scale_fmt(float(np.float32(amax)), int(fmt)))
 
 
-def quantize_block32(x: np.ndarray):
+def quantize_block32(x: np.ndarray, fmt: int = E4M3):
     """1x32 along the last axis: returns (codes uint8, scales float32 [rows, cols/32])."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows, cols = x.shape
     assert cols % 32 == 0
     q = np.empty((rows, cols), dtype=np.uint8)
     s = np.empty((rows, cols // 32), dtype=np.float32)
-    _L().oracle_quantize_block32(_p(x), rows, cols, _p(q), _p(s))
+    _L().oracle_quantize_block32_fmt(_p(x), rows, cols, int(fmt), _p(q), _p(s))
     return q, s
 
 
 # --------------------------------------------------------------------- GEMM
 def gemm(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray, block: bool,
-         out_kind: int = OUT_BF16, want_exact: bool = False, threads=None):
+         out_kind: int = OUT_BF16, want_exact: bool = False, threads=None, a_fmt: int = E4M3,
+         b_fmt: int = E4M3):
     """C = (sA A)(sB B)^T.  Returns (C_rounded float32 [M,N], bound float64 [M,N], exact|None)."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -170,12 +203,14 @@ def gemm(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray, block: 
     C = np.empty((M, N), dtype=np.float32)
     bound = np.empty((M, N), dtype=np.float64)
     exact = np.empty((M, N), dtype=np.float64) if want_exact else None
-    _L().oracle_gemm(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), M, N, K, int(out_kind),
-                     _p(C), _p(exact) if exact is not None else None, _p(bound), _threads(threads))
+    _L().oracle_gemm_fmt(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt),
+                         int(b_fmt), M, N, K, int(out_kind), _p(C),
+                         _p(exact) if exact is not None else None, _p(bound), _threads(threads))
     return C, bound, exact
 
 
-def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, threads=None):
+def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, threads=None,
+                a_fmt: int = E4M3, b_fmt: int = E4M3):
     """Only the elements (pi[s], pj[s]).  Returns (C float32 [n], bound float64 [n], exact [n])."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -189,9 +224,9 @@ def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, t
     C = np.empty(n, dtype=np.float32)
     bound = np.empty(n, dtype=np.float64)
     exact = np.empty(n, dtype=np.float64)
-    _L().oracle_gemm_sample(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), M, N, K,
-                            int(out_kind), _p(pi), _p(pj), n, _p(C), _p(exact), _p(bound),
-                            _threads(threads))
+    _L().oracle_gemm_sample_fmt(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt),
+                                int(b_fmt), M, N, K, int(out_kind), _p(pi), _p(pj), n, _p(C),
+                                _p(exact), _p(bound), _threads(threads))
     return C, bound, exact
 
 

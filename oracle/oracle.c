@@ -12,6 +12,12 @@
  *     Blackwell GPUs" (format paragraph: E4M3 preferred for its range /
  *     precision balance) and the dtype in "Triton FP8 CUTLASS-named kernel
  *     benchmarking" (parameter list: torch.float8_e4m3fn).
+ *   - E5M2 (the other FP8 format the JAX/Blackwell page's format paragraph
+ *     weighs against E4M3; the Triton tutorial ch. 12, section 12.6.1 lists
+ *     FP8 among the fifth-generation tensor core's types): 1 sign, 5 exponent
+ *     bits (bias 15), 2 mantissa bits, with infinities and NaNs in the top
+ *     binade (the IEEE-style layout); largest finite 57344.  Operands of a
+ *     GEMM may mix the two formats.
  *   - Quantisation x -> RNE_satfinite(fl32(x / s)) with a per-tensor scale
  *     s = fl32(amax / 448) or a 1x32 block scale along K equal to the smallest
  *     power of two >= amax / 448 (the microscaling paragraph of the JAX/Blackwell
@@ -25,9 +31,11 @@
  *   - The grouped raster order of output tiles ("GROUP_M" swizzle of the
  *     persistent matmul in the Triton tutorial ch. 12, section 12.7).
  *
- * All arithmetic is fp64.  Per-block inner sums are exact: each product of two
- * E4M3 values is an integer multiple of 2^-18 with magnitude <= 448^2 < 2^18,
- * so any sum of fewer than 2^17 of them fits in the 53-bit significand.
+ * All arithmetic is fp64.  Per-block inner sums are exact for E4M3: each
+ * product of two E4M3 values is an integer multiple of 2^-18 with magnitude
+ * <= 448^2 < 2^18, so any sum of fewer than 2^17 of them fits in the 53-bit
+ * significand.  With E5M2 operands products span 2^-32 .. 2^32 and a sum may
+ * round (relative error <= K 2^-53, far inside the tolerance).
  * Steps the pages fix in fp32 (fl32(amax/448), fl32(x/s), fl32(sA*sB),
  * fl32(alpha*acc)) are done in fp32 here too.
  *
@@ -67,15 +75,42 @@ ORACLE_EXPORT void oracle_e4m3_table(double *out256) {
     for (int c = 0; c < 256; ++c) out256[c] = oracle_e4m3_decode((uint8_t)c);
 }
 
-/* Round a finite, non-negative real y to the E4M3 grid with round-to-nearest,
- * ties to even mantissa, then saturate to 448.  Works on the magnitude; the
- * caller supplies the sign.  Returns the 7-bit magnitude code. */
-static uint8_t e4m3_mag_code(double y) {
+/* Value of an E5M2 bit pattern: 1 sign bit, 5 exponent bits with bias 15, 2
+ * mantissa bits.  Exponent field 0 is subnormal (m * 2^-16); exponent field 31
+ * is infinity (m = 0) or NaN (m != 0); the largest finite value is
+ * 1.75 * 2^15 = 57344. */
+ORACLE_EXPORT double oracle_e5m2_decode(uint8_t code) {
+    int s = (code >> 7) & 1;
+    int e = (code >> 2) & 31;
+    int m = code & 3;
+    double mag;
+    if (e == 31) {
+        if (m != 0) return NAN;
+        mag = INFINITY;
+    } else if (e == 0) {
+        mag = ldexp((double)m, -16);
+    } else {
+        mag = ldexp(1.0 + (double)m / 4.0, e - 15);
+    }
+    return s ? -mag : mag;
+}
+
+ORACLE_EXPORT void oracle_e5m2_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e5m2_decode((uint8_t)c);
+}
+
+/* Round a finite, non-negative real y to the grid of an FP8 format with
+ * `mbits` mantissa bits and exponent bias `bias` (normal binades from 2^(1 -
+ * bias) up; below that the subnormal quantum 2^(1 - bias - mbits)), with
+ * round-to-nearest, ties to even mantissa, then saturate to `maxv`.  Works on
+ * the magnitude; the caller supplies the sign.  Returns the 7-bit magnitude
+ * code. */
+static uint8_t fp8_mag_code(double y, int mbits, int bias, double maxv) {
     if (y == 0.0) return 0;
-    /* exponent of the leading bit, clamped to the subnormal range */
-    int E = ilogb(y);
-    if (E < -6) E = -6; /* below 2^-6 the spacing is the subnormal quantum 2^-9 */
-    double quantum = ldexp(1.0, E - 3);
+    const int emin = 1 - bias;
+    int E = ilogb(y); /* exponent of the leading bit */
+    if (E < emin) E = emin;
+    double quantum = ldexp(1.0, E - mbits);
     double n = y / quantum; /* exact: power-of-two division */
     double fl = floor(n);
     double frac = n - fl;
@@ -87,16 +122,15 @@ static uint8_t e4m3_mag_code(double y) {
     else
         r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
     double v = r * quantum; /* rounded magnitude, may carry into next binade */
-    if (v > 448.0) v = 448.0; /* satfinite */
+    if (v > maxv) v = maxv; /* satfinite */
     /* encode v exactly */
-    if (v < ldexp(1.0, -6)) {
-        int m = (int)(v / ldexp(1.0, -9));
-        return (uint8_t)m;
-    }
+    if (v < ldexp(1.0, emin)) return (uint8_t)(int)(v / ldexp(1.0, emin - mbits));
     int e = ilogb(v);
-    int m = (int)((v / ldexp(1.0, e) - 1.0) * 8.0);
-    return (uint8_t)(((e + 7) << 3) | m);
+    int m = (int)((v / ldexp(1.0, e) - 1.0) * (double)(1 << mbits));
+    return (uint8_t)(((e + bias) << mbits) | m);
 }
+
+static uint8_t e4m3_mag_code(double y) { return fp8_mag_code(y, 3, 7, 448.0); }
 
 /* E4M3 code of the fp32 value y: RNE, satfinite, NaN -> 0x7F, -0 -> 0x80. */
 ORACLE_EXPORT uint8_t oracle_e4m3_encode(float y) {
@@ -106,6 +140,24 @@ ORACLE_EXPORT uint8_t oracle_e4m3_encode(float y) {
     if (isinf(a)) return (uint8_t)(sign | 0x7E);
     return (uint8_t)(sign | e4m3_mag_code(a));
 }
+
+/* E5M2 code of the fp32 value y: RNE, satfinite (infinities saturate to the
+ * largest finite 57344 as well), NaN -> 0x7F, -0 -> 0x80. */
+ORACLE_EXPORT uint8_t oracle_e5m2_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (isinf(a)) return (uint8_t)(sign | 0x7B);
+    return (uint8_t)(sign | fp8_mag_code(a, 2, 15, 57344.0));
+}
+
+/* FP8 formats of the quantisers and GEMM operands */
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1 };
+
+static uint8_t encode_fmt(float y, int fmt) {
+    return fmt == ORACLE_E5M2 ? oracle_e5m2_encode(y) : oracle_e4m3_encode(y);
+}
+static double fmt_max(int fmt) { return fmt == ORACLE_E5M2 ? 57344.0 : 448.0; }
 
 /* ------------------------------------------------------------------ */
 /* bf16 rounding                                                       */
@@ -160,34 +212,43 @@ static float amax_of(const float *x, int64_t n, int64_t stride) {
     return m;
 }
 
-/* Per-tensor quantisation: s = fl32(amax / 448), q = RNE_satfinite(fl32(x / s)).
- * When s comes out as 0 (amax = 0, or amax so small that the quotient
- * underflows) s = 1 is used instead, so no division by zero happens. */
-ORACLE_EXPORT void oracle_quantize_tensor(const float *x, int64_t rows, int64_t cols,
-                                          uint8_t *q, float *scale_out) {
+/* Per-tensor quantisation: s = fl32(amax / fmax) (fmax = 448 for E4M3, 57344
+ * for E5M2), q = RNE_satfinite(fl32(x / s)).  When s comes out as 0 (amax = 0,
+ * or amax so small that the quotient underflows) s = 1 is used instead, so no
+ * division by zero happens. */
+ORACLE_EXPORT void oracle_quantize_tensor_fmt(const float *x, int64_t rows, int64_t cols,
+                                              int fmt, uint8_t *q, float *scale_out) {
     float amax = amax_of(x, rows * cols, 1);
-    float s = amax / 448.0f;
+    float s = amax / (float)fmt_max(fmt);
     if (s == 0.0f) s = 1.0f;
-    for (int64_t i = 0; i < rows * cols; ++i) q[i] = oracle_e4m3_encode(x[i] / s);
+    for (int64_t i = 0; i < rows * cols; ++i) q[i] = encode_fmt(x[i] / s, fmt);
     *scale_out = s;
 }
 
-/* The power-of-two block scale: the smallest 2^e with 2^e * 448 >= amax,
+ORACLE_EXPORT void oracle_quantize_tensor(const float *x, int64_t rows, int64_t cols,
+                                          uint8_t *q, float *scale_out) {
+    oracle_quantize_tensor_fmt(x, rows, cols, ORACLE_E4M3, q, scale_out);
+}
+
+/* The power-of-two block scale: the smallest 2^e with 2^e * fmax >= amax,
  * clamped to e in [-126, 127]; amax = 0 gives 1. */
-ORACLE_EXPORT float oracle_pow2_scale(float amax) {
+ORACLE_EXPORT float oracle_pow2_scale_fmt(float amax, int fmt) {
     if (amax == 0.0f || isnan(amax)) return 1.0f;
     if (isinf(amax)) return ldexpf(1.0f, 127);
     int e = -126;
     /* linear search is fine: at most 254 steps, exact comparisons in fp64 */
-    while (e < 127 && ldexp(448.0, e) < (double)amax) ++e;
+    while (e < 127 && ldexp(fmt_max(fmt), e) < (double)amax) ++e;
     return ldexpf(1.0f, e);
 }
+
+ORACLE_EXPORT float oracle_pow2_scale(float amax) { return oracle_pow2_scale_fmt(amax, ORACLE_E4M3); }
 
 typedef struct {
     const float *x;
     uint8_t *q;
     float *scales;
     int64_t cols, r0, r1;
+    int fmt;
 } quant_job;
 
 static void *quant_block32_rows(void *arg);
@@ -195,8 +256,8 @@ static void *quant_block32_rows(void *arg);
 /* 1x32 block quantisation along the contiguous (K) axis.  cols % 32 == 0.
  * scales: [rows, cols/32] fp32, each a power of two.  Rows are independent, so
  * they are split across up to 64 threads (no effect on the result). */
-ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t cols,
-                                           uint8_t *q, float *scales) {
+ORACLE_EXPORT void oracle_quantize_block32_fmt(const float *x, int64_t rows, int64_t cols,
+                                               int fmt, uint8_t *q, float *scales) {
     int nt = (int)(rows * cols / (1 << 20));
     if (nt < 1) nt = 1;
     if (nt > 64) nt = 64;
@@ -206,6 +267,7 @@ ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t
     int64_t per = (rows + nt - 1) / nt;
     for (int t = 0; t < nt; ++t) {
         jobs[t].x = x; jobs[t].q = q; jobs[t].scales = scales; jobs[t].cols = cols;
+        jobs[t].fmt = fmt;
         jobs[t].r0 = t * per < rows ? t * per : rows;
         jobs[t].r1 = (t + 1) * per < rows ? (t + 1) * per : rows;
         if (nt == 1 || pthread_create(&tid[t], NULL, quant_block32_rows, &jobs[t]) != 0) {
@@ -215,6 +277,11 @@ ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t
     }
     for (int t = 0; t < nt; ++t)
         if (nt > 1 && tid[t]) pthread_join(tid[t], NULL);
+}
+
+ORACLE_EXPORT void oracle_quantize_block32(const float *x, int64_t rows, int64_t cols,
+                                           uint8_t *q, float *scales) {
+    oracle_quantize_block32_fmt(x, rows, cols, ORACLE_E4M3, q, scales);
 }
 
 static void *quant_block32_rows(void *arg) {
@@ -227,9 +294,9 @@ static void *quant_block32_rows(void *arg) {
     for (int64_t r = j->r0; r < j->r1; ++r) {
         for (int64_t b = 0; b < nb; ++b) {
             const float *blk = x + r * cols + b * 32;
-            float s = oracle_pow2_scale(amax_of(blk, 32, 1));
+            float s = oracle_pow2_scale_fmt(amax_of(blk, 32, 1), j->fmt);
             scales[r * nb + b] = s;
-            for (int k = 0; k < 32; ++k) q[r * cols + b * 32 + k] = oracle_e4m3_encode(blk[k] / s);
+            for (int k = 0; k < 32; ++k) q[r * cols + b * 32 + k] = encode_fmt(blk[k] / s, j->fmt);
         }
     }
     return NULL;
@@ -245,6 +312,7 @@ typedef struct {
     const uint8_t *A, *B;
     const float *sfa, *sfb; /* block: [M,K/32], [N,K/32]; tensor: 1 value each */
     int block;
+    const double *ta, *tb; /* decode tables of A's and B's format */
     int64_t M, N, K;
     int out_kind;
     float *C;        /* rounded output (bf16 values held in float, or fp32) */
@@ -255,13 +323,15 @@ typedef struct {
     int64_t n_samples;
 } gemm_job;
 
-static double dec_tab[256];
-static int dec_ready = 0;
-static void ensure_table(void) {
-    if (!dec_ready) {
-        oracle_e4m3_table(dec_tab);
-        dec_ready = 1;
-    }
+static double dec_e4m3[256], dec_e5m2[256];
+static pthread_once_t dec_once = PTHREAD_ONCE_INIT;
+static void fill_tables(void) {
+    oracle_e4m3_table(dec_e4m3);
+    oracle_e5m2_table(dec_e5m2);
+}
+static const double *table_of(int fmt) {
+    pthread_once(&dec_once, fill_tables);
+    return fmt == ORACLE_E5M2 ? dec_e5m2 : dec_e4m3;
 }
 
 /* One output element.  Block mode:
@@ -281,7 +351,7 @@ static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, dou
         for (int64_t kb = 0; kb < nb; ++kb) {
             double part = 0.0, apart = 0.0;
             for (int64_t k = kb * 32; k < kb * 32 + 32; ++k) {
-                double p = dec_tab[a[k]] * dec_tab[b[k]];
+                double p = g->ta[a[k]] * g->tb[b[k]];
                 part += p;
                 apart += fabs(p);
             }
@@ -293,7 +363,7 @@ static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, dou
     } else {
         double acc = 0.0, aacc = 0.0;
         for (int64_t k = 0; k < g->K; ++k) {
-            double p = dec_tab[a[k]] * dec_tab[b[k]];
+            double p = g->ta[a[k]] * g->tb[b[k]];
             acc += p;
             aacc += fabs(p);
         }
@@ -349,34 +419,52 @@ static void run_jobs(gemm_job proto, int64_t n_items, int threads) {
 }
 
 /* Full GEMM.  block = 0: sfa, sfb each point to one fp32 per-tensor scale.
- * block = 1: sfa [M, K/32], sfb [N, K/32].  C, exact, bound: [M, N]. */
-ORACLE_EXPORT void oracle_gemm(const uint8_t *A, const uint8_t *B, const float *sfa,
-                               const float *sfb, int block, int64_t M, int64_t N, int64_t K,
-                               int out_kind, float *C, double *exact, double *bound,
-                               int threads) {
-    ensure_table();
+ * block = 1: sfa [M, K/32], sfb [N, K/32].  a_fmt, b_fmt: ORACLE_E4M3 or
+ * ORACLE_E5M2.  C, exact, bound: [M, N]. */
+ORACLE_EXPORT void oracle_gemm_fmt(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                   const float *sfb, int block, int a_fmt, int b_fmt, int64_t M,
+                                   int64_t N, int64_t K, int out_kind, float *C, double *exact,
+                                   double *bound, int threads) {
     gemm_job g;
     memset(&g, 0, sizeof g);
     g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.ta = table_of(a_fmt); g.tb = table_of(b_fmt);
     g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
     g.C = C; g.exact = exact; g.bound = bound;
     run_jobs(g, M, threads);
 }
 
+ORACLE_EXPORT void oracle_gemm(const uint8_t *A, const uint8_t *B, const float *sfa,
+                               const float *sfb, int block, int64_t M, int64_t N, int64_t K,
+                               int out_kind, float *C, double *exact, double *bound,
+                               int threads) {
+    oracle_gemm_fmt(A, B, sfa, sfb, block, ORACLE_E4M3, ORACLE_E4M3, M, N, K, out_kind, C, exact,
+                    bound, threads);
+}
+
 /* Sampled GEMM: only the n elements (pi[s], pj[s]). Outputs are length n. */
+ORACLE_EXPORT void oracle_gemm_sample_fmt(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                          const float *sfb, int block, int a_fmt, int b_fmt,
+                                          int64_t M, int64_t N, int64_t K, int out_kind,
+                                          const int64_t *pi, const int64_t *pj, int64_t n,
+                                          float *C, double *exact, double *bound, int threads) {
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.ta = table_of(a_fmt); g.tb = table_of(b_fmt);
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    g.pi = pi; g.pj = pj; g.n_samples = n;
+    run_jobs(g, n, threads);
+}
+
 ORACLE_EXPORT void oracle_gemm_sample(const uint8_t *A, const uint8_t *B, const float *sfa,
                                       const float *sfb, int block, int64_t M, int64_t N,
                                       int64_t K, int out_kind, const int64_t *pi,
                                       const int64_t *pj, int64_t n, float *C, double *exact,
                                       double *bound, int threads) {
-    ensure_table();
-    gemm_job g;
-    memset(&g, 0, sizeof g);
-    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
-    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
-    g.C = C; g.exact = exact; g.bound = bound;
-    g.pi = pi; g.pj = pj; g.n_samples = n;
-    run_jobs(g, n, threads);
+    oracle_gemm_sample_fmt(A, B, sfa, sfb, block, ORACLE_E4M3, ORACLE_E4M3, M, N, K, out_kind, pi,
+                           pj, n, C, exact, bound, threads);
 }
 
 /* ------------------------------------------------------------------ */
