@@ -29,12 +29,15 @@ FP8G_ERR_DEVICE = 7
 
 FP8G_OUT_BF16 = 0
 FP8G_OUT_F32 = 1
+FP8G_E4M3 = 0
+FP8G_E5M2 = 1
 FP8G_MAX_EXPERTS = 64
 
 # Every symbol include/fp8gemm.h declares.
 EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
-    "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8_gemm_status", "fp8g_status_string",
+    "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
+    "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
 
@@ -83,6 +86,16 @@ def load():
         lib.fp8g_gemm_plan.argtypes = [ctypes.c_int, i64, i64, i64, P, P, P, P, P]
         lib.fp8g_quantize_e4m3.restype = st
         lib.fp8g_quantize_e4m3.argtypes = [P, i64, i64, i32, P, P, P]
+        lib.fp8g_quantize.restype = st
+        lib.fp8g_quantize.argtypes = [P, i64, i64, i32, i32, P, P, P]
+        lib.fp8_gemm_fmt.restype = st
+        lib.fp8_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, i64, i64, i64, P]
+        lib.fp8_gemm_blockscaled_fmt.restype = st
+        lib.fp8_gemm_blockscaled_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, i64, i64,
+                                                 i64, P]
+        lib.fp8_grouped_gemm_fmt.restype = st
+        lib.fp8_grouped_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, i64,
+                                             i64, i64, P, P, P]
         lib.fp8_gemm_status.restype = st
         lib.fp8_gemm_status.argtypes = [P, P]
         lib.fp8g_status_string.restype = ctypes.c_char_p
@@ -169,6 +182,33 @@ def fp8g_quantize_e4m3(x, rows: int, cols: int, block: int, q, scales, stream=No
                                      _stream(stream)), "fp8g_quantize_e4m3")
 
 
+def fp8g_quantize(x, rows: int, cols: int, block: int, fmt: int, q, scales, stream=None):
+    _check(load().fp8g_quantize(_ptr(x), rows, cols, int(block), int(fmt), _ptr(q),
+                                _ptr(scales), _stream(stream)), "fp8g_quantize")
+
+
+def fp8_gemm_fmt(A, B, scale_a, scale_b, C, out: int, a_fmt: int, b_fmt: int, M: int, N: int,
+                 K: int, stream=None):
+    _check(load().fp8_gemm_fmt(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), _ptr(C), int(out),
+                               int(a_fmt), int(b_fmt), M, N, K, _stream(stream)), "fp8_gemm_fmt")
+
+
+def fp8_gemm_blockscaled_fmt(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, M: int,
+                             N: int, K: int, stream=None):
+    _check(load().fp8_gemm_blockscaled_fmt(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C),
+                                           int(out), int(a_fmt), int(b_fmt), M, N, K,
+                                           _stream(stream)), "fp8_gemm_blockscaled_fmt")
+
+
+def fp8_grouped_gemm_fmt(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, counts, E: int,
+                         N: int, K: int, total_rows: int, offsets_out=None, tile_map_out=None,
+                         stream=None):
+    _check(load().fp8_grouped_gemm_fmt(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C), int(out),
+                                       int(a_fmt), int(b_fmt), _ptr(counts), E, N, K, total_rows,
+                                       _ptr(offsets_out), _ptr(tile_map_out), _stream(stream)),
+           "fp8_grouped_gemm_fmt")
+
+
 def fp8_gemm_status(stream=None):
     """Returns (status, detail) and clears the device status word."""
     detail = ctypes.c_int32(0)
@@ -192,8 +232,8 @@ def fp8g_version() -> int:
 # Allocation helpers over torch (device memory is plumbing); the work is the
 # ABI call above.
 
-def quantize(x, block: int = 32, stream=None):
-    """fp32 CUDA tensor [rows, cols] -> (uint8 codes, fp32 scales)."""
+def quantize(x, block: int = 32, stream=None, fmt: int = FP8G_E4M3):
+    """fp32 CUDA tensor [rows, cols] -> (uint8 codes, fp32 scales) in format fmt."""
     import torch
     assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2
     x = x.contiguous()
@@ -203,7 +243,7 @@ def quantize(x, block: int = 32, stream=None):
         s = torch.empty((rows, cols // 32), dtype=torch.float32, device=x.device)
     else:
         s = torch.empty((1,), dtype=torch.float32, device=x.device)
-    fp8g_quantize_e4m3(x, rows, cols, block, q, s, stream)
+    fp8g_quantize(x, rows, cols, block, fmt, q, s, stream)
     return q, s
 
 

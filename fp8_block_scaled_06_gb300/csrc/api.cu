@@ -206,7 +206,9 @@ fp8g_status check_common(const void *A, const void *B, const void *C, int out, i
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
-                     void *scratch, size_t scratch_bytes) {
+                     void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt) {
+    if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
+        return FP8G_ERR_INVALID_ARG;
     DevInfo di;
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
@@ -231,6 +233,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.tile_map_out = tile_map_out;
     p.status = di.status;
     p.timeout_ns = timeout_ns();
+    p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
 
     GemmMaps maps;
     const int64_t rows_a = M > 0 ? M : 1;  // grouped with zero rows: A is never read
@@ -314,32 +317,55 @@ using namespace fp8g;
 
 extern "C" {
 
-fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const float *scale_b,
-                     void *C, int out, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+fp8g_status fp8_gemm_fmt(const void *A, const void *B, const float *scale_a,
+                         const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     fp8g_status st = check_common(A, B, C, out, M, N, K);
     if (st != FP8G_OK) return st;
     if (scale_a == nullptr || scale_b == nullptr) return FP8G_ERR_INVALID_ARG;
     if (!aligned(scale_a, 4) || !aligned(scale_b, 4)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeTensor, A, B, scale_a, scale_b, C, out, M, N, K, nullptr, 0, nullptr,
-                    nullptr, stream, nullptr, 0);
+                    nullptr, stream, nullptr, 0, a_fmt, b_fmt);
 }
 
-fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
-                                 const float *sfb, void *C, int out, int64_t M, int64_t N,
-                                 int64_t K, cudaStream_t stream) {
+fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                     void *C, int out, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return fp8_gemm_fmt(A, B, scale_a, scale_b, C, out, FP8G_E4M3, FP8G_E4M3, M, N, K, stream);
+}
+
+fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
+                                     const float *sfb, void *C, int out, int32_t a_fmt,
+                                     int32_t b_fmt, int64_t M, int64_t N, int64_t K,
+                                     cudaStream_t stream) {
     fp8g_status st = check_common(A, B, C, out, M, N, K);
     if (st != FP8G_OK) return st;
     if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
     if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
-                    stream, nullptr, 0);
+                    stream, nullptr, 0, a_fmt, b_fmt);
+}
+
+fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
+                                 const float *sfb, void *C, int out, int64_t M, int64_t N,
+                                 int64_t K, cudaStream_t stream) {
+    return fp8_gemm_blockscaled_fmt(A, B, sfa, sfb, C, out, FP8G_E4M3, FP8G_E4M3, M, N, K,
+                                    stream);
 }
 
 fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, const float *sfb,
                              void *C, int out, const int32_t *counts, int32_t E, int64_t N,
                              int64_t K, int64_t total_rows, int32_t *offsets_out,
                              int32_t *tile_map_out, cudaStream_t stream) {
+    return fp8_grouped_gemm_fmt(A, B, sfa, sfb, C, out, FP8G_E4M3, FP8G_E4M3, counts, E, N, K,
+                                total_rows, offsets_out, tile_map_out, stream);
+}
+
+fp8g_status fp8_grouped_gemm_fmt(const void *A, const void *B, const float *sfa,
+                                 const float *sfb, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                                 const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                 int64_t total_rows, int32_t *offsets_out, int32_t *tile_map_out,
+                                 cudaStream_t stream) {
     if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
     if (E < 1) return FP8G_ERR_INVALID_ARG;
     if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
@@ -359,7 +385,7 @@ fp8g_status fp8_grouped_gemm(const void *A, const void *B, const float *sfa, con
     if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
     if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
-                    offsets_out, tile_map_out, stream, nullptr, 0);
+                    offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt);
 }
 
 fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
@@ -394,7 +420,13 @@ fp8g_status fp8g_gemm_plan(int block, int64_t M, int64_t N, int64_t K, int32_t *
 
 fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32_t block,
                                uint8_t *q, float *scales, cudaStream_t stream) {
+    return fp8g_quantize(x, rows, cols, block, FP8G_E4M3, q, scales, stream);
+}
+
+fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block, int32_t fmt,
+                          uint8_t *q, float *scales, cudaStream_t stream) {
     if (x == nullptr || q == nullptr || scales == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (fmt != FP8G_E4M3 && fmt != FP8G_E5M2) return FP8G_ERR_INVALID_ARG;
     if (rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
     if (block != 0 && block != 32) return FP8G_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4)) return FP8G_ERR_ALIGNMENT;
@@ -405,9 +437,9 @@ fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
     const cudaError_t e =
-        block == 32 ? launch_quantize_block32(x, rows, cols, q, scales, di.num_sms, stream)
-                    : launch_quantize_tensor(x, rows * cols, q, scales, di.status, di.num_sms,
-                                             stream);
+        block == 32 ? launch_quantize_block32(x, rows, cols, fmt, q, scales, di.num_sms, stream)
+                    : launch_quantize_tensor(x, rows * cols, fmt, q, scales, di.status,
+                                             di.num_sms, stream);
     return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

@@ -369,14 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                           ptx::desc_kmajor_sw128(b0 + k * 32),
-                                          ptx::idesc_mxf8(kBM, BN, (uint32_t)k), sf_tmem,
+                                          ptx::idesc_mxf8(kBM, BN, (uint32_t)k) | p.ab_fmt, sf_tmem,
                                           sf_tmem + C_::SFB_COL,
                                           (kb != kb_begin || k != 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_f8(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                                        ptx::desc_kmajor_sw128(b0 + k * 32), ptx::idesc_f8(kBM, BN),
+                                        ptx::desc_kmajor_sw128(b0 + k * 32),
+                                        ptx::idesc_f8(kBM, BN) | p.ab_fmt,
                                         (kb != kb_begin || k != 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar_empty(stage));

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             int32_t lt = 0;
-            constexpr uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN);
+            const uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN) | p.ab_fmt;
             for (int32_t t = t_first; t < T; t += t_step, ++lt) {
                 const int acc = lt % PC::NUM_ACC;
                 const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
                                                ptx::desc_kmajor_sw128(b0 + k * 32),
-                                               ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k), sf,
+                                               ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k) | p.ab_fmt, sf,
                                                sf + 8, (kb | k) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll

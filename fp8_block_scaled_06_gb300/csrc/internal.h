@@ -41,6 +41,7 @@ struct GemmParams {
     const uint8_t *sfa_pk; // block modes: packed UE8M0 scale chunks of A and B
     const uint8_t *sfb_pk;
     int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
+    uint32_t ab_fmt;       // operand formats as MMA instruction-descriptor bits (A: 7-9, B: 10-12)
 };
 
 // TMA descriptors of one launch: E4M3 operands and, for block-scaled CTA
@@ -73,10 +74,11 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
 // api.cu: checks done by the caller; scratch == nullptr takes the packed
 // scale temporary from the library pool, otherwise uses [scratch,
 // scratch + scratch_bytes) (FP8G_ERR_UNSUPPORTED_SHAPE if it is too small).
+// a_fmt, b_fmt: operand formats (FP8G_E4M3 / FP8G_E5M2).
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
-                     void *scratch, size_t scratch_bytes);
+                     void *scratch, size_t scratch_bytes, int a_fmt = 0, int b_fmt = 0);
 
 // scales.cu: fp32 1x32 scales -> packed UE8M0 chunks.  One launch packs
 // two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid
@@ -95,9 +97,10 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
                                int32_t E, unsigned int *status, cudaStream_t s);
 
 // quant.cu
-cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float *scale,
+// quant.cu (fmt: FP8G_E4M3 or FP8G_E5M2)
+cudaError_t launch_quantize_tensor(const float *x, int64_t n, int fmt, uint8_t *q, float *scale,
                                    unsigned int *status, int num_sms, cudaStream_t s);
-cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, uint8_t *q,
-                                    float *scales, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, int fmt,
+                                    uint8_t *q, float *scales, int num_sms, cudaStream_t s);
 
 }  // namespace fp8g

@@ -1,15 +1,16 @@
-// Operand quantiser: fp32 -> E4M3 codes + fp32 scales (data preparation for
-// the GEMM entry points).
+// Operand quantiser: fp32 -> FP8 codes + fp32 scales (data preparation for
+// the GEMM entry points).  Formats: E4M3 (largest finite fmax = 448) and E5M2
+// (fmax = 57344), the two FP8 formats of the format paragraph of "Optimizing
+// FP8 GEMM kernels in JAX with Triton for Blackwell GPUs".
 //
-// Per-tensor: s = fl32(amax / 448) over the non-NaN |x| (1 if that is 0).
+// Per-tensor: s = fl32(amax / fmax) over the non-NaN |x| (1 if that is 0).
 // 1x32 block along the contiguous axis: s = the smallest power of two with
-// 448 s >= block amax, so every |x / s| <= 448 and the scale is exactly an
+// fmax s >= block amax, so every |x / s| <= fmax and the scale is exactly an
 // 8-bit exponent (UE8M0) — the microscaling form of the parameter paragraph of
-// "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell GPUs" and the
-// MXFP8 micro-scaling of the Triton tutorial ch. 12, 12.6.1; its "fine-grained
-// quantisation" advice against FP8 underflow is the reason for the block form.
-// q = E4M3(fl32(x / s)), round to nearest even, saturating (cvt ... satfinite),
-// NaN -> 0x7F.
+// the same page and the MXFP8 micro-scaling of the Triton tutorial ch. 12,
+// 12.6.1; its "fine-grained quantisation" advice against FP8 underflow is the
+// reason for the block form.  q = FP8(fl32(x / s)), round to nearest even,
+// saturating (cvt ... satfinite), NaN -> 0x7F (a NaN code in both formats).
 //
 // HBM-bound elementwise kernels: 16-byte loads, 8-byte stores, a grid of a
 // few CTAs per SM striding over the tensor.
@@ -19,10 +20,28 @@ namespace fp8g {
 
 namespace {
 
-// Two fp32 values -> two E4M3 bytes (lo at the lower address).
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+// FMT 0: E4M3, 1: E5M2.  Largest finite value 1.75 * 2^kEmax[FMT].
+template <int FMT>
+struct Fp8Fmt;
+template <>
+struct Fp8Fmt<0> {
+    static constexpr float kMax = 448.0f;
+    static constexpr int kEmax = 8;
+};
+template <>
+struct Fp8Fmt<1> {
+    static constexpr float kMax = 57344.0f;
+    static constexpr int kEmax = 15;
+};
+
+// Two fp32 values -> two FP8 bytes (lo at the lower address).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    if constexpr (FMT == 0)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     uint32_t v = r;
     if (isnan(lo)) v = (v & 0xFF00u) | 0x7Fu;
     if (isnan(hi)) v = (v & 0x00FFu) | 0x7F00u;
@@ -30,12 +49,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 // 8 values -> 8 codes packed little-endian.
+template <int FMT>
 __device__ __forceinline__ uint2 quant8(const float4 a, const float4 b, float s) {
     uint2 o;
-    o.x = e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
-          (e4m3x2(__fdiv_rn(a.z, s), __fdiv_rn(a.w, s)) << 16);
-    o.y = e4m3x2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) |
-          (e4m3x2(__fdiv_rn(b.z, s), __fdiv_rn(b.w, s)) << 16);
+    o.x = fp8x2<FMT>(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
+          (fp8x2<FMT>(__fdiv_rn(a.z, s), __fdiv_rn(a.w, s)) << 16);
+    o.y = fp8x2<FMT>(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) |
+          (fp8x2<FMT>(__fdiv_rn(b.z, s), __fdiv_rn(b.w, s)) << 16);
     return o;
 }
 
@@ -46,10 +66,11 @@ __device__ __forceinline__ float absmax8(const float4 a, const float4 b) {
     return m;
 }
 
-// Smallest power of two s with 448 s >= amax (amax >= 0, not NaN), as an
-// exponent clamped to [-126, 127].  With amax = m 2^E, 1 <= m < 2: 448 = 1.75 2^8,
-// so e = E - 8 when m <= 1.75 and E - 7 otherwise (m > 1.75 <=> mantissa field
-// above 0x600000).
+// Smallest power of two s with fmax s >= amax (amax >= 0, not NaN), as an
+// exponent clamped to [-126, 127].  With amax = m 2^E, 1 <= m < 2 and
+// fmax = 1.75 2^emax: e = E - emax when m <= 1.75 and E - emax + 1 otherwise
+// (m > 1.75 <=> mantissa field above 0x600000).
+template <int FMT>
 __device__ __forceinline__ float pow2_scale(float amax) {
     if (amax == 0.0f) return 1.0f;
     const uint32_t bits = __float_as_uint(amax);
@@ -61,7 +82,7 @@ __device__ __forceinline__ float pow2_scale(float amax) {
         if (ex == 0) {
             e = -126;
         } else {
-            e = (ex - 127) - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+            e = (ex - 127) - Fp8Fmt<FMT>::kEmax + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
         }
         e = max(-126, min(127, e));
     }
@@ -69,6 +90,7 @@ __device__ __forceinline__ float pow2_scale(float amax) {
 }
 
 // 1x32 blocks: 4 threads per block, 8 consecutive values per thread.
+template <int FMT>
 __global__ void quant_block32_kernel(const float *__restrict__ x, int64_t n8, uint8_t *__restrict__ q,
                                      float *__restrict__ scales) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -86,9 +108,9 @@ __global__ void quant_block32_kernel(const float *__restrict__ x, int64_t n8, ui
         float m = absmax8(a, b);
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const float s = pow2_scale(m);
+        const float s = pow2_scale<FMT>(m);
         if (active) {
-            reinterpret_cast<uint2 *>(q)[g] = quant8(a, b, s);
+            reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
             if ((g & 3) == 0) scales[g >> 2] = s;
         }
     }
@@ -110,42 +132,48 @@ __global__ void amax_kernel(const float *__restrict__ x, int64_t n, unsigned int
     if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
 }
 
+template <int FMT>
 __device__ __forceinline__ float tensor_scale(const float *amax_slot) {
     const float amax = *amax_slot;
-    float s = __fdiv_rn(amax, 448.0f);
+    float s = __fdiv_rn(amax, Fp8Fmt<FMT>::kMax);
     if (s == 0.0f) s = 1.0f;
     return s;
 }
 
 // x: n values, n % 8 == 0; the scale slot still holds amax.
+template <int FMT>
 __global__ void quant_tensor_kernel(const float *__restrict__ x, int64_t n8, uint8_t *__restrict__ q,
                                     const float *__restrict__ amax_slot) {
-    const float s = tensor_scale(amax_slot);
+    const float s = tensor_scale<FMT>(amax_slot);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += stride) {
         const float4 a = reinterpret_cast<const float4 *>(x)[2 * g];
         const float4 b = reinterpret_cast<const float4 *>(x)[2 * g + 1];
-        reinterpret_cast<uint2 *>(q)[g] = quant8(a, b, s);
+        reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
     }
 }
 
-__global__ void finish_scale_kernel(float *slot) { *slot = tensor_scale(slot); }
+template <int FMT>
+__global__ void finish_scale_kernel(float *slot) { *slot = tensor_scale<FMT>(slot); }
 
 }  // namespace
 
-cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, uint8_t *q,
-                                    float *scales, int num_sms, cudaStream_t s) {
+cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, int fmt,
+                                    uint8_t *q, float *scales, int num_sms, cudaStream_t s) {
     const int64_t n8 = rows * cols / 8;
     if (n8 == 0) return cudaSuccess;
     const int threads = 256;
     int64_t blocks = (n8 + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
-    quant_block32_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scales);
+    if (fmt == 1)
+        quant_block32_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scales);
+    else
+        quant_block32_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scales);
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float *scale,
+cudaError_t launch_quantize_tensor(const float *x, int64_t n, int fmt, uint8_t *q, float *scale,
                                    unsigned int *status, int num_sms, cudaStream_t s) {
     (void)status;
     cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), s);
@@ -161,10 +189,16 @@ cudaError_t launch_quantize_tensor(const float *x, int64_t n, uint8_t *q, float 
     if (n8 > 0) {
         blocks = (n8 + threads - 1) / threads;
         if (blocks > cap) blocks = cap;
-        quant_tensor_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scale);
+        if (fmt == 1)
+            quant_tensor_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scale);
+        else
+            quant_tensor_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scale);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    finish_scale_kernel<<<1, 1, 0, s>>>(scale);
+    if (fmt == 1)
+        finish_scale_kernel<1><<<1, 1, 0, s>>>(scale);
+    else
+        finish_scale_kernel<0><<<1, 1, 0, s>>>(scale);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,15 @@ typedef enum {
 
 typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
 
+/*
+ * FP8 operand formats [JAX-BW format paragraph: E4M3 for its range/precision
+ * balance, E5M2 the wider-range alternative].  E4M3 ("fn"): bias 7, 3
+ * mantissa bits, no infinities, NaN = S.1111.111, largest finite 448.  E5M2:
+ * bias 15, 2 mantissa bits, infinities and NaNs in the top binade, largest
+ * finite 57344.  The entry points without a format argument take E4M3.
+ */
+typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1 } fp8g_format;
+
 /* Largest expert count accepted by fp8_grouped_gemm. */
 #define FP8G_MAX_EXPERTS 64
 
@@ -188,6 +197,35 @@ FP8G_API fp8g_status fp8g_gemm_plan(int block, int64_t M, int64_t N, int64_t K, 
  */
 FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32_t block,
                                uint8_t *q, float *scales, cudaStream_t stream);
+
+/*
+ * fp8g_quantize_e4m3 with the output format `fmt` (fp8g_format): with
+ * FP8G_E5M2 the bound 448 becomes 57344 throughout (s = fl32(amax/57344), or
+ * the smallest power of two with 57344*s >= amax; saturation to +-57344;
+ * infinities saturate too; NaN -> 0x7F).  A bad `fmt` is FP8G_ERR_INVALID_ARG.
+ */
+FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block,
+                          int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
+
+/*
+ * The GEMM entry points with explicit operand formats (fp8g_format each for
+ * A and B, mixed allowed: the tensor core's kind::f8f6f4 and
+ * kind::mxf8f6f4 MMAs take either format per operand).  Everything else as
+ * fp8_gemm / fp8_gemm_blockscaled / fp8_grouped_gemm; a bad format is
+ * FP8G_ERR_INVALID_ARG.  Parity: the same tolerance as for E4M3.
+ */
+FP8G_API fp8g_status fp8_gemm_fmt(const void *A, const void *B, const float *scale_a,
+                         const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+FP8G_API fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
+                                     const float *sfb, void *C, int out, int32_t a_fmt,
+                                     int32_t b_fmt, int64_t M, int64_t N, int64_t K,
+                                     cudaStream_t stream);
+FP8G_API fp8g_status fp8_grouped_gemm_fmt(const void *A, const void *B, const float *sfa,
+                                 const float *sfb, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                                 const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                 int64_t total_rows, int32_t *offsets_out, int32_t *tile_map_out,
+                                 cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
