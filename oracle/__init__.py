@@ -43,6 +43,9 @@ OUT_BF16 = 0
 OUT_F32 = 1
 E4M3 = 0
 E5M2 = 1
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_GELU = 2
 
 
 def build(force: bool = False) -> str:
@@ -81,6 +84,14 @@ def _L():
             lib.oracle_pow2_scale_fmt.restype = ctypes.c_float
             lib.oracle_pow2_scale_fmt.argtypes = [ctypes.c_float, ctypes.c_int]
             lib.oracle_quantize_block32_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
+            lib.oracle_act.restype = ctypes.c_double
+            lib.oracle_act.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.oracle_gemm_ex.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                           ctypes.c_int, i64, i64, i64, ctypes.c_int, P, P, P,
+                                           ctypes.c_int]
+            lib.oracle_gemm_sample_ex.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, P, ctypes.c_int, i64, i64, i64,
+                                                  ctypes.c_int, P, P, i64, P, P, P, ctypes.c_int]
             lib.oracle_gemm_fmt.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             i64, i64, i64, ctypes.c_int, P, P, P, ctypes.c_int]
             lib.oracle_gemm_sample_fmt.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int,
@@ -185,9 +196,14 @@ def quantize_block32(x: np.ndarray, fmt: int = E4M3):
 
 
 # --------------------------------------------------------------------- GEMM
+def act(y: float, kind: int) -> float:
+    """The fused epilogue's activation in fp64 (ACT_NONE, ACT_RELU, ACT_GELU)."""
+    return float(_L().oracle_act(float(y), int(kind)))
+
+
 def gemm(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray, block: bool,
          out_kind: int = OUT_BF16, want_exact: bool = False, threads=None, a_fmt: int = E4M3,
-         b_fmt: int = E4M3):
+         b_fmt: int = E4M3, bias=None, act_kind: int = ACT_NONE):
     """C = (sA A)(sB B)^T.  Returns (C_rounded float32 [M,N], bound float64 [M,N], exact|None)."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -203,14 +219,18 @@ def gemm(A: np.ndarray, B: np.ndarray, sfa: np.ndarray, sfb: np.ndarray, block: 
     C = np.empty((M, N), dtype=np.float32)
     bound = np.empty((M, N), dtype=np.float64)
     exact = np.empty((M, N), dtype=np.float64) if want_exact else None
-    _L().oracle_gemm_fmt(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt),
-                         int(b_fmt), M, N, K, int(out_kind), _p(C),
-                         _p(exact) if exact is not None else None, _p(bound), _threads(threads))
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        assert bias.shape == (N,)
+    _L().oracle_gemm_ex(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt), int(b_fmt),
+                        _p(bias) if bias is not None else None, int(act_kind), M, N, K,
+                        int(out_kind), _p(C), _p(exact) if exact is not None else None,
+                        _p(bound), _threads(threads))
     return C, bound, exact
 
 
 def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, threads=None,
-                a_fmt: int = E4M3, b_fmt: int = E4M3):
+                a_fmt: int = E4M3, b_fmt: int = E4M3, bias=None, act_kind: int = ACT_NONE):
     """Only the elements (pi[s], pj[s]).  Returns (C float32 [n], bound float64 [n], exact [n])."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -224,9 +244,13 @@ def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, t
     C = np.empty(n, dtype=np.float32)
     bound = np.empty(n, dtype=np.float64)
     exact = np.empty(n, dtype=np.float64)
-    _L().oracle_gemm_sample_fmt(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt),
-                                int(b_fmt), M, N, K, int(out_kind), _p(pi), _p(pj), n, _p(C),
-                                _p(exact), _p(bound), _threads(threads))
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        assert bias.shape == (N,)
+    _L().oracle_gemm_sample_ex(_p(A), _p(B), _p(sfa), _p(sfb), int(bool(block)), int(a_fmt),
+                               int(b_fmt), _p(bias) if bias is not None else None, int(act_kind),
+                               M, N, K, int(out_kind), _p(pi), _p(pj), n, _p(C), _p(exact),
+                               _p(bound), _threads(threads))
     return C, bound, exact
 
 

@@ -30,6 +30,9 @@
  *     multiply B[e] (MoE paragraph of the JAX/Blackwell page).
  *   - The grouped raster order of output tiles ("GROUP_M" swizzle of the
  *     persistent matmul in the Triton tutorial ch. 12, section 12.7).
+ *   - A fused epilogue after the GEMM value v: act(v + bias[j]) with act none,
+ *     ReLU or GELU (the bias_add_relu case in the benchmark list of the Triton
+ *     FP8 benchmarking page; GELU in its erf form x * Phi(x)), in fp64.
  *
  * All arithmetic is fp64.  Per-block inner sums are exact for E4M3: each
  * product of two E4M3 values is an integer multiple of 2^-18 with magnitude
@@ -307,6 +310,15 @@ static void *quant_block32_rows(void *arg) {
 /* ------------------------------------------------------------------ */
 
 enum { ORACLE_OUT_BF16 = 0, ORACLE_OUT_F32 = 1 };
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2 };
+
+/* Activation in fp64.  ReLU: y < 0 ? 0 : y (NaN stays NaN).  GELU:
+ * y * Phi(y) = 0.5 y (1 + erf(y / sqrt 2)). */
+ORACLE_EXPORT double oracle_act(double y, int act) {
+    if (act == ORACLE_ACT_RELU) return y < 0.0 ? 0.0 : y;
+    if (act == ORACLE_ACT_GELU) return 0.5 * y * (1.0 + erf(y / sqrt(2.0)));
+    return y;
+}
 
 typedef struct {
     const uint8_t *A, *B;
@@ -321,6 +333,8 @@ typedef struct {
     int64_t row_begin, row_end;
     const int64_t *pi, *pj; /* sampled mode: element list (nullable) */
     int64_t n_samples;
+    const float *bias;      /* fused epilogue: [N] (nullable) */
+    int act;
 } gemm_job;
 
 static double dec_e4m3[256], dec_e5m2[256];
@@ -371,10 +385,19 @@ static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, dou
         v = (double)(float)((double)alpha * acc);
         absum = fabs((double)g->sfa[0] * (double)g->sfb[0]) * aacc;
     }
+    double lip = 1.0, extra = 0.0;
+    if (g->bias != NULL || g->act != ORACLE_ACT_NONE) {
+        /* epilogue: y = act(v + bias[j]); |GELU'| <= 1.13; the GPU adds the
+         * bias and evaluates the activation in fp32 (2^-20 relative covers it) */
+        double b = g->bias != NULL ? (double)g->bias[j] : 0.0;
+        extra = ldexp(fabs(v) + fabs(b), -20);
+        v = oracle_act(v + b, g->act);
+        if (g->act == ORACLE_ACT_GELU) lip = 1.13;
+    }
     float r = (g->out_kind == ORACLE_OUT_BF16) ? oracle_bf16_round(v) : (float)v;
     *out = r;
     if (exact) *exact = v;
-    if (bound) *bound = ldexp(absum, -8) + oracle_bf16_ulp((double)r);
+    if (bound) *bound = lip * ldexp(absum, -8) + extra + oracle_bf16_ulp((double)r);
 }
 
 static void *gemm_worker(void *arg) {
@@ -421,6 +444,22 @@ static void run_jobs(gemm_job proto, int64_t n_items, int threads) {
 /* Full GEMM.  block = 0: sfa, sfb each point to one fp32 per-tensor scale.
  * block = 1: sfa [M, K/32], sfb [N, K/32].  a_fmt, b_fmt: ORACLE_E4M3 or
  * ORACLE_E5M2.  C, exact, bound: [M, N]. */
+/* GEMM with operand formats and the fused epilogue (bias [N] nullable, act). */
+ORACLE_EXPORT void oracle_gemm_ex(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                  const float *sfb, int block, int a_fmt, int b_fmt,
+                                  const float *bias, int act, int64_t M, int64_t N, int64_t K,
+                                  int out_kind, float *C, double *exact, double *bound,
+                                  int threads) {
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.ta = table_of(a_fmt); g.tb = table_of(b_fmt);
+    g.bias = bias; g.act = act;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    run_jobs(g, M, threads);
+}
+
 ORACLE_EXPORT void oracle_gemm_fmt(const uint8_t *A, const uint8_t *B, const float *sfa,
                                    const float *sfb, int block, int a_fmt, int b_fmt, int64_t M,
                                    int64_t N, int64_t K, int out_kind, float *C, double *exact,
@@ -443,6 +482,23 @@ ORACLE_EXPORT void oracle_gemm(const uint8_t *A, const uint8_t *B, const float *
 }
 
 /* Sampled GEMM: only the n elements (pi[s], pj[s]). Outputs are length n. */
+ORACLE_EXPORT void oracle_gemm_sample_ex(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                         const float *sfb, int block, int a_fmt, int b_fmt,
+                                         const float *bias, int act, int64_t M, int64_t N,
+                                         int64_t K, int out_kind, const int64_t *pi,
+                                         const int64_t *pj, int64_t n, float *C, double *exact,
+                                         double *bound, int threads) {
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = block;
+    g.ta = table_of(a_fmt); g.tb = table_of(b_fmt);
+    g.bias = bias; g.act = act;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    g.pi = pi; g.pj = pj; g.n_samples = n;
+    run_jobs(g, n, threads);
+}
+
 ORACLE_EXPORT void oracle_gemm_sample_fmt(const uint8_t *A, const uint8_t *B, const float *sfa,
                                           const float *sfb, int block, int a_fmt, int b_fmt,
                                           int64_t M, int64_t N, int64_t K, int out_kind,
