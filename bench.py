@@ -40,6 +40,8 @@ WORKLOADS = {
     "moe": dict(kind="grouped", M=32768, N=14336, K=4096, seed=4),
     "square1024": dict(kind="tensor", M=1024, N=1024, K=1024, seed=1),
     "tensor8192": dict(kind="tensor", M=8192, N=8192, K=8192, seed=3),
+    # E4M3 activations x E5M2 weights, block-scaled (the mixed-format path)
+    "mixed8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, b_fmt=1),
 }
 METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
 
@@ -139,8 +141,8 @@ def make_inputs(wl: dict, device):
     else:
         w = synth.large_block(wl["M"], seed=wl["seed"])
         bs = 32
-    qa, sa = fp8g.quantize(w.A.to(device), bs)
-    qb, sb = fp8g.quantize(w.B.to(device), bs)
+    qa, sa = fp8g.quantize(w.A.to(device), bs, fmt=wl.get("a_fmt", 0))
+    qb, sb = fp8g.quantize(w.B.to(device), bs, fmt=wl.get("b_fmt", 0))
     return w, dict(qa=qa, sa=sa, qb=qb, sb=sb)
 
 
@@ -162,6 +164,10 @@ def run_once(fp8g, wl, w, t, C, stream):
                               t["qa"].shape[0], None, None, stream)
     elif wl["kind"] == "tensor":
         fp8g.fp8_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"], wl["K"], stream)
+    elif "a_fmt" in wl or "b_fmt" in wl:
+        fp8g.fp8_gemm_blockscaled_fmt(t["qa"], t["qb"], t["sa"], t["sb"], C, out,
+                                      wl.get("a_fmt", 0), wl.get("b_fmt", 0), wl["M"], wl["N"],
+                                      wl["K"], stream)
     else:
         fp8g.fp8_gemm_blockscaled(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"],
                                   wl["K"], stream)
@@ -198,9 +204,10 @@ def oracle_inputs(wl, w):
                     N=N, K=K, desc=f"rows of expert {e} (all {N} columns)")
     block = wl["kind"] != "tensor"
     qfn = oracle.quantize_block32 if block else oracle.quantize_tensor
-    qa, sa = qfn(w.A.numpy())
-    qb, sb = qfn(w.B.numpy())
+    qa, sa = qfn(w.A.numpy(), wl.get("a_fmt", 0))
+    qb, sb = qfn(w.B.numpy(), wl.get("b_fmt", 0))
     return dict(A=qa, sa=sa, B=qb, sb=sb, block=block, N=wl["N"], K=wl["K"],
+                a_fmt=wl.get("a_fmt", 0), b_fmt=wl.get("b_fmt", 0),
                 desc=f"rows of A (all {wl['N']} columns)")
 
 
@@ -218,7 +225,8 @@ def cpu_baseline(oi: dict, budget_s: float = 12.0):
         a = np.ascontiguousarray(oi["A"][:r])
         s = np.ascontiguousarray(oi["sa"][:r]) if block else oi["sa"]
         t0 = time.perf_counter()
-        oracle.gemm(a, oi["B"], s, oi["sb"], block, oracle.OUT_BF16, threads=threads)
+        oracle.gemm(a, oi["B"], s, oi["sb"], block, oracle.OUT_BF16, threads=threads,
+                    a_fmt=oi.get("a_fmt", 0), b_fmt=oi.get("b_fmt", 0))
         dt = time.perf_counter() - t0
         spent += dt
         flops = 2.0 * r * N * K
@@ -358,9 +366,12 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 accumulate",
+        "dtype": (["e4m3", "e5m2"][wl.get("a_fmt", 0)] + " x " + ["e4m3", "e5m2"][wl.get("b_fmt", 0)]
+                  + " -> f32 accumulate"),
         "data": "synthetic (seeded CPU generators, quantised on the GPU)",
         "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"],
+                   "formats": ["e4m3", "e5m2"][wl.get("a_fmt", 0)] + " x " +
+                              ["e4m3", "e5m2"][wl.get("b_fmt", 0)],
                    "scales": {"block": "1x32 along K, power of two",
                               "grouped": "1x32 along K, power of two",
                               "tensor": "per tensor"}[wl["kind"]],

@@ -31,13 +31,17 @@ FP8G_OUT_BF16 = 0
 FP8G_OUT_F32 = 1
 FP8G_E4M3 = 0
 FP8G_E5M2 = 1
+FP8G_ACT_NONE = 0
+FP8G_ACT_RELU = 1
+FP8G_ACT_GELU = 2
 FP8G_MAX_EXPERTS = 64
 
 # Every symbol include/fp8gemm.h declares.
 EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
-    "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_status", "fp8g_status_string",
+    "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
+    "fp8_grouped_gemm_ex", "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
 
@@ -93,6 +97,15 @@ def load():
         lib.fp8_gemm_blockscaled_fmt.restype = st
         lib.fp8_gemm_blockscaled_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, i64, i64,
                                                  i64, P]
+        lib.fp8_gemm_ex.restype = st
+        lib.fp8_gemm_ex.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, i64, i64, i64,
+                                    P]
+        lib.fp8_gemm_blockscaled_ex.restype = st
+        lib.fp8_gemm_blockscaled_ex.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, i64,
+                                                i64, i64, P]
+        lib.fp8_grouped_gemm_ex.restype = st
+        lib.fp8_grouped_gemm_ex.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, P, i32,
+                                            i64, i64, i64, P, P, P]
         lib.fp8_grouped_gemm_fmt.restype = st
         lib.fp8_grouped_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, i64,
                                              i64, i64, P, P, P]
@@ -207,6 +220,29 @@ def fp8_grouped_gemm_fmt(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, co
                                        int(a_fmt), int(b_fmt), _ptr(counts), E, N, K, total_rows,
                                        _ptr(offsets_out), _ptr(tile_map_out), _stream(stream)),
            "fp8_grouped_gemm_fmt")
+
+
+def fp8_gemm_ex(A, B, scale_a, scale_b, C, out: int, a_fmt: int, b_fmt: int, bias, act: int,
+                M: int, N: int, K: int, stream=None):
+    _check(load().fp8_gemm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), _ptr(C), int(out),
+                              int(a_fmt), int(b_fmt), _ptr(bias), int(act), M, N, K,
+                              _stream(stream)), "fp8_gemm_ex")
+
+
+def fp8_gemm_blockscaled_ex(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bias, act: int,
+                            M: int, N: int, K: int, stream=None):
+    _check(load().fp8_gemm_blockscaled_ex(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C),
+                                          int(out), int(a_fmt), int(b_fmt), _ptr(bias), int(act),
+                                          M, N, K, _stream(stream)), "fp8_gemm_blockscaled_ex")
+
+
+def fp8_grouped_gemm_ex(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bias, act: int,
+                        counts, E: int, N: int, K: int, total_rows: int, offsets_out=None,
+                        tile_map_out=None, stream=None):
+    _check(load().fp8_grouped_gemm_ex(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C), int(out),
+                                      int(a_fmt), int(b_fmt), _ptr(bias), int(act), _ptr(counts),
+                                      E, N, K, total_rows, _ptr(offsets_out), _ptr(tile_map_out),
+                                      _stream(stream)), "fp8_grouped_gemm_ex")
 
 
 def fp8_gemm_status(stream=None):

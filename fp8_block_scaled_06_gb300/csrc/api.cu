@@ -206,9 +206,13 @@ fp8g_status check_common(const void *A, const void *B, const void *C, int out, i
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
-                     void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt) {
+                     void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt,
+                     const float *bias, int act) {
     if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
         return FP8G_ERR_INVALID_ARG;
+    if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
+        return FP8G_ERR_INVALID_ARG;
+    if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
     DevInfo di;
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
@@ -234,6 +238,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.status = di.status;
     p.timeout_ns = timeout_ns();
     p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
+    p.bias = bias;
+    p.act = act;
 
     GemmMaps maps;
     const int64_t rows_a = M > 0 ? M : 1;  // grouped with zero rows: A is never read
@@ -317,15 +323,23 @@ using namespace fp8g;
 
 extern "C" {
 
-fp8g_status fp8_gemm_fmt(const void *A, const void *B, const float *scale_a,
-                         const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
-                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+fp8g_status fp8_gemm_ex(const void *A, const void *B, const float *scale_a,
+                        const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                        const float *bias, int32_t act, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream) {
     fp8g_status st = check_common(A, B, C, out, M, N, K);
     if (st != FP8G_OK) return st;
     if (scale_a == nullptr || scale_b == nullptr) return FP8G_ERR_INVALID_ARG;
     if (!aligned(scale_a, 4) || !aligned(scale_b, 4)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeTensor, A, B, scale_a, scale_b, C, out, M, N, K, nullptr, 0, nullptr,
-                    nullptr, stream, nullptr, 0, a_fmt, b_fmt);
+                    nullptr, stream, nullptr, 0, a_fmt, b_fmt, bias, act);
+}
+
+fp8g_status fp8_gemm_fmt(const void *A, const void *B, const float *scale_a,
+                         const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return fp8_gemm_ex(A, B, scale_a, scale_b, C, out, a_fmt, b_fmt, nullptr, FP8G_ACT_NONE, M, N,
+                       K, stream);
 }
 
 fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -333,17 +347,25 @@ fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a, const f
     return fp8_gemm_fmt(A, B, scale_a, scale_b, C, out, FP8G_E4M3, FP8G_E4M3, M, N, K, stream);
 }
 
-fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
-                                     const float *sfb, void *C, int out, int32_t a_fmt,
-                                     int32_t b_fmt, int64_t M, int64_t N, int64_t K,
-                                     cudaStream_t stream) {
+fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const float *sfa,
+                                    const float *sfb, void *C, int out, int32_t a_fmt,
+                                    int32_t b_fmt, const float *bias, int32_t act, int64_t M,
+                                    int64_t N, int64_t K, cudaStream_t stream) {
     fp8g_status st = check_common(A, B, C, out, M, N, K);
     if (st != FP8G_OK) return st;
     if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
     if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
-                    stream, nullptr, 0, a_fmt, b_fmt);
+                    stream, nullptr, 0, a_fmt, b_fmt, bias, act);
+}
+
+fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
+                                     const float *sfb, void *C, int out, int32_t a_fmt,
+                                     int32_t b_fmt, int64_t M, int64_t N, int64_t K,
+                                     cudaStream_t stream) {
+    return fp8_gemm_blockscaled_ex(A, B, sfa, sfb, C, out, a_fmt, b_fmt, nullptr, FP8G_ACT_NONE,
+                                   M, N, K, stream);
 }
 
 fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
@@ -366,6 +388,15 @@ fp8g_status fp8_grouped_gemm_fmt(const void *A, const void *B, const float *sfa,
                                  const int32_t *counts, int32_t E, int64_t N, int64_t K,
                                  int64_t total_rows, int32_t *offsets_out, int32_t *tile_map_out,
                                  cudaStream_t stream) {
+    return fp8_grouped_gemm_ex(A, B, sfa, sfb, C, out, a_fmt, b_fmt, nullptr, FP8G_ACT_NONE,
+                               counts, E, N, K, total_rows, offsets_out, tile_map_out, stream);
+}
+
+fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const float *sfa,
+                                const float *sfb, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                                const float *bias, int32_t act, const int32_t *counts, int32_t E,
+                                int64_t N, int64_t K, int64_t total_rows, int32_t *offsets_out,
+                                int32_t *tile_map_out, cudaStream_t stream) {
     if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
     if (E < 1) return FP8G_ERR_INVALID_ARG;
     if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
@@ -385,7 +416,7 @@ fp8g_status fp8_grouped_gemm_fmt(const void *A, const void *B, const float *sfa,
     if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
     if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
-                    offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt);
+                    offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt, bias, act);
 }
 
 fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,

@@ -468,6 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t row = (int64_t)ti.row0 + q * 32 + lane;
             if (row < ti.row_end) {
                 const int64_t ncol0 = (int64_t)ti.n0 + col0;
+                float a_t = alpha;  // scale left for the stores below
+                if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
+                    const float *brow = p.bias != nullptr ? p.bias + (int64_t)ti.e * p.N : nullptr;
+#pragma unroll
+                    for (int c = 0; c < C_::CW / 32; ++c)
+                        epi32(r[c], alpha, brow, p.act, ncol0 + c * 32, p.N);
+                    a_t = 1.0f;
+                }
                 if constexpr (OUT_F32) {
                     float *out = reinterpret_cast<float *>(p.C) + row * p.N + ncol0;
 #pragma unroll
@@ -476,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int v = 0; v < 8; ++v) {
                             if (ncol0 + c * 32 + v * 4 < p.N) {
                                 float4 o;
-                                o.x = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 0]));
-                                o.y = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 1]));
-                                o.z = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 2]));
-                                o.w = __fmul_rn(alpha, __uint_as_float(r[c][4 * v + 3]));
+                                o.x = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 0]));
+                                o.y = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 1]));
+                                o.z = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 2]));
+                                o.w = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 3]));
                                 *reinterpret_cast<float4 *>(out + c * 32 + v * 4) = o;
                             }
                         }
@@ -494,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int h = 0; h < 4; ++h) {
                                     const float lo =
-                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h]));
+                                        __fmul_rn(a_t, __uint_as_float(r[c][8 * v + 2 * h]));
                                     const float hi =
-                                        __fmul_rn(alpha, __uint_as_float(r[c][8 * v + 2 * h + 1]));
+                                        __fmul_rn(a_t, __uint_as_float(r[c][8 * v + 2 * h + 1]));
                                     __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
                                     pk[h] = *reinterpret_cast<uint32_t *>(&b2);
                                 }
@@ -595,16 +603,25 @@ roles_done:
                 const int64_t grow = (int64_t)ti.row0 + row;
                 const int64_t gcol = (int64_t)ti.n0 + col;
                 if (grow < ti.row_end && gcol < p.N) {
+                    float a_t = alpha;
+                    if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
+                        // N % 4 == 0 for the outputs (16-byte rows), so all four are in range
+                        acc.x = epi1(__fmul_rn(alpha, acc.x), p.bias, p.act, gcol);
+                        acc.y = epi1(__fmul_rn(alpha, acc.y), p.bias, p.act, gcol + 1);
+                        acc.z = epi1(__fmul_rn(alpha, acc.z), p.bias, p.act, gcol + 2);
+                        acc.w = epi1(__fmul_rn(alpha, acc.w), p.bias, p.act, gcol + 3);
+                        a_t = 1.0f;
+                    }
                     if constexpr (OUT_F32) {
-                        float4 o = make_float4(__fmul_rn(alpha, acc.x), __fmul_rn(alpha, acc.y),
-                                               __fmul_rn(alpha, acc.z), __fmul_rn(alpha, acc.w));
+                        float4 o = make_float4(__fmul_rn(a_t, acc.x), __fmul_rn(a_t, acc.y),
+                                               __fmul_rn(a_t, acc.z), __fmul_rn(a_t, acc.w));
                         *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + grow * p.N +
                                                     gcol) = o;
                     } else {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(alpha, acc.x),
-                                                                  __fmul_rn(alpha, acc.y));
-                        __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(alpha, acc.z),
-                                                                  __fmul_rn(alpha, acc.w));
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(a_t, acc.x),
+                                                                  __fmul_rn(a_t, acc.y));
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(a_t, acc.z),
+                                                                  __fmul_rn(a_t, acc.w));
                         *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) +
                                                    grow * p.N + gcol) =
                             make_uint2(*reinterpret_cast<uint32_t *>(&lo),

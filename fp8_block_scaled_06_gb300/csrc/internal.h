@@ -42,6 +42,8 @@ struct GemmParams {
     const uint8_t *sfb_pk;
     int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
     uint32_t ab_fmt;       // operand formats as MMA instruction-descriptor bits (A: 7-9, B: 10-12)
+    const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
+    int32_t act;           // fused epilogue activation: FP8G_ACT_*
 };
 
 // TMA descriptors of one launch: E4M3 operands and, for block-scaled CTA
@@ -78,7 +80,8 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
-                     void *scratch, size_t scratch_bytes, int a_fmt = 0, int b_fmt = 0);
+                     void *scratch, size_t scratch_bytes, int a_fmt = 0, int b_fmt = 0,
+                     const float *bias = nullptr, int act = 0);
 
 // scales.cu: fp32 1x32 scales -> packed UE8M0 chunks.  One launch packs
 // two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid

@@ -93,6 +93,31 @@ __device__ __forceinline__ bool wait_bar_landed_warp(uint32_t bar, uint32_t pari
     return ok != 0;
 }
 
+// Fused epilogue on one output value of column `col`:
+//   v = act(fl32(v + bias[col]))   (bias row may be null; act FP8G_ACT_*)
+// applied after the per-tensor scale and before the output rounding.  ReLU
+// keeps NaN (v < 0 ? 0 : v); GELU is the erf form 0.5 v (1 + erf(v / sqrt 2)).
+__device__ __forceinline__ float epi1(float v, const float *brow, int act, int64_t col) {
+    if (brow != nullptr) v = __fadd_rn(v, __ldg(brow + col));
+    if (act == FP8G_ACT_RELU) {
+        v = v < 0.0f ? 0.0f : v;
+    } else if (act == FP8G_ACT_GELU) {
+        v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    }
+    return v;
+}
+
+// The fused epilogue in place on 32 consecutive accumulator columns
+// [col0, col0 + 32) held as fp32 bit patterns (columns >= N are skipped; they
+// are never stored): r = act(fl32(fl32(alpha * r) + bias)).
+__device__ __forceinline__ void epi32(uint32_t (&r)[32], float alpha, const float *brow, int act,
+                                      int64_t col0, int64_t N) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (col0 + i < N)
+            r[i] = __float_as_uint(epi1(__fmul_rn(alpha, __uint_as_float(r[i])), brow, act, col0 + i));
+}
+
 // Grouped GEMM problem list, computed by every CTA from the device counts:
 // row_off[e] = first row of expert e (exclusive prefix of counts), tile_off[e]
 // = first output tile of expert e (experts in index order, ceil(M_e/bm) *

@@ -87,6 +87,15 @@ typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
  */
 typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1 } fp8g_format;
 
+/*
+ * Fused-epilogue activations [TRITON-FP8 benchmark list: a bias_add_relu
+ * epilogue beside the plain GEMM].  Applied per output element after the
+ * per-tensor scale and an optional per-column bias, before the output
+ * rounding:  out( act( fl32( fl32(alpha * acc) + bias[j] ) ) ).
+ * RELU: v < 0 ? 0 : v (NaN stays NaN).  GELU: 0.5 v (1 + erf(v / sqrt 2)).
+ */
+typedef enum { FP8G_ACT_NONE = 0, FP8G_ACT_RELU = 1, FP8G_ACT_GELU = 2 } fp8g_act;
+
 /* Largest expert count accepted by fp8_grouped_gemm. */
 #define FP8G_MAX_EXPERTS 64
 
@@ -226,6 +235,30 @@ FP8G_API fp8g_status fp8_grouped_gemm_fmt(const void *A, const void *B, const fl
                                  const int32_t *counts, int32_t E, int64_t N, int64_t K,
                                  int64_t total_rows, int32_t *offsets_out, int32_t *tile_map_out,
                                  cudaStream_t stream);
+
+/*
+ * The GEMM entry points with operand formats and a fused epilogue: `bias`
+ * (nullable) is a device fp32 [N] (grouped: [E, N], expert e's row for its
+ * rows of C), 4-byte aligned; `act` is an fp8g_act.  out = out(act(fl32(v +
+ * bias[j]))) with v the value the plain entry point would round.  Parity:
+ * |C - ref| <= L (2^-8 sum_k |sA a||sB b|) + 2^-20 (|v| + |bias|) + 1 bf16
+ * ulp(|ref|), L = 1 (none, ReLU) or 1.13 (GELU, the bound of |GELU'|); the
+ * 2^-20 term covers the fp32 bias add and activation.  Bad `act` or
+ * formats: FP8G_ERR_INVALID_ARG.
+ */
+FP8G_API fp8g_status fp8_gemm_ex(const void *A, const void *B, const float *scale_a,
+                        const float *scale_b, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                        const float *bias, int32_t act, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream);
+FP8G_API fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const float *sfa,
+                                    const float *sfb, void *C, int out, int32_t a_fmt,
+                                    int32_t b_fmt, const float *bias, int32_t act, int64_t M,
+                                    int64_t N, int64_t K, cudaStream_t stream);
+FP8G_API fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const float *sfa,
+                                const float *sfb, void *C, int out, int32_t a_fmt, int32_t b_fmt,
+                                const float *bias, int32_t act, const int32_t *counts, int32_t E,
+                                int64_t N, int64_t K, int64_t total_rows, int32_t *offsets_out,
+                                int32_t *tile_map_out, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
