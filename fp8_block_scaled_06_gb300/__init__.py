@@ -31,6 +31,8 @@ FP8G_OUT_BF16 = 0
 FP8G_OUT_F32 = 1
 FP8G_E4M3 = 0
 FP8G_E5M2 = 1
+FP8G_IN_F32 = 0
+FP8G_IN_BF16 = 1
 FP8G_ACT_NONE = 0
 FP8G_ACT_RELU = 1
 FP8G_ACT_GELU = 2
@@ -41,7 +43,7 @@ EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
-    "fp8_grouped_gemm_ex", "fp8_gemm_status", "fp8g_status_string",
+    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
 
@@ -106,6 +108,11 @@ def load():
         lib.fp8_grouped_gemm_ex.restype = st
         lib.fp8_grouped_gemm_ex.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, P, i32,
                                             i64, i64, i64, P, P, P]
+        lib.fp8_grouped_gemm_scatter.restype = st
+        lib.fp8_grouped_gemm_scatter.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, P,
+                                                 i32, i64, i64, i64, P, i64, P, P, P]
+        lib.fp8g_quantize_rows.restype = st
+        lib.fp8g_quantize_rows.argtypes = [P, i32, i64, i64, P, i64, i32, i32, P, P, P]
         lib.fp8_grouped_gemm_fmt.restype = st
         lib.fp8_grouped_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, i64,
                                              i64, i64, P, P, P]
@@ -243,6 +250,23 @@ def fp8_grouped_gemm_ex(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bia
                                       int(a_fmt), int(b_fmt), _ptr(bias), int(act), _ptr(counts),
                                       E, N, K, total_rows, _ptr(offsets_out), _ptr(tile_map_out),
                                       _stream(stream)), "fp8_grouped_gemm_ex")
+
+
+def fp8_grouped_gemm_scatter(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bias,
+                             act: int, counts, E: int, N: int, K: int, total_rows: int, c_row_of,
+                             c_rows: int, offsets_out=None, tile_map_out=None, stream=None):
+    _check(load().fp8_grouped_gemm_scatter(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C),
+                                           int(out), int(a_fmt), int(b_fmt), _ptr(bias), int(act),
+                                           _ptr(counts), E, N, K, total_rows, _ptr(c_row_of),
+                                           c_rows, _ptr(offsets_out), _ptr(tile_map_out),
+                                           _stream(stream)), "fp8_grouped_gemm_scatter")
+
+
+def fp8g_quantize_rows(x, in_dtype: int, x_rows: int, cols: int, rows, n_rows: int, block: int,
+                       fmt: int, q, scales, stream=None):
+    _check(load().fp8g_quantize_rows(_ptr(x), int(in_dtype), x_rows, cols, _ptr(rows), n_rows,
+                                     int(block), int(fmt), _ptr(q), _ptr(scales),
+                                     _stream(stream)), "fp8g_quantize_rows")
 
 
 def fp8_gemm_status(stream=None):

@@ -207,7 +207,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt,
-                     const float *bias, int act) {
+                     const float *bias, int act, const int32_t *c_row_of, int64_t c_rows) {
     if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
         return FP8G_ERR_INVALID_ARG;
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
@@ -240,6 +240,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
     p.bias = bias;
     p.act = act;
+    p.c_row_of = c_row_of;
+    p.c_rows = c_rows;
 
     GemmMaps maps;
     const int64_t rows_a = M > 0 ? M : 1;  // grouped with zero rows: A is never read
@@ -397,6 +399,20 @@ fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const float *sfa,
                                 const float *bias, int32_t act, const int32_t *counts, int32_t E,
                                 int64_t N, int64_t K, int64_t total_rows, int32_t *offsets_out,
                                 int32_t *tile_map_out, cudaStream_t stream) {
+    return fp8_grouped_gemm_scatter(A, B, sfa, sfb, C, out, a_fmt, b_fmt, bias, act, counts, E, N,
+                                    K, total_rows, nullptr, total_rows, offsets_out, tile_map_out,
+                                    stream);
+}
+
+fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, const float *sfa,
+                                     const float *sfb, void *C, int out, int32_t a_fmt,
+                                     int32_t b_fmt, const float *bias, int32_t act,
+                                     const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                     int64_t total_rows, const int32_t *c_row_of, int64_t c_rows,
+                                     int32_t *offsets_out, int32_t *tile_map_out,
+                                     cudaStream_t stream) {
+    if (c_row_of != nullptr && (!aligned(c_row_of, 4) || c_rows < 1)) return FP8G_ERR_INVALID_ARG;
+    if (c_row_of != nullptr && c_rows >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
     if (E < 1) return FP8G_ERR_INVALID_ARG;
     if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
@@ -416,7 +432,8 @@ fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const float *sfa,
     if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
     if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
-                    offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt, bias, act);
+                    offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt, bias, act,
+                    c_row_of, c_row_of != nullptr ? c_rows : total_rows);
 }
 
 fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
@@ -456,21 +473,32 @@ fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t cols, int32
 
 fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block, int32_t fmt,
                           uint8_t *q, float *scales, cudaStream_t stream) {
+    return fp8g_quantize_rows(x, FP8G_IN_F32, rows, cols, nullptr, rows, block, fmt, q, scales,
+                              stream);
+}
+
+fp8g_status fp8g_quantize_rows(const void *x, int32_t in_dtype, int64_t x_rows, int64_t cols,
+                               const int32_t *rows, int64_t n_rows, int32_t block, int32_t fmt,
+                               uint8_t *q, float *scales, cudaStream_t stream) {
     if (x == nullptr || q == nullptr || scales == nullptr) return FP8G_ERR_INVALID_ARG;
     if (fmt != FP8G_E4M3 && fmt != FP8G_E5M2) return FP8G_ERR_INVALID_ARG;
-    if (rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
+    if (in_dtype != FP8G_IN_F32 && in_dtype != FP8G_IN_BF16) return FP8G_ERR_INVALID_ARG;
+    if (x_rows < 1 || n_rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
+    if (rows == nullptr && n_rows > x_rows) return FP8G_ERR_INVALID_ARG;
+    if (rows != nullptr && !aligned(rows, 4)) return FP8G_ERR_ALIGNMENT;
     if (block != 0 && block != 32) return FP8G_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4)) return FP8G_ERR_ALIGNMENT;
     if (block == 32 && cols % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (block == 0 && cols % 8 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (rows >= ((int64_t)1 << 40) / cols) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (cols % 8 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (x_rows >= ((int64_t)1 << 40) / cols || n_rows >= ((int64_t)1 << 40) / cols ||
+        x_rows > INT32_MAX)
+        return FP8G_ERR_UNSUPPORTED_SHAPE;
     DevInfo di;
     fp8g_status st = device_info(di);
     if (st != FP8G_OK) return st;
-    const cudaError_t e =
-        block == 32 ? launch_quantize_block32(x, rows, cols, fmt, q, scales, di.num_sms, stream)
-                    : launch_quantize_tensor(x, rows * cols, fmt, q, scales, di.status,
-                                             di.num_sms, stream);
+    const cudaError_t e = launch_quantize_rows(x, in_dtype == FP8G_IN_BF16, x_rows, cols, rows,
+                                               n_rows, block, fmt, q, scales, di.status,
+                                               di.num_sms, stream);
     return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

@@ -357,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_shared(bar_acce(acc), 0));
 
-            const int64_t row = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;
-            if (row < ti.row_end) {
+            const int64_t arow = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;  // routed row
+            const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;       // row of C
+            if (row >= 0) {
                 const int64_t ncol0 = (int64_t)ti.pn * kPairBN + col0;
                 float a_t = alpha;  // scale left for the stores below
                 if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {

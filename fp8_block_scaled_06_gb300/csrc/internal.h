@@ -44,6 +44,8 @@ struct GemmParams {
     uint32_t ab_fmt;       // operand formats as MMA instruction-descriptor bits (A: 7-9, B: 10-12)
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
+    const int32_t *c_row_of;  // grouped scatter: row of C for routed row r (null: r)
+    int64_t c_rows;           // rows of C when scattering
 };
 
 // TMA descriptors of one launch: E4M3 operands and, for block-scaled CTA
@@ -81,7 +83,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes, int a_fmt = 0, int b_fmt = 0,
-                     const float *bias = nullptr, int act = 0);
+                     const float *bias = nullptr, int act = 0, const int32_t *c_row_of = nullptr,
+                     int64_t c_rows = 0);
 
 // scales.cu: fp32 1x32 scales -> packed UE8M0 chunks.  One launch packs
 // two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid
@@ -100,10 +103,12 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
                                int32_t E, unsigned int *status, cudaStream_t s);
 
 // quant.cu
-// quant.cu (fmt: FP8G_E4M3 or FP8G_E5M2)
-cudaError_t launch_quantize_tensor(const float *x, int64_t n, int fmt, uint8_t *q, float *scale,
-                                   unsigned int *status, int num_sms, cudaStream_t s);
-cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, int fmt,
-                                    uint8_t *q, float *scales, int num_sms, cudaStream_t s);
+// quant.cu: output row r quantises source row rows[r] (rows null: row r) of
+// x [x_rows, cols] (fp32, or bf16 if in_bf16); block 0 per-tensor or 32; fmt
+// FP8G_E4M3 / FP8G_E5M2.  Bad row indices record FP8G_ERR_INVALID_ARG.
+cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int64_t cols,
+                                 const int32_t *rows, int64_t n_rows, int32_t block, int fmt,
+                                 uint8_t *q, float *scales, unsigned int *status, int num_sms,
+                                 cudaStream_t s);
 
 }  // namespace fp8g

@@ -93,6 +93,19 @@ __device__ __forceinline__ bool wait_bar_landed_warp(uint32_t bar, uint32_t pari
     return ok != 0;
 }
 
+// Row of C that routed row `row` is stored to: c_row_of[row] when scattering
+// (grouped GEMM), else `row`.  An index outside [0, c_rows) records
+// FP8G_ERR_INVALID_ARG (detail: row) and returns -1 (the row is not stored).
+__device__ __forceinline__ int64_t out_row(const GemmParams &p, int64_t row) {
+    if (p.c_row_of == nullptr) return row;
+    const int64_t c = __ldg(p.c_row_of + row);
+    if (c < 0 || c >= p.c_rows) {
+        record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)row);
+        return -1;
+    }
+    return c;
+}
+
 // Fused epilogue on one output value of column `col`:
 //   v = act(fl32(v + bias[col]))   (bias row may be null; act FP8G_ACT_*)
 // applied after the per-tensor scale and before the output rounding.  ReLU

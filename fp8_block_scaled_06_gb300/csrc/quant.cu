@@ -12,8 +12,13 @@
 // reason for the block form.  q = FP8(fl32(x / s)), round to nearest even,
 // saturating (cvt ... satfinite), NaN -> 0x7F (a NaN code in both formats).
 //
+// The source is fp32 or bf16 (activations; widened exactly), and the output
+// rows may gather source rows through an index list (the routing step of the
+// MoE paragraph of the JAX/Blackwell page: tokens copied into expert order),
+// so that gather, scale and quantisation take one pass over HBM.
+//
 // HBM-bound elementwise kernels: 16-byte loads, 8-byte stores, a grid of a
-// few CTAs per SM striding over the tensor.
+// few CTAs per SM striding over the output.
 #include "internal.h"
 
 namespace fp8g {
@@ -89,11 +94,51 @@ __device__ __forceinline__ float pow2_scale(float amax) {
     return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
-// 1x32 blocks: 4 threads per block, 8 consecutive values per thread.
-template <int FMT>
-__global__ void quant_block32_kernel(const float *__restrict__ x, int64_t n8, uint8_t *__restrict__ q,
+// Eight consecutive values of the source at element offset `off` (a multiple
+// of 8), fp32 or bf16 (widened exactly).
+template <bool BF16>
+__device__ __forceinline__ void load8(const void *x, int64_t off, float4 &a, float4 &b) {
+    if constexpr (BF16) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + off));
+        a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+        b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                        __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(x) + off);
+        a = __ldg(p);
+        b = __ldg(p + 1);
+    }
+}
+
+// Output row r reads source row rows[r] (rows == null: row r).  A source row
+// outside [0, x_rows) records FP8G_ERR_INVALID_ARG (detail: r) and reads as
+// zeros; nothing outside the source is read.
+struct RowMap {
+    const void *x;
+    const int32_t *rows;
+    int64_t x_rows, cols;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ int64_t src_row(const RowMap &m, int64_t r, bool &ok) {
+    const int64_t s = m.rows != nullptr ? (int64_t)__ldg(m.rows + r) : r;
+    ok = s >= 0 && s < m.x_rows;
+    return ok ? s : 0;
+}
+
+__device__ __forceinline__ void bad_row(const RowMap &m, int64_t r) {
+    if (atomicCAS(&m.status[0], 0u, (unsigned)FP8G_ERR_INVALID_ARG) == 0u)
+        atomicExch(&m.status[1], (unsigned)r);
+}
+
+// 1x32 blocks: 4 threads per block, 8 consecutive values per thread; groups of
+// 8 values g = r * cols / 8 + c (a block's 4 groups share a row: cols % 32 == 0).
+template <int FMT, bool BF16>
+__global__ void quant_block32_kernel(RowMap m, int64_t n8, uint8_t *__restrict__ q,
                                      float *__restrict__ scales) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t g_per_row = m.cols / 8;
     // warp-uniform loop (the shuffles need all 32 lanes); the 4 threads of one
     // block are in range together because n8 is a multiple of 4
     for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); g0 < n8;
@@ -102,13 +147,18 @@ __global__ void quant_block32_kernel(const float *__restrict__ x, int64_t n8, ui
         const bool active = g < n8;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
         if (active) {
-            a = reinterpret_cast<const float4 *>(x)[2 * g];
-            b = reinterpret_cast<const float4 *>(x)[2 * g + 1];
+            const int64_t r = g / g_per_row;
+            bool ok;
+            const int64_t sr = src_row(m, r, ok);
+            if (ok)
+                load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
+            else if ((g - r * g_per_row) == 0)
+                bad_row(m, r);
         }
-        float m = absmax8(a, b);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const float s = pow2_scale<FMT>(m);
+        float am = absmax8(a, b);
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const float s = pow2_scale<FMT>(am);
         if (active) {
             reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
             if ((g & 3) == 0) scales[g >> 2] = s;
@@ -116,20 +166,27 @@ __global__ void quant_block32_kernel(const float *__restrict__ x, int64_t n8, ui
     }
 }
 
-__global__ void amax_kernel(const float *__restrict__ x, int64_t n, unsigned int *__restrict__ out) {
+template <bool BF16>
+__global__ void amax_kernel(RowMap m, int64_t n8, unsigned int *__restrict__ out) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    float m = 0.0f;
-    const int64_t n4 = n / 4;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        const float4 v = reinterpret_cast<const float4 *>(x)[i];
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    const int64_t g_per_row = m.cols / 8;
+    float am = 0.0f;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += stride) {
+        const int64_t r = g / g_per_row;
+        bool ok;
+        const int64_t sr = src_row(m, r, ok);
+        if (!ok) {
+            if ((g - r * g_per_row) == 0) bad_row(m, r);
+            continue;
+        }
+        float4 a, b;
+        load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
+        am = fmaxf(am, absmax8(a, b));
     }
-    for (int64_t i = n4 * 4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        m = fmaxf(m, fabsf(x[i]));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     // non-negative floats order like their bit patterns
-    if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(am));
 }
 
 template <int FMT>
@@ -140,15 +197,19 @@ __device__ __forceinline__ float tensor_scale(const float *amax_slot) {
     return s;
 }
 
-// x: n values, n % 8 == 0; the scale slot still holds amax.
-template <int FMT>
-__global__ void quant_tensor_kernel(const float *__restrict__ x, int64_t n8, uint8_t *__restrict__ q,
+// the scale slot still holds amax
+template <int FMT, bool BF16>
+__global__ void quant_tensor_kernel(RowMap m, int64_t n8, uint8_t *__restrict__ q,
                                     const float *__restrict__ amax_slot) {
     const float s = tensor_scale<FMT>(amax_slot);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t g_per_row = m.cols / 8;
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += stride) {
-        const float4 a = reinterpret_cast<const float4 *>(x)[2 * g];
-        const float4 b = reinterpret_cast<const float4 *>(x)[2 * g + 1];
+        const int64_t r = g / g_per_row;
+        bool ok;
+        const int64_t sr = src_row(m, r, ok);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (ok) load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
         reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
     }
 }
@@ -158,48 +219,44 @@ __global__ void finish_scale_kernel(float *slot) { *slot = tensor_scale<FMT>(slo
 
 }  // namespace
 
-cudaError_t launch_quantize_block32(const float *x, int64_t rows, int64_t cols, int fmt,
-                                    uint8_t *q, float *scales, int num_sms, cudaStream_t s) {
-    const int64_t n8 = rows * cols / 8;
+namespace {
+
+template <int FMT, bool BF16>
+cudaError_t launch_rows(const RowMap &m, int64_t n_rows, int32_t block, uint8_t *q, float *scales,
+                        int num_sms, cudaStream_t s) {
+    const int64_t n8 = n_rows * m.cols / 8;
     if (n8 == 0) return cudaSuccess;
     const int threads = 256;
-    int64_t blocks = (n8 + threads - 1) / threads;
     const int64_t cap = (int64_t)num_sms * 8;
+    int64_t blocks = (n8 + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
-    if (fmt == 1)
-        quant_block32_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scales);
-    else
-        quant_block32_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scales);
+    if (block == 32) {
+        quant_block32_kernel<FMT, BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8, q, scales);
+        return cudaGetLastError();
+    }
+    cudaError_t e = cudaMemsetAsync(scales, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    amax_kernel<BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8,
+                                                            reinterpret_cast<unsigned int *>(scales));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    quant_tensor_kernel<FMT, BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8, q, scales);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    finish_scale_kernel<FMT><<<1, 1, 0, s>>>(scales);
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_tensor(const float *x, int64_t n, int fmt, uint8_t *q, float *scale,
-                                   unsigned int *status, int num_sms, cudaStream_t s) {
-    (void)status;
-    cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), s);
-    if (e != cudaSuccess) return e;
-    const int threads = 256;
-    int64_t blocks = (n / 4 + threads - 1) / threads;
-    const int64_t cap = (int64_t)num_sms * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    amax_kernel<<<(unsigned)blocks, threads, 0, s>>>(x, n, reinterpret_cast<unsigned int *>(scale));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t n8 = n / 8;
-    if (n8 > 0) {
-        blocks = (n8 + threads - 1) / threads;
-        if (blocks > cap) blocks = cap;
-        if (fmt == 1)
-            quant_tensor_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scale);
-        else
-            quant_tensor_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(x, n8, q, scale);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+}  // namespace
+
+cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int64_t cols,
+                                 const int32_t *rows, int64_t n_rows, int32_t block, int fmt,
+                                 uint8_t *q, float *scales, unsigned int *status, int num_sms,
+                                 cudaStream_t s) {
+    const RowMap m{x, rows, x_rows, cols, status};
     if (fmt == 1)
-        finish_scale_kernel<1><<<1, 1, 0, s>>>(scale);
-    else
-        finish_scale_kernel<0><<<1, 1, 0, s>>>(scale);
-    return cudaGetLastError();
+        return in_bf16 ? launch_rows<1, true>(m, n_rows, block, q, scales, num_sms, s)
+                       : launch_rows<1, false>(m, n_rows, block, q, scales, num_sms, s);
+    return in_bf16 ? launch_rows<0, true>(m, n_rows, block, q, scales, num_sms, s)
+                   : launch_rows<0, false>(m, n_rows, block, q, scales, num_sms, s);
 }
 
 }  // namespace fp8g

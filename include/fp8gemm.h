@@ -216,6 +216,25 @@ FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t co
 FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block,
                           int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
 
+/* Source element types of fp8g_quantize_rows. */
+typedef enum { FP8G_IN_F32 = 0, FP8G_IN_BF16 = 1 } fp8g_in_dtype;
+
+/*
+ * Activation quantiser with a row gather [JAX-BW MoE paragraph: tokens routed
+ * to experts; its fine-grained quantisation advice]: output row r (of n_rows)
+ * is row rows[r] of x [x_rows, cols] quantised as fp8g_quantize does (rows
+ * null: row r, n_rows <= x_rows).  x is fp32 or bf16 (in_dtype; bf16 is
+ * widened exactly), 16-byte aligned; rows: device int32 [n_rows], 4-byte
+ * aligned; q: uint8 [n_rows, cols]; scales: [n_rows, cols/32] (block 32) or
+ * [1].  Gather, scale and quantisation are one pass over HBM (per-tensor:
+ * two).  cols % 8 == 0 (block 32: cols % 32 == 0).  A row index outside
+ * [0, x_rows) records FP8G_ERR_INVALID_ARG in the status word (detail: r) and
+ * quantises zeros for that row.
+ */
+FP8G_API fp8g_status fp8g_quantize_rows(const void *x, int32_t in_dtype, int64_t x_rows,
+                               int64_t cols, const int32_t *rows, int64_t n_rows, int32_t block,
+                               int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
+
 /*
  * The GEMM entry points with explicit operand formats (fp8g_format each for
  * A and B, mixed allowed: the tensor core's kind::f8f6f4 and
@@ -259,6 +278,23 @@ FP8G_API fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const flo
                                 const float *bias, int32_t act, const int32_t *counts, int32_t E,
                                 int64_t N, int64_t K, int64_t total_rows, int32_t *offsets_out,
                                 int32_t *tile_map_out, cudaStream_t stream);
+
+/*
+ * fp8_grouped_gemm_ex whose output rows are scattered [JAX-BW MoE paragraph:
+ * expert outputs return to token order]: routed row r (expert order) is
+ * stored to row c_row_of[r] of C [c_rows, N] (device int32 [total_rows],
+ * 4-byte aligned; null: row r, c_rows = total_rows).  Rows of C that no
+ * routed row names are not written; two routed rows naming one row of C
+ * race (the caller's responsibility).  An index outside [0, c_rows) records
+ * FP8G_ERR_INVALID_ARG (detail: r) and that row is not stored.
+ */
+FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, const float *sfa,
+                                     const float *sfb, void *C, int out, int32_t a_fmt,
+                                     int32_t b_fmt, const float *bias, int32_t act,
+                                     const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                     int64_t total_rows, const int32_t *c_row_of, int64_t c_rows,
+                                     int32_t *offsets_out, int32_t *tile_map_out,
+                                     cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
