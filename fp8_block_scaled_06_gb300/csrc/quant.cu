@@ -132,56 +132,83 @@ __device__ __forceinline__ void bad_row(const RowMap &m, int64_t r) {
         atomicExch(&m.status[1], (unsigned)r);
 }
 
-// 1x32 blocks: 4 threads per block, 8 consecutive values per thread; groups of
-// 8 values g = r * cols / 8 + c (a block's 4 groups share a row: cols % 32 == 0).
+// Work layout: CTAs stride over output rows; within a row the CTA's threads
+// take groups of 8 consecutive values (g and g + blockDim.x per pass, both
+// loads issued before either is used).  A 1x32 block is 4 consecutive groups,
+// held by 4 consecutive lanes (blockDim.x and cols / 8 are multiples of 4), so
+// its amax is two shuffles; lanes past the row's end stay in the pass
+// (inactive) until the whole warp is done, so the shuffles always see all 32
+// lanes.  (Measured on 8192 x 8192: one warp per row with 4-8 groups in
+// flight per lane was 10-30% slower.)
+constexpr int kQThreads = 256;
+
+// Divide by a power-of-two scale: x * (1/s) is exactly x / s (both are the
+// exact real x 2^-e rounded once), and 1/s is exact for s in 2^-126..2^127.
+template <int FMT>
+__device__ __forceinline__ uint2 quant8_pow2(const float4 a, const float4 b, float s) {
+    const float r = __frcp_rn(s);
+    uint2 o;
+    o.x = fp8x2<FMT>(__fmul_rn(a.x, r), __fmul_rn(a.y, r)) |
+          (fp8x2<FMT>(__fmul_rn(a.z, r), __fmul_rn(a.w, r)) << 16);
+    o.y = fp8x2<FMT>(__fmul_rn(b.x, r), __fmul_rn(b.y, r)) |
+          (fp8x2<FMT>(__fmul_rn(b.z, r), __fmul_rn(b.w, r)) << 16);
+    return o;
+}
+
 template <int FMT, bool BF16>
-__global__ void quant_block32_kernel(RowMap m, int64_t n8, uint8_t *__restrict__ q,
-                                     float *__restrict__ scales) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t g_per_row = m.cols / 8;
-    // warp-uniform loop (the shuffles need all 32 lanes); the 4 threads of one
-    // block are in range together because n8 is a multiple of 4
-    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); g0 < n8;
-         g0 += stride) {
-        const int64_t g = g0 + (threadIdx.x & 31);
-        const bool active = g < n8;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (active) {
-            const int64_t r = g / g_per_row;
-            bool ok;
-            const int64_t sr = src_row(m, r, ok);
-            if (ok)
-                load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
-            else if ((g - r * g_per_row) == 0)
-                bad_row(m, r);
-        }
-        float am = absmax8(a, b);
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        const float s = pow2_scale<FMT>(am);
-        if (active) {
-            reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
-            if ((g & 3) == 0) scales[g >> 2] = s;
+__global__ void __launch_bounds__(kQThreads) quant_block32_kernel(RowMap m, int64_t n_rows,
+                                                                 uint8_t *__restrict__ q,
+                                                                 float *__restrict__ scales) {
+    constexpr int U = 2;  // groups per thread and pass
+    const int64_t gpr = m.cols / 8;  // groups of 8 per row
+    const int64_t wbase = threadIdx.x & ~31;
+    for (int64_t r = blockIdx.x; r < n_rows; r += gridDim.x) {
+        bool ok;
+        const int64_t sr = src_row(m, r, ok);
+        if (!ok && threadIdx.x == 0) bad_row(m, r);
+        const int64_t in0 = sr * m.cols, out0 = r * gpr;
+        for (int64_t c0 = wbase; c0 < gpr; c0 += U * kQThreads) {
+            float4 a[U], b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (threadIdx.x & 31) + u * kQThreads;
+                a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                b[u] = a[u];
+                if (ok && c < gpr) load8<BF16>(m.x, in0 + c * 8, a[u], b[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (threadIdx.x & 31) + u * kQThreads;
+                float am = absmax8(a[u], b[u]);
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+                const float sc = pow2_scale<FMT>(am);
+                if (c < gpr) {
+                    reinterpret_cast<uint2 *>(q)[out0 + c] = quant8_pow2<FMT>(a[u], b[u], sc);
+                    if ((c & 3) == 0) scales[(out0 + c) >> 2] = sc;
+                }
+            }
         }
     }
 }
 
 template <bool BF16>
-__global__ void amax_kernel(RowMap m, int64_t n8, unsigned int *__restrict__ out) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t g_per_row = m.cols / 8;
+__global__ void __launch_bounds__(kQThreads) amax_kernel(RowMap m, int64_t n_rows,
+                                                        unsigned int *__restrict__ out) {
+    const int64_t gpr = m.cols / 8;
     float am = 0.0f;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += stride) {
-        const int64_t r = g / g_per_row;
+    for (int64_t r = blockIdx.x; r < n_rows; r += gridDim.x) {
         bool ok;
         const int64_t sr = src_row(m, r, ok);
         if (!ok) {
-            if ((g - r * g_per_row) == 0) bad_row(m, r);
-            continue;
+            if (threadIdx.x == 0) bad_row(m, r);
+            continue;  // block-uniform
         }
-        float4 a, b;
-        load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
-        am = fmaxf(am, absmax8(a, b));
+        for (int64_t c = threadIdx.x; c < gpr; c += kQThreads) {
+            float4 a, b;
+            load8<BF16>(m.x, sr * m.cols + c * 8, a, b);
+            am = fmaxf(am, absmax8(a, b));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -199,18 +226,19 @@ __device__ __forceinline__ float tensor_scale(const float *amax_slot) {
 
 // the scale slot still holds amax
 template <int FMT, bool BF16>
-__global__ void quant_tensor_kernel(RowMap m, int64_t n8, uint8_t *__restrict__ q,
-                                    const float *__restrict__ amax_slot) {
+__global__ void __launch_bounds__(kQThreads) quant_tensor_kernel(RowMap m, int64_t n_rows,
+                                                                uint8_t *__restrict__ q,
+                                                                const float *__restrict__ amax_slot) {
     const float s = tensor_scale<FMT>(amax_slot);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t g_per_row = m.cols / 8;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += stride) {
-        const int64_t r = g / g_per_row;
+    const int64_t gpr = m.cols / 8;
+    for (int64_t r = blockIdx.x; r < n_rows; r += gridDim.x) {
         bool ok;
         const int64_t sr = src_row(m, r, ok);
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (ok) load8<BF16>(m.x, sr * m.cols + (g - r * g_per_row) * 8, a, b);
-        reinterpret_cast<uint2 *>(q)[g] = quant8<FMT>(a, b, s);
+        for (int64_t c = threadIdx.x; c < gpr; c += kQThreads) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (ok) load8<BF16>(m.x, sr * m.cols + c * 8, a, b);
+            reinterpret_cast<uint2 *>(q)[r * gpr + c] = quant8<FMT>(a, b, s);
+        }
     }
 }
 
@@ -224,22 +252,18 @@ namespace {
 template <int FMT, bool BF16>
 cudaError_t launch_rows(const RowMap &m, int64_t n_rows, int32_t block, uint8_t *q, float *scales,
                         int num_sms, cudaStream_t s) {
-    const int64_t n8 = n_rows * m.cols / 8;
-    if (n8 == 0) return cudaSuccess;
-    const int threads = 256;
-    const int64_t cap = (int64_t)num_sms * 8;
-    int64_t blocks = (n8 + threads - 1) / threads;
-    if (blocks > cap) blocks = cap;
+    if (n_rows == 0 || m.cols == 0) return cudaSuccess;
+    const int64_t cap = (int64_t)num_sms * 8;  // 8 CTAs of 256 threads per SM
+    const unsigned blocks = (unsigned)(n_rows < cap ? n_rows : cap);
     if (block == 32) {
-        quant_block32_kernel<FMT, BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8, q, scales);
+        quant_block32_kernel<FMT, BF16><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
         return cudaGetLastError();
     }
     cudaError_t e = cudaMemsetAsync(scales, 0, sizeof(float), s);
     if (e != cudaSuccess) return e;
-    amax_kernel<BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8,
-                                                            reinterpret_cast<unsigned int *>(scales));
+    amax_kernel<BF16><<<blocks, kQThreads, 0, s>>>(m, n_rows, reinterpret_cast<unsigned int *>(scales));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    quant_tensor_kernel<FMT, BF16><<<(unsigned)blocks, threads, 0, s>>>(m, n8, q, scales);
+    quant_tensor_kernel<FMT, BF16><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     finish_scale_kernel<FMT><<<1, 1, 0, s>>>(scales);
     return cudaGetLastError();
