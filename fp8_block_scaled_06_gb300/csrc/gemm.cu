@@ -34,6 +34,8 @@
 // copies and MMAs are drained with bounded waits, and tensor memory is freed.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "kernel_common.cuh"
@@ -682,6 +684,43 @@ cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelCh
     return cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, p);
 }
 
+// Clusters of `S` split-K CTAs that can be resident at once on the current
+// device (cudaOccupancyMaxActiveClusters; cached per device).  Clusters are
+// placed inside one GPC, so the count is not SMs / S: on GB300 (152 SMs) with
+// these ~200 KB CTAs, 76 pairs fit but only 36 clusters of four.  A grid of
+// more clusters would run the rest as a second wave.  0 if unknown.
+int max_split_clusters(int S) {
+    static std::atomic<int> cache[64][kMaxSplit + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || S < 1 || S > kMaxSplit)
+        return 0;
+    int v = cache[dev][S].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    using C_ = Cfg<kModeBlock, 128, 1, 6>;  // the larger of the two split-K footprints
+    auto kern = gemm_kernel<kModeBlock, 128, 1, 6, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM_BYTES) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(S * 64), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();  // clear
+        return 0;
+    }
+    cache[dev][S].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 }  // namespace
 
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -710,11 +749,16 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     const int64_t num_kb = (K + kBK - 1) / kBK;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kc.BN - 1) / kc.BN);
     // Few output tiles: 128-wide tiles, K split over a cluster of S CTAs per
-    // tile (S a power of two <= kMaxSplit and <= the K blocks, S * tiles <= SMs).
+    // tile (S a power of two <= kMaxSplit and <= the K blocks, S * tiles <= SMs,
+    // and every cluster resident at once).
     if (tiles * 2 <= num_sms && num_kb >= 2) {
         const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
         int S = 1;
-        while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) S *= 2;
+        while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) {
+            const int cap = max_split_clusters(S * 2);
+            if (cap > 0 && tiles128 > cap) break;
+            S *= 2;
+        }
         if (S >= 2) {
             kc.BN = 128;
             kc.b_rows = 128;

@@ -239,6 +239,27 @@ def test_split_k_ranges(K):
     assert_within(C, ref, bound, f"split-K per-tensor {M}x{N}x{K}")
 
 
+def test_split_k_clusters_all_resident():
+    """M=128, N=4864: 38 tiles of 128 x 128.  Clusters of four would need 38
+    co-resident clusters; GB300 holds 36 of this kernel's four-CTA clusters
+    (a cluster stays inside one GPC), so the plan takes 38 pairs (76 CTAs)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 128, 4864, 4096
+    p = fp8g.fp8g_gemm_plan(1, M, N, K)
+    if sms == 152:
+        assert p["split_k"] == 2 and p["grid"] == 76
+    A = synth.normal((M, K), seed=48)
+    B = synth.normal((N, K), seed=49)
+    qa, sa, qa_o, sa_o = quant_both(A, 32)
+    qb, sb, qb_o, sb_o = quant_both(B, 32)
+    C = run_gemm(qa, sa, qb, sb, True, "bf16")
+    rng = np.random.default_rng(48)
+    pi = rng.integers(0, M, 3000)
+    pj = rng.integers(0, N, 3000)
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16)
+    assert_within(C[pi, pj], ref, bound, "split-K 128x4864x4096")
+
+
 # ------------------------------------------------- per-tensor on CTA pairs
 def test_tensor_pair_chosen_for_large():
     p = fp8g.fp8g_gemm_plan(0, 4096, 4608, 512)
