@@ -177,7 +177,7 @@ def run_once(fp8g, wl, w, t, C, stream):
 # of the dominant kernel, from the ncu capture summarised in
 # profiles/gemm_pair_block_8192_ncu.md.  Valid only for the kernel source that
 # capture measured; workloads without a capture report null.
-TRAFFIC_BYTES = {"large8192": 270_027_776 + 117_301_504}
+TRAFFIC_BYTES = {}
 
 
 def launches_per_call(fp8g, wl) -> int:

@@ -281,7 +281,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
     // 256-wide tiles take B's scales replicated for one 128x256b tensor-memory
     // copy (4 KB per 256 rows and K step instead of 1 KB)
-    const bool repB = kc.BN == 256;
+    const bool repB = kc.BN == 256 && !kc.pair;
     const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (repB ? 4 : 1);
     void *ws = nullptr;
     if (scratch != nullptr) {
@@ -306,8 +306,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         // uint32 (one 512-byte chunk per row)
         const uint64_t dSA[2] = {128u, (uint64_t)p.num_kb * (uint64_t)p.n_rtA};
         const uint32_t bSA[2] = {128u, 1u};
-        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB * 4};
-        const uint32_t bSB[2] = {128u, 8u};  // 4 KB: one replicated 256-row block
+        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB};
+        const uint32_t bSB[2] = {128u, 2u};  // 1 KB: the two 128-row chunks of a 256-row tile
         if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSA, bSA,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
             tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSB, bSB,

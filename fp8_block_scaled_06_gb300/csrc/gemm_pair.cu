@@ -48,13 +48,14 @@ constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
 // its own 128 rows of A but of all 256 rows (both halves) of the tile's B,
 // and tcgen05.cp.cta_group::2 copies each CTA's shared memory into its own
 // tensor memory.  (Established on GB300 by the exact scale-layout test: with
-// only the CTA's own half of B's scales the results are wrong.)  Each copy
-// instruction costs the MMA stream about 6% (measured), so per K step: A's
-// 128 rows with one 32x128b.warpx4 copy (replicated over the four lane
-// quarters by the copy) and B's 256 rows with one 128x256b copy from a
-// source the packing kernel already replicated (4 KB).
+// only the CTA's own half of B's scales the results are wrong.)  Per K step
+// three 32x128b.warpx4 copies (each replicated over the four lane quarters by
+// the copy): A's 128 rows, B's rows 0-127 and 128-255, from 1.5 KB of packed
+// chunks.  Issued by their own warp the copies overlap the MMAs, so three
+// small copies beat one 128x256b copy from a pre-replicated 4 KB source
+// (which saved copy instructions when the MMA thread issued them).
 constexpr int kSfaBytes = 512;
-constexpr int kSfbBytes = 4096;
+constexpr int kSfbBytes = 1024;  // B's two 128-row chunks
 
 template <int MODE>
 struct PairCfg {
@@ -253,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
                         ptx::tma_load_2d_pair(dst, &tmSA, fb, 0,
                                               kb * p.n_rtA + ti.rtA0 + (int32_t)rank);
-                        // replicated B block of pair tile pn: 8 rows of 512 B
+                        // B's chunks of pair tile pn: 128-row tiles 2 pn and 2 pn + 1
                         ptx::tma_load_2d_pair(dst + kSfaBytes, &tmSB, fb, 0,
-                                              ((ti.e * p.num_kb + kb) * (p.n_rtB / 2) + ti.pn) * 8);
+                                              (ti.e * p.num_kb + kb) * p.n_rtB + 2 * ti.pn);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -324,7 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                     const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
                     ptx::tc_cp_32x128b_warpx4_pair(sf, ptx::desc_sf_chunk(cs));
-                    ptx::tc_cp_128x256b_pair(sf + 8, ptx::desc_sf_128x256b(cs + kSfaBytes));
+                    // B's rows 0-127 to columns 8-11, rows 128-255 to 12-15 (each
+                    // replicated over the lane quarters by the copy)
+                    ptx::tc_cp_32x128b_warpx4_pair(sf + 8, ptx::desc_sf_chunk(cs + kSfaBytes));
+                    ptx::tc_cp_32x128b_warpx4_pair(sf + 12,
+                                                   ptx::desc_sf_chunk(cs + kSfaBytes + 512));
                     ptx::tc_commit_pair_mc(bar_sfr(stage), 0x1);
                     if (++stage == kStages) {
                         stage = 0;
