@@ -190,6 +190,78 @@ def launches_per_call(fp8g, wl) -> int:
     return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
 
 
+def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
+    """Per-step milliseconds of the end-to-end loop (see the caller).  With
+    lanes > 1 each step's copies are split into contiguous chunks over that
+    many streams per direction (measured on GB300: 4 lanes were slower, 1086
+    against 1197 TFLOPS on the 8192^3 workload; the host link, not one copy
+    engine, is the limit)."""
+    host = {k: v.cpu().pin_memory() for k, v in t.items()}
+    nbuf = 2
+    dev_in = [{k: torch.empty_like(v) for k, v in t.items()} for _ in range(nbuf)]
+    dev_C = [C] + [torch.empty_like(C) for _ in range(nbuf - 1)]
+    host_C = [torch.empty(C.shape, dtype=C.dtype).pin_memory() for _ in range(nbuf)]
+    s_in = [torch.cuda.Stream(device) for _ in range(lanes)]
+    s_gemm = torch.cuda.Stream(device)
+    s_out = [torch.cuda.Stream(device) for _ in range(lanes)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done = [[ev() for _ in range(lanes)] for _ in range(nbuf)]
+    gemm_done = [ev() for _ in range(nbuf)]
+    out_done = [[ev() for _ in range(lanes)] for _ in range(nbuf)]
+    first = [True] * nbuf
+
+    def chunks(a, b):
+        """Matching contiguous pieces of two same-shape tensors, ~lanes per pair."""
+        fa, fb = a.reshape(-1), b.reshape(-1)
+        n = fa.numel()
+        step_ = max(1, -(-n // lanes))
+        return [(fa[o:o + step_], fb[o:o + step_]) for o in range(0, n, step_)]
+
+    def step(i):
+        b = i % nbuf
+        pieces = [p for k in dev_in[b] for p in chunks(dev_in[b][k], host[k])]
+        for j, s_ in enumerate(s_in):
+            with torch.cuda.stream(s_):
+                if not first[b]:
+                    s_.wait_event(gemm_done[b])
+                for dst, src in pieces[j::lanes]:
+                    dst.copy_(src, non_blocking=True)
+                in_done[b][j].record(s_)
+        for j in range(lanes):
+            s_gemm.wait_event(in_done[b][j])
+            if not first[b]:
+                s_gemm.wait_event(out_done[b][j])
+        run_once(fp8g, wl, w, dev_in[b], dev_C[b], s_gemm)
+        gemm_done[b].record(s_gemm)
+        outs = chunks(host_C[b], dev_C[b])
+        for j, s_ in enumerate(s_out):
+            with torch.cuda.stream(s_):
+                s_.wait_event(gemm_done[b])
+                for dst, src in outs[j::lanes]:
+                    dst.copy_(src, non_blocking=True)
+                out_done[b][j].record(s_)
+        first[b] = False
+
+    for i in range(2 * nbuf):  # warm-up
+        step(i)
+    torch.cuda.synchronize(device)
+    n = max(3, min(50, steps // 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    start = torch.cuda.Stream(device)
+    e0.record(start)
+    for s_ in s_in:
+        s_.wait_stream(start)
+    for i in range(n):
+        step(i)
+    end = torch.cuda.Stream(device)
+    for s_ in s_in + s_out + [s_gemm]:
+        end.wait_stream(s_)
+    e1.record(end)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / n
+
+
 def oracle_inputs(wl, w):
     """The oracle's own quantisation of the workload (done once, untimed)."""
     import oracle
@@ -311,31 +383,17 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
 
-    # end to end through the C ABI with host buffers: H2D of the inputs from
-    # pinned memory, the GEMM, D2H of C, every step
-    host = {k: v.cpu().pin_memory() for k, v in t.items()}
-    Ch = torch.empty(C.shape, dtype=C.dtype).pin_memory()
-    dev_in = {k: torch.empty_like(v) for k, v in t.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = Ch.numel() * Ch.element_size()
-    e2e_steps = max(3, min(50, args.steps // 20))
-    for _ in range(2):
-        for k in dev_in:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        run_once(fp8g, wl, w, dev_in, C, stream)
-        Ch.copy_(C, non_blocking=True)
-    torch.cuda.synchronize(device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for k in dev_in:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        run_once(fp8g, wl, w, dev_in, C, stream)
-        Ch.copy_(C, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # end to end through the C ABI with host buffers: every step copies its
+    # inputs from pinned host memory, runs the GEMM and copies C back to pinned
+    # host memory.  Copies and GEMMs of consecutive steps overlap (copy
+    # streams per direction, a compute stream, two device buffers each),
+    # ordered by events: step i's GEMM waits for its inputs and for step
+    # i - 2's read-back of the same C buffer; step i's input copy waits for
+    # step i - 2's GEMM.  Timed from the first copy in to the last copy out,
+    # over the whole dependency chain.
+    e2e_ms = e2e_pipelined(fp8g, wl, w, t, C, device, args.steps)
+    h2d = sum(v.numel() * v.element_size() for v in t.values())
+    d2h = C.numel() * C.element_size()
 
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16"]          # measured bf16 burst x nominal fp8/bf16 ratio (2)
@@ -380,7 +438,10 @@ def main():
         "roofline": roof,
         "achieved_hbm_gbs": round(hbm_gbs, 1),
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOPS",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 4),
+                "overlap": "two buffers, a copy-in, a compute and a copy-out stream: step "
+                           "i+1's copy in and step i-1's copy out run during step i's GEMM"},
         "gpu_launches": args.steps * launches_per_call(fp8g, wl),
         "clocks": clocks,
         "wall_s": round(wall, 3),
