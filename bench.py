@@ -177,7 +177,7 @@ def run_once(fp8g, wl, w, t, C, stream):
 # of the dominant kernel, from the ncu capture summarised in
 # profiles/gemm_pair_block_8192_ncu.md.  Valid only for the kernel source that
 # capture measured; workloads without a capture report null.
-TRAFFIC_BYTES = {}
+TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536}
 
 
 def launches_per_call(fp8g, wl) -> int:
