@@ -84,6 +84,7 @@ def _L():
             lib.oracle_pow2_scale_fmt.restype = ctypes.c_float
             lib.oracle_pow2_scale_fmt.argtypes = [ctypes.c_float, ctypes.c_int]
             lib.oracle_quantize_block32_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
+            lib.oracle_quantize_block32_literal.argtypes = [P, i64, i64, ctypes.c_int, P, P]
             lib.oracle_act.restype = ctypes.c_double
             lib.oracle_act.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_gemm_ex.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
@@ -184,14 +185,16 @@ def pow2_scale(amax: float, fmt: int = E4M3) -> float:
     return float(_L().oracle_pow2_scale_fmt(float(np.float32(amax)), int(fmt)))
 
 
-def quantize_block32(x: np.ndarray, fmt: int = E4M3):
-    """1x32 along the last axis: returns (codes uint8, scales float32 [rows, cols/32])."""
+def quantize_block32(x: np.ndarray, fmt: int = E4M3, literal: bool = False):
+    """1x32 along the last axis: returns (codes uint8, scales float32 [rows, cols/32]).
+    literal: block scale fl32(amax / fmax) instead of the power of two."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows, cols = x.shape
     assert cols % 32 == 0
     q = np.empty((rows, cols), dtype=np.uint8)
     s = np.empty((rows, cols // 32), dtype=np.float32)
-    _L().oracle_quantize_block32_fmt(_p(x), rows, cols, int(fmt), _p(q), _p(s))
+    fn = _L().oracle_quantize_block32_literal if literal else _L().oracle_quantize_block32_fmt
+    fn(_p(x), rows, cols, int(fmt), _p(q), _p(s))
     return q, s
 
 

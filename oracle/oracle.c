@@ -252,6 +252,7 @@ typedef struct {
     float *scales;
     int64_t cols, r0, r1;
     int fmt;
+    int literal; /* block scale fl32(amax / fmax) instead of the power of two */
 } quant_job;
 
 static void *quant_block32_rows(void *arg);
@@ -259,8 +260,24 @@ static void *quant_block32_rows(void *arg);
 /* 1x32 block quantisation along the contiguous (K) axis.  cols % 32 == 0.
  * scales: [rows, cols/32] fp32, each a power of two.  Rows are independent, so
  * they are split across up to 64 threads (no effect on the result). */
+/* 1x32 block quantisation with the literal block scale s = fl32(amax / fmax)
+ * (1 when that is 0): the "fp32 scale = block amax/448" wording of the
+ * workloads, taken literally rather than rounded up to a power of two. */
+static void quantize_block32_impl(const float *x, int64_t rows, int64_t cols, int fmt,
+                                  int literal, uint8_t *q, float *scales);
+
+ORACLE_EXPORT void oracle_quantize_block32_literal(const float *x, int64_t rows, int64_t cols,
+                                                   int fmt, uint8_t *q, float *scales) {
+    quantize_block32_impl(x, rows, cols, fmt, 1, q, scales);
+}
+
 ORACLE_EXPORT void oracle_quantize_block32_fmt(const float *x, int64_t rows, int64_t cols,
                                                int fmt, uint8_t *q, float *scales) {
+    quantize_block32_impl(x, rows, cols, fmt, 0, q, scales);
+}
+
+static void quantize_block32_impl(const float *x, int64_t rows, int64_t cols, int fmt,
+                                  int literal, uint8_t *q, float *scales) {
     int nt = (int)(rows * cols / (1 << 20));
     if (nt < 1) nt = 1;
     if (nt > 64) nt = 64;
@@ -271,6 +288,7 @@ ORACLE_EXPORT void oracle_quantize_block32_fmt(const float *x, int64_t rows, int
     for (int t = 0; t < nt; ++t) {
         jobs[t].x = x; jobs[t].q = q; jobs[t].scales = scales; jobs[t].cols = cols;
         jobs[t].fmt = fmt;
+        jobs[t].literal = literal;
         jobs[t].r0 = t * per < rows ? t * per : rows;
         jobs[t].r1 = (t + 1) * per < rows ? (t + 1) * per : rows;
         if (nt == 1 || pthread_create(&tid[t], NULL, quant_block32_rows, &jobs[t]) != 0) {
@@ -297,7 +315,13 @@ static void *quant_block32_rows(void *arg) {
     for (int64_t r = j->r0; r < j->r1; ++r) {
         for (int64_t b = 0; b < nb; ++b) {
             const float *blk = x + r * cols + b * 32;
-            float s = oracle_pow2_scale_fmt(amax_of(blk, 32, 1), j->fmt);
+            float s;
+            if (j->literal) {
+                s = amax_of(blk, 32, 1) / (float)fmt_max(j->fmt);
+                if (s == 0.0f) s = 1.0f;
+            } else {
+                s = oracle_pow2_scale_fmt(amax_of(blk, 32, 1), j->fmt);
+            }
             scales[r * nb + b] = s;
             for (int k = 0; k < 32; ++k) q[r * cols + b * 32 + k] = encode_fmt(blk[k] / s, j->fmt);
         }
