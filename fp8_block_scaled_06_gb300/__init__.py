@@ -31,6 +31,7 @@ FP8G_OUT_BF16 = 0
 FP8G_OUT_F32 = 1
 FP8G_E4M3 = 0
 FP8G_E5M2 = 1
+FP8G_BLOCK32_LITERAL = 33
 FP8G_IN_F32 = 0
 FP8G_IN_BF16 = 1
 FP8G_ACT_NONE = 0
@@ -43,7 +44,8 @@ EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
-    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_status", "fp8g_status_string",
+    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_blockscaled_promote",
+    "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
 
@@ -111,6 +113,9 @@ def load():
         lib.fp8_grouped_gemm_scatter.restype = st
         lib.fp8_grouped_gemm_scatter.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, P,
                                                  i32, i64, i64, i64, P, i64, P, P, P]
+        lib.fp8_gemm_blockscaled_promote.restype = st
+        lib.fp8_gemm_blockscaled_promote.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32,
+                                                     i64, i64, i64, P]
         lib.fp8g_quantize_rows.restype = st
         lib.fp8g_quantize_rows.argtypes = [P, i32, i64, i64, P, i64, i32, i32, P, P, P]
         lib.fp8_grouped_gemm_fmt.restype = st
@@ -262,6 +267,14 @@ def fp8_grouped_gemm_scatter(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int
                                            _stream(stream)), "fp8_grouped_gemm_scatter")
 
 
+def fp8_gemm_blockscaled_promote(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bias,
+                                 act: int, M: int, N: int, K: int, stream=None):
+    _check(load().fp8_gemm_blockscaled_promote(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C),
+                                               int(out), int(a_fmt), int(b_fmt), _ptr(bias),
+                                               int(act), M, N, K, _stream(stream)),
+           "fp8_gemm_blockscaled_promote")
+
+
 def fp8g_quantize_rows(x, in_dtype: int, x_rows: int, cols: int, rows, n_rows: int, block: int,
                        fmt: int, q, scales, stream=None):
     _check(load().fp8g_quantize_rows(_ptr(x), int(in_dtype), x_rows, cols, _ptr(rows), n_rows,
@@ -299,7 +312,7 @@ def quantize(x, block: int = 32, stream=None, fmt: int = FP8G_E4M3):
     x = x.contiguous()
     rows, cols = x.shape
     q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
-    if block == 32:
+    if block != 0:
         s = torch.empty((rows, cols // 32), dtype=torch.float32, device=x.device)
     else:
         s = torch.empty((1,), dtype=torch.float32, device=x.device)

@@ -362,6 +362,61 @@ fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const float *s
                     stream, nullptr, 0, a_fmt, b_fmt, bias, act);
 }
 
+fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const float *sfa,
+                                         const float *sfb, void *C, int out, int32_t a_fmt,
+                                         int32_t b_fmt, const float *bias, int32_t act, int64_t M,
+                                         int64_t N, int64_t K, cudaStream_t stream) {
+    fp8g_status st = check_common(A, B, C, out, M, N, K);
+    if (st != FP8G_OK) return st;
+    if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
+    if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
+        return FP8G_ERR_INVALID_ARG;
+    if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
+        return FP8G_ERR_INVALID_ARG;
+    // the scales' rows (K/32 fp32) are TMA rows: 16-byte multiples
+    if (K % 128 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
+    if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
+    DevInfo di;
+    if ((st = device_info(di)) != FP8G_OK) return st;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_kb = (int32_t)(K / kBK);
+    p.npm = (int32_t)((M + kBM - 1) / kBM);
+    p.npn = (int32_t)((N + 127) / 128);
+    p.T = (int64_t)p.npm * p.npn;
+    p.split = 1;
+    p.sa = sfa;
+    p.sb = sfb;
+    p.sfc = K / 32;
+    p.C = C;
+    p.status = di.status;
+    p.timeout_ns = timeout_ns();
+    p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
+    p.bias = bias;
+    p.act = act;
+    GemmMaps maps;
+    const uint64_t dA[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
+    const uint32_t box[2] = {(uint32_t)kBK, 128u};
+    const uint64_t dSA[2] = {(uint64_t)(K / 32), (uint64_t)M};
+    const uint64_t dSB[2] = {(uint64_t)(K / 32), (uint64_t)N};
+    const uint32_t bS[2] = {4u, 128u};  // 4 K blocks x 128 rows of fp32
+    if ((st = tmap_u8(A, 2, dA, box, di.dev, maps.A)) != FP8G_OK) return st;
+    if ((st = tmap_u8(B, 2, dB, box, di.dev, maps.B)) != FP8G_OK) return st;
+    if ((st = tmap_encode(sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dSA, bS,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA)) != FP8G_OK)
+        return st;
+    if ((st = tmap_encode(sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dSB, bS,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB)) != FP8G_OK)
+        return st;
+    const int grid = (int)(p.T < di.num_sms ? p.T : di.num_sms);
+    const cudaError_t e = launch_gemm_promote(out == FP8G_OUT_F32, maps, p, grid, stream);
+    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
 fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
                                      const float *sfb, void *C, int out, int32_t a_fmt,
                                      int32_t b_fmt, int64_t M, int64_t N, int64_t K,
@@ -486,9 +541,9 @@ fp8g_status fp8g_quantize_rows(const void *x, int32_t in_dtype, int64_t x_rows, 
     if (x_rows < 1 || n_rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
     if (rows == nullptr && n_rows > x_rows) return FP8G_ERR_INVALID_ARG;
     if (rows != nullptr && !aligned(rows, 4)) return FP8G_ERR_ALIGNMENT;
-    if (block != 0 && block != 32) return FP8G_ERR_INVALID_ARG;
+    if (block != 0 && block != 32 && block != FP8G_BLOCK32_LITERAL) return FP8G_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scales, 4)) return FP8G_ERR_ALIGNMENT;
-    if (block == 32 && cols % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (block != 0 && cols % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (cols % 8 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
     if (x_rows >= ((int64_t)1 << 40) / cols || n_rows >= ((int64_t)1 << 40) / cols ||
         x_rows > INT32_MAX)

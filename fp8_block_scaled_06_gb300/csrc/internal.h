@@ -70,6 +70,11 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                         const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
 
+// gemm_promote.cu: arbitrary fp32 1x32 scales (maps.SA / maps.SB: the fp32
+// scale arrays, box 4 x 128); grid CTAs over 128 x 128 tiles.
+cudaError_t launch_gemm_promote(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,
+                                cudaStream_t stream);
+
 // gemm_pair.cu (per-tensor and block-scaled, CTA pairs)
 cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                              int grid, cudaStream_t stream);
@@ -106,6 +111,7 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
 // quant.cu: output row r quantises source row rows[r] (rows null: row r) of
 // x [x_rows, cols] (fp32, or bf16 if in_bf16); block 0 per-tensor or 32; fmt
 // FP8G_E4M3 / FP8G_E5M2.  Bad row indices record FP8G_ERR_INVALID_ARG.
+// block FP8G_BLOCK32_LITERAL: 1x32 blocks with s = fl32(amax / fmax).
 cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int64_t cols,
                                  const int32_t *rows, int64_t n_rows, int32_t block, int fmt,
                                  uint8_t *q, float *scales, unsigned int *status, int num_sms,

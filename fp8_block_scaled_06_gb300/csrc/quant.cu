@@ -155,7 +155,9 @@ __device__ __forceinline__ uint2 quant8_pow2(const float4 a, const float4 b, flo
     return o;
 }
 
-template <int FMT, bool BF16>
+// LITERAL: s = fl32(amax / fmax) (1 when that is 0) and q = FP8(fl32(x / s)),
+// instead of the power-of-two scale.
+template <int FMT, bool BF16, bool LITERAL>
 __global__ void __launch_bounds__(kQThreads) quant_block32_kernel(RowMap m, int64_t n_rows,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales) {
@@ -182,9 +184,16 @@ __global__ void __launch_bounds__(kQThreads) quant_block32_kernel(RowMap m, int6
                 float am = absmax8(a[u], b[u]);
                 am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
                 am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-                const float sc = pow2_scale<FMT>(am);
+                float sc;
+                if constexpr (LITERAL) {
+                    sc = __fdiv_rn(am, Fp8Fmt<FMT>::kMax);
+                    if (sc == 0.0f) sc = 1.0f;
+                } else {
+                    sc = pow2_scale<FMT>(am);
+                }
                 if (c < gpr) {
-                    reinterpret_cast<uint2 *>(q)[out0 + c] = quant8_pow2<FMT>(a[u], b[u], sc);
+                    reinterpret_cast<uint2 *>(q)[out0 + c] =
+                        LITERAL ? quant8<FMT>(a[u], b[u], sc) : quant8_pow2<FMT>(a[u], b[u], sc);
                     if ((c & 3) == 0) scales[(out0 + c) >> 2] = sc;
                 }
             }
@@ -256,7 +265,11 @@ cudaError_t launch_rows(const RowMap &m, int64_t n_rows, int32_t block, uint8_t 
     const int64_t cap = (int64_t)num_sms * 8;  // 8 CTAs of 256 threads per SM
     const unsigned blocks = (unsigned)(n_rows < cap ? n_rows : cap);
     if (block == 32) {
-        quant_block32_kernel<FMT, BF16><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
+        quant_block32_kernel<FMT, BF16, false><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
+        return cudaGetLastError();
+    }
+    if (block == FP8G_BLOCK32_LITERAL) {
+        quant_block32_kernel<FMT, BF16, true><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
         return cudaGetLastError();
     }
     cudaError_t e = cudaMemsetAsync(scales, 0, sizeof(float), s);

@@ -216,6 +216,15 @@ FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t co
 FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block,
                           int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
 
+/*
+ * `block` value of the quantisers for 1x32 blocks with the literal scale
+ * s = fl32(amax / fmax) (1 when that is 0) — the "fp32 scale = block
+ * amax/448" wording taken literally — and q = FP8(fl32(x / s)).  Such scales
+ * are generally not powers of two: use them with
+ * fp8_gemm_blockscaled_promote.
+ */
+#define FP8G_BLOCK32_LITERAL 33
+
 /* Source element types of fp8g_quantize_rows. */
 typedef enum { FP8G_IN_F32 = 0, FP8G_IN_BF16 = 1 } fp8g_in_dtype;
 
@@ -273,6 +282,24 @@ FP8G_API fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const
                                     const float *sfb, void *C, int out, int32_t a_fmt,
                                     int32_t b_fmt, const float *bias, int32_t act, int64_t M,
                                     int64_t N, int64_t K, cudaStream_t stream);
+/*
+ * 1x32 block-scaled GEMM for arbitrary fp32 scales [JAX-BW warp
+ * specialisation paragraph: the promotion warp role; the workloads' literal
+ * "fp32 scale = block amax/448"].  Same C = sum_kb sfa*sfb*partial_kb as
+ * fp8_gemm_blockscaled, but any finite fp32 scale (NaN and infinities
+ * propagate) rather than only powers of two: the tensor core computes each
+ * 32-wide K block's unscaled partial and CUDA-core warps scale and accumulate
+ * it in fp32 (fma(fl32(sfa*sfb), partial, acc)); ceiling well below the
+ * power-of-two path.  Operand formats, bias and activation as
+ * fp8_gemm_blockscaled_ex.  K % 128 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE);
+ * sfa, sfb 16-byte aligned.  Runs one kernel; allocates nothing.  Parity: the
+ * tolerance of fp8_gemm_blockscaled (plus the epilogue term when used).
+ */
+FP8G_API fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const float *sfa,
+                                         const float *sfb, void *C, int out, int32_t a_fmt,
+                                         int32_t b_fmt, const float *bias, int32_t act, int64_t M,
+                                         int64_t N, int64_t K, cudaStream_t stream);
+
 FP8G_API fp8g_status fp8_grouped_gemm_ex(const void *A, const void *B, const float *sfa,
                                 const float *sfb, void *C, int out, int32_t a_fmt, int32_t b_fmt,
                                 const float *bias, int32_t act, const int32_t *counts, int32_t E,
