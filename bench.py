@@ -42,6 +42,8 @@ WORKLOADS = {
     "tensor8192": dict(kind="tensor", M=8192, N=8192, K=8192, seed=3),
     # E4M3 activations x E5M2 weights, block-scaled (the mixed-format path)
     "mixed8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, b_fmt=1),
+    # literal fp32 block scales amax/448 (promotion GEMM)
+    "literal8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, literal=True),
 }
 METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
 
@@ -141,6 +143,8 @@ def make_inputs(wl: dict, device):
     else:
         w = synth.large_block(wl["M"], seed=wl["seed"])
         bs = 32
+    if wl.get("literal"):
+        bs = fp8g.FP8G_BLOCK32_LITERAL
     qa, sa = fp8g.quantize(w.A.to(device), bs, fmt=wl.get("a_fmt", 0))
     qb, sb = fp8g.quantize(w.B.to(device), bs, fmt=wl.get("b_fmt", 0))
     return w, dict(qa=qa, sa=sa, qb=qb, sb=sb)
@@ -164,6 +168,10 @@ def run_once(fp8g, wl, w, t, C, stream):
                               t["qa"].shape[0], None, None, stream)
     elif wl["kind"] == "tensor":
         fp8g.fp8_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"], wl["K"], stream)
+    elif wl.get("literal"):
+        fp8g.fp8_gemm_blockscaled_promote(t["qa"], t["qb"], t["sa"], t["sb"], C, out,
+                                          wl.get("a_fmt", 0), wl.get("b_fmt", 0), None,
+                                          fp8g.FP8G_ACT_NONE, wl["M"], wl["N"], wl["K"], stream)
     elif "a_fmt" in wl or "b_fmt" in wl:
         fp8g.fp8_gemm_blockscaled_fmt(t["qa"], t["qb"], t["sa"], t["sb"], C, out,
                                       wl.get("a_fmt", 0), wl.get("b_fmt", 0), wl["M"], wl["N"],
@@ -187,6 +195,8 @@ def launches_per_call(fp8g, wl) -> int:
         return 1
     if wl["kind"] == "grouped":
         return 2
+    if wl.get("literal"):
+        return 1
     return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
 
 
@@ -275,9 +285,13 @@ def oracle_inputs(wl, w):
                     B=qb.reshape(E, N, K)[e], sb=sb.reshape(E, N, K // 32)[e], block=True,
                     N=N, K=K, desc=f"rows of expert {e} (all {N} columns)")
     block = wl["kind"] != "tensor"
-    qfn = oracle.quantize_block32 if block else oracle.quantize_tensor
-    qa, sa = qfn(w.A.numpy(), wl.get("a_fmt", 0))
-    qb, sb = qfn(w.B.numpy(), wl.get("b_fmt", 0))
+    if wl.get("literal"):
+        qa, sa = oracle.quantize_block32(w.A.numpy(), wl.get("a_fmt", 0), literal=True)
+        qb, sb = oracle.quantize_block32(w.B.numpy(), wl.get("b_fmt", 0), literal=True)
+    else:
+        qfn = oracle.quantize_block32 if block else oracle.quantize_tensor
+        qa, sa = qfn(w.A.numpy(), wl.get("a_fmt", 0))
+        qb, sb = qfn(w.B.numpy(), wl.get("b_fmt", 0))
     return dict(A=qa, sa=sa, B=qb, sb=sb, block=block, N=wl["N"], K=wl["K"],
                 a_fmt=wl.get("a_fmt", 0), b_fmt=wl.get("b_fmt", 0),
                 desc=f"rows of A (all {wl['N']} columns)")
@@ -430,9 +444,10 @@ def main():
         "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"],
                    "formats": ["e4m3", "e5m2"][wl.get("a_fmt", 0)] + " x " +
                               ["e4m3", "e5m2"][wl.get("b_fmt", 0)],
-                   "scales": {"block": "1x32 along K, power of two",
+                   "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
+                              {"block": "1x32 along K, power of two",
                               "grouped": "1x32 along K, power of two",
-                              "tensor": "per tensor"}[wl["kind"]],
+                              "tensor": "per tensor"}[wl["kind"]]),
                    "out": w.out, "l2": f"inputs rotated over {copies} copies > 2x L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roof,

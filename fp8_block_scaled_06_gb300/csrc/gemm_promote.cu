@@ -43,12 +43,16 @@ constexpr int kPStage = kPA + kPB + kPSA + kPSB;
 constexpr int kPOffBar = kPStages * kPStage;
 // full[S], empty[S], pfull[NB], pempty[NB], drain
 constexpr int kPNumBars = 2 * kPStages + 2 * kPBufs + 1;
-constexpr int kPOffMisc = kPOffBar + kPNumBars * 8;
+// per promotion warp: its 32 columns' B scales of the current stage,
+// transposed to [K block][column] so a K block's 32 values are contiguous
+constexpr int kPOffT = (kPOffBar + kPNumBars * 8 + 15) / 16 * 16;  // float4 reads
+constexpr int kPOffMisc = kPOffT + kPEpiWarps * 4 * 32 * 4;
 constexpr int kPSmem = kPOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t kPTmemCols = kPBufs * kPBN;
 static_assert(kPSmem <= 232448, "shared memory over the per-CTA limit");
 static_assert(kPStage % 1024 == 0, "swizzled tiles need 1024-byte aligned stages");
 static_assert(kPTmemCols <= 512, "tensor memory over budget");
+static_assert(kPOffT % 16 == 0 && kPOffMisc % 16 == 0, "16-byte aligned scratch");
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int q = warp & 3;             // tensor-memory lane quarter: rows 32 q ..
         const int col0 = (ew >> 2) * 32;    // 32 columns of the 128
         const int r = q * 32 + lane;        // row in the tile
+        float *sbt = reinterpret_cast<float *>(smem + kPOffT) + ew * 4 * 32;
         uint32_t stage = 0, phase = 0, g = 0;
         for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
             int32_t pm, pn;
@@ -180,6 +185,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 const float *sa_s = reinterpret_cast<const float *>(smem + stage * kPStage + kPA + kPB);
                 const float *sb_s = sa_s + kBM * 4;
+                {
+                    // lane l: column col0 + l's 4 K blocks -> sbt[k][l]
+                    const float4 v = *reinterpret_cast<const float4 *>(sb_s + (col0 + lane) * 4);
+                    __syncwarp();  // the previous stage's reads of sbt are done
+                    sbt[0 * 32 + lane] = v.x;
+                    sbt[1 * 32 + lane] = v.y;
+                    sbt[2 * 32 + lane] = v.z;
+                    sbt[3 * 32 + lane] = v.w;
+                    __syncwarp();
+                }
 #pragma unroll 1
                 for (int k = 0; k < kBK / 32; ++k, ++g) {
                     const uint32_t buf = g % kPBufs;
@@ -197,10 +212,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar_pempty(buf));
                     const float sa = sa_s[r * 4 + k];
+                    const float4 *sbk = reinterpret_cast<const float4 *>(sbt + k * 32);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        acc[c] = __fmaf_rn(__fmul_rn(sa, sb_s[(col0 + c) * 4 + k]),
-                                           __uint_as_float(pv[c]), acc[c]);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 sb = sbk[c4];  // the same address in every lane: broadcast
+                        acc[4 * c4 + 0] = __fmaf_rn(__fmul_rn(sa, sb.x), __uint_as_float(pv[4 * c4 + 0]),
+                                                    acc[4 * c4 + 0]);
+                        acc[4 * c4 + 1] = __fmaf_rn(__fmul_rn(sa, sb.y), __uint_as_float(pv[4 * c4 + 1]),
+                                                    acc[4 * c4 + 1]);
+                        acc[4 * c4 + 2] = __fmaf_rn(__fmul_rn(sa, sb.z), __uint_as_float(pv[4 * c4 + 2]),
+                                                    acc[4 * c4 + 2]);
+                        acc[4 * c4 + 3] = __fmaf_rn(__fmul_rn(sa, sb.w), __uint_as_float(pv[4 * c4 + 3]),
+                                                    acc[4 * c4 + 3]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar_empty(stage));
