@@ -44,7 +44,7 @@ EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
-    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_blockscaled_promote",
+    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_blockscaled_promote", "fp8g_wait_selftest",
     "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
@@ -116,6 +116,8 @@ def load():
         lib.fp8_gemm_blockscaled_promote.restype = st
         lib.fp8_gemm_blockscaled_promote.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32,
                                                      i64, i64, i64, P]
+        lib.fp8g_wait_selftest.restype = st
+        lib.fp8g_wait_selftest.argtypes = [ctypes.c_uint32, P]
         lib.fp8g_quantize_rows.restype = st
         lib.fp8g_quantize_rows.argtypes = [P, i32, i64, i64, P, i64, i32, i32, P, P, P]
         lib.fp8_grouped_gemm_fmt.restype = st
@@ -280,6 +282,10 @@ def fp8g_quantize_rows(x, in_dtype: int, x_rows: int, cols: int, rows, n_rows: i
     _check(load().fp8g_quantize_rows(_ptr(x), int(in_dtype), x_rows, cols, _ptr(rows), n_rows,
                                      int(block), int(fmt), _ptr(q), _ptr(scales),
                                      _stream(stream)), "fp8g_quantize_rows")
+
+
+def fp8g_wait_selftest(timeout_us: int, stream=None):
+    _check(load().fp8g_wait_selftest(int(timeout_us), _stream(stream)), "fp8g_wait_selftest")
 
 
 def fp8_gemm_status(stream=None):

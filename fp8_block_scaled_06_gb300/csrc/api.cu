@@ -588,6 +588,15 @@ const char *fp8g_status_string(fp8g_status s) {
     return "unknown status";
 }
 
+fp8g_status fp8g_wait_selftest(uint32_t timeout_us, cudaStream_t stream) {
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return FP8G_ERR_INVALID_ARG;
+    DevInfo di;
+    const fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const cudaError_t e = launch_wait_selftest(di.status, (uint64_t)timeout_us * 1000ull, stream);
+    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
 void fp8g_set_wait_timeout_ms(uint32_t ms) {
     if (ms == 0) {
         g_timeout_ns.store(0, std::memory_order_relaxed);

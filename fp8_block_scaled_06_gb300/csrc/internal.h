@@ -70,6 +70,9 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                         const KernelChoice &kc, cudaStream_t stream);
 KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sms);
 
+// selftest.cu: one warp, one wait that runs out after timeout_ns
+cudaError_t launch_wait_selftest(unsigned int *status, uint64_t timeout_ns, cudaStream_t s);
+
 // gemm_promote.cu: arbitrary fp32 1x32 scales (maps.SA / maps.SB: the fp32
 // scale arrays, box 4 x 128); grid CTAs over 128 x 128 tiles.
 cudaError_t launch_gemm_promote(bool out_f32, const GemmMaps &maps, const GemmParams &p, int grid,

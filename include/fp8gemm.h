@@ -331,6 +331,17 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
  */
 FP8G_API fp8g_status fp8_gemm_status(cudaStream_t stream, int32_t *detail);
 
+/*
+ * Diagnostic (the source pages have no counterpart): launches a one-warp
+ * kernel that makes one mbarrier wait complete and then waits, with the same
+ * bounded-wait code as the GEMM kernels, on a barrier that nothing arrives at.
+ * After timeout_us microseconds (1 .. 10^7) that wait gives up and records
+ * FP8G_ERR_TIMEOUT with detail 0xDEAD in the status word, and the kernel
+ * returns.  Read it with fp8_gemm_status.  Shows on a live GPU that a wait
+ * which cannot complete ends in a host-visible error, not a hang.
+ */
+FP8G_API fp8g_status fp8g_wait_selftest(uint32_t timeout_us, cudaStream_t stream);
+
 /* Static English description of a status code. */
 FP8G_API const char *fp8g_status_string(fp8g_status status);
 
