@@ -279,8 +279,9 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
     const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
-    // 256-wide tiles take B's scales replicated for one 128x256b tensor-memory
-    // copy (4 KB per 256 rows and K step instead of 1 KB)
+    // single-CTA 256-wide tiles take B's scales replicated for one 128x256b
+    // tensor-memory copy (4 KB per 256 rows and K step instead of 1 KB); CTA
+    // pairs take plain 512-byte chunks (three warpx4 copies per K step)
     const bool repB = kc.BN == 256 && !kc.pair;
     const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (repB ? 4 : 1);
     void *ws = nullptr;

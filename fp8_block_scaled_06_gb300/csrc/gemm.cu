@@ -62,7 +62,7 @@ struct Cfg {
     // Packed UE8M0 scales per stage (4 K blocks per row): A's 128 rows (512 B,
     // one replicating 32x128b copy); B's rows: 128 -> 512 B the same way,
     // 256 -> 4 KB already replicated over the four lane quarters (one
-    // 128x256b copy; each copy instruction costs the MMA stream ~6%).
+    // 128x256b copy, issued by the scale-copy warp).
     static constexpr bool kRepB = kBlock && BN == 256;
     static constexpr int SFB_BYTES = kBlock ? (kRepB ? 4096 : BN * 4) : 0;
     static constexpr int CHUNK_BYTES = kBlock ? kBM * 4 + SFB_BYTES : 0;

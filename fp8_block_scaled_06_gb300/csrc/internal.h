@@ -104,7 +104,7 @@ struct PackArgs {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;
-    int32_t rep;  // B of CTA pairs: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
+    int32_t rep;  // B of single-CTA 256-wide tiles: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
 };
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
