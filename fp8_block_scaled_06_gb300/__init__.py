@@ -45,6 +45,7 @@ EXPORTS = (
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
     "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_blockscaled_promote", "fp8g_wait_selftest",
+    "fp8g_kernel_timing_begin", "fp8g_kernel_timing_end",
     "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
 )
@@ -116,6 +117,10 @@ def load():
         lib.fp8_gemm_blockscaled_promote.restype = st
         lib.fp8_gemm_blockscaled_promote.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32,
                                                      i64, i64, i64, P]
+        lib.fp8g_kernel_timing_begin.restype = st
+        lib.fp8g_kernel_timing_begin.argtypes = [i32]
+        lib.fp8g_kernel_timing_end.restype = st
+        lib.fp8g_kernel_timing_end.argtypes = [P, i32, P]
         lib.fp8g_wait_selftest.restype = st
         lib.fp8g_wait_selftest.argtypes = [ctypes.c_uint32, P]
         lib.fp8g_quantize_rows.restype = st
@@ -282,6 +287,18 @@ def fp8g_quantize_rows(x, in_dtype: int, x_rows: int, cols: int, rows, n_rows: i
     _check(load().fp8g_quantize_rows(_ptr(x), int(in_dtype), x_rows, cols, _ptr(rows), n_rows,
                                      int(block), int(fmt), _ptr(q), _ptr(scales),
                                      _stream(stream)), "fp8g_quantize_rows")
+
+
+def fp8g_kernel_timing_begin(n: int):
+    _check(load().fp8g_kernel_timing_begin(int(n)), "fp8g_kernel_timing_begin")
+
+
+def fp8g_kernel_timing_end(cap: int) -> list:
+    """GEMM-kernel durations (ms) of the calls recorded since begin."""
+    ms = (ctypes.c_float * max(int(cap), 1))()
+    n = ctypes.c_int32(0)
+    _check(load().fp8g_kernel_timing_end(ms, int(cap), ctypes.byref(n)), "fp8g_kernel_timing_end")
+    return [float(ms[i]) for i in range(n.value)]
 
 
 def fp8g_wait_selftest(timeout_us: int, stream=None):

@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -203,6 +204,31 @@ fp8g_status check_common(const void *A, const void *B, const void *C, int out, i
 
 }  // namespace
 
+// Kernel timing (fp8g_kernel_timing_begin / _end): events of the library
+// recorded on the call's stream right before and right after the GEMM
+// kernel's launch.
+std::mutex g_timing_mu;
+std::vector<cudaEvent_t> g_timing_start, g_timing_end;
+int32_t g_timing_n = 0;
+uint64_t g_timing_seq = 0;
+
+template <class F>
+cudaError_t timed_launch(cudaStream_t stream, F &&launch) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_timing_mu);
+        if (g_timing_n > 0) {
+            const int32_t i = (int32_t)(g_timing_seq++ % (uint64_t)g_timing_n);
+            e0 = g_timing_start[i];
+            e1 = g_timing_end[i];
+        }
+    }
+    if (e0 != nullptr && cudaEventRecord(e0, stream) != cudaSuccess) return cudaGetLastError();
+    const cudaError_t e = launch();
+    if (e == cudaSuccess && e1 != nullptr) return cudaEventRecord(e1, stream);
+    return e;
+}
+
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
@@ -263,13 +289,17 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     maps.SA = maps.A;
     maps.SB = maps.A;
     if (mode == kModeTensor) {
-        const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        const cudaError_t e = timed_launch(stream, [&] {
+            return launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        });
         return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
     }
     if (kc.split > 1) {
         // split-K (few output tiles): the GEMM converts its own scale chunks
         // from the fp32 scales (p.sa, p.sb; row stride p.sfc)
-        const cudaError_t e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        const cudaError_t e = timed_launch(stream, [&] {
+            return launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        });
         return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
     }
     // Block modes: pack the fp32 scales into UE8M0 chunks (a stream-ordered
@@ -315,7 +345,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
             e = cudaErrorInvalidValue;
     }
-    if (e == cudaSuccess) e = launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+    if (e == cudaSuccess)
+        e = timed_launch(stream, [&] { return launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream); });
     const cudaError_t ef = scratch != nullptr ? cudaSuccess : cudaFreeAsync(ws, stream);
     return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
 }
@@ -414,7 +445,8 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
                           CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB)) != FP8G_OK)
         return st;
     const int grid = (int)(p.T < di.num_sms ? p.T : di.num_sms);
-    const cudaError_t e = launch_gemm_promote(out == FP8G_OUT_F32, maps, p, grid, stream);
+    const cudaError_t e = timed_launch(
+        stream, [&] { return launch_gemm_promote(out == FP8G_OUT_F32, maps, p, grid, stream); });
     return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
@@ -587,6 +619,53 @@ const char *fp8g_status_string(fp8g_status s) {
         case FP8G_ERR_DEVICE: return "no usable sm_103 device";
     }
     return "unknown status";
+}
+
+fp8g_status fp8g_kernel_timing_begin(int32_t n) {
+    if (n < 1 || n > (1 << 20)) return FP8G_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (g_timing_n != 0) return FP8G_ERR_INVALID_ARG;  // already on
+    g_timing_start.assign((size_t)n, nullptr);
+    g_timing_end.assign((size_t)n, nullptr);
+    for (int32_t i = 0; i < n; ++i)
+        if (cudaEventCreate(&g_timing_start[i]) != cudaSuccess ||
+            cudaEventCreate(&g_timing_end[i]) != cudaSuccess) {
+            for (auto e : g_timing_start)
+                if (e) cudaEventDestroy(e);
+            for (auto e : g_timing_end)
+                if (e) cudaEventDestroy(e);
+            g_timing_start.clear();
+            g_timing_end.clear();
+            return FP8G_ERR_CUDA;
+        }
+    g_timing_n = n;
+    g_timing_seq = 0;
+    return FP8G_OK;
+}
+
+fp8g_status fp8g_kernel_timing_end(float *ms, int32_t cap, int32_t *count) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (g_timing_n == 0) return FP8G_ERR_INVALID_ARG;
+    const int32_t rec = (int32_t)(g_timing_seq < (uint64_t)g_timing_n ? g_timing_seq : g_timing_n);
+    fp8g_status st = FP8G_OK;
+    int32_t got = 0;
+    for (int32_t i = 0; i < rec && i < cap && ms != nullptr; ++i) {
+        float t = 0.0f;
+        if (cudaEventSynchronize(g_timing_end[i]) != cudaSuccess ||
+            cudaEventElapsedTime(&t, g_timing_start[i], g_timing_end[i]) != cudaSuccess) {
+            st = FP8G_ERR_CUDA;
+            break;
+        }
+        ms[got++] = t;
+    }
+    if (count) *count = got;
+    for (auto e : g_timing_start) cudaEventDestroy(e);
+    for (auto e : g_timing_end) cudaEventDestroy(e);
+    g_timing_start.clear();
+    g_timing_end.clear();
+    g_timing_n = 0;
+    g_timing_seq = 0;
+    return st;
 }
 
 fp8g_status fp8g_wait_selftest(uint32_t timeout_us, cudaStream_t stream) {

@@ -332,6 +332,24 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
 FP8G_API fp8g_status fp8_gemm_status(cudaStream_t stream, int32_t *detail);
 
 /*
+ * Kernel timing (the source pages have no counterpart; for benchmarks).
+ * fp8g_kernel_timing_begin(n) creates n pairs of CUDA events on the current
+ * device; each following GEMM call (any GEMM entry point, any stream or host
+ * thread) records pair i on its stream immediately before launching its GEMM
+ * kernel and immediately after, for its first n calls (i = 0, 1, ...).
+ * fp8g_kernel_timing_end(ms, cap, count) waits for the recorded calls,
+ * writes their GEMM-kernel durations in milliseconds (without the scale
+ * packing that block calls launch first) to ms[0 .. *count), frees the events
+ * and turns the recording off.  Recording costs each call two stream
+ * operations and keeps the GEMM's prologue from overlapping the packing
+ * kernel, so measure throughput with the recording off.
+ * Errors: FP8G_ERR_INVALID_ARG (n outside 1 .. 2^20, begin while on, end
+ * while off), FP8G_ERR_CUDA.
+ */
+FP8G_API fp8g_status fp8g_kernel_timing_begin(int32_t n);
+FP8G_API fp8g_status fp8g_kernel_timing_end(float *ms, int32_t cap, int32_t *count);
+
+/*
  * Diagnostic (the source pages have no counterpart): launches a one-warp
  * kernel that makes one mbarrier wait complete and then waits, with the same
  * bounded-wait code as the GEMM kernels, on a barrier that nothing arrives at.

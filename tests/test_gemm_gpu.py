@@ -358,3 +358,30 @@ def test_block_single_cta_256_tiles():
     pj = np.concatenate([rng.integers(0, N, 4096), [N - 1, 0, 255, 256]])
     ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16)
     assert_within(C[pi, pj], ref, bound, "block single-CTA 256-wide")
+
+
+def test_kernel_timing_hook():
+    """The library's kernel timing records one duration per GEMM call, each
+    shorter than the whole call (which also packs the scales)."""
+    M = N = K = 2048
+    A = synth.normal((M, K), seed=71)
+    B = synth.normal((N, K), seed=72)
+    qa, sa, _, _ = quant_both(A, 32)
+    qb, sb, _, _ = quant_both(B, 32)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8g_kernel_timing_begin(4)
+    with pytest.raises(fp8g.Fp8gError):
+        fp8g.fp8g_kernel_timing_begin(4)                 # already recording
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(6):
+        fp8g.fp8_gemm_blockscaled(qa, qb, sa, sb, C, 0, M, N, K)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = fp8g.fp8g_kernel_timing_end(8)
+    assert len(ms) == 4 and all(0 < t for t in ms)
+    assert sum(ms) < e0.elapsed_time(e1)
+    assert fp8g.fp8_gemm_status()[0] == 0
+    with pytest.raises(fp8g.Fp8gError):
+        fp8g.fp8g_kernel_timing_end(1)                   # not recording
