@@ -43,6 +43,7 @@ OUT_BF16 = 0
 OUT_F32 = 1
 E4M3 = 0
 E5M2 = 1
+E2M1 = 2
 ACT_NONE = 0
 ACT_RELU = 1
 ACT_GELU = 2
@@ -78,6 +79,11 @@ def _L():
             lib.oracle_e5m2_decode.restype = ctypes.c_double
             lib.oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
             lib.oracle_e5m2_table.argtypes = [P]
+            lib.oracle_e2m1_decode.restype = ctypes.c_double
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_table.argtypes = [P]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
             lib.oracle_e5m2_encode.restype = ctypes.c_uint8
             lib.oracle_e5m2_encode.argtypes = [ctypes.c_float]
             lib.oracle_quantize_tensor_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
@@ -160,6 +166,20 @@ def e5m2_table() -> np.ndarray:
 
 def e5m2_encode(y: float) -> int:
     return int(_L().oracle_e5m2_encode(float(np.float32(y))))
+
+
+def e2m1_decode(code: int) -> float:
+    return float(_L().oracle_e2m1_decode(int(code) & 0xFF))
+
+
+def e2m1_table() -> np.ndarray:
+    out = np.zeros(256, dtype=np.float64)
+    _L().oracle_e2m1_table(_p(out))
+    return out
+
+
+def e2m1_encode(y: float) -> int:
+    return int(_L().oracle_e2m1_encode(float(np.float32(y))))
 
 
 def bf16_round(x: float) -> float:

@@ -17,7 +17,11 @@
  *     FP8 among the fifth-generation tensor core's types): 1 sign, 5 exponent
  *     bits (bias 15), 2 mantissa bits, with infinities and NaNs in the top
  *     binade (the IEEE-style layout); largest finite 57344.  Operands of a
- *     GEMM may mix the two formats.
+ *     GEMM may mix the formats.
+ *   - E2M1 (FP4, the microscaling element format of the MXFP4 variant the
+ *     Triton tutorial ch. 12 lists beside MXFP8): 1 sign, 2 exponent bits
+ *     (bias 1), 1 mantissa bit, values 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
+ *     infinities or NaNs.  Held one code per byte (low four bits).
  *   - Quantisation x -> RNE_satfinite(fl32(x / s)) with a per-tensor scale
  *     s = fl32(amax / 448) or a 1x32 block scale along K equal to the smallest
  *     power of two >= amax / 448 (the microscaling paragraph of the JAX/Blackwell
@@ -102,6 +106,21 @@ ORACLE_EXPORT void oracle_e5m2_table(double *out256) {
     for (int c = 0; c < 256; ++c) out256[c] = oracle_e5m2_decode((uint8_t)c);
 }
 
+/* Value of an E2M1 code in the low four bits of a byte (the high four bits
+ * are ignored): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit.
+ * Exponent field 0 is subnormal (m * 0.5); largest value 1.5 * 2^2 = 6. */
+ORACLE_EXPORT double oracle_e2m1_decode(uint8_t code) {
+    int s = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+ORACLE_EXPORT void oracle_e2m1_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e2m1_decode((uint8_t)c);
+}
+
 /* Round a finite, non-negative real y to the grid of an FP8 format with
  * `mbits` mantissa bits and exponent bias `bias` (normal binades from 2^(1 -
  * bias) up; below that the subnormal quantum 2^(1 - bias - mbits)), with
@@ -154,13 +173,27 @@ ORACLE_EXPORT uint8_t oracle_e5m2_encode(float y) {
     return (uint8_t)(sign | fp8_mag_code(a, 2, 15, 57344.0));
 }
 
-/* FP8 formats of the quantisers and GEMM operands */
-enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1 };
+/* E2M1 code of the fp32 value y: RNE, satfinite (to +-6, infinities too),
+ * NaN -> 0x07 (E2M1 has no NaN; the library's quantiser does the same), -0 ->
+ * 0x08.  One code per byte, high four bits zero. */
+ORACLE_EXPORT uint8_t oracle_e2m1_encode(float y) {
+    if (isnan(y)) return 0x07;
+    uint8_t sign = signbit(y) ? 0x08 : 0x00;
+    double a = fabs((double)y);
+    if (isinf(a)) return (uint8_t)(sign | 0x07);
+    return (uint8_t)(sign | fp8_mag_code(a, 1, 1, 6.0));
+}
+
+/* Element formats of the quantisers and GEMM operands */
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1, ORACLE_E2M1 = 2 };
 
 static uint8_t encode_fmt(float y, int fmt) {
+    if (fmt == ORACLE_E2M1) return oracle_e2m1_encode(y);
     return fmt == ORACLE_E5M2 ? oracle_e5m2_encode(y) : oracle_e4m3_encode(y);
 }
-static double fmt_max(int fmt) { return fmt == ORACLE_E5M2 ? 57344.0 : 448.0; }
+static double fmt_max(int fmt) {
+    return fmt == ORACLE_E2M1 ? 6.0 : fmt == ORACLE_E5M2 ? 57344.0 : 448.0;
+}
 
 /* ------------------------------------------------------------------ */
 /* bf16 rounding                                                       */
@@ -361,15 +394,16 @@ typedef struct {
     int act;
 } gemm_job;
 
-static double dec_e4m3[256], dec_e5m2[256];
+static double dec_e4m3[256], dec_e5m2[256], dec_e2m1[256];
 static pthread_once_t dec_once = PTHREAD_ONCE_INIT;
 static void fill_tables(void) {
     oracle_e4m3_table(dec_e4m3);
     oracle_e5m2_table(dec_e5m2);
+    oracle_e2m1_table(dec_e2m1);
 }
 static const double *table_of(int fmt) {
     pthread_once(&dec_once, fill_tables);
-    return fmt == ORACLE_E5M2 ? dec_e5m2 : dec_e4m3;
+    return fmt == ORACLE_E2M1 ? dec_e2m1 : fmt == ORACLE_E5M2 ? dec_e5m2 : dec_e4m3;
 }
 
 /* One output element.  Block mode:
