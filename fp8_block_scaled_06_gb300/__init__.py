@@ -31,6 +31,7 @@ FP8G_OUT_BF16 = 0
 FP8G_OUT_F32 = 1
 FP8G_E4M3 = 0
 FP8G_E5M2 = 1
+FP8G_E2M1 = 2
 FP8G_BLOCK32_LITERAL = 33
 FP8G_IN_F32 = 0
 FP8G_IN_BF16 = 1
@@ -329,12 +330,14 @@ def fp8g_version() -> int:
 # ABI call above.
 
 def quantize(x, block: int = 32, stream=None, fmt: int = FP8G_E4M3):
-    """fp32 CUDA tensor [rows, cols] -> (uint8 codes, fp32 scales) in format fmt."""
+    """fp32 CUDA tensor [rows, cols] -> (uint8 codes, fp32 scales) in format fmt
+    (E2M1: two codes per byte, codes [rows, cols/2])."""
     import torch
     assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2
     x = x.contiguous()
     rows, cols = x.shape
-    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    qcols = cols // 2 if fmt == FP8G_E2M1 else cols
+    q = torch.empty((rows, qcols), dtype=torch.uint8, device=x.device)
     if block != 0:
         s = torch.empty((rows, cols // 32), dtype=torch.float32, device=x.device)
     else:

@@ -111,11 +111,11 @@ fp8g_status device_info(DevInfo &di) {
 // ------------------------------------------------------------ tensor maps
 struct TmapKey {
     const void *ptr;
-    int rank, dtype, esize, swizzle, dev;
+    int rank, dtype, ebits, swizzle, dev;
     uint64_t dims[3];
     uint32_t box[3];
     bool operator==(const TmapKey &o) const {
-        return ptr == o.ptr && rank == o.rank && dtype == o.dtype && esize == o.esize &&
+        return ptr == o.ptr && rank == o.rank && dtype == o.dtype && ebits == o.ebits &&
                swizzle == o.swizzle && dev == o.dev && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
                std::memcmp(box, o.box, sizeof box) == 0;
     }
@@ -131,15 +131,15 @@ TmapEntry g_cache[kCacheSize];
 int g_cache_next = 0;
 
 // Dense row-major tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost,
-// contiguous), element size esize bytes, zero fill out of bounds.
-fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int esize, int rank,
+// contiguous), element size ebits bits, zero fill out of bounds.
+fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int ebits, int rank,
                         const uint64_t *dims, const uint32_t *box, CUtensorMapSwizzle swz, int dev,
                         CUtensorMap &out) {
     TmapKey key{};
     key.ptr = ptr;
     key.rank = rank;
     key.dtype = (int)dtype;
-    key.esize = esize;
+    key.ebits = ebits;
     key.swizzle = (int)swz;
     key.dev = dev;
     for (int i = 0; i < rank; ++i) {
@@ -154,13 +154,13 @@ fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int esize, i
         }
     cuuint64_t gdim[3], gstride[2];
     cuuint32_t bdim[3], estr[3];
-    uint64_t stride = (uint64_t)esize;
+    uint64_t stride_bits = (uint64_t)ebits;
     for (int i = 0; i < rank; ++i) {
         gdim[i] = dims[i];
         bdim[i] = box[i];
         estr[i] = 1;
-        if (i > 0) gstride[i - 1] = stride;
-        stride *= dims[i];
+        if (i > 0) gstride[i - 1] = stride_bits / 8;
+        stride_bits *= dims[i];
     }
     CUtensorMap m;
     const CUresult r = g_encode(&m, dtype, (cuuint32_t)rank, const_cast<void *>(ptr), gdim, gstride,
@@ -177,14 +177,41 @@ fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int esize, i
     return FP8G_OK;
 }
 
-// E4M3 operand: 128-byte swizzle (the tcgen05 K-major SW128 layout).
-fp8g_status tmap_u8(const void *ptr, int rank, const uint64_t *dims, const uint32_t *box, int dev,
-                    CUtensorMap &out) {
-    return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rank, dims, box,
+// Operand tile map, 128-byte swizzle (the tcgen05 K-major SW128 layout).
+// dims / box count elements.  FP8: one byte per element in memory and in
+// shared memory.  E2M1: two codes per byte in memory (the first in the low
+// nibble); the 16U4_ALIGN16B load widens every 16 codes (8 bytes) to a
+// 16-byte slot of shared memory, the 8 data bytes followed by 8 unused ones,
+// which is how kind::f8f6f4 / mxf8f6f4 MMAs read 4-bit operands, so a tile
+// takes the same shared memory as an FP8 tile of the same shape; the load
+// counts only the packed bytes (half of that) toward the stage's mbarrier.
+fp8g_status tmap_operand(const void *ptr, int fmt, int rank, const uint64_t *dims,
+                         const uint32_t *box, int dev, CUtensorMap &out) {
+    if (fmt == FP8G_E2M1)
+        return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, rank, dims, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
+    return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 8, rank, dims, box,
                        CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_fmt(int f) { return f == FP8G_E4M3 || f == FP8G_E5M2 || f == FP8G_E2M1; }
+
+// The MMA instruction descriptor's A / B type field (kind::f8f6f4 and
+// kind::mxf8f6f4): E4M3 0, E5M2 1, E2M1 5.
+uint32_t mma_type(int f) { return f == FP8G_E2M1 ? 5u : (uint32_t)f; }
+
+// Packed E2M1 operands: the 16U4_ALIGN16B tile map wants K a multiple of 128
+// and the operand's base 32-byte aligned (its row stride, K / 2 bytes, is
+// then a multiple of 64).
+fp8g_status check_e2m1(const void *A, const void *B, int a_fmt, int b_fmt, int64_t K) {
+    if (a_fmt != FP8G_E2M1 && b_fmt != FP8G_E2M1) return FP8G_OK;
+    if (K % 128 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if ((a_fmt == FP8G_E2M1 && !aligned(A, 32)) || (b_fmt == FP8G_E2M1 && !aligned(B, 32)))
+        return FP8G_ERR_ALIGNMENT;
+    return FP8G_OK;
+}
 
 constexpr int64_t kMaxDim = (int64_t)1 << 31;
 
@@ -234,13 +261,15 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt,
                      const float *bias, int act, const int32_t *c_row_of, int64_t c_rows) {
-    if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
+    if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt))
         return FP8G_ERR_INVALID_ARG;
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
         return FP8G_ERR_INVALID_ARG;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
+    fp8g_status st = check_e2m1(M > 0 ? A : B, B, M > 0 ? a_fmt : b_fmt, b_fmt, K);
+    if (st != FP8G_OK) return st;
     DevInfo di;
-    fp8g_status st = device_info(di);
+    st = device_info(di);
     if (st != FP8G_OK) return st;
     const KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
     GemmParams p{};
@@ -263,28 +292,32 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.tile_map_out = tile_map_out;
     p.status = di.status;
     p.timeout_ns = timeout_ns();
-    p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
+    p.ab_fmt = (mma_type(a_fmt) << 7) | (mma_type(b_fmt) << 10);
+    p.a_e2m1 = a_fmt == FP8G_E2M1;
+    p.b_e2m1 = b_fmt == FP8G_E2M1;
     p.bias = bias;
     p.act = act;
     p.c_row_of = c_row_of;
     p.c_rows = c_rows;
 
     GemmMaps maps;
-    const int64_t rows_a = M > 0 ? M : 1;  // grouped with zero rows: A is never read
+    // grouped with zero rows: A is never read (a one-row map over B stands in)
+    const int64_t rows_a = M > 0 ? M : 1;
     const void *a_ptr = M > 0 ? A : B;
+    const int a_map_fmt = M > 0 ? a_fmt : b_fmt;
     {
         const uint64_t dA[2] = {(uint64_t)K, (uint64_t)rows_a};
         const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
-        if ((st = tmap_u8(a_ptr, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
+        if ((st = tmap_operand(a_ptr, a_map_fmt, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
     }
     if (mode == kModeGrouped) {
         const uint64_t dB[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
         const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.b_rows, 1u};
-        if ((st = tmap_u8(B, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        if ((st = tmap_operand(B, b_fmt, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     } else {
         const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
         const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
-        if ((st = tmap_u8(B, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        if ((st = tmap_operand(B, b_fmt, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     }
     maps.SA = maps.A;
     maps.SB = maps.A;
@@ -339,9 +372,9 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         const uint32_t bSA[2] = {128u, 1u};
         const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB};
         const uint32_t bSB[2] = {128u, 2u};  // 1 KB: the two 128-row chunks of a 256-row tile
-        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSA, bSA,
+        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
-            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 2, dSB, bSB,
+            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSB, bSB,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
             e = cudaErrorInvalidValue;
     }
@@ -401,12 +434,13 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     fp8g_status st = check_common(A, B, C, out, M, N, K);
     if (st != FP8G_OK) return st;
     if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
-    if ((a_fmt != FP8G_E4M3 && a_fmt != FP8G_E5M2) || (b_fmt != FP8G_E4M3 && b_fmt != FP8G_E5M2))
+    if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt))
         return FP8G_ERR_INVALID_ARG;
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
         return FP8G_ERR_INVALID_ARG;
     // the scales' rows (K/32 fp32) are TMA rows: 16-byte multiples
     if (K % 128 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if ((st = check_e2m1(A, B, a_fmt, b_fmt, K)) != FP8G_OK) return st;
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
     DevInfo di;
@@ -426,7 +460,9 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     p.C = C;
     p.status = di.status;
     p.timeout_ns = timeout_ns();
-    p.ab_fmt = ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10);
+    p.ab_fmt = (mma_type(a_fmt) << 7) | (mma_type(b_fmt) << 10);
+    p.a_e2m1 = a_fmt == FP8G_E2M1;
+    p.b_e2m1 = b_fmt == FP8G_E2M1;
     p.bias = bias;
     p.act = act;
     GemmMaps maps;
@@ -436,12 +472,12 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     const uint64_t dSA[2] = {(uint64_t)(K / 32), (uint64_t)M};
     const uint64_t dSB[2] = {(uint64_t)(K / 32), (uint64_t)N};
     const uint32_t bS[2] = {4u, 128u};  // 4 K blocks x 128 rows of fp32
-    if ((st = tmap_u8(A, 2, dA, box, di.dev, maps.A)) != FP8G_OK) return st;
-    if ((st = tmap_u8(B, 2, dB, box, di.dev, maps.B)) != FP8G_OK) return st;
-    if ((st = tmap_encode(sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dSA, bS,
+    if ((st = tmap_operand(A, a_fmt, 2, dA, box, di.dev, maps.A)) != FP8G_OK) return st;
+    if ((st = tmap_operand(B, b_fmt, 2, dB, box, di.dev, maps.B)) != FP8G_OK) return st;
+    if ((st = tmap_encode(sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, 2, dSA, bS,
                           CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA)) != FP8G_OK)
         return st;
-    if ((st = tmap_encode(sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dSB, bS,
+    if ((st = tmap_encode(sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, 2, dSB, bS,
                           CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB)) != FP8G_OK)
         return st;
     const int grid = (int)(p.T < di.num_sms ? p.T : di.num_sms);
@@ -569,7 +605,7 @@ fp8g_status fp8g_quantize_rows(const void *x, int32_t in_dtype, int64_t x_rows, 
                                const int32_t *rows, int64_t n_rows, int32_t block, int32_t fmt,
                                uint8_t *q, float *scales, cudaStream_t stream) {
     if (x == nullptr || q == nullptr || scales == nullptr) return FP8G_ERR_INVALID_ARG;
-    if (fmt != FP8G_E4M3 && fmt != FP8G_E5M2) return FP8G_ERR_INVALID_ARG;
+    if (!valid_fmt(fmt)) return FP8G_ERR_INVALID_ARG;
     if (in_dtype != FP8G_IN_F32 && in_dtype != FP8G_IN_BF16) return FP8G_ERR_INVALID_ARG;
     if (x_rows < 1 || n_rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
     if (rows == nullptr && n_rows > x_rows) return FP8G_ERR_INVALID_ARG;

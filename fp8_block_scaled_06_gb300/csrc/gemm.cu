@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
     constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES : C_::TX_BYTES;
+    const uint32_t tx_bytes = kTxBytes - (p.a_e2m1 ? C_::A_BYTES / 2 : 0) -
+                              (p.b_e2m1 ? C_::B_BYTES / 2 : 0);
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA tiles need 1024-byte alignment in the shared window
     const uint32_t raw_base = ptx::smem_addr(smem_raw);
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = bar_full(stage);
-                    ptx::mbar_arrive_expect_tx(fb, kTxBytes);
+                    ptx::mbar_arrive_expect_tx(fb, tx_bytes);
                     ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb, kb * kBK,
                                      ti.row0);
                     if constexpr (MODE == kModeGrouped)

@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Both CTAs' copies complete on the even CTA's full barrier (TMA
         // cta_group::2), which expects both halves; the odd CTA does not arrive.
         if (lane == 0) {
+            const uint32_t tx_bytes = PC::TX - (p.a_e2m1 ? kA / 2 : 0) - (p.b_e2m1 ? kB / 2 : 0);
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {
                 const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_empty(stage), phase ^ 1u, abort_flag, p, 0 * 256 + stage))
                         goto roles_done;
                     const uint32_t fb = leader ? bar_full(stage) : ptx::map_shared(bar_full(stage), 0);
-                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * PC::TX);
+                    if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * tx_bytes);
                     ptx::tma_load_2d_pair(sbase + PC::OFF_A + stage * kA, &tmA, fb, kb * kBK, row0);
                     if constexpr (MODE == kModeGrouped)
                         ptx::tma_load_3d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0,

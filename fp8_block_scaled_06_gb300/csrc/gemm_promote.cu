@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) {
         // ===== TMA producer =====
         if (lane == 0) {
+            const uint32_t tx_bytes =
+                kPStage - (p.a_e2m1 ? kPA / 2 : 0) - (p.b_e2m1 ? kPB / 2 : 0);
             uint32_t stage = 0, phase = 0;
             for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
                 int32_t pm, pn;
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         goto roles_done;
                     const uint32_t fb = bar_full(stage);
                     const uint32_t st = sbase + stage * kPStage;
-                    ptx::mbar_arrive_expect_tx(fb, kPStage);
+                    ptx::mbar_arrive_expect_tx(fb, tx_bytes);
                     ptx::tma_load_2d(st, &tmA, fb, kb * kBK, row0);
                     ptx::tma_load_2d(st + kPA, &tmB, fb, kb * kBK, n0);
                     ptx::tma_load_2d(st + kPA + kPB, &tmSA, fb, kb * 4, row0);

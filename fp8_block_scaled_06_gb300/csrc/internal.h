@@ -42,6 +42,10 @@ struct GemmParams {
     const uint8_t *sfb_pk;
     int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
     uint32_t ab_fmt;       // operand formats as MMA instruction-descriptor bits (A: 7-9, B: 10-12)
+    // Packed E2M1 operands (two codes per byte): their tile loads deliver the
+    // packed byte count, half a tile's shared-memory footprint, so each stage
+    // expects that many fewer transaction bytes.
+    int32_t a_e2m1, b_e2m1;
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
     const int32_t *c_row_of;  // grouped scatter: row of C for routed row r (null: r)

@@ -1,7 +1,9 @@
-// Operand quantiser: fp32 -> FP8 codes + fp32 scales (data preparation for
-// the GEMM entry points).  Formats: E4M3 (largest finite fmax = 448) and E5M2
-// (fmax = 57344), the two FP8 formats of the format paragraph of "Optimizing
-// FP8 GEMM kernels in JAX with Triton for Blackwell GPUs".
+// Operand quantiser: fp32 -> FP8 / FP4 codes + fp32 scales (data preparation
+// for the GEMM entry points).  Formats: E4M3 (largest finite fmax = 448) and
+// E5M2 (fmax = 57344), the two FP8 formats of the format paragraph of
+// "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell GPUs", and
+// E2M1 (fmax = 6, two codes per byte, the first in the low nibble), the FP4
+// element of the micro-scaling formats of the Triton tutorial ch. 12, 12.6.1.
 //
 // Per-tensor: s = fl32(amax / fmax) over the non-NaN |x| (1 if that is 0).
 // 1x32 block along the contiguous axis: s = the smallest power of two with
@@ -10,57 +12,94 @@
 // the same page and the MXFP8 micro-scaling of the Triton tutorial ch. 12,
 // 12.6.1; its "fine-grained quantisation" advice against FP8 underflow is the
 // reason for the block form.  q = FP8(fl32(x / s)), round to nearest even,
-// saturating (cvt ... satfinite), NaN -> 0x7F (a NaN code in both formats).
+// saturating (cvt ... satfinite), NaN -> 0x7F (a NaN code in both FP8
+// formats; E2M1 has none and takes +6).
 //
 // The source is fp32 or bf16 (activations; widened exactly), and the output
 // rows may gather source rows through an index list (the routing step of the
 // MoE paragraph of the JAX/Blackwell page: tokens copied into expert order),
 // so that gather, scale and quantisation take one pass over HBM.
 //
-// HBM-bound elementwise kernels: 16-byte loads, 8-byte stores, a grid of a
-// few CTAs per SM striding over the output.
+// HBM-bound elementwise kernels: 16-byte loads, 8-byte (E2M1: 4-byte)
+// stores, a grid of a few CTAs per SM striding over the output.
 #include "internal.h"
 
 namespace fp8g {
 
 namespace {
 
-// FMT 0: E4M3, 1: E5M2.  Largest finite value 1.75 * 2^kEmax[FMT].
+// FMT 0: E4M3, 1: E5M2, 2: E2M1 (FP4, two codes per byte).  Largest finite
+// value kMax = mmax * 2^kEmax; kMantOver is the fp32 mantissa field above
+// which a value m 2^E (1 <= m < 2) exceeds mmax * 2^E (mmax = 1.75 or 1.5).
 template <int FMT>
 struct Fp8Fmt;
 template <>
 struct Fp8Fmt<0> {
     static constexpr float kMax = 448.0f;
     static constexpr int kEmax = 8;
+    static constexpr uint32_t kMantOver = 0x600000u;
 };
 template <>
 struct Fp8Fmt<1> {
     static constexpr float kMax = 57344.0f;
     static constexpr int kEmax = 15;
+    static constexpr uint32_t kMantOver = 0x600000u;
+};
+template <>
+struct Fp8Fmt<2> {
+    static constexpr float kMax = 6.0f;
+    static constexpr int kEmax = 2;
+    static constexpr uint32_t kMantOver = 0x400000u;
 };
 
-// Two fp32 values -> two FP8 bytes (lo at the lower address).
+// Two fp32 values -> their codes, lo first: FP8 two bytes (lo at the lower
+// address), E2M1 one byte (lo in the low nibble).  NaN, which E2M1 cannot
+// hold, becomes code 7 (+6) there.
 template <int FMT>
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
-    uint16_t r;
-    if constexpr (FMT == 0)
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    else
-        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    uint32_t v = r;
+    uint32_t v;
+    if constexpr (FMT == 2) {
+        asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+            : "=r"(v)
+            : "f"(hi), "f"(lo));
+        if (isnan(lo)) v = (v & 0xF0u) | 0x07u;
+        if (isnan(hi)) v = (v & 0x0Fu) | 0x70u;
+        return v;
+    } else {
+        uint16_t r;
+        if constexpr (FMT == 0)
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        else
+            asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        v = r;
+    }
     if (isnan(lo)) v = (v & 0xFF00u) | 0x7Fu;
     if (isnan(hi)) v = (v & 0x00FFu) | 0x7F00u;
     return v;
 }
 
-// 8 values -> 8 codes packed little-endian.
+// Codes of four values, first value lowest.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x4(float x0, float x1, float x2, float x3) {
+    return fp8x2<FMT>(x0, x1) | (fp8x2<FMT>(x2, x3) << (FMT == 2 ? 8 : 16));
+}
+
+// Store the codes of group g (values 8g .. 8g+7 of the output): 8 bytes
+// (FP8) or 4 bytes (E2M1) at g times that size.
+template <int FMT>
+__device__ __forceinline__ void store8(uint8_t *q, int64_t g, uint2 o) {
+    if constexpr (FMT == 2)
+        reinterpret_cast<uint32_t *>(q)[g] = o.x | (o.y << 16);
+    else
+        reinterpret_cast<uint2 *>(q)[g] = o;
+}
+
+// 8 values -> their codes (first four in .x), for store8.
 template <int FMT>
 __device__ __forceinline__ uint2 quant8(const float4 a, const float4 b, float s) {
     uint2 o;
-    o.x = fp8x2<FMT>(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)) |
-          (fp8x2<FMT>(__fdiv_rn(a.z, s), __fdiv_rn(a.w, s)) << 16);
-    o.y = fp8x2<FMT>(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)) |
-          (fp8x2<FMT>(__fdiv_rn(b.z, s), __fdiv_rn(b.w, s)) << 16);
+    o.x = fp8x4<FMT>(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s), __fdiv_rn(a.z, s), __fdiv_rn(a.w, s));
+    o.y = fp8x4<FMT>(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s), __fdiv_rn(b.z, s), __fdiv_rn(b.w, s));
     return o;
 }
 
@@ -87,7 +126,7 @@ __device__ __forceinline__ float pow2_scale(float amax) {
         if (ex == 0) {
             e = -126;
         } else {
-            e = (ex - 127) - Fp8Fmt<FMT>::kEmax + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+            e = (ex - 127) - Fp8Fmt<FMT>::kEmax + ((bits & 0x7FFFFFu) > Fp8Fmt<FMT>::kMantOver ? 1 : 0);
         }
         e = max(-126, min(127, e));
     }
@@ -148,10 +187,8 @@ template <int FMT>
 __device__ __forceinline__ uint2 quant8_pow2(const float4 a, const float4 b, float s) {
     const float r = __frcp_rn(s);
     uint2 o;
-    o.x = fp8x2<FMT>(__fmul_rn(a.x, r), __fmul_rn(a.y, r)) |
-          (fp8x2<FMT>(__fmul_rn(a.z, r), __fmul_rn(a.w, r)) << 16);
-    o.y = fp8x2<FMT>(__fmul_rn(b.x, r), __fmul_rn(b.y, r)) |
-          (fp8x2<FMT>(__fmul_rn(b.z, r), __fmul_rn(b.w, r)) << 16);
+    o.x = fp8x4<FMT>(__fmul_rn(a.x, r), __fmul_rn(a.y, r), __fmul_rn(a.z, r), __fmul_rn(a.w, r));
+    o.y = fp8x4<FMT>(__fmul_rn(b.x, r), __fmul_rn(b.y, r), __fmul_rn(b.z, r), __fmul_rn(b.w, r));
     return o;
 }
 
@@ -192,8 +229,9 @@ __global__ void __launch_bounds__(kQThreads) quant_block32_kernel(RowMap m, int6
                     sc = pow2_scale<FMT>(am);
                 }
                 if (c < gpr) {
-                    reinterpret_cast<uint2 *>(q)[out0 + c] =
-                        LITERAL ? quant8<FMT>(a[u], b[u], sc) : quant8_pow2<FMT>(a[u], b[u], sc);
+                    store8<FMT>(q, out0 + c,
+                                LITERAL ? quant8<FMT>(a[u], b[u], sc)
+                                        : quant8_pow2<FMT>(a[u], b[u], sc));
                     if ((c & 3) == 0) scales[(out0 + c) >> 2] = sc;
                 }
             }
@@ -246,7 +284,7 @@ __global__ void __launch_bounds__(kQThreads) quant_tensor_kernel(RowMap m, int64
         for (int64_t c = threadIdx.x; c < gpr; c += kQThreads) {
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
             if (ok) load8<BF16>(m.x, sr * m.cols + c * 8, a, b);
-            reinterpret_cast<uint2 *>(q)[r * gpr + c] = quant8<FMT>(a, b, s);
+            store8<FMT>(q, r * gpr + c, quant8<FMT>(a, b, s));
         }
     }
 }
@@ -289,6 +327,9 @@ cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int
                                  uint8_t *q, float *scales, unsigned int *status, int num_sms,
                                  cudaStream_t s) {
     const RowMap m{x, rows, x_rows, cols, status};
+    if (fmt == 2)
+        return in_bf16 ? launch_rows<2, true>(m, n_rows, block, q, scales, num_sms, s)
+                       : launch_rows<2, false>(m, n_rows, block, q, scales, num_sms, s);
     if (fmt == 1)
         return in_bf16 ? launch_rows<1, true>(m, n_rows, block, q, scales, num_sms, s)
                        : launch_rows<1, false>(m, n_rows, block, q, scales, num_sms, s);

@@ -79,13 +79,22 @@ typedef enum {
 typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
 
 /*
- * FP8 operand formats [JAX-BW format paragraph: E4M3 for its range/precision
- * balance, E5M2 the wider-range alternative].  E4M3 ("fn"): bias 7, 3
- * mantissa bits, no infinities, NaN = S.1111.111, largest finite 448.  E5M2:
- * bias 15, 2 mantissa bits, infinities and NaNs in the top binade, largest
- * finite 57344.  The entry points without a format argument take E4M3.
+ * Operand element formats [JAX-BW format paragraph: E4M3 for its
+ * range/precision balance, E5M2 the wider-range alternative; TUT-12 12.6.1:
+ * the fifth-generation tensor core's FP4 micro-scaling formats].  E4M3
+ * ("fn"): bias 7, 3 mantissa bits, no infinities, NaN = S.1111.111, largest
+ * finite 448.  E5M2: bias 15, 2 mantissa bits, infinities and NaNs in the top
+ * binade, largest finite 57344.  Both one code per byte.  E2M1 (FP4; with 1x32
+ * power-of-two scales this is MXFP4): bias 1, 1 mantissa bit, values 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6, no infinities or NaNs (the quantiser saturates to +-6
+ * and writes NaN as +6); two codes per byte, element 2j in the low nibble of
+ * byte j, so a row of K elements takes K/2 bytes.  A GEMM with an E2M1
+ * operand needs K % 128 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE) and that
+ * operand 32-byte aligned (else FP8G_ERR_ALIGNMENT); it runs at the FP8 MMA
+ * rate (kind::f8f6f4 / mxf8f6f4) and reads half the operand bytes.  The entry
+ * points without a format argument take E4M3.
  */
-typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1 } fp8g_format;
+typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1, FP8G_E2M1 = 2 } fp8g_format;
 
 /*
  * Fused-epilogue activations [TRITON-FP8 benchmark list: a bias_add_relu
@@ -211,7 +220,9 @@ FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t co
  * fp8g_quantize_e4m3 with the output format `fmt` (fp8g_format): with
  * FP8G_E5M2 the bound 448 becomes 57344 throughout (s = fl32(amax/57344), or
  * the smallest power of two with 57344*s >= amax; saturation to +-57344;
- * infinities saturate too; NaN -> 0x7F).  A bad `fmt` is FP8G_ERR_INVALID_ARG.
+ * infinities saturate too; NaN -> 0x7F).  With FP8G_E2M1 the bound is 6
+ * (saturation to +-6, NaN -> code 7) and q holds two codes per byte: uint8
+ * [rows, cols/2].  A bad `fmt` is FP8G_ERR_INVALID_ARG.
  */
 FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block,
                           int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
@@ -234,7 +245,8 @@ typedef enum { FP8G_IN_F32 = 0, FP8G_IN_BF16 = 1 } fp8g_in_dtype;
  * is row rows[r] of x [x_rows, cols] quantised as fp8g_quantize does (rows
  * null: row r, n_rows <= x_rows).  x is fp32 or bf16 (in_dtype; bf16 is
  * widened exactly), 16-byte aligned; rows: device int32 [n_rows], 4-byte
- * aligned; q: uint8 [n_rows, cols]; scales: [n_rows, cols/32] (block 32) or
+ * aligned; q: uint8 [n_rows, cols] (E2M1: [n_rows, cols/2]); scales:
+ * [n_rows, cols/32] (block 32) or
  * [1].  Gather, scale and quantisation are one pass over HBM (per-tensor:
  * two).  cols % 8 == 0 (block 32: cols % 32 == 0).  A row index outside
  * [0, x_rows) records FP8G_ERR_INVALID_ARG in the status word (detail: r) and
@@ -247,7 +259,8 @@ FP8G_API fp8g_status fp8g_quantize_rows(const void *x, int32_t in_dtype, int64_t
 /*
  * The GEMM entry points with explicit operand formats (fp8g_format each for
  * A and B, mixed allowed: the tensor core's kind::f8f6f4 and
- * kind::mxf8f6f4 MMAs take either format per operand).  Everything else as
+ * kind::mxf8f6f4 MMAs take any of the three per operand; an E2M1 operand
+ * is packed, two codes per byte, with the rules of fp8g_format).  Everything else as
  * fp8_gemm / fp8_gemm_blockscaled / fp8_grouped_gemm; a bad format is
  * FP8G_ERR_INVALID_ARG.  Parity: the same tolerance as for E4M3.
  */
