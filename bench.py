@@ -44,7 +44,12 @@ WORKLOADS = {
     "mixed8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, b_fmt=1),
     # literal fp32 block scales amax/448 (promotion GEMM)
     "literal8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, literal=True),
+    # E2M1 x E2M1 with power-of-two 1x32 scales (MXFP4), two codes per byte
+    "mxfp4_8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
 }
+FMT_NAMES = ["e4m3", "e5m2", "e2m1"]
+# bytes per element of each format in memory (E2M1: two codes per byte)
+FMT_BYTES = [1.0, 1.0, 0.5]
 METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
 
 
@@ -153,11 +158,13 @@ def make_inputs(wl: dict, device):
 def algorithmic_bytes(wl: dict, w) -> int:
     M, N, K = wl["M"], wl["N"], wl["K"]
     out_b = 4 if w.out == "f32" else 2
+    ea, eb = FMT_BYTES[wl.get("a_fmt", 0)], FMT_BYTES[wl.get("b_fmt", 0)]
     if wl["kind"] == "grouped":
         E = w.B.shape[0]
-        return M * K + E * N * K + 4 * (M * K // 32 + E * N * K // 32) + M * N * out_b + 4 * E
+        return int(M * K * ea + E * N * K * eb + 4 * (M * K // 32 + E * N * K // 32) +
+                   M * N * out_b + 4 * E)
     sf = 8 if wl["kind"] == "tensor" else 4 * (M * K // 32 + N * K // 32)
-    return M * K + N * K + sf + M * N * out_b
+    return int(M * K * ea + N * K * eb + sf + M * N * out_b)
 
 
 def run_once(fp8g, wl, w, t, C, stream):
@@ -182,10 +189,12 @@ def run_once(fp8g, wl, w, t, C, stream):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# of the dominant kernel, from the ncu capture summarised in
-# profiles/gemm_pair_block_8192_ncu.md.  Valid only for the kernel source that
-# capture measured; workloads without a capture report null.
-TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536}
+# of the dominant kernel, from the ncu captures summarised in
+# profiles/gemm_pair_block_8192_ncu.md and profiles/gemm_pair_mxfp4_8192_ncu.md.
+# Valid only for the kernel source those captures measured; workloads without
+# a capture report null.
+TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536,
+                 "mxfp4_8192": 111_368_192 + 92_802_304}
 
 
 def launches_per_call(fp8g, wl) -> int:
@@ -450,6 +459,8 @@ def main():
     roof["kernel_ms"] = round(kernel_ms, 5)
     roof["peak_source"] = (f"{peaks['src']}: fp8 = 2 x bf16 burst {peaks['bf16']} TFLOP/s"
                            if tensor_bound else f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
+    if 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
+        roof["peak_source"] += " (E2M1 operands run on the FP8-rate MMA, kind::f8f6f4)"
     roof["nominal_frac"] = round(max(flops / 4.5e15, abytes / 8e12) / (kernel_ms * 1e-3), 4)
 
     line = {
@@ -463,12 +474,12 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": (["e4m3", "e5m2"][wl.get("a_fmt", 0)] + " x " + ["e4m3", "e5m2"][wl.get("b_fmt", 0)]
+        "dtype": (FMT_NAMES[wl.get("a_fmt", 0)] + " x " + FMT_NAMES[wl.get("b_fmt", 0)]
                   + " -> f32 accumulate"),
         "data": "synthetic (seeded CPU generators, quantised on the GPU)",
         "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"],
-                   "formats": ["e4m3", "e5m2"][wl.get("a_fmt", 0)] + " x " +
-                              ["e4m3", "e5m2"][wl.get("b_fmt", 0)],
+                   "formats": FMT_NAMES[wl.get("a_fmt", 0)] + " x " +
+                              FMT_NAMES[wl.get("b_fmt", 0)],
                    "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
                               {"block": "1x32 along K, power of two",
                               "grouped": "1x32 along K, power of two",
