@@ -189,12 +189,22 @@ def run_once(fp8g, wl, w, t, C, stream):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# of the dominant kernel, from the ncu captures summarised in
-# profiles/gemm_pair_block_8192_ncu.md and profiles/gemm_pair_mxfp4_8192_ncu.md.
+# of the dominant kernel, from the ncu captures summarised in profiles/.
 # Valid only for the kernel source those captures measured; workloads without
 # a capture report null.
-TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536,
-                 "mxfp4_8192": 111_368_192 + 92_802_304}
+TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536}
+
+
+def fp4_rate(fp8g, wl) -> bool:
+    """Whether the call runs the FP4-rate MMA: E2M1 x E2M1 block-scaled on CTA
+    pairs with K % 256 == 0 (the library's own selection rule)."""
+    if wl.get("a_fmt", 0) != 2 or wl.get("b_fmt", 0) != 2 or wl["K"] % 256:
+        return False
+    if wl["kind"] == "grouped":
+        return fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 256
+    if wl["kind"] != "block" or wl.get("literal"):
+        return False
+    return fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["BM"] == 256
 
 
 def launches_per_call(fp8g, wl) -> int:
@@ -436,16 +446,20 @@ def main():
     d2h = C.numel() * C.element_size()
 
     peaks = _peaks()
-    fp8_peak = 2.0 * peaks["bf16"]          # measured bf16 burst x nominal fp8/bf16 ratio (2)
+    # measured bf16 burst x the nominal dense ratio of the MMA kind that runs:
+    # FP8 (and E2M1 on the FP8-rate MMA) 2, FP4 (kind::mxf4) 13.5 / 2.25 = 6
+    f4 = fp4_rate(fp8g, wl)
+    ratio = 6.0 if f4 else 2.0
+    tc_peak = ratio * peaks["bf16"]
     tflops = flops / (ms * 1e-3) / 1e12
     hbm_gbs = abytes / (ms * 1e-3) / 1e9
     k_tflops = flops / (kernel_ms * 1e-3) / 1e12
     k_hbm_gbs = abytes / (kernel_ms * 1e-3) / 1e9
-    tensor_bound = (flops / (fp8_peak * 1e12)) >= (abytes / (peaks["hbm"] * 1e9))
+    tensor_bound = (flops / (tc_peak * 1e12)) >= (abytes / (peaks["hbm"] * 1e9))
     if tensor_bound:
-        roof = {"bound": "tensor", "achieved": round(k_tflops, 1), "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": round(k_tflops / fp8_peak, 4),
-                "call_achieved": round(tflops, 1), "call_frac": round(tflops / fp8_peak, 4)}
+        roof = {"bound": "tensor", "achieved": round(k_tflops, 1), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(k_tflops / tc_peak, 4),
+                "call_achieved": round(tflops, 1), "call_frac": round(tflops / tc_peak, 4)}
     else:
         roof = {"bound": "hbm", "achieved": round(k_hbm_gbs, 1), "peak": peaks["hbm"],
                 "unit": "GB/s", "frac": round(k_hbm_gbs / peaks["hbm"], 4),
@@ -457,11 +471,15 @@ def main():
                      f"timed region" if kms else
                      "the GEMM kernel (the call's only launch) over the timed region")
     roof["kernel_ms"] = round(kernel_ms, 5)
-    roof["peak_source"] = (f"{peaks['src']}: fp8 = 2 x bf16 burst {peaks['bf16']} TFLOP/s"
-                           if tensor_bound else f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
-    if 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
-        roof["peak_source"] += " (E2M1 operands run on the FP8-rate MMA, kind::f8f6f4)"
-    roof["nominal_frac"] = round(max(flops / 4.5e15, abytes / 8e12) / (kernel_ms * 1e-3), 4)
+    roof["peak_source"] = (f"{peaks['src']}: {'fp4 = 6' if f4 else 'fp8 = 2'} x bf16 burst "
+                           f"{peaks['bf16']} TFLOP/s" if tensor_bound else
+                           f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
+    if f4 and tensor_bound:
+        roof["peak_source"] += " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)"
+    elif 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
+        roof["peak_source"] += " (E2M1 operands on the FP8-rate MMA, kind::f8f6f4)"
+    roof["nominal_frac"] = round(max(flops / (13.5e15 if f4 else 4.5e15), abytes / 8e12) /
+                                 (kernel_ms * 1e-3), 4)
 
     line = {
         "metric": METRIC,

@@ -272,11 +272,17 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     st = device_info(di);
     if (st != FP8G_OK) return st;
     const KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
+    // MXFP4 on CTA pairs runs at the FP4 rate (kind::mxf4, 256 K elements per
+    // stage); every other E2M1 case takes the FP8-rate MMA with 4-bit loads
+    const bool f4 = kc.pair && mode != kModeTensor && a_fmt == FP8G_E2M1 &&
+                    b_fmt == FP8G_E2M1 && K % 256 == 0;
     GemmParams p{};
     p.M = M;
     p.N = N;
     p.K = K;
-    p.num_kb = (int32_t)((K + kBK - 1) / kBK);
+    p.num_kb = f4 ? (int32_t)(K / 256) : (int32_t)((K + kBK - 1) / kBK);
+    p.f4 = f4;
+    const int32_t num_kg = f4 ? 2 * p.num_kb : p.num_kb;  // 128-wide K groups of the scales
     p.npm = (int32_t)((M + kc.BM - 1) / kc.BM);
     p.npn = (int32_t)((N + kc.BN - 1) / kc.BN);
     p.T = (int64_t)p.npm * p.npn;
@@ -305,19 +311,24 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     const int64_t rows_a = M > 0 ? M : 1;
     const void *a_ptr = M > 0 ? A : B;
     const int a_map_fmt = M > 0 ? a_fmt : b_fmt;
+    // operand maps count elements; the FP4-rate kernel views its packed
+    // operands as dense bytes (K / 2 per row, 128 bytes = 256 codes per box row)
+    const uint64_t kdim = f4 ? (uint64_t)(K / 2) : (uint64_t)K;
+    const int map_fmt_a = f4 ? FP8G_E4M3 : a_map_fmt;
+    const int map_fmt_b = f4 ? FP8G_E4M3 : b_fmt;
     {
-        const uint64_t dA[2] = {(uint64_t)K, (uint64_t)rows_a};
+        const uint64_t dA[2] = {kdim, (uint64_t)rows_a};
         const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
-        if ((st = tmap_operand(a_ptr, a_map_fmt, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
+        if ((st = tmap_operand(a_ptr, map_fmt_a, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
     }
     if (mode == kModeGrouped) {
-        const uint64_t dB[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)E};
+        const uint64_t dB[3] = {kdim, (uint64_t)N, (uint64_t)E};
         const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.b_rows, 1u};
-        if ((st = tmap_operand(B, b_fmt, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        if ((st = tmap_operand(B, map_fmt_b, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     } else {
-        const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
+        const uint64_t dB[2] = {kdim, (uint64_t)N};
         const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
-        if ((st = tmap_operand(B, b_fmt, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        if ((st = tmap_operand(B, map_fmt_b, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
     }
     maps.SA = maps.A;
     maps.SB = maps.A;
@@ -341,12 +352,12 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.n_rtA = (int32_t)(mode == kModeGrouped ? M / kBM + E : (M + kBM - 1) / kBM);
     p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    const size_t bytesA = packed_scale_bytes(p.num_kb, p.n_rtA, 1);
+    const size_t bytesA = packed_scale_bytes(num_kg, p.n_rtA, 1);
     // single-CTA 256-wide tiles take B's scales replicated for one 128x256b
     // tensor-memory copy (4 KB per 256 rows and K step instead of 1 KB); CTA
     // pairs take plain 512-byte chunks (three warpx4 copies per K step)
     const bool repB = kc.BN == 256 && !kc.pair;
-    const size_t bytesB = packed_scale_bytes(p.num_kb, p.n_rtB, zB) * (repB ? 4 : 1);
+    const size_t bytesB = packed_scale_bytes(num_kg, p.n_rtB, zB) * (repB ? 4 : 1);
     void *ws = nullptr;
     if (scratch != nullptr) {
         // caller-provided scratch (the allocation-free entry point)
@@ -362,15 +373,15 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     uint8_t *pkB = pkA + bytesA;
     PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
     PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, repB ? 1 : 0};
-    cudaError_t e = launch_pack_scales(pa, pb, p.sfc, p.num_kb, E, di.status, stream);
+    cudaError_t e = launch_pack_scales(pa, pb, p.sfc, num_kg, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;
     if (e == cudaSuccess && kc.pair) {
         // CTA pairs fetch the packed chunks by TMA: each array as rows of 128
         // uint32 (one 512-byte chunk per row)
-        const uint64_t dSA[2] = {128u, (uint64_t)p.num_kb * (uint64_t)p.n_rtA};
+        const uint64_t dSA[2] = {128u, (uint64_t)num_kg * (uint64_t)p.n_rtA};
         const uint32_t bSA[2] = {128u, 1u};
-        const uint64_t dSB[2] = {128u, (uint64_t)zB * p.num_kb * (uint64_t)p.n_rtB};
+        const uint64_t dSB[2] = {128u, (uint64_t)zB * num_kg * (uint64_t)p.n_rtB};
         const uint32_t bSB[2] = {128u, 2u};  // 1 KB: the two 128-row chunks of a 256-row tile
         if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||

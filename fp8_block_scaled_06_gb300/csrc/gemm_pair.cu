@@ -26,6 +26,14 @@
 // one accumulator plus per-stage scale factors block-scaled; an accumulator
 // is released as soon as it is in registers) is allocated and freed by both
 // CTAs together.
+//
+// F4 (E2M1 x E2M1 with 1x32 power-of-two scales, i.e. MXFP4, at the FP4
+// rate): kind::mxf4 reads dense 4-bit operands, so the packed codes are
+// loaded as plain bytes and a 128-byte swizzled row of a stage holds 256 K
+// elements; each of the four MMAs per stage takes K = 64 (32 bytes, the same
+// descriptor step as FP8) with two scale bytes per row.  A stage therefore
+// carries two 128-wide K groups of packed scales (3 KB: A's two chunks, B's
+// two pairs of chunks), copied to a second set of scale columns.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -57,10 +65,12 @@ constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
 constexpr int kSfaBytes = 512;
 constexpr int kSfbBytes = 1024;  // B's two 128-row chunks
 
-template <int MODE>
+template <int MODE, bool F4>
 struct PairCfg {
     static constexpr bool kBlock = MODE != kModeTensor;
-    static constexpr int CHUNK = kBlock ? kSfaBytes + kSfbBytes : 0;  // packed scales per stage
+    static_assert(kBlock || !F4, "FP4-rate MMAs are block-scaled");
+    // packed scales per stage (F4: two 128-wide K groups)
+    static constexpr int CHUNK = kBlock ? (F4 ? 2 : 1) * (kSfaBytes + kSfbBytes) : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + kStages * kA;
     static constexpr int OFF_SF = OFF_B + kStages * kB;
@@ -76,7 +86,8 @@ struct PairCfg {
     static constexpr int OFF_GROUP = OFF_MISC + 16;  // row_off, tile_off, rt_off [E + 1]
     static constexpr int SMEM_BYTES = OFF_GROUP + 3 * (FP8G_MAX_EXPERTS + 1) * 4 + 1024;
     static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
-    static constexpr int SF_COLS = kBlock ? 16 : 0;  // A: cols 0-3, B: cols 8-15
+    // A: cols 0-3, B: cols 8-15 (F4: the second K group's at 16-19, 24-31)
+    static constexpr int SF_COLS = kBlock ? (F4 ? 32 : 16) : 0;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
     static_assert(256 + kStages * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
@@ -138,12 +149,12 @@ __device__ __forceinline__ PairTile pair_tile(int32_t t, const GemmParams &p, co
     return ti;
 }
 
-template <int MODE, bool OUT_F32>
+template <int MODE, bool OUT_F32, bool F4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
-    using PC = PairCfg<MODE>;
+    using PC = PairCfg<MODE, F4>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = ptx::smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -227,7 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Both CTAs' copies complete on the even CTA's full barrier (TMA
         // cta_group::2), which expects both halves; the odd CTA does not arrive.
         if (lane == 0) {
-            const uint32_t tx_bytes = PC::TX - (p.a_e2m1 ? kA / 2 : 0) - (p.b_e2m1 ? kB / 2 : 0);
+            // F4 loads dense bytes; otherwise an E2M1 operand's 4-bit tile
+            // load counts only its packed bytes
+            const uint32_t tx_bytes =
+                F4 ? PC::TX : PC::TX - (p.a_e2m1 ? kA / 2 : 0) - (p.b_e2m1 ? kB / 2 : 0);
+            const int32_t num_kg = F4 ? 2 * p.num_kb : p.num_kb;  // K groups of the packed scales
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {
                 const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
@@ -252,12 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (PC::kBlock) {
                         // packed UE8M0 chunks (512-byte rows of the packed arrays):
                         // this CTA's 128 rows of A; the tile's 256 rows of B
+                        // (F4: K groups 2 kb and 2 kb + 1, A's two chunks first,
+                        // then B's two pairs)
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
-                        ptx::tma_load_2d_pair(dst, &tmSA, fb, 0,
-                                              kb * p.n_rtA + ti.rtA0 + (int32_t)rank);
-                        // B's chunks of pair tile pn: 128-row tiles 2 pn and 2 pn + 1
-                        ptx::tma_load_2d_pair(dst + kSfaBytes, &tmSB, fb, 0,
-                                              (ti.e * p.num_kb + kb) * p.n_rtB + 2 * ti.pn);
+                        constexpr int G = F4 ? 2 : 1;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const int32_t kg = G * kb + g;
+                            ptx::tma_load_2d_pair(dst + g * kSfaBytes, &tmSA, fb, 0,
+                                                  kg * p.n_rtA + ti.rtA0 + (int32_t)rank);
+                            // B's chunks of pair tile pn: 128-row tiles 2 pn and 2 pn + 1
+                            ptx::tma_load_2d_pair(dst + G * kSfaBytes + g * kSfbBytes, &tmSB, fb, 0,
+                                                  (ti.e * num_kg + kg) * p.n_rtB + 2 * ti.pn);
+                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -288,7 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t a0 = sbase + PC::OFF_A + stage * kA;
                     const uint32_t b0 = sbase + PC::OFF_B + stage * kB;
-                    if constexpr (PC::kBlock) {
+                    if constexpr (F4) {
+                        // MMA k: K elements 64k .. 64k + 63 = scale blocks 2k, 2k + 1,
+                        // in K group k / 2 (columns + 16 (k / 2)), bytes 2 (k % 2), + 1
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k) {
+                            const uint32_t sfk = sf + 16 * (k >> 1);
+                            ptx::mma_mxf4_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                               ptx::desc_kmajor_sw128(b0 + k * 32),
+                                               ptx::idesc_mxf4(2 * kBM, kPairBN, 2u * (k & 1)),
+                                               sfk, sfk + 8, (kb | k) != 0 ? 1u : 0u);
+                        }
+                    } else if constexpr (PC::kBlock) {
                         const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
@@ -325,12 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                     const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
-                    ptx::tc_cp_32x128b_warpx4_pair(sf, ptx::desc_sf_chunk(cs));
-                    // B's rows 0-127 to columns 8-11, rows 128-255 to 12-15 (each
-                    // replicated over the lane quarters by the copy)
-                    ptx::tc_cp_32x128b_warpx4_pair(sf + 8, ptx::desc_sf_chunk(cs + kSfaBytes));
-                    ptx::tc_cp_32x128b_warpx4_pair(sf + 12,
-                                                   ptx::desc_sf_chunk(cs + kSfaBytes + 512));
+                    constexpr int G = F4 ? 2 : 1;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        // K group g: A's rows to columns 16 g + 0-3; B's rows 0-127
+                        // to 16 g + 8-11, rows 128-255 to 16 g + 12-15 (each
+                        // replicated over the lane quarters by the copy)
+                        const uint32_t sfg = sf + 16 * g;
+                        const uint32_t cb = cs + G * kSfaBytes + g * kSfbBytes;
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg, ptx::desc_sf_chunk(cs + g * kSfaBytes));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + 8, ptx::desc_sf_chunk(cb));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + 12, ptx::desc_sf_chunk(cb + 512));
+                    }
                     ptx::tc_commit_pair_mc(bar_sfr(stage), 0x1);
                     if (++stage == kStages) {
                         stage = 0;
@@ -440,10 +480,10 @@ roles_done:
     }
 }
 
-template <int MODE, bool OUT_F32>
+template <int MODE, bool OUT_F32, bool F4 = false>
 cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
-    using PC = PairCfg<MODE>;
-    auto kern = gemm_pair_kernel<MODE, OUT_F32>;
+    using PC = PairCfg<MODE, F4>;
+    auto kern = gemm_pair_kernel<MODE, OUT_F32, F4>;
     static unsigned long long attr_done = 0ull;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -475,6 +515,13 @@ cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cud
 
 cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                              int grid, cudaStream_t stream) {
+    if (p.f4 && mode == kModeBlock)
+        return out_f32 ? launch_pair<kModeBlock, true, true>(maps, p, grid, stream)
+                       : launch_pair<kModeBlock, false, true>(maps, p, grid, stream);
+    if (p.f4 && mode == kModeGrouped)
+        return out_f32 ? launch_pair<kModeGrouped, true, true>(maps, p, grid, stream)
+                       : launch_pair<kModeGrouped, false, true>(maps, p, grid, stream);
+    if (p.f4) return cudaErrorInvalidValue;
     if (mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true>(maps, p, grid, stream)
                        : launch_pair<kModeBlock, false>(maps, p, grid, stream);

@@ -46,6 +46,10 @@ struct GemmParams {
     // packed byte count, half a tile's shared-memory footprint, so each stage
     // expects that many fewer transaction bytes.
     int32_t a_e2m1, b_e2m1;
+    // E2M1 x E2M1 block-scaled on CTA pairs at the FP4 rate (kind::mxf4):
+    // operands loaded as dense bytes, 256 K elements per stage, num_kb = K /
+    // 256, the packed scale arrays holding 2 * num_kb chunks per row tile.
+    int32_t f4;
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
     const int32_t *c_row_of;  // grouped scatter: row of C for routed row r (null: r)

@@ -336,6 +336,20 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// kind::mxf4: dense 4-bit E2M1 operands (two codes per byte in shared memory,
+// the first in the low nibble), K = 64 per instruction, two UE8M0 scales per
+// row (scale_vec::2X: the bytes sf_id and sf_id + 1 of the row's word).
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
@@ -420,6 +434,13 @@ __host__ __device__ constexpr uint32_t idesc_f8(uint32_t M, uint32_t N) {
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sf_id) {
     return ((sf_id & 3u) << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
            ((sf_id & 3u) << 29);
+}
+
+// Instruction descriptor, kind::mxf4 block_scale: the fields of idesc_mxf8
+// with A and B E2M1 (format 1 of this kind, bits 7-9 and 10-12); sf_id 0 or 2
+// (a pair of scale bytes per row).
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id) {
+    return idesc_mxf8(M, N, sf_id) | (1u << 7) | (1u << 10);
 }
 
 }  // namespace ptx

@@ -186,3 +186,115 @@ def test_e2m1_grouped():
         ref, bound, _ = oracle.gemm(qa_o[r0:r1], qb_o[e], sa_o[r0:r1], sb_o[e], True,
                                     oracle.OUT_BF16, a_fmt=F4, b_fmt=F4)
         assert_within(Ch[r0:r1], ref, bound, f"E2M1 grouped expert {e}")
+
+
+# ---------------------------------------------------------------- FP4 rate
+# MXFP4 (E2M1 x E2M1, 1x32 power-of-two scales) on CTA pairs with K % 256 == 0
+# runs kind::mxf4: dense 4-bit operands, K = 64 per MMA, two scale bytes per
+# row per MMA.  Pair shapes: at least a wave of 128 x 256 tiles.
+
+def test_mxfp4_pair_scale_layout_exact():
+    """B[j, k] = 1 at k = j mod K, else 0, with random power-of-two scales on
+    both sides: C[i, j] = a(i, k) sfa(i, k/32) sfb(j, k/32) for k = j mod K,
+    one exact product per output (fp32 out).  Every K block of every stage
+    appears, so a wrong scale byte, K group or nibble fails bit-exactly."""
+    M, N, K = 2048, 2560, 512
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["BM"] == 256
+    rng = np.random.default_rng(5)
+    ca = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    cb = np.zeros((N, K), np.uint8)
+    cb[np.arange(N), np.arange(N) % K] = 2                       # E2M1 code 2 = 1.0
+    sfa = np.exp2(rng.integers(-4, 5, (M, K // 32))).astype(np.float32)
+    sfb = np.exp2(rng.integers(-4, 5, (N, K // 32))).astype(np.float32)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    fp8g.fp8_gemm_blockscaled_fmt(torch.from_numpy(pack_e2m1(ca)).cuda(),
+                                  torch.from_numpy(pack_e2m1(cb)).cuda(),
+                                  torch.from_numpy(sfa).cuda(), torch.from_numpy(sfb).cuda(), C,
+                                  fp8g.FP8G_OUT_F32, F4, F4, M, N, K)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    k = np.arange(N) % K
+    want = (oracle.e2m1_table()[ca[:, k]] * sfa[:, k // 32] * sfb[np.arange(N), k // 32][None, :])
+    got = C.cpu().numpy()
+    assert np.array_equal(got, want.astype(np.float32)), f"{int((got != want).sum())} mismatches"
+
+
+def _sampled(qa_o, qb_o, sa_o, sb_o, Ch, M, N, pts, what):
+    rng = np.random.default_rng(M + N)
+    edge_i = np.array([0, 1, 127, 128, 255, 256, M - 1, M - 2, M - 129])
+    edge_j = np.array([0, 1, 127, 128, 255, 256, N - 1, N - 2, N - 129])
+    pi = np.concatenate([np.repeat(edge_i, edge_j.size), rng.integers(0, M, pts)])
+    pj = np.concatenate([np.tile(edge_j, edge_i.size), rng.integers(0, N, pts)])
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16,
+                                       a_fmt=F4, b_fmt=F4)
+    assert_within(Ch[pi, pj], ref, bound, what)
+
+
+@pytest.mark.parametrize("M,N,K", [(2100, 2600, 768), (2048, 2560, 384)])
+def test_mxfp4_pair_ragged_sampled(M, N, K):
+    """Ragged M and N on pairs: K = 768 takes the FP4-rate kernel (3 stages);
+    K = 384 (not a multiple of 256) the FP8-rate pair kernel with 4-bit loads."""
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["BM"] == 256
+    A = synth.normal((M, K), seed=M)
+    B = synth.normal((N, K), seed=N) * 3.0
+    qa, sa, qa_o, sa_o = _quant(A, 32, F4)
+    qb, sb, qb_o, sb_o = _quant(B, 32, F4)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_gemm_blockscaled_fmt(qa, qb, sa, sb, C, 0, F4, F4, M, N, K)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    _sampled(qa_o, qb_o, sa_o, sb_o, C.float().cpu().numpy(), M, N, 4000,
+             f"MXFP4 pairs {M}x{N}x{K}")
+
+
+def test_mxfp4_pair_full_f32():
+    """A whole pair-shaped output against the oracle (fp32 out, one stage)."""
+    M, N, K = 2304, 2304, 256
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["BM"] == 256
+    A = synth.normal((M, K), seed=8)
+    B = synth.normal((N, K), seed=9)
+    qa, sa, qa_o, sa_o = _quant(A, 32, F4)
+    qb, sb, qb_o, sb_o = _quant(B, 32, F4)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    fp8g.fp8_gemm_blockscaled_fmt(qa, qb, sa, sb, C, fp8g.FP8G_OUT_F32, F4, F4, M, N, K)
+    assert fp8g.fp8_gemm_status()[0] == 0
+    ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, True, oracle.OUT_F32, a_fmt=F4, b_fmt=F4)
+    assert_within(C.cpu().numpy(), ref, bound, "MXFP4 pairs full f32")
+
+
+def test_mxfp4_grouped_pairs_sampled():
+    """Grouped MoE GEMM on pairs at the FP4 rate: empty, one-row and ragged
+    experts; offsets and tile map bit-exact; sampled outputs per expert."""
+    counts = np.array([3000, 0, 70, 9000, 257, 1, 0, 129], np.int32)
+    E, N, K = counts.size, 2048, 512
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, E)
+    assert plan["BM"] == 256
+    w = synth.small_grouped(counts, N, K, seed=29)
+    qa, sa, qa_o, sa_o = _quant(w.A, 32, F4)
+    qb, sb, qb_o, sb_o = _quant(w.B.reshape(E * N, K), 32, F4)
+    C = torch.full((rows, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    tmap = torch.full((plan["max_tiles"], 4), -1, dtype=torch.int32, device="cuda")
+    fp8g.fp8_grouped_gemm_fmt(qa, qb.reshape(E, N, K // 2), sa, sb.reshape(E, N, K // 32), C, 0,
+                              F4, F4, torch.from_numpy(counts).cuda(), E, N, K, rows, offs, tmap)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    offs_o = oracle.grouped_offsets(counts)
+    assert np.array_equal(offs.cpu().numpy(), offs_o)
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert np.array_equal(tmap.cpu().numpy()[:want.shape[0]], want)
+    Ch = C.float().cpu().numpy()
+    qb_o = qb_o.reshape(E, N, K)
+    sb_o = sb_o.reshape(E, N, K // 32)
+    rng = np.random.default_rng(30)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        r0, r1 = int(offs_o[e]), int(offs_o[e + 1])
+        m = r1 - r0
+        pi = np.concatenate([[0, m - 1, min(255, m - 1), min(256, m - 1)], rng.integers(0, m, 300)])
+        pj = rng.integers(0, N, pi.size)
+        ref, bound, _ = oracle.gemm_sample(qa_o[r0:r1], qb_o[e], sa_o[r0:r1], sb_o[e], True, pi,
+                                           pj, oracle.OUT_BF16, a_fmt=F4, b_fmt=F4)
+        assert_within(Ch[r0 + pi, pj], ref, bound, f"MXFP4 grouped expert {e}")
