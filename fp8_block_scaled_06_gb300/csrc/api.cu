@@ -305,6 +305,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.act = act;
     p.c_row_of = c_row_of;
     p.c_rows = c_rows;
+    p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
 
     GemmMaps maps;
     // grouped with zero rows: A is never read (a one-row map over B stands in)

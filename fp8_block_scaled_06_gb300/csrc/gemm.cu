@@ -481,43 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         epi32(r[c], alpha, brow, p.act, ncol0 + c * 32, p.N);
                     a_t = 1.0f;
                 }
-                if constexpr (OUT_F32) {
-                    float *out = reinterpret_cast<float *>(p.C) + row * p.N + ncol0;
 #pragma unroll
-                    for (int c = 0; c < C_::CW / 32; ++c)
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            if (ncol0 + c * 32 + v * 4 < p.N) {
-                                float4 o;
-                                o.x = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 0]));
-                                o.y = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 1]));
-                                o.z = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 2]));
-                                o.w = __fmul_rn(a_t, __uint_as_float(r[c][4 * v + 3]));
-                                *reinterpret_cast<float4 *>(out + c * 32 + v * 4) = o;
-                            }
-                        }
-                } else {
-                    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.C) + row * p.N + ncol0;
-#pragma unroll
-                    for (int c = 0; c < C_::CW / 32; ++c)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            if (ncol0 + c * 32 + v * 8 < p.N) {
-                                uint32_t pk[4];
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const float lo =
-                                        __fmul_rn(a_t, __uint_as_float(r[c][8 * v + 2 * h]));
-                                    const float hi =
-                                        __fmul_rn(a_t, __uint_as_float(r[c][8 * v + 2 * h + 1]));
-                                    __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                                    pk[h] = *reinterpret_cast<uint32_t *>(&b2);
-                                }
-                                *reinterpret_cast<uint4 *>(out + c * 32 + v * 8) =
-                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            }
-                        }
-                }
+                for (int c = 0; c < C_::CW / 32; ++c)
+                    store_row32<OUT_F32>(p.C, row, p.N, ncol0 + c * 32, r[c], a_t, p.st32 != 0);
             }
         }
     }

@@ -50,6 +50,7 @@ struct GemmParams {
     // operands loaded as dense bytes, 256 K elements per stage, num_kb = K /
     // 256, the packed scale arrays holding 2 * num_kb chunks per row tile.
     int32_t f4;
+    int32_t st32;             // epilogue: 32-byte stores (C 32-byte aligned, rows multiples of 32 B)
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
     const int32_t *c_row_of;  // grouped scatter: row of C for routed row r (null: r)

@@ -1,6 +1,8 @@
 // Device helpers shared by the GEMM kernels: the grouped raster order of
 // output tiles and the bounded mbarrier waits with their error reporting.
 #pragma once
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -174,6 +176,57 @@ __device__ __forceinline__ void grouped_prefix(const GemmParams &p, int bm, int3
             for (int e = 0; e <= p.E; ++e) p.offsets_out[e] = row_off[e];
     }
     __syncthreads();
+}
+
+// Columns ncol .. ncol + 31 of row `row` of C (row stride N) from 32 fp32
+// accumulator words times a_t, bf16 (RNE) or fp32, none at or past column N
+// (N is a multiple of 8 / 4 elements and ncol of 32, so every store is
+// whole).  wide: 32-byte stores, each a whole L2 sector (C 32-byte aligned,
+// rows a multiple of 32 bytes); otherwise 16-byte stores.  With one row per
+// lane a warp's store touches 32 rows: 16-byte stores leave every sector
+// half-written and double the L2 write requests, which the concurrent TMA
+// operand loads of the next tile then queue behind.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_row32(void *C, int64_t row, int64_t N, int64_t ncol,
+                                            const uint32_t (&r)[32], float a_t, bool wide) {
+    if constexpr (OUT_F32) {
+        float *out = reinterpret_cast<float *>(C) + row * N + ncol;
+        uint32_t o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(a_t, __uint_as_float(r[i])));
+        if (wide) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                if (ncol + v * 8 < N) ptx::st_global_v8(out + v * 8, o + 8 * v);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                if (ncol + v * 4 < N)
+                    *reinterpret_cast<uint4 *>(out + v * 4) =
+                        make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+    } else {
+        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(C) + row * N + ncol;
+        uint32_t pk[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            const float lo = __fmul_rn(a_t, __uint_as_float(r[2 * h]));
+            const float hi = __fmul_rn(a_t, __uint_as_float(r[2 * h + 1]));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+            pk[h] = *reinterpret_cast<uint32_t *>(&b2);
+        }
+        if (wide) {
+#pragma unroll
+            for (int v = 0; v < 2; ++v)
+                if (ncol + v * 16 < N) ptx::st_global_v8(out + v * 16, pk + 8 * v);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                if (ncol + v * 8 < N)
+                    *reinterpret_cast<uint4 *>(out + v * 8) =
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+    }
 }
 
 }  // namespace fp8g

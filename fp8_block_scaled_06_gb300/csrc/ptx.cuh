@@ -424,6 +424,13 @@ __device__ __forceinline__ uint64_t desc_sf_chunk(uint32_t saddr) {
 // Instruction descriptor, kind::f8f6f4: fp32 accumulator (bits 4-5 = 1),
 // A and B E4M3 (format 0 in bits 7-9 / 10-12), both K-major, N >> 3 in bits
 // 17-22, M >> 4 in bits 24-28.
+// 32-byte global store (one whole L2 sector); p 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *o) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(o[0]),
+                 "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
+}
+
 __host__ __device__ constexpr uint32_t idesc_f8(uint32_t M, uint32_t N) {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
