@@ -229,4 +229,90 @@ __device__ __forceinline__ void store_row32(void *C, int64_t row, int64_t N, int
     }
 }
 
+// Quad transpose of 32-byte chunks: lane 4q + p holds the 4 chunks (8 words
+// each, w[8c .. 8c + 7]) of one row segment; afterwards slot t holds chunk p
+// of lane 4q + t's segment.  Two xor-shuffle exchanges of the off-diagonal
+// halves: 2 x 2 blocks of chunks with lane ^ 2, then single chunks with
+// lane ^ 1.
+__device__ __forceinline__ void quad_transpose(uint32_t (&w)[32], int lane) {
+    const bool hi = (lane & 2) != 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t send = hi ? w[j] : w[16 + j];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+        if (hi)
+            w[j] = recv;
+        else
+            w[16 + j] = recv;
+    }
+    const bool odd = (lane & 1) != 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t send = odd ? w[16 * k + i] : w[16 * k + 8 + i];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            if (odd)
+                w[16 * k + i] = recv;
+            else
+                w[16 * k + 8 + i] = recv;
+        }
+}
+
+// Whole warp: lane L's 128-byte row segment (w, 32 words) goes to seg (null:
+// a row past the output, nothing stored; 32-byte aligned).  After
+// quad_transpose, store step t has lane 4q + p write chunk p of lane
+// 4q + t's segment, so each store instruction writes eight whole 128-byte
+// segments instead of 32 sectors of 32 different rows.  chunk_ok: chunk p of
+// every segment lies inside the row (the same columns for every row).
+__device__ __forceinline__ void store_seg128(uint8_t *seg, uint32_t (&w)[32], int lane,
+                                             bool chunk_ok) {
+    quad_transpose(w, lane);
+    const int p = lane & 3;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        uint8_t *dst = reinterpret_cast<uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(seg), (lane & ~3) | t));
+        if (dst != nullptr && chunk_ok) ptx::st_global_v8(dst + 32 * p, w + 8 * t);
+    }
+}
+
+// Whole warp, one row per lane (row < 0: past the output): columns
+// ncol .. ncol + 63 of C from 64 fp32 accumulator words (r[0], r[1]) times
+// a_t, as 128-byte segments through store_seg128 (bf16: one segment, fp32:
+// two).  C 32-byte aligned with rows a multiple of 32 bytes; ncol a multiple
+// of 64; columns at or past N (a multiple of 16 / 8) are not written.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_rows64(void *C, int64_t row, int64_t N, int64_t ncol,
+                                             const uint32_t (&r)[2][32], float a_t, int lane) {
+    const int p = lane & 3;
+    if constexpr (OUT_F32) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                w[i] = __float_as_uint(__fmul_rn(a_t, __uint_as_float(r[c][i])));
+            uint8_t *seg = row >= 0 ? reinterpret_cast<uint8_t *>(
+                                          reinterpret_cast<float *>(C) + row * N + ncol + 32 * c)
+                                    : nullptr;
+            store_seg128(seg, w, lane, ncol + 32 * c + 8 * p < N);
+        }
+    } else {
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            const uint32_t *src = r[h >> 4];
+            const float lo = __fmul_rn(a_t, __uint_as_float(src[(2 * h) & 31]));
+            const float hi = __fmul_rn(a_t, __uint_as_float(src[(2 * h + 1) & 31]));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+            w[h] = *reinterpret_cast<uint32_t *>(&b2);
+        }
+        uint8_t *seg = row >= 0 ? reinterpret_cast<uint8_t *>(
+                                      reinterpret_cast<__nv_bfloat16 *>(C) + row * N + ncol)
+                                : nullptr;
+        store_seg128(seg, w, lane, ncol + 16 * p < N);
+    }
+}
+
 }  // namespace fp8g
