@@ -192,7 +192,8 @@ def run_once(fp8g, wl, w, t, C, stream):
 # of the dominant kernel, from the ncu captures summarised in profiles/.
 # Valid only for the kernel source those captures measured; workloads without
 # a capture report null.
-TRAFFIC_BYTES = {"large8192": 248_740_608 + 117_057_536}
+TRAFFIC_BYTES = {"large8192": 262_422_784 + 117_014_528,
+                 "mxfp4_8192": 107_195_136 + 95_988_992}
 
 
 def fp4_rate(fp8g, wl) -> bool:
