@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "internal.h"
@@ -121,14 +122,27 @@ struct TmapKey {
     }
 };
 
-constexpr int kCacheSize = 128;
-struct TmapEntry {
-    TmapKey key;
-    CUtensorMap map;
-    bool used;
+struct TmapKeyHash {
+    size_t operator()(const TmapKey &k) const {
+        uint64_t h = 1469598103934665603ull;  // FNV-1a over the fields
+        auto mix = [&h](uint64_t v) {
+            for (int i = 0; i < 8; ++i) {
+                h ^= (v >> (8 * i)) & 0xFFu;
+                h *= 1099511628211ull;
+            }
+        };
+        mix(reinterpret_cast<uintptr_t>(k.ptr));
+        mix(((uint64_t)k.rank << 48) ^ ((uint64_t)k.dtype << 32) ^ ((uint64_t)k.ebits << 16) ^
+            ((uint64_t)k.swizzle << 8) ^ (uint64_t)k.dev);
+        for (int i = 0; i < 3; ++i) mix(k.dims[i] ^ ((uint64_t)k.box[i] << 40));
+        return (size_t)h;
+    }
 };
-TmapEntry g_cache[kCacheSize];
-int g_cache_next = 0;
+
+// Encoded maps by key; cleared when it reaches kCacheMax entries (a process
+// that keeps creating new operand buffers does not grow it without bound).
+constexpr size_t kCacheMax = 4096;
+std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_cache;
 
 // Dense row-major tensor [dims[rank-1]] ... [dims[0]] (dims[0] innermost,
 // contiguous), element size ebits bits, zero fill out of bounds.
@@ -147,11 +161,11 @@ fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int ebits, i
         key.box[i] = box[i];
     }
     std::lock_guard<std::mutex> lk(g_mu);
-    for (int i = 0; i < kCacheSize; ++i)
-        if (g_cache[i].used && g_cache[i].key == key) {
-            out = g_cache[i].map;
-            return FP8G_OK;
-        }
+    const auto it = g_cache.find(key);
+    if (it != g_cache.end()) {
+        out = it->second;
+        return FP8G_OK;
+    }
     cuuint64_t gdim[3], gstride[2];
     cuuint32_t bdim[3], estr[3];
     uint64_t stride_bits = (uint64_t)ebits;
@@ -168,11 +182,8 @@ fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int ebits, i
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return FP8G_ERR_CUDA;
-    TmapEntry &e = g_cache[g_cache_next];
-    g_cache_next = (g_cache_next + 1) % kCacheSize;
-    e.key = key;
-    e.map = m;
-    e.used = true;
+    if (g_cache.size() >= kCacheMax) g_cache.clear();
+    g_cache.emplace(key, m);
     out = m;
     return FP8G_OK;
 }
@@ -736,8 +747,7 @@ void fp8g_set_wait_timeout_ms(uint32_t ms) {
 
 void fp8g_shutdown(void) {
     std::lock_guard<std::mutex> lk(g_mu);
-    for (int i = 0; i < kCacheSize; ++i) g_cache[i].used = false;
-    g_cache_next = 0;
+    g_cache.clear();
     for (int d = 0; d < kMaxDevices; ++d)
         if (g_pool_ok[d]) cudaMemPoolTrimTo(g_pool[d], 0);
 }
