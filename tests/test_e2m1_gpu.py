@@ -298,3 +298,47 @@ def test_mxfp4_grouped_pairs_sampled():
         ref, bound, _ = oracle.gemm_sample(qa_o[r0:r1], qb_o[e], sa_o[r0:r1], sb_o[e], True, pi,
                                            pj, oracle.OUT_BF16, a_fmt=F4, b_fmt=F4)
         assert_within(Ch[r0 + pi, pj], ref, bound, f"MXFP4 grouped expert {e}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (129, 48, 128), (7, 264, 384)])
+def test_e2m1_tiny_and_single_stage(M, N, K):
+    """A single 128-wide K stage, one output row, N of one MMA width."""
+    _gemm(F4, F4, True, M, N, K)
+    _gemm(F4, 0, False, M, N, K)
+
+
+def test_e2m1_grouped_zero_rows():
+    """No routed rows at all: offsets all zero, nothing written, status OK."""
+    E, N, K = 3, 128, 256
+    qa = torch.zeros((1, K // 2), dtype=torch.uint8, device="cuda")
+    qb = torch.zeros((E, N, K // 2), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((1, K // 32), device="cuda")
+    sb = torch.ones((E, N, K // 32), device="cuda")
+    C = torch.full((1, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    fp8g.fp8_grouped_gemm_fmt(qa, qb, sa, sb, C, 0, F4, F4, counts, E, N, K, 0, offs)
+    assert fp8g.fp8_gemm_status()[0] == 0
+    assert (offs.cpu().numpy() == 0).all()
+    assert (C.float() == 5.0).all()
+
+
+def test_mxfp4_pair_bias_relu_sampled():
+    """The fused epilogue (per-column bias, ReLU) on the FP4-rate kernel."""
+    M, N, K = 2304, 2560, 512
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["BM"] == 256
+    A = synth.normal((M, K), seed=51)
+    B = synth.normal((N, K), seed=52)
+    qa, sa, qa_o, sa_o = _quant(A, 32, F4)
+    qb, sb, qb_o, sb_o = _quant(B, 32, F4)
+    bias = np.random.default_rng(53).normal(0, 3, N).astype(np.float32)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_gemm_blockscaled_ex(qa, qb, sa, sb, C, 0, F4, F4, torch.from_numpy(bias).cuda(),
+                                 fp8g.FP8G_ACT_RELU, M, N, K)
+    assert fp8g.fp8_gemm_status()[0] == 0
+    rng = np.random.default_rng(54)
+    pi = np.concatenate([[0, M - 1], rng.integers(0, M, 3000)])
+    pj = np.concatenate([[N - 1, 0], rng.integers(0, N, 3000)])
+    ref, bound, _ = oracle.gemm_sample(qa_o, qb_o, sa_o, sb_o, True, pi, pj, oracle.OUT_BF16,
+                                       a_fmt=F4, b_fmt=F4, bias=bias, act_kind=oracle.ACT_RELU)
+    assert_within(C.float().cpu().numpy()[pi, pj], ref, bound, "MXFP4 pairs bias + ReLU")
