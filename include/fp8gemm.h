@@ -90,9 +90,12 @@ typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
  * and writes NaN as +6); two codes per byte, element 2j in the low nibble of
  * byte j, so a row of K elements takes K/2 bytes.  A GEMM with an E2M1
  * operand needs K % 128 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE) and that
- * operand 32-byte aligned (else FP8G_ERR_ALIGNMENT); it runs at the FP8 MMA
- * rate (kind::f8f6f4 / mxf8f6f4) and reads half the operand bytes.  The entry
- * points without a format argument take E4M3.
+ * operand 32-byte aligned (else FP8G_ERR_ALIGNMENT), and reads half the
+ * operand bytes.  E2M1 x E2M1 with 1x32 power-of-two scales on shapes that
+ * take CTA pairs (see fp8g_gemm_plan: BM = 256) and K % 256 == 0 runs the
+ * FP4-rate MMA (kind::mxf4); every other E2M1 call runs the FP8-rate MMA
+ * (kind::f8f6f4 / mxf8f6f4).  The entry points without a format argument
+ * take E4M3.
  */
 typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1, FP8G_E2M1 = 2 } fp8g_format;
 
