@@ -124,6 +124,12 @@ def _L():
             lib.oracle_grouped_tile_map.argtypes = [P, i32, i64, i64, i64, i64, P, i64]
             lib.oracle_grouped_gemm.argtypes = [P, P, P, P, P, i32, i64, i64, ctypes.c_int, P,
                                                 P, P, ctypes.c_int]
+            lib.oracle_quantize_nvfp4.argtypes = [P, i64, i64, P, P, P]
+            lib.oracle_gemm_nvfp4.argtypes = [P, P, P, P, ctypes.c_float, ctypes.c_float, i64, i64,
+                                              i64, ctypes.c_int, P, P, P, ctypes.c_int]
+            lib.oracle_gemm_nvfp4_sample.argtypes = [P, P, P, P, ctypes.c_float, ctypes.c_float,
+                                                     i64, i64, i64, ctypes.c_int, P, P, i64, P, P,
+                                                     P, ctypes.c_int]
             lib.oracle_gemm_flops.restype = ctypes.c_double
             lib.oracle_gemm_flops.argtypes = [i64, i64, i64]
             _lib = lib
@@ -274,6 +280,66 @@ def gemm_sample(A, B, sfa, sfb, block: bool, pi, pj, out_kind: int = OUT_BF16, t
                                int(b_fmt), _p(bias) if bias is not None else None, int(act_kind),
                                M, N, K, int(out_kind), _p(pi), _p(pj), n, _p(C), _p(exact),
                                _p(bound), _threads(threads))
+    return C, bound, exact
+
+
+# ----------------------------------------------------------------- NVFP4
+def quantize_nvfp4(x: np.ndarray):
+    """NVFP4 along the last axis (cols % 16 == 0): returns (E2M1 codes uint8
+    [rows, cols], one per byte; E4M3 block-scale codes uint8 [rows, cols/16];
+    the tensor scale g, a float)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sf = np.empty((rows, cols // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    _L().oracle_quantize_nvfp4(_p(x), rows, cols, _p(q), _p(sf), _p(g))
+    return q, sf, float(g[0])
+
+
+def nvfp4_scales(sf_codes: np.ndarray) -> np.ndarray:
+    """E4M3 block-scale codes -> their values (exact in fp32)."""
+    return e4m3_table()[np.asarray(sf_codes, dtype=np.uint8)].astype(np.float32)
+
+
+def gemm_nvfp4(A, B, sfa_codes, sfb_codes, ga: float, gb: float, out_kind: int = OUT_BF16,
+               threads=None):
+    """C = out(fl32(fl32(ga gb) * sum_kb16 sa sb sum a b)) over E2M1 codes (one per
+    byte).  Returns (C float32 [M,N], bound float64 [M,N], exact [M,N])."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sfa = np.ascontiguousarray(nvfp4_scales(sfa_codes))
+    sfb = np.ascontiguousarray(nvfp4_scales(sfb_codes))
+    M, K = A.shape
+    N = B.shape[0]
+    assert K % 16 == 0 and sfa.shape == (M, K // 16) and sfb.shape == (N, K // 16)
+    C = np.empty((M, N), dtype=np.float32)
+    bound = np.empty((M, N), dtype=np.float64)
+    exact = np.empty((M, N), dtype=np.float64)
+    _L().oracle_gemm_nvfp4(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb), M, N, K,
+                           int(out_kind), _p(C), _p(exact), _p(bound), _threads(threads))
+    return C, bound, exact
+
+
+def gemm_nvfp4_sample(A, B, sfa_codes, sfb_codes, ga: float, gb: float, pi, pj,
+                      out_kind: int = OUT_BF16, threads=None):
+    """Only the elements (pi[s], pj[s]) of gemm_nvfp4."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sfa = np.ascontiguousarray(nvfp4_scales(sfa_codes))
+    sfb = np.ascontiguousarray(nvfp4_scales(sfb_codes))
+    pi = np.ascontiguousarray(pi, dtype=np.int64)
+    pj = np.ascontiguousarray(pj, dtype=np.int64)
+    M, K = A.shape
+    N = B.shape[0]
+    n = pi.size
+    C = np.empty(n, dtype=np.float32)
+    bound = np.empty(n, dtype=np.float64)
+    exact = np.empty(n, dtype=np.float64)
+    _L().oracle_gemm_nvfp4_sample(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb), M, N, K,
+                                  int(out_kind), _p(pi), _p(pj), n, _p(C), _p(exact), _p(bound),
+                                  _threads(threads))
     return C, bound, exact
 
 

@@ -34,6 +34,12 @@
  *     multiply B[e] (MoE paragraph of the JAX/Blackwell page).
  *   - The grouped raster order of output tiles ("GROUP_M" swizzle of the
  *     persistent matmul in the Triton tutorial ch. 12, section 12.7).
+ *   - NVFP4 (the other FP4 micro-scaling format the Triton tutorial ch. 12,
+ *     section 12.6.1 names, beside MXFP8 / MXFP4): E2M1 elements, one E4M3
+ *     block scale per 16 elements along K, one fp32 scale per tensor.  The
+ *     pages print no recipe; the reading taken is stated at
+ *     oracle_quantize_nvfp4.  GEMM: the 1x16 block-scaled sum times
+ *     alpha = fl32(gA gB), rounded once: fl32(alpha * sum).
  *   - A fused epilogue after the GEMM value v: act(v + bias[j]) with act none,
  *     ReLU or GELU (the bias_add_relu case in the benchmark list of the Triton
  *     FP8 benchmarking page; GELU in its erf form x * Phi(x)), in fp64.
@@ -392,6 +398,8 @@ typedef struct {
     int64_t n_samples;
     const float *bias;      /* fused epilogue: [N] (nullable) */
     int act;
+    int use_alpha;          /* block mode: v = fl32(alpha * sum) (NVFP4's global scales) */
+    float alpha;
 } gemm_job;
 
 static double dec_e4m3[256], dec_e5m2[256], dec_e2m1[256];
@@ -406,8 +414,10 @@ static const double *table_of(int fmt) {
     return fmt == ORACLE_E2M1 ? dec_e2m1 : fmt == ORACLE_E5M2 ? dec_e5m2 : dec_e4m3;
 }
 
-/* One output element.  Block mode:
+/* One output element.  Block mode (block = 16: 1x16 blocks, scales
+ * [M,K/16], [N,K/16]; any other nonzero value: 1x32 blocks):
  *   v = sum_kb sfa[i,kb] * sfb[j,kb] * (sum_{k in kb} dec(a_ik) dec(b_jk))
+ * and with use_alpha v = fl32(alpha * v).
  * Tensor mode:
  *   acc = sum_k dec(a_ik) dec(b_jk), alpha = fl32(sA * sB), v = fl32(alpha * acc)
  * The tolerance bound is 2^-8 * sum_k |sA a_ik| |sB b_jk| + 1 bf16 ulp of the
@@ -418,11 +428,12 @@ static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, dou
     const uint8_t *b = g->B + j * g->K;
     double v, absum = 0.0;
     if (g->block) {
-        int64_t nb = g->K / 32;
+        const int64_t bs = g->block == 16 ? 16 : 32;
+        int64_t nb = g->K / bs;
         double total = 0.0;
         for (int64_t kb = 0; kb < nb; ++kb) {
             double part = 0.0, apart = 0.0;
-            for (int64_t k = kb * 32; k < kb * 32 + 32; ++k) {
+            for (int64_t k = kb * bs; k < kb * bs + bs; ++k) {
                 double p = g->ta[a[k]] * g->tb[b[k]];
                 part += p;
                 apart += fabs(p);
@@ -432,6 +443,10 @@ static void one_element(const gemm_job *g, int64_t i, int64_t j, float *out, dou
             absum += fabs(sc) * apart;
         }
         v = total;
+        if (g->use_alpha) {
+            v = (double)(float)((double)g->alpha * total);
+            absum *= fabs((double)g->alpha);
+        }
     } else {
         double acc = 0.0, aacc = 0.0;
         for (int64_t k = 0; k < g->K; ++k) {
@@ -579,6 +594,69 @@ ORACLE_EXPORT void oracle_gemm_sample(const uint8_t *A, const uint8_t *B, const 
                                       double *bound, int threads) {
     oracle_gemm_sample_fmt(A, B, sfa, sfb, block, ORACLE_E4M3, ORACLE_E4M3, M, N, K, out_kind, pi,
                            pj, n, C, exact, bound, threads);
+}
+
+/* NVFP4 GEMM: A, B E2M1 codes (one per byte) [M,K], [N,K]; sfa, sfb the
+ * decoded block scales [M,K/16], [N,K/16] (exact in fp32); ga, gb the
+ * tensors' fp32 scales.  C = out(fl32(fl32(ga gb) * sum)).  K % 16 == 0. */
+ORACLE_EXPORT void oracle_gemm_nvfp4(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                     const float *sfb, float ga, float gb, int64_t M, int64_t N,
+                                     int64_t K, int out_kind, float *C, double *exact,
+                                     double *bound, int threads) {
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = 16;
+    g.ta = table_of(ORACLE_E2M1); g.tb = table_of(ORACLE_E2M1);
+    g.use_alpha = 1; g.alpha = ga * gb;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    run_jobs(g, M, threads);
+}
+
+ORACLE_EXPORT void oracle_gemm_nvfp4_sample(const uint8_t *A, const uint8_t *B, const float *sfa,
+                                            const float *sfb, float ga, float gb, int64_t M,
+                                            int64_t N, int64_t K, int out_kind, const int64_t *pi,
+                                            const int64_t *pj, int64_t n, float *C, double *exact,
+                                            double *bound, int threads) {
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = 16;
+    g.ta = table_of(ORACLE_E2M1); g.tb = table_of(ORACLE_E2M1);
+    g.use_alpha = 1; g.alpha = ga * gb;
+    g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
+    g.C = C; g.exact = exact; g.bound = bound;
+    g.pi = pi; g.pj = pj; g.n_samples = n;
+    run_jobs(g, n, threads);
+}
+
+/* NVFP4 quantisation of x [rows, cols] (cols % 16 == 0), the reading taken
+ * (the pages name the format and print no recipe):
+ *   g = fl32(amax / 2688) over the non-NaN |x| (2688 = 6 x 448, the largest
+ *       E2M1 value times the largest E4M3 scale), 1 when that is 0;
+ *   per 1x16 block along cols: t = fl32(amax_b / fl32(6 g)),
+ *       s = the E4M3 code of t, round to nearest even, saturating (t >= 0);
+ *   elements: d = fl32(dec(s) * g); q = the E2M1 code of fl32(x / d), round
+ *       to nearest even, saturating, NaN -> +6; all codes 0 when d is 0.
+ * q: one E2M1 code per byte [rows, cols]; sf: E4M3 codes [rows, cols/16];
+ * g_out: g. */
+ORACLE_EXPORT void oracle_quantize_nvfp4(const float *x, int64_t rows, int64_t cols, uint8_t *q,
+                                         uint8_t *sf, float *g_out) {
+    const float amax = amax_of(x, rows * cols, 1);
+    float g = amax / 2688.0f;
+    if (g == 0.0f) g = 1.0f;
+    const float g6 = 6.0f * g;
+    const int64_t nb = cols / 16;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *xb = x + r * cols + b * 16;
+            uint8_t *qb = q + r * cols + b * 16;
+            const float t = amax_of(xb, 16, 1) / g6;
+            const uint8_t s = oracle_e4m3_encode(t);
+            const float d = (float)oracle_e4m3_decode(s) * g;
+            for (int k = 0; k < 16; ++k) qb[k] = d > 0.0f ? oracle_e2m1_encode(xb[k] / d) : 0;
+            sf[r * nb + b] = s;
+        }
+    *g_out = g;
 }
 
 /* ------------------------------------------------------------------ */
