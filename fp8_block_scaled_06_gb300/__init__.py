@@ -45,7 +45,8 @@ EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
-    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows", "fp8_gemm_blockscaled_promote", "fp8g_wait_selftest",
+    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows",
+    "fp8_gemm_blockscaled_promote", "fp8g_quantize_nvfp4", "fp8_gemm_nvfp4", "fp8g_wait_selftest",
     "fp8g_kernel_timing_begin", "fp8g_kernel_timing_end",
     "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
@@ -98,6 +99,11 @@ def load():
         lib.fp8g_quantize_e4m3.argtypes = [P, i64, i64, i32, P, P, P]
         lib.fp8g_quantize.restype = st
         lib.fp8g_quantize.argtypes = [P, i64, i64, i32, i32, P, P, P]
+        lib.fp8g_quantize_nvfp4.restype = st
+        lib.fp8g_quantize_nvfp4.argtypes = [P, i32, i64, i64, P, P, P, P]
+        lib.fp8_gemm_nvfp4.restype = st
+        lib.fp8_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, P, i32, i64, i64, i64,
+                                       P]
         lib.fp8_gemm_fmt.restype = st
         lib.fp8_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, i64, i64, i64, P]
         lib.fp8_gemm_blockscaled_fmt.restype = st
@@ -281,6 +287,33 @@ def fp8_gemm_blockscaled_promote(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt:
                                                int(out), int(a_fmt), int(b_fmt), _ptr(bias),
                                                int(act), M, N, K, _stream(stream)),
            "fp8_gemm_blockscaled_promote")
+
+
+def fp8g_quantize_nvfp4(x, in_dtype: int, rows: int, cols: int, q, sf, g, stream=None):
+    _check(load().fp8g_quantize_nvfp4(_ptr(x), int(in_dtype), rows, cols, _ptr(q), _ptr(sf),
+                                      _ptr(g), _stream(stream)), "fp8g_quantize_nvfp4")
+
+
+def fp8_gemm_nvfp4(A, B, sfa, sfb, ga, gb, C, out: int, bias, act: int, M: int, N: int, K: int,
+                   stream=None):
+    _check(load().fp8_gemm_nvfp4(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ga), _ptr(gb),
+                                 _ptr(C), int(out), _ptr(bias), int(act), M, N, K,
+                                 _stream(stream)), "fp8_gemm_nvfp4")
+
+
+def quantize_nvfp4(x, stream=None):
+    """fp32 or bf16 CUDA tensor [rows, cols] -> (codes uint8 [rows, cols/2],
+    E4M3 block-scale codes uint8 [rows, cols/16], tensor scale fp32 [1])."""
+    import torch
+    assert x.is_cuda and x.dim() == 2 and x.dtype in (torch.float32, torch.bfloat16)
+    x = x.contiguous()
+    rows, cols = x.shape
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+    g = torch.empty((1,), dtype=torch.float32, device=x.device)
+    dt = FP8G_IN_BF16 if x.dtype == torch.bfloat16 else FP8G_IN_F32
+    fp8g_quantize_nvfp4(x, dt, rows, cols, q, sf, g, stream)
+    return q, sf, g
 
 
 def fp8g_quantize_rows(x, in_dtype: int, x_rows: int, cols: int, rows, n_rows: int, block: int,

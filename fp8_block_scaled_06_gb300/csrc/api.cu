@@ -509,6 +509,111 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
+fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa, const uint8_t *sfb,
+                           const float *ga, const float *gb, void *C, int out, const float *bias,
+                           int32_t act, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    fp8g_status st = check_common(A, B, C, out, M, N, K);
+    if (st != FP8G_OK) return st;
+    if (sfa == nullptr || sfb == nullptr || ga == nullptr || gb == nullptr)
+        return FP8G_ERR_INVALID_ARG;
+    if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
+        return FP8G_ERR_INVALID_ARG;
+    if (K % 256 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(A, 32) || !aligned(B, 32) || !aligned(sfa, 4) || !aligned(sfb, 4) ||
+        !aligned(ga, 4) || !aligned(gb, 4))
+        return FP8G_ERR_ALIGNMENT;
+    if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
+    DevInfo di;
+    if ((st = device_info(di)) != FP8G_OK) return st;
+    // CTA pairs (kind::mxf4nvf4 is issued with cta_group::2) whatever the shape
+    KernelChoice kc;
+    kc.BM = 256;
+    kc.BN = 256;
+    kc.b_rows = 128;
+    kc.split = 1;
+    kc.cluster = 2;
+    kc.pair = true;
+    const int64_t pairs = ((M + 255) / 256) * ((N + 255) / 256);
+    kc.grid = (int)(2 * (pairs < di.num_sms / 2 ? pairs : di.num_sms / 2));
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_kb = (int32_t)(K / 256);
+    p.npm = (int32_t)((M + 255) / 256);
+    p.npn = (int32_t)((N + 255) / 256);
+    p.T = (int64_t)p.npm * p.npn;
+    p.split = 1;
+    p.kb_per_split = p.num_kb;
+    p.C = C;
+    p.status = di.status;
+    p.timeout_ns = timeout_ns();
+    p.f4 = 2;
+    p.ga = ga;
+    p.gb = gb;
+    p.bias = bias;
+    p.act = act;
+    p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
+    const int32_t n_kg = (int32_t)(K / 64);  // 64-wide K groups: one MMA's four scales
+    p.n_rtA = (int32_t)((M + kBM - 1) / kBM);
+    p.n_rtB = (int32_t)(p.npn * 2);
+    if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    GemmMaps maps;
+    {
+        // packed codes as dense bytes, K / 2 per row (128 bytes = 256 codes per box row)
+        const uint64_t dA[2] = {(uint64_t)(K / 2), (uint64_t)M};
+        const uint64_t dB[2] = {(uint64_t)(K / 2), (uint64_t)N};
+        const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
+        const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
+        if ((st = tmap_operand(A, FP8G_E4M3, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
+        if ((st = tmap_operand(B, FP8G_E4M3, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+    }
+    const size_t bytesA = packed_scale_bytes(n_kg, p.n_rtA, 1);
+    const size_t bytesB = packed_scale_bytes(n_kg, p.n_rtB, 1);
+    cudaMemPool_t pool;
+    if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    uint8_t *pkA = static_cast<uint8_t *>(ws);
+    uint8_t *pkB = pkA + bytesA;
+    cudaError_t e = launch_pack_nvfp4(sfa, M, p.n_rtA, pkA, sfb, N, p.n_rtB, pkB, n_kg, K / 16,
+                                      stream);
+    if (e == cudaSuccess) {
+        const uint64_t dSA[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtA};
+        const uint32_t bSA[2] = {128u, 1u};
+        const uint64_t dSB[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtB};
+        const uint32_t bSB[2] = {128u, 2u};
+        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
+            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSB, bSB,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
+            e = cudaErrorInvalidValue;
+    }
+    if (e == cudaSuccess)
+        e = timed_launch(stream, [&] {
+            return launch_gemm(kModeBlock, out == FP8G_OUT_F32, maps, p, kc, stream);
+        });
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+fp8g_status fp8g_quantize_nvfp4(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,
+                                uint8_t *q, uint8_t *sf, float *g, cudaStream_t stream) {
+    if (x == nullptr || q == nullptr || sf == nullptr || g == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (in_dtype != FP8G_IN_F32 && in_dtype != FP8G_IN_BF16) return FP8G_ERR_INVALID_ARG;
+    if (rows < 1 || cols < 1) return FP8G_ERR_INVALID_ARG;
+    if (cols % 16 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (rows >= ((int64_t)1 << 40) / cols || rows > INT32_MAX) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(q, 4) || !aligned(g, 4)) return FP8G_ERR_ALIGNMENT;
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const cudaError_t e = launch_quantize_nvfp4(x, in_dtype == FP8G_IN_BF16, rows, cols, q, sf, g,
+                                                di.status, di.num_sms, stream);
+    return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
 fp8g_status fp8_gemm_blockscaled_fmt(const void *A, const void *B, const float *sfa,
                                      const float *sfb, void *C, int out, int32_t a_fmt,
                                      int32_t b_fmt, int64_t M, int64_t N, int64_t K,

@@ -27,13 +27,17 @@
 // is released as soon as it is in registers) is allocated and freed by both
 // CTAs together.
 //
-// F4 (E2M1 x E2M1 with 1x32 power-of-two scales, i.e. MXFP4, at the FP4
+// F4 = 1 (E2M1 x E2M1 with 1x32 power-of-two scales, i.e. MXFP4, at the FP4
 // rate): kind::mxf4 reads dense 4-bit operands, so the packed codes are
 // loaded as plain bytes and a 128-byte swizzled row of a stage holds 256 K
 // elements; each of the four MMAs per stage takes K = 64 (32 bytes, the same
 // descriptor step as FP8) with two scale bytes per row.  A stage therefore
 // carries two 128-wide K groups of packed scales (3 KB: A's two chunks, B's
 // two pairs of chunks), copied to a second set of scale columns.
+// F4 = 2 (NVFP4: 1x16 E4M3 block scales, kind::mxf4nvf4 scale_vec::4X): the
+// same operand stages, but each MMA reads four scale bytes per row, so a stage
+// carries four 64-wide K groups of scales (6 KB); tensor memory then holds
+// 12 scale columns per group (48 per stage), which leaves room for 5 stages.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -47,7 +51,6 @@ namespace {
 constexpr int kThreads = 640;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
-constexpr int kStages = 6;
 constexpr int kPairBN = 256;                 // output tile: 256 x 256 per pair
 constexpr int kA = kBM * kBK;                // 16 KB: this CTA's 128 rows of A
 constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
@@ -65,32 +68,38 @@ constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
 constexpr int kSfaBytes = 512;
 constexpr int kSfbBytes = 1024;  // B's two 128-row chunks
 
-template <int MODE, bool F4>
+template <int MODE, int F4>
 struct PairCfg {
     static constexpr bool kBlock = MODE != kModeTensor;
-    static_assert(kBlock || !F4, "FP4-rate MMAs are block-scaled");
-    // packed scales per stage (F4: two 128-wide K groups)
-    static constexpr int CHUNK = kBlock ? (F4 ? 2 : 1) * (kSfaBytes + kSfbBytes) : 0;
+    static_assert(kBlock || F4 == 0, "FP4-rate MMAs are block-scaled");
+    static constexpr int STAGES = F4 == 2 ? 5 : 6;
+    // K groups of packed scales per stage: 128-wide (FP8, MXFP4) or 64-wide (NVFP4)
+    static constexpr int G = F4 == 2 ? 4 : F4 == 1 ? 2 : 1;
+    static constexpr int CHUNK = kBlock ? G * (kSfaBytes + kSfbBytes) : 0;  // packed scales per stage
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + kStages * kA;
-    static constexpr int OFF_SF = OFF_B + kStages * kB;
-    static constexpr int OFF_BAR = OFF_SF + kStages * CHUNK;
+    static constexpr int OFF_B = OFF_A + STAGES * kA;
+    static constexpr int OFF_SF = OFF_B + STAGES * kB;
+    static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK;
     // Accumulators: per-tensor double-buffers the 256-column accumulator (the
     // next tile's MMAs never wait for the epilogue); block modes keep one and
     // use the other columns for the scale factors of each stage.
     static constexpr int NUM_ACC = kBlock ? 1 : 2;
     // full, (spare), empty [S]; acc_full, acc_empty [NUM_ACC]; drain (MMA
     // thread), drain (scale-copy thread), scales ready [S]
-    static constexpr int NUM_BARS = 4 * kStages + 2 * NUM_ACC + 2;
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;  // row_off, tile_off, rt_off [E + 1]
     static constexpr int SMEM_BYTES = OFF_GROUP + 3 * (FP8G_MAX_EXPERTS + 1) * 4 + 1024;
     static constexpr uint32_t TX = kA + kB + CHUNK;            // bytes per CTA per stage
-    // A: cols 0-3, B: cols 8-15 (F4: the second K group's at 16-19, 24-31)
-    static constexpr int SF_COLS = kBlock ? (F4 ? 32 : 16) : 0;
+    // Scale columns of K group g of a stage: A's at g SFG .. + 3, B's 256 rows
+    // at g SFG + SFB .. + 7 (FP8 / MXFP4: A 0-3, B 8-15, the second group 16
+    // later; NVFP4: packed 12 per group)
+    static constexpr int SFG = F4 == 2 ? 12 : 16;
+    static constexpr int SFB = F4 == 2 ? 4 : 8;
+    static constexpr int SF_COLS = kBlock ? G * SFG : 0;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
-    static_assert(256 + kStages * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
+    static_assert(256 + STAGES * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
     static_assert(OFF_SF % 128 == 0 && CHUNK % 128 == 0, "TMA destination alignment");
 };
 constexpr int kCW = kPairBN / 4;  // columns per epilogue warp
@@ -149,7 +158,7 @@ __device__ __forceinline__ PairTile pair_tile(int32_t t, const GemmParams &p, co
     return ti;
 }
 
-template <int MODE, bool OUT_F32, bool F4>
+template <int MODE, bool OUT_F32, int F4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA,
@@ -166,13 +175,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PC::OFF_BAR);
     auto bar_full = [&](int s) { return ptx::smem_addr(&bars[s]); };
-    auto bar_peer = [&](int s) { return ptx::smem_addr(&bars[kStages + s]); };
-    auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[2 * kStages + s]); };
-    auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[3 * kStages + a]); };
-    auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[3 * kStages + PC::NUM_ACC + a]); };
-    const uint32_t bar_drain = ptx::smem_addr(&bars[3 * kStages + 2 * PC::NUM_ACC]);
-    const uint32_t bar_drain_sf = ptx::smem_addr(&bars[3 * kStages + 2 * PC::NUM_ACC + 1]);
-    auto bar_sfr = [&](int s) { return ptx::smem_addr(&bars[3 * kStages + 2 * PC::NUM_ACC + 2 + s]); };
+    auto bar_peer = [&](int s) { return ptx::smem_addr(&bars[PC::STAGES + s]); };
+    auto bar_empty = [&](int s) { return ptx::smem_addr(&bars[2 * PC::STAGES + s]); };
+    auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[3 * PC::STAGES + a]); };
+    auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[3 * PC::STAGES + PC::NUM_ACC + a]); };
+    const uint32_t bar_drain = ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC]);
+    const uint32_t bar_drain_sf = ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 1]);
+    auto bar_sfr = [&](int s) { return ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 2 + s]); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PC::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + PC::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + PC::OFF_GROUP);
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < PC::STAGES; ++s) {
             ptx::mbar_init(bar_full(s), 1);
             ptx::mbar_init(bar_peer(s), 1);
             ptx::mbar_init(bar_empty(s), 1);
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // load counts only its packed bytes
             const uint32_t tx_bytes =
                 F4 ? PC::TX : PC::TX - (p.a_e2m1 ? kA / 2 : 0) - (p.b_e2m1 ? kB / 2 : 0);
-            const int32_t num_kg = F4 ? 2 * p.num_kb : p.num_kb;  // K groups of the packed scales
+            const int32_t num_kg = PC::G * p.num_kb;  // K groups of the packed scales
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {
                 const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
@@ -267,10 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (PC::kBlock) {
                         // packed UE8M0 chunks (512-byte rows of the packed arrays):
                         // this CTA's 128 rows of A; the tile's 256 rows of B
-                        // (F4: K groups 2 kb and 2 kb + 1, A's two chunks first,
-                        // then B's two pairs)
+                        // (G > 1: K groups G kb .. G kb + G - 1, A's chunks first,
+                        // then B's pairs)
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
-                        constexpr int G = F4 ? 2 : 1;
+                        constexpr int G = PC::G;
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const int32_t kg = G * kb + g;
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   (ti.e * num_kg + kg) * p.n_rtB + 2 * ti.pn);
                         }
                     }
-                    if (++stage == kStages) {
+                    if (++stage == PC::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -310,7 +319,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t a0 = sbase + PC::OFF_A + stage * kA;
                     const uint32_t b0 = sbase + PC::OFF_B + stage * kB;
-                    if constexpr (F4) {
+                    if constexpr (F4 == 2) {
+                        // MMA k: K elements 64k .. 64k + 63 = K group k's four
+                        // 16-wide scale blocks (the whole word, sf_id 0)
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k) {
+                            const uint32_t sfk = sf + PC::SFG * k;
+                            ptx::mma_nvf4_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                               ptx::desc_kmajor_sw128(b0 + k * 32),
+                                               ptx::idesc_nvf4(2 * kBM, kPairBN), sfk,
+                                               sfk + PC::SFB, (kb | k) != 0 ? 1u : 0u);
+                        }
+                    } else if constexpr (F4 == 1) {
                         // MMA k: K elements 64k .. 64k + 63 = scale blocks 2k, 2k + 1,
                         // in K group k / 2 (columns + 16 (k / 2)), bytes 2 (k % 2), + 1
                         const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
@@ -338,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              (kb | k) != 0 ? 1u : 0u);
                     }
                     ptx::tc_commit_pair_mc(bar_empty(stage), 0x3);
-                    if (++stage == kStages) {
+                    if (++stage == PC::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -359,20 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                     const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
-                    constexpr int G = F4 ? 2 : 1;
+                    constexpr int G = PC::G;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        // K group g: A's rows to columns 16 g + 0-3; B's rows 0-127
-                        // to 16 g + 8-11, rows 128-255 to 16 g + 12-15 (each
-                        // replicated over the lane quarters by the copy)
-                        const uint32_t sfg = sf + 16 * g;
+                        // K group g: A's rows to columns SFG g + 0-3; B's rows
+                        // 0-127 to SFG g + SFB + 0-3, rows 128-255 to the next
+                        // four (each replicated over the lane quarters by the copy)
+                        const uint32_t sfg = sf + PC::SFG * g;
                         const uint32_t cb = cs + G * kSfaBytes + g * kSfbBytes;
                         ptx::tc_cp_32x128b_warpx4_pair(sfg, ptx::desc_sf_chunk(cs + g * kSfaBytes));
-                        ptx::tc_cp_32x128b_warpx4_pair(sfg + 8, ptx::desc_sf_chunk(cb));
-                        ptx::tc_cp_32x128b_warpx4_pair(sfg + 12, ptx::desc_sf_chunk(cb + 512));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB, ptx::desc_sf_chunk(cb));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB + 4,
+                                                       ptx::desc_sf_chunk(cb + 512));
                     }
                     ptx::tc_commit_pair_mc(bar_sfr(stage), 0x1);
-                    if (++stage == kStages) {
+                    if (++stage == PC::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -386,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = (ew >> 2) * kCW;
         float alpha = 1.0f;
         if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        if constexpr (F4 == 2) alpha = __fmul_rn(p.ga[0], p.gb[0]);  // NVFP4 tensor scales
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
@@ -418,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // FP4-rate tiles end twice as often: their stores go out as whole
             // 128-byte row segments (measured 8192^3: +1.8%; on the FP8-rate
             // tiles the shuffles cost more than the coalescing saves, -0.5%)
-            if (F4 && p.st32) {
+            if (F4 != 0 && p.st32) {
                 store_rows64<OUT_F32>(p.C, row, p.N, ncol0, r, a_t, lane);  // whole warp
             } else if (row >= 0) {
 #pragma unroll
@@ -454,7 +477,7 @@ roles_done:
     }
 }
 
-template <int MODE, bool OUT_F32, bool F4 = false>
+template <int MODE, bool OUT_F32, int F4 = 0>
 cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cudaStream_t stream) {
     using PC = PairCfg<MODE, F4>;
     auto kern = gemm_pair_kernel<MODE, OUT_F32, F4>;
@@ -489,12 +512,15 @@ cudaError_t launch_pair(const GemmMaps &maps, const GemmParams &p, int grid, cud
 
 cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                              int grid, cudaStream_t stream) {
-    if (p.f4 && mode == kModeBlock)
-        return out_f32 ? launch_pair<kModeBlock, true, true>(maps, p, grid, stream)
-                       : launch_pair<kModeBlock, false, true>(maps, p, grid, stream);
-    if (p.f4 && mode == kModeGrouped)
-        return out_f32 ? launch_pair<kModeGrouped, true, true>(maps, p, grid, stream)
-                       : launch_pair<kModeGrouped, false, true>(maps, p, grid, stream);
+    if (p.f4 == 2 && mode == kModeBlock)
+        return out_f32 ? launch_pair<kModeBlock, true, 2>(maps, p, grid, stream)
+                       : launch_pair<kModeBlock, false, 2>(maps, p, grid, stream);
+    if (p.f4 == 1 && mode == kModeBlock)
+        return out_f32 ? launch_pair<kModeBlock, true, 1>(maps, p, grid, stream)
+                       : launch_pair<kModeBlock, false, 1>(maps, p, grid, stream);
+    if (p.f4 == 1 && mode == kModeGrouped)
+        return out_f32 ? launch_pair<kModeGrouped, true, 1>(maps, p, grid, stream)
+                       : launch_pair<kModeGrouped, false, 1>(maps, p, grid, stream);
     if (p.f4) return cudaErrorInvalidValue;
     if (mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true>(maps, p, grid, stream)

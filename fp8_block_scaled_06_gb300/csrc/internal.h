@@ -49,7 +49,8 @@ struct GemmParams {
     // E2M1 x E2M1 block-scaled on CTA pairs at the FP4 rate (kind::mxf4):
     // operands loaded as dense bytes, 256 K elements per stage, num_kb = K /
     // 256, the packed scale arrays holding 2 * num_kb chunks per row tile.
-    int32_t f4;
+    int32_t f4;               // 1: MXFP4 (kind::mxf4); 2: NVFP4 (kind::mxf4nvf4, 1x16 E4M3 scales)
+    const float *ga, *gb;     // NVFP4: the tensors' fp32 scales (epilogue alpha = fl32(ga gb))
     int32_t st32;             // epilogue: 32-byte stores (C 32-byte aligned, rows multiples of 32 B)
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
@@ -115,6 +116,11 @@ struct PackArgs {
     const int32_t *counts;
     int32_t rep;  // B of single-CTA 256-wide tiles: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
 };
+// NVFP4: E4M3 scale codes [rows, K/16] -> the same 512-byte chunks, a K group
+// being 64 wide (4 blocks of 16, one MMA's word); rows past the operand 1.0.
+cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
+                              const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
+                              int32_t n_kg, int64_t sfc, cudaStream_t s);
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
                                int32_t E, unsigned int *status, cudaStream_t s);
@@ -124,6 +130,9 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
 // x [x_rows, cols] (fp32, or bf16 if in_bf16); block 0 per-tensor or 32; fmt
 // FP8G_E4M3 / FP8G_E5M2.  Bad row indices record FP8G_ERR_INVALID_ARG.
 // block FP8G_BLOCK32_LITERAL: 1x32 blocks with s = fl32(amax / fmax).
+cudaError_t launch_quantize_nvfp4(const void *x, int in_bf16, int64_t rows, int64_t cols,
+                                  uint8_t *q, uint8_t *sf, float *g, unsigned int *status,
+                                  int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int64_t cols,
                                  const int32_t *rows, int64_t n_rows, int32_t block, int fmt,
                                  uint8_t *q, float *scales, unsigned int *status, int num_sms,

@@ -350,6 +350,19 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// kind::mxf4nvf4, scale_vec::4X: dense 4-bit E2M1 operands, K = 64, four
+// E4M3 (UE4M3) scales per row, one per 16 elements (the whole 32-bit word).
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
@@ -448,6 +461,12 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
 // (a pair of scale bytes per row).
 __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id) {
     return idesc_mxf8(M, N, sf_id) | (1u << 7) | (1u << 10);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with UE4M3 scales: A and B E2M1
+// (format 1), scale type bit 23 clear (UE4M3), scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+    return (idesc_mxf8(M, N, 0) & ~(1u << 23)) | (1u << 7) | (1u << 10);
 }
 
 }  // namespace ptx

@@ -292,6 +292,61 @@ __global__ void __launch_bounds__(kQThreads) quant_tensor_kernel(RowMap m, int64
 template <int FMT>
 __global__ void finish_scale_kernel(float *slot) { *slot = tensor_scale<FMT>(slot); }
 
+// ---------------------------------------------------------------- NVFP4
+// E4M3 value of a non-negative code (0x7F: NaN), from its bit fields.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (c == 0x7Fu) return __int_as_float(0x7FC00000);
+    return e == 0 ? (float)m * 0.001953125f : __int_as_float((int)((e + 120u) << 23 | m << 20));
+}
+
+// g = fl32(amax / 2688) (2688 = 6 x 448), 1 when that is 0.
+__device__ __forceinline__ float nvfp4_g(const float *amax_slot) {
+    float g = __fdiv_rn(*amax_slot, 2688.0f);
+    if (g == 0.0f) g = 1.0f;
+    return g;
+}
+
+// NVFP4: a 1x16 block is two groups of 8 held by two consecutive lanes.  Per
+// block t = fl32(amax_b / fl32(6 g)), s = E4M3(t) (RNE, saturating), d =
+// fl32(dec(s) g), codes E2M1(fl32(x / d)) (all 0 when d is not positive).
+// q: two codes per byte [rows, cols/2]; sf: one E4M3 code per block
+// [rows, cols/16]; the slot still holds the tensor's amax.
+template <bool BF16>
+__global__ void __launch_bounds__(kQThreads) quant_nvfp4_kernel(RowMap m, int64_t n_rows,
+                                                               uint8_t *__restrict__ q,
+                                                               uint8_t *__restrict__ sf,
+                                                               const float *amax_slot) {
+    const float g = nvfp4_g(amax_slot);
+    const float g6 = __fmul_rn(6.0f, g);
+    const int64_t gpr = m.cols / 8;  // groups of 8 per row
+    const int64_t wbase = threadIdx.x & ~31;
+    for (int64_t r = blockIdx.x; r < n_rows; r += gridDim.x) {
+        bool ok;
+        const int64_t sr = src_row(m, r, ok);
+        const int64_t in0 = sr * m.cols, out0 = r * gpr;
+        for (int64_t c0 = wbase; c0 < gpr; c0 += kQThreads) {
+            const int64_t c = c0 + (threadIdx.x & 31);
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (ok && c < gpr) load8<BF16>(m.x, in0 + c * 8, a, b);
+            float am = absmax8(a, b);
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            uint16_t sc;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(sc) : "f"(0.0f), "f"(__fdiv_rn(am, g6)));
+            const uint32_t s = sc & 0xFFu;
+            const float d = __fmul_rn(e4m3_value(s), g);
+            uint2 o = make_uint2(0u, 0u);
+            if (d > 0.0f) o = quant8<2>(a, b, d);
+            if (c < gpr) {
+                store8<2>(q, out0 + c, o);
+                if ((c & 1) == 0) sf[(out0 + c) >> 1] = (uint8_t)s;
+            }
+        }
+    }
+}
+
+__global__ void finish_nvfp4_kernel(float *slot) { *slot = nvfp4_g(slot); }
+
 }  // namespace
 
 namespace {
@@ -321,6 +376,28 @@ cudaError_t launch_rows(const RowMap &m, int64_t n_rows, int32_t block, uint8_t 
 }
 
 }  // namespace
+
+cudaError_t launch_quantize_nvfp4(const void *x, int in_bf16, int64_t rows, int64_t cols,
+                                  uint8_t *q, uint8_t *sf, float *g, unsigned int *status,
+                                  int num_sms, cudaStream_t s) {
+    const RowMap m{x, nullptr, rows, cols, status};
+    const int64_t cap = (int64_t)num_sms * 8;
+    const unsigned blocks = (unsigned)(rows < cap ? rows : cap);
+    cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    if (in_bf16) {
+        amax_kernel<true><<<blocks, kQThreads, 0, s>>>(m, rows, reinterpret_cast<unsigned int *>(g));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        quant_nvfp4_kernel<true><<<blocks, kQThreads, 0, s>>>(m, rows, q, sf, g);
+    } else {
+        amax_kernel<false><<<blocks, kQThreads, 0, s>>>(m, rows, reinterpret_cast<unsigned int *>(g));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        quant_nvfp4_kernel<false><<<blocks, kQThreads, 0, s>>>(m, rows, q, sf, g);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    finish_nvfp4_kernel<<<1, 1, 0, s>>>(g);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int64_t cols,
                                  const int32_t *rows, int64_t n_rows, int32_t block, int fmt,

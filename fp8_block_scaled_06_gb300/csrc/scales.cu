@@ -158,7 +158,50 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
             atomicExch(&status[1], 0u);
 }
 
+// NVFP4 scale codes: one thread per (operand, row, 64-wide K group): the
+// group's four codes (4 consecutive bytes of the row) become word w = row / 32
+// of datapath d = row % 32 of the chunk; consecutive threads take consecutive
+// groups of one row (coalesced loads).  Rows past the operand: 1.0 (0x38).
+__global__ void __launch_bounds__(256) pack_nvfp4_kernel(const uint8_t *sfa, int64_t rows_a,
+                                                        int32_t n_rt_a, uint8_t *dst_a,
+                                                        const uint8_t *sfb, int64_t rows_b,
+                                                        int32_t n_rt_b, uint8_t *dst_b,
+                                                        int32_t n_kg, int64_t sfc) {
+    ptx::grid_dep_launch();  // the GEMM may start its prologue now
+    const int64_t per_a = (int64_t)n_rt_a * kBM * n_kg;
+    const int64_t total = per_a + (int64_t)n_rt_b * kBM * n_kg;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const bool isa = i < per_a;
+        const int64_t k = isa ? i : i - per_a;
+        const int32_t kg = (int32_t)(k % n_kg);
+        const int64_t row = k / n_kg;
+        const uint8_t *src = isa ? sfa : sfb;
+        const int64_t rows = isa ? rows_a : rows_b;
+        const int32_t n_rt = isa ? n_rt_a : n_rt_b;
+        uint32_t word = 0x38383838u;
+        if (row < rows) word = __ldg(reinterpret_cast<const uint32_t *>(src + row * sfc) + kg);
+        const int64_t rt = row / kBM;
+        const int r = (int)(row % kBM);
+        uint8_t *out = (isa ? dst_a : dst_b) + ((int64_t)kg * n_rt + rt) * 512 + 16 * (r & 31) +
+                       4 * (r >> 5);
+        *reinterpret_cast<uint32_t *>(out) = word;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
+                              const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
+                              int32_t n_kg, int64_t sfc, cudaStream_t s) {
+    const int64_t total = ((int64_t)n_rt_a + n_rt_b) * kBM * n_kg;
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pack_nvfp4_kernel<<<(unsigned)blocks, 256, 0, s>>>(sfa, rows_a, n_rt_a, dst_a, sfb, rows_b,
+                                                       n_rt_b, dst_b, n_kg, sfc);
+    return cudaGetLastError();
+}
 
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
     return (size_t)z * (size_t)n_kg * (size_t)n_rt * 512u;

@@ -231,6 +231,42 @@ FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, i
                           int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);
 
 /*
+ * NVFP4 quantiser [TUT-12 12.6.1: NVFP4 among the fifth-generation tensor
+ * core's micro-scaling formats; the pages print no recipe, the reading taken
+ * is this]: E2M1 elements, one E4M3 scale per 1x16 block along cols, one fp32
+ * scale g per tensor.
+ *   g = fl32(amax / 2688) over the non-NaN |x| (2688 = 6 x 448), 1 if that is 0;
+ *   per block: t = fl32(amax_b / fl32(6 g)), s = E4M3(t) rounded to nearest
+ *   even, saturating; d = fl32(dec(s) g); q = E2M1(fl32(x / d)) rounded to
+ *   nearest even, saturating, NaN -> +6; all codes 0 when d is 0.
+ * x: device fp32 or bf16 (in_dtype) [rows, cols], 16-byte aligned, finite
+ * apart from NaNs; q: uint8 [rows, cols/2], two codes per byte (element 2j in
+ * the low nibble), 4-byte aligned; sf: uint8 E4M3 codes [rows, cols/16]; g:
+ * device fp32[1], 4-byte aligned.  cols % 16 == 0 (else
+ * FP8G_ERR_UNSUPPORTED_SHAPE).  Runs three kernels (amax, quantise, g).
+ */
+FP8G_API fp8g_status fp8g_quantize_nvfp4(const void *x, int32_t in_dtype, int64_t rows,
+                                         int64_t cols, uint8_t *q, uint8_t *sf, float *g,
+                                         cudaStream_t stream);
+
+/*
+ * NVFP4 GEMM [TUT-12 12.6.1]:
+ *   C[i,j] = out( act( fl32( fl32(ga gb) * sum_kb sa[i,kb] sb[j,kb] sum_{k in kb} a_ik b_jk ) + bias[j] ) )
+ * over 1x16 K blocks.  A [M, K/2], B [N, K/2]: E2M1 codes two per byte, as
+ * fp8g_quantize_nvfp4 writes them, 32-byte aligned; sfa [M, K/16], sfb
+ * [N, K/16]: E4M3 scale codes (positive; the tensor core applies them
+ * exactly), 4-byte aligned; ga, gb: device fp32[1] each (the tensors' g);
+ * bias (nullable) fp32 [N]; act an fp8g_act.  K % 256 == 0 (else
+ * FP8G_ERR_UNSUPPORTED_SHAPE).  Runs two kernels: the scale packing and the
+ * GEMM on CTA pairs with the FP4-rate kind::mxf4nvf4 MMA (scale_vec::4X),
+ * for every shape.  Parity: the tolerance of the block-scaled GEMM.
+ */
+FP8G_API fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa,
+                                    const uint8_t *sfb, const float *ga, const float *gb, void *C,
+                                    int out, const float *bias, int32_t act, int64_t M, int64_t N,
+                                    int64_t K, cudaStream_t stream);
+
+/*
  * `block` value of the quantisers for 1x32 blocks with the literal scale
  * s = fl32(amax / fmax) (1 when that is 0) — the "fp32 scale = block
  * amax/448" wording taken literally — and q = FP8(fl32(x / s)).  Such scales

@@ -125,11 +125,12 @@ def _L():
             lib.oracle_grouped_gemm.argtypes = [P, P, P, P, P, i32, i64, i64, ctypes.c_int, P,
                                                 P, P, ctypes.c_int]
             lib.oracle_quantize_nvfp4.argtypes = [P, i64, i64, P, P, P]
-            lib.oracle_gemm_nvfp4.argtypes = [P, P, P, P, ctypes.c_float, ctypes.c_float, i64, i64,
-                                              i64, ctypes.c_int, P, P, P, ctypes.c_int]
+            lib.oracle_gemm_nvfp4.argtypes = [P, P, P, P, ctypes.c_float, ctypes.c_float, P,
+                                              ctypes.c_int, i64, i64, i64, ctypes.c_int, P, P, P,
+                                              ctypes.c_int]
             lib.oracle_gemm_nvfp4_sample.argtypes = [P, P, P, P, ctypes.c_float, ctypes.c_float,
-                                                     i64, i64, i64, ctypes.c_int, P, P, i64, P, P,
-                                                     P, ctypes.c_int]
+                                                     P, ctypes.c_int, i64, i64, i64, ctypes.c_int,
+                                                     P, P, i64, P, P, P, ctypes.c_int]
             lib.oracle_gemm_flops.restype = ctypes.c_double
             lib.oracle_gemm_flops.argtypes = [i64, i64, i64]
             _lib = lib
@@ -303,10 +304,18 @@ def nvfp4_scales(sf_codes: np.ndarray) -> np.ndarray:
     return e4m3_table()[np.asarray(sf_codes, dtype=np.uint8)].astype(np.float32)
 
 
+def _bias(bias, N):
+    if bias is None:
+        return None
+    bias = np.ascontiguousarray(bias, dtype=np.float32)
+    assert bias.shape == (N,)
+    return bias
+
+
 def gemm_nvfp4(A, B, sfa_codes, sfb_codes, ga: float, gb: float, out_kind: int = OUT_BF16,
-               threads=None):
-    """C = out(fl32(fl32(ga gb) * sum_kb16 sa sb sum a b)) over E2M1 codes (one per
-    byte).  Returns (C float32 [M,N], bound float64 [M,N], exact [M,N])."""
+               threads=None, bias=None, act_kind: int = ACT_NONE):
+    """C = out(act(fl32(fl32(ga gb) * sum_kb16 sa sb sum a b) + bias)) over E2M1
+    codes (one per byte).  Returns (C float32 [M,N], bound float64 [M,N], exact [M,N])."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
     sfa = np.ascontiguousarray(nvfp4_scales(sfa_codes))
@@ -317,13 +326,15 @@ def gemm_nvfp4(A, B, sfa_codes, sfb_codes, ga: float, gb: float, out_kind: int =
     C = np.empty((M, N), dtype=np.float32)
     bound = np.empty((M, N), dtype=np.float64)
     exact = np.empty((M, N), dtype=np.float64)
-    _L().oracle_gemm_nvfp4(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb), M, N, K,
+    bias = _bias(bias, N)
+    _L().oracle_gemm_nvfp4(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb),
+                           _p(bias) if bias is not None else None, int(act_kind), M, N, K,
                            int(out_kind), _p(C), _p(exact), _p(bound), _threads(threads))
     return C, bound, exact
 
 
 def gemm_nvfp4_sample(A, B, sfa_codes, sfb_codes, ga: float, gb: float, pi, pj,
-                      out_kind: int = OUT_BF16, threads=None):
+                      out_kind: int = OUT_BF16, threads=None, bias=None, act_kind: int = ACT_NONE):
     """Only the elements (pi[s], pj[s]) of gemm_nvfp4."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -337,7 +348,9 @@ def gemm_nvfp4_sample(A, B, sfa_codes, sfb_codes, ga: float, gb: float, pi, pj,
     C = np.empty(n, dtype=np.float32)
     bound = np.empty(n, dtype=np.float64)
     exact = np.empty(n, dtype=np.float64)
-    _L().oracle_gemm_nvfp4_sample(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb), M, N, K,
+    bias = _bias(bias, N)
+    _L().oracle_gemm_nvfp4_sample(_p(A), _p(B), _p(sfa), _p(sfb), float(ga), float(gb),
+                                  _p(bias) if bias is not None else None, int(act_kind), M, N, K,
                                   int(out_kind), _p(pi), _p(pj), n, _p(C), _p(exact), _p(bound),
                                   _threads(threads))
     return C, bound, exact

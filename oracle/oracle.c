@@ -598,24 +598,27 @@ ORACLE_EXPORT void oracle_gemm_sample(const uint8_t *A, const uint8_t *B, const 
 
 /* NVFP4 GEMM: A, B E2M1 codes (one per byte) [M,K], [N,K]; sfa, sfb the
  * decoded block scales [M,K/16], [N,K/16] (exact in fp32); ga, gb the
- * tensors' fp32 scales.  C = out(fl32(fl32(ga gb) * sum)).  K % 16 == 0. */
+ * tensors' fp32 scales; bias (nullable) / act the fused epilogue.
+ * C = out(act(fl32(fl32(ga gb) * sum) + bias[j])).  K % 16 == 0. */
 ORACLE_EXPORT void oracle_gemm_nvfp4(const uint8_t *A, const uint8_t *B, const float *sfa,
-                                     const float *sfb, float ga, float gb, int64_t M, int64_t N,
-                                     int64_t K, int out_kind, float *C, double *exact,
-                                     double *bound, int threads) {
+                                     const float *sfb, float ga, float gb, const float *bias,
+                                     int act, int64_t M, int64_t N, int64_t K, int out_kind,
+                                     float *C, double *exact, double *bound, int threads) {
     gemm_job g;
     memset(&g, 0, sizeof g);
     g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = 16;
     g.ta = table_of(ORACLE_E2M1); g.tb = table_of(ORACLE_E2M1);
     g.use_alpha = 1; g.alpha = ga * gb;
+    g.bias = bias; g.act = act;
     g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
     g.C = C; g.exact = exact; g.bound = bound;
     run_jobs(g, M, threads);
 }
 
 ORACLE_EXPORT void oracle_gemm_nvfp4_sample(const uint8_t *A, const uint8_t *B, const float *sfa,
-                                            const float *sfb, float ga, float gb, int64_t M,
-                                            int64_t N, int64_t K, int out_kind, const int64_t *pi,
+                                            const float *sfb, float ga, float gb,
+                                            const float *bias, int act, int64_t M, int64_t N,
+                                            int64_t K, int out_kind, const int64_t *pi,
                                             const int64_t *pj, int64_t n, float *C, double *exact,
                                             double *bound, int threads) {
     gemm_job g;
@@ -623,6 +626,7 @@ ORACLE_EXPORT void oracle_gemm_nvfp4_sample(const uint8_t *A, const uint8_t *B, 
     g.A = A; g.B = B; g.sfa = sfa; g.sfb = sfb; g.block = 16;
     g.ta = table_of(ORACLE_E2M1); g.tb = table_of(ORACLE_E2M1);
     g.use_alpha = 1; g.alpha = ga * gb;
+    g.bias = bias; g.act = act;
     g.M = M; g.N = N; g.K = K; g.out_kind = out_kind;
     g.C = C; g.exact = exact; g.bound = bound;
     g.pi = pi; g.pj = pj; g.n_samples = n;
