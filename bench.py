@@ -46,6 +46,8 @@ WORKLOADS = {
     "literal8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, literal=True),
     # E2M1 x E2M1 with power-of-two 1x32 scales (MXFP4), two codes per byte
     "mxfp4_8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
+    # NVFP4: E2M1 with 1x16 E4M3 block scales and an fp32 scale per tensor
+    "nvfp4_8192": dict(kind="nvfp4", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
 }
 FMT_NAMES = ["e4m3", "e5m2", "e2m1"]
 # bytes per element of each format in memory (E2M1: two codes per byte)
@@ -139,6 +141,11 @@ def make_inputs(wl: dict, device):
         sb = sb.reshape(E, N, K // 32)
         counts = torch.from_numpy(w.counts).to(device)
         return w, dict(qa=qa, sa=sa, qb=qb, sb=sb, counts=counts)
+    if wl["kind"] == "nvfp4":
+        w = synth.large_block(wl["M"], seed=wl["seed"])
+        qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
+        qb, sb, gb = fp8g.quantize_nvfp4(w.B.to(device))
+        return w, dict(qa=qa, sa=sa, ga=ga, qb=qb, sb=sb, gb=gb)
     if wl["kind"] == "tensor":
         w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")
         bs = 0
@@ -163,6 +170,8 @@ def algorithmic_bytes(wl: dict, w) -> int:
         E = w.B.shape[0]
         return int(M * K * ea + E * N * K * eb + 4 * (M * K // 32 + E * N * K // 32) +
                    M * N * out_b + 4 * E)
+    if wl["kind"] == "nvfp4":   # E4M3 scale bytes per 16 elements + two fp32 tensor scales
+        return int(M * K * ea + N * K * eb + (M + N) * K // 16 + 8 + M * N * out_b)
     sf = 8 if wl["kind"] == "tensor" else 4 * (M * K // 32 + N * K // 32)
     return int(M * K * ea + N * K * eb + sf + M * N * out_b)
 
@@ -173,6 +182,9 @@ def run_once(fp8g, wl, w, t, C, stream):
         E, N, K = t["qb"].shape
         fp8g.fp8_grouped_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, t["counts"], E, N, K,
                               t["qa"].shape[0], None, None, stream)
+    elif wl["kind"] == "nvfp4":
+        fp8g.fp8_gemm_nvfp4(t["qa"], t["qb"], t["sa"], t["sb"], t["ga"], t["gb"], C, out, None,
+                            fp8g.FP8G_ACT_NONE, wl["M"], wl["N"], wl["K"], stream)
     elif wl["kind"] == "tensor":
         fp8g.fp8_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, wl["M"], wl["N"], wl["K"], stream)
     elif wl.get("literal"):
@@ -199,6 +211,8 @@ TRAFFIC_BYTES = {"large8192": 262_422_784 + 117_014_528,
 def fp4_rate(fp8g, wl) -> bool:
     """Whether the call runs the FP4-rate MMA: E2M1 x E2M1 block-scaled on CTA
     pairs with K % 256 == 0 (the library's own selection rule)."""
+    if wl["kind"] == "nvfp4":
+        return True                 # kind::mxf4nvf4 on CTA pairs for every shape
     if wl.get("a_fmt", 0) != 2 or wl.get("b_fmt", 0) != 2 or wl["K"] % 256:
         return False
     if wl["kind"] == "grouped":
@@ -213,7 +227,7 @@ def launches_per_call(fp8g, wl) -> int:
     block-scaled paths that do not split K (split-K converts scales itself)."""
     if wl["kind"] == "tensor":
         return 1
-    if wl["kind"] == "grouped":
+    if wl["kind"] in ("grouped", "nvfp4"):
         return 2
     if wl.get("literal"):
         return 1
@@ -304,6 +318,11 @@ def oracle_inputs(wl, w):
         return dict(A=qa[offs[e]:offs[e + 1]], sa=sa[offs[e]:offs[e + 1]],
                     B=qb.reshape(E, N, K)[e], sb=sb.reshape(E, N, K // 32)[e], block=True,
                     N=N, K=K, desc=f"rows of expert {e} (all {N} columns)")
+    if wl["kind"] == "nvfp4":
+        qa, sa, ga = oracle.quantize_nvfp4(w.A.numpy())
+        qb, sb, gb = oracle.quantize_nvfp4(w.B.numpy())
+        return dict(A=qa, sa=sa, B=qb, sb=sb, ga=ga, gb=gb, nv=True, block=True, N=wl["N"],
+                    K=wl["K"], desc=f"rows of A (all {wl['N']} columns)")
     block = wl["kind"] != "tensor"
     if wl.get("literal"):
         qa, sa = oracle.quantize_block32(w.A.numpy(), wl.get("a_fmt", 0), literal=True)
@@ -331,8 +350,12 @@ def cpu_baseline(oi: dict, budget_s: float = 12.0):
         a = np.ascontiguousarray(oi["A"][:r])
         s = np.ascontiguousarray(oi["sa"][:r]) if block else oi["sa"]
         t0 = time.perf_counter()
-        oracle.gemm(a, oi["B"], s, oi["sb"], block, oracle.OUT_BF16, threads=threads,
-                    a_fmt=oi.get("a_fmt", 0), b_fmt=oi.get("b_fmt", 0))
+        if oi.get("nv"):
+            oracle.gemm_nvfp4(a, oi["B"], s, oi["sb"], oi["ga"], oi["gb"], oracle.OUT_BF16,
+                              threads=threads)
+        else:
+            oracle.gemm(a, oi["B"], s, oi["sb"], block, oracle.OUT_BF16, threads=threads,
+                        a_fmt=oi.get("a_fmt", 0), b_fmt=oi.get("b_fmt", 0))
         dt = time.perf_counter() - t0
         spent += dt
         flops = 2.0 * r * N * K
@@ -476,7 +499,9 @@ def main():
                            f"{peaks['bf16']} TFLOP/s" if tensor_bound else
                            f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
     if f4 and tensor_bound:
-        roof["peak_source"] += " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)"
+        roof["peak_source"] += (" (NVFP4: the FP4-rate MMA, kind::mxf4nvf4 scale_vec::4X)"
+                                if wl["kind"] == "nvfp4" else
+                                " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)")
     elif 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
         roof["peak_source"] += " (E2M1 operands on the FP8-rate MMA, kind::f8f6f4)"
     roof["nominal_frac"] = round(max(flops / (13.5e15 if f4 else 4.5e15), abytes / 8e12) /
@@ -501,8 +526,9 @@ def main():
                               FMT_NAMES[wl.get("b_fmt", 0)],
                    "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
                               {"block": "1x32 along K, power of two",
-                              "grouped": "1x32 along K, power of two",
-                              "tensor": "per tensor"}[wl["kind"]]),
+                               "grouped": "1x32 along K, power of two",
+                               "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
+                               "tensor": "per tensor"}[wl["kind"]]),
                    "out": w.out, "l2": f"inputs rotated over {copies} copies > 2x L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roof,
@@ -537,7 +563,7 @@ def reference_arm(args, wl, world, rank):
     elif wl["M"] == 128:
         w = synth.skinny_block(seed=wl["seed"])
     else:
-        w = synth.large_block(wl["M"], seed=wl["seed"])
+        w = synth.large_block(wl["M"], seed=wl["seed"])   # block, nvfp4
     oi = oracle_inputs(wl, w)
     budget = min(10.0, max(0.01, 60.0 / (args.steps + args.warmup)))
     for _ in range(args.warmup):

@@ -580,10 +580,11 @@ fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa, con
     cudaError_t e = launch_pack_nvfp4(sfa, M, p.n_rtA, pkA, sfb, N, p.n_rtB, pkB, n_kg, K / 16,
                                       stream);
     if (e == cudaSuccess) {
+        // a stage's four K-group chunks are adjacent rows per 128-row tile
         const uint64_t dSA[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtA};
-        const uint32_t bSA[2] = {128u, 1u};
+        const uint32_t bSA[2] = {128u, 4u};
         const uint64_t dSB[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtB};
-        const uint32_t bSB[2] = {128u, 2u};
+        const uint32_t bSB[2] = {128u, 8u};
         if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
                         CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
             tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSB, bSB,

@@ -84,9 +84,13 @@ struct PairCfg {
     // next tile's MMAs never wait for the epilogue); block modes keep one and
     // use the other columns for the scale factors of each stage.
     static constexpr int NUM_ACC = kBlock ? 1 : 2;
+    // Scale-copy issuers: one warp, two for NVFP4 (12 copies per stage are
+    // more than one thread issues in a stage's time; measured 8192^3: 3955 ->
+    // 5610 TFLOPS without them)
+    static constexpr int SF_WARPS = F4 == 2 ? 2 : 1;
     // full, (spare), empty [S]; acc_full, acc_empty [NUM_ACC]; drain (MMA
-    // thread), drain (scale-copy thread), scales ready [S]
-    static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 2;
+    // thread), drain (scale-copy threads) [SF_WARPS], scales ready [S]
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 1 + SF_WARPS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_GROUP = OFF_MISC + 16;  // row_off, tile_off, rt_off [E + 1]
     static constexpr int SMEM_BYTES = OFF_GROUP + 3 * (FP8G_MAX_EXPERTS + 1) * 4 + 1024;
@@ -180,8 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_accf = [&](int a) { return ptx::smem_addr(&bars[3 * PC::STAGES + a]); };
     auto bar_acce = [&](int a) { return ptx::smem_addr(&bars[3 * PC::STAGES + PC::NUM_ACC + a]); };
     const uint32_t bar_drain = ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC]);
-    const uint32_t bar_drain_sf = ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 1]);
-    auto bar_sfr = [&](int s) { return ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 2 + s]); };
+    auto bar_drain_sf = [&](int w) {
+        return ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 1 + w]);
+    };
+    auto bar_sfr = [&](int s) {
+        return ptx::smem_addr(&bars[3 * PC::STAGES + 2 * PC::NUM_ACC + 1 + PC::SF_WARPS + s]);
+    };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PC::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + PC::OFF_MISC + 4);
     int32_t *row_off = reinterpret_cast<int32_t *>(smem + PC::OFF_GROUP);
@@ -194,14 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_full(s), 1);
             ptx::mbar_init(bar_peer(s), 1);
             ptx::mbar_init(bar_empty(s), 1);
-            ptx::mbar_init(bar_sfr(s), 1);
+            ptx::mbar_init(bar_sfr(s), PC::SF_WARPS);
         }
         for (int a = 0; a < PC::NUM_ACC; ++a) {
             ptx::mbar_init(bar_accf(a), 1);
             ptx::mbar_init(bar_acce(a), 2 * kEpiWarps);
         }
         ptx::mbar_init(bar_drain, 1);
-        ptx::mbar_init(bar_drain_sf, 1);
+        for (int w = 0; w < PC::SF_WARPS; ++w) ptx::mbar_init(bar_drain_sf(w), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -280,6 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // then B's pairs)
                         const uint32_t dst = sbase + PC::OFF_SF + stage * PC::CHUNK;
                         constexpr int G = PC::G;
+                        if constexpr (F4 == 2) {
+                            // NVFP4 chunks: a stage's 4 groups adjacent per 128-row
+                            // tile: A's 4 chunks (2 KB), B's two tiles x 4 (4 KB)
+                            ptx::tma_load_2d_pair(dst, &tmSA, fb, 0,
+                                                  (kb * p.n_rtA + ti.rtA0 + (int32_t)rank) * 4);
+                            ptx::tma_load_2d_pair(dst + G * kSfaBytes, &tmSB, fb, 0,
+                                                  (kb * p.n_rtB + 2 * ti.pn) * 4);
+                        } else
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
                             const int32_t kg = G * kb + g;
@@ -367,10 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_commit_pair_mc(bar_accf(acc), 0x3);
             }
         }
-    } else if (run && warp == 2 && leader && PC::kBlock) {
+    } else if (run && warp >= 2 && warp < 2 + PC::SF_WARPS && leader && PC::kBlock) {
         // ===== scale-factor copies (even CTA, block modes) =====
         // Tensor-memory slot of a stage is rewritten only after "full" of its
         // next use, i.e. after the producer saw the MMAs that read it complete.
+        // With two issuing warps, warp 2 + h copies K groups h G/2 .. and both
+        // commit to the stage's "scales ready" barrier (arrival count 2).
+        const int h = warp - 2;
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {
@@ -381,17 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                     const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
                     constexpr int G = PC::G;
+                    constexpr int GW = G / PC::SF_WARPS;  // groups per issuing warp
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int gi = 0; gi < GW; ++gi) {
+                        const int g = h * GW + gi;
                         // K group g: A's rows to columns SFG g + 0-3; B's rows
                         // 0-127 to SFG g + SFB + 0-3, rows 128-255 to the next
-                        // four (each replicated over the lane quarters by the copy)
+                        // four (each replicated over the lane quarters by the copy).
+                        // Source chunks: B's rows 0-127 / 128-255 of group g at
+                        // g * 1 KB and + 512 (NVFP4: g * 512 and 2 KB + g * 512)
                         const uint32_t sfg = sf + PC::SFG * g;
-                        const uint32_t cb = cs + G * kSfaBytes + g * kSfbBytes;
+                        const uint32_t cb = cs + G * kSfaBytes;
+                        const uint32_t b0 = F4 == 2 ? cb + g * 512 : cb + g * kSfbBytes;
+                        const uint32_t b1 = F4 == 2 ? cb + G * 512 + g * 512 : b0 + 512;
                         ptx::tc_cp_32x128b_warpx4_pair(sfg, ptx::desc_sf_chunk(cs + g * kSfaBytes));
-                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB, ptx::desc_sf_chunk(cb));
-                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB + 4,
-                                                       ptx::desc_sf_chunk(cb + 512));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB, ptx::desc_sf_chunk(b0));
+                        ptx::tc_cp_32x128b_warpx4_pair(sfg + PC::SFB + 4, ptx::desc_sf_chunk(b1));
                     }
                     ptx::tc_commit_pair_mc(bar_sfr(stage), 0x1);
                     if (++stage == PC::STAGES) {
@@ -456,8 +480,9 @@ roles_done:
     __syncthreads();
     if (*abort_flag) {
         // drain the tensor-core work each issuing thread may have in flight
-        if (leader && (warp == 1 || (warp == 2 && PC::kBlock)) && lane == 0) {
-            const uint32_t db = warp == 1 ? bar_drain : bar_drain_sf;
+        if (leader && (warp == 1 || (warp >= 2 && warp < 2 + PC::SF_WARPS && PC::kBlock)) &&
+            lane == 0) {
+            const uint32_t db = warp == 1 ? bar_drain : bar_drain_sf(warp - 2);
             ptx::tc_commit_pair(db);
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(db, 0) && ptx::globaltimer() - t0 < p.timeout_ns) {

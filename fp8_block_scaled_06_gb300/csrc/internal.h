@@ -117,7 +117,8 @@ struct PackArgs {
     int32_t rep;  // B of single-CTA 256-wide tiles: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
 };
 // NVFP4: E4M3 scale codes [rows, K/16] -> the same 512-byte chunks, a K group
-// being 64 wide (4 blocks of 16, one MMA's word); rows past the operand 1.0.
+// being 64 wide (4 blocks of 16, one MMA's word), the four groups of a
+// 256-wide stage adjacent per 128-row tile; rows past the operand 1.0.
 cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
                               const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
                               int32_t n_kg, int64_t sfc, cudaStream_t s);

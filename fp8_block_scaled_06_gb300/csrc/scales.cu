@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
 // group's four codes (4 consecutive bytes of the row) become word w = row / 32
 // of datapath d = row % 32 of the chunk; consecutive threads take consecutive
 // groups of one row (coalesced loads).  Rows past the operand: 1.0 (0x38).
+// Chunk order: the four K groups of one 256-wide GEMM stage are adjacent,
+// chunk(kg, rt) at ((kg / 4 * n_rt + rt) * 4 + kg % 4) * 512, so a stage's
+// scales of one 128-row tile are one 2 KB load.
 __global__ void __launch_bounds__(256) pack_nvfp4_kernel(const uint8_t *sfa, int64_t rows_a,
                                                         int32_t n_rt_a, uint8_t *dst_a,
                                                         const uint8_t *sfb, int64_t rows_b,
@@ -183,8 +186,8 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(const uint8_t *sfa, int
         if (row < rows) word = __ldg(reinterpret_cast<const uint32_t *>(src + row * sfc) + kg);
         const int64_t rt = row / kBM;
         const int r = (int)(row % kBM);
-        uint8_t *out = (isa ? dst_a : dst_b) + ((int64_t)kg * n_rt + rt) * 512 + 16 * (r & 31) +
-                       4 * (r >> 5);
+        uint8_t *out = (isa ? dst_a : dst_b) + (((int64_t)(kg >> 2) * n_rt + rt) * 4 + (kg & 3)) * 512 +
+                       16 * (r & 31) + 4 * (r >> 5);
         *reinterpret_cast<uint32_t *>(out) = word;
     }
 }
