@@ -519,7 +519,8 @@ fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa, con
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
         return FP8G_ERR_INVALID_ARG;
     if (K % 256 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(A, 32) || !aligned(B, 32) || !aligned(sfa, 4) || !aligned(sfb, 4) ||
+    // scale rows are read 16 bytes at a time (K / 16 bytes per row, K % 256 == 0)
+    if (!aligned(A, 32) || !aligned(B, 32) || !aligned(sfa, 16) || !aligned(sfb, 16) ||
         !aligned(ga, 4) || !aligned(gb, 4))
         return FP8G_ERR_ALIGNMENT;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;

@@ -158,37 +158,49 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
             atomicExch(&status[1], 0u);
 }
 
-// NVFP4 scale codes: one thread per (operand, row, 64-wide K group): the
-// group's four codes (4 consecutive bytes of the row) become word w = row / 32
-// of datapath d = row % 32 of the chunk; consecutive threads take consecutive
-// groups of one row (coalesced loads).  Rows past the operand: 1.0 (0x38).
+// NVFP4 scale codes -> chunks.  A block takes one 128-row tile and 8
+// 64-wide K groups of one operand (blockIdx.z: 0 A, 1 B): thread t loads row
+// t / 2's four codes words of K groups kg0 + 4 (t % 2) .. + 3 (16 bytes), the
+// words go through shared memory, and warp g stores K group kg0 + g's whole
+// chunk (32 x 16 bytes: datapath d holds rows d, 32 + d, 64 + d, 96 + d).
 // Chunk order: the four K groups of one 256-wide GEMM stage are adjacent,
 // chunk(kg, rt) at ((kg / 4 * n_rt + rt) * 4 + kg % 4) * 512, so a stage's
-// scales of one 128-row tile are one 2 KB load.
-__global__ void __launch_bounds__(256) pack_nvfp4_kernel(const uint8_t *sfa, int64_t rows_a,
-                                                        int32_t n_rt_a, uint8_t *dst_a,
-                                                        const uint8_t *sfb, int64_t rows_b,
-                                                        int32_t n_rt_b, uint8_t *dst_b,
-                                                        int32_t n_kg, int64_t sfc) {
+// scales of one 128-row tile are one 2 KB load.  Rows past the operand: 1.0
+// (0x38).  n_kg is a multiple of 4 (K % 256 == 0).
+struct PackNv {
+    const uint8_t *src;
+    int64_t rows;
+    int32_t n_rt;
+    uint8_t *dst;
+};
+
+__global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int32_t n_kg,
+                                                        int64_t sfc) {
+    __shared__ uint32_t words[8][kBM];
     ptx::grid_dep_launch();  // the GEMM may start its prologue now
-    const int64_t per_a = (int64_t)n_rt_a * kBM * n_kg;
-    const int64_t total = per_a + (int64_t)n_rt_b * kBM * n_kg;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const bool isa = i < per_a;
-        const int64_t k = isa ? i : i - per_a;
-        const int32_t kg = (int32_t)(k % n_kg);
-        const int64_t row = k / n_kg;
-        const uint8_t *src = isa ? sfa : sfb;
-        const int64_t rows = isa ? rows_a : rows_b;
-        const int32_t n_rt = isa ? n_rt_a : n_rt_b;
-        uint32_t word = 0x38383838u;
-        if (row < rows) word = __ldg(reinterpret_cast<const uint32_t *>(src + row * sfc) + kg);
-        const int64_t rt = row / kBM;
-        const int r = (int)(row % kBM);
-        uint8_t *out = (isa ? dst_a : dst_b) + (((int64_t)(kg >> 2) * n_rt + rt) * 4 + (kg & 3)) * 512 +
-                       16 * (r & 31) + 4 * (r >> 5);
-        *reinterpret_cast<uint32_t *>(out) = word;
+    const PackNv &j = blockIdx.z == 0 ? a : b;
+    const int rt = blockIdx.y;
+    if (rt >= j.n_rt) return;  // block-uniform
+    const int kg0 = blockIdx.x * 8;
+    {
+        const int r = threadIdx.x >> 1, hh = threadIdx.x & 1;
+        const int64_t row = (int64_t)rt * kBM + r;
+        const int k = kg0 + 4 * hh;
+        uint4 w = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        if (row < j.rows && k < n_kg)
+            w = __ldg(reinterpret_cast<const uint4 *>(j.src + row * sfc) + k / 4);
+        words[4 * hh + 0][r] = w.x;
+        words[4 * hh + 1][r] = w.y;
+        words[4 * hh + 2][r] = w.z;
+        words[4 * hh + 3][r] = w.w;
+    }
+    __syncthreads();
+    const int g = threadIdx.x >> 5, d = threadIdx.x & 31;
+    const int kg = kg0 + g;
+    if (kg < n_kg) {
+        const uint4 o = make_uint4(words[g][d], words[g][32 + d], words[g][64 + d], words[g][96 + d]);
+        *reinterpret_cast<uint4 *>(j.dst + (((int64_t)(kg >> 2) * j.n_rt + rt) * 4 + (kg & 3)) * 512 +
+                                   16 * d) = o;
     }
 }
 
@@ -197,12 +209,12 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(const uint8_t *sfa, int
 cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
                               const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
                               int32_t n_kg, int64_t sfc, cudaStream_t s) {
-    const int64_t total = ((int64_t)n_rt_a + n_rt_b) * kBM * n_kg;
-    if (total <= 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    pack_nvfp4_kernel<<<(unsigned)blocks, 256, 0, s>>>(sfa, rows_a, n_rt_a, dst_a, sfb, rows_b,
-                                                       n_rt_b, dst_b, n_kg, sfc);
+    const int ny = n_rt_a > n_rt_b ? n_rt_a : n_rt_b;
+    if (n_kg <= 0 || ny <= 0) return cudaSuccess;
+    const PackNv ja{sfa, rows_a, n_rt_a, dst_a};
+    const PackNv jb{sfb, rows_b, n_rt_b, dst_b};
+    const dim3 grid((unsigned)((n_kg + 7) / 8), (unsigned)ny, 2u);
+    pack_nvfp4_kernel<<<grid, 256, 0, s>>>(ja, jb, n_kg, sfc);
     return cudaGetLastError();
 }
 

@@ -255,7 +255,7 @@ FP8G_API fp8g_status fp8g_quantize_nvfp4(const void *x, int32_t in_dtype, int64_
  * over 1x16 K blocks.  A [M, K/2], B [N, K/2]: E2M1 codes two per byte, as
  * fp8g_quantize_nvfp4 writes them, 32-byte aligned; sfa [M, K/16], sfb
  * [N, K/16]: E4M3 scale codes (positive; the tensor core applies them
- * exactly), 4-byte aligned; ga, gb: device fp32[1] each (the tensors' g);
+ * exactly), 16-byte aligned; ga, gb: device fp32[1] each (the tensors' g);
  * bias (nullable) fp32 [N]; act an fp8g_act.  K % 256 == 0 (else
  * FP8G_ERR_UNSUPPORTED_SHAPE).  Runs two kernels: the scale packing and the
  * GEMM on CTA pairs with the FP4-rate kind::mxf4nvf4 MMA (scale_vec::4X),

@@ -133,5 +133,7 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
     assert _err(fp8g.fp8_gemm_nvfp4, P + 16, P, P, P, P, P, P, 0, None, 0, 8, 8, 256, 0) == \
         fp8g.FP8G_ERR_ALIGNMENT
     assert _err(fp8g.fp8_gemm_nvfp4, P, P, P, P, None, P, P, 0, None, 0, 8, 8, 256, 0) == E
+    assert _err(fp8g.fp8_gemm_nvfp4, P, P, P + 4, P, P, P, P, 0, None, 0, 8, 8, 256, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
     assert _err(fp8g.fp8g_quantize_nvfp4, P, 0, 4, 40, P, P, P, 0) == \
         fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
