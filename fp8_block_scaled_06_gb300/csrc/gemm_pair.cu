@@ -1,4 +1,6 @@
-// Per-tensor FP8 GEMM on CTA pairs (tcgen05 cta_group::2), sm_103a.
+// FP8 / FP4 GEMMs on CTA pairs (tcgen05 cta_group::2), sm_103a: per-tensor,
+// block-scaled and grouped FP8 (any E4M3 / E5M2 / E2M1 operand pairing on the
+// FP8-rate MMA), MXFP4 and NVFP4 on the FP4-rate MMAs.
 //
 // Why: the single-CTA kernel stages 48 KB per 128-wide K step for a 128x256
 // output tile, so four stages fill shared memory and cannot hide the refill
@@ -17,6 +19,8 @@
 //            from the MMA thread, each copy stalled the MMA stream (~6-7% per
 //            copy instruction); from their own warp the copies overlap the
 //            previous stages' MMAs (8192^3: 395 -> 363 us).
+//   warp 3   even CTA, NVFP4 only: a second scale-copy warp (half the K
+//            groups; both commit to "scales ready")
 //   warps 4-19 both CTAs: epilogue of the CTA's 128 accumulator rows; the
 //            accumulator release is counted on the even CTA's barrier
 // The MMA thread's commits go to both CTAs' barriers (multicast), so each
@@ -36,8 +40,9 @@
 // two pairs of chunks), copied to a second set of scale columns.
 // F4 = 2 (NVFP4: 1x16 E4M3 block scales, kind::mxf4nvf4 scale_vec::4X): the
 // same operand stages, but each MMA reads four scale bytes per row, so a stage
-// carries four 64-wide K groups of scales (6 KB); tensor memory then holds
-// 12 scale columns per group (48 per stage), which leaves room for 5 stages.
+// carries four 64-wide K groups of scales (6 KB, loaded as two copies: the
+// packing keeps a stage's groups adjacent); tensor memory then holds 12 scale
+// columns per group (48 per stage), which leaves room for 5 stages.
 #include <cuda_bf16.h>
 
 #include "internal.h"

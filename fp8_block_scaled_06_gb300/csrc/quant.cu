@@ -20,6 +20,10 @@
 // MoE paragraph of the JAX/Blackwell page: tokens copied into expert order),
 // so that gather, scale and quantisation take one pass over HBM.
 //
+// NVFP4 (the other FP4 micro-scaling format of 12.6.1): E2M1 codes, one E4M3
+// scale per 1x16 block and an fp32 scale per tensor (quant_nvfp4_kernel; the
+// recipe is stated there).
+//
 // HBM-bound elementwise kernels: 16-byte loads, 8-byte (E2M1: 4-byte)
 // stores, a grid of a few CTAs per SM striding over the output.
 #include "internal.h"
