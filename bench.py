@@ -204,8 +204,9 @@ def run_once(fp8g, wl, w, t, C, stream):
 # of the dominant kernel, from the ncu captures summarised in profiles/.
 # Valid only for the kernel source those captures measured; workloads without
 # a capture report null.
-TRAFFIC_BYTES = {"large8192": 262_422_784 + 117_014_528,
-                 "mxfp4_8192": 107_195_136 + 95_988_992}
+TRAFFIC_BYTES = {"large8192": 260_747_776 + 117_235_712,
+                 "mxfp4_8192": 107_155_200 + 95_997_440,
+                 "nvfp4_8192": 113_520_384 + 98_173_184}
 
 
 def fp4_rate(fp8g, wl) -> bool:
