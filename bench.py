@@ -1,7 +1,8 @@
 """FP8 GEMM throughput on GB300: TFLOPS and fraction of the roofline.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload large8192|large4096|skinny|moe|square1024|tensor8192]
+                [--workload large8192|large4096|skinny|moe|square1024|tensor8192|
+                            mixed8192|literal8192|mxfp4_8192|nvfp4_8192|moe_nvfp4]
 
 One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
 scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
@@ -48,6 +49,8 @@ WORKLOADS = {
     "mxfp4_8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
     # NVFP4: E2M1 with 1x16 E4M3 block scales and an fp32 scale per tensor
     "nvfp4_8192": dict(kind="nvfp4", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
+    # the MoE workload in NVFP4 (each expert's weight with its own tensor scale)
+    "moe_nvfp4": dict(kind="grouped_nvfp4", M=32768, N=14336, K=4096, seed=4, a_fmt=2, b_fmt=2),
 }
 FMT_NAMES = ["e4m3", "e5m2", "e2m1"]
 # bytes per element of each format in memory (E2M1: two codes per byte)
@@ -141,6 +144,14 @@ def make_inputs(wl: dict, device):
         sb = sb.reshape(E, N, K // 32)
         counts = torch.from_numpy(w.counts).to(device)
         return w, dict(qa=qa, sa=sa, qb=qb, sb=sb, counts=counts)
+    if wl["kind"] == "grouped_nvfp4":
+        w = synth.moe_grouped(seed=wl["seed"])
+        qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
+        qbs = [fp8g.quantize_nvfp4(w.B[e].to(device)) for e in range(w.B.shape[0])]
+        qb, sb, gb = (torch.stack([q[0] for q in qbs]), torch.stack([q[1] for q in qbs]),
+                      torch.cat([q[2] for q in qbs]))
+        counts = torch.from_numpy(w.counts).to(device)
+        return w, dict(qa=qa, sa=sa, ga=ga, qb=qb, sb=sb, gb=gb, counts=counts)
     if wl["kind"] == "nvfp4":
         w = synth.large_block(wl["M"], seed=wl["seed"])
         qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
@@ -170,6 +181,10 @@ def algorithmic_bytes(wl: dict, w) -> int:
         E = w.B.shape[0]
         return int(M * K * ea + E * N * K * eb + 4 * (M * K // 32 + E * N * K // 32) +
                    M * N * out_b + 4 * E)
+    if wl["kind"] == "grouped_nvfp4":   # E4M3 scale bytes per 16; fp32 gA and E gB
+        E = w.B.shape[0]
+        return int(M * K * ea + E * N * K * eb + (M + E * N) * K // 16 + 4 * (1 + E) +
+                   M * N * out_b + 4 * E)
     if wl["kind"] == "nvfp4":   # E4M3 scale bytes per 16 elements + two fp32 tensor scales
         return int(M * K * ea + N * K * eb + (M + N) * K // 16 + 8 + M * N * out_b)
     sf = 8 if wl["kind"] == "tensor" else 4 * (M * K // 32 + N * K // 32)
@@ -182,6 +197,11 @@ def run_once(fp8g, wl, w, t, C, stream):
         E, N, K = t["qb"].shape
         fp8g.fp8_grouped_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, t["counts"], E, N, K,
                               t["qa"].shape[0], None, None, stream)
+    elif wl["kind"] == "grouped_nvfp4":
+        E, N, K2 = t["qb"].shape
+        fp8g.fp8_grouped_gemm_nvfp4(t["qa"], t["qb"], t["sa"], t["sb"], t["ga"], t["gb"], C, out,
+                                    None, fp8g.FP8G_ACT_NONE, t["counts"], E, N, 2 * K2,
+                                    t["qa"].shape[0], None, None, stream)
     elif wl["kind"] == "nvfp4":
         fp8g.fp8_gemm_nvfp4(t["qa"], t["qb"], t["sa"], t["sb"], t["ga"], t["gb"], C, out, None,
                             fp8g.FP8G_ACT_NONE, wl["M"], wl["N"], wl["K"], stream)
@@ -212,7 +232,7 @@ TRAFFIC_BYTES = {"large8192": 260_747_776 + 117_235_712,
 def fp4_rate(fp8g, wl) -> bool:
     """Whether the call runs the FP4-rate MMA: E2M1 x E2M1 block-scaled on CTA
     pairs with K % 256 == 0 (the library's own selection rule)."""
-    if wl["kind"] == "nvfp4":
+    if wl["kind"] in ("nvfp4", "grouped_nvfp4"):
         return True                 # kind::mxf4nvf4 on CTA pairs for every shape
     if wl.get("a_fmt", 0) != 2 or wl.get("b_fmt", 0) != 2 or wl["K"] % 256:
         return False
@@ -228,7 +248,7 @@ def launches_per_call(fp8g, wl) -> int:
     block-scaled paths that do not split K (split-K converts scales itself)."""
     if wl["kind"] == "tensor":
         return 1
-    if wl["kind"] in ("grouped", "nvfp4"):
+    if wl["kind"] in ("grouped", "nvfp4", "grouped_nvfp4"):
         return 2
     if wl.get("literal"):
         return 1
@@ -319,6 +339,15 @@ def oracle_inputs(wl, w):
         return dict(A=qa[offs[e]:offs[e + 1]], sa=sa[offs[e]:offs[e + 1]],
                     B=qb.reshape(E, N, K)[e], sb=sb.reshape(E, N, K // 32)[e], block=True,
                     N=N, K=K, desc=f"rows of expert {e} (all {N} columns)")
+    if wl["kind"] == "grouped_nvfp4":
+        N, K = wl["N"], wl["K"]
+        offs = oracle.grouped_offsets(w.counts)
+        e = int(np.argmax(w.counts))                 # the largest expert
+        qa, sa, ga = oracle.quantize_nvfp4(w.A.numpy())
+        qb, sb, gb = oracle.quantize_nvfp4(w.B[e].numpy())
+        return dict(A=qa[offs[e]:offs[e + 1]], sa=sa[offs[e]:offs[e + 1]], B=qb, sb=sb, ga=ga,
+                    gb=gb, nv=True, block=True, N=N, K=K,
+                    desc=f"rows of expert {e} (all {N} columns)")
     if wl["kind"] == "nvfp4":
         qa, sa, ga = oracle.quantize_nvfp4(w.A.numpy())
         qb, sb, gb = oracle.quantize_nvfp4(w.B.numpy())
@@ -501,7 +530,7 @@ def main():
                            f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
     if f4 and tensor_bound:
         roof["peak_source"] += (" (NVFP4: the FP4-rate MMA, kind::mxf4nvf4 scale_vec::4X)"
-                                if wl["kind"] == "nvfp4" else
+                                if wl["kind"] in ("nvfp4", "grouped_nvfp4") else
                                 " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)")
     elif 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
         roof["peak_source"] += " (E2M1 operands on the FP8-rate MMA, kind::f8f6f4)"
@@ -529,6 +558,8 @@ def main():
                               {"block": "1x32 along K, power of two",
                                "grouped": "1x32 along K, power of two",
                                "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
+                               "grouped_nvfp4": "1x16 along K, E4M3, fp32 for A and per "
+                                                "expert weight (NVFP4)",
                                "tensor": "per tensor"}[wl["kind"]]),
                    "out": w.out, "l2": f"inputs rotated over {copies} copies > 2x L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
@@ -557,7 +588,7 @@ def reference_arm(args, wl, world, rank):
     if rank != 0:
         return
     import synth
-    if wl["kind"] == "grouped":
+    if wl["kind"] in ("grouped", "grouped_nvfp4"):
         w = synth.moe_grouped(seed=wl["seed"])
     elif wl["kind"] == "tensor":
         w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")

@@ -46,7 +46,8 @@ EXPORTS = (
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
     "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows",
-    "fp8_gemm_blockscaled_promote", "fp8g_quantize_nvfp4", "fp8_gemm_nvfp4", "fp8g_wait_selftest",
+    "fp8_gemm_blockscaled_promote", "fp8g_quantize_nvfp4", "fp8_gemm_nvfp4",
+    "fp8_grouped_gemm_nvfp4", "fp8g_wait_selftest",
     "fp8g_kernel_timing_begin", "fp8g_kernel_timing_end",
     "fp8_gemm_status", "fp8g_status_string",
     "fp8g_set_wait_timeout_ms", "fp8g_shutdown", "fp8g_version",
@@ -104,6 +105,9 @@ def load():
         lib.fp8_gemm_nvfp4.restype = st
         lib.fp8_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, P, i32, i64, i64, i64,
                                        P]
+        lib.fp8_grouped_gemm_nvfp4.restype = st
+        lib.fp8_grouped_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, P, i32, P, i32,
+                                               i64, i64, i64, P, P, P]
         lib.fp8_gemm_fmt.restype = st
         lib.fp8_gemm_fmt.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, i64, i64, i64, P]
         lib.fp8_gemm_blockscaled_fmt.restype = st
@@ -299,6 +303,16 @@ def fp8_gemm_nvfp4(A, B, sfa, sfb, ga, gb, C, out: int, bias, act: int, M: int, 
     _check(load().fp8_gemm_nvfp4(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ga), _ptr(gb),
                                  _ptr(C), int(out), _ptr(bias), int(act), M, N, K,
                                  _stream(stream)), "fp8_gemm_nvfp4")
+
+
+def fp8_grouped_gemm_nvfp4(A, B, sfa, sfb, ga, gb, C, out: int, bias, act: int, counts, E: int,
+                           N: int, K: int, total_rows: int, offsets_out=None, tile_map_out=None,
+                           stream=None):
+    _check(load().fp8_grouped_gemm_nvfp4(_ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ga),
+                                         _ptr(gb), _ptr(C), int(out), _ptr(bias), int(act),
+                                         _ptr(counts), E, N, K, total_rows, _ptr(offsets_out),
+                                         _ptr(tile_map_out), _stream(stream)),
+           "fp8_grouped_gemm_nvfp4")
 
 
 def quantize_nvfp4(x, stream=None):

@@ -407,6 +407,110 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
+// NVFP4 on CTA pairs (kind::mxf4nvf4 is issued with cta_group::2) whatever
+// the shape: pack the E4M3 scale codes into the pair kernel's chunks (a
+// stream-ordered temporary from the library pool), run the GEMM, return the
+// temporary.  Grouped: A's row tiles are expert-local and B holds E matrices.
+fp8g_status run_nvfp4(int mode, const void *A, const void *B, const uint8_t *sfa,
+                      const uint8_t *sfb, const float *ga, const float *gb, void *C, int out,
+                      const float *bias, int32_t act, int64_t M, int64_t N, int64_t K,
+                      const int32_t *counts, int32_t E, int32_t *offsets_out,
+                      int32_t *tile_map_out, cudaStream_t stream) {
+    DevInfo di;
+    fp8g_status st = device_info(di);
+    if (st != FP8G_OK) return st;
+    const bool grouped = mode == kModeGrouped;
+    KernelChoice kc;
+    kc.BM = 256;
+    kc.BN = 256;
+    kc.b_rows = 128;
+    kc.split = 1;
+    kc.cluster = 2;
+    kc.pair = true;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_kb = (int32_t)(K / 256);
+    p.npm = (int32_t)((M + 255) / 256);
+    p.npn = (int32_t)((N + 255) / 256);
+    p.T = (int64_t)p.npm * p.npn;
+    // grouped: at most M / 256 + E row tiles of 256 (the kernel counts them)
+    const int64_t pairs = grouped ? (M / 256 + E) * p.npn : p.T;
+    kc.grid = (int)(2 * (pairs < di.num_sms / 2 ? pairs : di.num_sms / 2));
+    p.split = 1;
+    p.kb_per_split = p.num_kb;
+    p.C = C;
+    p.counts = counts;
+    p.E = E;
+    p.offsets_out = offsets_out;
+    p.tile_map_out = tile_map_out;
+    p.c_rows = M;
+    p.status = di.status;
+    p.timeout_ns = timeout_ns();
+    p.f4 = 2;
+    p.ga = ga;
+    p.gb = gb;
+    p.bias = bias;
+    p.act = act;
+    p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
+    const int32_t n_kg = (int32_t)(K / 64);  // 64-wide K groups: one MMA's four scales
+    const int32_t zB = grouped ? E : 1;
+    p.n_rtA = (int32_t)(grouped ? M / kBM + E : (M + kBM - 1) / kBM);
+    p.n_rtB = (int32_t)(p.npn * 2);
+    if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    // chunk rows are int32 TMA coordinates
+    if ((int64_t)n_kg * p.n_rtA * 4 >= kMaxDim || (int64_t)zB * n_kg * p.n_rtB * 4 >= kMaxDim)
+        return FP8G_ERR_UNSUPPORTED_SHAPE;
+    GemmMaps maps;
+    {
+        // packed codes as dense bytes, K / 2 per row (128 bytes = 256 codes per
+        // box row); grouped with zero rows: A is never read (B stands in)
+        const uint64_t dA[2] = {(uint64_t)(K / 2), (uint64_t)(M > 0 ? M : 1)};
+        const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
+        if ((st = tmap_operand(M > 0 ? A : B, FP8G_E4M3, 2, dA, bA, di.dev, maps.A)) != FP8G_OK)
+            return st;
+        if (grouped) {
+            const uint64_t dB[3] = {(uint64_t)(K / 2), (uint64_t)N, (uint64_t)E};
+            const uint32_t bB[3] = {(uint32_t)kBK, (uint32_t)kc.b_rows, 1u};
+            if ((st = tmap_operand(B, FP8G_E4M3, 3, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        } else {
+            const uint64_t dB[2] = {(uint64_t)(K / 2), (uint64_t)N};
+            const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
+            if ((st = tmap_operand(B, FP8G_E4M3, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+        }
+    }
+    const size_t bytesA = packed_scale_bytes(n_kg, p.n_rtA, 1);
+    const size_t bytesB = packed_scale_bytes(n_kg, p.n_rtB, zB);
+    cudaMemPool_t pool;
+    if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    uint8_t *pkA = static_cast<uint8_t *>(ws);
+    uint8_t *pkB = pkA + bytesA;
+    cudaError_t e = launch_pack_nvfp4(sfa, M, p.n_rtA, pkA, grouped ? counts : nullptr, sfb, N,
+                                      p.n_rtB, zB, pkB, n_kg, K / 16, E, stream);
+    if (e == cudaSuccess) {
+        // a stage's four K-group chunks are adjacent rows per 128-row tile
+        const uint64_t dSA[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtA};
+        const uint32_t bSA[2] = {128u, 4u};
+        const uint64_t dSB[2] = {128u, (uint64_t)zB * n_kg * (uint64_t)p.n_rtB};
+        const uint32_t bSB[2] = {128u, 8u};
+        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
+            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSB, bSB,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
+            e = cudaErrorInvalidValue;
+    }
+    if (e == cudaSuccess)
+        e = timed_launch(stream, [&] {
+            return launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
+        });
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
 }  // namespace fp8g
 
 using namespace fp8g;
@@ -524,80 +628,42 @@ fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa, con
         !aligned(ga, 4) || !aligned(gb, 4))
         return FP8G_ERR_ALIGNMENT;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
-    DevInfo di;
-    if ((st = device_info(di)) != FP8G_OK) return st;
-    // CTA pairs (kind::mxf4nvf4 is issued with cta_group::2) whatever the shape
-    KernelChoice kc;
-    kc.BM = 256;
-    kc.BN = 256;
-    kc.b_rows = 128;
-    kc.split = 1;
-    kc.cluster = 2;
-    kc.pair = true;
-    const int64_t pairs = ((M + 255) / 256) * ((N + 255) / 256);
-    kc.grid = (int)(2 * (pairs < di.num_sms / 2 ? pairs : di.num_sms / 2));
-    GemmParams p{};
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.num_kb = (int32_t)(K / 256);
-    p.npm = (int32_t)((M + 255) / 256);
-    p.npn = (int32_t)((N + 255) / 256);
-    p.T = (int64_t)p.npm * p.npn;
-    p.split = 1;
-    p.kb_per_split = p.num_kb;
-    p.C = C;
-    p.status = di.status;
-    p.timeout_ns = timeout_ns();
-    p.f4 = 2;
-    p.ga = ga;
-    p.gb = gb;
-    p.bias = bias;
-    p.act = act;
-    p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
-    const int32_t n_kg = (int32_t)(K / 64);  // 64-wide K groups: one MMA's four scales
-    p.n_rtA = (int32_t)((M + kBM - 1) / kBM);
-    p.n_rtB = (int32_t)(p.npn * 2);
-    if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    GemmMaps maps;
-    {
-        // packed codes as dense bytes, K / 2 per row (128 bytes = 256 codes per box row)
-        const uint64_t dA[2] = {(uint64_t)(K / 2), (uint64_t)M};
-        const uint64_t dB[2] = {(uint64_t)(K / 2), (uint64_t)N};
-        const uint32_t bA[2] = {(uint32_t)kBK, (uint32_t)kBM};
-        const uint32_t bB[2] = {(uint32_t)kBK, (uint32_t)kc.b_rows};
-        if ((st = tmap_operand(A, FP8G_E4M3, 2, dA, bA, di.dev, maps.A)) != FP8G_OK) return st;
-        if ((st = tmap_operand(B, FP8G_E4M3, 2, dB, bB, di.dev, maps.B)) != FP8G_OK) return st;
+    return run_nvfp4(kModeBlock, A, B, sfa, sfb, ga, gb, C, out, bias, act, M, N, K, nullptr, 1,
+                     nullptr, nullptr, stream);
+}
+
+fp8g_status fp8_grouped_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa,
+                                   const uint8_t *sfb, const float *ga, const float *gb, void *C,
+                                   int out, const float *bias, int32_t act, const int32_t *counts,
+                                   int32_t E, int64_t N, int64_t K, int64_t total_rows,
+                                   int32_t *offsets_out, int32_t *tile_map_out,
+                                   cudaStream_t stream) {
+    if (counts == nullptr || sfa == nullptr || sfb == nullptr || ga == nullptr || gb == nullptr)
+        return FP8G_ERR_INVALID_ARG;
+    if (E < 1) return FP8G_ERR_INVALID_ARG;
+    if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (total_rows < 0) return FP8G_ERR_INVALID_ARG;
+    if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
+        return FP8G_ERR_INVALID_ARG;
+    if (total_rows > 0) {
+        fp8g_status st = check_common(A, B, C, out, total_rows, N, K);
+        if (st != FP8G_OK) return st;
+        if (!aligned(A, 32)) return FP8G_ERR_ALIGNMENT;
+    } else {
+        if (B == nullptr) return FP8G_ERR_INVALID_ARG;
+        if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
+        if (N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
     }
-    const size_t bytesA = packed_scale_bytes(n_kg, p.n_rtA, 1);
-    const size_t bytesB = packed_scale_bytes(n_kg, p.n_rtB, 1);
-    cudaMemPool_t pool;
-    if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
-    void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
-        return FP8G_ERR_CUDA;
-    uint8_t *pkA = static_cast<uint8_t *>(ws);
-    uint8_t *pkB = pkA + bytesA;
-    cudaError_t e = launch_pack_nvfp4(sfa, M, p.n_rtA, pkA, sfb, N, p.n_rtB, pkB, n_kg, K / 16,
-                                      stream);
-    if (e == cudaSuccess) {
-        // a stage's four K-group chunks are adjacent rows per 128-row tile
-        const uint64_t dSA[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtA};
-        const uint32_t bSA[2] = {128u, 4u};
-        const uint64_t dSB[2] = {128u, (uint64_t)n_kg * (uint64_t)p.n_rtB};
-        const uint32_t bSB[2] = {128u, 8u};
-        if (tmap_encode(pkA, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSA, bSA,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SA) != FP8G_OK ||
-            tmap_encode(pkB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 32, 2, dSB, bSB,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, di.dev, maps.SB) != FP8G_OK)
-            e = cudaErrorInvalidValue;
-    }
-    if (e == cudaSuccess)
-        e = timed_launch(stream, [&] {
-            return launch_gemm(kModeBlock, out == FP8G_OUT_F32, maps, p, kc, stream);
-        });
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
+    if (N >= kMaxDim || K >= kMaxDim || (int64_t)E * N >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (K % 256 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(B, 32) || !aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(ga, 4) ||
+        !aligned(gb, 4) || !aligned(counts, 4))
+        return FP8G_ERR_ALIGNMENT;
+    if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
+    if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
+    if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
+    return run_nvfp4(kModeGrouped, A, B, sfa, sfb, ga, gb, C, out, bias, act, total_rows, N, K,
+                     counts, E, offsets_out, tile_map_out, stream);
 }
 
 fp8g_status fp8g_quantize_nvfp4(const void *x, int32_t in_dtype, int64_t rows, int64_t cols,

@@ -42,7 +42,9 @@
 // same operand stages, but each MMA reads four scale bytes per row, so a stage
 // carries four 64-wide K groups of scales (6 KB, loaded as two copies: the
 // packing keeps a stage's groups adjacent); tensor memory then holds 12 scale
-// columns per group (48 per stage), which leaves room for 5 stages.
+// columns per group (48 per stage), which leaves room for 5 stages.  The
+// output is scaled by the product of the two fp32 tensor scales, per expert
+// on the grouped GEMM (each expert's B has its own).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -298,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // tile: A's 4 chunks (2 KB), B's two tiles x 4 (4 KB)
                             ptx::tma_load_2d_pair(dst, &tmSA, fb, 0,
                                                   (kb * p.n_rtA + ti.rtA0 + (int32_t)rank) * 4);
+                            // (B: expert e's chunks follow e whole matrices)
                             ptx::tma_load_2d_pair(dst + G * kSfaBytes, &tmSB, fb, 0,
-                                                  (kb * p.n_rtB + 2 * ti.pn) * 4);
+                                                  ((ti.e * p.num_kb + kb) * p.n_rtB + 2 * ti.pn) * 4);
                         } else
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
@@ -458,13 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t arow = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;  // routed row
             const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;       // row of C
             const int64_t ncol0 = (int64_t)ti.pn * kPairBN + col0;
-            float a_t = alpha;  // scale left for the stores below
+            // NVFP4 grouped: each expert's B carries its own tensor scale
+            float alpha_e = alpha;
+            if constexpr (F4 == 2 && MODE == kModeGrouped) alpha_e = __fmul_rn(p.ga[0], p.gb[ti.e]);
+            float a_t = alpha_e;  // scale left for the stores below
             if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
                 // every lane (rows past the output too: they are not stored)
                 const float *brow = p.bias != nullptr ? p.bias + (int64_t)ti.e * p.N : nullptr;
 #pragma unroll
                 for (int c = 0; c < kCW / 32; ++c)
-                    epi32(r[c], alpha, brow, p.act, ncol0 + c * 32, p.N);
+                    epi32(r[c], alpha_e, brow, p.act, ncol0 + c * 32, p.N);
                 a_t = 1.0f;
             }
             // FP4-rate tiles end twice as often: their stores go out as whole
@@ -545,6 +551,9 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
     if (p.f4 == 2 && mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true, 2>(maps, p, grid, stream)
                        : launch_pair<kModeBlock, false, 2>(maps, p, grid, stream);
+    if (p.f4 == 2 && mode == kModeGrouped)
+        return out_f32 ? launch_pair<kModeGrouped, true, 2>(maps, p, grid, stream)
+                       : launch_pair<kModeGrouped, false, 2>(maps, p, grid, stream);
     if (p.f4 == 1 && mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true, 1>(maps, p, grid, stream)
                        : launch_pair<kModeBlock, false, 1>(maps, p, grid, stream);

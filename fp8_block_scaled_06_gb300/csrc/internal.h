@@ -118,10 +118,13 @@ struct PackArgs {
 };
 // NVFP4: E4M3 scale codes [rows, K/16] -> the same 512-byte chunks, a K group
 // being 64 wide (4 blocks of 16, one MMA's word), the four groups of a
-// 256-wide stage adjacent per 128-row tile; rows past the operand 1.0.
+// 256-wide stage adjacent per 128-row tile; rows past the operand 1.0.  A
+// with expert-local row tiles when counts is set (E experts); B as z_b
+// matrices of rows_b rows.
 cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
-                              const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
-                              int32_t n_kg, int64_t sfc, cudaStream_t s);
+                              const int32_t *counts, const uint8_t *sfb, int64_t rows_b,
+                              int32_t n_rt_b, int32_t z_b, uint8_t *dst_b, int32_t n_kg,
+                              int64_t sfc, int32_t E, cudaStream_t s);
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
                                int32_t E, unsigned int *status, cudaStream_t s);

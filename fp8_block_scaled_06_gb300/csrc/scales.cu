@@ -159,36 +159,66 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
 }
 
 // NVFP4 scale codes -> chunks.  A block takes one 128-row tile and 8
-// 64-wide K groups of one operand (blockIdx.z: 0 A, 1 B): thread t loads row
-// t / 2's four codes words of K groups kg0 + 4 (t % 2) .. + 3 (16 bytes), the
-// words go through shared memory, and warp g stores K group kg0 + g's whole
-// chunk (32 x 16 bytes: datapath d holds rows d, 32 + d, 64 + d, 96 + d).
-// Chunk order: the four K groups of one 256-wide GEMM stage are adjacent,
-// chunk(kg, rt) at ((kg / 4 * n_rt + rt) * 4 + kg % 4) * 512, so a stage's
-// scales of one 128-row tile are one 2 KB load.  Rows past the operand: 1.0
-// (0x38).  n_kg is a multiple of 4 (K % 256 == 0).
+// 64-wide K groups of one operand (blockIdx.z: 0 A, z >= 1 B's matrix z - 1):
+// thread t loads row t / 2's four codes words of K groups kg0 + 4 (t % 2) ..
+// + 3 (16 bytes), the words go through shared memory, and warp g stores K
+// group kg0 + g's whole chunk (32 x 16 bytes: datapath d holds rows d,
+// 32 + d, 64 + d, 96 + d).  Chunk order: the four K groups of one 256-wide
+// GEMM stage are adjacent, chunk(z, kg, rt) at
+// (z * n_kg * n_rt + (kg / 4 * n_rt + rt) * 4 + kg % 4) * 512, so a stage's
+// scales of one 128-row tile are one 2 KB load.  Grouped A (counts set): row
+// tiles are expert-local, numbered in expert order as the GEMM numbers them.
+// Rows past the operand or the expert: 1.0 (0x38).  n_kg is a multiple of 4
+// (K % 256 == 0).
 struct PackNv {
     const uint8_t *src;
     int64_t rows;
     int32_t n_rt;
     uint8_t *dst;
+    const int32_t *counts;  // A of the grouped GEMM, else null
 };
 
 __global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int32_t n_kg,
-                                                        int64_t sfc) {
+                                                        int64_t sfc, int32_t E) {
     __shared__ uint32_t words[8][kBM];
+    __shared__ int64_t base_lim[2];
     ptx::grid_dep_launch();  // the GEMM may start its prologue now
     const PackNv &j = blockIdx.z == 0 ? a : b;
     const int rt = blockIdx.y;
     if (rt >= j.n_rt) return;  // block-uniform
+    const int64_t z = blockIdx.z == 0 ? 0 : (int64_t)blockIdx.z - 1;
+    const uint8_t *src = j.src + z * j.rows * sfc;
+    uint8_t *dst = j.dst + z * n_kg * j.n_rt * 512;
+    int64_t base = (int64_t)rt * kBM, limit = j.rows;
+    if (j.counts != nullptr) {
+        if (threadIdx.x == 0) {
+            // this tile's expert: the first whose tiles end past rt
+            int64_t ro = 0, to = 0, b0 = 0, lim = 0;
+            for (int e = 0; e < E; ++e) {
+                const int64_t c = j.counts[e] > 0 ? j.counts[e] : 0;
+                const int64_t nt = (c + kBM - 1) / kBM;
+                if (rt >= to && rt < to + nt) {
+                    b0 = ro + (rt - to) * kBM;
+                    lim = ro + c;
+                }
+                ro += c;
+                to += nt;
+            }
+            base_lim[0] = b0;
+            base_lim[1] = lim;  // 0 for padding tiles past the last expert
+        }
+        __syncthreads();
+        base = base_lim[0];
+        limit = base_lim[1] < j.rows ? base_lim[1] : j.rows;
+    }
     const int kg0 = blockIdx.x * 8;
     {
         const int r = threadIdx.x >> 1, hh = threadIdx.x & 1;
-        const int64_t row = (int64_t)rt * kBM + r;
+        const int64_t row = base + r;
         const int k = kg0 + 4 * hh;
         uint4 w = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
-        if (row < j.rows && k < n_kg)
-            w = __ldg(reinterpret_cast<const uint4 *>(j.src + row * sfc) + k / 4);
+        if (row < limit && k < n_kg)
+            w = __ldg(reinterpret_cast<const uint4 *>(src + row * sfc) + k / 4);
         words[4 * hh + 0][r] = w.x;
         words[4 * hh + 1][r] = w.y;
         words[4 * hh + 2][r] = w.z;
@@ -199,7 +229,7 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int
     const int kg = kg0 + g;
     if (kg < n_kg) {
         const uint4 o = make_uint4(words[g][d], words[g][32 + d], words[g][64 + d], words[g][96 + d]);
-        *reinterpret_cast<uint4 *>(j.dst + (((int64_t)(kg >> 2) * j.n_rt + rt) * 4 + (kg & 3)) * 512 +
+        *reinterpret_cast<uint4 *>(dst + (((int64_t)(kg >> 2) * j.n_rt + rt) * 4 + (kg & 3)) * 512 +
                                    16 * d) = o;
     }
 }
@@ -207,14 +237,15 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int
 }  // namespace
 
 cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a, uint8_t *dst_a,
-                              const uint8_t *sfb, int64_t rows_b, int32_t n_rt_b, uint8_t *dst_b,
-                              int32_t n_kg, int64_t sfc, cudaStream_t s) {
+                              const int32_t *counts, const uint8_t *sfb, int64_t rows_b,
+                              int32_t n_rt_b, int32_t z_b, uint8_t *dst_b, int32_t n_kg,
+                              int64_t sfc, int32_t E, cudaStream_t s) {
     const int ny = n_rt_a > n_rt_b ? n_rt_a : n_rt_b;
-    if (n_kg <= 0 || ny <= 0) return cudaSuccess;
-    const PackNv ja{sfa, rows_a, n_rt_a, dst_a};
-    const PackNv jb{sfb, rows_b, n_rt_b, dst_b};
-    const dim3 grid((unsigned)((n_kg + 7) / 8), (unsigned)ny, 2u);
-    pack_nvfp4_kernel<<<grid, 256, 0, s>>>(ja, jb, n_kg, sfc);
+    if (n_kg <= 0 || ny <= 0 || z_b < 1) return cudaSuccess;
+    const PackNv ja{sfa, rows_a, n_rt_a, dst_a, counts};
+    const PackNv jb{sfb, rows_b, n_rt_b, dst_b, nullptr};
+    const dim3 grid((unsigned)((n_kg + 7) / 8), (unsigned)ny, (unsigned)(1 + z_b));
+    pack_nvfp4_kernel<<<grid, 256, 0, s>>>(ja, jb, n_kg, sfc, E);
     return cudaGetLastError();
 }
 

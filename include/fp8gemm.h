@@ -267,6 +267,32 @@ FP8G_API fp8g_status fp8_gemm_nvfp4(const void *A, const void *B, const uint8_t 
                                     int64_t K, cudaStream_t stream);
 
 /*
+ * Grouped (MoE) NVFP4 GEMM [TUT-12 12.6.1 for the arithmetic; JAX-BW MoE
+ * paragraph for the grouping]: the rows of A [total_rows, K/2] are sorted by
+ * expert, counts[e] of them for expert e (device int32[E], summing to
+ * total_rows, else FP8G_ERR_INVALID_ARG through the status word), and expert
+ * e's rows are multiplied by its own weight B[e] [N, K/2] (B: [E, N, K/2]):
+ *   C[r,j] = out( act( fl32( fl32(ga gb[e]) * sum_kb sa[r,kb] sb[e,j,kb] sum_k a_rk b_ejk ) + bias[e,j] ) )
+ * sfa [total_rows, K/16], sfb [E, N, K/16]: E4M3 scale codes, 16-byte
+ * aligned; ga device fp32[1] (A's g), gb device fp32[E] (each expert's g);
+ * bias (nullable) fp32 [E, N]; C [total_rows, N] in expert order.  A, B
+ * 32-byte aligned; K % 256 == 0; 1 <= E <= FP8G_MAX_EXPERTS; total_rows may
+ * be 0 (A and C then unused, may be null).  offsets_out (nullable, device
+ * int32[E+1]) receives the exclusive prefix of counts; tile_map_out
+ * (nullable, device int32[4 * ((total_rows / 256 + E) * ceil(N / 256))],
+ * 16-byte aligned) one entry per 256 x 256 tile: expert, row tile within the
+ * expert, column tile, 0.  Runs two kernels (scale packing, GEMM on CTA
+ * pairs at the FP4 rate).  Parity: the tolerance of the block-scaled GEMM,
+ * per expert.
+ */
+FP8G_API fp8g_status fp8_grouped_gemm_nvfp4(const void *A, const void *B, const uint8_t *sfa,
+                                            const uint8_t *sfb, const float *ga, const float *gb,
+                                            void *C, int out, const float *bias, int32_t act,
+                                            const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                            int64_t total_rows, int32_t *offsets_out,
+                                            int32_t *tile_map_out, cudaStream_t stream);
+
+/*
  * `block` value of the quantisers for 1x32 blocks with the literal scale
  * s = fl32(amax / fmax) (1 when that is 0) — the "fp32 scale = block
  * amax/448" wording taken literally — and q = FP8(fl32(x / s)).  Such scales

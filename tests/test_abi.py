@@ -135,5 +135,21 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
     assert _err(fp8g.fp8_gemm_nvfp4, P, P, P, P, None, P, P, 0, None, 0, 8, 8, 256, 0) == E
     assert _err(fp8g.fp8_gemm_nvfp4, P, P, P + 4, P, P, P, P, 0, None, 0, 8, 8, 256, 0) == \
         fp8g.FP8G_ERR_ALIGNMENT
+    # grouped NVFP4: as the dense one, plus the experts, the counts and the tile map
+    gn = fp8g.fp8_grouped_gemm_nvfp4
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, P, 2, 8, 128, 8, None, None, 0) == \
+        fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, None, 2, 8, 256, 8, None, None, 0) == E
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, P, 0, 8, 256, 8, None, None, 0) == E
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, P, fp8g.FP8G_MAX_EXPERTS + 1, 8, 256, 8,
+                None, None, 0) == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, P, 2, 8, 256, -1, None, None, 0) == E
+    assert _err(gn, P, P + 16, P, P, P, P, P, 0, None, 0, P, 2, 8, 256, 8, None, None, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(gn, P, P, P, P, P, P + 2, P, 0, None, 0, P, 2, 8, 256, 8, None, None, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 0, P, 2, 8, 256, 8, None, P + 4, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(gn, P, P, P, P, P, P, P, 0, None, 3, P, 2, 8, 256, 8, None, None, 0) == E
     assert _err(fp8g.fp8g_quantize_nvfp4, P, 0, 4, 40, P, P, P, 0) == \
         fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
