@@ -12,8 +12,10 @@ file's comments:
 - E4M3 decode / RNE-satfinite encode (``float8_e4m3fn``; format paragraph of
   "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell GPUs" and the
   dtype in "Triton FP8 CUTLASS-named kernel benchmarking"); the same for E5M2,
-  the other FP8 format that paragraph weighs, and GEMMs whose operands mix
-  the two (``fmt`` arguments: E4M3 = 0, E5M2 = 1).
+  the other FP8 format that paragraph weighs, E2M1 (FP4) and E2M3 / E3M2
+  (FP6), the element formats of the micro-scaling variants (Triton tutorial
+  ch. 12, 12.6.1 and 12.6.4), and GEMMs whose operands mix them (``fmt``
+  arguments: E4M3 = 0, E5M2 = 1, E2M1 = 2, E2M3 = 3, E3M2 = 4).
 - per-tensor (s = amax/448) and 1x32 power-of-two block quantisation
   (microscaling paragraph of the JAX/Blackwell page; Triton tutorial ch. 12,
   section 12.6.1, MXFP8).
@@ -44,6 +46,8 @@ OUT_F32 = 1
 E4M3 = 0
 E5M2 = 1
 E2M1 = 2
+E2M3 = 3
+E3M2 = 4
 ACT_NONE = 0
 ACT_RELU = 1
 ACT_GELU = 2
@@ -84,6 +88,12 @@ def _L():
             lib.oracle_e2m1_table.argtypes = [P]
             lib.oracle_e2m1_encode.restype = ctypes.c_uint8
             lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            for f in ("e2m3", "e3m2"):
+                getattr(lib, f"oracle_{f}_decode").restype = ctypes.c_double
+                getattr(lib, f"oracle_{f}_decode").argtypes = [ctypes.c_uint8]
+                getattr(lib, f"oracle_{f}_table").argtypes = [P]
+                getattr(lib, f"oracle_{f}_encode").restype = ctypes.c_uint8
+                getattr(lib, f"oracle_{f}_encode").argtypes = [ctypes.c_float]
             lib.oracle_e5m2_encode.restype = ctypes.c_uint8
             lib.oracle_e5m2_encode.argtypes = [ctypes.c_float]
             lib.oracle_quantize_tensor_fmt.argtypes = [P, i64, i64, ctypes.c_int, P, P]
@@ -187,6 +197,19 @@ def e2m1_table() -> np.ndarray:
 
 def e2m1_encode(y: float) -> int:
     return int(_L().oracle_e2m1_encode(float(np.float32(y))))
+
+
+def fp6_table(fmt: int) -> np.ndarray:
+    """Values of the 256 byte codes of E2M3 (fmt 3) or E3M2 (fmt 4); the high
+    two bits of a byte are ignored."""
+    out = np.zeros(256, dtype=np.float64)
+    getattr(_L(), "oracle_e2m3_table" if fmt == E2M3 else "oracle_e3m2_table")(_p(out))
+    return out
+
+
+def fp6_encode(y: float, fmt: int) -> int:
+    fn = _L().oracle_e2m3_encode if fmt == E2M3 else _L().oracle_e3m2_encode
+    return int(fn(float(np.float32(y))))
 
 
 def bf16_round(x: float) -> float:

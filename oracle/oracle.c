@@ -22,6 +22,13 @@
  *     Triton tutorial ch. 12 lists beside MXFP8): 1 sign, 2 exponent bits
  *     (bias 1), 1 mantissa bit, values 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
  *     infinities or NaNs.  Held one code per byte (low four bits).
+ *   - E2M3 and E3M2 (FP6: the Triton tutorial ch. 12 lists FP6 among the
+ *     fifth-generation tensor core's types in its 12.6.1 hardware table and
+ *     an FP6 GEMM in its 12.6.4 stability table; it prints no layout, so the
+ *     microscaling element formats are taken): 1 sign bit and 2 exponent
+ *     bits (bias 1) + 3 mantissa bits, largest 7.5, or 3 exponent bits (bias
+ *     3) + 2 mantissa bits, largest 28; exponent field 0 subnormal; no
+ *     infinities or NaNs.  Held one code per byte (low six bits).
  *   - Quantisation x -> RNE_satfinite(fl32(x / s)) with a per-tensor scale
  *     s = fl32(amax / 448) or a 1x32 block scale along K equal to the smallest
  *     power of two >= amax / 448 (the microscaling paragraph of the JAX/Blackwell
@@ -48,7 +55,9 @@
  * product of two E4M3 values is an integer multiple of 2^-18 with magnitude
  * <= 448^2 < 2^18, so any sum of fewer than 2^17 of them fits in the 53-bit
  * significand.  With E5M2 operands products span 2^-32 .. 2^32 and a sum may
- * round (relative error <= K 2^-53, far inside the tolerance).
+ * round (relative error <= K 2^-53, far inside the tolerance).  E2M1, E2M3
+ * and E3M2 values are multiples of 2^-1, 2^-3 and 2^-4 below 28, so their
+ * products with each other or with E4M3 are exact in the same way.
  * Steps the pages fix in fp32 (fl32(amax/448), fl32(x/s), fl32(sA*sB),
  * fl32(alpha*acc)) are done in fp32 here too.
  *
@@ -127,6 +136,31 @@ ORACLE_EXPORT void oracle_e2m1_table(double *out256) {
     for (int c = 0; c < 256; ++c) out256[c] = oracle_e2m1_decode((uint8_t)c);
 }
 
+/* Value of an FP6 code in the low six bits of a byte (the high two bits are
+ * ignored): sign bit 5, then `ebits` exponent bits with bias `bias` and
+ * 5 - ebits mantissa bits.  Exponent field 0 is subnormal. */
+static double fp6_decode(uint8_t code, int ebits, int bias) {
+    const int mbits = 5 - ebits;
+    int s = (code >> 5) & 1;
+    int e = (code >> mbits) & ((1 << ebits) - 1);
+    int m = code & ((1 << mbits) - 1);
+    double mag = e == 0 ? ldexp((double)m, 1 - bias - mbits)
+                        : ldexp(1.0 + (double)m / (double)(1 << mbits), e - bias);
+    return s ? -mag : mag;
+}
+
+/* E2M3: bias 1, values k/8 below 2, up to 1.875 * 2^2 = 7.5. */
+ORACLE_EXPORT double oracle_e2m3_decode(uint8_t code) { return fp6_decode(code, 2, 1); }
+/* E3M2: bias 3, subnormals m/16, up to 1.75 * 2^4 = 28. */
+ORACLE_EXPORT double oracle_e3m2_decode(uint8_t code) { return fp6_decode(code, 3, 3); }
+
+ORACLE_EXPORT void oracle_e2m3_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e2m3_decode((uint8_t)c);
+}
+ORACLE_EXPORT void oracle_e3m2_table(double *out256) {
+    for (int c = 0; c < 256; ++c) out256[c] = oracle_e3m2_decode((uint8_t)c);
+}
+
 /* Round a finite, non-negative real y to the grid of an FP8 format with
  * `mbits` mantissa bits and exponent bias `bias` (normal binades from 2^(1 -
  * bias) up; below that the subnormal quantum 2^(1 - bias - mbits)), with
@@ -190,15 +224,45 @@ ORACLE_EXPORT uint8_t oracle_e2m1_encode(float y) {
     return (uint8_t)(sign | fp8_mag_code(a, 1, 1, 6.0));
 }
 
+/* E2M3 / E3M2 codes of the fp32 value y: RNE, satfinite (to the largest
+ * value, infinities too), NaN -> 0x1F (the largest positive value: FP6 has
+ * no NaN; the library's quantiser does the same), -0 -> 0x20.  One code per
+ * byte, high two bits zero. */
+ORACLE_EXPORT uint8_t oracle_e2m3_encode(float y) {
+    if (isnan(y)) return 0x1F;
+    uint8_t sign = signbit(y) ? 0x20 : 0x00;
+    double a = fabs((double)y);
+    if (isinf(a)) return (uint8_t)(sign | 0x1F);
+    return (uint8_t)(sign | fp8_mag_code(a, 3, 1, 7.5));
+}
+ORACLE_EXPORT uint8_t oracle_e3m2_encode(float y) {
+    if (isnan(y)) return 0x1F;
+    uint8_t sign = signbit(y) ? 0x20 : 0x00;
+    double a = fabs((double)y);
+    if (isinf(a)) return (uint8_t)(sign | 0x1F);
+    return (uint8_t)(sign | fp8_mag_code(a, 2, 3, 28.0));
+}
+
 /* Element formats of the quantisers and GEMM operands */
-enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1, ORACLE_E2M1 = 2 };
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1, ORACLE_E2M1 = 2, ORACLE_E2M3 = 3, ORACLE_E3M2 = 4 };
 
 static uint8_t encode_fmt(float y, int fmt) {
-    if (fmt == ORACLE_E2M1) return oracle_e2m1_encode(y);
-    return fmt == ORACLE_E5M2 ? oracle_e5m2_encode(y) : oracle_e4m3_encode(y);
+    switch (fmt) {
+    case ORACLE_E2M1: return oracle_e2m1_encode(y);
+    case ORACLE_E2M3: return oracle_e2m3_encode(y);
+    case ORACLE_E3M2: return oracle_e3m2_encode(y);
+    case ORACLE_E5M2: return oracle_e5m2_encode(y);
+    default: return oracle_e4m3_encode(y);
+    }
 }
 static double fmt_max(int fmt) {
-    return fmt == ORACLE_E2M1 ? 6.0 : fmt == ORACLE_E5M2 ? 57344.0 : 448.0;
+    switch (fmt) {
+    case ORACLE_E2M1: return 6.0;
+    case ORACLE_E2M3: return 7.5;
+    case ORACLE_E3M2: return 28.0;
+    case ORACLE_E5M2: return 57344.0;
+    default: return 448.0;
+    }
 }
 
 /* ------------------------------------------------------------------ */
@@ -402,16 +466,24 @@ typedef struct {
     float alpha;
 } gemm_job;
 
-static double dec_e4m3[256], dec_e5m2[256], dec_e2m1[256];
+static double dec_e4m3[256], dec_e5m2[256], dec_e2m1[256], dec_e2m3[256], dec_e3m2[256];
 static pthread_once_t dec_once = PTHREAD_ONCE_INIT;
 static void fill_tables(void) {
     oracle_e4m3_table(dec_e4m3);
     oracle_e5m2_table(dec_e5m2);
     oracle_e2m1_table(dec_e2m1);
+    oracle_e2m3_table(dec_e2m3);
+    oracle_e3m2_table(dec_e3m2);
 }
 static const double *table_of(int fmt) {
     pthread_once(&dec_once, fill_tables);
-    return fmt == ORACLE_E2M1 ? dec_e2m1 : fmt == ORACLE_E5M2 ? dec_e5m2 : dec_e4m3;
+    switch (fmt) {
+    case ORACLE_E2M1: return dec_e2m1;
+    case ORACLE_E2M3: return dec_e2m3;
+    case ORACLE_E3M2: return dec_e3m2;
+    case ORACLE_E5M2: return dec_e5m2;
+    default: return dec_e4m3;
+    }
 }
 
 /* One output element.  Block mode (block = 16: 1x16 blocks, scales
@@ -515,8 +587,9 @@ static void run_jobs(gemm_job proto, int64_t n_items, int threads) {
 }
 
 /* Full GEMM.  block = 0: sfa, sfb each point to one fp32 per-tensor scale.
- * block = 1: sfa [M, K/32], sfb [N, K/32].  a_fmt, b_fmt: ORACLE_E4M3 or
- * ORACLE_E5M2.  C, exact, bound: [M, N]. */
+ * block = 1: sfa [M, K/32], sfb [N, K/32].  a_fmt, b_fmt: ORACLE_E4M3,
+ * ORACLE_E5M2, ORACLE_E2M1, ORACLE_E2M3 or ORACLE_E3M2.  C, exact, bound:
+ * [M, N]. */
 /* GEMM with operand formats and the fused epilogue (bias [N] nullable, act). */
 ORACLE_EXPORT void oracle_gemm_ex(const uint8_t *A, const uint8_t *B, const float *sfa,
                                   const float *sfb, int block, int a_fmt, int b_fmt,
