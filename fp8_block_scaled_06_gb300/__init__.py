@@ -32,6 +32,8 @@ FP8G_OUT_F32 = 1
 FP8G_E4M3 = 0
 FP8G_E5M2 = 1
 FP8G_E2M1 = 2
+FP8G_E2M3 = 3
+FP8G_E3M2 = 4
 FP8G_BLOCK32_LITERAL = 33
 FP8G_IN_F32 = 0
 FP8G_IN_BF16 = 1
@@ -376,14 +378,24 @@ def fp8g_version() -> int:
 # Allocation helpers over torch (device memory is plumbing); the work is the
 # ABI call above.
 
+def packed_cols(cols: int, fmt: int) -> int:
+    """Bytes of a row of `cols` codes in format fmt."""
+    if fmt == FP8G_E2M1:
+        return cols // 2
+    if fmt in (FP8G_E2M3, FP8G_E3M2):
+        return cols * 3 // 4
+    return cols
+
+
 def quantize(x, block: int = 32, stream=None, fmt: int = FP8G_E4M3):
     """fp32 CUDA tensor [rows, cols] -> (uint8 codes, fp32 scales) in format fmt
-    (E2M1: two codes per byte, codes [rows, cols/2])."""
+    (E2M1: two codes per byte, codes [rows, cols/2]; FP6: four codes per three
+    bytes, codes [rows, 3 cols/4])."""
     import torch
     assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2
     x = x.contiguous()
     rows, cols = x.shape
-    qcols = cols // 2 if fmt == FP8G_E2M1 else cols
+    qcols = packed_cols(cols, fmt)
     q = torch.empty((rows, qcols), dtype=torch.uint8, device=x.device)
     if block != 0:
         s = torch.empty((rows, cols // 32), dtype=torch.float32, device=x.device)

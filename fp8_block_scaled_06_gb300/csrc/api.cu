@@ -196,10 +196,16 @@ fp8g_status tmap_encode(const void *ptr, CUtensorMapDataType dtype, int ebits, i
 // which is how kind::f8f6f4 / mxf8f6f4 MMAs read 4-bit operands, so a tile
 // takes the same shared memory as an FP8 tile of the same shape; the load
 // counts only the packed bytes (half of that) toward the stage's mbarrier.
+// FP6 (E2M3, E3M2): four codes per three bytes in memory; the 16U6_ALIGN16B
+// load widens every 16 codes (12 bytes) to a 16-byte slot (4 unused bytes)
+// and counts three quarters of the tile.
 fp8g_status tmap_operand(const void *ptr, int fmt, int rank, const uint64_t *dims,
                          const uint32_t *box, int dev, CUtensorMap &out) {
     if (fmt == FP8G_E2M1)
         return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, rank, dims, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
+    if (fmt == FP8G_E2M3 || fmt == FP8G_E3M2)
+        return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B, 6, rank, dims, box,
                            CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
     return tmap_encode(ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 8, rank, dims, box,
                        CU_TENSOR_MAP_SWIZZLE_128B, dev, out);
@@ -207,19 +213,25 @@ fp8g_status tmap_operand(const void *ptr, int fmt, int rank, const uint64_t *dim
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_fmt(int f) { return f == FP8G_E4M3 || f == FP8G_E5M2 || f == FP8G_E2M1; }
+bool valid_fmt(int f) { return f >= FP8G_E4M3 && f <= FP8G_E3M2; }
 
 // The MMA instruction descriptor's A / B type field (kind::f8f6f4 and
-// kind::mxf8f6f4): E4M3 0, E5M2 1, E2M1 5.
+// kind::mxf8f6f4): E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5.
 uint32_t mma_type(int f) { return f == FP8G_E2M1 ? 5u : (uint32_t)f; }
 
-// Packed E2M1 operands: the 16U4_ALIGN16B tile map wants K a multiple of 128
-// and the operand's base 32-byte aligned (its row stride, K / 2 bytes, is
-// then a multiple of 64).
-fp8g_status check_e2m1(const void *A, const void *B, int a_fmt, int b_fmt, int64_t K) {
-    if (a_fmt != FP8G_E2M1 && b_fmt != FP8G_E2M1) return FP8G_OK;
+// Packed operands (E2M1, FP6)
+bool packed_fmt(int f) { return f == FP8G_E2M1 || f == FP8G_E2M3 || f == FP8G_E3M2; }
+
+// Eighths of an operand tile that its packed load does not deliver.
+int32_t gap8(int f) { return f == FP8G_E2M1 ? 4 : (f == FP8G_E2M3 || f == FP8G_E3M2) ? 2 : 0; }
+
+// Packed operands: the 16U4 / 16U6 tile maps want K a multiple of 128 and the
+// operand's base 32-byte aligned (its row stride, K / 2 or 3K / 4 bytes, is
+// then a multiple of 32).
+fp8g_status check_packed(const void *A, const void *B, int a_fmt, int b_fmt, int64_t K) {
+    if (!packed_fmt(a_fmt) && !packed_fmt(b_fmt)) return FP8G_OK;
     if (K % 128 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if ((a_fmt == FP8G_E2M1 && !aligned(A, 32)) || (b_fmt == FP8G_E2M1 && !aligned(B, 32)))
+    if ((packed_fmt(a_fmt) && !aligned(A, 32)) || (packed_fmt(b_fmt) && !aligned(B, 32)))
         return FP8G_ERR_ALIGNMENT;
     return FP8G_OK;
 }
@@ -277,7 +289,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
         return FP8G_ERR_INVALID_ARG;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
-    fp8g_status st = check_e2m1(M > 0 ? A : B, B, M > 0 ? a_fmt : b_fmt, b_fmt, K);
+    fp8g_status st = check_packed(M > 0 ? A : B, B, M > 0 ? a_fmt : b_fmt, b_fmt, K);
     if (st != FP8G_OK) return st;
     DevInfo di;
     st = device_info(di);
@@ -310,8 +322,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.status = di.status;
     p.timeout_ns = timeout_ns();
     p.ab_fmt = (mma_type(a_fmt) << 7) | (mma_type(b_fmt) << 10);
-    p.a_e2m1 = a_fmt == FP8G_E2M1;
-    p.b_e2m1 = b_fmt == FP8G_E2M1;
+    p.a_gap8 = gap8(a_fmt);
+    p.b_gap8 = gap8(b_fmt);
     p.bias = bias;
     p.act = act;
     p.c_row_of = c_row_of;
@@ -567,7 +579,7 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
         return FP8G_ERR_INVALID_ARG;
     // the scales' rows (K/32 fp32) are TMA rows: 16-byte multiples
     if (K % 128 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if ((st = check_e2m1(A, B, a_fmt, b_fmt, K)) != FP8G_OK) return st;
+    if ((st = check_packed(A, B, a_fmt, b_fmt, K)) != FP8G_OK) return st;
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
     DevInfo di;
@@ -588,8 +600,8 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     p.status = di.status;
     p.timeout_ns = timeout_ns();
     p.ab_fmt = (mma_type(a_fmt) << 7) | (mma_type(b_fmt) << 10);
-    p.a_e2m1 = a_fmt == FP8G_E2M1;
-    p.b_e2m1 = b_fmt == FP8G_E2M1;
+    p.a_gap8 = gap8(a_fmt);
+    p.b_gap8 = gap8(b_fmt);
     p.bias = bias;
     p.act = act;
     GemmMaps maps;

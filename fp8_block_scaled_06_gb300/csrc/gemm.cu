@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
     constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES : C_::TX_BYTES;
-    const uint32_t tx_bytes = kTxBytes - (p.a_e2m1 ? C_::A_BYTES / 2 : 0) -
-                              (p.b_e2m1 ? C_::B_BYTES / 2 : 0);
+    const uint32_t tx_bytes = kTxBytes - C_::A_BYTES / 8 * (uint32_t)p.a_gap8 -
+                              C_::B_BYTES / 8 * (uint32_t)p.b_gap8;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA tiles need 1024-byte alignment in the shared window
     const uint32_t raw_base = ptx::smem_addr(smem_raw);

@@ -262,10 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Both CTAs' copies complete on the even CTA's full barrier (TMA
         // cta_group::2), which expects both halves; the odd CTA does not arrive.
         if (lane == 0) {
-            // F4 loads dense bytes; otherwise an E2M1 operand's 4-bit tile
-            // load counts only its packed bytes
+            // F4 loads dense bytes; otherwise a packed (E2M1, FP6) operand's
+            // tile load counts only its packed bytes
             const uint32_t tx_bytes =
-                F4 ? PC::TX : PC::TX - (p.a_e2m1 ? kA / 2 : 0) - (p.b_e2m1 ? kB / 2 : 0);
+                F4 ? PC::TX
+                   : PC::TX - kA / 8 * (uint32_t)p.a_gap8 - kB / 8 * (uint32_t)p.b_gap8;
             const int32_t num_kg = PC::G * p.num_kb;  // K groups of the packed scales
             uint32_t stage = 0, phase = 0;
             for (int32_t t = t_first; t < T; t += t_step) {

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ===== TMA producer =====
         if (lane == 0) {
             const uint32_t tx_bytes =
-                kPStage - (p.a_e2m1 ? kPA / 2 : 0) - (p.b_e2m1 ? kPB / 2 : 0);
+                kPStage - kPA / 8 * (uint32_t)p.a_gap8 - kPB / 8 * (uint32_t)p.b_gap8;
             uint32_t stage = 0, phase = 0;
             for (int32_t t = blockIdx.x; t < T; t += gridDim.x) {
                 int32_t pm, pn;

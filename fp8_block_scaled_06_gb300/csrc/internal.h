@@ -42,10 +42,12 @@ struct GemmParams {
     const uint8_t *sfb_pk;
     int32_t n_rtA, n_rtB;  // 128-row tiles per K group in the packed arrays
     uint32_t ab_fmt;       // operand formats as MMA instruction-descriptor bits (A: 7-9, B: 10-12)
-    // Packed E2M1 operands (two codes per byte): their tile loads deliver the
-    // packed byte count, half a tile's shared-memory footprint, so each stage
-    // expects that many fewer transaction bytes.
-    int32_t a_e2m1, b_e2m1;
+    // Packed operands (E2M1 two codes per byte, FP6 four codes per three
+    // bytes): their tile loads deliver the packed byte count, not the tile's
+    // shared-memory footprint (16 codes widened to 16 bytes), so each stage
+    // expects that many fewer transaction bytes: gap8 eighths of the operand's
+    // tile (E2M1 4, FP6 2, FP8 0).
+    int32_t a_gap8, b_gap8;
     // E2M1 x E2M1 block-scaled on CTA pairs at the FP4 rate (kind::mxf4):
     // operands loaded as dense bytes, 256 K elements per stage, num_kb = K /
     // 256, the packed scale arrays holding 2 * num_kb chunks per row tile.

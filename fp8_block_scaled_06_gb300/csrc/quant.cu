@@ -3,7 +3,10 @@
 // E5M2 (fmax = 57344), the two FP8 formats of the format paragraph of
 // "Optimizing FP8 GEMM kernels in JAX with Triton for Blackwell GPUs", and
 // E2M1 (fmax = 6, two codes per byte, the first in the low nibble), the FP4
-// element of the micro-scaling formats of the Triton tutorial ch. 12, 12.6.1.
+// element of the micro-scaling formats of the Triton tutorial ch. 12, 12.6.1,
+// and the FP6 elements E2M3 (fmax = 7.5) and E3M2 (fmax = 28), the tensor
+// core's FP6 types of that page's 12.6.1 table (four codes per three bytes,
+// code i in bits 6i .. 6i+5 of a little-endian bit string).
 //
 // Per-tensor: s = fl32(amax / fmax) over the non-NaN |x| (1 if that is 0).
 // 1x32 block along the contiguous axis: s = the smallest power of two with
@@ -13,7 +16,7 @@
 // 12.6.1; its "fine-grained quantisation" advice against FP8 underflow is the
 // reason for the block form.  q = FP8(fl32(x / s)), round to nearest even,
 // saturating (cvt ... satfinite), NaN -> 0x7F (a NaN code in both FP8
-// formats; E2M1 has none and takes +6).
+// formats; E2M1 has none and takes +6, FP6 its largest value, code 0x1F).
 //
 // The source is fp32 or bf16 (activations; widened exactly), and the output
 // rows may gather source rows through an index list (the routing step of the
@@ -24,17 +27,18 @@
 // scale per 1x16 block and an fp32 scale per tensor (quant_nvfp4_kernel; the
 // recipe is stated there).
 //
-// HBM-bound elementwise kernels: 16-byte loads, 8-byte (E2M1: 4-byte)
-// stores, a grid of a few CTAs per SM striding over the output.
+// HBM-bound elementwise kernels: 16-byte loads, 8-byte (E2M1: 4-byte; FP6:
+// three 2-byte) stores, a grid of a few CTAs per SM striding over the output.
 #include "internal.h"
 
 namespace fp8g {
 
 namespace {
 
-// FMT 0: E4M3, 1: E5M2, 2: E2M1 (FP4, two codes per byte).  Largest finite
-// value kMax = mmax * 2^kEmax; kMantOver is the fp32 mantissa field above
-// which a value m 2^E (1 <= m < 2) exceeds mmax * 2^E (mmax = 1.75 or 1.5).
+// FMT 0: E4M3, 1: E5M2, 2: E2M1 (FP4, two codes per byte), 3: E2M3, 4: E3M2
+// (FP6, four codes per three bytes).  Largest finite value kMax = mmax *
+// 2^kEmax; kMantOver is the fp32 mantissa field above which a value m 2^E
+// (1 <= m < 2) exceeds mmax * 2^E (mmax = 1.75, 1.5 or 1.875).
 template <int FMT>
 struct Fp8Fmt;
 template <>
@@ -55,10 +59,23 @@ struct Fp8Fmt<2> {
     static constexpr int kEmax = 2;
     static constexpr uint32_t kMantOver = 0x400000u;
 };
+template <>
+struct Fp8Fmt<3> {
+    static constexpr float kMax = 7.5f;
+    static constexpr int kEmax = 2;
+    static constexpr uint32_t kMantOver = 0x700000u;
+};
+template <>
+struct Fp8Fmt<4> {
+    static constexpr float kMax = 28.0f;
+    static constexpr int kEmax = 4;
+    static constexpr uint32_t kMantOver = 0x600000u;
+};
 
-// Two fp32 values -> their codes, lo first: FP8 two bytes (lo at the lower
-// address), E2M1 one byte (lo in the low nibble).  NaN, which E2M1 cannot
-// hold, becomes code 7 (+6) there.
+// Two fp32 values -> their codes, lo first: FP8 and FP6 two bytes (lo at the
+// lower address; FP6 codes in the low six bits), E2M1 one byte (lo in the low
+// nibble).  NaN, which E2M1 and FP6 cannot hold, becomes their largest
+// positive value (E2M1 code 7, FP6 code 0x1F).
 template <int FMT>
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
     uint32_t v;
@@ -73,12 +90,17 @@ __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
         uint16_t r;
         if constexpr (FMT == 0)
             asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-        else
+        else if constexpr (FMT == 1)
             asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        else if constexpr (FMT == 3)
+            asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+        else
+            asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
         v = r;
     }
-    if (isnan(lo)) v = (v & 0xFF00u) | 0x7Fu;
-    if (isnan(hi)) v = (v & 0x00FFu) | 0x7F00u;
+    constexpr uint32_t kNan = FMT >= 3 ? 0x1Fu : 0x7Fu;
+    if (isnan(lo)) v = (v & 0xFF00u) | kNan;
+    if (isnan(hi)) v = (v & 0x00FFu) | (kNan << 8);
     return v;
 }
 
@@ -89,13 +111,26 @@ __device__ __forceinline__ uint32_t fp8x4(float x0, float x1, float x2, float x3
 }
 
 // Store the codes of group g (values 8g .. 8g+7 of the output): 8 bytes
-// (FP8) or 4 bytes (E2M1) at g times that size.
+// (FP8), 4 bytes (E2M1) or 6 bytes (FP6: the eight six-bit codes as a 48-bit
+// little-endian string) at g times that size.
 template <int FMT>
 __device__ __forceinline__ void store8(uint8_t *q, int64_t g, uint2 o) {
-    if constexpr (FMT == 2)
+    if constexpr (FMT == 2) {
         reinterpret_cast<uint32_t *>(q)[g] = o.x | (o.y << 16);
-    else
+    } else if constexpr (FMT >= 3) {
+        uint64_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v |= (uint64_t)((o.x >> (8 * i)) & 0x3Fu) << (6 * i);
+            v |= (uint64_t)((o.y >> (8 * i)) & 0x3Fu) << (24 + 6 * i);
+        }
+        uint16_t *p = reinterpret_cast<uint16_t *>(q + 6 * g);  // 2-byte aligned
+        p[0] = (uint16_t)v;
+        p[1] = (uint16_t)(v >> 16);
+        p[2] = (uint16_t)(v >> 32);
+    } else {
         reinterpret_cast<uint2 *>(q)[g] = o;
+    }
 }
 
 // 8 values -> their codes (first four in .x), for store8.
@@ -408,6 +443,12 @@ cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int
                                  uint8_t *q, float *scales, unsigned int *status, int num_sms,
                                  cudaStream_t s) {
     const RowMap m{x, rows, x_rows, cols, status};
+    if (fmt == 3)
+        return in_bf16 ? launch_rows<3, true>(m, n_rows, block, q, scales, num_sms, s)
+                       : launch_rows<3, false>(m, n_rows, block, q, scales, num_sms, s);
+    if (fmt == 4)
+        return in_bf16 ? launch_rows<4, true>(m, n_rows, block, q, scales, num_sms, s)
+                       : launch_rows<4, false>(m, n_rows, block, q, scales, num_sms, s);
     if (fmt == 2)
         return in_bf16 ? launch_rows<2, true>(m, n_rows, block, q, scales, num_sms, s)
                        : launch_rows<2, false>(m, n_rows, block, q, scales, num_sms, s);

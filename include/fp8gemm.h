@@ -96,8 +96,24 @@ typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F32 = 1 } fp8g_out;
  * FP4-rate MMA (kind::mxf4); every other E2M1 call runs the FP8-rate MMA
  * (kind::f8f6f4 / mxf8f6f4).  The entry points without a format argument
  * take E4M3.
+ * FP6 [TUT-12 12.6.1 hardware table, 12.6.4 stability table; with 1x32
+ * power-of-two scales this is MXFP6]: E2M3 (bias 1, 3 mantissa bits, values
+ * k/8 below 2, largest 7.5) and E3M2 (bias 3, 2 mantissa bits, subnormals
+ * k/16, largest 28), no infinities or NaNs (the quantiser saturates and
+ * writes NaN as the largest positive value, code 0x1F).  Four codes in three
+ * bytes: code i of a row in bits 6i .. 6i+5 of the row read as a
+ * little-endian bit string, so a row of K elements takes 3K/4 bytes.  The
+ * GEMM rules of E2M1 apply (K % 128 == 0, the operand 32-byte aligned); FP6
+ * runs the FP8-rate MMA and reads three quarters of the operand bytes.  Any
+ * two formats may be paired.
  */
-typedef enum { FP8G_E4M3 = 0, FP8G_E5M2 = 1, FP8G_E2M1 = 2 } fp8g_format;
+typedef enum {
+    FP8G_E4M3 = 0,
+    FP8G_E5M2 = 1,
+    FP8G_E2M1 = 2,
+    FP8G_E2M3 = 3,
+    FP8G_E3M2 = 4
+} fp8g_format;
 
 /*
  * Fused-epilogue activations [TRITON-FP8 benchmark list: a bias_add_relu
@@ -225,7 +241,9 @@ FP8G_API fp8g_status fp8g_quantize_e4m3(const float *x, int64_t rows, int64_t co
  * the smallest power of two with 57344*s >= amax; saturation to +-57344;
  * infinities saturate too; NaN -> 0x7F).  With FP8G_E2M1 the bound is 6
  * (saturation to +-6, NaN -> code 7) and q holds two codes per byte: uint8
- * [rows, cols/2].  A bad `fmt` is FP8G_ERR_INVALID_ARG.
+ * [rows, cols/2].  With FP8G_E2M3 / FP8G_E3M2 the bound is 7.5 / 28
+ * (saturation, NaN -> code 0x1F) and q holds four codes per three bytes:
+ * uint8 [rows, 3 cols/4].  A bad `fmt` is FP8G_ERR_INVALID_ARG.
  */
 FP8G_API fp8g_status fp8g_quantize(const float *x, int64_t rows, int64_t cols, int32_t block,
                           int32_t fmt, uint8_t *q, float *scales, cudaStream_t stream);

@@ -95,7 +95,7 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
     reject bad arguments on the host, before any device work (no GPU here)."""
     P = 1 << 20
     E = fp8g.FP8G_ERR_INVALID_ARG
-    assert _err(fp8g.fp8_gemm_fmt, P, P, P, P, P, 0, 3, 0, 8, 8, 16, 0) == E      # bad A format
+    assert _err(fp8g.fp8_gemm_fmt, P, P, P, P, P, 0, 5, 0, 8, 8, 16, 0) == E      # bad A format
     # packed E2M1 operands: K % 128, the operand 32-byte aligned
     assert _err(fp8g.fp8_gemm_fmt, P, P, P, P, P, 0, 2, 0, 8, 8, 64, 0) == \
         fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
@@ -104,6 +104,14 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
     assert _err(fp8g.fp8_gemm_blockscaled_promote, P + 16, P, P, P, P, 0, 2, 0, None, 0, 8, 8,
                 128, 0) == fp8g.FP8G_ERR_ALIGNMENT
     assert _err(fp8g.fp8_gemm_blockscaled_fmt, P, P, P, P, P, 0, 0, 5, 8, 8, 64, 0) == E
+    assert _err(fp8g.fp8_gemm_blockscaled_fmt, P, P, P, P, P, 0, 0, -1, 8, 8, 64, 0) == E
+    # packed FP6 operands (E2M3 3, E3M2 4): the rules of E2M1
+    assert _err(fp8g.fp8_gemm_fmt, P, P, P, P, P, 0, 3, 0, 8, 8, 64, 0) == \
+        fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert _err(fp8g.fp8_gemm_blockscaled_fmt, P, P + 16, P, P, P, 0, 0, 4, 8, 8, 128, 0) == \
+        fp8g.FP8G_ERR_ALIGNMENT
+    assert _err(fp8g.fp8_grouped_gemm_ex, P + 16, P, P, P, P, 0, 4, 3, None, 0, P, 2, 8, 128, 8,
+                None, None, 0) == fp8g.FP8G_ERR_ALIGNMENT
     assert _err(fp8g.fp8_gemm_ex, P, P, P, P, P, 0, 0, 0, None, 3, 8, 8, 16, 0) == E  # bad act
     assert _err(fp8g.fp8_gemm_blockscaled_ex, P, P, P, P, P, 0, 0, 0, P + 2, 1, 8, 8, 64, 0) == \
         fp8g.FP8G_ERR_ALIGNMENT                                                  # bias alignment
@@ -111,7 +119,7 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
                 None, 0) == E
     assert _err(fp8g.fp8_gemm_blockscaled_promote, P, P, P, P, P, 0, 0, 0, None, 0, 8, 8, 96,
                 0) == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE                            # K % 128
-    assert _err(fp8g.fp8_gemm_blockscaled_promote, P, P, P, P, P, 0, 0, 3, None, 0, 8, 8, 128,
+    assert _err(fp8g.fp8_gemm_blockscaled_promote, P, P, P, P, P, 0, 0, 5, None, 0, 8, 8, 128,
                 0) == E
     assert _err(fp8g.fp8_grouped_gemm_scatter, P, P, P, P, P, 0, 0, 0, None, 0, P, 2, 8, 64, 8,
                 P + 2, 16, None, None, 0) == E                                   # misaligned map
@@ -119,7 +127,7 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
                 P, 0, None, None, 0) == E                                        # no rows of C
     # quantiser: source type, format, block mode, gather without rows > source rows
     assert _err(fp8g.fp8g_quantize_rows, P, 2, 4, 64, None, 4, 32, 0, P, P, 0) == E
-    assert _err(fp8g.fp8g_quantize_rows, P, 0, 4, 64, None, 4, 32, 3, P, P, 0) == E
+    assert _err(fp8g.fp8g_quantize_rows, P, 0, 4, 64, None, 4, 32, 5, P, P, 0) == E
     assert _err(fp8g.fp8g_quantize_rows, P, 0, 4, 64, None, 4, 17, 0, P, P, 0) == E
     assert _err(fp8g.fp8g_quantize_rows, P, 0, 4, 64, None, 5, 32, 0, P, P, 0) == E
     assert _err(fp8g.fp8g_quantize_rows, P, 1, 4, 40, None, 4, fp8g.FP8G_BLOCK32_LITERAL, 0, P,

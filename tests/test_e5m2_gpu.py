@@ -133,9 +133,9 @@ def test_bad_format_rejected():
     s = torch.ones(1, device="cuda")
     C = torch.empty(128, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fp8g.Fp8gError) as e:
-        fp8g.fp8_gemm_fmt(q, q, s, s, C, 0, 3, 0, 128, 128, 128)
+        fp8g.fp8_gemm_fmt(q, q, s, s, C, 0, 5, 0, 128, 128, 128)
     assert e.value.status == fp8g.FP8G_ERR_INVALID_ARG
     x = torch.zeros(4, 32, device="cuda")
     with pytest.raises(fp8g.Fp8gError) as e:
-        fp8g.fp8g_quantize(x, 4, 32, 32, 3, q, s)
+        fp8g.fp8g_quantize(x, 4, 32, 32, 5, q, s)
     assert e.value.status == fp8g.FP8G_ERR_INVALID_ARG
