@@ -2,7 +2,8 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload large8192|large4096|skinny|moe|square1024|tensor8192|
-                            mixed8192|literal8192|mxfp4_8192|nvfp4_8192|moe_nvfp4]
+                            mixed8192|literal8192|mxfp4_8192|mxfp6_8192|nvfp4_8192|
+                            moe_nvfp4]
 
 One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
 scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
@@ -47,14 +48,17 @@ WORKLOADS = {
     "literal8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, literal=True),
     # E2M1 x E2M1 with power-of-two 1x32 scales (MXFP4), two codes per byte
     "mxfp4_8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
+    # E2M3 x E2M3 with power-of-two 1x32 scales (MXFP6), four codes per 3 bytes
+    "mxfp6_8192": dict(kind="block", M=8192, N=8192, K=8192, seed=3, a_fmt=3, b_fmt=3),
     # NVFP4: E2M1 with 1x16 E4M3 block scales and an fp32 scale per tensor
     "nvfp4_8192": dict(kind="nvfp4", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
     # the MoE workload in NVFP4 (each expert's weight with its own tensor scale)
     "moe_nvfp4": dict(kind="grouped_nvfp4", M=32768, N=14336, K=4096, seed=4, a_fmt=2, b_fmt=2),
 }
-FMT_NAMES = ["e4m3", "e5m2", "e2m1"]
-# bytes per element of each format in memory (E2M1: two codes per byte)
-FMT_BYTES = [1.0, 1.0, 0.5]
+FMT_NAMES = ["e4m3", "e5m2", "e2m1", "e2m3", "e3m2"]
+# bytes per element of each format in memory (E2M1: two codes per byte; FP6:
+# four codes per three bytes)
+FMT_BYTES = [1.0, 1.0, 0.5, 0.75, 0.75]
 METRIC = "FP8 GEMM TFLOPS and % of GB300 roofline (tensor peak or HBM) at 1 GPU"
 
 
@@ -226,7 +230,8 @@ def run_once(fp8g, wl, w, t, C, stream):
 # a capture report null.
 TRAFFIC_BYTES = {"large8192": 260_747_776 + 117_235_712,
                  "mxfp4_8192": 107_155_200 + 95_997_440,
-                 "nvfp4_8192": 113_520_384 + 98_173_184}
+                 "nvfp4_8192": 113_520_384 + 98_173_184,
+                 "mxfp6_8192": 167_501_824 + 110_660_864}
 
 
 def fp4_rate(fp8g, wl) -> bool:
@@ -532,8 +537,8 @@ def main():
         roof["peak_source"] += (" (NVFP4: the FP4-rate MMA, kind::mxf4nvf4 scale_vec::4X)"
                                 if wl["kind"] in ("nvfp4", "grouped_nvfp4") else
                                 " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)")
-    elif 2 in (wl.get("a_fmt", 0), wl.get("b_fmt", 0)) and tensor_bound:
-        roof["peak_source"] += " (E2M1 operands on the FP8-rate MMA, kind::f8f6f4)"
+    elif {2, 3, 4} & {wl.get("a_fmt", 0), wl.get("b_fmt", 0)} and tensor_bound:
+        roof["peak_source"] += " (E2M1 / FP6 operands on the FP8-rate MMA, kind::f8f6f4)"
     roof["nominal_frac"] = round(max(flops / (13.5e15 if f4 else 4.5e15), abytes / 8e12) /
                                  (kernel_ms * 1e-3), 4)
 
