@@ -205,3 +205,44 @@ def test_fp6_promote_literal_scales():
     ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, True, oracle.OUT_BF16, a_fmt=E3M2,
                                 b_fmt=E2M3, bias=bias, act_kind=oracle.ACT_GELU)
     assert_within(C.float().cpu().numpy(), ref, bound, "FP6 literal promote")
+
+
+def test_fp6_grouped_pairs_sampled():
+    """Grouped MoE GEMM on CTA pairs (the 3-D 16U6 map of B, expert-local
+    256-row tiles) with E3M2 activations and E2M3 weights: empty, one-row and
+    ragged experts; offsets and tile map bit-exact; sampled outputs per
+    expert."""
+    counts = np.array([3000, 0, 70, 9000, 257, 1, 0, 129], np.int32)
+    E, N, K = counts.size, 2048, 512
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, E)
+    assert plan["BM"] == 256
+    w = synth.small_grouped(counts, N, K, seed=31)
+    qa, sa, qa_o, sa_o = _quant(w.A, 32, E3M2)
+    qb, sb, qb_o, sb_o = _quant(w.B.reshape(E * N, K), 32, E2M3)
+    C = torch.full((rows, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    tmap = torch.full((plan["max_tiles"], 4), -1, dtype=torch.int32, device="cuda")
+    fp8g.fp8_grouped_gemm_fmt(qa, qb.reshape(E, N, 3 * K // 4), sa, sb.reshape(E, N, K // 32), C,
+                              0, E3M2, E2M3, torch.from_numpy(counts).cuda(), E, N, K, rows, offs,
+                              tmap)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    offs_o = oracle.grouped_offsets(counts)
+    assert np.array_equal(offs.cpu().numpy(), offs_o)
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert np.array_equal(tmap.cpu().numpy()[:want.shape[0]], want)
+    Ch = C.float().cpu().numpy()
+    qb_o = qb_o.reshape(E, N, K)
+    sb_o = sb_o.reshape(E, N, K // 32)
+    rng = np.random.default_rng(32)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        r0, r1 = int(offs_o[e]), int(offs_o[e + 1])
+        m = r1 - r0
+        pi = np.concatenate([[0, m - 1, min(255, m - 1), min(256, m - 1)], rng.integers(0, m, 300)])
+        pj = rng.integers(0, N, pi.size)
+        ref, bound, _ = oracle.gemm_sample(qa_o[r0:r1], qb_o[e], sa_o[r0:r1], sb_o[e], True, pi,
+                                           pj, oracle.OUT_BF16, a_fmt=E3M2, b_fmt=E2M3)
+        assert_within(Ch[r0 + pi, pj], ref, bound, f"FP6 grouped pairs expert {e}")
