@@ -1,0 +1,61 @@
+"""Host logic of bench.py that needs no GPU: the algorithmic bytes that are
+the numerator of every HBM roofline figure, per workload, against the
+per-array sums written out here (A and B at their stored element size, the
+scales the call reads, C once), and the workload table's sizes."""
+from types import SimpleNamespace
+
+import pytest
+import torch
+
+import bench
+
+MiB = 1 << 20
+
+
+def _w(out="bf16", experts=None):
+    B = torch.empty((experts, 1, 1)) if experts else torch.empty((1, 1))
+    return SimpleNamespace(out=out, B=B)
+
+
+# name -> (A bytes, B bytes, scale bytes, C bytes), each written out
+EXPECTED = {
+    # E4M3 8192^3, fp32 1x32 scales of A and B, bf16 C
+    "large8192": (64 * MiB, 64 * MiB, 2 * 4 * 8192 * 256, 128 * MiB),
+    # per-tensor: two fp32 scales
+    "tensor8192": (64 * MiB, 64 * MiB, 8, 128 * MiB),
+    # E2M1: half a byte per element
+    "mxfp4_8192": (32 * MiB, 32 * MiB, 2 * 4 * 8192 * 256, 128 * MiB),
+    # FP6: three quarters of a byte per element
+    "mxfp6_8192": (48 * MiB, 48 * MiB, 2 * 4 * 8192 * 256, 128 * MiB),
+    # NVFP4: E4M3 scale bytes per 16 elements (4 MiB per operand) + gA, gB
+    "nvfp4_8192": (32 * MiB, 32 * MiB, 2 * 4 * MiB + 8, 128 * MiB),
+    # skinny 128 x 4096 x 4096
+    "skinny": (128 * 4096, 16 * MiB, 4 * (128 + 4096) * 128, 128 * 4096 * 2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EXPECTED))
+def test_algorithmic_bytes(name):
+    wl = bench.WORKLOADS[name]
+    assert bench.algorithmic_bytes(wl, _w()) == sum(EXPECTED[name])
+
+
+def test_algorithmic_bytes_grouped():
+    """MoE: 32768 routed rows, 8 experts of [14336, 4096]; the FP8 form reads
+    fp32 1x32 scales and the counts, the NVFP4 form E4M3 scale bytes, gA, the
+    8 gB and the counts."""
+    rows, E, N, K = 32768, 8, 14336, 4096
+    fp8 = rows * K + E * N * K + 4 * (rows + E * N) * K // 32 + rows * N * 2 + 4 * E
+    assert bench.algorithmic_bytes(bench.WORKLOADS["moe"], _w(experts=E)) == fp8
+    nv = rows * K // 2 + E * N * K // 2 + (rows + E * N) * K // 16 + 4 * (1 + E) + \
+        rows * N * 2 + 4 * E
+    assert bench.algorithmic_bytes(bench.WORKLOADS["moe_nvfp4"], _w(experts=E)) == nv
+
+
+def test_workload_table():
+    """Every workload is named by its sizes; formats are the library's codes."""
+    for name, wl in bench.WORKLOADS.items():
+        assert wl["kind"] in ("block", "tensor", "grouped", "nvfp4", "grouped_nvfp4"), name
+        assert wl.get("a_fmt", 0) in range(5) and wl.get("b_fmt", 0) in range(5), name
+        assert wl["M"] > 0 and wl["N"] > 0 and wl["K"] % 32 == 0, name
+    assert len(bench.FMT_NAMES) == len(bench.FMT_BYTES) == 5
