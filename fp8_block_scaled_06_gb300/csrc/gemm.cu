@@ -3,7 +3,9 @@
 //   C = (sA A)(sB B)^T,  A[M,K], B[N,K] row-major, fp32 accumulation in tensor
 //   memory, bf16 or fp32 output.  Three modes: per-tensor scales, 1x32 block
 //   scales along K (applied by the block-scaled tensor-core MMA), and the
-//   grouped (MoE) form of the block-scaled GEMM.
+//   grouped (MoE) form of the block-scaled GEMM.  Operands E4M3 or any other
+//   kind::f8f6f4 element (E5M2, E2M3, E3M2, E2M1; the packed ones load
+//   through the 4- and 6-bit tile types), one format per operand.
 //
 // Design (GB300-native; the pages' Triton/Pallas kernels are prior art only):
 //   - one CTA per SM, persistent over output tiles in the grouped raster order

@@ -1,6 +1,6 @@
-// FP8 / FP4 GEMMs on CTA pairs (tcgen05 cta_group::2), sm_103a: per-tensor,
-// block-scaled and grouped FP8 (any E4M3 / E5M2 / E2M1 operand pairing on the
-// FP8-rate MMA), MXFP4 and NVFP4 on the FP4-rate MMAs.
+// FP8 / FP6 / FP4 GEMMs on CTA pairs (tcgen05 cta_group::2), sm_103a:
+// per-tensor, block-scaled and grouped, any E4M3 / E5M2 / E2M3 / E3M2 / E2M1
+// operand pairing on the FP8-rate MMA; MXFP4 and NVFP4 on the FP4-rate MMAs.
 //
 // Why: the single-CTA kernel stages 48 KB per 128-wide K step for a 128x256
 // output tile, so four stages fill shared memory and cannot hide the refill
