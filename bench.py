@@ -228,10 +228,11 @@ def run_once(fp8g, wl, w, t, C, stream):
 # of the dominant kernel, from the ncu captures summarised in profiles/.
 # Valid only for the kernel source those captures measured: an entry leaves
 # this table when its kernel changes, and workloads without a capture of the
-# current kernel report null.  (The 8192^3 E4M3, MXFP4 and NVFP4 pair-kernel
-# captures predate the last change to that kernel's source; their summaries
-# stay in profiles/ as the record of that build.)
-TRAFFIC_BYTES = {"mxfp6_8192": 167_501_824 + 110_660_864}
+# current kernel report null.
+TRAFFIC_BYTES = {"large8192": 261_927_680 + 116_877_312,
+                 "mxfp4_8192": 107_267_584 + 95_654_144,
+                 "nvfp4_8192": 113_694_976 + 97_257_984,
+                 "mxfp6_8192": 167_501_824 + 110_660_864}
 
 
 def fp4_rate(fp8g, wl) -> bool:
