@@ -523,6 +523,22 @@ fp8g_status run_nvfp4(int mode, const void *A, const void *B, const uint8_t *sfa
     return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
+fp8g_status check_blockscaled_args(const void *A, const void *B, const float *sfa,
+                                  const float *sfb, const void *C, int out, int64_t M, int64_t N,
+                                  int64_t K) {
+    const fp8g_status st = check_common(A, B, C, out, M, N, K);
+    if (st != FP8G_OK) return st;
+    if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
+    return FP8G_OK;
+}
+
+fp8g_status device_ready() {
+    DevInfo di;
+    return device_info(di);
+}
+
 }  // namespace fp8g
 
 using namespace fp8g;
@@ -557,11 +573,8 @@ fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const float *s
                                     const float *sfb, void *C, int out, int32_t a_fmt,
                                     int32_t b_fmt, const float *bias, int32_t act, int64_t M,
                                     int64_t N, int64_t K, cudaStream_t stream) {
-    fp8g_status st = check_common(A, B, C, out, M, N, K);
+    const fp8g_status st = check_blockscaled_args(A, B, sfa, sfb, C, out, M, N, K);
     if (st != FP8G_OK) return st;
-    if (sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
-    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(sfa, 16) || !aligned(sfb, 16)) return FP8G_ERR_ALIGNMENT;
     return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,
                     stream, nullptr, 0, a_fmt, b_fmt, bias, act);
 }

@@ -106,6 +106,16 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      const float *bias = nullptr, int act = 0, const int32_t *c_row_of = nullptr,
                      int64_t c_rows = 0);
 
+// api.cu: the host-side argument checks of the 1x32 block-scaled GEMM, in the
+// order fp8_gemm_blockscaled applies them (shared by its allocation-free
+// form, so both return the same status for the same bad arguments); and the
+// current device's usability (an sm_103 device, status word and tensor-map
+// encoder set up), FP8G_OK or the status a GEMM call would return.
+fp8g_status check_blockscaled_args(const void *A, const void *B, const float *sfa,
+                                  const float *sfb, const void *C, int out, int64_t M, int64_t N,
+                                  int64_t K);
+fp8g_status device_ready();
+
 // scales.cu: fp32 1x32 scales -> packed UE8M0 chunks.  One launch packs
 // two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid
 // rows per z), dst chunks ((z * n_kg + kg) * n_rt + rt) * 512; counts != null

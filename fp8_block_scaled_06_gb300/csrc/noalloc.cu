@@ -42,8 +42,6 @@ fp8g_status noalloc_scratch(void **out) {
     return FP8G_OK;
 }
 
-bool is_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace fp8g
 
@@ -54,21 +52,12 @@ extern "C" {
 fp8g_status fp8_gemm_blockscaled_noalloc(const void *A, const void *B, const float *sfa,
                                          const float *sfb, void *C, int out, int64_t M, int64_t N,
                                          int64_t K, cudaStream_t stream) {
-    if (A == nullptr || B == nullptr || C == nullptr || sfa == nullptr || sfb == nullptr)
-        return FP8G_ERR_INVALID_ARG;
-    if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
-    const int64_t kMax = (int64_t)1 << 31;
-    if (M >= kMax || N >= kMax || K >= kMax) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (!is_aligned(A, 16) || !is_aligned(B, 16) || !is_aligned(C, 16) || !is_aligned(sfa, 16) ||
-        !is_aligned(sfb, 16))
-        return FP8G_ERR_ALIGNMENT;
-    if (K % 16 != 0) return FP8G_ERR_ALIGNMENT;
-    if ((N * (out == FP8G_OUT_F32 ? 4 : 2)) % 16 != 0) return FP8G_ERR_ALIGNMENT;
-    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    void *scratch = nullptr;
-    const fp8g_status st = noalloc_scratch(&scratch);
+    // the checks of fp8_gemm_blockscaled, in its order, then the device's
+    fp8g_status st = check_blockscaled_args(A, B, sfa, sfb, C, out, M, N, K);
     if (st != FP8G_OK) return st;
+    if ((st = device_ready()) != FP8G_OK) return st;
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != FP8G_OK) return st;
     // run_gemm returns FP8G_ERR_UNSUPPORTED_SHAPE, before launching anything,
     // when the packed scales would not fit in the array.
     return run_gemm(kModeBlock, A, B, sfa, sfb, C, out, M, N, K, nullptr, 0, nullptr, nullptr,

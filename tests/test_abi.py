@@ -161,3 +161,29 @@ def test_host_checks_of_the_wider_entry_points(fp8g):
     assert _err(gn, P, P, P, P, P, P, P, 0, None, 3, P, 2, 8, 256, 8, None, None, 0) == E
     assert _err(fp8g.fp8g_quantize_nvfp4, P, 0, 4, 40, P, P, P, 0) == \
         fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+
+
+def test_noalloc_checks_match_blockscaled(fp8g):
+    """The allocation-free block-scaled GEMM applies fp8_gemm_blockscaled's
+    argument checks in the same order: the same bad call gets the same status
+    from both (host only; nothing here reaches a device)."""
+    P = 1 << 20
+    cases = [
+        (0, P, P, P, P, 0, 8, 8, 64),          # null A
+        (P, P, None, P, P, 0, 8, 8, 64),       # null sfa
+        (P, P, P, P, P, 2, 8, 8, 64),          # bad output kind
+        (P, P, P, P, P, 0, 0, 8, 64),          # M = 0
+        (P, P, P, P, P, 0, 8, 8, 1 << 31),     # K too large
+        (P + 8, P, P, P, P, 0, 8, 8, 64),      # A misaligned
+        (P, P, P, P, P, 0, 8, 8, 40),          # K % 16
+        (P, P, P, P, P, 0, 8, 4, 64),          # N * 2 % 16
+        (P, P, P, P, P, 0, 8, 8, 48),          # K % 32
+        (P, P, P + 4, P, P, 0, 8, 8, 64),      # sfa misaligned
+        (P, P, P + 4, P, P, 0, 8, 8, 48),      # sfa misaligned and K % 32: shape first
+        (P, P, None, P, P, 0, 8, 8, 48),       # null sfa and K % 32: null first
+        (P, P, None, P, P, 0, 0, 8, 64),       # null sfa and M = 0: shape first
+    ]
+    for args in cases:
+        a = _err(fp8g.fp8_gemm_blockscaled, *args, 0)
+        b = _err(fp8g.fp8_gemm_blockscaled_noalloc, *args, 0)
+        assert a == b, (args, a, b)
