@@ -80,21 +80,24 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks / throttle reasons, sampled every 10 ms with the host
+    time of each sample, so that the record can be cut to the window in which
+    the GPU ran the timed calls."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 10
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host perf_counter time, csv line)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.index), "-lms", "50"],
+                 "-i", str(self.index), "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -103,9 +106,12 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.perf_counter(), ln.strip()))
 
-    def stop(self) -> dict:
+    def stop(self, t0: float | None = None, t_region: float | None = None,
+             t1: float | None = None, tail_ms: float = 0.0) -> dict:
+        """Summary of the samples taken in [t0, t1] (host times; all samples if
+        t0 is None); [t0, t_region] is the timed region itself."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -114,9 +120,15 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self._t.join(timeout=2)
-        sm, smax, reasons, power = [], None, set(), []
+        return self.summarize(self.lines, t0, t_region, t1, tail_ms)
+
+    @classmethod
+    def summarize(cls, lines, t0=None, t_region=None, t1=None, tail_ms: float = 0.0) -> dict:
+        sm, smax, reasons, power, in_region = [], None, set(), [], 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for th, ln in lines:
+            if t0 is not None and not (t0 <= th <= t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -126,12 +138,20 @@ class ClockSampler:
                 power.append(float(f[3]))
             except ValueError:
                 continue
+            if t0 is not None and th <= t_region:
+                in_region += 1
             for name, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        out = {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+               "reasons": sorted(reasons), "samples": len(sm),
+               "power_w_max": max(power) if power else None}
+        if t0 is not None:
+            out["samples_in_timed_region"] = in_region
+            out["window"] = (f"every {cls.INTERVAL_MS} ms over the timed region "
+                             f"({(t_region - t0) * 1e3:.1f} ms) and a {tail_ms:.0f}-ms run of "
+                             f"the same calls queued right behind it")
+        return out
 
 
 def make_inputs(wl: dict, device):
@@ -316,7 +336,7 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
     for i in range(2 * nbuf):  # warm-up
         step(i)
     torch.cuda.synchronize(device)
-    n = max(3, min(50, steps // 20))
+    n = max(20, min(50, steps // 20))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     start = torch.cuda.Stream(device)
@@ -330,7 +350,7 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
         end.wait_stream(s_)
     e1.record(end)
     torch.cuda.synchronize(device)
-    return e0.elapsed_time(e1) / n
+    return e0.elapsed_time(e1) / n, n
 
 
 def oracle_inputs(wl, w):
@@ -402,6 +422,23 @@ def cpu_baseline(oi: dict, budget_s: float = 12.0):
             "sample": f"{r} {oi['desc']}, K={K}: {flops:.3e} FLOP in {dt:.3f} s"}
 
 
+def config_of(name: str, wl: dict, out: str, world: int) -> dict:
+    """The workload's description: the same dict on both arms of the bench."""
+    return {"workload": name, "M": wl["M"], "N": wl["N"], "K": wl["K"],
+            "formats": FMT_NAMES[wl.get("a_fmt", 0)] + " x " + FMT_NAMES[wl.get("b_fmt", 0)],
+            "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
+                       {"block": "1x32 along K, power of two",
+                        "grouped": "1x32 along K, power of two",
+                        "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
+                        "grouped_nvfp4": "1x16 along K, E4M3, fp32 for A and per "
+                                         "expert weight (NVFP4)",
+                        "tensor": "per tensor"}[wl["kind"]]),
+            "out": out,
+            "l2": "GPU arm: each timed step reads one of several copies of the inputs "
+                  "totalling > 2x L2 (count in l2_copies)",
+            "parallelism": "replicas" if world > 1 else "1 GPU"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,15 +481,27 @@ def main():
     sets = [t] + [{k: v.clone() for k, v in t.items()} for _ in range(copies - 1)]
     stream = torch.cuda.current_stream(device)
 
+    wu0 = torch.cuda.Event(enable_timing=True)
+    wu1 = torch.cuda.Event(enable_timing=True)
+    wu0.record(stream)
     for i in range(args.warmup):
         run_once(fp8g, wl, w, sets[i % copies], C, stream)
+    wu1.record(stream)
     torch.cuda.synchronize(device)
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"GEMM status {st} detail {detail}"
+    call_ms_est = max(wu0.elapsed_time(wu1) / args.warmup, 1e-3)
 
+    # Clocks: a short timed region (the default --steps gives ~0.5 s, a
+    # 20-step run a few ms) holds few 10-ms samples, so the same calls keep
+    # running, untimed, for TAIL_MS right behind it, and the record covers the
+    # region and that tail.  Samples taken while the GPU idled before the
+    # region are left out.
+    TAIL_MS = 250.0
+    n_tail = int(min(20000, max(1, -(-TAIL_MS // call_ms_est))))
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(device)
@@ -463,11 +512,16 @@ def main():
     for i in range(args.steps):
         run_once(fp8g, wl, w, sets[i % copies], C, stream)
     ev1.record(stream)
-    torch.cuda.synchronize(device)
+    for i in range(n_tail):
+        run_once(fp8g, wl, w, sets[(args.steps + i) % copies], C, stream)
+    ev1.synchronize()
     wall = time.perf_counter() - wall0
+    torch.cuda.synchronize(device)
+    wall_end = time.perf_counter()
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
+    region_s = ev0.elapsed_time(ev1) * 1e-3
+    clocks = sampler.stop(wall0, wall0 + region_s, wall_end, tail_ms=n_tail * call_ms_est)
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"GEMM status {st} detail {detail}"
     ms = ev0.elapsed_time(ev1) / args.steps
@@ -501,7 +555,7 @@ def main():
     # i - 2's read-back of the same C buffer; step i's input copy waits for
     # step i - 2's GEMM.  Timed from the first copy in to the last copy out,
     # over the whole dependency chain.
-    e2e_ms = e2e_pipelined(fp8g, wl, w, t, C, device, args.steps)
+    e2e_ms, e2e_steps = e2e_pipelined(fp8g, wl, w, t, C, device, args.steps)
     h2d = sum(v.numel() * v.element_size() for v in t.values())
     d2h = C.numel() * C.element_size()
 
@@ -557,23 +611,15 @@ def main():
         "dtype": (FMT_NAMES[wl.get("a_fmt", 0)] + " x " + FMT_NAMES[wl.get("b_fmt", 0)]
                   + " -> f32 accumulate"),
         "data": "synthetic (seeded CPU generators, quantised on the GPU)",
-        "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"],
-                   "formats": FMT_NAMES[wl.get("a_fmt", 0)] + " x " +
-                              FMT_NAMES[wl.get("b_fmt", 0)],
-                   "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
-                              {"block": "1x32 along K, power of two",
-                               "grouped": "1x32 along K, power of two",
-                               "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
-                               "grouped_nvfp4": "1x16 along K, E4M3, fp32 for A and per "
-                                                "expert weight (NVFP4)",
-                               "tensor": "per tensor"}[wl["kind"]]),
-                   "out": w.out, "l2": f"inputs rotated over {copies} copies > 2x L2",
-                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": config_of(args.workload, wl, w.out, world),
+        "l2_copies": copies,
         "roofline": roof,
         "achieved_hbm_gbs": round(hbm_gbs, 1),
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOPS",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_ms, 4),
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "inputs": "the call's own inputs: quantised operand codes and their scales, "
+                          "in pinned host memory",
                 "overlap": "two buffers, a copy-in, a compute and a copy-out stream: step "
                            "i+1's copy in and step i-1's copy out run during step i's GEMM"},
         "gpu_launches": args.steps * launches_per_call(fp8g, wl),
@@ -618,7 +664,7 @@ def reference_arm(args, wl, world, rank):
             "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic (seeded CPU generators)",
-            "config": {"workload": args.workload, "M": wl["M"], "N": wl["N"], "K": wl["K"]},
+            "config": config_of(args.workload, wl, w.out, world),
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOPS", "cores": cb["cores"],
                              "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": round(v, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,

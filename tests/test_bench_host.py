@@ -59,3 +59,27 @@ def test_workload_table():
         assert wl.get("a_fmt", 0) in range(5) and wl.get("b_fmt", 0) in range(5), name
         assert wl["M"] > 0 and wl["N"] > 0 and wl["K"] % 32 == 0, name
     assert len(bench.FMT_NAMES) == len(bench.FMT_BYTES) == 5
+
+
+def test_clock_record_keeps_the_load_window():
+    """Samples before the timed region (GPU idle) are left out; the region's
+    own samples are counted; throttle reasons come only from the window."""
+    def row(mhz, w, slow="Not Active", cap="Not Active"):
+        return f"0, {mhz}, 2070, {w}, 0x0, {slow}, Not Active, Not Active, {cap}"
+    lines = [(0.00, row(2070, 150, slow="Active")),      # idle, before the region
+             (0.10, row(1950, 1300)), (0.11, row(1950, 1350, cap="Active")),
+             (0.20, row(1900, 1390)), (0.30, row(1890, 1395)),
+             (0.50, row(2070, 160))]                     # after the tail
+    c = bench.ClockSampler.summarize(lines, 0.05, 0.12, 0.35, tail_ms=200.0)
+    assert c["samples"] == 4 and c["samples_in_timed_region"] == 2
+    assert c["sm_mhz"] == 1925.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"] and c["power_w_max"] == 1395.0
+    assert "200-ms run" in c["window"]
+
+
+def test_both_arms_describe_the_same_workload():
+    for name, wl in bench.WORKLOADS.items():
+        a = bench.config_of(name, wl, "bf16", 1)
+        assert a == bench.config_of(name, wl, "bf16", 1) and a["workload"] == name
+        assert set(a) == {"workload", "M", "N", "K", "formats", "scales", "out", "l2",
+                          "parallelism"}
