@@ -481,24 +481,37 @@ def main():
     sets = [t] + [{k: v.clone() for k, v in t.items()} for _ in range(copies - 1)]
     stream = torch.cuda.current_stream(device)
 
-    wu0 = torch.cuda.Event(enable_timing=True)
-    wu1 = torch.cuda.Event(enable_timing=True)
-    wu0.record(stream)
     for i in range(args.warmup):
         run_once(fp8g, wl, w, sets[i % copies], C, stream)
-    wu1.record(stream)
     torch.cuda.synchronize(device)
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"GEMM status {st} detail {detail}"
-    call_ms_est = max(wu0.elapsed_time(wu1) / args.warmup, 1e-3)
+    # a few more untimed calls give the per-call time that sizes the clock tail
+    n_est = max(3, min(20, args.warmup))
+    wu0 = torch.cuda.Event(enable_timing=True)
+    wu1 = torch.cuda.Event(enable_timing=True)
+    wu0.record(stream)
+    for i in range(n_est):
+        run_once(fp8g, wl, w, sets[i % copies], C, stream)
+    wu1.record(stream)
+    torch.cuda.synchronize(device)
+    call_ms_est = max(wu0.elapsed_time(wu1) / n_est, 1e-3)
 
-    # Clocks: a short timed region (the default --steps gives ~0.5 s, a
-    # 20-step run a few ms) holds few 10-ms samples, so the same calls keep
-    # running, untimed, for TAIL_MS right behind it, and the record covers the
-    # region and that tail.  Samples taken while the GPU idled before the
-    # region are left out.
+    # GPU timeline, back to back: the timed region (K calls); the kernel-timing
+    # pass (below); a tail of the same calls, untimed, for TAIL_MS.  Clocks are
+    # sampled over all three: a short region (a 20-step run lasts a few ms)
+    # holds few samples on its own.  Samples taken while the GPU idled before
+    # the region are left out.
+    # The GEMM kernel alone (the roofline's "achieved"): the library records
+    # CUDA events on the launching stream around each call's GEMM kernel
+    # launch (after the scale packing, for block calls); a pass of its own,
+    # because the recording keeps the GEMM's prologue from overlapping the
+    # packing kernel (calls that launch only the GEMM: the timed region itself
+    # is that kernel, and events around each launch would only add launch gaps)
     TAIL_MS = 250.0
     n_tail = int(min(20000, max(1, -(-TAIL_MS // call_ms_est))))
+    kpass = launches_per_call(fp8g, wl) > 1
+    nk = max(3, min(args.steps, 300))
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
@@ -512,16 +525,25 @@ def main():
     for i in range(args.steps):
         run_once(fp8g, wl, w, sets[i % copies], C, stream)
     ev1.record(stream)
-    for i in range(n_tail):
-        run_once(fp8g, wl, w, sets[(args.steps + i) % copies], C, stream)
+    kms = []
+    if kpass:
+        fp8g.fp8g_kernel_timing_begin(nk)
+        for i in range(nk):
+            run_once(fp8g, wl, w, sets[i % copies], C, stream)
     ev1.synchronize()
     wall = time.perf_counter() - wall0
+    if kpass:
+        kms = fp8g.fp8g_kernel_timing_end(nk)   # waits for the pass (every call records)
+    for i in range(n_tail):
+        run_once(fp8g, wl, w, sets[(args.steps + i) % copies], C, stream)
     torch.cuda.synchronize(device)
     wall_end = time.perf_counter()
     if dist is not None:
         dist.barrier()
     region_s = ev0.elapsed_time(ev1) * 1e-3
     clocks = sampler.stop(wall0, wall0 + region_s, wall_end, tail_ms=n_tail * call_ms_est)
+    clocks["after_region"] = (f"{nk} kernel-timing calls, then {n_tail} calls"
+                              if kpass else f"{n_tail} calls")
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"GEMM status {st} detail {detail}"
     ms = ev0.elapsed_time(ev1) / args.steps
@@ -529,23 +551,7 @@ def main():
         tt = torch.tensor([ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-
-    # the GEMM kernel alone (the roofline's "achieved"): the library records CUDA
-    # events on the launching stream around each call's GEMM kernel launch
-    # (after the scale packing, for block calls); a separate pass, because the
-    # recording keeps the GEMM's prologue from overlapping the packing kernel
-    # (calls that launch only the GEMM: the timed region itself is that kernel,
-    # and events around each launch would only add launch gaps)
-    kms = []
-    kernel_ms = ms
-    if launches_per_call(fp8g, wl) > 1:
-        nk = max(3, min(args.steps, 300))
-        fp8g.fp8g_kernel_timing_begin(nk)
-        for i in range(nk):
-            run_once(fp8g, wl, w, sets[i % copies], C, stream)
-        torch.cuda.synchronize(device)
-        kms = fp8g.fp8g_kernel_timing_end(nk)
-        kernel_ms = float(np.mean(kms)) if kms else ms
+    kernel_ms = float(np.mean(kms)) if kms else ms
 
     # end to end through the C ABI with host buffers: every step copies its
     # inputs from pinned host memory, runs the GEMM and copies C back to pinned
@@ -580,8 +586,8 @@ def main():
                 "call_achieved": round(hbm_gbs, 1), "call_frac": round(hbm_gbs / peaks["hbm"], 4)}
     roof["traffic"] = TRAFFIC_BYTES.get(args.workload)
     roof["timed"] = (f"GEMM kernel alone: mean of {len(kms)} launches, CUDA events the library "
-                     f"records on the launching stream around the launch (a pass after the "
-                     f"timed region); call_* = the whole call (packing + GEMM kernel) over the "
+                     f"records on the launching stream around the launch (a pass right after "
+                     f"the timed region); call_* = the whole call (packing + GEMM kernel) over the "
                      f"timed region" if kms else
                      "the GEMM kernel (the call's only launch) over the timed region")
     roof["kernel_ms"] = round(kernel_ms, 5)
