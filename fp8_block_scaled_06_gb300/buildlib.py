@@ -13,7 +13,7 @@ OBJ_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8g.so")
 SOURCES = ["gemm.cu", "gemm_pair.cu", "gemm_promote.cu", "scales.cu", "quant.cu", "api.cu",
            "noalloc.cu", "selftest.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh", "quant_math.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -26,11 +26,10 @@
 // The MMA thread's commits go to both CTAs' barriers (multicast), so each
 // producer learns when a stage is free and each epilogue when its rows are
 // final.  Persistent over 256x256 tiles in the grouped raster order.  Every
-// wait is bounded; tensor memory (512 columns: two 256-column accumulators
-// per-tensor; FP8-rate block-scaled, a ring of three 128-column halves, each
-// K step being two N = 128 MMAs, plus per-stage scale factors; FP4-rate, one
-// accumulator plus scale factors; an accumulator is released as soon as it
-// is in registers) is allocated and freed by both CTAs together.
+// wait is bounded; tensor memory (512 columns: two accumulators per-tensor,
+// one accumulator plus per-stage scale factors block-scaled; an accumulator
+// is released as soon as it is in registers) is allocated and freed by both
+// CTAs together.
 //
 // F4 = 1 (E2M1 x E2M1 with 1x32 power-of-two scales, i.e. MXFP4, at the FP4
 // rate): kind::mxf4 reads dense 4-bit operands, so the packed codes are
@@ -69,11 +68,8 @@ constexpr int kB = (kPairBN / 2) * kBK;      // 16 KB: this CTA's half of B
 // tensor memory.  (Established on GB300 by the exact scale-layout test: with
 // only the CTA's own half of B's scales the results are wrong.)  Per K step
 // three 32x128b.warpx4 copies (each replicated over the four lane quarters by
-// the copy): A's 128 rows and B's two 128-row chunks, from 1.5 KB of packed
-// chunks.  FP8-rate kernels issue two N = 128 MMAs per K step, each reading
-// 64 rows of B from each CTA, so their B chunks are packed by half MMA (rows
-// 0-63 and 128-191 of the tile, then 64-127 and 192-255); the FP4-rate
-// kernels read rows 0-127, then 128-255.  Issued by their own warp the copies overlap the MMAs, so three
+// the copy): A's 128 rows, B's rows 0-127 and 128-255, from 1.5 KB of packed
+// chunks.  Issued by their own warp the copies overlap the MMAs, so three
 // small copies beat one 128x256b copy from a pre-replicated 4 KB source
 // (which saved copy instructions when the MMA thread issued them).
 constexpr int kSfaBytes = 512;
@@ -92,18 +88,9 @@ struct PairCfg {
     static constexpr int OFF_SF = OFF_B + STAGES * kB;
     static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK;
     // Accumulators: per-tensor double-buffers the 256-column accumulator (the
-    // next tile's MMAs never wait for the epilogue).  FP8-rate block modes
-    // (HALF) issue each K step as two N = 128 MMAs into two 128-column halves
-    // taken from a ring of three (384 columns; the scale factors of 6 stages
-    // take 96 more): a tile's first half goes to the slot no earlier tile
-    // still holds, so the next tile starts while the epilogue drains this one
-    // (one 256-column accumulator made the first MMA of every tile wait for
-    // the whole drain, ~5% of a K = 4096 tile).  FP4-rate block modes keep one
-    // 256-column accumulator: their scale columns leave no room for more.
-    static constexpr bool HALF = kBlock && F4 == 0;
-    static constexpr int NUM_ACC = HALF ? 3 : kBlock ? 1 : 2;
-    static constexpr int ACC_COLS = HALF ? kPairBN / 2 : kPairBN;  // columns per accumulator slot
-    static constexpr int SF_BASE = NUM_ACC * ACC_COLS;               // first scale-factor column
+    // next tile's MMAs never wait for the epilogue); block modes keep one and
+    // use the other columns for the scale factors of each stage.
+    static constexpr int NUM_ACC = kBlock ? 1 : 2;
     // Scale-copy issuers: one warp, two for NVFP4 (12 copies per stage are
     // more than one thread issues in a stage's time; measured 8192^3: 3955 ->
     // 5610 TFLOPS without them)
@@ -123,36 +110,10 @@ struct PairCfg {
     static constexpr int SF_COLS = kBlock ? G * SFG : 0;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
-    static_assert(SF_BASE + STAGES * SF_COLS <= (int)TMEM_COLS, "tensor memory over budget");
+    static_assert(256 + STAGES * SF_COLS <= (int)TMEM_COLS || !kBlock, "tensor memory over budget");
     static_assert(OFF_SF % 128 == 0 && CHUNK % 128 == 0, "TMA destination alignment");
 };
 constexpr int kCW = kPairBN / 4;  // columns per epilogue warp
-
-// HALF accumulators: K steps of a tile issued for its first half alone, ahead
-// of the wait for the second half's slot (the previous tile's first half).
-// Those MMAs queue behind the previous tile's, so the tensor pipe keeps
-// working while that tile's epilogue drains the slot; the stages stay held
-// until the second half's MMAs of the same steps follow.
-#ifndef FP8G_PAIR_LEAD_KB
-#define FP8G_PAIR_LEAD_KB 3
-#endif
-constexpr int kLeadKb = FP8G_PAIR_LEAD_KB;
-static_assert(kLeadKb >= 1 && kLeadKb <= 5, "lead K steps must leave the ring a free stage");
-
-// One half MMA set of a stage (HALF accumulators): four K = 32
-// kind::mxf8f6f4 MMAs, M = 256, N = 128, into accumulator slot d.  Half h
-// reads rows 64 h .. 64 h + 63 of each CTA's 128 rows of B (columns 64 h +
-// [0, 64) and 128 + 64 h + [0, 64) of the 256-wide tile) and the scale
-// columns of its packed chunk (B's chunk 2 pn + h holds exactly those rows).
-__device__ __forceinline__ void mma_half(uint32_t d, uint32_t a0, uint32_t b0, int h, uint32_t sf,
-                                         uint32_t ab_fmt, int kb) {
-#pragma unroll
-    for (int k = 0; k < kBK / 32; ++k)
-        ptx::mma_mxf8_pair(d, ptx::desc_kmajor_sw128(a0 + k * 32),
-                           ptx::desc_kmajor_sw128(b0 + h * (kB / 2) + k * 32),
-                           ptx::idesc_mxf8(2 * kBM, kPairBN / 2, (uint32_t)k) | ab_fmt, sf,
-                           sf + 8 + 4 * h, (kb | k) != 0 ? 1u : 0u);
-}
 
 
 // Bounded wait with cluster-scope acquire (barriers remote CTAs arrive on).
@@ -363,64 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (run && warp == 1 && leader) {
         // ===== MMA issuer (even CTA): 256 x 256 x 32 per instruction =====
-        if (lane == 0 && PC::HALF) {
-            // Tile lt's halves use slots x % 3 for x = 2 lt, 2 lt + 1 (the
-            // x / 3-th use of the slot): the first half's slot last held tile
-            // lt - 2's second half, the second half's slot tile lt - 1's
-            // first half, which the epilogue drains first.
-            uint32_t stage = 0, phase = 0;
-            int32_t lt = 0;
-            for (int32_t t = t_first; t < T; t += t_step, ++lt) {
-                const int32_t x0 = 2 * lt;
-                const int s0 = x0 % 3, s1 = (x0 + 1) % 3;
-                const uint32_t u0 = (uint32_t)((x0 / 3) & 1), u1 = (uint32_t)(((x0 + 1) / 3) & 1);
-                const uint32_t d0 = tmem_base + s0 * PC::ACC_COLS;
-                const uint32_t d1 = tmem_base + s1 * PC::ACC_COLS;
-                if (!wait_bar_cluster(bar_acce(s0), u0 ^ 1u, abort_flag, p, 1 * 256 + 64 + s0))
-                    goto roles_done;
-                ptx::tc_fence_after();
-                const int lead = p.num_kb < kLeadKb ? p.num_kb : kLeadKb;
-                const uint32_t stage0 = stage;
-                for (int kb = 0; kb < lead; ++kb) {
-                    if (!wait_bar(bar_sfr(stage), phase, abort_flag, p, 1 * 256 + stage))
-                        goto roles_done;
-                    ptx::tc_fence_after();
-                    mma_half(d0, sbase + PC::OFF_A + stage * kA, sbase + PC::OFF_B + stage * kB, 0,
-                             tmem_base + PC::SF_BASE + stage * PC::SF_COLS, p.ab_fmt, kb);
-                    if (++stage == PC::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!wait_bar_cluster(bar_acce(s1), u1 ^ 1u, abort_flag, p, 1 * 256 + 64 + s1))
-                    goto roles_done;
-                ptx::tc_fence_after();
-                uint32_t st = stage0;
-                for (int kb = 0; kb < lead; ++kb) {
-                    mma_half(d1, sbase + PC::OFF_A + st * kA, sbase + PC::OFF_B + st * kB, 1,
-                             tmem_base + PC::SF_BASE + st * PC::SF_COLS, p.ab_fmt, kb);
-                    ptx::tc_commit_pair_mc(bar_empty(st), 0x3);
-                    if (++st == (uint32_t)PC::STAGES) st = 0;
-                }
-                for (int kb = lead; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(bar_sfr(stage), phase, abort_flag, p, 1 * 256 + stage))
-                        goto roles_done;
-                    ptx::tc_fence_after();
-                    const uint32_t a0 = sbase + PC::OFF_A + stage * kA;
-                    const uint32_t b0 = sbase + PC::OFF_B + stage * kB;
-                    const uint32_t sf = tmem_base + PC::SF_BASE + stage * PC::SF_COLS;
-                    mma_half(d0, a0, b0, 0, sf, p.ab_fmt, kb);
-                    mma_half(d1, a0, b0, 1, sf, p.ab_fmt, kb);
-                    ptx::tc_commit_pair_mc(bar_empty(stage), 0x3);
-                    if (++stage == PC::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                ptx::tc_commit_pair_mc(bar_accf(s0), 0x3);
-                ptx::tc_commit_pair_mc(bar_accf(s1), 0x3);
-            }
-        } else if (lane == 0) {
+        if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             int32_t lt = 0;
             const uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN) | p.ab_fmt;
@@ -443,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (F4 == 2) {
                         // MMA k: K elements 64k .. 64k + 63 = K group k's four
                         // 16-wide scale blocks (the whole word, sf_id 0)
-                        const uint32_t sf = tmem_base + PC::SF_BASE + stage * PC::SF_COLS;
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k) {
                             const uint32_t sfk = sf + PC::SFG * k;
@@ -455,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else if constexpr (F4 == 1) {
                         // MMA k: K elements 64k .. 64k + 63 = scale blocks 2k, 2k + 1,
                         // in K group k / 2 (columns + 16 (k / 2)), bytes 2 (k % 2), + 1
-                        const uint32_t sf = tmem_base + PC::SF_BASE + stage * PC::SF_COLS;
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k) {
                             const uint32_t sfk = sf + 16 * (k >> 1);
@@ -465,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                sfk, sfk + 8, (kb | k) != 0 ? 1u : 0u);
                         }
                     } else if constexpr (PC::kBlock) {
-                        const uint32_t sf = tmem_base + PC::SF_BASE + stage * PC::SF_COLS;
+                        const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
                             ptx::mma_mxf8_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
@@ -502,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(bar_full(stage), phase, abort_flag, p, 2 * 256 + stage))
                         goto roles_done;
                     ptx::tc_fence_after();
-                    const uint32_t sf = tmem_base + PC::SF_BASE + stage * PC::SF_COLS;
+                    const uint32_t sf = tmem_base + 256 + stage * PC::SF_COLS;
                     const uint32_t cs = sbase + PC::OFF_SF + stage * PC::CHUNK;
                     constexpr int G = PC::G;
                     constexpr int GW = G / PC::SF_WARPS;  // groups per issuing warp
@@ -541,54 +445,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const PairTile ti = pair_tile<MODE>(t, p, row_off, tile_off, rt_off);
+            const int acc = lt % PC::NUM_ACC;
+            const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
+            if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc, 128)) break;
+            ptx::tc_fence_after();
             uint32_t r[kCW / 32][32];
-            int64_t ncol[kCW / 32];  // first column of C of each 32-column group
-            const uint32_t lane_q = (uint32_t)(q * 32) << 16;
-            if constexpr (PC::HALF) {
-                // slot x % 3 of half-accumulator use x = 2 lt + h: 32 columns of
-                // each half per warp.  Half h's slot column c holds tile column
-                // 64 h + c (c < 64, the even CTA's B rows) or 128 + 64 h + c - 64.
-                // The first half's slot is released first: the next tile's
-                // second half waits for it.
-                const int cg = ew >> 2;
-                bool ok = true;
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(q * 32) << 16) + acc * kPairBN + col0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int32_t x = 2 * lt + h;
-                    const int sl = x % 3;
-                    if (!wait_bar_warp(bar_accf(sl), (uint32_t)((x / 3) & 1), abort_flag, p,
-                                       3 * 256 + sl, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    ptx::tmem_ld_32x32b_x32(tmem_base + lane_q + sl * PC::ACC_COLS + cg * 32, r[h]);
-                    ptx::tmem_ld_wait();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_shared(bar_acce(sl), 0));
-                    ncol[h] = (int64_t)ti.pn * kPairBN + (cg < 2 ? 0 : kPairBN / 2) + 64 * h +
-                              32 * (cg & 1);
-                }
-                if (!ok) break;
-            } else {
-                const int acc = lt % PC::NUM_ACC;
-                const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
-                if (!wait_bar_warp(bar_accf(acc), acc_par, abort_flag, p, 3 * 256 + acc, 128)) break;
-                ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + lane_q + acc * PC::ACC_COLS + col0;
-#pragma unroll
-                for (int c = 0; c < kCW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-                ptx::tmem_ld_wait();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_shared(bar_acce(acc), 0));
-#pragma unroll
-                for (int c = 0; c < kCW / 32; ++c) ncol[c] = (int64_t)ti.pn * kPairBN + col0 + 32 * c;
-            }
+            for (int c = 0; c < kCW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_shared(bar_acce(acc), 0));
 
             const int64_t arow = (int64_t)ti.row0 + rank * kBM + q * 32 + lane;  // routed row
             const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;       // row of C
+            const int64_t ncol0 = (int64_t)ti.pn * kPairBN + col0;
             // NVFP4 grouped: each expert's B carries its own tensor scale
             float alpha_e = alpha;
             if constexpr (F4 == 2 && MODE == kModeGrouped) alpha_e = __fmul_rn(p.ga[0], p.gb[ti.e]);
@@ -597,18 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // every lane (rows past the output too: they are not stored)
                 const float *brow = p.bias != nullptr ? p.bias + (int64_t)ti.e * p.N : nullptr;
 #pragma unroll
-                for (int c = 0; c < kCW / 32; ++c) epi32(r[c], alpha_e, brow, p.act, ncol[c], p.N);
+                for (int c = 0; c < kCW / 32; ++c)
+                    epi32(r[c], alpha_e, brow, p.act, ncol0 + c * 32, p.N);
                 a_t = 1.0f;
             }
             // FP4-rate tiles end twice as often: their stores go out as whole
             // 128-byte row segments (measured 8192^3: +1.8%; on the FP8-rate
             // tiles the shuffles cost more than the coalescing saves, -0.5%)
             if (F4 != 0 && p.st32) {
-                store_rows64<OUT_F32>(p.C, row, p.N, ncol[0], r, a_t, lane);  // whole warp
+                store_rows64<OUT_F32>(p.C, row, p.N, ncol0, r, a_t, lane);  // whole warp
             } else if (row >= 0) {
 #pragma unroll
                 for (int c = 0; c < kCW / 32; ++c)
-                    store_row32<OUT_F32>(p.C, row, p.N, ncol[c], r[c], a_t, p.st32 != 0);
+                    store_row32<OUT_F32>(p.C, row, p.N, ncol0 + c * 32, r[c], a_t, p.st32 != 0);
             }
         }
     }

@@ -126,11 +126,7 @@ struct PackArgs {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;
-    // B of single-CTA 256-wide tiles (1): 4 KB per (z, kg, 256-row tile),
-    // replicated for tcgen05.cp 128x256b; B of the FP8-rate block-scaled CTA
-    // pairs (2): chunk 2 pn + h holds rows 64 h + [0, 64) and 128 + 64 h +
-    // [0, 64) of 256-row tile pn (the rows of one N = 128 half MMA); else 0
-    int32_t rep;
+    int32_t rep;  // B of single-CTA 256-wide tiles: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
 };
 // NVFP4: E4M3 scale codes [rows, K/16] -> the same 512-byte chunks, a K group
 // being 64 wide (4 blocks of 16, one MMA's word), the four groups of a

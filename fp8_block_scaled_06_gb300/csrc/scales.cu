@@ -17,12 +17,6 @@
 // Grouped A: row tiles are expert-local (an expert's rows start a new tile),
 // numbered in expert order, like the GEMM's tile list.
 //
-// B of the FP8-rate block-scaled CTA-pair kernels (rep == 2): those kernels
-// issue each K step as two N = 128 MMAs, each reading 64 rows of B from each
-// CTA of the pair, so the two chunks of a 256-row tile pn hold the rows of
-// one such MMA each: chunk 2 pn + h = rows 64 h + [0, 64) then
-// 128 + 64 h + [0, 64) of the tile (chunk row r is the MMA's row r).
-//
 // HBM-bound: one launch packs both operands.  A block takes one 128-row tile
 // and 8 K groups: it reads the tile's 128-byte row segments coalesced (8
 // threads per row, 16 bytes each, all loads issued before any is used),
@@ -46,8 +40,7 @@ struct PackJob {
     int32_t n_rt, nz;
     uint8_t *dst;
     const int32_t *counts;  // grouped A: expert-local row tiles
-    int32_t rep;            // 1: replicated 256-row layout (B of single-CTA 256-wide
-                            // tiles); 2: chunks by N = 128 half MMA (B of CTA pairs)
+    int32_t rep;            // replicated 256-row layout (B of 256-wide tiles)
 };
 
 // blockIdx.z < a.nz packs operand a (z = blockIdx.z), the rest operand b.
@@ -98,16 +91,11 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
     const int64_t k0 = (int64_t)kg * 4;
     const bool vec = (sfc % 4) == 0;
     const float *zsrc = j.src + (int64_t)z * j.z_rows * sfc;
-    // operand row of chunk row r (rep == 2: the N = 128 half MMA's rows)
-    const int64_t half0 = (int64_t)(rt >> 1) * 2 * kBM + (kBM / 2) * (rt & 1);
-    auto src_row = [&](int r) -> int64_t {
-        return j.rep == 2 ? half0 + (r < kBM / 2 ? r : kBM / 2 + r) : base + r;
-    };
     // all loads first (independent): rows threadIdx.x / 8 + 16 p
     uint32_t v[kBM / kRowsPerPass][4];
 #pragma unroll
     for (int pss = 0; pss < kBM / kRowsPerPass; ++pss) {
-        const int64_t row = src_row(pss * kRowsPerPass + threadIdx.x / kKgPerBlock);
+        const int64_t row = base + pss * kRowsPerPass + threadIdx.x / kKgPerBlock;
         const bool in = row < limit && kg < n_kg;
         const float *srow = zsrc + (in ? row : 0) * sfc;
         if (vec) {
@@ -128,7 +116,7 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
     for (int pss = 0; pss < kBM / kRowsPerPass; ++pss) {
         const int r = pss * kRowsPerPass + threadIdx.x / kKgPerBlock;
         uint32_t word = 0x7F7F7F7Fu;  // rows past the operand: scale 1
-        if (src_row(r) < limit) {
+        if (base + r < limit) {
             word = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -142,9 +130,9 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
     // 16-byte output groups: the words of rows d, 32 + d, 64 + d, 96 + d of one
     // K group (byte 16 d + 4 w of a chunk is row 32 w + d)
     // per z: n_kg x n_rt chunks of 512 B, or (replicated) n_kg x n_rt / 2 blocks of 4 KB
-    uint8_t *zdst = j.dst + (int64_t)z * n_kg * j.n_rt * (j.rep == 1 ? 2048 : 512);
+    uint8_t *zdst = j.dst + (int64_t)z * n_kg * j.n_rt * (j.rep ? 2048 : 512);
     const int nk = n_kg - kg0 < kKgPerBlock ? n_kg - kg0 : kKgPerBlock;
-    if (j.rep == 1) {
+    if (j.rep) {
         // 4 KB per (z, K group, 256-row tile): the 128-lane x 32-byte source of
         // one tcgen05.cp 128x256b; lane L = 32 q + d holds rows 32 w + d of
         // both 128-row halves h (bytes 128 h + 4 w of its 32), identical for
