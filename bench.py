@@ -54,6 +54,19 @@ WORKLOADS = {
     "nvfp4_8192": dict(kind="nvfp4", M=8192, N=8192, K=8192, seed=3, a_fmt=2, b_fmt=2),
     # the MoE workload in NVFP4 (each expert's weight with its own tensor scale)
     "moe_nvfp4": dict(kind="grouped_nvfp4", M=32768, N=14336, K=4096, seed=4, a_fmt=2, b_fmt=2),
+    # MoE from bf16 token activations, the routed rows' 1x32 E4M3 quantisation
+    # inside the timed step: fp8_grouped_gemm_quant (one call) against
+    # fp8g_quantize_rows + fp8_grouped_gemm (two calls).  At the full MoE size
+    # the call runs the two steps itself (256-row tiles); with 128 tokens
+    # (decoding: 256 routed rows) it fuses the quantiser into the GEMM.
+    "moe_bf16": dict(kind="grouped_quant", M=32768, N=14336, K=4096, seed=4, tokens=16384,
+                     fused=True),
+    "moe_bf16_2call": dict(kind="grouped_quant", M=32768, N=14336, K=4096, seed=4,
+                           tokens=16384, fused=False),
+    "decode_bf16": dict(kind="grouped_quant", M=256, N=14336, K=4096, seed=4, tokens=128,
+                        fused=True),
+    "decode_bf16_2call": dict(kind="grouped_quant", M=256, N=14336, K=4096, seed=4, tokens=128,
+                              fused=False),
 }
 FMT_NAMES = ["e4m3", "e5m2", "e2m1", "e2m3", "e3m2"]
 # bytes per element of each format in memory (E2M1: two codes per byte; FP6:
@@ -168,6 +181,17 @@ def make_inputs(wl: dict, device):
         sb = sb.reshape(E, N, K // 32)
         counts = torch.from_numpy(w.counts).to(device)
         return w, dict(qa=qa, sa=sa, qb=qb, sb=sb, counts=counts)
+    if wl["kind"] == "grouped_quant":
+        X, idx, w = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])
+        E, N, K = w.B.shape
+        qb, sb = fp8g.quantize(w.B.reshape(E * N, K).to(device), 32)
+        rows = int(w.counts.sum())
+        # tmp_*: the two-call path's quantised rows (outputs of its first call)
+        return w, dict(X=X.to(torch.bfloat16).to(device), idx=idx.to(device),
+                       qb=qb.reshape(E, N, K), sb=sb.reshape(E, N, K // 32),
+                       counts=torch.from_numpy(w.counts).to(device),
+                       tmp_qa=torch.empty((rows, K), dtype=torch.uint8, device=device),
+                       tmp_sa=torch.empty((rows, K // 32), dtype=torch.float32, device=device))
     if wl["kind"] == "grouped_nvfp4":
         w = synth.moe_grouped(seed=wl["seed"])
         qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
@@ -205,6 +229,10 @@ def algorithmic_bytes(wl: dict, w) -> int:
         E = w.B.shape[0]
         return int(M * K * ea + E * N * K * eb + 4 * (M * K // 32 + E * N * K // 32) +
                    M * N * out_b + 4 * E)
+    if wl["kind"] == "grouped_quant":   # bf16 routed rows read once; int32 routing index
+        E = w.B.shape[0]
+        return int(M * K * 2 + 4 * M + E * N * K * eb + 4 * E * N * K // 32 +
+                   M * N * out_b + 4 * E)
     if wl["kind"] == "grouped_nvfp4":   # E4M3 scale bytes per 16; fp32 gA and E gB
         E = w.B.shape[0]
         return int(M * K * ea + E * N * K * eb + (M + E * N) * K // 16 + 4 * (1 + E) +
@@ -217,7 +245,20 @@ def algorithmic_bytes(wl: dict, w) -> int:
 
 def run_once(fp8g, wl, w, t, C, stream):
     out = fp8g.FP8G_OUT_F32 if w.out == "f32" else fp8g.FP8G_OUT_BF16
-    if wl["kind"] == "grouped":
+    if wl["kind"] == "grouped_quant":
+        E, N, K = t["qb"].shape
+        rows = t["tmp_qa"].shape[0]
+        if wl["fused"]:
+            fp8g.fp8_grouped_gemm_quant(t["X"], fp8g.FP8G_IN_BF16, t["X"].shape[0], t["idx"],
+                                        t["qb"], t["sb"], C, out, fp8g.FP8G_E4M3, None,
+                                        fp8g.FP8G_ACT_NONE, t["counts"], E, N, K, rows,
+                                        stream=stream)
+        else:
+            fp8g.fp8g_quantize_rows(t["X"], fp8g.FP8G_IN_BF16, t["X"].shape[0], K, t["idx"], rows,
+                                    32, fp8g.FP8G_E4M3, t["tmp_qa"], t["tmp_sa"], stream)
+            fp8g.fp8_grouped_gemm(t["tmp_qa"], t["qb"], t["tmp_sa"], t["sb"], C, out,
+                                  t["counts"], E, N, K, rows, None, None, stream)
+    elif wl["kind"] == "grouped":
         E, N, K = t["qb"].shape
         fp8g.fp8_grouped_gemm(t["qa"], t["qb"], t["sa"], t["sb"], C, out, t["counts"], E, N, K,
                               t["qa"].shape[0], None, None, stream)
@@ -276,6 +317,10 @@ def launches_per_call(fp8g, wl) -> int:
         return 1
     if wl["kind"] in ("grouped", "nvfp4", "grouped_nvfp4"):
         return 2
+    if wl["kind"] == "grouped_quant":
+        # quantiser (unless fused into the GEMM), B's scale packing, GEMM
+        fused = wl["fused"] and fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128
+        return 2 if fused else 3
     if wl.get("literal"):
         return 1
     return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
@@ -287,7 +332,7 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
     many streams per direction (measured on GB300: 4 lanes were slower, 1086
     against 1197 TFLOPS on the 8192^3 workload; the host link, not one copy
     engine, is the limit)."""
-    host = {k: v.cpu().pin_memory() for k, v in t.items()}
+    host = {k: v.cpu().pin_memory() for k, v in t.items() if not k.startswith("tmp_")}
     nbuf = 2
     dev_in = [{k: torch.empty_like(v) for k, v in t.items()} for _ in range(nbuf)]
     dev_C = [C] + [torch.empty_like(C) for _ in range(nbuf - 1)]
@@ -310,7 +355,7 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
 
     def step(i):
         b = i % nbuf
-        pieces = [p for k in dev_in[b] for p in chunks(dev_in[b][k], host[k])]
+        pieces = [p for k in host for p in chunks(dev_in[b][k], host[k])]
         for j, s_ in enumerate(s_in):
             with torch.cuda.stream(s_):
                 if not first[b]:
@@ -356,7 +401,12 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
 def oracle_inputs(wl, w):
     """The oracle's own quantisation of the workload (done once, untimed)."""
     import oracle
-    if wl["kind"] == "grouped":
+    if wl["kind"] == "grouped_quant":   # the bf16 tokens, gathered
+        import synth
+        X, idx, _ = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])
+        w = synth.Workload(w.name, w.M, w.N, w.K, True, w.out,
+                           X.to(torch.bfloat16).float()[idx.long()], w.B, w.counts)
+    if wl["kind"] in ("grouped", "grouped_quant"):
         E, N, K = w.B.shape
         qa, sa = oracle.quantize_block32(w.A.numpy())
         qb, sb = oracle.quantize_block32(w.B.reshape(E * N, K).numpy())
@@ -429,6 +479,10 @@ def config_of(name: str, wl: dict, out: str, world: int) -> dict:
             "scales": ("1x32 along K, literal fp32 amax/448" if wl.get("literal") else
                        {"block": "1x32 along K, power of two",
                         "grouped": "1x32 along K, power of two",
+                        "grouped_quant": "1x32 along K, power of two; A quantised from bf16 "
+                                         "tokens inside the step" + (
+                                             " (one call)" if wl.get("fused") else
+                                             " (two calls)"),
                         "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
                         "grouped_nvfp4": "1x16 along K, E4M3, fp32 for A and per "
                                          "expert weight (NVFP4)",
@@ -468,7 +522,7 @@ def main():
     w, t = make_inputs(wl, device)
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"quantiser status {st}"
-    rows = t["qa"].shape[0]
+    rows = (t["qa"] if "qa" in t else t["tmp_qa"]).shape[0]
     out_dt = torch.float32 if w.out == "f32" else torch.bfloat16
     C = torch.empty((rows, wl["N"]), dtype=out_dt, device=device)
     flops = w.flops
@@ -476,7 +530,8 @@ def main():
 
     # rotate over input copies whose total exceeds 2x L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    in_bytes = sum(v.numel() * v.element_size() for k, v in t.items() if k != "counts")
+    in_bytes = sum(v.numel() * v.element_size() for k, v in t.items()
+                   if k != "counts" and not k.startswith("tmp_"))
     copies = max(1, min(8, -(-2 * l2 // max(in_bytes, 1))))
     sets = [t] + [{k: v.clone() for k, v in t.items()} for _ in range(copies - 1)]
     stream = torch.cuda.current_stream(device)
@@ -562,7 +617,7 @@ def main():
     # step i - 2's GEMM.  Timed from the first copy in to the last copy out,
     # over the whole dependency chain.
     e2e_ms, e2e_steps = e2e_pipelined(fp8g, wl, w, t, C, device, args.steps)
-    h2d = sum(v.numel() * v.element_size() for v in t.values())
+    h2d = sum(v.numel() * v.element_size() for k, v in t.items() if not k.startswith("tmp_"))
     d2h = C.numel() * C.element_size()
 
     peaks = _peaks()
@@ -646,7 +701,9 @@ def reference_arm(args, wl, world, rank):
     if rank != 0:
         return
     import synth
-    if wl["kind"] in ("grouped", "grouped_nvfp4"):
+    if wl["kind"] == "grouped_quant":
+        w = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])[2]
+    elif wl["kind"] in ("grouped", "grouped_nvfp4"):
         w = synth.moe_grouped(seed=wl["seed"])
     elif wl["kind"] == "tensor":
         w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")

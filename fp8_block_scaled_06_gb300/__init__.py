@@ -47,7 +47,8 @@ EXPORTS = (
     "fp8_gemm", "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_grouped_gemm", "fp8g_grouped_plan",
     "fp8g_gemm_plan", "fp8g_quantize_e4m3", "fp8g_quantize", "fp8_gemm_fmt",
     "fp8_gemm_blockscaled_fmt", "fp8_grouped_gemm_fmt", "fp8_gemm_ex", "fp8_gemm_blockscaled_ex",
-    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8g_quantize_rows",
+    "fp8_grouped_gemm_ex", "fp8_grouped_gemm_scatter", "fp8_grouped_gemm_quant",
+    "fp8g_quantize_rows",
     "fp8_gemm_blockscaled_promote", "fp8g_quantize_nvfp4", "fp8_gemm_nvfp4",
     "fp8_grouped_gemm_nvfp4", "fp8g_wait_selftest",
     "fp8g_kernel_timing_begin", "fp8g_kernel_timing_end",
@@ -127,6 +128,9 @@ def load():
         lib.fp8_grouped_gemm_scatter.restype = st
         lib.fp8_grouped_gemm_scatter.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32, P,
                                                  i32, i64, i64, i64, P, i64, P, P, P]
+        lib.fp8_grouped_gemm_quant.restype = st
+        lib.fp8_grouped_gemm_quant.argtypes = [P, i32, i64, P, P, P, P, ctypes.c_int, i32, P, i32,
+                                               P, i32, i64, i64, i64, P, i64, P, P, P, P, P]
         lib.fp8_gemm_blockscaled_promote.restype = st
         lib.fp8_gemm_blockscaled_promote.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32,
                                                      i64, i64, i64, P]
@@ -285,6 +289,21 @@ def fp8_grouped_gemm_scatter(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int
                                            _ptr(counts), E, N, K, total_rows, _ptr(c_row_of),
                                            c_rows, _ptr(offsets_out), _ptr(tile_map_out),
                                            _stream(stream)), "fp8_grouped_gemm_scatter")
+
+
+def fp8_grouped_gemm_quant(X, x_dtype: int, x_rows: int, rows, B, sfb, C, out: int, b_fmt: int,
+                           bias, act: int, counts, E: int, N: int, K: int, total_rows: int,
+                           c_row_of=None, c_rows: int = 0, qa_out=None, sfa_out=None,
+                           offsets_out=None, tile_map_out=None, stream=None):
+    """Grouped GEMM from fp32 / bf16 activations: gather, 1x32 E4M3 quantisation
+    (inside the GEMM kernel when the plan runs single-CTA tiles) and the
+    grouped GEMM with bias / activation and row scatter."""
+    _check(load().fp8_grouped_gemm_quant(_ptr(X), int(x_dtype), x_rows, _ptr(rows), _ptr(B),
+                                         _ptr(sfb), _ptr(C), int(out), int(b_fmt), _ptr(bias),
+                                         int(act), _ptr(counts), int(E), N, K, total_rows,
+                                         _ptr(c_row_of), c_rows, _ptr(qa_out), _ptr(sfa_out),
+                                         _ptr(offsets_out), _ptr(tile_map_out),
+                                         _stream(stream)), "fp8_grouped_gemm_quant")
 
 
 def fp8_gemm_blockscaled_promote(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int, bias,

@@ -252,6 +252,36 @@ fp8g_status check_common(const void *A, const void *B, const void *C, int out, i
     return FP8G_OK;
 }
 
+// Argument rules of the grouped GEMM (fp8_grouped_gemm_scatter and the
+// entry points built on it), checked on the host before any launch.
+fp8g_status check_grouped_args(const void *A, const void *B, const float *sfa, const float *sfb,
+                                const void *C, int out, const int32_t *counts, int32_t E,
+                                int64_t N, int64_t K, int64_t total_rows,
+                                const int32_t *c_row_of, int64_t c_rows,
+                                const int32_t *offsets_out, const int32_t *tile_map_out) {
+    if (c_row_of != nullptr && (!aligned(c_row_of, 4) || c_rows < 1)) return FP8G_ERR_INVALID_ARG;
+    if (c_row_of != nullptr && c_rows >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
+    if (E < 1) return FP8G_ERR_INVALID_ARG;
+    if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (total_rows < 0) return FP8G_ERR_INVALID_ARG;
+    if (total_rows > 0) {
+        fp8g_status st = check_common(A, B, C, out, total_rows, N, K);
+        if (st != FP8G_OK) return st;
+    } else {
+        if (B == nullptr) return FP8G_ERR_INVALID_ARG;
+        if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
+        if (N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
+        if (!aligned(B, 16) || K % 16 != 0) return FP8G_ERR_ALIGNMENT;
+    }
+    if (N >= kMaxDim || (int64_t)E * N >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(counts, 4)) return FP8G_ERR_ALIGNMENT;
+    if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
+    if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
+    return FP8G_OK;
+}
+
 }  // namespace
 
 // Kernel timing (fp8g_kernel_timing_begin / _end): events of the library
@@ -283,7 +313,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes, int a_fmt, int b_fmt,
-                     const float *bias, int act, const int32_t *c_row_of, int64_t c_rows) {
+                     const float *bias, int act, const int32_t *c_row_of, int64_t c_rows,
+                     const FusedQuant *fq) {
     if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt))
         return FP8G_ERR_INVALID_ARG;
     if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
@@ -329,12 +360,24 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.c_row_of = c_row_of;
     p.c_rows = c_rows;
     p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
+    if (fq != nullptr) {
+        // the kernel quantises A itself (single CTAs only)
+        if (mode != kModeGrouped || kc.pair || kc.split > 1 || f4) return FP8G_ERR_INVALID_ARG;
+        p.xq = fq->x;
+        p.xq_bf16 = fq->bf16;
+        p.xq_rows = fq->rows;
+        p.xq_src_rows = fq->src_rows;
+        p.qa_out = fq->qa_out;
+        p.sfa_out = fq->sfa_out;
+    }
 
     GemmMaps maps;
-    // grouped with zero rows: A is never read (a one-row map over B stands in)
-    const int64_t rows_a = M > 0 ? M : 1;
-    const void *a_ptr = M > 0 ? A : B;
-    const int a_map_fmt = M > 0 ? a_fmt : b_fmt;
+    // grouped with zero rows, or A quantised in the kernel: A is never read
+    // (a one-row map over B stands in)
+    const bool a_read = M > 0 && fq == nullptr;
+    const int64_t rows_a = a_read ? M : 1;
+    const void *a_ptr = a_read ? A : B;
+    const int a_map_fmt = a_read ? a_fmt : b_fmt;
     // operand maps count elements; the FP4-rate kernel views its packed
     // operands as dense bytes (K / 2 per row, 128 bytes = 256 codes per box row)
     const uint64_t kdim = f4 ? (uint64_t)(K / 2) : (uint64_t)K;
@@ -376,7 +419,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     p.n_rtA = (int32_t)(mode == kModeGrouped ? M / kBM + E : (M + kBM - 1) / kBM);
     p.n_rtB = (int32_t)(((N + kc.BN - 1) / kc.BN) * (kc.BN / kBM));
     if (p.n_rtA > 65535 || p.n_rtB > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    const size_t bytesA = packed_scale_bytes(num_kg, p.n_rtA, 1);
+    // (the fused quantiser writes A's chunks into each stage itself)
+    const size_t bytesA = fq != nullptr ? 0 : packed_scale_bytes(num_kg, p.n_rtA, 1);
     // single-CTA 256-wide tiles take B's scales replicated for one 128x256b
     // tensor-memory copy (4 KB per 256 rows and K step instead of 1 KB); CTA
     // pairs take plain 512-byte chunks (three warpx4 copies per K step)
@@ -395,7 +439,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     }
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
-    PackArgs pa{sa, M, 0, p.n_rtA, M > 0 ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
+    PackArgs pa{sa, M, 0, p.n_rtA, a_read ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
     PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, repB ? 1 : 0};
     cudaError_t e = launch_pack_scales(pa, pb, p.sfc, num_kg, E, di.status, stream);
     p.sfa_pk = pkA;
@@ -756,30 +800,78 @@ fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, const float *
                                      int64_t total_rows, const int32_t *c_row_of, int64_t c_rows,
                                      int32_t *offsets_out, int32_t *tile_map_out,
                                      cudaStream_t stream) {
-    if (c_row_of != nullptr && (!aligned(c_row_of, 4) || c_rows < 1)) return FP8G_ERR_INVALID_ARG;
-    if (c_row_of != nullptr && c_rows >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (counts == nullptr || sfa == nullptr || sfb == nullptr) return FP8G_ERR_INVALID_ARG;
-    if (E < 1) return FP8G_ERR_INVALID_ARG;
-    if (E > FP8G_MAX_EXPERTS) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (total_rows < 0) return FP8G_ERR_INVALID_ARG;
-    if (total_rows > 0) {
-        fp8g_status st = check_common(A, B, C, out, total_rows, N, K);
-        if (st != FP8G_OK) return st;
-    } else {
-        if (B == nullptr) return FP8G_ERR_INVALID_ARG;
-        if (out != FP8G_OUT_BF16 && out != FP8G_OUT_F32) return FP8G_ERR_INVALID_ARG;
-        if (N < 1 || K < 1) return FP8G_ERR_INVALID_ARG;
-        if (!aligned(B, 16) || K % 16 != 0) return FP8G_ERR_ALIGNMENT;
-    }
-    if (N >= kMaxDim || (int64_t)E * N >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (K % 32 != 0) return FP8G_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(counts, 4)) return FP8G_ERR_ALIGNMENT;
-    if (offsets_out != nullptr && !aligned(offsets_out, 4)) return FP8G_ERR_ALIGNMENT;
-    if (tile_map_out != nullptr && !aligned(tile_map_out, 16)) return FP8G_ERR_ALIGNMENT;
+    const fp8g_status st = check_grouped_args(A, B, sfa, sfb, C, out, counts, E, N, K, total_rows,
+                                              c_row_of, c_rows, offsets_out, tile_map_out);
+    if (st != FP8G_OK) return st;
     return run_gemm(kModeGrouped, A, B, sfa, sfb, C, out, total_rows, N, K, counts, E,
                     offsets_out, tile_map_out, stream, nullptr, 0, a_fmt, b_fmt, bias, act,
                     c_row_of, c_row_of != nullptr ? c_rows : total_rows);
 }
+
+fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_rows,
+                                   const int32_t *rows, const void *B, const float *sfb, void *C,
+                                   int out, int32_t b_fmt, const float *bias, int32_t act,
+                                   const int32_t *counts, int32_t E, int64_t N, int64_t K,
+                                   int64_t total_rows, const int32_t *c_row_of, int64_t c_rows,
+                                   uint8_t *qa_out, float *sfa_out, int32_t *offsets_out,
+                                   int32_t *tile_map_out, cudaStream_t stream) {
+    if (x_dtype != FP8G_IN_F32 && x_dtype != FP8G_IN_BF16) return FP8G_ERR_INVALID_ARG;
+    if ((qa_out == nullptr) != (sfa_out == nullptr)) return FP8G_ERR_INVALID_ARG;
+    if (total_rows > 0) {
+        if (X == nullptr || x_rows < 1) return FP8G_ERR_INVALID_ARG;
+        if (rows == nullptr && total_rows > x_rows) return FP8G_ERR_INVALID_ARG;
+        if (x_rows >= kMaxDim) return FP8G_ERR_UNSUPPORTED_SHAPE;
+        if (!aligned(X, 16)) return FP8G_ERR_ALIGNMENT;
+        if (rows != nullptr && !aligned(rows, 4)) return FP8G_ERR_ALIGNMENT;
+    }
+    if (qa_out != nullptr && (!aligned(qa_out, 16) || !aligned(sfa_out, 16)))
+        return FP8G_ERR_ALIGNMENT;
+    // the grouped GEMM's own rules; the quantised A (X's place when it stays
+    // in shared memory) stands in for A and its scales
+    const void *a_arg = qa_out != nullptr ? static_cast<const void *>(qa_out) : X;
+    const float *sfa_arg = sfa_out != nullptr ? sfa_out : sfb;
+    fp8g_status st = check_grouped_args(a_arg, B, sfa_arg, sfb, C, out, counts, E, N, K,
+                                        total_rows, c_row_of, c_rows, offsets_out, tile_map_out);
+    if (st != FP8G_OK) return st;
+    if (!valid_fmt(b_fmt)) return FP8G_ERR_INVALID_ARG;
+    const int64_t c_rows_eff = c_row_of != nullptr ? c_rows : total_rows;
+    DevInfo di;
+    if ((st = device_info(di)) != FP8G_OK) return st;
+    const KernelChoice kc = choose_kernel(kModeGrouped, total_rows, N, K, di.num_sms);
+    if (total_rows > 0 && !kc.pair) {
+        // one kernel: the GEMM quantises each tile of A it multiplies
+        const FusedQuant fq{X, x_dtype == FP8G_IN_BF16 ? 1 : 0, rows, x_rows, qa_out, sfa_out};
+        return run_gemm(kModeGrouped, nullptr, B, nullptr, sfb, C, out, total_rows, N, K, counts,
+                        E, offsets_out, tile_map_out, stream, nullptr, 0, FP8G_E4M3, b_fmt, bias,
+                        act, c_row_of, c_rows_eff, &fq);
+    }
+    // two kernels: gather-quantise, then the grouped GEMM
+    uint8_t *qa = qa_out;
+    float *sa = sfa_out;
+    void *tmp = nullptr;
+    if (total_rows > 0 && qa == nullptr) {
+        cudaMemPool_t pool;
+        if ((st = scale_pool(di.dev, pool)) != FP8G_OK) return st;
+        const size_t code_bytes = ((size_t)total_rows * (size_t)K + 255) / 256 * 256;
+        const size_t scale_bytes = (size_t)total_rows * (size_t)(K / 32) * 4;
+        if (cudaMallocFromPoolAsync(&tmp, code_bytes + scale_bytes, pool, stream) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        qa = static_cast<uint8_t *>(tmp);
+        sa = reinterpret_cast<float *>(qa + code_bytes);
+    }
+    if (total_rows > 0)
+        st = fp8g_quantize_rows(X, x_dtype, x_rows, K, rows, total_rows, 32, FP8G_E4M3, qa, sa,
+                                stream);
+    if (st == FP8G_OK)
+        st = run_gemm(kModeGrouped, qa, B, total_rows > 0 ? sa : sfb, sfb, C, out, total_rows, N,
+                      K, counts, E, offsets_out, tile_map_out, stream, nullptr, 0, FP8G_E4M3,
+                      b_fmt, bias, act, c_row_of, c_rows_eff);
+    if (tmp != nullptr && cudaFreeAsync(tmp, stream) != cudaSuccess && st == FP8G_OK)
+        st = FP8G_ERR_CUDA;
+    return st;
+}
+
+
 
 fp8g_status fp8g_grouped_plan(int64_t N, int64_t K, int64_t total_rows, int32_t E, int32_t *BM,
                               int32_t *BN, int32_t *G, int64_t *max_tiles) {

@@ -41,6 +41,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 #include "kernel_common.cuh"
+#include "quant_math.cuh"
 
 namespace fp8g {
 
@@ -200,6 +201,94 @@ __device__ __forceinline__ bool convert_scales(const GemmParams &p, const Tile &
     return ok;
 }
 
+// Fused activation quantiser (grouped GEMM, single CTA; epilogue warp ew of
+// 16): quantises this CTA's 128-row tile of A for K step kb into ring stage
+// it % STAGES, from the routed rows' source activations: E4M3 codes with one
+// power-of-two scale per 1x32 block, by the arithmetic of fp8g_quantize_rows
+// (quant_math.cuh), so the codes and scales equal that quantiser's bit for
+// bit.  Thread (ew, lane) takes row 8 ew + lane / 4 and the stage's 32-wide K
+// block lane % 4.  The codes go to the stage's A tile in the 128-byte-swizzle
+// K-major layout the TMA load would have written (16-byte chunk c of row r at
+// (c ^ (r % 8)) * 16 within the row's 128 bytes, 8-row groups of 1 KB), the
+// scales' UE8M0 codes to the stage's A chunk (byte 16 d + 4 w + j = row 32 w +
+// d, block j).  Rows past the expert and blocks past K: zeros, code 127
+// (scale 1), as the TMA zero fill and the scale packer give.  A source row
+// outside [0, xq_src_rows) records FP8G_ERR_INVALID_ARG (detail: the routed
+// row) and reads as zeros.  With qa_out set, the CTAs of tile column 0 also
+// store the codes and fp32 scales of their rows.  The loads are issued before
+// the wait for the stage.  Returns false when the CTA is aborting.
+template <int STAGES, bool BF16>
+__device__ __forceinline__ bool fq_stage(const GemmParams &p, const Tile &ti, int kb, uint32_t it,
+                                         int ew, uint32_t a_base, uint32_t a_bytes,
+                                         uint32_t sf_base, uint32_t chunk_bytes, uint64_t *bars,
+                                         volatile int *abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
+    const int r = ew * 8 + (lane >> 2);
+    const int j = lane & 3;
+    const int64_t grow = (int64_t)ti.row0 + r;
+    const int64_t k0 = (int64_t)kb * kBK + 32 * j;
+    const bool in_tile = grow < ti.row_end && k0 < p.K;  // a routed row's block
+    bool live = in_tile;
+    int64_t src = 0;
+    if (live) {
+        src = p.xq_rows != nullptr ? (int64_t)__ldg(p.xq_rows + grow) : grow;
+        if (src < 0 || src >= p.xq_src_rows) {
+            if (j == 0) record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)grow);
+            live = false;
+        }
+    }
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        v[2 * q + 1] = v[2 * q];
+        if (live) load8<BF16>(p.xq, src * p.K + k0 + 8 * q, v[2 * q], v[2 * q + 1]);
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) am = fmaxf(am, absmax8(v[2 * q], v[2 * q + 1]));
+    const float s = live ? pow2_scale<0>(am) : 1.0f;
+    uint2 o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = quant8_pow2<0>(v[2 * q], v[2 * q + 1], s);
+    const uint4 c0 = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+    const uint4 c1 = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
+    if (p.qa_out != nullptr && ti.pn == 0 && in_tile) {
+        uint4 *dq = reinterpret_cast<uint4 *>(p.qa_out + grow * p.K + k0);
+        dq[0] = c0;
+        dq[1] = c1;
+        p.sfa_out[grow * p.sfc + k0 / 32] = s;
+    }
+    // the row's scale word: block j's code in byte j (the four lanes of the row)
+    uint32_t word = ((__float_as_uint(s) >> 23) & 0xFFu) << (8 * j);
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (!wait_bar_warp(ptx::smem_addr(&bars[STAGES + stage]), phase ^ 1u, abort_flag, p,
+                       6 * 256 + stage))
+        return false;
+    const uint32_t row_base = a_base + stage * a_bytes + (uint32_t)(r >> 3) * 1024u +
+                              (uint32_t)(r & 7) * 128u;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                     row_base + ((uint32_t)((2 * j) ^ (r & 7)) << 4)),
+                 "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w)
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                     row_base + ((uint32_t)((2 * j + 1) ^ (r & 7)) << 4)),
+                 "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w)
+                 : "memory");
+    if (j == 0)
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes +
+                                                       16u * (uint32_t)(r & 31) +
+                                                       4u * (uint32_t)(r >> 5)),
+                     "r"(word)
+                     : "memory");
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[stage]));
+    return true;
+}
+
 // SPLIT: the CTAs of one cluster share an output tile, each taking a
 // contiguous range of K blocks; their fp32 partials meet in distributed shared
 // memory (see the end of the kernel).  Partial layout in the idle operand
@@ -213,7 +302,9 @@ __device__ __forceinline__ uint32_t split_offset(int S, int row, int col) {
     const int s = col / cols, c4 = (col % cols) >> 2;
     return (uint32_t)(s * kBM * cols + row * cols) * 4u + (uint32_t)((c4 ^ (row & 7)) << 4);
 }
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
+// FQ (grouped, single CTA): the epilogue warps also quantise A in the kernel
+// (fq_stage); the producer loads only B and B's scale chunk.
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
@@ -222,8 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of reading chunks that a packing kernel wrote
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
-    constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES : C_::TX_BYTES;
-    const uint32_t tx_bytes = kTxBytes - C_::A_BYTES / 8 * (uint32_t)p.a_gap8 -
+    static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && NUM_ACC == 1 && kEpiWarps * 8 == kBM),
+                  "fused quantiser: grouped single-CTA kernel, 8 rows per epilogue warp");
+    constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES
+                                  : FQ      ? C_::B_BYTES + C_::SFB_BYTES
+                                            : C_::TX_BYTES;
+    const uint32_t tx_bytes = kTxBytes - (FQ ? 0u : C_::A_BYTES / 8 * (uint32_t)p.a_gap8) -
                               C_::B_BYTES / 8 * (uint32_t)p.b_gap8;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled TMA tiles need 1024-byte alignment in the shared window
@@ -251,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar_full(s), kInlineSF ? 1 + kSfWarps : 1);
+            ptx::mbar_init(bar_full(s), kInlineSF ? 1 + kSfWarps : FQ ? 1 + kEpiWarps : 1);
             ptx::mbar_init(bar_empty(s), 1);
             ptx::mbar_init(bar_sfr(s), 1);
         }
@@ -316,8 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         goto roles_done;
                     const uint32_t fb = bar_full(stage);
                     ptx::mbar_arrive_expect_tx(fb, tx_bytes);
-                    ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb, kb * kBK,
-                                     ti.row0);
+                    if constexpr (!FQ)
+                        ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb,
+                                         kb * kBK, ti.row0);
                     if constexpr (MODE == kModeGrouped)
                         ptx::tma_load_3d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
                                          kb * kBK, ti.n0, ti.e);
@@ -331,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint8_t *sb_src =
                             p.sfb_pk +
                             (((int64_t)ti.e * p.num_kb + kb) * p.n_rtB + ti.n0 / kBM) * 512;
-                        ptx::bulk_load(dst, sa_src, kBM * 4, fb);
+                        if constexpr (!FQ) ptx::bulk_load(dst, sa_src, kBM * 4, fb);
                         if constexpr (C_::kRepB) {
                             const uint8_t *sb_rep =
                                 p.sfb_pk +
@@ -425,6 +521,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else if (FQ && warp >= kEpiWarp0) {
+        // ===== fused quantiser + epilogue =====
+        // Each warp quantises its 8 rows of A for every K step (fq_stage) and
+        // drains / stores the previous tile's accumulator once the first
+        // min(STAGES - 1, num_kb) steps of the next tile are quantised: those
+        // steps wait only for the previous tile's MMAs, and the next tile's
+        // first MMA waits for that drain (one accumulator), so neither order
+        // can deadlock.
+        const int ew = warp - kEpiWarp0;
+        const int q = warp & 3;
+        const int col0 = (ew >> 2) * C_::CW;
+        const bool bf16 = p.xq_bf16 != 0;
+        int32_t ltd = 0;  // tiles drained
+        uint32_t it = 0;  // K steps quantised (the ring's stage counter)
+        Tile prev{};
+        bool have_prev = false;
+        auto drain_store = [&](const Tile &ti) -> bool {
+            if (!wait_bar_warp(bar_accf(0), (uint32_t)(ltd & 1), abort_flag, p, 3 * 256, 128))
+                return false;
+            ptx::tc_fence_after();
+            uint32_t r[C_::CW / 32][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + col0;
+#pragma unroll
+            for (int c = 0; c < C_::CW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_acce(0));
+            ++ltd;
+            const int64_t arow = (int64_t)ti.row0 + q * 32 + lane;          // routed row
+            const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;  // row of C
+            if (row >= 0) {
+                const int64_t ncol0 = (int64_t)ti.n0 + col0;
+                if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
+                    const float *brow = p.bias != nullptr ? p.bias + (int64_t)ti.e * p.N : nullptr;
+#pragma unroll
+                    for (int c = 0; c < C_::CW / 32; ++c)
+                        epi32(r[c], 1.0f, brow, p.act, ncol0 + c * 32, p.N);
+                }
+#pragma unroll
+                for (int c = 0; c < C_::CW / 32; ++c)
+                    store_row32<OUT_F32>(p.C, row, p.N, ncol0 + c * 32, r[c], 1.0f, p.st32 != 0);
+            }
+            return true;
+        };
+        for (int32_t t = t_first; t < T; t += t_step) {
+            const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
+            const int pre = p.num_kb < STAGES - 1 ? p.num_kb : STAGES - 1;
+            for (int kb = 0; kb <= p.num_kb; ++kb) {
+                if (kb == pre && have_prev) {
+                    if (!drain_store(prev)) goto roles_done;
+                    have_prev = false;
+                }
+                if (kb < p.num_kb) {
+                    const bool ok =
+                        bf16 ? fq_stage<STAGES, true>(p, ti, kb, it, ew, sbase + C_::OFF_A,
+                                                      C_::A_BYTES, sbase + C_::OFF_SF,
+                                                      C_::CHUNK_BYTES, bars, abort_flag)
+                             : fq_stage<STAGES, false>(p, ti, kb, it, ew, sbase + C_::OFF_A,
+                                                       C_::A_BYTES, sbase + C_::OFF_SF,
+                                                       C_::CHUNK_BYTES, bars, abort_flag);
+                    if (!ok) goto roles_done;
+                    ++it;
+                }
+            }
+            prev = ti;
+            have_prev = true;
+        }
+        if (have_prev) (void)drain_store(prev);
     } else if (warp >= kEpiWarp0) {
         // ===== epilogue =====
         const int ew = warp - kEpiWarp0;
@@ -611,13 +776,13 @@ roles_done:
     }
 }
 
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT>
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
 cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
                        cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
     static_assert(!SPLIT || 2 * kBM * BN * 4 <= STAGES * (C_::A_BYTES + C_::B_BYTES),
                   "split-K partial must fit in the operand ring");
-    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT>;
+    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT, FQ>;
     // The shared-memory opt-in is per device; the flag races benignly (the
     // attribute set is idempotent).
     static unsigned long long attr_done = 0ull;
@@ -757,6 +922,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
 cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const GemmParams &p,
                         const KernelChoice &kc, cudaStream_t stream) {
     const bool split = kc.split > 1;
+    if (kc.pair && p.xq != nullptr) return cudaErrorInvalidValue;
     if (kc.pair) return launch_gemm_pair(mode, out_f32, maps, p, kc.grid, stream);
     if (mode == kModeTensor) {
         if (split)
@@ -770,6 +936,11 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                            : launch_one<kModeBlock, 128, 1, 6, false, true>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
+    } else if (p.xq != nullptr) {
+        // fused activation quantiser (single CTAs only: the caller checks the plan)
+        if (kc.pair || split) return cudaErrorInvalidValue;
+        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, true>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 256, 1, 4, false, false, true>(maps, p, kc, stream);
     } else {
         return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeGrouped, 256, 1, 4, false, false>(maps, p, kc, stream);

@@ -58,6 +58,18 @@ struct GemmParams {
     int32_t act;           // fused epilogue activation: FP8G_ACT_*
     const int32_t *c_row_of;  // grouped scatter: row of C for routed row r (null: r)
     int64_t c_rows;           // rows of C when scattering
+    // Fused activation quantiser (grouped GEMM on single CTAs): A is not read
+    // from memory; each stage's 128 x 128 tile of A is quantised in the kernel
+    // (E4M3, 1x32 power-of-two scales) from routed row r = source row
+    // xq_rows[r] (null: r) of xq [xq_src_rows, K] (fp32, or bf16 if xq_bf16).
+    // qa_out [rows, K] / sfa_out [rows, K/32] (nullable) receive the codes and
+    // scales, written by the CTAs of the first column of tiles.
+    const void *xq;
+    int32_t xq_bf16;
+    const int32_t *xq_rows;
+    int64_t xq_src_rows;
+    uint8_t *qa_out;
+    float *sfa_out;
 };
 
 // TMA descriptors of one launch: E4M3 operands and, for block-scaled CTA
@@ -99,12 +111,22 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
 // scale temporary from the library pool, otherwise uses [scratch,
 // scratch + scratch_bytes) (FP8G_ERR_UNSUPPORTED_SHAPE if it is too small).
 // a_fmt, b_fmt: operand formats (FP8G_E4M3 / FP8G_E5M2).
+// fq (grouped mode only, single-CTA plan): the fused activation quantiser's
+// source (GemmParams::xq ..); A and sa are then not read.
+struct FusedQuant {
+    const void *x;
+    int32_t bf16;
+    const int32_t *rows;
+    int64_t src_rows;
+    uint8_t *qa_out;
+    float *sfa_out;
+};
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
                      void *scratch, size_t scratch_bytes, int a_fmt = 0, int b_fmt = 0,
                      const float *bias = nullptr, int act = 0, const int32_t *c_row_of = nullptr,
-                     int64_t c_rows = 0);
+                     int64_t c_rows = 0, const FusedQuant *fq = nullptr);
 
 // api.cu: the host-side argument checks of the 1x32 block-scaled GEMM, in the
 // order fp8_gemm_blockscaled applies them (shared by its allocation-free

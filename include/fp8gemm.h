@@ -420,6 +420,44 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
                                      cudaStream_t stream);
 
 /*
+ * Grouped (MoE) GEMM from unquantised activations [JAX-BW MoE paragraph:
+ * tokens routed to experts; its fine-grained (1x32) quantisation advice
+ * against FP8 underflow].  The result equals
+ *   fp8g_quantize_rows(X, x_dtype, x_rows, K, rows, total_rows, 32, FP8G_E4M3,
+ *                      qa, sfa)
+ *   fp8_grouped_gemm_scatter(qa, B, sfa, sfb, C, out, FP8G_E4M3, b_fmt, bias,
+ *                            act, counts, E, N, K, total_rows, c_row_of,
+ *                            c_rows, offsets_out, tile_map_out)
+ * bit for bit: routed row r (expert order) is source row rows[r] of X
+ * [x_rows, K] (rows null: row r, total_rows <= x_rows), quantised to E4M3
+ * with one power-of-two scale per 1x32 block, then multiplied by its
+ * expert's B[e].  When the grouped plan runs one CTA per 128-row tile
+ * (fp8g_grouped_plan BM = 128: few routed rows, e.g. decoding), the
+ * quantisation happens inside the GEMM kernel: each CTA quantises the tile
+ * of A it is about to multiply from X into shared memory, so A is never
+ * written to or read back from memory (one kernel, plus the packing of B's
+ * scales).  Otherwise (BM = 256) the two steps run as two kernels with the
+ * codes in qa_out / sfa_out, or in a stream-ordered temporary from the
+ * library's pool when those are null.
+ * X: fp32 or bf16 (x_dtype, FP8G_IN_*), 16-byte aligned; rows: device int32
+ * [total_rows], 4-byte aligned; qa_out (nullable) uint8 [total_rows, K] and
+ * sfa_out (nullable) fp32 [total_rows, K/32], both or neither, 16-byte
+ * aligned: they receive the codes and scales (when the counts are valid).
+ * K % 32 == 0.  Other arguments and rules as fp8_grouped_gemm_scatter.  A
+ * source row outside [0, x_rows) records FP8G_ERR_INVALID_ARG (detail: the
+ * routed row) and that row quantises as zeros.  Parity: the quantiser's
+ * codes and scales bit-exact, the GEMM within the block-scaled tolerance.
+ */
+FP8G_API fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_rows,
+                                           const int32_t *rows, const void *B, const float *sfb,
+                                           void *C, int out, int32_t b_fmt, const float *bias,
+                                           int32_t act, const int32_t *counts, int32_t E,
+                                           int64_t N, int64_t K, int64_t total_rows,
+                                           const int32_t *c_row_of, int64_t c_rows,
+                                           uint8_t *qa_out, float *sfa_out, int32_t *offsets_out,
+                                           int32_t *tile_map_out, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word (FP8G_OK if no kernel recorded an error since the last call).
  * `detail` (nullable) receives a kernel-specific code for the first error

@@ -173,3 +173,16 @@ def small_grouped(counts, N: int, K: int, seed: int = 7, out: str = "bf16") -> W
     A = normal((max(rows, 0), K), seed)
     B = normal((counts.size, N, K), seed + 1000, std=0.02)
     return Workload(f"grouped{counts.size}x{N}x{K}", rows, N, K, True, out, A, B, counts)
+
+
+def moe_tokens(seed: int = 4, experts: int = 8, tokens: int = 16384, N: int = 14336,
+               K: int = 4096, out: str = "bf16"):
+    """The MoE workload before routing: token activations X [tokens, K] (the
+    rows moe_grouped gathers), the routed-row -> token index (routed row r of
+    the expert-ordered list takes token r % tokens: each token's two slots are
+    rows t and t + tokens), and the grouped workload itself (counts, B)."""
+    w = moe_grouped(seed, experts, tokens, N, K, out)
+    X = normal((tokens, K), seed)
+    idx = (torch.arange(w.M) % tokens).to(torch.int32)
+    return X, idx, w
+

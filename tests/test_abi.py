@@ -187,3 +187,31 @@ def test_noalloc_checks_match_blockscaled(fp8g):
         a = _err(fp8g.fp8_gemm_blockscaled, *args, 0)
         b = _err(fp8g.fp8_gemm_blockscaled_noalloc, *args, 0)
         assert a == b, (args, a, b)
+
+
+def test_fused_quant_host_checks(fp8g):
+    """fp8_grouped_gemm_quant: source type, copies both-or-neither, gather
+    without an index past the source, alignment of X and the copies, and the
+    grouped GEMM's own rules, all before any device work."""
+    P = 1 << 20
+    f = fp8g.fp8_grouped_gemm_quant
+    E = fp8g.FP8G_ERR_INVALID_ARG
+    A = fp8g.FP8G_ERR_ALIGNMENT
+    ok = dict(X=P, x_dtype=1, x_rows=8, rows=P, B=P, sfb=P, C=P, out=0, b_fmt=0, bias=None,
+              act=0, counts=P, E=2, N=8, K=64, total_rows=8)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return _err(f, a["X"], a["x_dtype"], a["x_rows"], a["rows"], a["B"], a["sfb"], a["C"],
+                    a["out"], a["b_fmt"], a["bias"], a["act"], a["counts"], a["E"], a["N"],
+                    a["K"], a["total_rows"], None, 0, a.get("qa"), a.get("sa"), None, None, 0)
+    assert call(x_dtype=2) == E
+    assert call(qa=P) == E                                  # codes without scales
+    assert call(rows=None, x_rows=4) == E                   # 8 routed rows from 4 sources
+    assert call(X=P + 8) == A
+    assert call(rows=P + 2) == A
+    assert call(qa=P + 8, sa=P) == A
+    assert call(K=48) == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+    assert call(E=0) == E
+    assert call(counts=None) == E
+    assert call(b_fmt=7) == E

@@ -55,7 +55,8 @@ def test_algorithmic_bytes_grouped():
 def test_workload_table():
     """Every workload is named by its sizes; formats are the library's codes."""
     for name, wl in bench.WORKLOADS.items():
-        assert wl["kind"] in ("block", "tensor", "grouped", "nvfp4", "grouped_nvfp4"), name
+        assert wl["kind"] in ("block", "tensor", "grouped", "nvfp4", "grouped_nvfp4",
+                              "grouped_quant"), name
         assert wl.get("a_fmt", 0) in range(5) and wl.get("b_fmt", 0) in range(5), name
         assert wl["M"] > 0 and wl["N"] > 0 and wl["K"] % 32 == 0, name
     assert len(bench.FMT_NAMES) == len(bench.FMT_BYTES) == 5
@@ -83,3 +84,17 @@ def test_both_arms_describe_the_same_workload():
         assert a == bench.config_of(name, wl, "bf16", 1) and a["workload"] == name
         assert set(a) == {"workload", "M", "N", "K", "formats", "scales", "out", "l2",
                           "parallelism"}
+
+
+def test_algorithmic_bytes_from_tokens():
+    """MoE from bf16 tokens: each routed row's bf16 source read once, the int32
+    routing index, the FP8 weights and their fp32 1x32 scales, C, the counts
+    (the two-call path's extra write and read of the quantised rows is not
+    part of the method's traffic)."""
+    E, N, K = 8, 14336, 4096
+    for name, rows in (("decode_bf16", 256), ("moe_bf16", 32768)):
+        want = rows * K * 2 + 4 * rows + E * N * K + 4 * E * N * K // 32 + rows * N * 2 + 4 * E
+        assert bench.algorithmic_bytes(bench.WORKLOADS[name], _w(experts=E)) == want
+        two = bench.WORKLOADS[name + "_2call"]
+        assert bench.algorithmic_bytes(two, _w(experts=E)) == want and not two["fused"]
+
