@@ -57,7 +57,13 @@ constexpr int kEpiWarps = 16;
 constexpr int kSfWarps = 8;
 constexpr int kSfAhead = 4;
 
-template <int MODE, int BN, int NUM_ACC, int STAGES>
+// Split-K (SPLITC): the ring of a split-K CTA, then its receive region for
+// the peers' partial blocks: (S - 1) x 128 rows x (128 / S) columns of fp32,
+// at most 48 KB (S <= 4).
+constexpr int kSplitStages = 5;
+constexpr int kRecvBytes = 48 * 1024;
+
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool SPLITC = false>
 struct Cfg {
     static constexpr bool kBlock = MODE != kModeTensor;
     static constexpr int A_BYTES = kBM * kBK;
@@ -72,7 +78,8 @@ struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BAR = OFF_SF + STAGES * CHUNK_BYTES;
+    static constexpr int OFF_RECV = OFF_SF + STAGES * CHUNK_BYTES;
+    static constexpr int OFF_BAR = OFF_RECV + (SPLITC ? kRecvBytes : 0);
     // full[S], empty[S], acc_full[NA], acc_empty[NA], drain, split-K receive,
     // drain of the scale-copy thread, scales ready[S]
     static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 3;
@@ -290,25 +297,24 @@ __device__ __forceinline__ bool fq_stage(const GemmParams &p, const Tile &ti, in
 }
 
 // SPLIT: the CTAs of one cluster share an output tile, each taking a
-// contiguous range of K blocks; their fp32 partials meet in distributed shared
-// memory (see the end of the kernel).  Partial layout in the idle operand
-// ring: S column slices of 128 rows x BN/S floats, each contiguous (one bulk
-// copy), 16-byte groups of a row XOR-swizzled by (row & 7) so that the
-// epilogue's row-per-lane stores do not collide in shared-memory banks.
-// Behind the partial, S receive slots of one slice each.
-template <int BN>
-__device__ __forceinline__ uint32_t split_offset(int S, int row, int col) {
-    const int cols = BN / S;
-    const int s = col / cols, c4 = (col % cols) >> 2;
-    return (uint32_t)(s * kBM * cols + row * cols) * 4u + (uint32_t)((c4 ^ (row & 7)) << 4);
-}
+// contiguous range of K blocks; CTA o of the cluster owns columns
+// [o 128 / S, (o + 1) 128 / S) of the tile.  As soon as its accumulator is in
+// registers, each epilogue warp (32 rows x 32 columns) stages the block in
+// its CTA's idle operand ring and pushes it with one bulk copy into the
+// owner's receive region (slot: sender, row quarter, column group), counted
+// in bytes on the owner's receive barrier; the owner's warps wait for every
+// peer's block of their rows, add them to their own partial in rank order (a
+// fixed order, so results do not depend on timing) and store.  Blocks are row-major
+// 32 x 32 fp32, 16-byte chunks XOR-swizzled by row (lane = row: conflict-free).
 // FQ (grouped, single CTA): the epilogue warps also quantise A in the kernel
 // (fq_stage); the producer loads only B and B's scale chunk.
 template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
-    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
+    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES, SPLIT>;
+    static_assert(!SPLIT || (BN == 128 && C_::CW == 32 && STAGES * C_::A_BYTES >= kEpiWarps * 4096),
+                  "split-K: 32 x 32 blocks per epilogue warp, staged in the A ring");
     // split-K tiles are few: the kernel converts its own scale chunks instead
     // of reading chunks that a packing kernel wrote
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
@@ -357,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_drain, 1);
         ptx::mbar_init(bar_recv, 1);
         ptx::mbar_init(bar_drain_sf, 1);
+        if constexpr (SPLIT)  // the peers' blocks of this CTA's columns (one tile per cluster)
+            ptx::mbar_arrive_expect_tx(bar_recv, (uint32_t)((p.split - 1) * kBM * (BN / p.split) * 4));
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -368,6 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C_::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // Split-K: every CTA's receive barrier initialised before any peer's push
+    // (the wait is below, after the dependency wait)
+    if constexpr (SPLIT) ptx::cluster_arrive_release();
     // Everything above touched only shared / tensor memory and kernel
     // parameters; global memory (which the previous kernel on the stream may
     // still be writing, or reading) is accessed only after this wait.  The
@@ -380,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if constexpr (MODE == kModeGrouped) T = tile_off[p.E];
+    if constexpr (SPLIT) ptx::cluster_wait();
     const uint32_t tmem_base = *tmem_slot;
 
     // work of this CTA: tiles t_first, t_first + t_step, ...; K blocks [kb_begin, kb_end)
@@ -621,20 +633,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(bar_acce(acc));
 
             if constexpr (SPLIT) {
-                // fp32 partial of this K range -> own shared memory (the ring is
-                // idle: every MMA, hence every operand read, has completed),
-                // then made visible to the bulk copies that send it
-                const int row = q * 32 + lane;
-#pragma unroll
-                for (int c = 0; c < C_::CW / 32; ++c)
+                const int S = p.split;
+                const int rank = (int)ptx::cluster_rank();
+                const int cg = ew >> 2;                  // this warp's 32 columns of the 128
+                const int owner = cg * S / 4;            // CTA that sums these columns
+                const int cgi = cg - owner * (4 / S);    // 32-column group within its slice
+                auto chunk = [&](uint32_t blk, int v) {  // 16-byte chunk v of row `lane`
+                    return blk + (uint32_t)lane * 128u + ((uint32_t)(v ^ (lane & 7)) << 4);
+                };
+                if (owner != rank) {
+                    // the ring is idle (every MMA, hence every operand read, completed)
+                    const uint32_t blk = sbase + C_::OFF_A + (uint32_t)ew * 4096u;
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        *reinterpret_cast<uint4 *>(
-                            smem + C_::OFF_A + split_offset<BN>(p.split, row, col0 + c * 32 + v * 4)) =
-                            make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2],
-                                       r[c][4 * v + 3]);
-                ptx::fence_proxy_async_smem();
-                continue;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(chunk(blk, v)),
+                                     "r"(r[0][4 * v]), "r"(r[0][4 * v + 1]), "r"(r[0][4 * v + 2]),
+                                     "r"(r[0][4 * v + 3])
+                                     : "memory");
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int slot = rank < owner ? rank : rank - 1;
+                        const uint32_t dst = sbase + C_::OFF_RECV +
+                                             (uint32_t)(((slot * 4 + q) * (4 / S) + cgi) * 4096);
+                        ptx::bulk_push(ptx::map_shared(dst, (uint32_t)owner), blk, 4096u,
+                                       ptx::map_shared(bar_recv, (uint32_t)owner));
+                    }
+                    continue;
+                }
+                // own columns: every peer's block of these rows, then the sum in a
+                // fixed order: this CTA's partial, then the peers' in rank order
+                if (!wait_bar_landed_warp(bar_recv, 0, abort_flag, p, 4 * 256)) break;
+                for (int sl = 0; sl < S - 1; ++sl) {
+                    const uint32_t blk = sbase + C_::OFF_RECV +
+                                         (uint32_t)(((sl * 4 + q) * (4 / S) + cgi) * 4096);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float x0, x1, x2, x3;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+                                     : "r"(chunk(blk, v))
+                                     : "memory");
+                        r[0][4 * v] = __float_as_uint(__fadd_rn(__uint_as_float(r[0][4 * v]), x0));
+                        r[0][4 * v + 1] = __float_as_uint(__fadd_rn(__uint_as_float(r[0][4 * v + 1]), x1));
+                        r[0][4 * v + 2] = __float_as_uint(__fadd_rn(__uint_as_float(r[0][4 * v + 2]), x2));
+                        r[0][4 * v + 3] = __float_as_uint(__fadd_rn(__uint_as_float(r[0][4 * v + 3]), x3));
+                    }
+                }
             }
             const int64_t arow = (int64_t)ti.row0 + q * 32 + lane;  // routed row
             const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;  // row of C
@@ -674,100 +719,10 @@ roles_done:
         __syncthreads();
     }
     if constexpr (SPLIT) {
-        // CTA `rank` owns column slice `rank` of the tile.  After a cluster
-        // barrier (every partial written, every ring idle: an execution
-        // dependency only, so the arrive is relaxed; the partial's writes were
-        // ordered before the copies by the fence above and the CTA barrier at
-        // roles_done, the receive barrier's initialisation by its fence) each CTA pushes
-        // slice o of its partial into receive slot `rank` of CTA o with one
-        // bulk copy, counted in bytes on CTA o's receive barrier.  The owner
-        // sums the S slices in rank order (a fixed order, so results do not
-        // depend on timing) and stores them.  A CTA leaves only when every CTA
-        // has received everything, i.e. when no copy reads or writes its
-        // shared memory any more.
-        const int S = p.split;  // 2..kMaxSplit
-        const uint32_t rank = ptx::cluster_rank();
-        const bool has_tile = t_first < T;  // the same for the whole cluster
-        const uint32_t slice_bytes = (uint32_t)(kBM * (BN / S)) * 4u;
-        const uint32_t part = sbase + C_::OFF_A;
-        const uint32_t recv = part + (uint32_t)(kBM * BN) * 4u;
-        if (threadIdx.x == 0 && has_tile)
-            ptx::mbar_arrive_expect_tx(bar_recv, (uint32_t)(S - 1) * slice_bytes);
+        // A CTA leaves only when every CTA of the cluster has received all its
+        // blocks (each CTA arrives after its own receive barrier completed or
+        // gave up), i.e. when no copy reads or writes its shared memory.
         ptx::cluster_arrive_relaxed();
-        ptx::cluster_wait();
-        if (warp == 0) {
-            if (lane == 0 && has_tile)
-                for (int o = 0; o < S; ++o)
-                    if (o != (int)rank)
-                        ptx::bulk_push(ptx::map_shared(recv + rank * slice_bytes, (uint32_t)o),
-                                       part + (uint32_t)o * slice_bytes, slice_bytes,
-                                       ptx::map_shared(bar_recv, (uint32_t)o));
-            __syncwarp();
-        }
-        bool landed = true;
-        if (warp >= kEpiWarp0 && has_tile)
-            landed = wait_bar_landed_warp(bar_recv, 0, abort_flag, p, 4 * 256);
-        ptx::cluster_arrive_relaxed();
-        if (warp >= kEpiWarp0 && has_tile && landed && !*abort_flag) {
-            const Tile ti = get_tile<MODE, BN>(t_first, p, row_off, tile_off, rt_off);
-            const int cols = BN / S;
-            const int c4n = cols / 4;
-            float alpha = 1.0f;
-            if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
-            const int nthr = kEpiWarps * 32;
-            const float *own = reinterpret_cast<const float *>(smem + C_::OFF_A);
-            const float *rcv = own + kBM * BN;
-            for (int u = threadIdx.x - kEpiWarp0 * 32; u < kBM * c4n; u += nthr) {
-                const int row = u / c4n;
-                const int c4 = u % c4n;
-                const int off = row * cols + ((c4 ^ (row & 7)) << 2);  // floats in a slice
-                float4 v[kMaxSplit];
-#pragma unroll
-                for (int r = 0; r < kMaxSplit; ++r)
-                    if (r < S)
-                        v[r] = *reinterpret_cast<const float4 *>(
-                            (r == (int)rank ? own + (int)rank * kBM * cols : rcv + r * kBM * cols) +
-                            off);
-                float4 acc = v[0];
-#pragma unroll
-                for (int r = 1; r < kMaxSplit; ++r)
-                    if (r < S) {
-                        acc.x += v[r].x;
-                        acc.y += v[r].y;
-                        acc.z += v[r].z;
-                        acc.w += v[r].w;
-                    }
-                const int col = (int)rank * cols + c4 * 4;
-                const int64_t grow = (int64_t)ti.row0 + row;
-                const int64_t gcol = (int64_t)ti.n0 + col;
-                if (grow < ti.row_end && gcol < p.N) {
-                    float a_t = alpha;
-                    if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
-                        // N % 4 == 0 for the outputs (16-byte rows), so all four are in range
-                        acc.x = epi1(__fmul_rn(alpha, acc.x), p.bias, p.act, gcol);
-                        acc.y = epi1(__fmul_rn(alpha, acc.y), p.bias, p.act, gcol + 1);
-                        acc.z = epi1(__fmul_rn(alpha, acc.z), p.bias, p.act, gcol + 2);
-                        acc.w = epi1(__fmul_rn(alpha, acc.w), p.bias, p.act, gcol + 3);
-                        a_t = 1.0f;
-                    }
-                    if constexpr (OUT_F32) {
-                        float4 o = make_float4(__fmul_rn(a_t, acc.x), __fmul_rn(a_t, acc.y),
-                                               __fmul_rn(a_t, acc.z), __fmul_rn(a_t, acc.w));
-                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + grow * p.N +
-                                                    gcol) = o;
-                    } else {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(a_t, acc.x),
-                                                                  __fmul_rn(a_t, acc.y));
-                        __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(a_t, acc.z),
-                                                                  __fmul_rn(a_t, acc.w));
-                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) +
-                                                   grow * p.N + gcol) =
-                            make_uint2(*reinterpret_cast<uint32_t *>(&lo),
-                                       *reinterpret_cast<uint32_t *>(&hi));
-                    }
-                }
-            }
-        }
         ptx::cluster_wait();
     }
     if (warp == 1) {
@@ -779,9 +734,7 @@ roles_done:
 template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
 cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
                        cudaStream_t stream) {
-    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES>;
-    static_assert(!SPLIT || 2 * kBM * BN * 4 <= STAGES * (C_::A_BYTES + C_::B_BYTES),
-                  "split-K partial must fit in the operand ring");
+    using C_ = Cfg<MODE, BN, NUM_ACC, STAGES, SPLIT>;
     auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT, FQ>;
     // The shared-memory opt-in is per device; the flag races benignly (the
     // attribute set is idempotent).
@@ -831,8 +784,8 @@ int max_split_clusters(int S) {
         return 0;
     int v = cache[dev][S].load(std::memory_order_relaxed);
     if (v > 0) return v;
-    using C_ = Cfg<kModeBlock, 128, 1, 6>;  // the larger of the two split-K footprints
-    auto kern = gemm_kernel<kModeBlock, 128, 1, 6, false, true>;
+    using C_ = Cfg<kModeBlock, 128, 1, kSplitStages, true>;  // the larger split-K footprint
+    auto kern = gemm_kernel<kModeBlock, 128, 1, kSplitStages, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
@@ -926,14 +879,14 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
     if (kc.pair) return launch_gemm_pair(mode, out_f32, maps, p, kc.grid, stream);
     if (mode == kModeTensor) {
         if (split)
-            return out_f32 ? launch_one<kModeTensor, 128, 1, 6, true, true>(maps, p, kc, stream)
-                           : launch_one<kModeTensor, 128, 1, 6, false, true>(maps, p, kc, stream);
+            return out_f32 ? launch_one<kModeTensor, 128, 1, kSplitStages, true, true>(maps, p, kc, stream)
+                           : launch_one<kModeTensor, 128, 1, kSplitStages, false, true>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeTensor, 256, 2, 4, false, false>(maps, p, kc, stream);
     } else if (mode == kModeBlock) {
         if (split)
-            return out_f32 ? launch_one<kModeBlock, 128, 1, 6, true, true>(maps, p, kc, stream)
-                           : launch_one<kModeBlock, 128, 1, 6, false, true>(maps, p, kc, stream);
+            return out_f32 ? launch_one<kModeBlock, 128, 1, kSplitStages, true, true>(maps, p, kc, stream)
+                           : launch_one<kModeBlock, 128, 1, kSplitStages, false, true>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
     } else if (p.xq != nullptr) {

@@ -101,6 +101,11 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
+// First half of cluster_sync with release semantics (this thread's prior
+// writes, e.g. mbarrier initialisation, visible to the cluster at the wait).
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 // The two halves of cluster_sync, for work placed between them.  The relaxed
 // arrive orders no memory accesses (execution order only; it is much cheaper
 // than the release form, which waits for the thread's prior accesses).
