@@ -222,21 +222,28 @@ def make_inputs(wl: dict, device):
 
 
 def algorithmic_bytes(wl: dict, w) -> int:
+    """Bytes the call must move: each operand read once, C written once.
+    Grouped: only the weights (and scales) of experts that receive rows are
+    read; the counts and, from tokens, the routing index are read once."""
     M, N, K = wl["M"], wl["N"], wl["K"]
     out_b = 4 if w.out == "f32" else 2
     ea, eb = FMT_BYTES[wl.get("a_fmt", 0)], FMT_BYTES[wl.get("b_fmt", 0)]
+    counts = getattr(w, "counts", None)
+    E_all = w.B.shape[0] if w.B.dim() == 3 else 1
+    # experts whose weights are read (all of them when the counts are unknown)
+    E_used = int((np.asarray(counts) > 0).sum()) if counts is not None else E_all
     if wl["kind"] == "grouped":
-        E = w.B.shape[0]
+        E = E_used
         return int(M * K * ea + E * N * K * eb + 4 * (M * K // 32 + E * N * K // 32) +
-                   M * N * out_b + 4 * E)
+                   M * N * out_b + 4 * E_all)
     if wl["kind"] == "grouped_quant":   # bf16 routed rows read once; int32 routing index
-        E = w.B.shape[0]
+        E = E_used
         return int(M * K * 2 + 4 * M + E * N * K * eb + 4 * E * N * K // 32 +
-                   M * N * out_b + 4 * E)
+                   M * N * out_b + 4 * E_all)
     if wl["kind"] == "grouped_nvfp4":   # E4M3 scale bytes per 16; fp32 gA and E gB
-        E = w.B.shape[0]
+        E = E_used
         return int(M * K * ea + E * N * K * eb + (M + E * N) * K // 16 + 4 * (1 + E) +
-                   M * N * out_b + 4 * E)
+                   M * N * out_b + 4 * E_all)
     if wl["kind"] == "nvfp4":   # E4M3 scale bytes per 16 elements + two fp32 tensor scales
         return int(M * K * ea + N * K * eb + (M + N) * K // 16 + 8 + M * N * out_b)
     sf = 8 if wl["kind"] == "tensor" else 4 * (M * K // 32 + N * K // 32)

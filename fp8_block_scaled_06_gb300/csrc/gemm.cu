@@ -222,40 +222,77 @@ __device__ __forceinline__ bool convert_scales(const GemmParams &p, const Tile &
 // (scale 1), as the TMA zero fill and the scale packer give.  A source row
 // outside [0, xq_src_rows) records FP8G_ERR_INVALID_ARG (detail: the routed
 // row) and reads as zeros.  With qa_out set, the CTAs of tile column 0 also
-// store the codes and fp32 scales of their rows.  The loads are issued before
-// the wait for the stage.  Returns false when the CTA is aborting.
-template <int STAGES, bool BF16>
-__device__ __forceinline__ bool fq_stage(const GemmParams &p, const Tile &ti, int kb, uint32_t it,
-                                         int ew, uint32_t a_base, uint32_t a_bytes,
-                                         uint32_t sf_base, uint32_t chunk_bytes, uint64_t *bars,
-                                         volatile int *abort_flag) {
+// store the codes and fp32 scales of their rows.
+//
+// Two halves, so that a warp's loads for the next K step are in flight while
+// it converts and stores this one (one step at a time, each warp waited a
+// whole memory round trip per step): fq_fetch issues the loads (kept in their
+// source form), fq_put converts, waits for the stage and stores.
+template <bool BF16>
+struct FqIn {
+    uint4 u[BF16 ? 4 : 8];  // the block's 32 values: bf16 (4 words) or fp32 (8)
+    bool live;              // a routed row's block whose source row exists
+};
+
+// Routed row and first K of this lane's block of K step kb; whether the block
+// belongs to a routed row (and to K).
+__device__ __forceinline__ bool fq_block(const GemmParams &p, const Tile &ti, int kb, int ew,
+                                         int64_t &grow, int64_t &k0) {
     const int lane = threadIdx.x & 31;
+    grow = (int64_t)ti.row0 + ew * 8 + (lane >> 2);
+    k0 = (int64_t)kb * kBK + 32 * (lane & 3);
+    return grow < ti.row_end && k0 < p.K;
+}
+
+template <bool BF16>
+__device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, const Tile &ti, int kb, int ew) {
+    FqIn<BF16> in;
+    int64_t grow, k0;
+    in.live = fq_block(p, ti, kb, ew, grow, k0);
+    int64_t src = 0;
+    if (in.live) {
+        src = p.xq_rows != nullptr ? (int64_t)__ldg(p.xq_rows + grow) : grow;
+        if (src < 0 || src >= p.xq_src_rows) {
+            if ((threadIdx.x & 3) == 0) record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)grow);
+            in.live = false;
+        }
+    }
+    const uint4 *x = reinterpret_cast<const uint4 *>(
+        static_cast<const uint8_t *>(p.xq) + (src * p.K + k0) * (BF16 ? 2 : 4));
+#pragma unroll
+    for (int i = 0; i < (BF16 ? 4 : 8); ++i)
+        in.u[i] = in.live ? __ldg(x + i) : make_uint4(0u, 0u, 0u, 0u);
+    return in;
+}
+
+template <int STAGES, bool BF16>
+__device__ __forceinline__ bool fq_put(const GemmParams &p, const FqIn<BF16> &in, const Tile &ti,
+                                       int kb, uint32_t it, int ew, uint32_t a_base,
+                                       uint32_t a_bytes, uint32_t sf_base, uint32_t chunk_bytes,
+                                       uint64_t *bars, volatile int *abort_flag) {
+    const int lane = threadIdx.x & 31;
+    int64_t grow, k0;
+    const bool in_tile = fq_block(p, ti, kb, ew, grow, k0);
     const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
     const int r = ew * 8 + (lane >> 2);
     const int j = lane & 3;
-    const int64_t grow = (int64_t)ti.row0 + r;
-    const int64_t k0 = (int64_t)kb * kBK + 32 * j;
-    const bool in_tile = grow < ti.row_end && k0 < p.K;  // a routed row's block
-    bool live = in_tile;
-    int64_t src = 0;
-    if (live) {
-        src = p.xq_rows != nullptr ? (int64_t)__ldg(p.xq_rows + grow) : grow;
-        if (src < 0 || src >= p.xq_src_rows) {
-            if (j == 0) record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)grow);
-            live = false;
-        }
-    }
     float4 v[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        v[2 * q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        v[2 * q + 1] = v[2 * q];
-        if (live) load8<BF16>(p.xq, src * p.K + k0 + 8 * q, v[2 * q], v[2 * q + 1]);
+        if constexpr (BF16) {
+            bf16x8_to_f32(in.u[q], v[2 * q], v[2 * q + 1]);
+        } else {
+            const uint4 a = in.u[2 * q], b = in.u[2 * q + 1];
+            v[2 * q] = make_float4(__uint_as_float(a.x), __uint_as_float(a.y),
+                                   __uint_as_float(a.z), __uint_as_float(a.w));
+            v[2 * q + 1] = make_float4(__uint_as_float(b.x), __uint_as_float(b.y),
+                                       __uint_as_float(b.z), __uint_as_float(b.w));
+        }
     }
     float am = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) am = fmaxf(am, absmax8(v[2 * q], v[2 * q + 1]));
-    const float s = live ? pow2_scale<0>(am) : 1.0f;
+    const float s = in.live ? pow2_scale<0>(am) : 1.0f;
     uint2 o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) o[q] = quant8_pow2<0>(v[2 * q], v[2 * q + 1], s);
@@ -307,8 +344,9 @@ __device__ __forceinline__ bool fq_stage(const GemmParams &p, const Tile &ti, in
 // fixed order, so results do not depend on timing) and store.  Blocks are row-major
 // 32 x 32 fp32, 16-byte chunks XOR-swizzled by row (lane = row: conflict-free).
 // FQ (grouped, single CTA): the epilogue warps also quantise A in the kernel
-// (fq_stage); the producer loads only B and B's scale chunk.
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
+// (fq_fetch / fq_put) from fp32 (FQ = 1) or bf16 (FQ = 2) activations; the
+// producer loads only B and B's scale chunk.
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
@@ -533,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (FQ && warp >= kEpiWarp0) {
+    } else if (FQ != 0 && warp >= kEpiWarp0) {
         // ===== fused quantiser + epilogue =====
         // Each warp quantises its 8 rows of A for every K step (fq_stage) and
         // drains / stores the previous tile's accumulator once the first
@@ -544,7 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - kEpiWarp0;
         const int q = warp & 3;
         const int col0 = (ew >> 2) * C_::CW;
-        const bool bf16 = p.xq_bf16 != 0;
         int32_t ltd = 0;  // tiles drained
         uint32_t it = 0;  // K steps quantised (the ring's stage counter)
         Tile prev{};
@@ -578,28 +615,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return true;
         };
-        for (int32_t t = t_first; t < T; t += t_step) {
-            const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
-            const int pre = p.num_kb < STAGES - 1 ? p.num_kb : STAGES - 1;
-            for (int kb = 0; kb <= p.num_kb; ++kb) {
-                if (kb == pre && have_prev) {
-                    if (!drain_store(prev)) goto roles_done;
-                    have_prev = false;
-                }
-                if (kb < p.num_kb) {
-                    const bool ok =
-                        bf16 ? fq_stage<STAGES, true>(p, ti, kb, it, ew, sbase + C_::OFF_A,
-                                                      C_::A_BYTES, sbase + C_::OFF_SF,
-                                                      C_::CHUNK_BYTES, bars, abort_flag)
-                             : fq_stage<STAGES, false>(p, ti, kb, it, ew, sbase + C_::OFF_A,
-                                                       C_::A_BYTES, sbase + C_::OFF_SF,
-                                                       C_::CHUNK_BYTES, bars, abort_flag);
-                    if (!ok) goto roles_done;
+        // K steps in order over this CTA's tiles; the loads of the next step
+        // are issued before the current one is converted, except across a
+        // drain (no loads held in registers beside the accumulator)
+        {
+            constexpr bool BF = FQ == 2;
+            // bf16: one step of loads in flight ahead (16 registers); fp32
+            // (32 registers per step) fetches each step just before its use
+            constexpr bool kAhead = BF;
+            FqIn<BF> nxt;
+            bool have_nxt = false;
+            for (int32_t t = t_first; t < T; t += t_step) {
+                const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
+                const int pre = p.num_kb < STAGES - 1 ? p.num_kb : STAGES - 1;
+                for (int kb = 0; kb <= p.num_kb; ++kb) {
+                    if (kb == pre && have_prev) {
+                        if (!drain_store(prev)) goto roles_done;
+                        have_prev = false;
+                    }
+                    if (kb == p.num_kb) break;
+                    if (!have_nxt) nxt = fq_fetch<BF>(p, ti, kb, ew);
+                    const FqIn<BF> cur = nxt;
+                    have_nxt = false;
+                    if constexpr (kAhead) {
+                        if (kb + 1 < p.num_kb) {
+                            if (!(kb + 1 == pre && have_prev)) {
+                                nxt = fq_fetch<BF>(p, ti, kb + 1, ew);
+                                have_nxt = true;
+                            }
+                        } else if (t + t_step < T) {  // the next tile's first step: no drain before it
+                            nxt = fq_fetch<BF>(
+                                p, get_tile<MODE, BN>(t + t_step, p, row_off, tile_off, rt_off), 0,
+                                ew);
+                            have_nxt = true;
+                        }
+                    }
+                    if (!fq_put<STAGES, BF>(p, cur, ti, kb, it, ew, sbase + C_::OFF_A, C_::A_BYTES,
+                                            sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag))
+                        goto roles_done;
                     ++it;
                 }
+                prev = ti;
+                have_prev = true;
             }
-            prev = ti;
-            have_prev = true;
         }
         if (have_prev) (void)drain_store(prev);
     } else if (warp >= kEpiWarp0) {
@@ -731,7 +789,7 @@ roles_done:
     }
 }
 
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, bool FQ = false>
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0>
 cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
                        cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES, SPLIT>;
@@ -892,8 +950,11 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
     } else if (p.xq != nullptr) {
         // fused activation quantiser (single CTAs only: the caller checks the plan)
         if (kc.pair || split) return cudaErrorInvalidValue;
-        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, true>(maps, p, kc, stream)
-                       : launch_one<kModeGrouped, 256, 1, 4, false, false, true>(maps, p, kc, stream);
+        if (p.xq_bf16)
+            return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 2>(maps, p, kc, stream)
+                           : launch_one<kModeGrouped, 256, 1, 4, false, false, 2>(maps, p, kc, stream);
+        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 1>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 256, 1, 4, false, false, 1>(maps, p, kc, stream);
     } else {
         return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeGrouped, 256, 1, 4, false, false>(maps, p, kc, stream);

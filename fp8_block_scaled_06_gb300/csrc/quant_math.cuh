@@ -113,16 +113,22 @@ __device__ __forceinline__ float pow2_scale(float amax) {
     return __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
+// Eight bf16 values (one 16-byte word, first value lowest) widened exactly
+// to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float4 &a, float4 &b) {
+    a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                    __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+}
+
 // Eight consecutive values of the source at element offset `off` (a multiple
 // of 8), fp32 or bf16 (widened exactly).
 template <bool BF16>
 __device__ __forceinline__ void load8(const void *x, int64_t off, float4 &a, float4 &b) {
     if constexpr (BF16) {
         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + off));
-        a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-        b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
-                        __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+        bf16x8_to_f32(u, a, b);
     } else {
         const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(x) + off);
         a = __ldg(p);

@@ -12,9 +12,9 @@ import bench
 MiB = 1 << 20
 
 
-def _w(out="bf16", experts=None):
+def _w(out="bf16", experts=None, counts=None):
     B = torch.empty((experts, 1, 1)) if experts else torch.empty((1, 1))
-    return SimpleNamespace(out=out, B=B)
+    return SimpleNamespace(out=out, B=B, counts=counts)
 
 
 # name -> (A bytes, B bytes, scale bytes, C bytes), each written out
@@ -97,4 +97,14 @@ def test_algorithmic_bytes_from_tokens():
         assert bench.algorithmic_bytes(bench.WORKLOADS[name], _w(experts=E)) == want
         two = bench.WORKLOADS[name + "_2call"]
         assert bench.algorithmic_bytes(two, _w(experts=E)) == want and not two["fused"]
+
+
+def test_algorithmic_bytes_skip_empty_experts():
+    """Experts without routed rows: their weights and scales are never read."""
+    E, N, K = 8, 14336, 4096
+    counts = [208, 16158, 0, 0, 4, 14, 16384, 0]
+    rows = sum(counts)
+    used = 5
+    want = rows * K + used * N * K + 4 * (rows + used * N) * K // 32 + rows * N * 2 + 4 * E
+    assert bench.algorithmic_bytes(bench.WORKLOADS["moe"], _w(experts=E, counts=counts)) == want
 
