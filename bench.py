@@ -1,14 +1,17 @@
 """FP8 GEMM throughput on GB300: TFLOPS and fraction of the roofline.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload large8192|large4096|skinny|moe|square1024|tensor8192|
+                [--workload large8192|large4096|skinny|moe|square256|square1024|tensor8192|
                             mixed8192|literal8192|mxfp4_8192|mxfp6_8192|nvfp4_8192|
-                            moe_nvfp4]
+                            moe_nvfp4|moe_bf16|moe_bf16_2call|decode_bf16|
+                            decode_bf16_2call]
 
 One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
 scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
 already resident in HBM.  Operand quantisation is data preparation and is
-not timed (it is its own kernel and its own metric).  The default workload is
+not timed (it is its own kernel and its own metric), except in the MoE
+workloads from bf16 tokens (*_bf16*), whose step quantises the routed rows
+(fused into the GEMM, or as a pass of its own).  The default workload is
 the large block-scaled GEMM M=N=K=8192 (1x32 scales along K, N(0,1) with 0.1%
 x50 outliers, bf16 out), the shape the >= 70%-of-peak target is quoted on.
 
@@ -40,6 +43,10 @@ WORKLOADS = {
     "large4096": dict(kind="block", M=4096, N=4096, K=4096, seed=3),
     "skinny": dict(kind="block", M=128, N=4096, K=4096, seed=2),
     "moe": dict(kind="grouped", M=32768, N=14336, K=4096, seed=4),
+    # reduced MoE for profiling captures: 2 experts of the MoE's size, 2048
+    # tokens top-2 (2048 routed rows each), about 0.25 GB on the device
+    "moe_2x2048": dict(kind="grouped", M=4096, N=14336, K=4096, seed=4, experts=2, tokens=2048),
+    "square256": dict(kind="tensor", M=256, N=256, K=256, seed=0),
     "square1024": dict(kind="tensor", M=1024, N=1024, K=1024, seed=1),
     "tensor8192": dict(kind="tensor", M=8192, N=8192, K=8192, seed=3),
     # E4M3 activations x E5M2 weights, block-scaled (the mixed-format path)
@@ -173,7 +180,8 @@ def make_inputs(wl: dict, device):
     import fp8_block_scaled_06_gb300 as fp8g
 
     if wl["kind"] == "grouped":
-        w = synth.moe_grouped(seed=wl["seed"])
+        w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
+                                   tokens=wl.get("tokens", 16384))
         E, N, K = w.B.shape
         qa, sa = fp8g.quantize(w.A.to(device), 32)
         qb, sb = fp8g.quantize(w.B.reshape(E * N, K).to(device), 32)
@@ -193,7 +201,8 @@ def make_inputs(wl: dict, device):
                        tmp_qa=torch.empty((rows, K), dtype=torch.uint8, device=device),
                        tmp_sa=torch.empty((rows, K // 32), dtype=torch.float32, device=device))
     if wl["kind"] == "grouped_nvfp4":
-        w = synth.moe_grouped(seed=wl["seed"])
+        w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
+                                   tokens=wl.get("tokens", 16384))
         qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
         qbs = [fp8g.quantize_nvfp4(w.B[e].to(device)) for e in range(w.B.shape[0])]
         qb, sb, gb = (torch.stack([q[0] for q in qbs]), torch.stack([q[1] for q in qbs]),
@@ -711,7 +720,8 @@ def reference_arm(args, wl, world, rank):
     if wl["kind"] == "grouped_quant":
         w = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])[2]
     elif wl["kind"] in ("grouped", "grouped_nvfp4"):
-        w = synth.moe_grouped(seed=wl["seed"])
+        w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
+                                   tokens=wl.get("tokens", 16384))
     elif wl["kind"] == "tensor":
         w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")
     elif wl["M"] == 128:

@@ -244,21 +244,29 @@ __device__ __forceinline__ bool fq_block(const GemmParams &p, const Tile &ti, in
     return grow < ti.row_end && k0 < p.K;
 }
 
-template <bool BF16>
-__device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, const Tile &ti, int kb, int ew) {
-    FqIn<BF16> in;
-    int64_t grow, k0;
-    in.live = fq_block(p, ti, kb, ew, grow, k0);
-    int64_t src = 0;
-    if (in.live) {
-        src = p.xq_rows != nullptr ? (int64_t)__ldg(p.xq_rows + grow) : grow;
-        if (src < 0 || src >= p.xq_src_rows) {
-            if ((threadIdx.x & 3) == 0) record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)grow);
-            in.live = false;
-        }
+// This lane's source row of tile ti (one index load per tile; the same for
+// every K step): -1 for rows past the expert; a source row outside
+// [0, xq_src_rows) records FP8G_ERR_INVALID_ARG (detail: the routed row) and
+// gives -1.
+__device__ __forceinline__ int64_t fq_source(const GemmParams &p, const Tile &ti, int ew) {
+    const int lane = threadIdx.x & 31;
+    const int64_t grow = (int64_t)ti.row0 + ew * 8 + (lane >> 2);
+    if (grow >= ti.row_end) return -1;
+    const int64_t src = p.xq_rows != nullptr ? (int64_t)__ldg(p.xq_rows + grow) : grow;
+    if (src < 0 || src >= p.xq_src_rows) {
+        if ((lane & 3) == 0) record_error(p, FP8G_ERR_INVALID_ARG, (unsigned)grow);
+        return -1;
     }
+    return src;
+}
+
+template <bool BF16>
+__device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, int64_t src, int kb) {
+    FqIn<BF16> in;
+    const int64_t k0 = (int64_t)kb * kBK + 32 * (threadIdx.x & 3);
+    in.live = src >= 0 && k0 < p.K;
     const uint4 *x = reinterpret_cast<const uint4 *>(
-        static_cast<const uint8_t *>(p.xq) + (src * p.K + k0) * (BF16 ? 2 : 4));
+        static_cast<const uint8_t *>(p.xq) + ((in.live ? src : 0) * p.K + k0) * (BF16 ? 2 : 4));
 #pragma unroll
     for (int i = 0; i < (BF16 ? 4 : 8); ++i)
         in.u[i] = in.live ? __ldg(x + i) : make_uint4(0u, 0u, 0u, 0u);
@@ -276,26 +284,34 @@ __device__ __forceinline__ bool fq_put(const GemmParams &p, const FqIn<BF16> &in
     const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
     const int r = ew * 8 + (lane >> 2);
     const int j = lane & 3;
-    float4 v[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    // values 8q .. 8q + 7 of the block as fp32 (widened again where used, so
+    // that the 32 values never occupy 32 registers at once)
+    auto group = [&](int q, float4 &a, float4 &b) {
         if constexpr (BF16) {
-            bf16x8_to_f32(in.u[q], v[2 * q], v[2 * q + 1]);
+            bf16x8_to_f32(in.u[q], a, b);
         } else {
-            const uint4 a = in.u[2 * q], b = in.u[2 * q + 1];
-            v[2 * q] = make_float4(__uint_as_float(a.x), __uint_as_float(a.y),
-                                   __uint_as_float(a.z), __uint_as_float(a.w));
-            v[2 * q + 1] = make_float4(__uint_as_float(b.x), __uint_as_float(b.y),
-                                       __uint_as_float(b.z), __uint_as_float(b.w));
+            const uint4 x = in.u[2 * q], y = in.u[2 * q + 1];
+            a = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                            __uint_as_float(x.w));
+            b = make_float4(__uint_as_float(y.x), __uint_as_float(y.y), __uint_as_float(y.z),
+                            __uint_as_float(y.w));
         }
-    }
+    };
     float am = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) am = fmaxf(am, absmax8(v[2 * q], v[2 * q + 1]));
+    for (int q = 0; q < 4; ++q) {
+        float4 a, b;
+        group(q, a, b);
+        am = fmaxf(am, absmax8(a, b));
+    }
     const float s = in.live ? pow2_scale<0>(am) : 1.0f;
     uint2 o[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = quant8_pow2<0>(v[2 * q], v[2 * q + 1], s);
+    for (int q = 0; q < 4; ++q) {
+        float4 a, b;
+        group(q, a, b);
+        o[q] = quant8_pow2<0>(a, b, s);
+    }
     const uint4 c0 = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
     const uint4 c1 = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
     if (p.qa_out != nullptr && ti.pn == 0 && in_tile) {
@@ -625,8 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr bool kAhead = BF;
             FqIn<BF> nxt;
             bool have_nxt = false;
+            int64_t src_next = -1;  // the next tile's source row, once fetched ahead
             for (int32_t t = t_first; t < T; t += t_step) {
                 const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
+                const int64_t src = have_nxt ? src_next : fq_source(p, ti, ew);
                 const int pre = p.num_kb < STAGES - 1 ? p.num_kb : STAGES - 1;
                 for (int kb = 0; kb <= p.num_kb; ++kb) {
                     if (kb == pre && have_prev) {
@@ -634,19 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         have_prev = false;
                     }
                     if (kb == p.num_kb) break;
-                    if (!have_nxt) nxt = fq_fetch<BF>(p, ti, kb, ew);
+                    if (!have_nxt) nxt = fq_fetch<BF>(p, src, kb);
                     const FqIn<BF> cur = nxt;
                     have_nxt = false;
                     if constexpr (kAhead) {
                         if (kb + 1 < p.num_kb) {
                             if (!(kb + 1 == pre && have_prev)) {
-                                nxt = fq_fetch<BF>(p, ti, kb + 1, ew);
+                                nxt = fq_fetch<BF>(p, src, kb + 1);
                                 have_nxt = true;
                             }
                         } else if (t + t_step < T) {  // the next tile's first step: no drain before it
-                            nxt = fq_fetch<BF>(
-                                p, get_tile<MODE, BN>(t + t_step, p, row_off, tile_off, rt_off), 0,
-                                ew);
+                            src_next = fq_source(
+                                p, get_tile<MODE, BN>(t + t_step, p, row_off, tile_off, rt_off), ew);
+                            nxt = fq_fetch<BF>(p, src_next, 0);
                             have_nxt = true;
                         }
                     }
