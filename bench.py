@@ -43,6 +43,9 @@ WORKLOADS = {
     "large4096": dict(kind="block", M=4096, N=4096, K=4096, seed=3),
     "skinny": dict(kind="block", M=128, N=4096, K=4096, seed=2),
     "moe": dict(kind="grouped", M=32768, N=14336, K=4096, seed=4),
+    # eight independent skinny products (128 x 4096 x 4096 each, the skinny
+    # recipe) in one grouped call: the skinny shape batched into one launch
+    "skinny_x8": dict(kind="grouped", M=1024, N=4096, K=4096, seed=2, batch=8),
     # reduced MoE for profiling captures: 2 experts of the MoE's size, 2048
     # tokens top-2 (2048 routed rows each), about 0.25 GB on the device
     "moe_2x2048": dict(kind="grouped", M=4096, N=14336, K=4096, seed=4, experts=2, tokens=2048),
@@ -180,8 +183,9 @@ def make_inputs(wl: dict, device):
     import fp8_block_scaled_06_gb300 as fp8g
 
     if wl["kind"] == "grouped":
-        w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
-                                   tokens=wl.get("tokens", 16384))
+        w = (synth.skinny_batch(wl["batch"], seed=wl["seed"]) if "batch" in wl else
+             synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
+                               tokens=wl.get("tokens", 16384)))
         E, N, K = w.B.shape
         qa, sa = fp8g.quantize(w.A.to(device), 32)
         qb, sb = fp8g.quantize(w.B.reshape(E * N, K).to(device), 32)
@@ -202,7 +206,7 @@ def make_inputs(wl: dict, device):
                        tmp_sa=torch.empty((rows, K // 32), dtype=torch.float32, device=device))
     if wl["kind"] == "grouped_nvfp4":
         w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
-                                   tokens=wl.get("tokens", 16384))
+                              tokens=wl.get("tokens", 16384))
         qa, sa, ga = fp8g.quantize_nvfp4(w.A.to(device))
         qbs = [fp8g.quantize_nvfp4(w.B[e].to(device)) for e in range(w.B.shape[0])]
         qb, sb, gb = (torch.stack([q[0] for q in qbs]), torch.stack([q[1] for q in qbs]),
@@ -719,9 +723,11 @@ def reference_arm(args, wl, world, rank):
     import synth
     if wl["kind"] == "grouped_quant":
         w = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])[2]
+    elif "batch" in wl:
+        w = synth.skinny_batch(wl["batch"], seed=wl["seed"])
     elif wl["kind"] in ("grouped", "grouped_nvfp4"):
         w = synth.moe_grouped(seed=wl["seed"], experts=wl.get("experts", 8),
-                                   tokens=wl.get("tokens", 16384))
+                              tokens=wl.get("tokens", 16384))
     elif wl["kind"] == "tensor":
         w = synth.square_tensor(wl["M"], seed=wl["seed"], out="f32" if wl["M"] == 1024 else "bf16")
     elif wl["M"] == 128:

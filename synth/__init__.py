@@ -186,3 +186,15 @@ def moe_tokens(seed: int = 4, experts: int = 8, tokens: int = 16384, N: int = 14
     idx = (torch.arange(w.M) % tokens).to(torch.int32)
     return X, idx, w
 
+
+def skinny_batch(count: int = 8, seed: int = 2, M: int = 128, N: int = 4096, K: int = 4096,
+                 out: str = "bf16") -> Workload:
+    """`count` independent skinny products (the skinny_block recipe, problem i
+    drawn with seed + i), laid out as a grouped workload: A rows of problem i
+    at [i M, (i + 1) M), its B as B[i], counts M each."""
+    parts = [skinny_block(M, N, K, seed + i, out) for i in range(count)]
+    A = torch.cat([w.A for w in parts])
+    B = torch.stack([w.B for w in parts])
+    counts = np.full(count, M, dtype=np.int32)
+    return Workload(f"skinny{count}x{M}x{N}x{K}_batch", count * M, N, K, True, out, A, B, counts)
+

@@ -39,7 +39,8 @@ def _run(name):
     w, t = bench.make_inputs(wl, torch.device("cuda"))
     assert fp8g.fp8_gemm_status()[0] == 0
     dt = torch.float32 if w.out == "f32" else torch.bfloat16
-    C = torch.full((t["qa"].shape[0], wl["N"]), float("nan"), dtype=dt, device="cuda")
+    rows = (t["qa"] if "qa" in t else t["tmp_qa"]).shape[0]
+    C = torch.full((rows, wl["N"]), float("nan"), dtype=dt, device="cuda")
     bench.run_once(fp8g, wl, w, t, C, torch.cuda.current_stream())
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"status {st} detail {detail}"
@@ -127,3 +128,54 @@ def test_workload_moe_nvfp4_sampled():
         ref, bound, _ = oracle.gemm_nvfp4_sample(qa_o[r0:r1], qb_o, sa_o[r0:r1], sb_o, ga_o, gb_o,
                                                  pi[sel] - r0, pj[sel], oracle.OUT_BF16)
         assert_within(C[pi[sel], pj[sel]], ref, bound, f"moe_nvfp4 expert {e}")
+
+
+def _grouped_sampled(name, qa_o, sa_o, qb_o, sb_o, counts, C, seed):
+    rows = int(counts.sum())
+    N = qb_o.shape[1]
+    offs = oracle.grouped_offsets(counts)
+    pi, pj = _points(rows, N, seed)
+    expert = np.searchsorted(offs, pi, side="right") - 1
+    for e in np.unique(expert):
+        sel = np.flatnonzero(expert == e)
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        ref, bound, _ = oracle.gemm_sample(qa_o[r0:r1], qb_o[e], sa_o[r0:r1], sb_o[e],
+                                           True, pi[sel] - r0, pj[sel], oracle.OUT_BF16)
+        assert_within(C[pi[sel], pj[sel]], ref, bound, f"{name} problem {e}")
+
+
+def test_workload_skinny_x8_sampled():
+    """Eight independent skinny products (128 x 4096 x 4096, the skinny
+    recipe) in one grouped call: every code and scale bit-exact, sampled
+    outputs of every product against the oracle."""
+    wl, w, t, C = _run("skinny_x8")
+    E, N, K = w.B.shape
+    qa_o, sa_o = oracle.quantize_block32(w.A.numpy())
+    qb_o, sb_o = oracle.quantize_block32(w.B.reshape(E * N, K).numpy())
+    _same(t["qa"], qa_o, "skinny_x8 A codes")
+    _same(t["sa"], sa_o, "skinny_x8 A scales")
+    _same(t["qb"], qb_o, "skinny_x8 B codes")
+    _same(t["sb"], sb_o, "skinny_x8 B scales")
+    _grouped_sampled("skinny_x8", qa_o, sa_o, qb_o.reshape(E, N, K), sb_o.reshape(E, N, K // 32),
+                     w.counts, C, 6)
+
+
+def test_workload_decode_bf16_sampled():
+    """The decode-shaped MoE from bf16 tokens as the bench runs it, through
+    the one-call (fused quantiser) and the two-call paths: the same bits, and
+    sampled outputs against the oracle's quantisation of the gathered tokens
+    and its GEMM."""
+    import synth
+    wl, w, t, C = _run("decode_bf16")
+    wl2, _, t2, C2 = _run("decode_bf16_2call")
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+    X, idx, _ = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])
+    qa_o, sa_o = oracle.quantize_block32(X.to(torch.bfloat16).float().numpy()[idx.numpy()])
+    _same(t2["tmp_qa"], qa_o, "decode A codes (two calls)")
+    _same(t2["tmp_sa"], sa_o, "decode A scales (two calls)")
+    E, N, K = w.B.shape
+    qb_o, sb_o = oracle.quantize_block32(w.B.reshape(E * N, K).numpy())
+    _same(t["qb"], qb_o, "decode B codes")
+    _grouped_sampled("decode_bf16", qa_o, sa_o, qb_o.reshape(E, N, K), sb_o.reshape(E, N, K // 32),
+                     w.counts, C, 7)
+
