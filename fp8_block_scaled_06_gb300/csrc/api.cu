@@ -309,6 +309,68 @@ cudaError_t timed_launch(cudaStream_t stream, F &&launch) {
     return e;
 }
 
+// Literal-scale GEMM through TF32: A' = TF32(dec(A) sfa), B' likewise (one
+// HBM-bound pass each into a stream-ordered temporary from the library pool,
+// fp32 words), then C = out(act(A' B'^T + bias)) on the pair kernel's TF32
+// mode.  Each operand value is rounded once to TF32's 11 significant bits
+// (relative error <= 2^-11), so every product is within 2^-10 of the exact
+// one: inside the block-scaled tolerance 2^-8 sum |sa a| |sb b| + 1 ulp.
+static fp8g_status run_tf32(const uint8_t *A, const uint8_t *B, const float *sfa, const float *sfb,
+                     void *C, int out, int a_fmt, int b_fmt, const float *bias, int act,
+                     int64_t M, int64_t N, int64_t K, const KernelChoice &kc, const DevInfo &di,
+                     cudaStream_t stream) {
+    cudaMemPool_t pool;
+    fp8g_status st = scale_pool(di.dev, pool);
+    if (st != FP8G_OK) return st;
+    const size_t bytesA = ((size_t)M * (size_t)K * 4 + 255) / 256 * 256;
+    const size_t bytesB = (size_t)N * (size_t)K * 4;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytesA + bytesB, pool, stream) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    float *tA = static_cast<float *>(ws);
+    float *tB = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + bytesA);
+    cudaError_t e = launch_dequant_tf32(A, sfa, M, K, a_fmt, tA, di.num_sms, stream);
+    if (e == cudaSuccess) e = launch_dequant_tf32(B, sfb, N, K, b_fmt, tB, di.num_sms, stream);
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_kb = (int32_t)((K + 31) / 32);  // 32 fp32 values per 128-byte stage row
+    p.npm = (int32_t)((M + kc.BM - 1) / kc.BM);
+    p.npn = (int32_t)((N + kc.BN - 1) / kc.BN);
+    p.T = (int64_t)p.npm * p.npn;
+    p.split = 1;
+    p.kb_per_split = p.num_kb;
+    p.C = C;
+    p.status = di.status;
+    p.timeout_ns = timeout_ns();
+    p.f4 = 3;
+    p.bias = bias;
+    p.act = act;
+    p.c_rows = M;
+    p.st32 = aligned(C, 32) && (N * (out == FP8G_OUT_F32 ? 4 : 2)) % 32 == 0;
+    GemmMaps maps;
+    if (e == cudaSuccess) {
+        const uint64_t dA[2] = {(uint64_t)K, (uint64_t)M};
+        const uint64_t dB[2] = {(uint64_t)K, (uint64_t)N};
+        const uint32_t bA[2] = {32u, (uint32_t)kBM};
+        const uint32_t bB[2] = {32u, (uint32_t)kc.b_rows};
+        if (tmap_encode(tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, 2, dA, bA,
+                        CU_TENSOR_MAP_SWIZZLE_128B, di.dev, maps.A) != FP8G_OK ||
+            tmap_encode(tB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, 2, dB, bB,
+                        CU_TENSOR_MAP_SWIZZLE_128B, di.dev, maps.B) != FP8G_OK)
+            e = cudaErrorInvalidValue;
+        maps.SA = maps.A;
+        maps.SB = maps.A;
+    }
+    if (e == cudaSuccess)
+        e = timed_launch(stream, [&] {
+            return launch_gemm(kModeTensor, out == FP8G_OUT_F32, maps, p, kc, stream);
+        });
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return (e == cudaSuccess && ef == cudaSuccess) ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
 fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, const float *sb,
                      void *C, int out, int64_t M, int64_t N, int64_t K, const int32_t *counts,
                      int32_t E, int32_t *offsets_out, int32_t *tile_map_out, cudaStream_t stream,
@@ -641,6 +703,15 @@ fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const flo
     if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
     DevInfo di;
     if ((st = device_info(di)) != FP8G_OK) return st;
+    // At least a wave of 256 x 256 tiles with 1-byte codes: fold each scale
+    // into its operand once (dequantise to TF32) and run the TF32 tensor-core
+    // GEMM on CTA pairs, instead of promoting every K block's partial on CUDA
+    // cores (two fp32 operations per output per 32-wide K block)
+    const KernelChoice kc = choose_kernel(kModeTensor, M, N, K, di.num_sms);
+    if (kc.pair && (a_fmt == FP8G_E4M3 || a_fmt == FP8G_E5M2) &&
+        (b_fmt == FP8G_E4M3 || b_fmt == FP8G_E5M2))
+        return run_tf32(static_cast<const uint8_t *>(A), static_cast<const uint8_t *>(B), sfa, sfb,
+                        C, out, a_fmt, b_fmt, bias, act, M, N, K, kc, di, stream);
     GemmParams p{};
     p.M = M;
     p.N = N;

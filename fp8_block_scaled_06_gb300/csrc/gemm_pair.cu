@@ -45,6 +45,9 @@
 // columns per group (48 per stage), which leaves room for 5 stages.  The
 // output is scaled by the product of the two fp32 tensor scales, per expert
 // on the grouped GEMM (each expert's B has its own).
+// F4 = 3 (per-tensor mode, TF32): fp32 operands (32 K values per 128-byte
+// row of a stage) through kind::tf32 MMAs, alpha = 1: the literal-scale GEMM
+// after its operands were dequantised with their fp32 block scales.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -78,7 +81,8 @@ constexpr int kSfbBytes = 1024;  // B's two 128-row chunks
 template <int MODE, int F4>
 struct PairCfg {
     static constexpr bool kBlock = MODE != kModeTensor;
-    static_assert(kBlock || F4 == 0, "FP4-rate MMAs are block-scaled");
+    static_assert(kBlock || F4 == 0 || F4 == 3, "FP4-rate MMAs are block-scaled");
+    static_assert(F4 != 3 || !kBlock, "TF32 operands carry their scales (per-tensor mode)");
     static constexpr int STAGES = F4 == 2 ? 5 : 6;
     // K groups of packed scales per stage: 128-wide (FP8, MXFP4) or 64-wide (NVFP4)
     static constexpr int G = F4 == 2 ? 4 : F4 == 1 ? 2 : 1;
@@ -327,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             int32_t lt = 0;
-            const uint32_t idesc = ptx::idesc_f8(2 * kBM, kPairBN) | p.ab_fmt;
+            const uint32_t idesc = F4 == 3 ? ptx::idesc_tf32(2 * kBM, kPairBN)
+                                           : ptx::idesc_f8(2 * kBM, kPairBN) | p.ab_fmt;
             for (int32_t t = t_first; t < T; t += t_step, ++lt) {
                 const int acc = lt % PC::NUM_ACC;
                 const uint32_t acc_par = (uint32_t)((lt / PC::NUM_ACC) & 1);
@@ -376,6 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                ptx::desc_kmajor_sw128(b0 + k * 32),
                                                ptx::idesc_mxf8(2 * kBM, kPairBN, (uint32_t)k) | p.ab_fmt, sf,
                                                sf + 8, (kb | k) != 0 ? 1u : 0u);
+                    } else if constexpr (F4 == 3) {
+                        // TF32: 32 fp32 K values per 128-byte row, four K = 8 MMAs
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            ptx::mma_tf32_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                               ptx::desc_kmajor_sw128(b0 + k * 32), idesc,
+                                               (kb | k) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < kBK / 32; ++k)
@@ -440,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int col0 = (ew >> 2) * kCW;
         float alpha = 1.0f;
-        if constexpr (MODE == kModeTensor) alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        // (TF32 operands already carry their scales)
+        if constexpr (MODE == kModeTensor && F4 != 3) alpha = __fmul_rn(p.sa[0], p.sb[0]);
         if constexpr (F4 == 2) alpha = __fmul_rn(p.ga[0], p.gb[0]);  // NVFP4 tensor scales
         int32_t lt = 0;
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
@@ -561,6 +574,9 @@ cudaError_t launch_gemm_pair(int mode, bool out_f32, const GemmMaps &maps, const
     if (p.f4 == 1 && mode == kModeGrouped)
         return out_f32 ? launch_pair<kModeGrouped, true, 1>(maps, p, grid, stream)
                        : launch_pair<kModeGrouped, false, 1>(maps, p, grid, stream);
+    if (p.f4 == 3 && mode == kModeTensor)
+        return out_f32 ? launch_pair<kModeTensor, true, 3>(maps, p, grid, stream)
+                       : launch_pair<kModeTensor, false, 3>(maps, p, grid, stream);
     if (p.f4) return cudaErrorInvalidValue;
     if (mode == kModeBlock)
         return out_f32 ? launch_pair<kModeBlock, true>(maps, p, grid, stream)

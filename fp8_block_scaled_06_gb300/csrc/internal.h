@@ -51,7 +51,8 @@ struct GemmParams {
     // E2M1 x E2M1 block-scaled on CTA pairs at the FP4 rate (kind::mxf4):
     // operands loaded as dense bytes, 256 K elements per stage, num_kb = K /
     // 256, the packed scale arrays holding 2 * num_kb chunks per row tile.
-    int32_t f4;               // 1: MXFP4 (kind::mxf4); 2: NVFP4 (kind::mxf4nvf4, 1x16 E4M3 scales)
+    int32_t f4;               // 1: MXFP4 (kind::mxf4); 2: NVFP4 (kind::mxf4nvf4, 1x16 E4M3
+                              // scales); 3: TF32 operands (kind::tf32, per-tensor mode, alpha 1)
     const float *ga, *gb;     // NVFP4: the tensors' fp32 scales (epilogue alpha = fl32(ga gb))
     int32_t st32;             // epilogue: 32-byte stores (C 32-byte aligned, rows multiples of 32 B)
     const float *bias;     // fused epilogue: fp32 [N] (grouped [E, N]) or null
@@ -163,7 +164,11 @@ size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z);
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
                                int32_t E, unsigned int *status, cudaStream_t s);
 
-// quant.cu
+// quant.cu: A [rows, K] FP8 codes (fmt FP8G_E4M3 / FP8G_E5M2) with fp32 1x32
+// scales s [rows, K/32] -> out [rows, K] fp32 = TF32(fl32(dec(a) s)) (round to
+// nearest, ties away: exact TF32 values).
+cudaError_t launch_dequant_tf32(const uint8_t *a, const float *s, int64_t rows, int64_t K, int fmt,
+                                float *out, int num_sms, cudaStream_t stream);
 // quant.cu: output row r quantises source row rows[r] (rows null: row r) of
 // x [x_rows, cols] (fp32, or bf16 if in_bf16); block 0 per-tensor or 32; fmt
 // FP8G_E4M3 / FP8G_E5M2.  Bad row indices record FP8G_ERR_INVALID_ARG.

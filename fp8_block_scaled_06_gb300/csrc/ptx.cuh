@@ -371,6 +371,18 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// kind::tf32: fp32 operands in shared memory read as TF32 (8 bits of exponent,
+// 10 of mantissa), K = 8 per instruction (32 bytes of a K-major row, the
+// descriptor step of the FP8 kinds).
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // kind::mxf4: dense 4-bit E2M1 operands (two codes per byte in shared memory,
 // the first in the low nibble), K = 64 per instruction, two UE8M0 scales per
 // row (scale_vec::2X: the bytes sf_id and sf_id + 1 of the row's word).
@@ -481,6 +493,13 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *o) {
 
 __host__ __device__ constexpr uint32_t idesc_f8(uint32_t M, uint32_t N) {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::tf32: fp32 accumulator (bits 4-5 = 1), A and
+// B TF32 (format 2 of the 16-bit/TF32 kinds, bits 7-9 and 10-12), both
+// K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block_scale: B scale-factor byte id in

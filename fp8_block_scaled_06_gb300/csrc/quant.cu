@@ -254,6 +254,58 @@ __global__ void __launch_bounds__(kQThreads) quant_nvfp4_kernel(RowMap m, int64_
 
 __global__ void finish_nvfp4_kernel(float *slot) { *slot = nvfp4_g(slot); }
 
+// ------------------------------------------------- literal scales -> TF32
+// Value of an FP8 code from its bit fields: E4M3 (bias 7, subnormals m 2^-9,
+// S.1111.111 NaN) or E5M2 (bias 15, subnormals m 2^-16, exponent 31: inf for
+// m = 0, else NaN).
+template <int FMT>
+__device__ __forceinline__ float fp8_value(uint32_t c) {
+    const uint32_t sign = (c & 0x80u) << 24;
+    if constexpr (FMT == 0) {
+        const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+        if (e == 15u && m == 7u) return __uint_as_float(sign | 0x7FC00000u);
+        if (e == 0u) return __uint_as_float(sign | __float_as_uint((float)m * 0.001953125f));
+        return __uint_as_float(sign | (e + 120u) << 23 | m << 20);
+    } else {
+        const uint32_t e = (c >> 2) & 31u, m = c & 3u;
+        if (e == 31u) return __uint_as_float(sign | (m == 0u ? 0x7F800000u : 0x7FC00000u));
+        if (e == 0u) return __uint_as_float(sign | __float_as_uint((float)m * 1.52587890625e-5f));
+        return __uint_as_float(sign | (e + 112u) << 23 | m << 21);
+    }
+}
+
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// out = TF32(fl32(dec(a) s)) for 8 consecutive codes per thread (one 8-byte
+// load, two 16-byte stores; the 8 share one 1x32 block scale).  HBM-bound.
+template <int FMT>
+__global__ void __launch_bounds__(256) dequant_tf32_kernel(const uint8_t *__restrict__ a,
+                                                          const float *__restrict__ s,
+                                                          int64_t rows, int64_t K,
+                                                          float *__restrict__ out) {
+    const int64_t gpr = K / 8;  // groups of 8 per row
+    const int64_t n = rows * gpr;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = g / gpr, c = g - r * gpr;
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(a) + g);
+        const float sc = __ldg(s + r * (K / 32) + c / 4);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t code = ((i < 4 ? q.x : q.y) >> (8 * (i & 3))) & 0xFFu;
+            v[i] = to_tf32(__fmul_rn(fp8_value<FMT>(code), sc));
+        }
+        float4 *o = reinterpret_cast<float4 *>(out) + 2 * g;
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
 }  // namespace
 
 namespace {
@@ -325,6 +377,20 @@ cudaError_t launch_quantize_rows(const void *x, int in_bf16, int64_t x_rows, int
                        : launch_rows<1, false>(m, n_rows, block, q, scales, num_sms, s);
     return in_bf16 ? launch_rows<0, true>(m, n_rows, block, q, scales, num_sms, s)
                    : launch_rows<0, false>(m, n_rows, block, q, scales, num_sms, s);
+}
+
+cudaError_t launch_dequant_tf32(const uint8_t *a, const float *s, int64_t rows, int64_t K, int fmt,
+                                float *out, int num_sms, cudaStream_t stream) {
+    const int64_t n = rows * (K / 8);
+    if (n == 0) return cudaSuccess;
+    const int64_t cap = (int64_t)num_sms * 8;
+    const int64_t want = (n + 255) / 256;
+    const unsigned blocks = (unsigned)(want < cap ? want : cap);
+    if (fmt == FP8G_E5M2)
+        dequant_tf32_kernel<1><<<blocks, 256, 0, stream>>>(a, s, rows, K, out);
+    else
+        dequant_tf32_kernel<0><<<blocks, 256, 0, stream>>>(a, s, rows, K, out);
+    return cudaGetLastError();
 }
 
 }  // namespace fp8g

@@ -110,3 +110,44 @@ def test_promote_rejects_k_not_multiple_of_128():
         fp8g.fp8_gemm_blockscaled_promote(q, torch.zeros(128, 96, dtype=torch.uint8, device="cuda"),
                                           s, s, C, 0, 0, 0, None, 0, 128, 128, 96)
     assert e.value.status == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("fa,fb,out", [(0, 1, "f32"), (1, 0, "bf16")])
+def test_promote_tf32_route_full(fa, fb, out):
+    """Shapes with a wave of 256 x 256 tiles take the TF32 route (operands
+    dequantised with their fp32 scales, then the TF32 tensor-core GEMM on CTA
+    pairs): ragged M and N, signed arbitrary scales, E4M3 x E5M2 either way,
+    bias + GELU; the whole output against the oracle."""
+    M, N, K = 2000, 2600, 640
+    assert fp8g.fp8g_gemm_plan(0, M, N, K)["BM"] == 256          # the pair plan
+    rng = np.random.default_rng(fa * 2 + fb)
+    qa_o = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    qb_o = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    for q, f in ((qa_o, fa), (qb_o, fb)):
+        if f == 0:
+            q[(q & 0x7F) == 0x7F] = 0x30                            # no E4M3 NaN
+        else:
+            q[(q & 0x7C) == 0x7C] = 0x31                            # no E5M2 inf / NaN
+    sa_o = (rng.normal(size=(M, K // 32)) * 1e-2).astype(np.float32)
+    sb_o = (rng.normal(size=(N, K // 32)) * 3e-3).astype(np.float32)
+    bias = rng.normal(size=N).astype(np.float32)
+    C = _run(torch.from_numpy(qa_o).cuda(), torch.from_numpy(sa_o).cuda(),
+             torch.from_numpy(qb_o).cuda(), torch.from_numpy(sb_o).cuda(), M, N, K, out, fa, fb,
+             bias, fp8g.FP8G_ACT_GELU)
+    ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, True,
+                                oracle.OUT_F32 if out == "f32" else oracle.OUT_BF16, a_fmt=fa,
+                                b_fmt=fb, bias=bias, act_kind=oracle.ACT_GELU)
+    assert_within(C, ref, bound, f"promote TF32 route {fa}x{fb}")
+
+
+def test_promote_tf32_route_nan_propagates():
+    """A NaN code on the TF32 route gives NaN exactly in its row / column."""
+    M, N, K = 4096, 2048, 256
+    qa = torch.full((M, K), 0x38, dtype=torch.uint8, device="cuda")   # 1.0
+    qb = torch.full((N, K), 0x38, dtype=torch.uint8, device="cuda")
+    qa[17, 100] = 0x7F                                                 # NaN
+    s = torch.full((M, K // 32), 0.5, device="cuda")
+    sb = torch.full((N, K // 32), 0.25, device="cuda")
+    C = _run(qa, s, qb, sb, M, N, K, "f32")
+    assert np.isnan(C[17]).all() and not np.isnan(np.delete(C, 17, axis=0)).any()
+    assert (np.delete(C, 17, axis=0) == K * 0.5 * 0.25).all()          # exact sums
