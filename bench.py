@@ -4,7 +4,7 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload large8192|large4096|skinny|moe|square256|square1024|tensor8192|
                             mixed8192|literal8192|mxfp4_8192|mxfp6_8192|nvfp4_8192|
                             moe_nvfp4|moe_bf16|moe_bf16_2call|decode_bf16|
-                            decode_bf16_2call]
+                            decode_bf16_fused|decode_bf16_2call|skinny_x8|moe_2x2048]
 
 One step = one GEMM call (the whole hot path: tile scheduling, TMA ring,
 scale staging, tcgen05 MMA, epilogue) over one batch of synthetic input
@@ -65,18 +65,21 @@ WORKLOADS = {
     # the MoE workload in NVFP4 (each expert's weight with its own tensor scale)
     "moe_nvfp4": dict(kind="grouped_nvfp4", M=32768, N=14336, K=4096, seed=4, a_fmt=2, b_fmt=2),
     # MoE from bf16 token activations, the routed rows' 1x32 E4M3 quantisation
-    # inside the timed step: fp8_grouped_gemm_quant (one call) against
-    # fp8g_quantize_rows + fp8_grouped_gemm (two calls).  At the full MoE size
-    # the call runs the two steps itself (256-row tiles); with 128 tokens
-    # (decoding: 256 routed rows) it fuses the quantiser into the GEMM.
+    # inside the timed step: fp8_grouped_gemm_quant (one call; "fused": with
+    # FP8G_QUANT_FUSED, the quantiser inside the GEMM kernel where the plan
+    # runs single-CTA tiles) against fp8g_quantize_rows + fp8_grouped_gemm
+    # (two calls).  The full MoE size runs 256-row tiles (never fused);
+    # 128 tokens (decoding: 256 routed rows) run single-CTA tiles.
     "moe_bf16": dict(kind="grouped_quant", M=32768, N=14336, K=4096, seed=4, tokens=16384,
-                     fused=True),
+                     path="1call"),
     "moe_bf16_2call": dict(kind="grouped_quant", M=32768, N=14336, K=4096, seed=4,
-                           tokens=16384, fused=False),
+                           tokens=16384, path="2call"),
     "decode_bf16": dict(kind="grouped_quant", M=256, N=14336, K=4096, seed=4, tokens=128,
-                        fused=True),
+                        path="1call"),
+    "decode_bf16_fused": dict(kind="grouped_quant", M=256, N=14336, K=4096, seed=4, tokens=128,
+                              path="fused"),
     "decode_bf16_2call": dict(kind="grouped_quant", M=256, N=14336, K=4096, seed=4, tokens=128,
-                              fused=False),
+                              path="2call"),
 }
 FMT_NAMES = ["e4m3", "e5m2", "e2m1", "e2m3", "e3m2"]
 # bytes per element of each format in memory (E2M1: two codes per byte; FP6:
@@ -268,10 +271,11 @@ def run_once(fp8g, wl, w, t, C, stream):
     if wl["kind"] == "grouped_quant":
         E, N, K = t["qb"].shape
         rows = t["tmp_qa"].shape[0]
-        if wl["fused"]:
+        if wl["path"] != "2call":
             fp8g.fp8_grouped_gemm_quant(t["X"], fp8g.FP8G_IN_BF16, t["X"].shape[0], t["idx"],
                                         t["qb"], t["sb"], C, out, fp8g.FP8G_E4M3, None,
                                         fp8g.FP8G_ACT_NONE, t["counts"], E, N, K, rows,
+                                        flags=fp8g.FP8G_QUANT_FUSED if wl["path"] == "fused" else 0,
                                         stream=stream)
         else:
             fp8g.fp8g_quantize_rows(t["X"], fp8g.FP8G_IN_BF16, t["X"].shape[0], K, t["idx"], rows,
@@ -339,7 +343,8 @@ def launches_per_call(fp8g, wl) -> int:
         return 2
     if wl["kind"] == "grouped_quant":
         # quantiser (unless fused into the GEMM), B's scale packing, GEMM
-        fused = wl["fused"] and fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128
+        fused = (wl["path"] == "fused" and
+                 fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128)
         return 2 if fused else 3
     if wl.get("literal"):
         return 1
@@ -500,9 +505,11 @@ def config_of(name: str, wl: dict, out: str, world: int) -> dict:
                        {"block": "1x32 along K, power of two",
                         "grouped": "1x32 along K, power of two",
                         "grouped_quant": "1x32 along K, power of two; A quantised from bf16 "
-                                         "tokens inside the step" + (
-                                             " (one call)" if wl.get("fused") else
-                                             " (two calls)"),
+                                         "tokens inside the step" + {
+                                             "1call": " (one call, two kernels)",
+                                             "fused": " (one call, quantiser fused into the "
+                                                      "GEMM kernel)",
+                                             "2call": " (two calls)"}.get(wl.get("path"), ""),
                         "nvfp4": "1x16 along K, E4M3, and fp32 per tensor (NVFP4)",
                         "grouped_nvfp4": "1x16 along K, E4M3, fp32 for A and per "
                                          "expert weight (NVFP4)",

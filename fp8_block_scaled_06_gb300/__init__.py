@@ -41,6 +41,7 @@ FP8G_ACT_NONE = 0
 FP8G_ACT_RELU = 1
 FP8G_ACT_GELU = 2
 FP8G_MAX_EXPERTS = 64
+FP8G_QUANT_FUSED = 1
 
 # Every symbol include/fp8gemm.h declares.
 EXPORTS = (
@@ -130,7 +131,7 @@ def load():
                                                  i32, i64, i64, i64, P, i64, P, P, P]
         lib.fp8_grouped_gemm_quant.restype = st
         lib.fp8_grouped_gemm_quant.argtypes = [P, i32, i64, P, P, P, P, ctypes.c_int, i32, P, i32,
-                                               P, i32, i64, i64, i64, P, i64, P, P, P, P, P]
+                                               P, i32, i64, i64, i64, P, i64, P, P, P, P, i32, P]
         lib.fp8_gemm_blockscaled_promote.restype = st
         lib.fp8_gemm_blockscaled_promote.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, i32,
                                                      i64, i64, i64, P]
@@ -294,15 +295,16 @@ def fp8_grouped_gemm_scatter(A, B, sfa, sfb, C, out: int, a_fmt: int, b_fmt: int
 def fp8_grouped_gemm_quant(X, x_dtype: int, x_rows: int, rows, B, sfb, C, out: int, b_fmt: int,
                            bias, act: int, counts, E: int, N: int, K: int, total_rows: int,
                            c_row_of=None, c_rows: int = 0, qa_out=None, sfa_out=None,
-                           offsets_out=None, tile_map_out=None, stream=None):
+                           offsets_out=None, tile_map_out=None, flags: int = 0, stream=None):
     """Grouped GEMM from fp32 / bf16 activations: gather, 1x32 E4M3 quantisation
-    (inside the GEMM kernel when the plan runs single-CTA tiles) and the
-    grouped GEMM with bias / activation and row scatter."""
+    (inside the GEMM kernel with flags FP8G_QUANT_FUSED when the plan runs
+    single-CTA tiles) and the grouped GEMM with bias / activation and row
+    scatter."""
     _check(load().fp8_grouped_gemm_quant(_ptr(X), int(x_dtype), x_rows, _ptr(rows), _ptr(B),
                                          _ptr(sfb), _ptr(C), int(out), int(b_fmt), _ptr(bias),
                                          int(act), _ptr(counts), int(E), N, K, total_rows,
                                          _ptr(c_row_of), c_rows, _ptr(qa_out), _ptr(sfa_out),
-                                         _ptr(offsets_out), _ptr(tile_map_out),
+                                         _ptr(offsets_out), _ptr(tile_map_out), int(flags),
                                          _stream(stream)), "fp8_grouped_gemm_quant")
 
 

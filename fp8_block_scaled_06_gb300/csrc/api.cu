@@ -885,8 +885,9 @@ fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_row
                                    const int32_t *counts, int32_t E, int64_t N, int64_t K,
                                    int64_t total_rows, const int32_t *c_row_of, int64_t c_rows,
                                    uint8_t *qa_out, float *sfa_out, int32_t *offsets_out,
-                                   int32_t *tile_map_out, cudaStream_t stream) {
+                                   int32_t *tile_map_out, int32_t flags, cudaStream_t stream) {
     if (x_dtype != FP8G_IN_F32 && x_dtype != FP8G_IN_BF16) return FP8G_ERR_INVALID_ARG;
+    if (flags != 0 && flags != FP8G_QUANT_FUSED) return FP8G_ERR_INVALID_ARG;
     if ((qa_out == nullptr) != (sfa_out == nullptr)) return FP8G_ERR_INVALID_ARG;
     if (total_rows > 0) {
         if (X == nullptr || x_rows < 1) return FP8G_ERR_INVALID_ARG;
@@ -909,7 +910,7 @@ fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_row
     DevInfo di;
     if ((st = device_info(di)) != FP8G_OK) return st;
     const KernelChoice kc = choose_kernel(kModeGrouped, total_rows, N, K, di.num_sms);
-    if (total_rows > 0 && !kc.pair) {
+    if (flags == FP8G_QUANT_FUSED && total_rows > 0 && !kc.pair) {
         // one kernel: the GEMM quantises each tile of A it multiplies
         const FusedQuant fq{X, x_dtype == FP8G_IN_BF16 ? 1 : 0, rows, x_rows, qa_out, sfa_out};
         return run_gemm(kModeGrouped, nullptr, B, nullptr, sfb, C, out, total_rows, N, K, counts,

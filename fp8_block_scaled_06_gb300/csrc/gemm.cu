@@ -261,8 +261,7 @@ __device__ __forceinline__ int64_t fq_source(const GemmParams &p, const Tile &ti
 }
 
 template <bool BF16>
-__device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, int64_t src, int kb,
-                                               uint64_t pol) {
+__device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, int64_t src, int kb) {
     FqIn<BF16> in;
     const int64_t k0 = (int64_t)kb * kBK + 32 * (threadIdx.x & 3);
     in.live = src >= 0 && k0 < p.K;
@@ -270,7 +269,7 @@ __device__ __forceinline__ FqIn<BF16> fq_fetch(const GemmParams &p, int64_t src,
         static_cast<const uint8_t *>(p.xq) + ((in.live ? src : 0) * p.K + k0) * (BF16 ? 2 : 4));
 #pragma unroll
     for (int i = 0; i < (BF16 ? 4 : 8); ++i)
-        in.u[i] = in.live ? ptx::ldg_hint(x + i, pol) : make_uint4(0u, 0u, 0u, 0u);
+        in.u[i] = in.live ? __ldg(x + i) : make_uint4(0u, 0u, 0u, 0u);
     return in;
 }
 
@@ -465,7 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ===== TMA producer: A, B (and the packed scale chunks) per stage =====
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            const uint64_t b_pol = FQ != 0 ? ptx::policy_evict_first() : 0ull;
             for (int32_t t = t_first; t < T; t += t_step) {
                 const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
                 if constexpr (MODE == kModeGrouped) {
@@ -482,10 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (!FQ)
                         ptx::tma_load_2d(sbase + C_::OFF_A + stage * C_::A_BYTES, &tmA, fb,
                                          kb * kBK, ti.row0);
-                    if constexpr (FQ != 0)  // weights stream past the L2-resident activations
-                        ptx::tma_load_3d_hint(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
-                                              kb * kBK, ti.n0, ti.e, b_pol);
-                    else if constexpr (MODE == kModeGrouped)
+                    if constexpr (MODE == kModeGrouped)
                         ptx::tma_load_3d(sbase + C_::OFF_B + stage * C_::B_BYTES, &tmB, fb,
                                          kb * kBK, ti.n0, ti.e);
                     else
@@ -644,9 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bf16: one step of loads in flight ahead (16 registers); fp32
             // (32 registers per step) fetches each step just before its use
             constexpr bool kAhead = BF;
-            // the activations are re-read by every CTA of a row tile: keep them
-            // in L2 ahead of the weights streaming past (loaded evict-first)
-            const uint64_t x_pol = ptx::policy_evict_last();
             FqIn<BF> nxt;
             bool have_nxt = false;
             int64_t src_next = -1;  // the next tile's source row, once fetched ahead
@@ -660,19 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         have_prev = false;
                     }
                     if (kb == p.num_kb) break;
-                    if (!have_nxt) nxt = fq_fetch<BF>(p, src, kb, x_pol);
+                    if (!have_nxt) nxt = fq_fetch<BF>(p, src, kb);
                     const FqIn<BF> cur = nxt;
                     have_nxt = false;
                     if constexpr (kAhead) {
                         if (kb + 1 < p.num_kb) {
                             if (!(kb + 1 == pre && have_prev)) {
-                                nxt = fq_fetch<BF>(p, src, kb + 1, x_pol);
+                                nxt = fq_fetch<BF>(p, src, kb + 1);
                                 have_nxt = true;
                             }
                         } else if (t + t_step < T) {  // the next tile's first step: no drain before it
                             src_next = fq_source(
                                 p, get_tile<MODE, BN>(t + t_step, p, row_off, tile_off, rt_off), ew);
-                            nxt = fq_fetch<BF>(p, src_next, 0, x_pol);
+                            nxt = fq_fetch<BF>(p, src_next, 0);
                             have_nxt = true;
                         }
                     }

@@ -287,12 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         goto roles_done;
                     const uint32_t fb = leader ? bar_full(stage) : ptx::map_shared(bar_full(stage), 0);
                     if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * tx_bytes);
-                    ptx::tma_load_2d_pair(sbase + PC::OFF_A + stage * kA, &tmA, fb, kb * kBK, row0);
+                    // first K element of the stage: a 128-byte row holds 128 one-byte
+                    // elements, or 32 fp32 ones (TF32)
+                    const int32_t kx = F4 == 3 ? kb * (kBK / 4) : kb * kBK;
+                    ptx::tma_load_2d_pair(sbase + PC::OFF_A + stage * kA, &tmA, fb, kx, row0);
                     if constexpr (MODE == kModeGrouped)
-                        ptx::tma_load_3d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0,
+                        ptx::tma_load_3d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kx, nb0,
                                               ti.e);
                     else
-                        ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kb * kBK, nb0);
+                        ptx::tma_load_2d_pair(sbase + PC::OFF_B + stage * kB, &tmB, fb, kx, nb0);
                     if constexpr (PC::kBlock) {
                         // packed UE8M0 chunks (512-byte rows of the packed arrays):
                         // this CTA's 128 rows of A; the tile's 256 rows of B
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // FP4-rate tiles end twice as often: their stores go out as whole
             // 128-byte row segments (measured 8192^3: +1.8%; on the FP8-rate
             // tiles the shuffles cost more than the coalescing saves, -0.5%)
-            if (F4 != 0 && p.st32) {
+            if ((F4 == 1 || F4 == 2) && p.st32) {
                 store_rows64<OUT_F32>(p.C, row, p.N, ncol0, r, a_t, lane);  // whole warp
             } else if (row >= 0) {
 #pragma unroll

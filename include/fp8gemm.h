@@ -419,6 +419,9 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
                                      int32_t *offsets_out, int32_t *tile_map_out,
                                      cudaStream_t stream);
 
+/* `flags` of fp8_grouped_gemm_quant. */
+#define FP8G_QUANT_FUSED 1
+
 /*
  * Grouped (MoE) GEMM from unquantised activations [JAX-BW MoE paragraph:
  * tokens routed to experts; its fine-grained (1x32) quantisation advice
@@ -431,22 +434,26 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
  * bit for bit: routed row r (expert order) is source row rows[r] of X
  * [x_rows, K] (rows null: row r, total_rows <= x_rows), quantised to E4M3
  * with one power-of-two scale per 1x32 block, then multiplied by its
- * expert's B[e].  When the grouped plan runs one CTA per 128-row tile
- * (fp8g_grouped_plan BM = 128: few routed rows, e.g. decoding), the
- * quantisation happens inside the GEMM kernel: each CTA quantises the tile
- * of A it is about to multiply from X into shared memory, so A is never
- * written to or read back from memory (one kernel, plus the packing of B's
- * scales).  Otherwise (BM = 256) the two steps run as two kernels with the
- * codes in qa_out / sfa_out, or in a stream-ordered temporary from the
- * library's pool when those are null.
+ * expert's B[e].  flags 0: the two steps run as two kernels (plus the
+ * packing of the scales), the codes in qa_out / sfa_out or, when those are
+ * null, in a stream-ordered temporary from the library's pool.
+ * flags FP8G_QUANT_FUSED, when the grouped plan runs one CTA per 128-row
+ * tile (fp8g_grouped_plan BM = 128: few routed rows, e.g. decoding): the
+ * quantisation runs inside the GEMM kernel, each CTA quantising the tile of A
+ * it multiplies from X into shared memory, so the codes never go through
+ * memory (other plans: as flags 0).  On GB300 the two kernels are faster:
+ * every CTA of a row tile re-reads that tile's bf16 rows, 56 times for
+ * N = 14336, and those loads wait behind the weights streaming through the
+ * memory system (decode-shaped MoE: 183 against 83 us per call).
  * X: fp32 or bf16 (x_dtype, FP8G_IN_*), 16-byte aligned; rows: device int32
  * [total_rows], 4-byte aligned; qa_out (nullable) uint8 [total_rows, K] and
  * sfa_out (nullable) fp32 [total_rows, K/32], both or neither, 16-byte
  * aligned: they receive the codes and scales (when the counts are valid).
- * K % 32 == 0.  Other arguments and rules as fp8_grouped_gemm_scatter.  A
- * source row outside [0, x_rows) records FP8G_ERR_INVALID_ARG (detail: the
- * routed row) and that row quantises as zeros.  Parity: the quantiser's
- * codes and scales bit-exact, the GEMM within the block-scaled tolerance.
+ * K % 32 == 0; flags 0 or FP8G_QUANT_FUSED.  Other arguments and rules as
+ * fp8_grouped_gemm_scatter.  A source row outside [0, x_rows) records
+ * FP8G_ERR_INVALID_ARG (detail: the routed row) and that row quantises as
+ * zeros.  Parity: the quantiser's codes and scales bit-exact, the GEMM
+ * within the block-scaled tolerance.
  */
 FP8G_API fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_rows,
                                            const int32_t *rows, const void *B, const float *sfb,
@@ -455,7 +462,8 @@ FP8G_API fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int6
                                            int64_t N, int64_t K, int64_t total_rows,
                                            const int32_t *c_row_of, int64_t c_rows,
                                            uint8_t *qa_out, float *sfa_out, int32_t *offsets_out,
-                                           int32_t *tile_map_out, cudaStream_t stream);
+                                           int32_t *tile_map_out, int32_t flags,
+                                           cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status

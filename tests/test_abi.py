@@ -204,7 +204,8 @@ def test_fused_quant_host_checks(fp8g):
         a = dict(ok, **kw)
         return _err(f, a["X"], a["x_dtype"], a["x_rows"], a["rows"], a["B"], a["sfb"], a["C"],
                     a["out"], a["b_fmt"], a["bias"], a["act"], a["counts"], a["E"], a["N"],
-                    a["K"], a["total_rows"], None, 0, a.get("qa"), a.get("sa"), None, None, 0)
+                    a["K"], a["total_rows"], None, 0, a.get("qa"), a.get("sa"), None, None,
+                    a.get("flags", 0), 0)
     assert call(x_dtype=2) == E
     assert call(qa=P) == E                                  # codes without scales
     assert call(rows=None, x_rows=4) == E                   # 8 routed rows from 4 sources
@@ -215,3 +216,4 @@ def test_fused_quant_host_checks(fp8g):
     assert call(E=0) == E
     assert call(counts=None) == E
     assert call(b_fmt=7) == E
+    assert call(flags=2) == E

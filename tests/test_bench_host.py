@@ -96,7 +96,7 @@ def test_algorithmic_bytes_from_tokens():
         want = rows * K * 2 + 4 * rows + E * N * K + 4 * E * N * K // 32 + rows * N * 2 + 4 * E
         assert bench.algorithmic_bytes(bench.WORKLOADS[name], _w(experts=E)) == want
         two = bench.WORKLOADS[name + "_2call"]
-        assert bench.algorithmic_bytes(two, _w(experts=E)) == want and not two["fused"]
+        assert bench.algorithmic_bytes(two, _w(experts=E)) == want and two["path"] == "2call"
 
 
 def test_algorithmic_bytes_skip_empty_experts():

@@ -162,13 +162,15 @@ def test_workload_skinny_x8_sampled():
 
 def test_workload_decode_bf16_sampled():
     """The decode-shaped MoE from bf16 tokens as the bench runs it, through
-    the one-call (fused quantiser) and the two-call paths: the same bits, and
+    the fused quantiser, the one-call and the two-call paths: the same bits, and
     sampled outputs against the oracle's quantisation of the gathered tokens
     and its GEMM."""
     import synth
-    wl, w, t, C = _run("decode_bf16")
+    wl, w, t, C = _run("decode_bf16_fused")
     wl2, _, t2, C2 = _run("decode_bf16_2call")
     assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+    C1 = _run("decode_bf16")[3]
+    assert np.array_equal(C1.view(np.uint32), C2.view(np.uint32))
     X, idx, _ = synth.moe_tokens(seed=wl["seed"], tokens=wl["tokens"])
     qa_o, sa_o = oracle.quantize_block32(X.to(torch.bfloat16).float().numpy()[idx.numpy()])
     _same(t2["tmp_qa"], qa_o, "decode A codes (two calls)")

@@ -1,7 +1,8 @@
 """fp8_grouped_gemm_quant: the grouped (MoE) GEMM from fp32 / bf16 token
-activations, with the 1x32 E4M3 quantisation of the routed rows fused into
-the GEMM kernel when the plan runs single-CTA tiles (few routed rows) and run
-as a gather-quantise pass before the GEMM otherwise.
+activations.  With FP8G_QUANT_FUSED the 1x32 E4M3 quantisation of the routed
+rows runs inside the GEMM kernel when the plan runs single-CTA tiles (few
+routed rows); otherwise, and by default, as a gather-quantise pass before the
+GEMM.
 
 Parity: the codes and scales the call reports are bit-exact against the
 oracle's quantiser on the gathered rows; the outputs are within the
@@ -50,7 +51,7 @@ def _weights(E, N, K, seed):
 
 
 def _fused(X, tok, qb, sb, counts, N, K, crow=None, c_rows=0, bias=None, act=0, copies=True,
-           out=fp8g.FP8G_OUT_BF16):
+           out=fp8g.FP8G_OUT_BF16, flags=fp8g.FP8G_QUANT_FUSED):
     E = counts.size
     rows = int(counts.sum())
     dt = fp8g.FP8G_IN_BF16 if X.dtype == torch.bfloat16 else fp8g.FP8G_IN_F32
@@ -67,7 +68,7 @@ def _fused(X, tok, qb, sb, counts, N, K, crow=None, c_rows=0, bias=None, act=0, 
                                 None if bias is None else torch.from_numpy(bias).cuda(), act,
                                 torch.from_numpy(counts).cuda(), E, N, K, rows,
                                 None if crow is None else torch.from_numpy(crow).cuda(), c_rows,
-                                qa, sa, offs, tmap)
+                                qa, sa, offs, tmap, flags)
     st, detail = fp8g.fp8_gemm_status()
     assert st == 0, f"status {st} detail {detail}"
     return C, qa, sa, offs.cpu().numpy(), tmap.cpu().numpy(), plan
@@ -146,10 +147,11 @@ def test_fused_quantiser_full(dtype):
     assert_within(x, ref, bound, f"fused quantiser {dtype}")
     two = _two_calls(X, tok, qb, sb, counts, N, K, crow, 2 * T, bias, fp8g.FP8G_ACT_RELU)
     assert np.array_equal(x.view(np.uint32), two.float().cpu().numpy().view(np.uint32))
-    # no copies asked for: the same GEMM, the same bits
-    C2 = _fused(X, tok, qb, sb, counts, N, K, crow, 2 * T, bias, fp8g.FP8G_ACT_RELU,
-                copies=False)[0]
-    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
+    # no copies asked for, and the default two-kernel path: the same bits
+    for copies, flags in ((False, fp8g.FP8G_QUANT_FUSED), (True, 0), (False, 0)):
+        C2 = _fused(X, tok, qb, sb, counts, N, K, crow, 2 * T, bias, fp8g.FP8G_ACT_RELU,
+                    copies=copies, flags=flags)[0]
+        assert torch.equal(C2.view(torch.int16), C.view(torch.int16)), (copies, flags)
 
 
 def test_fused_entry_with_many_rows_takes_two_passes():
@@ -231,7 +233,7 @@ def test_fused_bad_source_row_recorded():
     sa = torch.full((128, K // 32), -1.0, device="cuda")
     fp8g.fp8_grouped_gemm_quant(X.cuda(), fp8g.FP8G_IN_F32, T, torch.from_numpy(tok).cuda(), qb,
                                 sb, C, 0, 0, None, 0, torch.from_numpy(counts).cuda(), E, N, K,
-                                128, None, 0, qa, sa, None, None)
+                                128, None, 0, qa, sa, None, None, fp8g.FP8G_QUANT_FUSED)
     st, detail = fp8g.fp8_gemm_status()
     assert st == fp8g.FP8G_ERR_INVALID_ARG and detail == 77
     assert (qa[77] == 0).all() and (sa[77] == 1.0).all() and (C[77].float() == 0.0).all()
@@ -248,6 +250,6 @@ def test_fused_zero_rows():
     X = torch.zeros(4, K, device="cuda")
     C = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
     fp8g.fp8_grouped_gemm_quant(X, fp8g.FP8G_IN_F32, 4, None, qb, sb, C, 0, 0, None, 0, counts, E,
-                                N, K, 0, None, 0, None, None, offs, None)
+                                N, K, 0, None, 0, None, None, offs, None, fp8g.FP8G_QUANT_FUSED)
     assert fp8g.fp8_gemm_status()[0] == fp8g.FP8G_OK
     assert (offs.cpu() == 0).all()
