@@ -334,6 +334,15 @@ def fp4_rate(fp8g, wl) -> bool:
     return fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["BM"] == 256
 
 
+def tf32_route(fp8g, wl) -> bool:
+    """Whether a literal-scale call takes the TF32 route (the library's rule:
+    1-byte codes on a shape with a wave of 256 x 256 tiles): two dequantising
+    passes, then a kind::tf32 GEMM."""
+    return (bool(wl.get("literal")) and wl.get("a_fmt", 0) in (0, 1) and
+            wl.get("b_fmt", 0) in (0, 1) and
+            fp8g.fp8g_gemm_plan(0, wl["M"], wl["N"], wl["K"])["BM"] == 256)
+
+
 def launches_per_call(fp8g, wl) -> int:
     """Kernels one call launches: the GEMM, plus the scale-packing kernel on the
     block-scaled paths that do not split K (split-K converts scales itself)."""
@@ -347,7 +356,7 @@ def launches_per_call(fp8g, wl) -> int:
                  fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128)
         return 2 if fused else 3
     if wl.get("literal"):
-        return 1
+        return 3 if tf32_route(fp8g, wl) else 1
     return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
 
 
@@ -649,10 +658,12 @@ def main():
 
     peaks = _peaks()
     # measured bf16 burst x the nominal dense ratio of the MMA kind that runs:
-    # FP8 (and E2M1 on the FP8-rate MMA) 2, FP4 (kind::mxf4) 13.5 / 2.25 = 6
+    # FP8 (and E2M1 on the FP8-rate MMA) 2, FP4 (kind::mxf4) 13.5 / 2.25 = 6,
+    # TF32 (the literal-scale route) 1.1 / 2.25
     f4 = fp4_rate(fp8g, wl)
-    ratio = 6.0 if f4 else 2.0
-    tc_peak = ratio * peaks["bf16"]
+    tf32 = tf32_route(fp8g, wl)
+    ratio = 6.0 if f4 else (1.1 / 2.25 if tf32 else 2.0)
+    tc_peak = round(ratio * peaks["bf16"], 1)
     tflops = flops / (ms * 1e-3) / 1e12
     hbm_gbs = abytes / (ms * 1e-3) / 1e9
     k_tflops = flops / (kernel_ms * 1e-3) / 1e12
@@ -669,20 +680,27 @@ def main():
     roof["traffic"] = TRAFFIC_BYTES.get(args.workload)
     roof["timed"] = (f"GEMM kernel alone: mean of {len(kms)} launches, CUDA events the library "
                      f"records on the launching stream around the launch (a pass right after "
-                     f"the timed region); call_* = the whole call (packing + GEMM kernel) over the "
-                     f"timed region" if kms else
+                     f"the timed region); call_* = the whole call (packing or dequantising "
+                     f"kernels + GEMM kernel) over the timed region" if kms else
                      "the GEMM kernel (the call's only launch) over the timed region")
     roof["kernel_ms"] = round(kernel_ms, 5)
-    roof["peak_source"] = (f"{peaks['src']}: {'fp4 = 6' if f4 else 'fp8 = 2'} x bf16 burst "
+    kind_ratio = "fp4 = 6" if f4 else ("tf32 = 1.1/2.25" if tf32 else "fp8 = 2")
+    roof["peak_source"] = (f"{peaks['src']}: {kind_ratio} x bf16 burst "
                            f"{peaks['bf16']} TFLOP/s" if tensor_bound else
                            f"{peaks['src']}: HBM copy {peaks['hbm']} GB/s")
+    if tf32 and tensor_bound:
+        roof["peak_source"] += (" (literal fp32 scales: operands dequantised to TF32, then the "
+                                "kind::tf32 GEMM on CTA pairs)")
+        fp8_peak = 2.0 * peaks["bf16"]
+        roof["call_frac_of_fp8_peak"] = round(tflops / fp8_peak, 4)
     if f4 and tensor_bound:
         roof["peak_source"] += (" (NVFP4: the FP4-rate MMA, kind::mxf4nvf4 scale_vec::4X)"
                                 if wl["kind"] in ("nvfp4", "grouped_nvfp4") else
                                 " (MXFP4 on CTA pairs: the FP4-rate MMA, kind::mxf4)")
     elif {2, 3, 4} & {wl.get("a_fmt", 0), wl.get("b_fmt", 0)} and tensor_bound:
         roof["peak_source"] += " (E2M1 / FP6 operands on the FP8-rate MMA, kind::f8f6f4)"
-    roof["nominal_frac"] = round(max(flops / (13.5e15 if f4 else 4.5e15), abytes / 8e12) /
+    roof["nominal_frac"] = round(max(flops / (13.5e15 if f4 else (1.1e15 if tf32 else 4.5e15)),
+                                     abytes / 8e12) /
                                  (kernel_ms * 1e-3), 4)
 
     line = {

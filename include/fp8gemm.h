@@ -383,13 +383,20 @@ FP8G_API fp8g_status fp8_gemm_blockscaled_ex(const void *A, const void *B, const
  * specialisation paragraph: the promotion warp role; the workloads' literal
  * "fp32 scale = block amax/448"].  Same C = sum_kb sfa*sfb*partial_kb as
  * fp8_gemm_blockscaled, but any finite fp32 scale (NaN and infinities
- * propagate) rather than only powers of two: the tensor core computes each
- * 32-wide K block's unscaled partial and CUDA-core warps scale and accumulate
- * it in fp32 (fma(fl32(sfa*sfb), partial, acc)); ceiling well below the
- * power-of-two path.  Operand formats, bias and activation as
- * fp8_gemm_blockscaled_ex.  K % 128 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE);
- * sfa, sfb 16-byte aligned.  Runs one kernel; allocates nothing.  Parity: the
- * tolerance of fp8_gemm_blockscaled (plus the epilogue term when used).
+ * propagate) rather than only powers of two.  Two routes, chosen by shape:
+ *   - at least a wave of 256 x 256 output tiles (fp8g_gemm_plan(0, M, N, K)
+ *     BM = 256) with 1-byte operands (E4M3 / E5M2): each operand is
+ *     dequantised once with its scales to TF32 (round to nearest, ties
+ *     away; every value within 2^-11 of fl32(dec(q) s)) into a stream-ordered
+ *     temporary of 4 (M + N) K bytes from the library's pool, then a
+ *     kind::tf32 tensor-core GEMM on CTA pairs: three kernels.  Each scaled
+ *     operand value must be finite in fp32.
+ *   - otherwise: the tensor core computes each 32-wide K block's unscaled
+ *     partial and CUDA-core warps scale and accumulate it in fp32
+ *     (fma(fl32(sfa*sfb), partial, acc)): one kernel, no allocation.
+ * Both lie within the block-scaled GEMM's tolerance.  Operand formats, bias
+ * and activation as fp8_gemm_blockscaled_ex.  K % 128 == 0 (else
+ * FP8G_ERR_UNSUPPORTED_SHAPE); sfa, sfb 16-byte aligned.
  */
 FP8G_API fp8g_status fp8_gemm_blockscaled_promote(const void *A, const void *B, const float *sfa,
                                          const float *sfb, void *C, int out, int32_t a_fmt,
