@@ -905,7 +905,13 @@ fp8g_status fp8_grouped_gemm_quant(const void *X, int32_t x_dtype, int64_t x_row
     fp8g_status st = check_grouped_args(a_arg, B, sfa_arg, sfb, C, out, counts, E, N, K,
                                         total_rows, c_row_of, c_rows, offsets_out, tile_map_out);
     if (st != FP8G_OK) return st;
+    // the rest of the GEMM's host rules, before anything is launched
     if (!valid_fmt(b_fmt)) return FP8G_ERR_INVALID_ARG;
+    if (act != FP8G_ACT_NONE && act != FP8G_ACT_RELU && act != FP8G_ACT_GELU)
+        return FP8G_ERR_INVALID_ARG;
+    if (bias != nullptr && !aligned(bias, 4)) return FP8G_ERR_ALIGNMENT;
+    if ((st = check_packed(B, B, FP8G_E4M3, b_fmt, K)) != FP8G_OK) return st;
+    if (total_rows / kBM + E > 65535) return FP8G_ERR_UNSUPPORTED_SHAPE;
     const int64_t c_rows_eff = c_row_of != nullptr ? c_rows : total_rows;
     DevInfo di;
     if ((st = device_info(di)) != FP8G_OK) return st;

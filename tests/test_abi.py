@@ -217,3 +217,9 @@ def test_fused_quant_host_checks(fp8g):
     assert call(counts=None) == E
     assert call(b_fmt=7) == E
     assert call(flags=2) == E
+    assert _err(f, P, 1, 8, P, P, P, P, 0, 0, None, 5, P, 2, 8, 64, 8, None, 0, None, None,
+                None, None, 0, 0) == E                                   # activation
+    assert _err(f, P, 1, 8, P, P + 16, P, P, 0, 2, None, 0, P, 2, 8, 128, 8, None, 0, None, None,
+                None, None, 0, 0) == A                                   # packed B alignment
+    assert _err(f, P, 1, 8, P, P, P, P, 0, 2, None, 0, P, 2, 8, 64, 8, None, 0, None, None,
+                None, None, 0, 0) == fp8g.FP8G_ERR_UNSUPPORTED_SHAPE     # packed B, K % 128
