@@ -314,7 +314,7 @@ def run_once(fp8g, wl, w, t, C, stream):
 # Valid only for the kernel source those captures measured: an entry leaves
 # this table when its kernel changes, and workloads without a capture of the
 # current kernel report null.
-TRAFFIC_BYTES = {"large8192": 261_226_240 + 116_971_776,
+TRAFFIC_BYTES = {"large8192": 257_933_312 + 117_130_752,
                  "mxfp4_8192": 107_267_584 + 95_654_144,
                  "nvfp4_8192": 113_694_976 + 97_257_984,
                  "mxfp6_8192": 167_501_824 + 110_660_864}
