@@ -352,15 +352,16 @@ __device__ __forceinline__ bool fq_put(const GemmParams &p, const FqIn<BF16> &in
 // SPLIT: the CTAs of one cluster share an output tile, each taking a
 // contiguous range of K blocks; CTA o of the cluster owns columns
 // [o 128 / S, (o + 1) 128 / S) of the tile.  As soon as its accumulator is in
-// registers, each epilogue warp (32 rows x 32 columns) stores its block with
-// 16-byte asynchronous remote stores (st.async) into the owner's receive
-// region (slot: sender, row quarter, column group), each counted in bytes on
-// the owner's receive barrier; the owner's warps wait for every peer's block
-// of their rows, add them to their own partial in rank order (a fixed order,
-// so results do not depend on timing) and store.  Blocks are row-major 32 x
-// 32 fp32, 16-byte chunks XOR-swizzled by row (lane = row: conflict-free).
-// (Staging each block in shared memory and pushing it with a bulk copy took
-// ~2 us from push to arrival on GB300.)
+// registers, each epilogue warp (32 rows x 32 columns) stages the block in
+// its CTA's idle operand ring and pushes it with one bulk copy into the
+// owner's receive region (slot: sender, row quarter, column group), counted
+// in bytes on the owner's receive barrier; the owner's warps wait for every
+// peer's block of their rows, add them to their own partial in rank order (a
+// fixed order, so results do not depend on timing) and store.  Blocks are row-major
+// 32 x 32 fp32, 16-byte chunks XOR-swizzled by row (lane = row: conflict-free).
+// (Sending the blocks straight from registers with 16-byte st.async remote
+// stores instead was slower on GB300: 14.8 against 13.2 us per 128 x 4096 x
+// 4096 call, the stores alone taking ~2.5 us to issue.)
 // FQ (grouped, single CTA): the epilogue warps also quantise A in the kernel
 // (fq_fetch / fq_put) from fp32 (FQ = 1) or bf16 (FQ = 2) activations; the
 // producer loads only B and B's scale chunk.
@@ -369,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES, SPLIT>;
-    static_assert(!SPLIT || (BN == 128 && C_::CW == 32), "split-K: 32 x 32 blocks per epilogue warp");
+    static_assert(!SPLIT || (BN == 128 && C_::CW == 32 && STAGES * C_::A_BYTES >= kEpiWarps * 4096),
+                  "split-K: 32 x 32 blocks per epilogue warp, staged in the A ring");
     // split-K tiles are few: the kernel converts its own scale chunks instead
     // of reading chunks that a packing kernel wrote
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
@@ -719,17 +721,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return blk + (uint32_t)lane * 128u + ((uint32_t)(v ^ (lane & 7)) << 4);
                 };
                 if (owner != rank) {
-                    // straight from registers into the owner's receive slot:
-                    // 16-byte remote stores, each counted on its receive barrier
-                    const int slot = rank < owner ? rank : rank - 1;
-                    const uint32_t blk = ptx::map_shared(
-                        sbase + C_::OFF_RECV + (uint32_t)(((slot * 4 + q) * (4 / S) + cgi) * 4096),
-                        (uint32_t)owner);
-                    const uint32_t rbar = ptx::map_shared(bar_recv, (uint32_t)owner);
+                    // the ring is idle (every MMA, hence every operand read, completed)
+                    const uint32_t blk = sbase + C_::OFF_A + (uint32_t)ew * 4096u;
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        ptx::st_async_v4(chunk(blk, v), r[0][4 * v], r[0][4 * v + 1],
-                                         r[0][4 * v + 2], r[0][4 * v + 3], rbar);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(chunk(blk, v)),
+                                     "r"(r[0][4 * v]), "r"(r[0][4 * v + 1]), "r"(r[0][4 * v + 2]),
+                                     "r"(r[0][4 * v + 3])
+                                     : "memory");
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int slot = rank < owner ? rank : rank - 1;
+                        const uint32_t dst = sbase + C_::OFF_RECV +
+                                             (uint32_t)(((slot * 4 + q) * (4 / S) + cgi) * 4096);
+                        ptx::bulk_push(ptx::map_shared(dst, (uint32_t)owner), blk, 4096u,
+                                       ptx::map_shared(bar_recv, (uint32_t)owner));
+                    }
                     continue;
                 }
                 // own columns: every peer's block of these rows, then the sum in a

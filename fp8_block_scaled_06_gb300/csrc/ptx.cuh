@@ -158,17 +158,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// 16-byte store into another CTA's shared memory (cluster address from
-// map_shared), counted in bytes on that CTA's mbarrier (its expect-tx).
-__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t cbar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-        "[%5];" ::"r"(caddr),
-        "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
-        : "memory");
-}
-
 // 1-D bulk copy global -> shared completing on an mbarrier (src, dst 16-byte
 // aligned; bytes a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
