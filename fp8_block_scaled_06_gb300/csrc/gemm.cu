@@ -909,6 +909,13 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
             kc.pair = true;
             kc.grid = 2 * (num_sms / 2);
         } else {
+            // Less than a wave: 128 x 128 tiles, twice as many, so the last
+            // wave idles half as long (each expert's rows are padded to whole
+            // tiles, so the tile count exceeds the estimate: decode-shaped
+            // MoE, 256 routed rows over 3 experts, N = 14336: 168 tiles of
+            // 128 x 256 on 148 SMs are two waves, the second 14% full)
+            kc.BN = 128;
+            kc.b_rows = 128;
             kc.grid = num_sms;
         }
         return kc;
@@ -969,13 +976,19 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
         return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
     } else if (p.xq != nullptr) {
-        // fused activation quantiser (single CTAs only: the caller checks the plan)
-        if (kc.pair || split) return cudaErrorInvalidValue;
+        // fused activation quantiser (single CTAs, 128 x 256 tiles: the caller
+        // sets the plan)
+        if (kc.pair || split || kc.BN != 256) return cudaErrorInvalidValue;
         if (p.xq_bf16)
             return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 2>(maps, p, kc, stream)
                            : launch_one<kModeGrouped, 256, 1, 4, false, false, 2>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 1>(maps, p, kc, stream)
                        : launch_one<kModeGrouped, 256, 1, 4, false, false, 1>(maps, p, kc, stream);
+    } else if (kc.BN == 128) {
+        // two 128-column accumulators: the epilogue of a tile overlaps the
+        // next tile's MMAs
+        return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 128, 2, 6, false, false>(maps, p, kc, stream);
     } else {
         return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeGrouped, 256, 1, 4, false, false>(maps, p, kc, stream);
