@@ -387,12 +387,7 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     DevInfo di;
     st = device_info(di);
     if (st != FP8G_OK) return st;
-    KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
-    if (fq != nullptr && !kc.pair) {
-        // the fused quantiser's kernel: 128 x 256 tiles (8 rows per epilogue warp)
-        kc.BN = 256;
-        kc.b_rows = 256;
-    }
+    const KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
     // MXFP4 on CTA pairs runs at the FP4 rate (kind::mxf4, 256 K elements per
     // stage); every other E2M1 case takes the FP8-rate MMA with 4-bit loads
     const bool f4 = kc.pair && mode != kModeTensor && a_fmt == FP8G_E2M1 &&

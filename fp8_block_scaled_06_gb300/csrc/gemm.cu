@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of reading chunks that a packing kernel wrote
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
-    static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && NUM_ACC == 1 && kEpiWarps * 8 == kBM),
+    static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && kEpiWarps * 8 == kBM),
                   "fused quantiser: grouped single-CTA kernel, 8 rows per epilogue warp");
     constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES
                                   : FQ      ? C_::B_BYTES + C_::SFB_BYTES
@@ -592,12 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (FQ != 0 && warp >= kEpiWarp0) {
         // ===== fused quantiser + epilogue =====
-        // Each warp quantises its 8 rows of A for every K step (fq_stage) and
-        // drains / stores the previous tile's accumulator once the first
-        // min(STAGES - 1, num_kb) steps of the next tile are quantised: those
-        // steps wait only for the previous tile's MMAs, and the next tile's
-        // first MMA waits for that drain (one accumulator), so neither order
-        // can deadlock.
+        // Each warp quantises its 8 rows of A for every K step (fq_fetch /
+        // fq_put) and drains / stores the previous tile's accumulator once
+        // the first min(STAGES - 1, num_kb) steps of the next tile are
+        // quantised: those steps wait only for the previous tile's MMAs, and
+        // a tile's first MMA waits only for the drain of the tile NUM_ACC
+        // before it, which came earlier, so neither order can deadlock.
         const int ew = warp - kEpiWarp0;
         const int q = warp & 3;
         const int col0 = (ew >> 2) * C_::CW;
@@ -606,17 +606,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         Tile prev{};
         bool have_prev = false;
         auto drain_store = [&](const Tile &ti) -> bool {
-            if (!wait_bar_warp(bar_accf(0), (uint32_t)(ltd & 1), abort_flag, p, 3 * 256, 128))
+            const int acc = ltd % NUM_ACC;
+            if (!wait_bar_warp(bar_accf(acc), (uint32_t)((ltd / NUM_ACC) & 1), abort_flag, p,
+                               3 * 256 + acc, 128))
                 return false;
             ptx::tc_fence_after();
             uint32_t r[C_::CW / 32][32];
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + col0;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + col0;
 #pragma unroll
             for (int c = 0; c < C_::CW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
             ptx::tmem_ld_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar_acce(0));
+            if (lane == 0) ptx::mbar_arrive(bar_acce(acc));
             ++ltd;
             const int64_t arow = (int64_t)ti.row0 + q * 32 + lane;          // routed row
             const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;  // row of C
@@ -976,22 +978,19 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
         return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
     } else if (p.xq != nullptr) {
-        // fused activation quantiser (single CTAs, 128 x 256 tiles: the caller
-        // sets the plan)
-        if (kc.pair || split || kc.BN != 256) return cudaErrorInvalidValue;
+        // fused activation quantiser (single CTAs, 128 x 128 tiles)
+        if (kc.pair || split || kc.BN != 128) return cudaErrorInvalidValue;
         if (p.xq_bf16)
-            return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 2>(maps, p, kc, stream)
-                           : launch_one<kModeGrouped, 256, 1, 4, false, false, 2>(maps, p, kc, stream);
-        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false, 1>(maps, p, kc, stream)
-                       : launch_one<kModeGrouped, 256, 1, 4, false, false, 1>(maps, p, kc, stream);
-    } else if (kc.BN == 128) {
-        // two 128-column accumulators: the epilogue of a tile overlaps the
-        // next tile's MMAs
+            return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false, 2>(maps, p, kc, stream)
+                           : launch_one<kModeGrouped, 128, 2, 6, false, false, 2>(maps, p, kc, stream);
+        return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false, 1>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 128, 2, 6, false, false, 1>(maps, p, kc, stream);
+    } else {
+        // 128 x 128 tiles, two 128-column accumulators: the epilogue of a tile
+        // overlaps the next tile's MMAs
+        if (kc.BN != 128) return cudaErrorInvalidValue;
         return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false>(maps, p, kc, stream)
                        : launch_one<kModeGrouped, 128, 2, 6, false, false>(maps, p, kc, stream);
-    } else {
-        return out_f32 ? launch_one<kModeGrouped, 256, 1, 4, true, false>(maps, p, kc, stream)
-                       : launch_one<kModeGrouped, 256, 1, 4, false, false>(maps, p, kc, stream);
     }
 }
 
