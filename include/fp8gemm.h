@@ -451,7 +451,7 @@ FP8G_API fp8g_status fp8_grouped_gemm_scatter(const void *A, const void *B, cons
  * memory (other plans: as flags 0).  On GB300 the two kernels are faster:
  * every CTA of a row tile re-reads that tile's bf16 rows, 56 times for
  * N = 14336, and those loads wait behind the weights streaming through the
- * memory system (decode-shaped MoE: 183 against 83 us per call).
+ * memory system (decode-shaped MoE: 176 against 72 us per call).
  * X: fp32 or bf16 (x_dtype, FP8G_IN_*), 16-byte aligned; rows: device int32
  * [total_rows], 4-byte aligned; qa_out (nullable) uint8 [total_rows, K] and
  * sfa_out (nullable) fp32 [total_rows, K/32], both or neither, 16-byte
