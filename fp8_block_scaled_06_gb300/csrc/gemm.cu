@@ -51,11 +51,10 @@ constexpr int kThreads = 640;  // 20 warps
 constexpr int kMaxSplit = 4;   // K-split cluster size (clusters of <= 4 CTAs co-schedule)
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
-// Block-scaled split-K: eight epilogue warps per K step convert the stage's
-// fp32 block scales (128 rows of A, 128 of B) into its UE8M0 chunk; two such
-// groups take alternate K steps, each with kSfAhead steps of loads in flight.
+// Block-scaled split-K: the epilogue warps convert the fp32 block scales (128
+// rows of A, 128 of B) of every K step into the stage's UE8M0 chunk, kSfWarps
+// warps per operand.
 constexpr int kSfWarps = 8;
-constexpr int kSfAhead = 4;
 
 // Split-K (SPLITC): the ring of a split-K CTA, then its receive region for
 // the peers' partial blocks: (S - 1) x 128 rows x (128 / S) columns of fp32,
@@ -133,79 +132,101 @@ __device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const i
     return ti;
 }
 
-// Block-scaled split-K, epilogue warp ew: writes the UE8M0 chunk (the layout
-// of scales.cu: byte 16 d + 4 w + j = row 32 w + d, K block j; A's 128 rows,
-// then B's) of every other K step of the tile into the ring, after the
-// stage's empty barrier, and counts one arrival per warp on its full barrier.
-// Rows past the operand and K blocks past K/32 get code 127; a scale that is
-// not a positive normal power of two records FP8G_ERR_SCALE_FORMAT.  Returns
-// false when the CTA is aborting.
-template <int STAGES>
-__device__ __forceinline__ bool convert_scales(const GemmParams &p, const Tile &ti, int kb_begin,
-                                               int kb_end, uint32_t it, int ew, uint32_t sf_base,
-                                               uint32_t chunk_bytes, uint64_t *bars,
-                                               volatile int *abort_flag) {
+// Block-scaled split-K, epilogue warp ew (of 2 kSfWarps): writes the UE8M0
+// chunk (the layout of scales.cu: byte 16 d + 4 w + j = row 32 w + d, K block
+// j; A's 128 rows, then B's) of each of the tile's K steps into the ring, after
+// the stage's empty barrier, and counts one arrival per warp and stage on its
+// full barrier.  Warps 0..7 take A's rows, 8..15 B's, 16 rows each.  K steps
+// go in windows of 8: lane (i, s) = (lane / 8, lane % 8) reads the 16 bytes of
+// step s for rows 4 j + i (j < 4) of the warp's 16, so eight lanes read one
+// row's 128 contiguous bytes and every load of a window is in flight at once.
+// (One row per lane and a step per load, each warp load touched 32 lines.)
+// sf_fetch issues a window's loads, sf_put converts and stores them.  Rows
+// past the operand and K blocks past K/32 get code 127; a scale that is not a
+// positive normal power of two sets `bad`.
+struct SfWindow {
+    uint32_t v[4][4];  // this lane's step: 4 fp32 scales of each of its 4 rows
+};
+
+__device__ __forceinline__ void sf_fetch(const GemmParams &p, const Tile &ti, int kb_begin, int n,
+                                         int w0, int ew, SfWindow &f) {
     const int lane = threadIdx.x & 31;
-    const uint32_t h = (uint32_t)(ew / kSfWarps);  // this group's K steps: it + i odd / even
-    const int g = (ew % kSfWarps) * 32 + lane;      // 0..255: A rows, then B rows
-    const bool isB = g >= kBM;
-    const int r = g & (kBM - 1);
-    const int64_t grow = isB ? (int64_t)ti.n0 + r : (int64_t)ti.row0 + r;
-    const bool valid = isB ? grow < p.N : grow < ti.row_end;
-    const float *src = (isB ? p.sb : p.sa) + (valid ? grow : 0) * p.sfc;
-    const uint32_t soff = (isB ? kBM * 4u : 0u) + 16u * (uint32_t)(r & 31) + 4u * (uint32_t)(r >> 5);
-    const bool vec = (p.sfc & 3) == 0;
-    const int n = kb_end - kb_begin;
-    bool bad = false, ok = true;
-    for (int i = ((it & 1u) == h) ? 0 : 1; i < n && ok; i += 2 * kSfAhead) {
-        uint32_t v[kSfAhead][4];
+    const bool isB = ew >= kSfWarps;
+    const int sl = lane & 7;
+    const int r0 = (ew % kSfWarps) * 16 + (lane >> 3);
+    const float *base = isB ? p.sb : p.sa;
+    const int64_t g0 = isB ? (int64_t)ti.n0 : (int64_t)ti.row0;
+    const int64_t gend = isB ? p.N : (int64_t)ti.row_end;
+    const bool live = w0 + sl < n;
+    const int64_t k0 = (int64_t)(kb_begin + w0 + sl) * 4;  // this lane's first scale column
 #pragma unroll
-        for (int j = 0; j < kSfAhead; ++j) {
-            const int ii = i + 2 * j;
-            const int64_t k0 = (int64_t)(kb_begin + ii) * 4;
-            if (vec) {
-                uint4 f = make_uint4(0u, 0u, 0u, 0u);
-                if (valid && ii < n) f = __ldg(reinterpret_cast<const uint4 *>(src + k0));
-                v[j][0] = f.x;
-                v[j][1] = f.y;
-                v[j][2] = f.z;
-                v[j][3] = f.w;
-            } else {
+    for (int j = 0; j < 4; ++j) {
+        const int64_t grow = g0 + r0 + 4 * j;
+        const bool valid = live && grow < gend;
+        const float *src = base + (valid ? grow * p.sfc + k0 : 0);
+        if ((p.sfc & 3) == 0) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (valid) x = __ldg(reinterpret_cast<const uint4 *>(src));
+            f.v[j][0] = x.x;
+            f.v[j][1] = x.y;
+            f.v[j][2] = x.z;
+            f.v[j][3] = x.w;
+        } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    v[j][q] = (valid && ii < n && k0 + q < p.sfc) ? __float_as_uint(__ldg(src + k0 + q))
-                                                                 : 0u;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kSfAhead; ++j) {
-            const int ii = i + 2 * j;
-            if (ii >= n) break;  // warp-uniform
-            const uint32_t gi = it + (uint32_t)ii;
-            const uint32_t stage = gi % STAGES, phase = (gi / STAGES) & 1u;
-            if (!wait_bar_warp(ptx::smem_addr(&bars[STAGES + stage]), phase ^ 1u, abort_flag, p,
-                               5 * 256 + stage)) {
-                ok = false;
-                break;
-            }
-            uint32_t word = 0x7F7F7F7Fu;
-            if (valid) {
-                word = 0;
-                const int64_t k0 = (int64_t)(kb_begin + ii) * 4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    word |= (k0 + q < p.sfc ? ue8m0_code(v[j][q], bad) : 127u) << (8 * q);
-            }
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes + soff),
-                         "r"(word)
-                         : "memory");
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[stage]));
+            for (int q = 0; q < 4; ++q)
+                f.v[j][q] = (valid && k0 + q < p.sfc) ? __float_as_uint(__ldg(src + q)) : 0u;
         }
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
-    return ok;
+}
+
+// Returns false when the CTA is aborting.
+template <int STAGES>
+__device__ __forceinline__ bool sf_put(const GemmParams &p, const Tile &ti, int kb_begin, int n,
+                                       int w0, uint32_t it, int ew, const SfWindow &f,
+                                       uint32_t sf_base, uint32_t chunk_bytes, uint64_t *bars,
+                                       volatile int *abort_flag, bool &bad) {
+    const int lane = threadIdx.x & 31;
+    const bool isB = ew >= kSfWarps;
+    const int sl = lane & 7;
+    const int r0 = (ew % kSfWarps) * 16 + (lane >> 3);
+    const int64_t g0 = isB ? (int64_t)ti.n0 : (int64_t)ti.row0;
+    const int64_t gend = isB ? p.N : (int64_t)ti.row_end;
+    const uint32_t half = isB ? kBM * 4u : 0u;
+    const bool live = w0 + sl < n;
+    const int64_t k0 = (int64_t)(kb_begin + w0 + sl) * 4;
+    uint32_t word[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        word[j] = 0x7F7F7F7Fu;
+        if (live && g0 + r0 + 4 * j < gend) {
+            word[j] = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                word[j] |= (k0 + q < p.sfc ? ue8m0_code(f.v[j][q], bad) : 127u) << (8 * q);
+        }
+    }
+    const int steps = n - w0 < 8 ? n - w0 : 8;
+    for (int t = 0; t < steps; ++t) {  // warp-uniform
+        const uint32_t gi = it + (uint32_t)(w0 + t);
+        const uint32_t stage = gi % STAGES, phase = (gi / STAGES) & 1u;
+        if (!wait_bar_warp(ptx::smem_addr(&bars[STAGES + stage]), phase ^ 1u, abort_flag, p,
+                           5 * 256 + stage))
+            return false;
+        if (sl == t) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t r = (uint32_t)(r0 + 4 * j);
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes + half +
+                                                             16u * (r & 31u) + 4u * (r >> 5)),
+                             "r"(word[j])
+                             : "memory");
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[stage]));
+    }
+    return true;
 }
 
 // Fused activation quantiser (grouped GEMM, single CTA; epilogue warp ew of
@@ -376,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of reading chunks that a packing kernel wrote
     constexpr bool kInlineSF = SPLIT && C_::kBlock;
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
+    static_assert(!SPLIT || MODE != kModeGrouped, "split-K: non-grouped only");
     static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && kEpiWarps * 8 == kBM),
                   "fused quantiser: grouped single-CTA kernel, 8 rows per epilogue warp");
     constexpr uint32_t kTxBytes = kInlineSF ? C_::A_BYTES + C_::B_BYTES
@@ -409,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar_full(s), kInlineSF ? 1 + kSfWarps : FQ ? 1 + kEpiWarps : 1);
+            ptx::mbar_init(bar_full(s), kInlineSF ? 1 + 2 * kSfWarps : FQ ? 1 + kEpiWarps : 1);
             ptx::mbar_init(bar_empty(s), 1);
             ptx::mbar_init(bar_sfr(s), 1);
         }
@@ -434,8 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_relinquish();
     }
     // Split-K: every CTA's receive barrier initialised before any peer's push
-    // (the wait is below, after the dependency wait)
     if constexpr (SPLIT) ptx::cluster_arrive_release();
+    // Non-grouped kernels need nothing from global memory before their roles
+    // start: they publish the barriers and the tensor-memory slot here, so
+    // that every role begins the moment the dependency wait returns (the
+    // first run of each role's code per launch is slow, ~0.25 us per stretch
+    // of new code on GB300, and a block-wide barrier after the wait made
+    // every role wait for the slowest).
+    constexpr bool kEarlySync = MODE != kModeGrouped;
+    if constexpr (kEarlySync) {
+        ptx::tc_fence_before();
+        __syncthreads();
+        if constexpr (SPLIT) ptx::cluster_wait();
+        ptx::tc_fence_after();
+    }
     // Everything above touched only shared / tensor memory and kernel
     // parameters; global memory (which the previous kernel on the stream may
     // still be writing, or reading) is accessed only after this wait.  The
@@ -443,12 +477,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
     int32_t T = (int32_t)p.T;
-    if constexpr (MODE == kModeGrouped) grouped_prefix(p, kBM, row_off, tile_off, rt_off);
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    if constexpr (MODE == kModeGrouped) T = tile_off[p.E];
-    if constexpr (SPLIT) ptx::cluster_wait();
+    // Split-K block scales: the epilogue warps convert the first window of
+    // the first tile's K steps right away, in one stretch of code, ahead of
+    // the operand loads
+    bool sf_ok0 = true;
+    if constexpr (kInlineSF) {
+        if (warp >= kEpiWarp0 && (int32_t)ptx::cluster_id_x() < T) {
+            const int rank = (int)ptx::cluster_rank();
+            const Tile ti = get_tile<MODE, BN>((int32_t)ptx::cluster_id_x(), p, nullptr, nullptr,
+                                               nullptr);
+            const int kb0 = rank * p.num_kb / p.split;
+            const int n = (rank + 1) * p.num_kb / p.split - kb0;
+            SfWindow f;
+            bool bad = false;
+            sf_fetch(p, ti, kb0, n, 0, warp - kEpiWarp0, f);
+            sf_ok0 = sf_put<STAGES>(p, ti, kb0, n, 0, 0u, warp - kEpiWarp0, f,
+                                    sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag, bad);
+            if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
+        }
+    }
+    if constexpr (!kEarlySync) {
+        if constexpr (MODE == kModeGrouped) grouped_prefix(p, kBM, row_off, tile_off, rt_off);
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        if constexpr (MODE == kModeGrouped) T = tile_off[p.E];
+    }
     const uint32_t tmem_base = *tmem_slot;
 
     // work of this CTA: tiles t_first, t_first + t_step, ...; K blocks [kb_begin, kb_end)
@@ -695,10 +749,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t t = t_first; t < T; t += t_step, ++lt) {
             const Tile ti = get_tile<MODE, BN>(t, p, row_off, tile_off, rt_off);
             if constexpr (kInlineSF) {
-                if (!convert_scales<STAGES>(p, ti, kb_begin, kb_end, it, ew,
-                                            sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag))
-                    break;
-                it += (uint32_t)(kb_end - kb_begin);
+                const int n = kb_end - kb_begin;
+                bool bad = false, ok = lt > 0 || sf_ok0;
+                // (the first tile's first window was converted after the dependency wait)
+                for (int w0 = lt == 0 ? 8 : 0; w0 < n && ok; w0 += 8) {
+                    SfWindow f;
+                    sf_fetch(p, ti, kb_begin, n, w0, ew, f);
+                    ok = sf_put<STAGES>(p, ti, kb_begin, n, w0, it, ew, f, sbase + C_::OFF_SF,
+                                        C_::CHUNK_BYTES, bars, abort_flag, bad);
+                }
+                if (__any_sync(0xffffffffu, bad) && lane == 0)
+                    record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
+                if (!ok) break;
+                it += (uint32_t)n;
             }
             const int acc = lt % NUM_ACC;
             const uint32_t acc_par = (uint32_t)((lt / NUM_ACC) & 1);
