@@ -154,16 +154,16 @@ __device__ __forceinline__ void sf_fetch(const GemmParams &p, const Tile &ti, in
     const bool isB = ew >= kSfWarps;
     const int sl = lane & 7;
     const int r0 = (ew % kSfWarps) * 16 + (lane >> 3);
-    const float *base = isB ? p.sb : p.sa;
-    const int64_t g0 = isB ? (int64_t)ti.n0 : (int64_t)ti.row0;
-    const int64_t gend = isB ? p.N : (int64_t)ti.row_end;
+    const int64_t g0 = (isB ? (int64_t)ti.n0 : (int64_t)ti.row0) + r0;  // row of j = 0
+    const int64_t left = (isB ? p.N : (int64_t)ti.row_end) - g0;     // rows from it on
     const bool live = w0 + sl < n;
     const int64_t k0 = (int64_t)(kb_begin + w0 + sl) * 4;  // this lane's first scale column
+    const float *row = (isB ? p.sb : p.sa) + (live && left > 0 ? g0 * p.sfc + k0 : 0);
+    const int64_t step = 4 * p.sfc;  // four rows on
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int64_t grow = g0 + r0 + 4 * j;
-        const bool valid = live && grow < gend;
-        const float *src = base + (valid ? grow * p.sfc + k0 : 0);
+        const bool valid = live && 4 * j < left;
+        const float *src = row + (valid ? j * step : 0);
         if ((p.sfc & 3) == 0) {
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (valid) x = __ldg(reinterpret_cast<const uint4 *>(src));
@@ -179,49 +179,80 @@ __device__ __forceinline__ void sf_fetch(const GemmParams &p, const Tile &ti, in
     }
 }
 
-// Returns false when the CTA is aborting.
+// UE8M0 codes of four fp32 scales in one word (byte q: scale q): their
+// exponent fields, which is ue8m0_code's result for every input (a NaN's
+// exponent field is 0xFF).  ue8m0_code's checks run only when some scale is
+// not a positive normal power of two (a set sign or mantissa bit, an
+// exponent field 0 or 0xFF).
+__device__ __forceinline__ uint32_t ue8m0_word(const uint32_t (&x)[4], bool &bad) {
+    const uint32_t w = __byte_perm(__byte_perm(x[0] << 1, x[1] << 1, 0x0073u),
+                                   __byte_perm(x[2] << 1, x[3] << 1, 0x0073u), 0x5410u);
+    if ((((x[0] | x[1] | x[2] | x[3]) & 0x807FFFFFu) | __vcmpeq4(w, 0u) | __vcmpeq4(w, ~0u)) != 0u) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) (void)ue8m0_code(x[q], bad);
+    }
+    return w;
+}
+
+// Returns false when the CTA is aborting.  With fresh = true (the first window
+// of a CTA's first tile: its first STAGES stages were never used) those
+// stages are filled without waiting and published with one proxy fence.
 template <int STAGES>
 __device__ __forceinline__ bool sf_put(const GemmParams &p, const Tile &ti, int kb_begin, int n,
                                        int w0, uint32_t it, int ew, const SfWindow &f,
                                        uint32_t sf_base, uint32_t chunk_bytes, uint64_t *bars,
-                                       volatile int *abort_flag, bool &bad) {
+                                       volatile int *abort_flag, bool &bad, bool fresh) {
     const int lane = threadIdx.x & 31;
     const bool isB = ew >= kSfWarps;
     const int sl = lane & 7;
     const int r0 = (ew % kSfWarps) * 16 + (lane >> 3);
-    const int64_t g0 = isB ? (int64_t)ti.n0 : (int64_t)ti.row0;
-    const int64_t gend = isB ? p.N : (int64_t)ti.row_end;
+    const int64_t left = (isB ? p.N : (int64_t)ti.row_end) -
+                         ((isB ? (int64_t)ti.n0 : (int64_t)ti.row0) + r0);
     const uint32_t half = isB ? kBM * 4u : 0u;
     const bool live = w0 + sl < n;
     const int64_t k0 = (int64_t)(kb_begin + w0 + sl) * 4;
+    const bool whole = k0 + 4 <= p.sfc;  // no K block of this step past K / 32
     uint32_t word[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         word[j] = 0x7F7F7F7Fu;
-        if (live && g0 + r0 + 4 * j < gend) {
-            word[j] = 0;
+        if (live && 4 * j < left) {
+            if (whole) {
+                word[j] = ue8m0_word(f.v[j], bad);
+            } else {
+                word[j] = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                word[j] |= (k0 + q < p.sfc ? ue8m0_code(f.v[j][q], bad) : 127u) << (8 * q);
+                for (int q = 0; q < 4; ++q)
+                    word[j] |= (k0 + q < p.sfc ? ue8m0_code(f.v[j][q], bad) : 127u) << (8 * q);
+            }
         }
     }
+    auto put = [&](uint32_t stage) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t r = (uint32_t)(r0 + 4 * j);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes + half +
+                                                         16u * (r & 31u) + 4u * (r >> 5)),
+                         "r"(word[j])
+                         : "memory");
+        }
+    };
     const int steps = n - w0 < 8 ? n - w0 : 8;
-    for (int t = 0; t < steps; ++t) {  // warp-uniform
+    int t0 = 0;
+    if (fresh) {
+        t0 = steps < STAGES ? steps : STAGES;
+        if (sl < t0) put((it + (uint32_t)sl) % STAGES);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane < t0) ptx::mbar_arrive(ptx::smem_addr(&bars[(it + (uint32_t)lane) % STAGES]));
+    }
+    for (int t = t0; t < steps; ++t) {  // warp-uniform
         const uint32_t gi = it + (uint32_t)(w0 + t);
         const uint32_t stage = gi % STAGES, phase = (gi / STAGES) & 1u;
         if (!wait_bar_warp(ptx::smem_addr(&bars[STAGES + stage]), phase ^ 1u, abort_flag, p,
                            5 * 256 + stage))
             return false;
-        if (sl == t) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t r = (uint32_t)(r0 + 4 * j);
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(sf_base + stage * chunk_bytes + half +
-                                                             16u * (r & 31u) + 4u * (r >> 5)),
-                             "r"(word[j])
-                             : "memory");
-            }
-        }
+        if (sl == t) put(stage);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[stage]));
@@ -492,7 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool bad = false;
             sf_fetch(p, ti, kb0, n, 0, warp - kEpiWarp0, f);
             sf_ok0 = sf_put<STAGES>(p, ti, kb0, n, 0, 0u, warp - kEpiWarp0, f,
-                                    sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag, bad);
+                                    sbase + C_::OFF_SF, C_::CHUNK_BYTES, bars, abort_flag, bad,
+                                    true);
             if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
         }
     }
@@ -756,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     SfWindow f;
                     sf_fetch(p, ti, kb_begin, n, w0, ew, f);
                     ok = sf_put<STAGES>(p, ti, kb_begin, n, w0, it, ew, f, sbase + C_::OFF_SF,
-                                        C_::CHUNK_BYTES, bars, abort_flag, bad);
+                                        C_::CHUNK_BYTES, bars, abort_flag, bad, false);
                 }
                 if (__any_sync(0xffffffffu, bad) && lane == 0)
                     record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
