@@ -83,7 +83,7 @@ struct PairCfg {
     static constexpr bool kBlock = MODE != kModeTensor;
     static_assert(kBlock || F4 == 0 || F4 == 3, "FP4-rate MMAs are block-scaled");
     static_assert(F4 != 3 || !kBlock, "TF32 operands carry their scales (per-tensor mode)");
-    static constexpr int STAGES = F4 == 2 ? 5 : 6;
+    static constexpr int STAGES = F4 == 2 ? 5 : kBlock ? 6 : 7;
     // K groups of packed scales per stage: 128-wide (FP8, MXFP4) or 64-wide (NVFP4)
     static constexpr int G = F4 == 2 ? 4 : F4 == 1 ? 2 : 1;
     static constexpr int CHUNK = kBlock ? G * (kSfaBytes + kSfbBytes) : 0;  // packed scales per stage
