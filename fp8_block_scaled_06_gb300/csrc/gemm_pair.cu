@@ -7,7 +7,8 @@
 // latency (measured tensor-pipe activity 64%).  A cluster of two CTAs
 // computes a 256x256 tile with one MMA stream: each CTA loads its own 128 rows
 // of A and 128 rows (one half) of B, 32 KB per K step, so each SM holds six
-// stages and the same MMA work per SM needs two thirds of the bytes.
+// stages (seven per-tensor, without scale chunks) and the same MMA work per
+// SM needs two thirds of the bytes.
 //
 // Roles (640 threads per CTA, as in the single-CTA kernel):
 //   warp 0   both CTAs: TMA producer for the CTA's own halves; both complete
