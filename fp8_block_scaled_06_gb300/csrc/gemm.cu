@@ -49,6 +49,11 @@ namespace {
 
 constexpr int kThreads = 640;  // 20 warps
 constexpr int kMaxSplit = 4;   // K-split cluster size (clusters of <= 4 CTAs co-schedule)
+// Per-tensor few-tile shapes with fewer K steps than this run one CTA per
+// 128 x 128 tile instead of splitting K (block-scaled ones keep the split:
+// it converts their scales in the kernel, where single CTAs need the packing
+// kernel's extra launch)
+constexpr int kMinSplitKbTensor = 16;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
 // Block-scaled split-K: the epilogue warps convert the fp32 block scales (128
@@ -1022,7 +1027,8 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     // Few output tiles: 128-wide tiles, K split over a cluster of S CTAs per
     // tile (S a power of two <= kMaxSplit and <= the K blocks, S * tiles <= SMs,
     // and every cluster resident at once).
-    if (tiles * 2 <= num_sms && num_kb >= 2) {
+    const bool split_ok = num_kb >= 2 && (mode != kModeTensor || num_kb >= kMinSplitKbTensor);
+    if (tiles * 2 <= num_sms && split_ok) {
         const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
         int S = 1;
         while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) {
@@ -1038,6 +1044,14 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
             kc.grid = (int)(tiles128 * S);
             return kc;
         }
+    }
+    if (mode == kModeTensor && tiles * 2 <= num_sms) {
+        // few tiles, short K: one CTA per 128 x 128 tile, two accumulators
+        kc.BN = 128;
+        kc.b_rows = 128;
+        const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+        kc.grid = (int)(t128 < num_sms ? t128 : num_sms);
+        return kc;
     }
     // At least a wave of tiles: 256 x 256 tiles on CTA pairs.
     if (tiles >= num_sms) {
@@ -1064,6 +1078,9 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
         if (split)
             return out_f32 ? launch_one<kModeTensor, 128, 1, kSplitStages, true, true>(maps, p, kc, stream)
                            : launch_one<kModeTensor, 128, 1, kSplitStages, false, true>(maps, p, kc, stream);
+        if (kc.BN == 128)  // few tiles, short K
+            return out_f32 ? launch_one<kModeTensor, 128, 2, 6, true, false>(maps, p, kc, stream)
+                           : launch_one<kModeTensor, 128, 2, 6, false, false>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeTensor, 256, 2, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeTensor, 256, 2, 4, false, false>(maps, p, kc, stream);
     } else if (mode == kModeBlock) {
