@@ -30,6 +30,25 @@ namespace fp8g {
 
 namespace {
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous one on the stream finishes; it calls grid_dep_wait before any
+// global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr int kKgPerBlock = 8;
 constexpr int kThreadsPack = 128;
 constexpr int kRowsPerPass = kThreadsPack / kKgPerBlock;  // 16
@@ -50,6 +69,10 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
     __shared__ int32_t row_off[FP8G_MAX_EXPERTS + 1];
     __shared__ int32_t rt_off[FP8G_MAX_EXPERTS + 1];
     __shared__ uint32_t words[kKgPerBlock][kBM];  // code word of (K group, row of the tile)
+    // Launched programmatically: the blocks may be placed while the previous
+    // kernel on the stream still runs (the last wave of a GEMM leaves SMs
+    // idle), but touch global memory only after it completed.
+    ptx::grid_dep_wait();
     ptx::grid_dep_launch();  // the GEMM may start its prologue now
     const bool first = (int)blockIdx.z < a.nz;
     const PackJob &j = first ? a : b;
@@ -182,7 +205,8 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int
                                                         int64_t sfc, int32_t E) {
     __shared__ uint32_t words[8][kBM];
     __shared__ int64_t base_lim[2];
-    ptx::grid_dep_launch();  // the GEMM may start its prologue now
+    ptx::grid_dep_wait();    // global memory only after the previous kernel (launched
+    ptx::grid_dep_launch();  // programmatically); the GEMM may start its prologue now
     const PackNv &j = blockIdx.z == 0 ? a : b;
     const int rt = blockIdx.y;
     if (rt >= j.n_rt) return;  // block-uniform
@@ -245,8 +269,7 @@ cudaError_t launch_pack_nvfp4(const uint8_t *sfa, int64_t rows_a, int32_t n_rt_a
     const PackNv ja{sfa, rows_a, n_rt_a, dst_a, counts};
     const PackNv jb{sfb, rows_b, n_rt_b, dst_b, nullptr};
     const dim3 grid((unsigned)((n_kg + 7) / 8), (unsigned)ny, (unsigned)(1 + z_b));
-    pack_nvfp4_kernel<<<grid, 256, 0, s>>>(ja, jb, n_kg, sfc, E);
-    return cudaGetLastError();
+    return launch_programmatic(pack_nvfp4_kernel, grid, dim3(256), s, ja, jb, n_kg, sfc, E);
 }
 
 size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
@@ -262,8 +285,8 @@ cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc
     const int ny = ja.n_rt > jb.n_rt ? ja.n_rt : jb.n_rt;
     if (nz <= 0 || ny <= 0) return cudaSuccess;
     dim3 grid((unsigned)((n_kg + kKgPerBlock - 1) / kKgPerBlock), (unsigned)ny, (unsigned)nz);
-    pack_scales_kernel<<<grid, kThreadsPack, 0, s>>>(ja, jb, sfc, n_kg, E, status);
-    return cudaGetLastError();
+    return launch_programmatic(pack_scales_kernel, grid, dim3(kThreadsPack), s, ja, jb, sfc, n_kg,
+                               E, status);
 }
 
 }  // namespace fp8g
