@@ -502,7 +502,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     uint8_t *pkA = static_cast<uint8_t *>(ws);
     uint8_t *pkB = pkA + bytesA;
     PackArgs pa{sa, M, 0, p.n_rtA, a_read ? 1 : 0, pkA, mode == kModeGrouped ? counts : nullptr, 0};
-    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, repB ? 1 : 0};
+    PackArgs pb{sb, N, N, p.n_rtB, zB, pkB, nullptr, repB ? 1 : 0,
+                mode == kModeGrouped ? counts : nullptr};
     cudaError_t e = launch_pack_scales(pa, pb, p.sfc, num_kg, E, di.status, stream);
     p.sfa_pk = pkA;
     p.sfb_pk = pkB;

@@ -143,6 +143,25 @@ fp8g_status device_ready();
 // two operands (nz = 0 skips one): src [nz][z_rows][sfc] (rows_total valid
 // rows per z), dst chunks ((z * n_kg + kg) * n_rt + rt) * 512; counts != null
 // numbers A's row tiles per expert.
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous one on the stream finishes; it calls grid_dep_wait before any
+// global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 struct PackArgs {
     const float *src;
     int64_t rows_total, z_rows;
@@ -150,6 +169,7 @@ struct PackArgs {
     uint8_t *dst;
     const int32_t *counts;
     int32_t rep;  // B of single-CTA 256-wide tiles: 4 KB per (z, kg, 256-row tile), replicated for tcgen05.cp 128x256b
+    const int32_t *zskip = nullptr;  // grouped B: matrices z with zskip[z] <= 0 (experts without rows) are skipped
 };
 // NVFP4: E4M3 scale codes [rows, K/16] -> the same 512-byte chunks, a K group
 // being 64 wide (4 blocks of 16, one MMA's word), the four groups of a

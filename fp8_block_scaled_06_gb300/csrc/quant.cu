@@ -30,6 +30,7 @@
 // HBM-bound elementwise kernels: 16-byte loads, 8-byte (E2M1: 4-byte; FP6:
 // three 2-byte) stores, a grid of a few CTAs per SM striding over the output.
 #include "internal.h"
+#include "ptx.cuh"
 #include "quant_math.cuh"
 
 namespace fp8g {
@@ -105,6 +106,9 @@ template <int FMT, bool BF16, bool LITERAL>
 __global__ void __launch_bounds__(kQThreads) quant_block32_kernel(RowMap m, int64_t n_rows,
                                                                  uint8_t *__restrict__ q,
                                                                  float *__restrict__ scales) {
+    // launched programmatically: global memory only after the previous kernel
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();  // a GEMM's scale packing may be placed now
     constexpr int U = 2;  // groups per thread and pass
     const int64_t gpr = m.cols / 8;  // groups of 8 per row
     const int64_t wbase = threadIdx.x & ~31;
@@ -316,14 +320,12 @@ cudaError_t launch_rows(const RowMap &m, int64_t n_rows, int32_t block, uint8_t 
     if (n_rows == 0 || m.cols == 0) return cudaSuccess;
     const int64_t cap = (int64_t)num_sms * 8;  // 8 CTAs of 256 threads per SM
     const unsigned blocks = (unsigned)(n_rows < cap ? n_rows : cap);
-    if (block == 32) {
-        quant_block32_kernel<FMT, BF16, false><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
-        return cudaGetLastError();
-    }
-    if (block == FP8G_BLOCK32_LITERAL) {
-        quant_block32_kernel<FMT, BF16, true><<<blocks, kQThreads, 0, s>>>(m, n_rows, q, scales);
-        return cudaGetLastError();
-    }
+    if (block == 32)
+        return launch_programmatic(quant_block32_kernel<FMT, BF16, false>, dim3(blocks),
+                                   dim3(kQThreads), s, m, n_rows, q, scales);
+    if (block == FP8G_BLOCK32_LITERAL)
+        return launch_programmatic(quant_block32_kernel<FMT, BF16, true>, dim3(blocks),
+                                   dim3(kQThreads), s, m, n_rows, q, scales);
     cudaError_t e = cudaMemsetAsync(scales, 0, sizeof(float), s);
     if (e != cudaSuccess) return e;
     amax_kernel<BF16><<<blocks, kQThreads, 0, s>>>(m, n_rows, reinterpret_cast<unsigned int *>(scales));

@@ -30,24 +30,6 @@ namespace fp8g {
 
 namespace {
 
-// Launch with programmatic stream serialization: the kernel may begin while
-// the previous one on the stream finishes; it calls grid_dep_wait before any
-// global memory access.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_programmatic(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
-                                Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
 
 constexpr int kKgPerBlock = 8;
 constexpr int kThreadsPack = 128;
@@ -60,6 +42,7 @@ struct PackJob {
     uint8_t *dst;
     const int32_t *counts;  // grouped A: expert-local row tiles
     int32_t rep;            // replicated 256-row layout (B of 256-wide tiles)
+    const int32_t *zskip;   // grouped B: matrix z of an expert without rows is not packed
 };
 
 // blockIdx.z < a.nz packs operand a (z = blockIdx.z), the rest operand b.
@@ -79,6 +62,9 @@ __global__ void __launch_bounds__(kThreadsPack) pack_scales_kernel(PackJob a, Pa
     const int z = first ? (int)blockIdx.z : (int)blockIdx.z - a.nz;
     const int rt = blockIdx.y;
     if (rt >= j.n_rt) return;  // block-uniform
+    // (no tile of the GEMM reads an empty expert's chunks; its scales are
+    // neither packed nor checked)
+    if (j.zskip != nullptr && j.zskip[z] <= 0) return;
     int64_t base, limit;
     if (j.counts != nullptr) {
         if (threadIdx.x == 0) {
@@ -210,6 +196,8 @@ __global__ void __launch_bounds__(256) pack_nvfp4_kernel(PackNv a, PackNv b, int
     const PackNv &j = blockIdx.z == 0 ? a : b;
     const int rt = blockIdx.y;
     if (rt >= j.n_rt) return;  // block-uniform
+    // grouped: an expert without rows has no tile, its B chunks are not packed
+    if (blockIdx.z > 0 && a.counts != nullptr && a.counts[blockIdx.z - 1] <= 0) return;
     const int64_t z = blockIdx.z == 0 ? 0 : (int64_t)blockIdx.z - 1;
     const uint8_t *src = j.src + z * j.rows * sfc;
     uint8_t *dst = j.dst + z * n_kg * j.n_rt * 512;
@@ -279,8 +267,8 @@ size_t packed_scale_bytes(int32_t n_kg, int32_t n_rt, int32_t z) {
 cudaError_t launch_pack_scales(const PackArgs &a, const PackArgs &b, int64_t sfc, int32_t n_kg,
                                int32_t E, unsigned int *status, cudaStream_t s) {
     if (n_kg <= 0) return cudaSuccess;
-    PackJob ja{a.src, a.rows_total, a.z_rows, a.n_rt, a.nz, a.dst, a.counts, a.rep};
-    PackJob jb{b.src, b.rows_total, b.z_rows, b.n_rt, b.nz, b.dst, b.counts, b.rep};
+    PackJob ja{a.src, a.rows_total, a.z_rows, a.n_rt, a.nz, a.dst, a.counts, a.rep, a.zskip};
+    PackJob jb{b.src, b.rows_total, b.z_rows, b.n_rt, b.nz, b.dst, b.counts, b.rep, b.zskip};
     const int nz = ja.nz + jb.nz;
     const int ny = ja.n_rt > jb.n_rt ? ja.n_rt : jb.n_rt;
     if (nz <= 0 || ny <= 0) return cudaSuccess;
