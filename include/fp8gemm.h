@@ -187,7 +187,8 @@ FP8G_API fp8g_status fp8_gemm_blockscaled_noalloc(const void *A, const void *B, 
  * B: [E, N, K]; sfa: fp32 [total_rows, K/32]; sfb: fp32 [E, N, K/32];
  * C: [total_rows, N]; counts: DEVICE int32[E], each >= 0, summing to total_rows
  * (checked on the device: a mismatch records FP8G_ERR_INVALID_ARG and writes
- * no output).  Empty experts produce no tiles and no rows.
+ * no output).  Empty experts produce no tiles and no rows; their weights and
+ * weight scales are not read (so their scales are not checked either).
  * offsets_out (nullable): device int32[E+1] receives the exclusive prefix.
  * tile_map_out (nullable): device int32[4 * max_tiles] (see fp8g_grouped_plan)
  * receives, for linear tile t, (expert, m_tile, n_tile, 0): experts in index
