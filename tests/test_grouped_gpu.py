@@ -120,6 +120,30 @@ def test_grouped_pair_ragged_sampled():
     assert_within(got, ref, bound, "grouped pair ragged")
 
 
+def test_grouped_empty_expert_scales_not_read():
+    """The weights of an expert without rows are not read: a malformed weight
+    scale there changes nothing (no status, same outputs), while the same
+    scale in an expert with rows records FP8G_ERR_SCALE_FORMAT."""
+    counts = np.array([0, 200, 0, 70], np.int32)
+    N, K = 256, 512
+    w = synth.small_grouped(counts, N, K, seed=81)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C0, _, _, _ = _run_grouped(qa, sa, qb, sb, counts)
+    sb_bad = sb.clone()
+    sb_bad[0, 5, 3] = 0.75       # not a power of two, in empty expert 0
+    sb_bad[2, N - 1, 0] = -4.0   # negative, in empty expert 2
+    C1, _, _, _ = _run_grouped(qa, sa, qb, sb_bad, counts)
+    assert np.array_equal(C0, C1)
+    sb_bad[1, 7, 1] = 0.75       # expert 1 has rows
+    rows = int(counts.sum())
+    C = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_grouped_gemm(qa, qb, sa, sb_bad, C, fp8g.FP8G_OUT_BF16,
+                          torch.from_numpy(counts).cuda(), counts.size, N, K, rows)
+    st, _ = fp8g.fp8_gemm_status()
+    assert st == fp8g.FP8G_ERR_SCALE_FORMAT
+    assert fp8g.fp8_gemm_status()[0] == fp8g.FP8G_OK
+
+
 def test_grouped_counts_mismatch_is_reported():
     counts = np.array([10, 20], np.int32)
     N, K = 128, 128
