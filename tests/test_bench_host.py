@@ -108,3 +108,13 @@ def test_algorithmic_bytes_skip_empty_experts():
     want = rows * K + used * N * K + 4 * (rows + used * N) * K // 32 + rows * N * 2 + 4 * E
     assert bench.algorithmic_bytes(bench.WORKLOADS["moe"], _w(experts=E, counts=counts)) == want
 
+
+
+def test_peak_burst_or_sustained_by_region_length():
+    """Short timed regions are measured against the bf16 burst rate, regions
+    of a second or more against the sustained rate."""
+    peaks = {"bf16": 1901.5, "bf16_sus": 1728.6, "hbm": 6759.2, "src": "measured"}
+    assert bench.bf16_peak_for(peaks, 0.007) == (False, 1901.5)
+    assert bench.bf16_peak_for(peaks, 0.999) == (False, 1901.5)
+    assert bench.bf16_peak_for(peaks, 1.0) == (True, 1728.6)
+    assert bench.bf16_peak_for(peaks, 2.1) == (True, 1728.6)
