@@ -104,6 +104,47 @@ def test_graph_capture_matches_eager():
     _check(C, ref_in, M, N, "graph replay")
 
 
+def test_graph_capture_grouped_from_tokens_two_calls():
+    """The grouped GEMM from bf16 tokens (quantiser, scale packing and GEMM,
+    each kernel placed while its predecessor finishes) captured twice back to
+    back in one graph: replays give the eager bits, for both calls."""
+    counts = np.array([300, 0, 5, 211], np.int32)
+    E, N, K = counts.size, 512, 1024
+    rows = int(counts.sum())
+    tokens = 320
+    g_ = torch.Generator().manual_seed(91)
+    X = torch.randn(tokens, K, generator=g_).to(torch.bfloat16).cuda()
+    idx = torch.randint(0, tokens, (rows,), generator=g_, dtype=torch.int32).cuda()
+    w = synth.small_grouped(counts, N, K, seed=92)
+    qb, sb = fp8g.quantize(w.B.reshape(E * N, K).cuda(), 32)
+    qb, sb = qb.reshape(E, N, K), sb.reshape(E, N, K // 32)
+    dc = torch.from_numpy(counts).cuda()
+
+    def call(C, stream):
+        fp8g.fp8_grouped_gemm_quant(X, fp8g.FP8G_IN_BF16, tokens, idx, qb, sb, C,
+                                    fp8g.FP8G_OUT_BF16, fp8g.FP8G_E4M3, None, fp8g.FP8G_ACT_NONE,
+                                    dc, E, N, K, rows, stream=stream)
+
+    C_eager = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    call(C_eager, None)
+    torch.cuda.synchronize()
+    assert fp8g.fp8_gemm_status()[0] == 0
+    Cs = [torch.full((rows, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for C in Cs:
+                call(C, s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert fp8g.fp8_gemm_status()[0] == 0
+    for C in Cs:
+        assert torch.equal(C, C_eager)
+
+
 def test_shutdown_releases_and_calls_continue():
     (gpu_in, ref_in) = _case(1024, 768, 1024, 11)
     qa, sa, qb, sb = gpu_in
