@@ -421,10 +421,14 @@ def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
                 out_done[b][j].record(s_)
         first[b] = False
 
+    t0 = time.perf_counter()
     for i in range(2 * nbuf):  # warm-up
         step(i)
     torch.cuda.synchronize(device)
-    n = max(20, min(50, steps // 20))
+    est = (time.perf_counter() - t0) / (2 * nbuf)
+    # 50 pipelined steps (the pipeline's fill and drain, one step's copies
+    # each, then weigh 1/50 on the result), fewer for a step above 40 ms
+    n = max(20, min(50, int(2.0 / max(est, 1e-6))))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     start = torch.cuda.Stream(device)
