@@ -467,9 +467,9 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
         });
         return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
     }
-    if (kc.split > 1) {
-        // split-K (few output tiles): the GEMM converts its own scale chunks
-        // from the fp32 scales (p.sa, p.sb; row stride p.sfc)
+    if (kc.split > 1 || kc.inl) {
+        // split-K or single CTAs on few tiles with short K: the GEMM converts
+        // its own scale chunks from the fp32 scales (p.sa, p.sb; row stride p.sfc)
         const cudaError_t e = timed_launch(stream, [&] {
             return launch_gemm(mode, out == FP8G_OUT_F32, maps, p, kc, stream);
         });
@@ -546,6 +546,7 @@ fp8g_status run_nvfp4(int mode, const void *A, const void *B, const uint8_t *sfa
     kc.split = 1;
     kc.cluster = 2;
     kc.pair = true;
+    kc.inl = false;
     GemmParams p{};
     p.M = M;
     p.N = N;

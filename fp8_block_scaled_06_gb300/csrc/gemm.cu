@@ -49,11 +49,10 @@ namespace {
 
 constexpr int kThreads = 640;  // 20 warps
 constexpr int kMaxSplit = 4;   // K-split cluster size (clusters of <= 4 CTAs co-schedule)
-// Per-tensor few-tile shapes with fewer K steps than this run one CTA per
-// 128 x 128 tile instead of splitting K (block-scaled ones keep the split:
-// it converts their scales in the kernel, where single CTAs need the packing
-// kernel's extra launch)
-constexpr int kMinSplitKbTensor = 16;
+// Few-tile shapes with fewer K steps than this run one CTA per 128 x 128 tile
+// instead of splitting K (the split-K exchange costs more than it saves);
+// block-scaled ones convert their scales in the kernel as split-K does
+constexpr int kMinSplitKb = 16;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 16;
 // Block-scaled split-K: the epilogue warps convert the fp32 block scales (128
@@ -422,7 +421,8 @@ __device__ __forceinline__ bool fq_put(const GemmParams &p, const FqIn<BF16> &in
 // FQ (grouped, single CTA): the epilogue warps also quantise A in the kernel
 // (fq_fetch / fq_put) from fp32 (FQ = 1) or bf16 (FQ = 2) activations; the
 // producer loads only B and B's scale chunk.
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0>
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0,
+          bool INL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
@@ -431,7 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   "split-K: 32 x 32 blocks per epilogue warp, staged in the A ring");
     // split-K tiles are few: the kernel converts its own scale chunks instead
     // of reading chunks that a packing kernel wrote
-    constexpr bool kInlineSF = SPLIT && C_::kBlock;
+    // INL: few-tile block-scaled shapes with short K on single CTAs (one tile
+    // each) convert their scales the same way
+    constexpr bool kInlineSF = (SPLIT || INL) && C_::kBlock;
+    static_assert(!INL || (!SPLIT && MODE == kModeBlock && FQ == 0), "inline scales, single CTAs");
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
     static_assert(!SPLIT || MODE != kModeGrouped, "split-K: non-grouped only");
     static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && kEpiWarps * 8 == kBM),
@@ -518,12 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the operand loads
     bool sf_ok0 = true;
     if constexpr (kInlineSF) {
-        if (warp >= kEpiWarp0 && (int32_t)ptx::cluster_id_x() < T) {
-            const int rank = (int)ptx::cluster_rank();
-            const Tile ti = get_tile<MODE, BN>((int32_t)ptx::cluster_id_x(), p, nullptr, nullptr,
-                                               nullptr);
-            const int kb0 = rank * p.num_kb / p.split;
-            const int n = (rank + 1) * p.num_kb / p.split - kb0;
+        const int32_t t0 = SPLIT ? (int32_t)ptx::cluster_id_x() : (int32_t)blockIdx.x;
+        if (warp >= kEpiWarp0 && t0 < T) {
+            const int rank = SPLIT ? (int)ptx::cluster_rank() : 0;
+            const int split = SPLIT ? p.split : 1;
+            const Tile ti = get_tile<MODE, BN>(t0, p, nullptr, nullptr, nullptr);
+            const int kb0 = rank * p.num_kb / split;
+            const int n = (rank + 1) * p.num_kb / split - kb0;
             SfWindow f;
             bool bad = false;
             sf_fetch(p, ti, kb0, n, 0, warp - kEpiWarp0, f);
@@ -912,11 +916,12 @@ roles_done:
     }
 }
 
-template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0>
+template <int MODE, int BN, int NUM_ACC, int STAGES, bool OUT_F32, bool SPLIT, int FQ = 0,
+          bool INL = false>
 cudaError_t launch_one(const GemmMaps &maps, const GemmParams &p, const KernelChoice &kc,
                        cudaStream_t stream) {
     using C_ = Cfg<MODE, BN, NUM_ACC, STAGES, SPLIT>;
-    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT, FQ>;
+    auto kern = gemm_kernel<MODE, BN, NUM_ACC, STAGES, OUT_F32, SPLIT, FQ, INL>;
     // The shared-memory opt-in is per device; the flag races benignly (the
     // attribute set is idempotent).
     static unsigned long long attr_done = 0ull;
@@ -1000,6 +1005,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     kc.split = 1;
     kc.cluster = 1;
     kc.pair = false;
+    kc.inl = false;
     if (mode == kModeGrouped) {
         // at least a wave of 128 x 256 tiles (counting rows as one problem):
         // 256 x 256 tiles on CTA pairs inside each expert
@@ -1027,8 +1033,7 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
     // Few output tiles: 128-wide tiles, K split over a cluster of S CTAs per
     // tile (S a power of two <= kMaxSplit and <= the K blocks, S * tiles <= SMs,
     // and every cluster resident at once).
-    const bool split_ok = num_kb >= 2 && (mode != kModeTensor || num_kb >= kMinSplitKbTensor);
-    if (tiles * 2 <= num_sms && split_ok) {
+    if (tiles * 2 <= num_sms && num_kb >= kMinSplitKb) {
         const int64_t tiles128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
         int S = 1;
         while (S * 2 <= kMaxSplit && S * 2 <= num_kb && tiles128 * S * 2 <= num_sms) {
@@ -1045,10 +1050,12 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
             return kc;
         }
     }
-    if (mode == kModeTensor && tiles * 2 <= num_sms) {
-        // few tiles, short K: one CTA per 128 x 128 tile, two accumulators
+    if (tiles * 2 <= num_sms) {
+        // few tiles, short K: one CTA per 128 x 128 tile, two accumulators;
+        // block-scaled: scales converted in the kernel (no packing kernel)
         kc.BN = 128;
         kc.b_rows = 128;
+        kc.inl = mode == kModeBlock;
         const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
         kc.grid = (int)(t128 < num_sms ? t128 : num_sms);
         return kc;
@@ -1087,6 +1094,9 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
         if (split)
             return out_f32 ? launch_one<kModeBlock, 128, 1, kSplitStages, true, true>(maps, p, kc, stream)
                            : launch_one<kModeBlock, 128, 1, kSplitStages, false, true>(maps, p, kc, stream);
+        if (kc.inl)  // few tiles, short K
+            return out_f32 ? launch_one<kModeBlock, 128, 2, 6, true, false, 0, true>(maps, p, kc, stream)
+                           : launch_one<kModeBlock, 128, 2, 6, false, false, 0, true>(maps, p, kc, stream);
         return out_f32 ? launch_one<kModeBlock, 256, 1, 4, true, false>(maps, p, kc, stream)
                        : launch_one<kModeBlock, 256, 1, 4, false, false>(maps, p, kc, stream);
     } else if (p.xq != nullptr) {

@@ -88,6 +88,7 @@ struct KernelChoice {
     int grid;    // CTAs launched
     int cluster; // CTAs per cluster
     bool pair;   // tcgen05 cta_group::2 kernel (gemm_pair.cu)
+    bool inl;    // block-scaled single CTAs converting their own scales (no packing kernel)
 };
 
 // gemm.cu

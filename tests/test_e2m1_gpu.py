@@ -124,7 +124,7 @@ def _gemm(fa, fb, block, M, N, K, sample=None):
 
 @pytest.mark.parametrize("fa,fb", [(F4, F4), (0, F4), (F4, 1)])
 @pytest.mark.parametrize("block", [False, True])
-@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (1536, 2048, 384)])
+@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (300, 392, 2048), (1536, 2048, 384)])
 def test_e2m1_gemm_full(fa, fb, block, M, N, K):
     _gemm(fa, fb, block, M, N, K)
 

@@ -68,7 +68,8 @@ def _run(qa, sa, qb, sb, fa, fb, block, out, M, N, K):
 
 @pytest.mark.parametrize("fa,fb", PAIRS)
 @pytest.mark.parametrize("block", [False, True])
-@pytest.mark.parametrize("M,N,K", [(300, 392, 256),      # split-K clusters
+@pytest.mark.parametrize("M,N,K", [(300, 392, 256),      # single CTAs, 128 x 128 (few tiles, short K)
+                                   (300, 392, 2048),     # split-K clusters (16 K steps)
                                    (1536, 2048, 384)])   # single-CTA tiles
 def test_gemm_formats_full(fa, fb, block, M, N, K):
     A, B = _operands(M, N, K, seed=M + 7 * fa + 3 * fb)

@@ -27,7 +27,7 @@ def _quant(x, block):
 
 @pytest.mark.parametrize("act", [0, 1, 2])
 @pytest.mark.parametrize("block", [False, True])
-@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (1536, 2048, 256)])
+@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (300, 392, 2048), (1536, 2048, 256)])
 def test_epilogue_full(act, block, M, N, K):
     g = torch.Generator().manual_seed(M + act)
     A = synth.normal((M, K), seed=M + 1)

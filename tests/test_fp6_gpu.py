@@ -149,7 +149,7 @@ def _gemm(fa, fb, block, M, N, K, sample=None):
 @pytest.mark.parametrize("fa,fb", [(E2M3, E2M3), (E3M2, E3M2), (E2M3, E3M2), (0, E3M2),
                                    (E3M2, F4), (E2M3, 1)])
 @pytest.mark.parametrize("block", [False, True])
-@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (1536, 2048, 384)])
+@pytest.mark.parametrize("M,N,K", [(300, 392, 256), (300, 392, 2048), (1536, 2048, 384)])
 def test_fp6_gemm_full(fa, fb, block, M, N, K):
     _gemm(fa, fb, block, M, N, K)
 

@@ -178,10 +178,13 @@ def _block_full(w):
 
 
 # ------------------------------------------------------------------- errors
-@pytest.mark.parametrize("M,N,K,bad_b", [(256, 256, 256, False),    # split-K: in-kernel check
-                                         (200, 392, 320, True),     # split-K, K/32 odd
-                                         (2048, 2048, 256, True)])  # packing kernel's check
-def test_scale_format_error_recorded(M, N, K, bad_b):
+@pytest.mark.parametrize("M,N,K,bad_b,path", [
+    (256, 256, 256, False, "inline"),    # single CTAs, in-kernel check
+    (200, 392, 320, True, "inline"),     # single CTAs, K/32 odd
+    (256, 256, 2048, False, "split"),    # split-K: in-kernel check
+    (200, 392, 2080, True, "split"),     # split-K, K/32 odd
+    (2048, 2048, 256, True, "pack")])    # packing kernel's check
+def test_scale_format_error_recorded(M, N, K, bad_b, path):
     qa = torch.zeros(M, K, dtype=torch.uint8, device="cuda")
     qb = torch.zeros(N, K, dtype=torch.uint8, device="cuda")
     sfa = torch.ones(M, K // 32, device="cuda")
@@ -190,7 +193,9 @@ def test_scale_format_error_recorded(M, N, K, bad_b):
         sfb[N - 1, K // 32 - 1] = -2.0                # negative
     else:
         sfa[3, 2] = 0.75                              # not a power of two
-    assert (fp8g.fp8g_gemm_plan(1, M, N, K)["split_k"] > 1) == (M < 1024)
+    plan = fp8g.fp8g_gemm_plan(1, M, N, K)
+    few = plan["BM"] == 128 and plan["BN"] == 128  # one CTA per 128 x 128 tile: scales inline
+    assert path == ("split" if plan["split_k"] > 1 else "inline" if few else "pack"), plan
     C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     fp8g.fp8_gemm_blockscaled(qa, qb, sfa, sfb, C, fp8g.FP8G_OUT_BF16, M, N, K)
     st, _ = fp8g.fp8_gemm_status()
@@ -225,18 +230,26 @@ def test_plan_reports_tiles():
     assert s["BN"] * (s["grid"] // s["split_k"]) >= 4096
 
 
-@pytest.mark.parametrize("K", [256, 384, 1024, 4096])
-def test_split_k_ranges(K):
-    """Few tiles -> K split over a cluster; ragged K-block counts per rank."""
+@pytest.mark.parametrize("K", [128, 256, 384, 1024, 2048, 2080, 2432, 4096])
+def test_few_tiles_split_k_or_single_cta(K):
+    """Few tiles: from 16 K steps K is split over a cluster (ragged K-block
+    counts per rank: 17 and 19 steps over 4); below, one CTA per 128 x 128
+    tile (block-scaled: scales converted in the kernel, no packing)."""
     M, N = 130, 392
     g = torch.Generator().manual_seed(K)
     A = synth.normal((M, K), seed=K)
     B = synth.normal((N, K), seed=K + 1) * torch.exp(torch.randn(N, 1, generator=g))
-    assert fp8g.fp8g_gemm_plan(1, M, N, K)["split_k"] >= 2
+    steps = -(-K // 128)
+    for block in (0, 1):
+        plan = fp8g.fp8g_gemm_plan(block, M, N, K)
+        if steps >= 16:
+            assert plan["split_k"] >= 2, plan
+        else:
+            assert plan["split_k"] == 1 and plan["BM"] == 128 and plan["BN"] == 128, plan
     C, ref, bound = _block_case(A, B, "bf16")
-    assert_within(C, ref, bound, f"split-K block {M}x{N}x{K}")
+    assert_within(C, ref, bound, f"few tiles block {M}x{N}x{K}")
     C, ref, bound = _tensor_case(A, B, "f32")
-    assert_within(C, ref, bound, f"split-K per-tensor {M}x{N}x{K}")
+    assert_within(C, ref, bound, f"few tiles per-tensor {M}x{N}x{K}")
 
 
 def test_split_k_clusters_all_resident():
