@@ -147,8 +147,9 @@ FP8G_API fp8g_status fp8_gemm(const void *A, const void *B, const float *scale_a
  * FP8G_ERR_SCALE_FORMAT in the status word (the output is then unspecified).
  * K % 32 == 0 (else FP8G_ERR_UNSUPPORTED_SHAPE).  Other rules as fp8_gemm.
  * Runs two kernels on `stream`: the scale packing (scales -> UE8M0 chunks,
- * which also performs the scale check) and the GEMM; split-K shapes (few
- * output tiles, plan split > 1) run the GEMM alone, which then converts and
+ * which also performs the scale check) and the GEMM; shapes with few output
+ * tiles (fewer than SMs / 2 tiles of 128 x 256: plan split > 1, or plan
+ * BM = BN = 128 below 16 K steps) run the GEMM alone, which then converts and
  * checks the scales of each K step itself.
  */
 FP8G_API fp8g_status fp8_gemm_blockscaled(const void *A, const void *B, const float *sfa,
