@@ -318,6 +318,25 @@ def run_once(fp8g, wl, w, t, C, stream):
                                   wl["K"], stream)
 
 
+def gemm_alone(fp8g, wl, t, C, stream, prepare=False):
+    """The grouped GEMM of a call from tokens on its quantised rows: the
+    two-call path's second call; the one-call path runs the same GEMM kernel
+    after its quantiser (prepare=True first writes the quantised rows, which
+    the one-call path keeps to itself).  None for other workloads."""
+    if wl["kind"] != "grouped_quant" or wl["path"] not in ("1call", "2call"):
+        return None
+    E, N, K = t["qb"].shape
+    if prepare:
+        fp8g.fp8g_quantize_rows(t["X"], fp8g.FP8G_IN_BF16, t["X"].shape[0], K, t["idx"],
+                                t["tmp_qa"].shape[0], 32, fp8g.FP8G_E4M3, t["tmp_qa"],
+                                t["tmp_sa"], stream)
+        return True
+    out = fp8g.FP8G_OUT_BF16 if C.dtype == torch.bfloat16 else fp8g.FP8G_OUT_F32
+    fp8g.fp8_grouped_gemm(t["tmp_qa"], t["qb"], t["tmp_sa"], t["sb"], C, out, t["counts"], E, N,
+                          K, t["tmp_qa"].shape[0], None, None, stream)
+    return True
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
 # of the dominant kernel, from the ncu captures summarised in profiles/.
 # Valid only for the kernel source those captures measured: an entry leaves
@@ -354,19 +373,24 @@ def tf32_route(fp8g, wl) -> bool:
 
 def launches_per_call(fp8g, wl) -> int:
     """Kernels one call launches: the GEMM, plus the scale-packing kernel on the
-    block-scaled paths that do not split K (split-K converts scales itself)."""
+    block-scaled plans that take packed scales (split-K, single CTAs on 128 x
+    128 tiles and grouped 128 x 128 tiles convert the scales themselves), plus
+    the quantiser of the routed rows (grouped calls from tokens)."""
     if wl["kind"] == "tensor":
         return 1
-    if wl["kind"] in ("grouped", "nvfp4", "grouped_nvfp4"):
+    if wl["kind"] in ("nvfp4", "grouped_nvfp4"):
         return 2
+    if wl["kind"] == "grouped":
+        # 128 x 128 tiles convert their own scales; CTA pairs take them packed
+        return 1 if fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128 else 2
     if wl["kind"] == "grouped_quant":
-        # quantiser (unless fused into the GEMM), B's scale packing, GEMM
-        fused = (wl["path"] == "fused" and
-                 fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128)
-        return 2 if fused else 3
+        # 128 x 128 tiles: quantiser + GEMM, or (fused) B's scale packing +
+        # GEMM; CTA pairs: quantiser, scale packing, GEMM
+        return 2 if fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128 else 3
     if wl.get("literal"):
         return 3 if tf32_route(fp8g, wl) else 1
-    return 1 if fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])["split_k"] > 1 else 2
+    plan = fp8g.fp8g_gemm_plan(1, wl["M"], wl["N"], wl["K"])
+    return 1 if plan["BM"] == 128 and plan["BN"] == 128 else 2
 
 
 def e2e_pipelined(fp8g, wl, w, t, C, device, steps, lanes=1):
@@ -615,6 +639,13 @@ def main():
     TAIL_MS = 250.0
     n_tail = int(min(20000, max(1, -(-TAIL_MS // call_ms_est))))
     kpass = launches_per_call(fp8g, wl) > 1
+    # calls from tokens whose GEMM is a call of its own that launches only
+    # the GEMM kernel (the two-call path's second call; the one-call path
+    # runs the same kernel): the kernel pass runs that call back to back,
+    # timed over the loop (events around each launch would add a launch gap
+    # of a few us to every one)
+    alone = (kpass and wl["kind"] == "grouped_quant" and wl["path"] in ("1call", "2call") and
+             fp8g.fp8g_grouped_plan(wl["N"], wl["K"], wl["M"], 8)["BM"] == 128)
     nk = max(3, min(args.steps, 300))
     sampler = ClockSampler(local)
     sampler.start()
@@ -630,13 +661,25 @@ def main():
         run_once(fp8g, wl, w, sets[i % copies], C, stream)
     ev1.record(stream)
     kms = []
-    if kpass:
+    if alone:
+        for i in range(min(copies, nk)):
+            gemm_alone(fp8g, wl, sets[i], C, stream, prepare=True)
+        ka0 = torch.cuda.Event(enable_timing=True)
+        ka1 = torch.cuda.Event(enable_timing=True)
+        ka0.record(stream)
+        for i in range(nk):
+            gemm_alone(fp8g, wl, sets[i % copies], C, stream)
+        ka1.record(stream)
+    elif kpass:
         fp8g.fp8g_kernel_timing_begin(nk)
         for i in range(nk):
             run_once(fp8g, wl, w, sets[i % copies], C, stream)
     ev1.synchronize()
     wall = time.perf_counter() - wall0
-    if kpass:
+    if alone:
+        ka1.synchronize()
+        kms = [ka0.elapsed_time(ka1) / nk]
+    elif kpass:
         kms = fp8g.fp8g_kernel_timing_end(nk)   # waits for the pass (every call records)
     for i in range(n_tail):
         run_once(fp8g, wl, w, sets[(args.steps + i) % copies], C, stream)
@@ -692,11 +735,18 @@ def main():
                 "unit": "GB/s", "frac": round(k_hbm_gbs / peaks["hbm"], 4),
                 "call_achieved": round(hbm_gbs, 1), "call_frac": round(hbm_gbs / peaks["hbm"], 4)}
     roof["traffic"] = TRAFFIC_BYTES.get(args.workload)
-    roof["timed"] = (f"GEMM kernel alone: mean of {len(kms)} launches, CUDA events the library "
-                     f"records on the launching stream around the launch (a pass right after "
-                     f"the timed region); call_* = the whole call (packing or dequantising "
-                     f"kernels + GEMM kernel) over the timed region" if kms else
-                     "the GEMM kernel (the call's only launch) over the timed region")
+    if alone:
+        roof["timed"] = (f"GEMM kernel alone: {nk} back-to-back fp8_grouped_gemm calls on the "
+                         f"quantised rows (the GEMM kernel their only launch), CUDA events around "
+                         f"the loop (a pass right after the timed region); call_* = the whole "
+                         f"step (quantiser + GEMM) over the timed region")
+    elif kms:
+        roof["timed"] = (f"GEMM kernel alone: mean of {len(kms)} launches, CUDA events the "
+                         f"library records on the launching stream around the launch (a pass "
+                         f"right after the timed region); call_* = the whole call (quantising, "
+                         f"packing or dequantising kernels + GEMM kernel) over the timed region")
+    else:
+        roof["timed"] = "the GEMM kernel (the call's only launch) over the timed region"
     roof["kernel_ms"] = round(kernel_ms, 5)
     kind_ratio = "fp4 = 6" if f4 else ("tf32 = 1.1/2.25" if tf32 else "fp8 = 2")
     roof["peak_source"] = (f"{peaks['src']}: {kind_ratio} x bf16 "

@@ -387,7 +387,8 @@ fp8g_status run_gemm(int mode, const void *A, const void *B, const float *sa, co
     DevInfo di;
     st = device_info(di);
     if (st != FP8G_OK) return st;
-    const KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
+    KernelChoice kc = choose_kernel(mode, M, N, K, di.num_sms);
+    if (fq != nullptr) kc.inl = false;  // the fused quantiser takes B's packed scale chunks
     // MXFP4 on CTA pairs runs at the FP4 rate (kind::mxf4, 256 K elements per
     // stage); every other E2M1 case takes the FP8-rate MMA with 4-bit loads
     const bool f4 = kc.pair && mode != kModeTensor && a_fmt == FP8G_E2M1 &&

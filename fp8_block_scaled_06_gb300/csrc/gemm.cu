@@ -136,9 +136,10 @@ __device__ __forceinline__ Tile get_tile(int32_t t, const GemmParams &p, const i
     return ti;
 }
 
-// Block-scaled split-K, epilogue warp ew (of 2 kSfWarps): writes the UE8M0
-// chunk (the layout of scales.cu: byte 16 d + 4 w + j = row 32 w + d, K block
-// j; A's 128 rows, then B's) of each of the tile's K steps into the ring, after
+// Block-scaled kernels that convert their own scales (split-K, single CTAs on
+// few tiles, grouped single CTAs), epilogue warp ew (of 2 kSfWarps): writes
+// the UE8M0 chunk (the layout of scales.cu: byte 16 d + 4 w + j = row 32 w +
+// d, K block j; A's 128 rows, then B's) of each of the tile's K steps into the ring, after
 // the stage's empty barrier, and counts one arrival per warp and stage on its
 // full barrier.  Warps 0..7 take A's rows, 8..15 B's, 16 rows each.  K steps
 // go in windows of 8: lane (i, s) = (lane / 8, lane % 8) reads the 16 bytes of
@@ -162,7 +163,9 @@ __device__ __forceinline__ void sf_fetch(const GemmParams &p, const Tile &ti, in
     const int64_t left = (isB ? p.N : (int64_t)ti.row_end) - g0;     // rows from it on
     const bool live = w0 + sl < n;
     const int64_t k0 = (int64_t)(kb_begin + w0 + sl) * 4;  // this lane's first scale column
-    const float *row = (isB ? p.sb : p.sa) + (live && left > 0 ? g0 * p.sfc + k0 : 0);
+    // grouped: B's scales are E matrices of N rows (ti.e = 0 otherwise)
+    const int64_t gz = isB ? (int64_t)ti.e * p.N + g0 : g0;
+    const float *row = (isB ? p.sb : p.sa) + (live && left > 0 ? gz * p.sfc + k0 : 0);
     const int64_t step = 4 * p.sfc;  // four rows on
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -434,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // INL: few-tile block-scaled shapes with short K on single CTAs (one tile
     // each) convert their scales the same way
     constexpr bool kInlineSF = (SPLIT || INL) && C_::kBlock;
-    static_assert(!INL || (!SPLIT && MODE == kModeBlock && FQ == 0), "inline scales, single CTAs");
+    static_assert(!INL || (!SPLIT && (MODE == kModeBlock || MODE == kModeGrouped) && FQ == 0),
+                  "inline scales, single CTAs");
     static_assert(!kInlineSF || (BN == kBM && kEpiWarps == 2 * kSfWarps), "inline scale layout");
     static_assert(!SPLIT || MODE != kModeGrouped, "split-K: non-grouped only");
     static_assert(!FQ || (MODE == kModeGrouped && !SPLIT && kEpiWarps * 8 == kBM),
@@ -516,11 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
     int32_t T = (int32_t)p.T;
-    // Split-K block scales: the epilogue warps convert the first window of
-    // the first tile's K steps right away, in one stretch of code, ahead of
-    // the operand loads
+    // Block scales converted in the kernel (split-K, single CTAs on few
+    // tiles): the epilogue warps convert the first window of the first tile's
+    // K steps right away, in one stretch of code, ahead of the operand loads.
+    // (Grouped kernels know their tiles only after the prefix sums below.)
     bool sf_ok0 = true;
-    if constexpr (kInlineSF) {
+    if constexpr (kInlineSF && MODE != kModeGrouped) {
         const int32_t t0 = SPLIT ? (int32_t)ptx::cluster_id_x() : (int32_t)blockIdx.x;
         if (warp >= kEpiWarp0 && t0 < T) {
             const int rank = SPLIT ? (int)ptx::cluster_rank() : 0;
@@ -778,6 +783,89 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (have_prev) (void)drain_store(prev);
+    } else if (kInlineSF && MODE == kModeGrouped && warp >= kEpiWarp0) {
+        // ===== grouped: scale conversion + epilogue =====
+        // Each warp converts its 16 rows' scales for every K step of this
+        // CTA's tiles (windows of 8 steps: sf_fetch / sf_put), and drains /
+        // stores the previous tile's accumulator once the next tile's first
+        // window is in the ring: those steps wait only for the previous
+        // tile's MMAs, and a tile's first MMA waits only for the drain of the
+        // tile NUM_ACC before it, which came earlier, so neither order can
+        // deadlock.  The next window's loads are issued before the current
+        // one is converted, so they are in flight across a drain as well.
+        const int ew = warp - kEpiWarp0;
+        const int q = warp & 3;
+        const int col0 = (ew >> 2) * C_::CW;
+        const int n = p.num_kb;
+        int32_t ltd = 0;  // tiles drained
+        uint32_t it = 0;  // K steps converted before the current tile (the ring's counter)
+        bool bad = false;
+        Tile prev{};
+        bool have_prev = false;
+        auto drain_store = [&](const Tile &ti) -> bool {
+            const int acc = ltd % NUM_ACC;
+            if (!wait_bar_warp(bar_accf(acc), (uint32_t)((ltd / NUM_ACC) & 1), abort_flag, p,
+                               3 * 256 + acc, 128))
+                return false;
+            ptx::tc_fence_after();
+            uint32_t r[C_::CW / 32][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + col0;
+#pragma unroll
+            for (int c = 0; c < C_::CW / 32; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar_acce(acc));
+            ++ltd;
+            const int64_t arow = (int64_t)ti.row0 + q * 32 + lane;          // routed row
+            const int64_t row = arow < ti.row_end ? out_row(p, arow) : -1;  // row of C
+            if (row >= 0) {
+                const int64_t ncol0 = (int64_t)ti.n0 + col0;
+                if (p.bias != nullptr || p.act != FP8G_ACT_NONE) {
+                    const float *brow = p.bias != nullptr ? p.bias + (int64_t)ti.e * p.N : nullptr;
+#pragma unroll
+                    for (int c = 0; c < C_::CW / 32; ++c)
+                        epi32(r[c], 1.0f, brow, p.act, ncol0 + c * 32, p.N);
+                }
+#pragma unroll
+                for (int c = 0; c < C_::CW / 32; ++c)
+                    store_row32<OUT_F32>(p.C, row, p.N, ncol0 + c * 32, r[c], 1.0f, p.st32 != 0);
+            }
+            return true;
+        };
+        SfWindow f;
+        Tile ti{};
+        if (t_first < T) {
+            ti = get_tile<MODE, BN>(t_first, p, row_off, tile_off, rt_off);
+            sf_fetch(p, ti, 0, n, 0, ew, f);
+        }
+        for (int32_t t = t_first; t < T; t += t_step) {
+            Tile tn = ti;  // the tile of the next window
+            for (int w0 = 0; w0 < n; w0 += 8) {
+                const SfWindow cur = f;
+                int wn = w0 + 8;
+                bool more = true;
+                if (wn >= n) {
+                    wn = 0;
+                    more = t + t_step < T;
+                    if (more) tn = get_tile<MODE, BN>(t + t_step, p, row_off, tile_off, rt_off);
+                }
+                if (more) sf_fetch(p, tn, 0, n, wn, ew, f);
+                if (!sf_put<STAGES>(p, ti, 0, n, w0, it, ew, cur, sbase + C_::OFF_SF,
+                                    C_::CHUNK_BYTES, bars, abort_flag, bad, it == 0 && w0 == 0))
+                    goto roles_done;
+                if (w0 == 0 && have_prev) {
+                    if (!drain_store(prev)) goto roles_done;
+                    have_prev = false;
+                }
+            }
+            it += (uint32_t)n;
+            prev = ti;
+            have_prev = true;
+            ti = tn;
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p, FP8G_ERR_SCALE_FORMAT, 0);
+        if (have_prev) (void)drain_store(prev);
     } else if (warp >= kEpiWarp0) {
         // ===== epilogue =====
         const int ew = warp - kEpiWarp0;
@@ -1021,9 +1109,13 @@ KernelChoice choose_kernel(int mode, int64_t M, int64_t N, int64_t K, int num_sm
             // wave idles half as long (each expert's rows are padded to whole
             // tiles, so the tile count exceeds the estimate: decode-shaped
             // MoE, 256 routed rows over 3 experts, N = 14336: 168 tiles of
-            // 128 x 256 on 148 SMs are two waves, the second 14% full)
+            // 128 x 256 on 148 SMs are two waves, the second 14% full).  The
+            // kernel converts its own block scales (no packing kernel, whose
+            // pass over the used experts' fp32 scales would precede it; a
+            // fused-quantiser call packs B's scales all the same)
             kc.BN = 128;
             kc.b_rows = 128;
+            kc.inl = true;
             kc.grid = num_sms;
         }
         return kc;
@@ -1109,10 +1201,10 @@ cudaError_t launch_gemm(int mode, bool out_f32, const GemmMaps &maps, const Gemm
                        : launch_one<kModeGrouped, 128, 2, 6, false, false, 1>(maps, p, kc, stream);
     } else {
         // 128 x 128 tiles, two 128-column accumulators: the epilogue of a tile
-        // overlaps the next tile's MMAs
-        if (kc.BN != 128) return cudaErrorInvalidValue;
-        return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false>(maps, p, kc, stream)
-                       : launch_one<kModeGrouped, 128, 2, 6, false, false>(maps, p, kc, stream);
+        // overlaps the next tile's MMAs; the kernel converts its own scales
+        if (kc.BN != 128 || !kc.inl) return cudaErrorInvalidValue;
+        return out_f32 ? launch_one<kModeGrouped, 128, 2, 6, true, false, 0, true>(maps, p, kc, stream)
+                       : launch_one<kModeGrouped, 128, 2, 6, false, false, 0, true>(maps, p, kc, stream);
     }
 }
 

@@ -45,9 +45,11 @@
  *     bytes, taken from a library-owned memory pool with
  *     cudaMallocFromPoolAsync on `stream` and returned with cudaFreeAsync on
  *     `stream` (stream-ordered, so calls on different streams never share
- *     it).  Shapes with few output tiles (split-K: see fp8g_gemm_plan) skip
- *     the temporary: the GEMM converts the scales itself.  The library also holds one status word per device (a static
- *     device variable) and a host-side tensor-map cache.
+ *     it).  Shapes with few output tiles (split-K, or one CTA per 128 x 128
+ *     tile: see fp8g_gemm_plan) and grouped calls on 128 x 128 tiles (see
+ *     fp8g_grouped_plan: BM = 128) skip the temporary: the GEMM converts the
+ *     scales itself.  The library also holds one status word per device (a
+ *     static device variable) and a host-side tensor-map cache.
  */
 #ifndef FP8GEMM_H
 #define FP8GEMM_H
@@ -190,6 +192,10 @@ FP8G_API fp8g_status fp8_gemm_blockscaled_noalloc(const void *A, const void *B, 
  * (checked on the device: a mismatch records FP8G_ERR_INVALID_ARG and writes
  * no output).  Empty experts produce no tiles and no rows; their weights and
  * weight scales are not read (so their scales are not checked either).
+ * Plans on 128 x 128 tiles (fewer rows than a wave of 128 x 256 tiles; see
+ * fp8g_grouped_plan) convert the scales inside the GEMM kernel, each CTA those
+ * of its own tiles; 256 x 256 tiles on CTA pairs take them repacked by a
+ * packing kernel first.
  * offsets_out (nullable): device int32[E+1] receives the exclusive prefix.
  * tile_map_out (nullable): device int32[4 * max_tiles] (see fp8g_grouped_plan)
  * receives, for linear tile t, (expert, m_tile, n_tile, 0): experts in index

@@ -62,6 +62,55 @@ def test_grouped_small_full(counts, N, K):
     assert (tmap[want.shape[0]:] == -1).all()
 
 
+def test_grouped_single_cta_several_tiles_per_cta():
+    """128 x 128 tiles that convert their own scales, more tiles than SMs (so
+    CTAs take two, the second one's scale windows converted while the first
+    drains), a ragged N (4160 = 32.5 tiles), K of 9 steps (a window of 8 and
+    one of 1) ending in a half K step (1120 = 8.75 x 128), and an expert of 3
+    rows beside empty ones."""
+    counts = np.array([3, 250, 0, 129], np.int32)
+    N, K = 4160, 1120
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, counts.size)
+    assert plan["BM"] == 128 and plan["BN"] == 128
+    tiles = int(sum(-(-c // 128) for c in counts)) * (-(-N // 128))
+    assert tiles > torch.cuda.get_device_properties(0).multi_processor_count
+    w = synth.small_grouped(counts, N, K, seed=41)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
+    ref, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts, oracle.OUT_BF16)
+    assert_within(C, ref, bound, f"grouped single-CTA {counts.tolist()} N={N} K={K}")
+    assert np.array_equal(offs, oracle.grouped_offsets(counts))
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert want.shape[0] == tiles
+    assert np.array_equal(tmap[:tiles], want)
+
+
+@pytest.mark.parametrize("where", ["A", "B_late"])
+def test_grouped_single_cta_bad_scale_recorded(where):
+    """A scale that is not a power of two, read by a single-CTA grouped tile,
+    records FP8G_ERR_SCALE_FORMAT: in a routed row of A, or in B's last K
+    step of an expert whose tiles come second on their CTAs."""
+    counts = np.array([3, 250, 0, 129], np.int32)
+    N, K = 4160, 1120
+    rows = int(counts.sum())
+    w = synth.small_grouped(counts, N, K, seed=43)
+    qa, sa, qb, sb, _, _, _, _ = _quant_grouped(w)
+    _run_grouped(qa, sa, qb, sb, counts)        # clean: status 0 (asserted there)
+    if where == "A":
+        sa = sa.clone()
+        sa[2, 17] = 3.0                          # expert 0's last row
+    else:
+        sb = sb.clone()
+        sb[3, N - 1, K // 32 - 1] = -0.5         # tiles 163, 164: second on CTAs 11, 12
+    C = torch.empty((rows, N), dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_grouped_gemm(qa, qb, sa, sb, C, fp8g.FP8G_OUT_BF16,
+                          torch.from_numpy(counts).cuda(), counts.size, N, K, rows)
+    st, _ = fp8g.fp8_gemm_status()
+    assert st == fp8g.FP8G_ERR_SCALE_FORMAT
+    assert fp8g.fp8_gemm_status()[0] == fp8g.FP8G_OK
+
+
 def test_grouped_equals_per_expert_gemms():
     """The grouped GEMM equals one block-scaled GEMM per expert.  The single
     GEMMs of these small shapes run their own plan (one CTA per 128 x 128
