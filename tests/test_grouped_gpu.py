@@ -86,6 +86,31 @@ def test_grouped_single_cta_several_tiles_per_cta():
     assert np.array_equal(tmap[:tiles], want)
 
 
+def test_grouped_single_cta_many_short_tiles():
+    """64 experts of 0..20 rows (many empty), N = 2048, K = 256: about five
+    tiles per CTA whose 2 K steps are fewer than the ring's stages, so every
+    tile's scales go in one window and each drain follows the next tile's
+    conversion."""
+    rng = np.random.default_rng(47)
+    counts = rng.integers(0, 21, 64).astype(np.int32)
+    counts[rng.random(64) < 0.25] = 0
+    N, K = 2048, 256
+    rows = int(counts.sum())
+    plan = fp8g.fp8g_grouped_plan(N, K, rows, counts.size)
+    assert plan["BM"] == 128 and plan["BN"] == 128
+    tiles = int((counts > 0).sum()) * (N // 128)
+    assert tiles >= 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    w = synth.small_grouped(counts, N, K, seed=48)
+    qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
+    ref, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts, oracle.OUT_BF16)
+    assert_within(C, ref, bound, "grouped single-CTA, 64 experts")
+    assert np.array_equal(offs, oracle.grouped_offsets(counts))
+    want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
+    assert want.shape[0] == tiles
+    assert np.array_equal(tmap[:tiles], want)
+
+
 @pytest.mark.parametrize("where", ["A", "B_late"])
 def test_grouped_single_cta_bad_scale_recorded(where):
     """A scale that is not a power of two, read by a single-CTA grouped tile,
