@@ -103,6 +103,35 @@ def test_epilogue_grouped_per_expert_bias():
         assert_within(Ch[offs[e] + pi, pj], ref, bound, f"grouped expert {e}")
 
 
+@pytest.mark.parametrize("act", [1, 2])
+def test_epilogue_grouped_single_cta_bias_f32(act):
+    """The grouped 128 x 128 plan (scales converted in the kernel): per-expert
+    bias and activation on fp32 output, ragged N and K, every element."""
+    counts = np.array([3, 250, 0, 129], np.int32)
+    E, N, K = counts.size, 1040, 1120
+    rows = int(counts.sum())
+    assert fp8g.fp8g_grouped_plan(N, K, rows, E)["BM"] == 128
+    w = synth.small_grouped(counts, N, K, seed=33 + act)
+    bias = np.random.default_rng(5 + act).normal(size=(E, N)).astype(np.float32)
+    qa, sa, qa_o, sa_o = _quant(w.A, 32)
+    qb, sb, qb_o, sb_o = _quant(w.B.reshape(E * N, K), 32)
+    C = torch.full((rows, N), float("nan"), dtype=torch.float32, device="cuda")
+    fp8g.fp8_grouped_gemm_ex(qa, qb.reshape(E, N, K), sa, sb.reshape(E, N, K // 32), C,
+                             fp8g.FP8G_OUT_F32, 0, 0, torch.from_numpy(bias).cuda(), act,
+                             torch.from_numpy(counts).cuda(), E, N, K, rows)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    Ch = C.cpu().numpy()
+    offs = oracle.grouped_offsets(counts)
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        ref, bound, _ = oracle.gemm(qa_o[offs[e]:offs[e + 1]], qb_o[e * N:(e + 1) * N],
+                                    sa_o[offs[e]:offs[e + 1]], sb_o[e * N:(e + 1) * N], True,
+                                    oracle.OUT_F32, bias=bias[e], act_kind=act)
+        assert_within(Ch[offs[e]:offs[e + 1]], ref, bound, f"grouped single-CTA expert {e}")
+
+
 def test_epilogue_bad_act_rejected():
     q = torch.zeros(128, 128, dtype=torch.uint8, device="cuda")
     s = torch.ones(1, device="cuda")

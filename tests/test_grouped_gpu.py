@@ -62,7 +62,8 @@ def test_grouped_small_full(counts, N, K):
     assert (tmap[want.shape[0]:] == -1).all()
 
 
-def test_grouped_single_cta_several_tiles_per_cta():
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_grouped_single_cta_several_tiles_per_cta(out):
     """128 x 128 tiles that convert their own scales, more tiles than SMs (so
     CTAs take two, the second one's scale windows converted while the first
     drains), a ragged N (4160 = 32.5 tiles), K of 9 steps (a window of 8 and
@@ -77,9 +78,10 @@ def test_grouped_single_cta_several_tiles_per_cta():
     assert tiles > torch.cuda.get_device_properties(0).multi_processor_count
     w = synth.small_grouped(counts, N, K, seed=41)
     qa, sa, qb, sb, qa_o, sa_o, qb_o, sb_o = _quant_grouped(w)
-    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts)
-    ref, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts, oracle.OUT_BF16)
-    assert_within(C, ref, bound, f"grouped single-CTA {counts.tolist()} N={N} K={K}")
+    C, offs, tmap, plan = _run_grouped(qa, sa, qb, sb, counts, out)
+    ref, bound, _ = oracle.grouped_gemm(qa_o, qb_o, sa_o, sb_o, counts,
+                                        oracle.OUT_BF16 if out == "bf16" else oracle.OUT_F32)
+    assert_within(C, ref, bound, f"grouped single-CTA {counts.tolist()} N={N} K={K} {out}")
     assert np.array_equal(offs, oracle.grouped_offsets(counts))
     want = oracle.grouped_tile_map(counts, N, plan["BM"], plan["BN"], plan["G"])
     assert want.shape[0] == tiles
