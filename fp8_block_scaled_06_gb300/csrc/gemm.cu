@@ -788,11 +788,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Each warp converts its 16 rows' scales for every K step of this
         // CTA's tiles (windows of 8 steps: sf_fetch / sf_put), and drains /
         // stores the previous tile's accumulator once the next tile's first
-        // window is in the ring: those steps wait only for the previous
-        // tile's MMAs, and a tile's first MMA waits only for the drain of the
-        // tile NUM_ACC before it, which came earlier, so neither order can
-        // deadlock.  The next window's loads are issued before the current
-        // one is converted, so they are in flight across a drain as well.
+        // window is in the ring.  Converting a step waits only for the MMAs of
+        // earlier steps (its ring slot), and a tile's MMAs wait only for the
+        // drain of the tile NUM_ACC before it, which came earlier, so this
+        // order cannot deadlock.  The next window's loads are issued before the
+        // current one is converted, so they are in flight across a drain too.
         const int ew = warp - kEpiWarp0;
         const int q = warp & 3;
         const int col0 = (ew >> 2) * C_::CW;
