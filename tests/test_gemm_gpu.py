@@ -351,6 +351,27 @@ def test_block_pair_scale_layout_exact():
     assert bad.size == 0, f"{bad.size} mismatches, e.g. {[(pi[b], pj[b], got[b], ref[b]) for b in bad[:4]]}"
 
 
+def test_block_pair_bf16_ragged_edges():
+    """bf16 output of the block-scaled CTA-pair kernel with ragged M and N:
+    the last tile's columns 2368.. lie past N = 2368, and the odd CTA of the
+    last row of tiles starts at row 2432, past M = 2404.  Every element within
+    the tolerance, and the rows after C untouched."""
+    M, N, K = 2404, 2368, 512
+    assert fp8g.fp8g_gemm_plan(1, M, N, K)["BM"] == 256
+    A = synth.normal((M, K), seed=91)
+    B = synth.normal((N, K), seed=92)
+    qa, sa, qa_o, sa_o = quant_both(A, 32)
+    qb, sb, qb_o, sb_o = quant_both(B, 32)
+    C_big = torch.full((M + 8, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = C_big[:M]
+    fp8g.fp8_gemm_blockscaled(qa, qb, sa, sb, C, fp8g.FP8G_OUT_BF16, M, N, K)
+    st, detail = fp8g.fp8_gemm_status()
+    assert st == 0, f"status {st} detail {detail}"
+    ref, bound, _ = oracle.gemm(qa_o, qb_o, sa_o, sb_o, True, oracle.OUT_BF16)
+    assert_within(C.float().cpu().numpy(), ref, bound, "pair bf16, ragged edges")
+    assert torch.isnan(C_big[M:].float()).all()
+
+
 def test_block_single_cta_256_tiles():
     """A block-scaled shape with between half a wave and a wave of 128x256
     tiles runs on single CTAs with 256-wide tiles (no split, no pair)."""
