@@ -104,10 +104,14 @@ def test_gemm_formats_pairs_sampled(fa, fb, block):
     assert_within(C[pi, pj], ref, bound, f"pairs fmt {fa}x{fb} block={block}")
 
 
-def test_grouped_e5m2_weights():
-    """E4M3 activations against E5M2 expert weights (grouped, block-scaled)."""
-    counts = np.array([130, 0, 5, 257], np.int32)
-    E, N, K = counts.size, 264, 256
+@pytest.mark.parametrize("counts,N,K", [([130, 0, 5, 257], 264, 256),
+                                          ([3, 250, 0, 129], 4160, 1120)])
+def test_grouped_e5m2_weights(counts, N, K):
+    """E4M3 activations against E5M2 expert weights (grouped, block-scaled);
+    the second shape puts two tiles on some CTAs and takes two scale windows
+    per tile (9 K steps, the last one partial)."""
+    counts = np.array(counts, np.int32)
+    E = counts.size
     w = synth.small_grouped(counts, N, K, seed=77)
     qa, sa, qa_o, sa_o = _quant(w.A, 32, E4)
     qb, sb, qb_o, sb_o = _quant(w.B.reshape(E * N, K), 32, E5)
